@@ -1,0 +1,140 @@
+"""ctypes wrapper around the double-precision CPU oracle (msc_oracle.c).
+
+TEST INFRASTRUCTURE.  Only tests/, ``__graft_entry__.smoke()`` and bench.py's
+CPU-baseline leg may import this module.  It shares nothing with the CUDA library
+and never touches the GPU.  Inputs are converted to float64 exactly (fp32 and
+bf16-rounded values are exact in double), outputs are float64.
+
+The arithmetic lives in msc_oracle.c; this file only marshals arrays.  Parity of
+each function is pinned in tests/test_oracle_pins.py (closed forms, special
+cases, brute force and finite differences), so none of them is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "msc_oracle.c")
+_LIB = os.path.join(_HERE, "libmsc_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile msc_oracle.c with gcc (-O2, no fast-math, OpenMP) in place."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+               "-o", _LIB + ".tmp", _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            lib.oracle_s6_fwd.argtypes = [_i64] * 4 + [_dp] * 11
+            lib.oracle_s6_fwd.restype = ctypes.c_int
+            lib.oracle_s6_bwd.argtypes = [_i64] * 4 + [_dp] * 17
+            lib.oracle_s6_bwd.restype = ctypes.c_int
+            lib.oracle_ssd_fwd.argtypes = [_i64] * 6 + [_dp] * 10
+            lib.oracle_ssd_fwd.restype = ctypes.c_int
+            lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def _f64(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return ctypes.cast(None, _dp)
+    return a.ctypes.data_as(_dp)
+
+
+def s6_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None,
+           return_last_state=False):
+    """S6 forward.  u, delta, z: [batch, dim, L]; A: [dim, N]; B, C: [batch, N, L];
+    D, delta_bias: [dim]; h0: [batch, dim, N].  Returns y (and h_last)."""
+    u, delta, A, B, C = map(_f64, (u, delta, A, B, C))
+    D, z, delta_bias, h0 = map(_f64, (D, z, delta_bias, h0))
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    assert delta.shape == u.shape and A.shape == (dim, N)
+    assert B.shape == (batch, N, L) and C.shape == (batch, N, L)
+    y = np.empty((batch, dim, L), np.float64)
+    h_last = np.empty((batch, dim, N), np.float64)
+    rc = _load().oracle_s6_fwd(batch, dim, L, N, _ptr(u), _ptr(delta), _ptr(A), _ptr(B),
+                               _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0),
+                               _ptr(y), _ptr(h_last))
+    if rc:
+        raise MemoryError("oracle_s6_fwd failed")
+    return (y, h_last) if return_last_state else y
+
+
+def s6_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, dy=None):
+    """S6 backward (zero initial state).  Returns a dict of float64 grads:
+    du, ddelta, dA, dB, dC, and dD / dz / ddelta_bias when the input is present."""
+    u, delta, A, B, C, dy = map(_f64, (u, delta, A, B, C, dy))
+    D, z, delta_bias = map(_f64, (D, z, delta_bias))
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    out = {
+        "du": np.empty_like(u), "ddelta": np.empty_like(u),
+        "dA": np.empty((dim, N)), "dB": np.empty((batch, N, L)), "dC": np.empty((batch, N, L)),
+        "dD": np.empty(dim), "dz": np.empty_like(u) if z is not None else None,
+        "ddelta_bias": np.empty(dim),
+    }
+    rc = _load().oracle_s6_bwd(batch, dim, L, N, _ptr(u), _ptr(delta), _ptr(A), _ptr(B),
+                               _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(dy),
+                               _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]),
+                               _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+                               _ptr(out["dz"]), _ptr(out["ddelta_bias"]))
+    if rc:
+        raise MemoryError("oracle_s6_bwd failed")
+    if D is None:
+        out["dD"] = None
+    if delta_bias is None:
+        out["ddelta_bias"] = None
+    return out
+
+
+def ssd_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, return_final_state=False):
+    """SSD forward.  x, z: [batch, L, heads, P]; delta: [batch, L, heads];
+    A, D, delta_bias: [heads]; B, C: [batch, L, groups, N]."""
+    x, delta, A, B, C = map(_f64, (x, delta, A, B, C))
+    D, z, delta_bias = map(_f64, (D, z, delta_bias))
+    batch, L, nheads, P = x.shape
+    ngroups, N = B.shape[2], B.shape[3]
+    y = np.empty_like(x)
+    fs = np.empty((batch, nheads, P, N))
+    rc = _load().oracle_ssd_fwd(batch, L, nheads, P, N, ngroups, _ptr(x), _ptr(delta),
+                                _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                _ptr(delta_bias), _ptr(y), _ptr(fs))
+    if rc:
+        raise ValueError("oracle_ssd_fwd failed (rc=%d)" % rc)
+    return (y, fs) if return_final_state else y

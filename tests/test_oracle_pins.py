@@ -1,0 +1,423 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these checks re-types the oracle's own loop.  Each compares it with an
+independent statement of the same quantity:
+
+  P1 materialised closed form of the S6 output (sum over sources s <= t of the
+     explicit decay products), written with numpy on tiny inputs;
+  P2 Delta -> 0 leaves only the feed-through D * u (times the gate);
+  P3 constant Delta, B, C: the scan is an LTI causal convolution (numpy.convolve
+     and an FFT convolution);
+  P4 SSD: the materialised semiseparable form y_i = sum_{j<=i} M_ij (C_i.B_j) Delta_j x_j
+     with M_ij = a_{j+1}...a_i, the S6 oracle with channels (head, p), and a
+     chunked block decomposition all agree;
+  P5 central finite differences of <w, y> against the hand-derived backward;
+  P6 linearity in u and the split scan [0,L) = [0,k) then [k,L) from h_last;
+  P7 the decay bound |h_t| <= sum |Delta B u| when A < 0;
+  P8 a single step and the study note's worked three-step recurrence by hand.
+A planted mistake in the oracle (a dropped term, a wrong sign or index, a
+transposed operand) fails at least one of them; test_planted_mistakes checks
+that on CPU copies of the oracle with such mistakes.
+"""
+import os
+import shutil
+import subprocess
+import ctypes
+
+import numpy as np
+import pytest
+from scipy.special import expit
+from scipy.signal import fftconvolve
+
+from oracle import oracle
+from selective_state_space_160_b300.inputs import s6_inputs, ssd_inputs
+
+
+def softplus(x):
+    return np.logaddexp(0.0, x)
+
+
+def silu(z):
+    return z * expit(z)
+
+
+def closed_form_s6(u, delta, A, B, C, D=None, z=None, bias=None):
+    """P1: y_t = [sum_{s<=t} sum_n C_tn (prod_{r=s+1..t} exp(Delta_r A_n)) Delta_s B_sn u_s
+    + D u_t] * silu(z_t), by explicit products (O(L^2 N))."""
+    f64 = lambda a: None if a is None else np.asarray(a, np.float64)
+    u, delta, A, B, C, D, z, bias = map(f64, (u, delta, A, B, C, D, z, bias))
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    y = np.zeros((batch, dim, L))
+    for b in range(batch):
+        for d in range(dim):
+            dt = softplus(delta[b, d].astype(np.float64) + (bias[d] if bias is not None else 0.0))
+            for t in range(L):
+                acc = 0.0
+                for s in range(t + 1):
+                    decay = np.ones(N)
+                    for r in range(s + 1, t + 1):
+                        decay = decay * np.exp(dt[r] * A[d])
+                    acc += np.sum(C[b, :, t] * decay * dt[s] * B[b, :, s] * u[b, d, s])
+                if D is not None:
+                    acc += D[d] * u[b, d, t]
+                if z is not None:
+                    acc *= silu(z[b, d, t])
+                y[b, d, t] = acc
+    return y
+
+
+def rel_err(a, b):
+    return float(np.max(np.abs(a - b) / (1.0 + np.abs(b))))
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return s6_inputs(2, 4, 24, 5, seed=11)
+
+
+# ----------------------------------------------------------------------------- P1
+@pytest.mark.parametrize("with_z,with_D,with_bias", [(True, True, True), (False, True, True),
+                                                     (True, False, False), (False, False, True)])
+def test_p1_closed_form(with_z, with_D, with_bias):
+    inp = s6_inputs(1, 3, 20, 4, seed=3, with_z=with_z, with_D=with_D, with_bias=with_bias)
+    y = oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                      inp["z"], inp["delta_bias"])
+    ref = closed_form_s6(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                         inp["z"], inp["delta_bias"])
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_p1_closed_form_config0_shape():
+    # tiny fp32 configuration: batch 1, 4 channels, L = 64, N = 16
+    inp = s6_inputs(1, 4, 64, 16, seed=160_000)
+    y = oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                      inp["z"], inp["delta_bias"])
+    ref = closed_form_s6(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                         inp["z"], inp["delta_bias"])
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- P2
+def test_p2_zero_delta_feedthrough(tiny):
+    inp = {k: (None if v is None else np.asarray(v, np.float64)) for k, v in tiny.items()}
+    bias = np.full(inp["A"].shape[0], -200.0)   # softplus(-200) ~ 1e-87 -> Delta = 0
+    y = oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                      inp["z"], bias)
+    ref = inp["D"][None, :, None] * inp["u"] * silu(inp["z"].astype(np.float64))
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- P3
+def test_p3_lti_convolution():
+    rng = np.random.default_rng(5)
+    batch, dim, L, N = 1, 3, 96, 6
+    u = rng.standard_normal((batch, dim, L))
+    delta = np.repeat(rng.standard_normal((batch, dim, 1)) * 0.5, L, axis=2)
+    A = -rng.uniform(0.1, 3.0, size=(dim, N))
+    Bc = rng.standard_normal((batch, N, 1))
+    Cc = rng.standard_normal((batch, N, 1))
+    B = np.repeat(Bc, L, axis=2)
+    C = np.repeat(Cc, L, axis=2)
+    D = rng.standard_normal(dim)
+    bias = rng.standard_normal(dim) * 0.3
+    y = oracle.s6_fwd(u, delta, A, B, C, D, None, bias)
+    k = np.arange(L)
+    for d in range(dim):
+        dt = softplus(delta[0, d, 0] + bias[d])
+        K = np.array([np.sum(Cc[0, :, 0] * np.exp(kk * dt * A[d]) * dt * Bc[0, :, 0]) for kk in k])
+        direct = np.convolve(K, u[0, d])[:L] + D[d] * u[0, d]
+        viafft = fftconvolve(K, u[0, d])[:L] + D[d] * u[0, d]
+        np.testing.assert_allclose(y[0, d], direct, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(y[0, d], viafft, rtol=1e-9, atol=1e-10)
+
+
+# ----------------------------------------------------------------------------- P4
+def materialised_ssd(x, delta, A, B, C, D=None, z=None, bias=None):
+    """y_i = sum_{j<=i} M_ij (C_i . B_j) Delta_j x_j + D x_i with M_ij = a_{j+1} ... a_i."""
+    f64 = lambda a: None if a is None else np.asarray(a, np.float64)
+    x, delta, A, B, C, D, z, bias = map(f64, (x, delta, A, B, C, D, z, bias))
+    batch, L, H, P = x.shape
+    G = B.shape[2]
+    hpg = H // G
+    y = np.zeros((batch, L, H, P))
+    for b in range(batch):
+        for h in range(H):
+            g = h // hpg
+            dt = softplus(delta[b, :, h].astype(np.float64) + (bias[h] if bias is not None else 0.0))
+            a = np.exp(dt * A[h])
+            M = np.zeros((L, L))
+            for i in range(L):
+                for j in range(i + 1):
+                    M[i, j] = np.prod(a[j + 1:i + 1])   # empty product = 1 on the diagonal
+            CB = C[b, :, g, :].astype(np.float64) @ B[b, :, g, :].astype(np.float64).T
+            Y = (M * CB) @ (dt[:, None] * x[b, :, h, :])
+            if D is not None:
+                Y = Y + D[h] * x[b, :, h, :]
+            if z is not None:
+                Y = Y * silu(z[b, :, h, :].astype(np.float64))
+            y[b, :, h, :] = Y
+    return y
+
+
+def chunked_ssd(x, delta, A, B, C, Q, D=None, bias=None):
+    """Block decomposition: intra-chunk masked matmul + inter-chunk state passing."""
+    f64 = lambda a: None if a is None else np.asarray(a, np.float64)
+    x, delta, A, B, C, D, bias = map(f64, (x, delta, A, B, C, D, bias))
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    hpg = H // G
+    y = np.zeros((batch, L, H, P))
+    for b in range(batch):
+        for h in range(H):
+            g = h // hpg
+            dt = softplus(delta[b, :, h].astype(np.float64) + (bias[h] if bias is not None else 0.0))
+            la = dt * A[h]                       # log a_t
+            S = np.zeros((P, N))                 # state entering the chunk
+            for c0 in range(0, L, Q):
+                c1 = min(c0 + Q, L)
+                cs = np.cumsum(la[c0:c1])        # inclusive within the chunk
+                n = c1 - c0
+                Lmat = np.zeros((n, n))
+                for i in range(n):
+                    for j in range(i + 1):
+                        Lmat[i, j] = np.exp(cs[i] - cs[j])
+                Cc = C[b, c0:c1, g, :].astype(np.float64)
+                Bc = B[b, c0:c1, g, :].astype(np.float64)
+                Xd = dt[c0:c1, None] * x[b, c0:c1, h, :]
+                Ydiag = (Lmat * (Cc @ Bc.T)) @ Xd
+                Yoff = np.exp(cs)[:, None] * (Cc @ S.T)
+                Yc = Ydiag + Yoff
+                if D is not None:
+                    Yc = Yc + D[h] * x[b, c0:c1, h, :]
+                y[b, c0:c1, h, :] = Yc
+                w = np.exp(cs[-1] - cs)          # decay from step j to the chunk end
+                S = np.exp(cs[-1]) * S + (w[:, None] * Xd).T @ Bc
+    return y
+
+
+def test_p4_ssd_materialised_and_s6_equivalence():
+    inp = ssd_inputs(2, 19, 4, 3, 5, ngroups=2, seed=7, bf16=False, with_z=True)
+    y, fs = oracle.ssd_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                           inp["z"], inp["delta_bias"], return_final_state=True)
+    ref = materialised_ssd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                           inp["z"], inp["delta_bias"])
+    np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+    # the same problem as an S6 scan with channels d = (head, p), Delta and A shared per head
+    batch, L, H, P = inp["x"].shape
+    G, N = inp["B"].shape[2], inp["B"].shape[3]
+    for g in range(G):
+        heads = range(g * (H // G), (g + 1) * (H // G))
+        u = np.concatenate([inp["x"][:, :, h, :].transpose(0, 2, 1) for h in heads], axis=1)
+        dl = np.concatenate([np.repeat(inp["delta"][:, None, :, h], P, axis=1) for h in heads], axis=1)
+        zz = np.concatenate([inp["z"][:, :, h, :].transpose(0, 2, 1) for h in heads], axis=1)
+        A6 = np.concatenate([np.full((P, N), inp["A"][h]) for h in heads], axis=0)
+        D6 = np.concatenate([np.full(P, inp["D"][h]) for h in heads])
+        b6 = np.concatenate([np.full(P, inp["delta_bias"][h]) for h in heads])
+        B6 = inp["B"][:, :, g, :].transpose(0, 2, 1)
+        C6 = inp["C"][:, :, g, :].transpose(0, 2, 1)
+        y6, h6 = oracle.s6_fwd(u, dl, A6, B6, C6, D6, zz, b6, return_last_state=True)
+        for i, h in enumerate(heads):
+            np.testing.assert_allclose(y[:, :, h, :], y6[:, i * P:(i + 1) * P, :].transpose(0, 2, 1),
+                                       rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(fs[:, h], h6[:, i * P:(i + 1) * P, :], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("Q", [4, 8])
+def test_p4_ssd_chunked_decomposition(Q):
+    inp = ssd_inputs(1, 21, 2, 3, 6, ngroups=1, seed=9, bf16=False)
+    y = oracle.ssd_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                       None, inp["delta_bias"])
+    ref = chunked_ssd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], Q, inp["D"],
+                      inp["delta_bias"])
+    np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- P5
+def _fd_check(inp, with_z=True, with_D=True, with_bias=True, eps=1e-6):
+    rng = np.random.default_rng(21)
+    keys = ["u", "delta", "A", "B", "C"] + (["D"] if with_D else []) + \
+           (["z"] if with_z else []) + (["delta_bias"] if with_bias else [])
+    base = {k: (None if inp.get(k) is None else np.asarray(inp[k], np.float64).copy())
+            for k in ["u", "delta", "A", "B", "C", "D", "z", "delta_bias"]}
+    if not with_z:
+        base["z"] = None
+    if not with_D:
+        base["D"] = None
+    if not with_bias:
+        base["delta_bias"] = None
+    y0 = oracle.s6_fwd(**{k: base[k] for k in base})
+    w = rng.standard_normal(y0.shape)
+    g = oracle.s6_bwd(dy=w, **{k: base[k] for k in base})
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "ddelta_bias"}
+    for k in keys:
+        arr = base[k]
+        fd = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = arr[idx]
+            arr[idx] = old + eps
+            fp = np.sum(w * oracle.s6_fwd(**base))
+            arr[idx] = old - eps
+            fm = np.sum(w * oracle.s6_fwd(**base))
+            arr[idx] = old
+            fd[idx] = (fp - fm) / (2 * eps)
+        an = g[names[k]]
+        scale = np.max(np.abs(fd)) + 1e-30
+        assert np.max(np.abs(an - fd)) <= 1e-6 * max(scale, 1.0), (k, np.max(np.abs(an - fd)), scale)
+
+
+def test_p5_finite_differences_full():
+    _fd_check(s6_inputs(2, 4, 16, 4, seed=13))
+
+
+def test_p5_finite_differences_no_gate_no_D():
+    _fd_check(s6_inputs(1, 3, 12, 3, seed=17), with_z=False, with_D=False, with_bias=False)
+
+
+def test_p5_finite_differences_config0_size():
+    # tiny configuration size (1 x 4 x 64, N = 16), gradients w.r.t. the shared B, C and A
+    inp = s6_inputs(1, 4, 64, 16, seed=160_000)
+    rng = np.random.default_rng(3)
+    base = {k: (None if v is None else np.asarray(v, np.float64).copy()) for k, v in inp.items()
+            if k in ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")}
+    y0 = oracle.s6_fwd(**base)
+    w = rng.standard_normal(y0.shape)
+    g = oracle.s6_bwd(dy=w, **base)
+    eps = 1e-6
+    for key, gname in (("B", "dB"), ("C", "dC"), ("A", "dA"), ("delta", "ddelta")):
+        arr = base[key]
+        for idx in [tuple(rng.integers(0, s) for s in arr.shape) for _ in range(12)]:
+            old = arr[idx]
+            arr[idx] = old + eps
+            fp = np.sum(w * oracle.s6_fwd(**base))
+            arr[idx] = old - eps
+            fm = np.sum(w * oracle.s6_fwd(**base))
+            arr[idx] = old
+            fd = (fp - fm) / (2 * eps)
+            assert abs(g[gname][idx] - fd) <= 1e-6 * max(1.0, abs(fd)), (key, idx, g[gname][idx], fd)
+
+
+# ----------------------------------------------------------------------------- P6
+def test_p6_linearity_in_u(tiny):
+    inp = tiny
+    rng = np.random.default_rng(1)
+    u2 = rng.standard_normal(inp["u"].shape)
+    args = dict(delta=inp["delta"], A=inp["A"], B=inp["B"], C=inp["C"], D=inp["D"],
+                z=inp["z"], delta_bias=inp["delta_bias"])
+    y1 = oracle.s6_fwd(inp["u"], **args)
+    y2 = oracle.s6_fwd(u2, **args)
+    y12 = oracle.s6_fwd(1.5 * inp["u"].astype(np.float64) - 0.25 * u2, **args)
+    np.testing.assert_allclose(y12, 1.5 * y1 - 0.25 * y2, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("k", [1, 7, 23])
+def test_p6_split_scan(tiny, k):
+    inp = tiny
+    L = inp["u"].shape[2]
+    args = dict(A=inp["A"], D=inp["D"], delta_bias=inp["delta_bias"])
+    y, hl = oracle.s6_fwd(inp["u"], inp["delta"], B=inp["B"], C=inp["C"], z=inp["z"],
+                          return_last_state=True, **args)
+    ya, ha = oracle.s6_fwd(inp["u"][:, :, :k], inp["delta"][:, :, :k], B=inp["B"][:, :, :k],
+                           C=inp["C"][:, :, :k], z=inp["z"][:, :, :k], return_last_state=True, **args)
+    yb, hb = oracle.s6_fwd(inp["u"][:, :, k:], inp["delta"][:, :, k:], B=inp["B"][:, :, k:],
+                           C=inp["C"][:, :, k:], z=inp["z"][:, :, k:], h0=ha,
+                           return_last_state=True, **args)
+    np.testing.assert_allclose(np.concatenate([ya, yb], axis=2), y, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(hb, hl, rtol=1e-12, atol=1e-13)
+    assert y.shape[2] == L
+
+
+# ----------------------------------------------------------------------------- P7
+def test_p7_decay_bound():
+    inp = s6_inputs(2, 6, 200, 16, seed=19)
+    y, hl = oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                          inp["z"], inp["delta_bias"], return_last_state=True)
+    dt = softplus(inp["delta"].astype(np.float64) + inp["delta_bias"][None, :, None])
+    # |h_L,n| <= sum_s |Delta_s B_sn u_s|
+    bound = np.einsum("bdl,bnl->bdn", np.abs(dt * inp["u"]), np.abs(inp["B"].astype(np.float64)))
+    assert np.all(np.abs(hl) <= bound * (1 + 1e-12))
+    assert np.all(np.isfinite(y))
+
+
+# ----------------------------------------------------------------------------- P8
+def test_p8_single_step():
+    rng = np.random.default_rng(2)
+    N = 16
+    u = rng.standard_normal((1, 1, 1))
+    delta = rng.standard_normal((1, 1, 1))
+    z = rng.standard_normal((1, 1, 1))
+    B = rng.standard_normal((1, N, 1))
+    C = rng.standard_normal((1, N, 1))
+    A = -np.arange(1.0, N + 1)[None, :]
+    D = np.array([0.7])
+    bias = np.array([-1.3])
+    y = oracle.s6_fwd(u, delta, A, B, C, D, z, bias)
+    dt = np.log1p(np.exp(delta[0, 0, 0] + bias[0]))
+    hand = (np.dot(C[0, :, 0], dt * B[0, :, 0] * u[0, 0, 0]) + D[0] * u[0, 0, 0]) \
+        * z[0, 0, 0] / (1.0 + np.exp(-z[0, 0, 0]))
+    assert abs(y[0, 0, 0] - hand) <= 1e-14 * (1 + abs(hand))
+
+
+def test_p8_study_note_three_steps():
+    # The study note's one-step pseudocode: h_t = exp(-Delta) h_{t-1} + Delta B x_t,
+    # y_t = C h_t, i.e. N = 1, A = -1, no D and no gate.  Delta_t = softplus(delta_t).
+    x = np.array([1.0, -2.0, 0.5])
+    dl = np.array([0.0, 1.0, -1.0])
+    Bv = np.array([2.0, 1.0, -1.0])
+    Cv = np.array([1.0, 3.0, 2.0])
+    y = oracle.s6_fwd(x[None, None], dl[None, None], np.array([[-1.0]]), Bv[None, None],
+                      Cv[None, None])
+    D0, D1, D2 = np.log(2.0), np.log(1 + np.e), np.log(1 + 1 / np.e)
+    h0 = D0 * 2.0 * 1.0
+    h1 = np.exp(-D1) * h0 + D1 * 1.0 * -2.0
+    h2 = np.exp(-D2) * h1 + D2 * -1.0 * 0.5
+    np.testing.assert_allclose(y[0, 0], [1.0 * h0, 3.0 * h1, 2.0 * h2], rtol=1e-14, atol=1e-15)
+
+
+# ------------------------------------------------------------------ planted mistakes
+MUTATIONS = [
+    # (description, original text, mutated text)
+    ("drop the input term", "+ dt * B[n * L + t] * u[t];\n            acc",
+     ";\n            acc"),
+    ("wrong sign of A", "double abar = exp(dt * A[n]);\n            h[n]",
+     "double abar = exp(-dt * A[n]);\n            h[n]"),
+    ("B and C swapped", "acc += C[n * L + t] * h[n];", "acc += B[n * L + t] * h[n];"),
+    ("drop D feed-through", "acc += D * u[t];\n        if (z) acc *= z[t] * sigmoid_d(z[t]);",
+     "if (z) acc *= z[t] * sigmoid_d(z[t]);"),
+    ("gate by sigmoid only", "if (z) acc *= z[t] * sigmoid_d(z[t]);", "if (z) acc *= sigmoid_d(z[t]);"),
+    ("bwd: lambda without decay", "double l = gp * C[n * L + t] + abar_next * lam[n];",
+     "double l = gp * C[n * L + t] + lam[n];"),
+    ("bwd: dA uses h_t", "dA_row[n] += l * dt * abar * hprev;",
+     "dA_row[n] += l * dt * abar * hs[(t + 1) * N + n];"),
+    ("ssd: decay index off by one", "double hv = a * H[p * N + n] + dt * xp * B[t * sb + n];",
+     "double hv = a * H[p * N + n] + dt * xp * B[(t > 0 ? t - 1 : t) * sb + n];"),
+]
+
+
+@pytest.mark.parametrize("desc,orig,mut", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistakes(tmp_path, desc, orig, mut, monkeypatch):
+    """Plant each mistake in a CPU copy of the oracle and check a pin catches it."""
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "msc_oracle.c")).read()
+    assert orig in src, desc
+    bad = tmp_path / "bad.c"
+    bad.write_text(src.replace(orig, mut, 1))
+    so = tmp_path / "libbad.so"
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", str(so), str(bad), "-lm"],
+                   check=True)
+    monkeypatch.setattr(oracle, "_LIB", str(so))
+    monkeypatch.setattr(oracle, "build", lambda force=False: str(so))
+    monkeypatch.setattr(oracle, "_lib", None)
+    caught = False
+    for pin in (lambda: test_p1_closed_form(True, True, True),
+                lambda: test_p5_finite_differences_full(),
+                lambda: test_p4_ssd_materialised_and_s6_equivalence()):
+        try:
+            pin()
+        except AssertionError:
+            caught = True
+            break
+    monkeypatch.setattr(oracle, "_lib", None)
+    assert caught, "no pin caught: " + desc
