@@ -1,0 +1,509 @@
+#!/usr/bin/env python3
+"""Benchmark of the Mamba selective scan on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--legs fwd_long,bwd,ssd|none]
+
+One step = one S6 forward of the Mamba-2.8B-layer workload (batch 8, d_inner
+5120, L 2048, N 16, bf16 u/delta/z/B/C, fp32 state and output, z-gate, D and
+Delta_bias on), all of selection, discretisation, scan, readout and gate in one
+kernel launch.  Metric: elements (batch * D * L) per second.  Inputs are
+resident in HBM (503 MB of inputs + 336 MB of output per step, larger than the
+126 MB L2, so no L2 flush is needed between steps).
+
+Printed on rank 0: one JSON line with value, roofline (live CUDA-event timing of
+the kernel against HBM / SFU / FP32 peaks), e2e (host buffers through the public
+API), the CPU oracle baseline, clocks sampled during the timed region, and
+`legs` (the long-sequence forward, the backward and the SSD chunked forward,
+each timed the same way).  Under torchrun (N > 1) every rank runs an
+independent replica (weak scaling, no collective in the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan elements/s (B·D·L) fwd/bwd on 1 B300; % of HBM/SFU roofline"
+UNIT = "elements/s"
+HEADLINE = dict(batch=8, dim=5120, L=2048, N=16)
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch, from one ncu capture,
+# keyed by kernel; valid only while the kernel source hash matches.
+NCU_TRAFFIC = {}
+
+
+def _sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:12]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def _pipe_peaks():
+    """Measured MUFU ex2 / FFMA / FFMA2 throughput of this GPU (probe library)."""
+    import ctypes
+    from selective_state_space_160_b300 import build as b
+    lib = ctypes.CDLL(b.build_probe())
+    res = (ctypes.c_float * 16)()
+    rc = lib.msc_probe_pipe_peaks(res, 4096)
+    if rc != 0:
+        raise RuntimeError("pipe probe failed: cuda error %d" % rc)
+    names = ["ex2", "ffma", "ffma2", "rcp"]
+    return {n: {"ops_per_s": res[4 * i], "per_sm_clk": res[4 * i + 1], "ms": res[4 * i + 2]}
+            for i, n in enumerate(names)}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.lines = []
+        self.sel = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if uuid and not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+            self.sel = ["-i", uuid] if uuid else []
+        except Exception:
+            self.sel = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"] + self.sel, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- workloads
+def s6_fwd_workload(batch, dim, L, N, bf16, seed, device_gen=False):
+    import torch
+    from selective_state_space_160_b300.inputs import s6_inputs, s6_inputs_torch, bf16_bits
+    if device_gen:
+        return s6_inputs_torch(batch, dim, L, N, seed=seed, bf16=bf16)
+    inp = s6_inputs(batch, dim, L, N, seed=seed, bf16=bf16)
+    out = {}
+    for k, v in inp.items():
+        if v is None:
+            out[k] = None
+        elif k in ("u", "delta", "z", "B", "C", "dy") and bf16:
+            out[k] = torch.from_numpy(bf16_bits(v).view(np.int16).copy()).view(torch.bfloat16).cuda()
+        else:
+            out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).cuda()
+    return out
+
+
+def time_launches(fn, steps, warmup, stream):
+    """CUDA-event time per call of fn() on `stream` (ms list)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def roofline_s6(elements, N, bytes_per_launch, ms, peaks, pipes, exps_per_elem_n=1.0,
+                fp32_per_elem_n=4.0, kernel=None, src=None):
+    """Roofline terms of an S6 kernel: HBM bytes, MUFU ex2 and FP32 work."""
+    t = ms * 1e-3
+    exps = elements * N * exps_per_elem_n
+    fp32 = elements * N * fp32_per_elem_n
+    hbm = bytes_per_launch / t / 1e9
+    terms = {
+        "hbm": {"achieved": hbm, "peak": peaks["hbm_gbs"], "unit": "GB/s"},
+        "sfu": {"achieved": exps / t / 1e9, "peak": pipes["ex2"]["ops_per_s"] / 1e9, "unit": "Gex2/s"},
+        "fp32": {"achieved": fp32 / t / 1e9, "peak": pipes["ffma2"]["ops_per_s"] / 1e9, "unit": "Gflop32/s"},
+    }
+    for v in terms.values():
+        v["frac"] = v["achieved"] / v["peak"]
+    bound = max(terms, key=lambda k: terms[k]["frac"])
+    sel = terms[bound]
+    traffic = None
+    if kernel and src and kernel in NCU_TRAFFIC and NCU_TRAFFIC[kernel]["src_sha"] == _sha(src):
+        traffic = NCU_TRAFFIC[kernel]["bytes_per_launch"]
+    out = {"bound": "hbm" if bound == "hbm" else "alu", "achieved": sel["achieved"], "peak": sel["peak"],
+           "unit": sel["unit"], "frac": sel["frac"], "traffic": traffic,
+           "algorithmic_bytes": bytes_per_launch, "kernel_ms": ms,
+           "terms": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                     for k, v in terms.items()},
+           "hbm_frac_nominal_8tbs": hbm / 8000.0, "peak_source": peaks["source"]}
+    return out
+
+
+# ----------------------------------------------------------------------------- legs
+def leg_fwd_long(peaks, pipes, steps=3, warmup=1):
+    import torch
+    import selective_state_space_160_b300 as msc
+    batch, dim, L, N = 1, 1536, 1 << 20, 16
+    inp = s6_fwd_workload(batch, dim, L, N, False, 160_002, device_gen=True)
+    y = torch.empty((batch, dim, L), dtype=torch.float32, device="cuda")
+    ws = torch.empty(msc.msc_selective_scan_fwd_workspace_size(batch, dim, L, N) + 1024,
+                     dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def fn():
+        msc.msc_selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                   inp["z"], inp["delta_bias"], y=y, workspace=ws)
+    ms = statistics.median(time_launches(fn, steps, warmup, st))
+    el = batch * dim * L
+    nbytes = el * 16 + 2 * batch * N * L * 4
+    res = {"workload": "S6 fwd batch 1, D 1536, L 2^20, N 16, fp32, segmented", "elements_per_s": el / (ms * 1e-3),
+           "ms": ms, "roofline": roofline_s6(el, N, nbytes, ms, peaks, pipes)}
+    del inp, y, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def leg_bwd(peaks, pipes, steps=5, warmup=2):
+    import torch
+    import selective_state_space_160_b300 as msc
+    batch, dim, L, N = 16, 2048, 2048, 16
+    inp = s6_fwd_workload(batch, dim, L, N, True, 160_003)
+    from selective_state_space_160_b300.inputs import s6_inputs_torch
+    dy = torch.randn((batch, dim, L), device="cuda", generator=torch.Generator(device="cuda").manual_seed(3)).to(torch.bfloat16)
+    st = torch.cuda.current_stream()
+
+    def fn():
+        msc.msc_selective_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                   inp["z"], inp["delta_bias"], dy)
+    ms = statistics.median(time_launches(fn, steps, warmup, st))
+    el = batch * dim * L
+    nbytes = el * 20 + 2 * batch * N * L * 2 + 2 * batch * N * L * 4
+    res = {"workload": "S6 bwd batch 16, D 2048, L 2048, N 16, bf16 in / fp32 grads", "elements_per_s": el / (ms * 1e-3),
+           "ms": ms, "roofline": roofline_s6(el, N, nbytes, ms, peaks, pipes, fp32_per_elem_n=12.0)}
+    del inp, dy
+    torch.cuda.empty_cache()
+    return res
+
+
+def leg_ssd(peaks, pipes, steps=5, warmup=2):
+    import torch
+    import selective_state_space_160_b300 as msc
+    from selective_state_space_160_b300.inputs import ssd_inputs, bf16_bits
+    b, L, H, P, N, Q = 4, 4096, 80, 64, 128, 256
+    inp = ssd_inputs(b, L, H, P, N, 1, seed=160_004, bf16=True)
+
+    def dev(a, bf):
+        if a is None:
+            return None
+        if bf:
+            return torch.from_numpy(bf16_bits(a).view(np.int16).copy()).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+    d = {k: dev(v, k in ("x", "delta", "B", "C", "z")) for k, v in inp.items()}
+    y = torch.empty((b, L, H, P), dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def fn():
+        msc.msc_ssd_chunked_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], d["D"], None,
+                                d["delta_bias"], chunk=Q, y=y)
+    ms = statistics.median(time_launches(fn, steps, warmup, st))
+    el = b * L * H * P
+    nbytes = el * 2 + b * L * H * 2 + 2 * b * L * N * 2 + el * 4
+    flops = 2.0 * b * (L // Q) * H * (Q * Q * P / 2 + 2 * Q * P * N) + 2.0 * b * (L // Q) * Q * Q * N / 2
+    t = ms * 1e-3
+    hbm = {"achieved": nbytes / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    ten = {"achieved": flops / t / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    hbm["frac"] = hbm["achieved"] / hbm["peak"]
+    ten["frac"] = ten["achieved"] / ten["peak"]
+    bound = "hbm" if hbm["frac"] >= ten["frac"] else "tensor"
+    sel = hbm if bound == "hbm" else ten
+    res = {"workload": "SSD fwd batch 4, heads 80, P 64, N 128, L 4096, chunk 256, bf16", "elements_per_s": el / t,
+           "ms": ms, "roofline": {"bound": bound, "achieved": sel["achieved"], "peak": sel["peak"],
+                                  "unit": sel["unit"], "frac": sel["frac"], "traffic": None,
+                                  "terms": {"hbm": hbm, "tensor": ten}}}
+    del d, y
+    torch.cuda.empty_cache()
+    return res
+
+
+# ----------------------------------------------------------------------------- reference arm
+def cpu_oracle_sample(target_s=12.0, max_rows=None):
+    """Time the CPU oracle on a bounded sample of the headline workload:
+    whole rows (L = 2048, N = 16, bf16-rounded inputs), as many channels of all
+    8 batch entries as fit in about target_s seconds."""
+    from oracle import oracle
+    from selective_state_space_160_b300.inputs import s6_inputs
+    b, L, N = HEADLINE["batch"], HEADLINE["L"], HEADLINE["N"]
+    dim = 8
+    inp = s6_inputs(b, dim, L, N, seed=160_001, bf16=True)
+    t0 = time.perf_counter()
+    oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["delta_bias"])
+    dt = time.perf_counter() - t0
+    rate = b * dim * L / dt
+    dim2 = int(max(8, min(512, rate * target_s / (b * L))))
+    if max_rows:
+        dim2 = min(dim2, max_rows)
+    inp = s6_inputs(b, dim2, L, N, seed=160_001, bf16=True)
+    t0 = time.perf_counter()
+    oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["delta_bias"])
+    dt = time.perf_counter() - t0
+    return {"value": b * dim2 * L / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "S6 fwd, batch 8 x %d of the 5120 channels x L 2048, N 16, bf16-rounded inputs, "
+                      "double precision, %.1f s" % (dim2, dt)}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from oracle import oracle
+    from selective_state_space_160_b300.inputs import s6_inputs
+    b, L, N = HEADLINE["batch"], HEADLINE["L"], HEADLINE["N"]
+    dim = 16
+    inp = s6_inputs(b, dim, L, N, seed=160_001, bf16=True)
+    f = lambda: oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                              inp["delta_bias"])
+    for _ in range(args.warmup):
+        f()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        f()
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    el = b * dim * L * args.steps
+    value = el / tot
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "S6 fwd batch 8, D 5120, L 2048, N 16, bf16 inputs (CPU oracle sample: "
+                                   "batch 8 x %d channels per step)" % dim, "global_batch": 8, "seq_len": 2048,
+                       "parallelism": "cpu oracle, rank 0 only"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": "batch 8 x %d channels x L 2048 per step" % dim},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main arm
+def run_ours(args):
+    import torch
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import selective_state_space_160_b300 as msc
+    from selective_state_space_160_b300 import build as msc_build
+    msc_build.build()
+    msc.load_library()
+    peaks = _peaks()
+    pipes = _pipe_peaks()
+
+    b, dim, L, N = HEADLINE["batch"], HEADLINE["dim"], HEADLINE["L"], HEADLINE["N"]
+    inp = s6_fwd_workload(b, dim, L, N, True, 160_001 + 1000 * rank)
+    y = torch.empty((b, dim, L), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    launches_per_step = 1 if msc.msc_selective_scan_fwd_workspace_size(b, dim, L, N) == 0 else 3
+
+    def step():
+        msc.msc_selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                   inp["z"], inp["delta_bias"], y=y)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for a, e in per:
+            a.record(stream)
+            step()
+            e.record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    _barrier(ws)
+    total_ms = start.elapsed_time(end)
+    kernel_ms = statistics.mean(a.elapsed_time(e) for a, e in per)
+    total_ms = _max_over_ranks(total_ms, ws)
+    el = b * dim * L
+    value = el * args.steps * ws / (total_ms * 1e-3)
+
+    # end to end through the public API with host buffers: H2D of this step's
+    # inputs from pinned memory, the call, D2H of y
+    host = {k: (inp[k].cpu().pin_memory() if inp[k] is not None else None) for k in ("u", "delta", "z", "B", "C")}
+    dev_in = {k: torch.empty_like(inp[k]) for k in host}
+    yh = torch.empty((b, dim, L), dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = yh.numel() * 4
+
+    def e2e_step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        msc.msc_selective_scan_fwd(dev_in["u"], dev_in["delta"], inp["A"], dev_in["B"], dev_in["C"], inp["D"],
+                                   dev_in["z"], inp["delta_bias"], y=y)
+        yh.copy_(y, non_blocking=True)
+
+    e2e_steps = max(2, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(s2.elapsed_time(e2), ws)
+    e2e_value = el * e2e_steps * ws / (e2e_ms * 1e-3)
+    del host, dev_in, yh
+
+    src = os.path.join(ROOT, "selective_state_space_160_b300", "csrc", "s6_fwd.cu")
+    nbytes = el * (2 + 2 + 2 + 4) + 2 * b * N * L * 2
+    roof = roofline_s6(el, N, nbytes, kernel_ms, peaks, pipes, kernel="s6_fwd_rows_kernel", src=src)
+
+    legs = {}
+    if rank == 0 and args.legs != "none":
+        del inp, y
+        torch.cuda.empty_cache()
+        for name in args.legs.split(","):
+            try:
+                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd}[name]
+                legs[name] = fn(peaks, pipes)
+            except Exception as ex:  # report, do not hide: a failing leg is printed as such
+                legs[name] = {"error": "%s: %s" % (type(ex).__name__, ex)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(target_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in / f32 compute", "data": "synthetic",
+            "config": {"workload": "S6 fwd batch 8, D 5120 (d_inner), L 2048, N 16, bf16 u/delta/z/B/C, "
+                                   "fp32 state and y, z-gate + D + Delta_bias",
+                       "global_batch": b * ws, "seq_len": L, "parallelism": "replicas" if ws > 1 else "single",
+                       "l2": "inputs (503 MB) + outputs (336 MB) per step exceed the 126 MB L2; no flush"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+            "pipe_peaks": {k: {"per_sm_clk": round(v["per_sm_clk"], 2), "ops_per_s": v["ops_per_s"]}
+                           for k, v in pipes.items()},
+            "legs": legs,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--legs", default="fwd_long,bwd,ssd")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

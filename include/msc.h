@@ -1,0 +1,141 @@
+/*
+ * msc.h -- C ABI of libmsc, the B300 (sm_103a) Mamba selective scan.
+ *
+ * Three operations, as the pages state the problem:
+ *
+ *  - S6 forward.  Selection Delta_t = softplus(delta_t + Delta_bias) ("Mamba: A
+ *    Survey" sec. 2.2; "Mamba decoded" sec. 5), exponential-Euler recurrence
+ *    h_t = exp(Delta_t A) (.) h_{t-1} + Delta_t B_t u_t ("Mamba decoded" sec. 6.3:
+ *    Mamba-1/2 are exponential-Euler), readout y_t = C_t . h_t + D u_t ("Mamba
+ *    decoded" sec. 3, D feed-through), gated by silu(z_t) ("Mamba: past and present",
+ *    selective SSM + gating).
+ *  - S6 backward by recomputation: states are recomputed on chip and never
+ *    stored to global memory ("Mamba: A Survey" sec. 2.2, recomputation).
+ *  - Mamba-2 SSD chunked forward: scalar A per head (A_t = alpha_t I), the
+ *    semiseparable form Y = M (X . B^T) C with M_ij = a_{j+1}...a_i ("Mamba: A
+ *    Survey" sec. 3.2; "Mamba decoded" sec. 6.2), computed by the block
+ *    decomposition on tcgen05 tensor cores.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller, contiguous,
+ *    row-major, 16-byte aligned.  The library allocates no device memory: any
+ *    scratch comes from the caller's `workspace`, whose size is given by the
+ *    matching *_workspace_size() query (0 means NULL may be passed).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on that stream; the host returns after enqueueing.
+ *  - Outputs are fully overwritten, including gradients that are sums.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns MSC_ERR_INVALID_ARG / MSC_ERR_UNSUPPORTED with a message in
+ *    msc_last_error() and launches nothing.  Launch failures return MSC_ERR_CUDA.
+ *  - bf16 applies to the streamed inputs (u, delta, z, B, C, dy, x).  A, D and
+ *    Delta_bias are always fp32; outputs and gradients are always fp32.
+ *  - NaN and Inf propagate unchecked.  No C++ exception crosses this boundary.
+ */
+#ifndef MSC_H_
+#define MSC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MSC_OK = 0,
+    MSC_ERR_INVALID_ARG = 1,   /* null required pointer, bad size, misalignment */
+    MSC_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels cover */
+    MSC_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    MSC_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out (see msc_check_device_status) */
+    MSC_ERR_WORKSPACE = 5      /* workspace NULL or smaller than the query returned */
+} msc_status;
+
+typedef enum { MSC_F32 = 0, MSC_BF16 = 1 } msc_dtype;
+
+/* ------------------------------------------------------------------ S6 forward
+ * Shapes: u, delta, z: [batch, dim, seqlen]; B, C: [batch, dstate, seqlen]
+ * (shared by all channels of a batch entry); A: [dim, dstate] fp32;
+ * D, delta_bias: [dim] fp32; h0, h_last: [batch, dim, dstate] fp32;
+ * y: [batch, dim, seqlen] fp32.
+ * Optional (may be NULL): D (no feed-through), z (no gate), delta_bias (0),
+ * h0 (zero initial state), h_last (final state not returned).
+ * Limits: batch, dim, seqlen >= 1; 1 <= dstate <= 16.
+ * Long sequences with few rows are split into segments whose carries are
+ * combined in the workspace (three launches); otherwise one launch, and the
+ * workspace size is 0. */
+size_t msc_selective_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
+                                             int64_t dstate);
+
+msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                  msc_dtype in_dtype,
+                                  const void* u, const void* delta, const float* A,
+                                  const void* B, const void* C, const float* D,
+                                  const void* z, const float* delta_bias, const float* h0,
+                                  float* y, float* h_last,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ----------------------------------------------------------------- S6 backward
+ * Same shapes and dtype as the forward (zero initial state), plus the upstream
+ * gradient dy [batch, dim, seqlen] (in_dtype).  Outputs (fp32, overwritten):
+ * du, ddelta: [batch, dim, seqlen]; dA: [dim, dstate]; dB, dC: [batch, dstate, seqlen];
+ * dD [dim] (required iff D != NULL); dz [batch, dim, seqlen] (required iff z != NULL);
+ * ddelta_bias [dim] (required iff delta_bias != NULL).
+ * The forward states are recomputed chunk by chunk on chip; dB, dC, dA, dD and
+ * ddelta_bias are sums accumulated with fp32 atomics, so their low bits depend
+ * on the order in which blocks finish. */
+size_t msc_selective_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
+                                             int64_t dstate);
+
+msc_status msc_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                  msc_dtype in_dtype,
+                                  const void* u, const void* delta, const float* A,
+                                  const void* B, const void* C, const float* D,
+                                  const void* z, const float* delta_bias, const void* dy,
+                                  float* du, float* ddelta, float* dA, float* dB, float* dC,
+                                  float* dD, float* dz, float* ddelta_bias,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------- SSD chunked fwd
+ * Shapes: x, z: [batch, seqlen, nheads, headdim]; delta: [batch, seqlen, nheads];
+ * A, D, delta_bias: [nheads] fp32; B, C: [batch, seqlen, ngroups, dstate];
+ * y: [batch, seqlen, nheads, headdim] fp32; final_state: [batch, nheads, headdim, dstate] fp32.
+ * Optional (may be NULL): D, z, delta_bias, final_state.
+ * Limits: in_dtype == MSC_BF16; headdim == 64; dstate == 128; ngroups divides
+ * nheads; chunk in {64, 128, 256}; seqlen >= 1 (ragged last chunk allowed).
+ * The result does not depend on `chunk` beyond rounding: it only sets where
+ * the chunk states are materialised.  A device-side bounded wait that runs out
+ * records MSC_ERR_TIMEOUT in the workspace (msc_check_device_status). */
+size_t msc_ssd_chunked_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
+                                          int64_t headdim, int64_t dstate, int64_t ngroups,
+                                          int64_t chunk);
+
+msc_status msc_ssd_chunked_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                               int64_t dstate, int64_t ngroups, int64_t chunk,
+                               msc_dtype in_dtype,
+                               const void* x, const void* delta, const float* A,
+                               const void* B, const void* C, const float* D, const void* z,
+                               const float* delta_bias, float* y, float* final_state,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------- utilities
+ * msc_check_device_status: synchronises `stream`, then reads the status word
+ * that device code keeps at the start of `workspace` (the workspace of the last
+ * call that used it).  Returns MSC_OK, MSC_ERR_TIMEOUT, or MSC_ERR_CUDA if the
+ * stream itself reports an error.  A NULL workspace returns MSC_OK after the sync. */
+msc_status msc_check_device_status(const void* workspace, void* stream);
+
+/* Static English name of a status code. */
+const char* msc_status_string(msc_status status);
+
+/* Message of the last failing call on this host thread ("" if none).  The
+ * pointer stays valid until the next library call on the same thread. */
+const char* msc_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int msc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSC_H_ */

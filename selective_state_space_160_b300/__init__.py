@@ -1,0 +1,280 @@
+"""Mamba selective scan (S6 forward / backward, Mamba-2 SSD chunked forward) for
+NVIDIA B300 (sm_103a).
+
+Every step of the computation runs in libmsc.so (hand-written CUDA behind the C
+ABI declared in include/msc.h).  This module only marshals arguments: it takes
+torch CUDA tensors, allocates outputs and workspace with torch, and passes raw
+device pointers plus the current CUDA stream to the library.  There is no CPU
+fallback: if the library is missing or a tensor is not on the GPU, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "load_library", "library_path",
+    "msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd",
+    "msc_selective_scan_fwd_workspace_size", "msc_selective_scan_bwd_workspace_size",
+    "msc_ssd_chunked_fwd_workspace_size", "msc_check_device_status", "msc_status_string",
+    "msc_last_error", "MscError", "MSC_F32", "MSC_BF16",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libmsc.so")
+_lock = threading.Lock()
+_lib = None
+
+MSC_OK, MSC_ERR_INVALID_ARG, MSC_ERR_UNSUPPORTED, MSC_ERR_CUDA, MSC_ERR_TIMEOUT, MSC_ERR_WORKSPACE = range(6)
+MSC_F32, MSC_BF16 = 0, 1
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_sz = ctypes.c_size_t
+
+# name -> (restype, argtypes); mirrors include/msc.h
+SIGNATURES = {
+    "msc_selective_scan_fwd_workspace_size": (_sz, [_i64] * 4),
+    "msc_selective_scan_fwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 11 + [_vp, _sz, _vp]),
+    "msc_selective_scan_bwd_workspace_size": (_sz, [_i64] * 4),
+    "msc_selective_scan_bwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 9 + [_vp] * 8 + [_vp, _sz, _vp]),
+    "msc_ssd_chunked_fwd_workspace_size": (_sz, [_i64] * 7),
+    "msc_ssd_chunked_fwd": (ctypes.c_int, [_i64] * 7 + [ctypes.c_int] + [_vp] * 10 + [_vp, _sz, _vp]),
+    "msc_check_device_status": (ctypes.c_int, [_vp, _vp]),
+    "msc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "msc_last_error": (ctypes.c_char_p, []),
+    "msc_version": (ctypes.c_int, []),
+}
+
+
+class MscError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("%s: %s" % (_status_name(status), message))
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libmsc.so (built in-tree).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    "libmsc.so not found at %s; build it with "
+                    "`python -m selective_state_space_160_b300.build`" % _LIB_PATH)
+            lib = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _status_name(s):
+    try:
+        return load_library().msc_status_string(int(s)).decode()
+    except Exception:  # library missing while formatting an error
+        return "status %d" % int(s)
+
+
+def msc_status_string(s) -> str:
+    return load_library().msc_status_string(int(s)).decode()
+
+
+def msc_last_error() -> str:
+    return load_library().msc_last_error().decode()
+
+
+def _check(status):
+    if status != MSC_OK:
+        raise MscError(status, msc_last_error())
+
+
+# ----------------------------------------------------------------------------- helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _dev_ptr(t, name, dtype=None, shape=None, optional=False):
+    torch = _torch()
+    if t is None:
+        if optional:
+            return None
+        raise ValueError("%s is required" % name)
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (this library has no CPU path)" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s (got %s)" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s (got %s)" % (name, tuple(shape), tuple(t.shape)))
+    return t.data_ptr()
+
+
+def _in_dtype(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return MSC_BF16
+    if t.dtype == torch.float32:
+        return MSC_F32
+    raise ValueError("streamed inputs must be float32 or bfloat16 (got %s)" % t.dtype)
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _workspace(nbytes, device, workspace=None, align=1024):
+    torch = _torch()
+    if nbytes == 0:
+        return None, 0
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small: %d < %d bytes" % (workspace.numel(), nbytes))
+        return workspace, workspace.numel() * workspace.element_size()
+    # torch's caching allocator returns 512-byte aligned blocks; over-allocate
+    # and offset for stricter alignment.
+    buf = torch.empty(nbytes + align, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % align
+    return buf[off:off + nbytes], nbytes
+
+
+# ----------------------------------------------------------------------------- S6
+def msc_selective_scan_fwd_workspace_size(batch, dim, seqlen, dstate) -> int:
+    return int(load_library().msc_selective_scan_fwd_workspace_size(batch, dim, seqlen, dstate))
+
+
+def msc_selective_scan_bwd_workspace_size(batch, dim, seqlen, dstate) -> int:
+    return int(load_library().msc_selective_scan_bwd_workspace_size(batch, dim, seqlen, dstate))
+
+
+def msc_selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None,
+                           return_last_state=False, y=None, workspace=None, stream=None):
+    """S6 forward.  u, delta, z: [batch, dim, L] (fp32 or bf16, all the same);
+    B, C: [batch, N, L] (same dtype); A: [dim, N] fp32; D, delta_bias: [dim] fp32;
+    h0: [batch, dim, N] fp32.  Returns y [batch, dim, L] fp32 (and h_last)."""
+    torch = _torch()
+    lib = load_library()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dt = _in_dtype(u)
+    tdt = u.dtype
+    args = [
+        _dev_ptr(u, "u"), _dev_ptr(delta, "delta", tdt, (batch, dim, L)),
+        _dev_ptr(A, "A", torch.float32, (dim, N)),
+        _dev_ptr(B, "B", tdt, (batch, N, L)), _dev_ptr(C, "C", tdt, (batch, N, L)),
+        _dev_ptr(D, "D", torch.float32, (dim,), optional=True),
+        _dev_ptr(z, "z", tdt, (batch, dim, L), optional=True),
+        _dev_ptr(delta_bias, "delta_bias", torch.float32, (dim,), optional=True),
+        _dev_ptr(h0, "h0", torch.float32, (batch, dim, N), optional=True),
+    ]
+    if y is None:
+        y = torch.empty((batch, dim, L), dtype=torch.float32, device=u.device)
+    h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device) if return_last_state else None
+    nbytes = msc_selective_scan_fwd_workspace_size(batch, dim, L, N)
+    ws, wsb = _workspace(nbytes, u.device, workspace)
+    st = lib.msc_selective_scan_fwd(batch, dim, L, N, dt, *args,
+                                    _dev_ptr(y, "y", torch.float32, (batch, dim, L)),
+                                    _dev_ptr(h_last, "h_last", optional=True),
+                                    ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream))
+    _check(st)
+    return (y, h_last) if return_last_state else y
+
+
+def msc_selective_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, dy=None,
+                           workspace=None, stream=None):
+    """S6 backward (zero initial state).  Returns a dict with du, ddelta, dA, dB,
+    dC and, when the matching input is given, dD, dz, ddelta_bias (all fp32)."""
+    torch = _torch()
+    lib = load_library()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dt = _in_dtype(u)
+    tdt = u.dtype
+    dev = u.device
+    f32 = torch.float32
+    out = {
+        "du": torch.empty((batch, dim, L), dtype=f32, device=dev),
+        "ddelta": torch.empty((batch, dim, L), dtype=f32, device=dev),
+        "dA": torch.empty((dim, N), dtype=f32, device=dev),
+        "dB": torch.empty((batch, N, L), dtype=f32, device=dev),
+        "dC": torch.empty((batch, N, L), dtype=f32, device=dev),
+        "dD": torch.empty((dim,), dtype=f32, device=dev) if D is not None else None,
+        "dz": torch.empty((batch, dim, L), dtype=f32, device=dev) if z is not None else None,
+        "ddelta_bias": torch.empty((dim,), dtype=f32, device=dev) if delta_bias is not None else None,
+    }
+    nbytes = msc_selective_scan_bwd_workspace_size(batch, dim, L, N)
+    ws, wsb = _workspace(nbytes, dev, workspace)
+    st = lib.msc_selective_scan_bwd(
+        batch, dim, L, N, dt,
+        _dev_ptr(u, "u"), _dev_ptr(delta, "delta", tdt, (batch, dim, L)),
+        _dev_ptr(A, "A", f32, (dim, N)),
+        _dev_ptr(B, "B", tdt, (batch, N, L)), _dev_ptr(C, "C", tdt, (batch, N, L)),
+        _dev_ptr(D, "D", f32, (dim,), optional=True),
+        _dev_ptr(z, "z", tdt, (batch, dim, L), optional=True),
+        _dev_ptr(delta_bias, "delta_bias", f32, (dim,), optional=True),
+        _dev_ptr(dy, "dy", tdt, (batch, dim, L)),
+        *[(_dev_ptr(out[k], k, optional=True)) for k in
+          ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")],
+        ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream))
+    _check(st)
+    return out
+
+
+# ----------------------------------------------------------------------------- SSD
+def msc_ssd_chunked_fwd_workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups, chunk) -> int:
+    return int(load_library().msc_ssd_chunked_fwd_workspace_size(batch, seqlen, nheads, headdim,
+                                                                 dstate, ngroups, chunk))
+
+
+def msc_ssd_chunked_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, chunk=256,
+                        return_final_state=False, y=None, workspace=None, stream=None,
+                        return_workspace=False):
+    """SSD forward.  x, z: [batch, L, heads, P] bf16; delta: [batch, L, heads] bf16;
+    A, D, delta_bias: [heads] fp32; B, C: [batch, L, groups, N] bf16.
+    Returns y [batch, L, heads, P] fp32 (and the final state [batch, heads, P, N])."""
+    torch = _torch()
+    lib = load_library()
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dt = _in_dtype(x)
+    tdt = x.dtype
+    f32 = torch.float32
+    dev = x.device
+    if y is None:
+        y = torch.empty((batch, L, H, P), dtype=f32, device=dev)
+    fs = torch.empty((batch, H, P, N), dtype=f32, device=dev) if return_final_state else None
+    nbytes = msc_ssd_chunked_fwd_workspace_size(batch, L, H, P, N, G, chunk)
+    ws, wsb = _workspace(nbytes, dev, workspace)
+    st = lib.msc_ssd_chunked_fwd(
+        batch, L, H, P, N, G, chunk, dt,
+        _dev_ptr(x, "x"), _dev_ptr(delta, "delta", tdt, (batch, L, H)),
+        _dev_ptr(A, "A", f32, (H,)),
+        _dev_ptr(B, "B", tdt, (batch, L, G, N)), _dev_ptr(C, "C", tdt, (batch, L, G, N)),
+        _dev_ptr(D, "D", f32, (H,), optional=True),
+        _dev_ptr(z, "z", tdt, (batch, L, H, P), optional=True),
+        _dev_ptr(delta_bias, "delta_bias", f32, (H,), optional=True),
+        _dev_ptr(y, "y", f32, (batch, L, H, P)), _dev_ptr(fs, "final_state", optional=True),
+        ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream))
+    _check(st)
+    res = (y, fs) if return_final_state else y
+    if return_workspace:
+        return res, ws
+    return res
+
+
+def msc_check_device_status(workspace=None, stream=None):
+    """Synchronise the stream and raise if device code recorded an error
+    (for example a bounded wait that ran out) in `workspace`."""
+    ptr = workspace.data_ptr() if workspace is not None else None
+    _check(load_library().msc_check_device_status(ptr, _stream_ptr(stream)))

@@ -1,0 +1,228 @@
+// msc_api.cu -- extern "C" entry points of libmsc: argument validation,
+// workspace sizing, status reporting; the work itself is in the kernels.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "msc_common.cuh"
+#include "msc_internal.h"
+
+namespace msc_host {
+
+static thread_local char g_last_error[512] = "";
+
+msc_status fail(msc_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+void clear_error() { g_last_error[0] = 0; }
+
+msc_status check_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return MSC_OK;
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define MSC_REQUIRE(cond, ...)                                          \
+    do {                                                                \
+        if (!(cond)) return fail(MSC_ERR_INVALID_ARG, __VA_ARGS__);     \
+    } while (0)
+
+#define MSC_PTR(p, name)                                                \
+    do {                                                                \
+        MSC_REQUIRE((p) != nullptr, "%s must not be NULL", name);       \
+        MSC_REQUIRE(aligned16(p), "%s must be 16-byte aligned", name);  \
+    } while (0)
+
+#define MSC_OPT_PTR(p, name)                                            \
+    do {                                                                \
+        if ((p) != nullptr) MSC_REQUIRE(aligned16(p), "%s must be 16-byte aligned", name); \
+    } while (0)
+
+static msc_status check_s6_dims(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                msc_dtype dt) {
+    MSC_REQUIRE(batch >= 1 && dim >= 1 && seqlen >= 1, "batch, dim and seqlen must be >= 1 (got %lld, %lld, %lld)",
+                (long long)batch, (long long)dim, (long long)seqlen);
+    MSC_REQUIRE(dt == MSC_F32 || dt == MSC_BF16, "in_dtype must be MSC_F32 or MSC_BF16");
+    if (dstate < 1 || dstate > 16)
+        return fail(MSC_ERR_UNSUPPORTED, "dstate must be in [1, 16] (got %lld)", (long long)dstate);
+    if (batch > 65535) return fail(MSC_ERR_UNSUPPORTED, "batch must be <= 65535");
+    if (dim > (int64_t)1 << 36) return fail(MSC_ERR_UNSUPPORTED, "dim too large");
+    // the largest element index must fit comfortably in int64 arithmetic
+    MSC_REQUIRE(batch * dim <= ((int64_t)1 << 40) && seqlen <= ((int64_t)1 << 40) / (batch * dim) * ((int64_t)1 << 20),
+                "batch * dim * seqlen too large");
+    return MSC_OK;
+}
+
+}  // namespace msc_host
+
+using namespace msc_host;
+
+extern "C" {
+
+int msc_version(void) { return 100; }
+
+const char* msc_status_string(msc_status s) {
+    switch (s) {
+        case MSC_OK: return "MSC_OK";
+        case MSC_ERR_INVALID_ARG: return "MSC_ERR_INVALID_ARG";
+        case MSC_ERR_UNSUPPORTED: return "MSC_ERR_UNSUPPORTED";
+        case MSC_ERR_CUDA: return "MSC_ERR_CUDA";
+        case MSC_ERR_TIMEOUT: return "MSC_ERR_TIMEOUT";
+        case MSC_ERR_WORKSPACE: return "MSC_ERR_WORKSPACE";
+    }
+    return "MSC_ERR_UNKNOWN";
+}
+
+const char* msc_last_error(void) { return g_last_error; }
+
+size_t msc_selective_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
+                                             int64_t dstate) {
+    if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > 16) return 0;
+    return s6_fwd_plan(batch, dim, seqlen, dstate).workspace;
+}
+
+msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                  msc_dtype in_dtype, const void* u, const void* delta,
+                                  const float* A, const void* B, const void* C, const float* D,
+                                  const void* z, const float* delta_bias, const float* h0,
+                                  float* y, float* h_last, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    clear_error();
+    msc_status s = check_s6_dims(batch, dim, seqlen, dstate, in_dtype);
+    if (s != MSC_OK) return s;
+    MSC_PTR(u, "u"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A"); MSC_PTR(B, "B");
+    MSC_PTR(C, "C"); MSC_PTR(y, "y");
+    MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z"); MSC_OPT_PTR(delta_bias, "delta_bias");
+    MSC_OPT_PTR(h0, "h0"); MSC_OPT_PTR(h_last, "h_last");
+    S6Plan plan = s6_fwd_plan(batch, dim, seqlen, dstate);
+    if (plan.workspace > 0) {
+        if (workspace == nullptr || workspace_bytes < plan.workspace)
+            return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", plan.workspace,
+                        workspace ? workspace_bytes : (size_t)0);
+        MSC_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "workspace must be 256-byte aligned");
+    }
+    S6FwdArgs a{};
+    a.batch = batch; a.dim = dim; a.L = seqlen; a.N = (int)dstate; a.bf16 = in_dtype == MSC_BF16;
+    a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C;
+    a.A = A; a.D = D; a.delta_bias = delta_bias; a.h0 = h0; a.y = y; a.h_last = h_last;
+    a.workspace = workspace;
+    return s6_fwd_launch(a, plan, static_cast<cudaStream_t>(stream));
+}
+
+size_t msc_selective_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
+                                             int64_t dstate) {
+    if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > 16) return 0;
+    return s6_bwd_workspace(batch, dim, seqlen, dstate);
+}
+
+msc_status msc_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                  msc_dtype in_dtype, const void* u, const void* delta,
+                                  const float* A, const void* B, const void* C, const float* D,
+                                  const void* z, const float* delta_bias, const void* dy,
+                                  float* du, float* ddelta, float* dA, float* dB, float* dC,
+                                  float* dD, float* dz, float* ddelta_bias, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    clear_error();
+    msc_status s = check_s6_dims(batch, dim, seqlen, dstate, in_dtype);
+    if (s != MSC_OK) return s;
+    MSC_PTR(u, "u"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A"); MSC_PTR(B, "B");
+    MSC_PTR(C, "C"); MSC_PTR(dy, "dy");
+    MSC_PTR(du, "du"); MSC_PTR(ddelta, "ddelta"); MSC_PTR(dA, "dA"); MSC_PTR(dB, "dB"); MSC_PTR(dC, "dC");
+    MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z"); MSC_OPT_PTR(delta_bias, "delta_bias");
+    MSC_REQUIRE((D == nullptr) == (dD == nullptr), "dD must be given exactly when D is given");
+    MSC_REQUIRE((z == nullptr) == (dz == nullptr), "dz must be given exactly when z is given");
+    MSC_REQUIRE((delta_bias == nullptr) == (ddelta_bias == nullptr),
+                "ddelta_bias must be given exactly when delta_bias is given");
+    MSC_OPT_PTR(dD, "dD"); MSC_OPT_PTR(dz, "dz"); MSC_OPT_PTR(ddelta_bias, "ddelta_bias");
+    const size_t need = s6_bwd_workspace(batch, dim, seqlen, dstate);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need)
+            return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
+                        workspace ? workspace_bytes : (size_t)0);
+        MSC_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "workspace must be 256-byte aligned");
+    }
+    S6BwdArgs a{};
+    a.batch = batch; a.dim = dim; a.L = seqlen; a.N = (int)dstate; a.bf16 = in_dtype == MSC_BF16;
+    a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C; a.dy = dy;
+    a.A = A; a.D = D; a.delta_bias = delta_bias;
+    a.du = du; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dz = dz;
+    a.ddelta_bias = ddelta_bias; a.workspace = workspace;
+    return s6_bwd_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t msc_ssd_chunked_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
+                                          int64_t headdim, int64_t dstate, int64_t ngroups,
+                                          int64_t chunk) {
+    if (batch < 1 || seqlen < 1 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1 ||
+        nheads % ngroups != 0 || chunk < 1)
+        return 0;
+    return ssd_workspace(batch, seqlen, nheads, headdim, dstate, ngroups, chunk);
+}
+
+msc_status msc_ssd_chunked_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                               int64_t dstate, int64_t ngroups, int64_t chunk, msc_dtype in_dtype,
+                               const void* x, const void* delta, const float* A, const void* B,
+                               const void* C, const float* D, const void* z,
+                               const float* delta_bias, float* y, float* final_state,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    clear_error();
+    MSC_REQUIRE(batch >= 1 && seqlen >= 1 && nheads >= 1 && headdim >= 1 && dstate >= 1 && ngroups >= 1,
+                "all sizes must be >= 1");
+    MSC_REQUIRE(nheads % ngroups == 0, "ngroups (%lld) must divide nheads (%lld)", (long long)ngroups,
+                (long long)nheads);
+    MSC_REQUIRE(in_dtype == MSC_F32 || in_dtype == MSC_BF16, "in_dtype must be MSC_F32 or MSC_BF16");
+    if (in_dtype != MSC_BF16) return fail(MSC_ERR_UNSUPPORTED, "SSD supports bf16 inputs only");
+    if (headdim != 64 || dstate != 128)
+        return fail(MSC_ERR_UNSUPPORTED, "SSD supports headdim 64 and dstate 128 (got %lld, %lld)",
+                    (long long)headdim, (long long)dstate);
+    if (chunk != 64 && chunk != 128 && chunk != 256)
+        return fail(MSC_ERR_UNSUPPORTED, "chunk must be 64, 128 or 256 (got %lld)", (long long)chunk);
+    if (batch > 65535 || nheads > 65535) return fail(MSC_ERR_UNSUPPORTED, "batch and nheads must be <= 65535");
+    MSC_REQUIRE(seqlen <= ((int64_t)1 << 31), "seqlen too large");
+    MSC_PTR(x, "x"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A"); MSC_PTR(B, "B"); MSC_PTR(C, "C");
+    MSC_PTR(y, "y");
+    MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z"); MSC_OPT_PTR(delta_bias, "delta_bias");
+    MSC_OPT_PTR(final_state, "final_state");
+    const size_t need = ssd_workspace(batch, seqlen, nheads, headdim, dstate, ngroups, chunk);
+    if (workspace == nullptr || workspace_bytes < need)
+        return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    MSC_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 1023u) == 0, "workspace must be 1024-byte aligned");
+    SsdArgs a{};
+    a.batch = batch; a.L = seqlen; a.H = nheads; a.P = headdim; a.N = dstate; a.G = ngroups; a.Q = chunk;
+    a.x = x; a.delta = delta; a.B = B; a.C = C; a.z = z; a.A = A; a.D = D; a.delta_bias = delta_bias;
+    a.y = y; a.final_state = final_state; a.workspace = workspace;
+    return ssd_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+msc_status msc_check_device_status(const void* workspace, void* stream) {
+    clear_error();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    if (workspace == nullptr) return MSC_OK;
+    unsigned int word[2] = {0, 0};
+    e = cudaMemcpy(word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    if (word[0] == MSC_OK) return MSC_OK;
+    if (word[0] == MSC_ERR_TIMEOUT)
+        return fail(MSC_ERR_TIMEOUT, "device-side wait ran out (site %u)", word[1]);
+    return fail((msc_status)word[0], "device status %u (site %u)", word[0], word[1]);
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// msc_internal.h -- launcher interfaces between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "msc.h"
+
+namespace msc_host {
+
+// Status word kept at the start of any non-empty workspace (device-side errors).
+constexpr size_t kStatusBytes = 256;
+
+struct S6Plan {
+    int G = 1;            // segments per row (1 = single launch)
+    int64_t seg_len = 0;  // timesteps per segment
+    size_t workspace = 0; // bytes
+};
+
+S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
+
+struct S6FwdArgs {
+    int64_t batch, dim, L;
+    int N;
+    bool bf16;
+    const void *u, *delta, *z, *B, *C;
+    const float *A, *D, *delta_bias, *h0;
+    float *y, *h_last;
+    void* workspace;
+};
+
+msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t stream);
+
+size_t s6_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
+
+struct S6BwdArgs {
+    int64_t batch, dim, L;
+    int N;
+    bool bf16;
+    const void *u, *delta, *z, *B, *C, *dy;
+    const float *A, *D, *delta_bias;
+    float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *ddelta_bias;
+    void* workspace;
+};
+
+msc_status s6_bwd_launch(const S6BwdArgs& a, cudaStream_t stream);
+
+struct SsdArgs {
+    int64_t batch, L, H, P, N, G, Q;
+    const void *x, *delta, *B, *C, *z;
+    const float *A, *D, *delta_bias;
+    float *y, *final_state;
+    void* workspace;
+};
+
+size_t ssd_workspace(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, int64_t G,
+                     int64_t Q);
+msc_status ssd_launch(const SsdArgs& a, cudaStream_t stream);
+
+}  // namespace msc_host

@@ -1,0 +1,368 @@
+// s6_fwd.cu -- S6 selective-scan forward on sm_103a.
+//
+// What it computes (per channel row (b, d), t = 0..L-1, n < N):
+//   Delta_t = softplus(delta_t + Delta_bias[d])          selection, bqwf survey sec. 2.2
+//   abar    = exp(Delta_t A[d,n]);  h_n = abar h_n + Delta_t B[b,n,t] u_t
+//                                                         exponential-Euler, Mamba 解密 sec. 6.3
+//   y_t     = (sum_n C[b,n,t] h_n + D[d] u_t) * silu(z_t)  readout + gate, Mamba 解密 sec. 3
+//
+// Design ("row-resident" scan).  The recurrence is sequential in t and the
+// selection makes it time-varying, so it is run as a sequential loop in which
+// one lane owns one channel row and keeps all N (<= 16) fp32 states in
+// registers.  Per (t, n) this costs one MUFU ex2 (exp(Delta A) as
+// ex2(Delta * A log2 e)) and four FP32 ops -- no scan overhead at all.  Rows
+// give the parallelism (b * dim rows); a CTA is one warp owning 32 rows of one
+// batch entry, stepping through time in tiles of 32 steps.  Each tile of
+// u / delta / z (32 rows x 32 steps) and of B / C (N x 32 steps, shared by the
+// warp's rows) is loaded with coalesced 16-byte loads, converted to fp32 and
+// staged in shared memory (row stride padded by 4 floats so the per-lane
+// 16-byte reads are conflict-free, B / C transposed to [t][n] so the per-step
+// read is a broadcast).  y is written back into the delta tile in place and
+// stored with coalesced 16-byte stores.  h never leaves registers.
+//
+// Few rows and a long sequence (b * dim too small to fill 148 SMs) split each
+// row into G segments: an aggregate pass computes, from a zero state, each
+// segment's end state and sum of Delta (segment decay exp(A sum Delta)); a tiny
+// carry pass chains them (h_in(g+1) = exp(A sum Delta_g) h_in(g) + H_g); the
+// full pass then runs every segment from its carry.  The chained operator is
+// the scan composition (a, b) o (a', b') = (a a', a' b + b') of the
+// associative parallel scan (study note: Blelloch's work-efficient scan).
+#include <algorithm>
+#include <cstdio>
+
+#include "msc_common.cuh"
+#include "msc_internal.h"
+
+namespace {
+
+constexpr int kRows = 32;  // channel rows per CTA (one per lane)
+constexpr int kT = 32;     // timesteps per staged tile
+constexpr int kNS = 16;    // state slots per lane (dstate <= 16)
+constexpr int kStride = kT + 4;
+
+enum { kModeFull = 0, kModeAgg = 1 };
+
+__device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+struct FwdParams {
+    const void* u;
+    const void* delta;
+    const void* z;
+    const void* B;
+    const void* C;
+    const float* A;
+    const float* D;
+    const float* delta_bias;
+    const float* h0;
+    float* y;
+    float* h_last;
+    float* seg_state;  // [rows, G, N]: aggregates, then carries
+    float* seg_dsum;   // [rows, G]
+    int64_t dim, L, seg_len;
+    int N, G;
+};
+
+// Stage a [kRows x kT] tile of a [rows, L] tensor (rows d0.. of batch entry b),
+// timesteps t0 .. t0 + nt - 1, as fp32 into dst[row][t] (zeros outside).
+template <bool kBF16, bool kVec>
+__device__ __forceinline__ void stage_rows(float (*dst)[kStride], const void* src, int64_t row0,
+                                           int nrows, int64_t L, int64_t t0, int nt, int lane) {
+    if constexpr (kVec) {
+        // 32 rows x 4 segments of 8 steps; 4 segments per lane.
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            int s = lane + 32 * i;
+            int r = s >> 2, tt = (s & 3) * 8;
+            float v[8];
+            if (r < nrows && tt + 8 <= nt) {
+                msc::ld8<kBF16>(src, (row0 + r) * L + t0 + tt, v);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    v[k] = (r < nrows && tt + k < nt) ? msc::ld_elem<kBF16>(src, (row0 + r) * L + t0 + tt + k) : 0.f;
+            }
+            *reinterpret_cast<float4*>(&dst[r][tt]) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(&dst[r][tt + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+        }
+    } else {
+        for (int e = lane; e < kRows * kT; e += 32) {
+            int r = e / kT, tt = e % kT;
+            dst[r][tt] = (r < nrows && tt < nt) ? msc::ld_elem<kBF16>(src, (row0 + r) * L + t0 + tt) : 0.f;
+        }
+    }
+}
+
+// Stage B or C of batch entry b ([N, L] slice) transposed into dst[t][n].
+template <bool kBF16, bool kVec>
+__device__ __forceinline__ void stage_bc(float (*dst)[kNS], const void* src, int64_t b, int N,
+                                         int64_t L, int64_t t0, int nt, int lane) {
+    const int64_t base = b * (int64_t)N * L;
+    if constexpr (kVec) {
+        // 16 slots x 4 segments of 8 steps; 2 segments per lane.
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            int s = lane + 32 * i;
+            int n = s >> 2, tt = (s & 3) * 8;
+            float v[8];
+            if (n < N && tt + 8 <= nt) {
+                msc::ld8<kBF16>(src, base + n * L + t0 + tt, v);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    v[k] = (n < N && tt + k < nt) ? msc::ld_elem<kBF16>(src, base + n * L + t0 + tt + k) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) dst[tt + k][n] = v[k];
+        }
+    } else {
+        for (int e = lane; e < kNS * kT; e += 32) {
+            int n = e / kT, tt = e % kT;
+            dst[tt][n] = (n < N && tt < nt) ? msc::ld_elem<kBF16>(src, base + n * L + t0 + tt) : 0.f;
+        }
+    }
+}
+
+template <bool kVec>
+__device__ __forceinline__ void store_rows(float* dst, float (*src)[kStride], int64_t row0, int nrows,
+                                           int64_t L, int64_t t0, int nt, int lane) {
+    if constexpr (kVec) {
+        // 32 rows x 8 segments of 4 steps; 8 segments per lane.
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int s = lane + 32 * i;
+            int r = s >> 3, tt = (s & 7) * 4;
+            if (r >= nrows) continue;
+            float4 v = *reinterpret_cast<const float4*>(&src[r][tt]);
+            float* q = dst + (row0 + r) * L + t0 + tt;
+            if (tt + 4 <= nt) {
+                __stcs(reinterpret_cast<float4*>(q), v);
+            } else {
+                if (tt + 0 < nt) q[0] = v.x;
+                if (tt + 1 < nt) q[1] = v.y;
+                if (tt + 2 < nt) q[2] = v.z;
+            }
+        }
+    } else {
+        for (int e = lane; e < kRows * kT; e += 32) {
+            int r = e / kT, tt = e % kT;
+            if (r < nrows && tt < nt) dst[(row0 + r) * L + t0 + tt] = src[r][tt];
+        }
+    }
+}
+
+template <bool kBF16, bool kVec, int kMode>
+__global__ void __launch_bounds__(32) s6_fwd_rows_kernel(const FwdParams p) {
+    __shared__ __align__(16) float s_u[kRows][kStride];
+    __shared__ __align__(16) float s_d[kRows][kStride];  // delta in, y out
+    __shared__ __align__(16) float s_z[kRows][kStride];
+    __shared__ __align__(16) float s_B[kT][kNS];
+    __shared__ __align__(16) float s_C[kT][kNS];
+
+    constexpr bool kFull = (kMode == kModeFull);
+    const int lane = threadIdx.x;
+    const int64_t b = blockIdx.y;
+    const int64_t d0 = (int64_t)blockIdx.x * kRows;
+    const int nrows = (int)imin64(kRows, p.dim - d0);
+    const int64_t d = d0 + lane;
+    const bool row_ok = lane < nrows;
+    const int64_t row = b * p.dim + (row_ok ? d : d0);
+    const int seg = blockIdx.z;
+    const int N = p.N;
+    const bool has_z = kFull && p.z != nullptr;
+
+    float A2[kNS], h[kNS];
+#pragma unroll
+    for (int n = 0; n < kNS; ++n) {
+        A2[n] = (row_ok && n < N) ? __ldg(p.A + d * N + n) * MSC_LOG2E : 0.f;
+        float h_init = 0.f;
+        if (kFull && row_ok && n < N) {
+            if (p.G > 1)
+                h_init = p.seg_state[((size_t)row * p.G + seg) * N + n];
+            else if (p.h0)
+                h_init = __ldg(p.h0 + row * N + n);
+        }
+        h[n] = h_init;
+    }
+    const float Dd = (kFull && p.D && row_ok) ? __ldg(p.D + d) : 0.f;
+    const float bias = (p.delta_bias && row_ok) ? __ldg(p.delta_bias + d) : 0.f;
+    float dsum = 0.f;
+
+    const int64_t t_begin = (int64_t)seg * p.seg_len;
+    const int64_t t_end = imin64(p.L, t_begin + p.seg_len);
+    const int64_t row0 = b * p.dim + d0;
+
+    for (int64_t t0 = t_begin; t0 < t_end; t0 += kT) {
+        const int nt = (int)imin64(kT, t_end - t0);
+        __syncwarp();
+        stage_rows<kBF16, kVec>(s_u, p.u, row0, nrows, p.L, t0, nt, lane);
+        stage_rows<kBF16, kVec>(s_d, p.delta, row0, nrows, p.L, t0, nt, lane);
+        if (has_z) stage_rows<kBF16, kVec>(s_z, p.z, row0, nrows, p.L, t0, nt, lane);
+        stage_bc<kBF16, kVec>(s_B, p.B, b, N, p.L, t0, nt, lane);
+        if (kFull) stage_bc<kBF16, kVec>(s_C, p.C, b, N, p.L, t0, nt, lane);
+        __syncwarp();
+
+        for (int tq = 0; tq < nt; tq += 4) {
+            const float4 u4 = *reinterpret_cast<const float4*>(&s_u[lane][tq]);
+            const float4 d4 = *reinterpret_cast<const float4*>(&s_d[lane][tq]);
+            float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (has_z) z4 = *reinterpret_cast<const float4*>(&s_z[lane][tq]);
+            const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
+            const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+            const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+            float yy[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                yy[k] = 0.f;
+                if (tq + k < nt) {
+                    const int t = tq + k;
+                    const float dt = msc::softplus_f(dd[k] + bias);
+                    const float dtu = dt * uu[k];
+                    if (!kFull) dsum += dt;
+                    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+                    for (int q = 0; q < kNS / 4; ++q) {
+                        const float4 bq = *reinterpret_cast<const float4*>(&s_B[t][4 * q]);
+                        const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+                        float cv[4] = {0.f, 0.f, 0.f, 0.f};
+                        if (kFull) {
+                            const float4 cq = *reinterpret_cast<const float4*>(&s_C[t][4 * q]);
+                            cv[0] = cq.x; cv[1] = cq.y; cv[2] = cq.z; cv[3] = cq.w;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int n = 4 * q + j;
+                            const float a = msc::ex2_approx(dt * A2[n]);
+                            h[n] = fmaf(a, h[n], dtu * bv[j]);
+                            if (kFull) {
+                                if (j == 0) acc0 = fmaf(cv[j], h[n], acc0);
+                                if (j == 1) acc1 = fmaf(cv[j], h[n], acc1);
+                                if (j == 2) acc2 = fmaf(cv[j], h[n], acc2);
+                                if (j == 3) acc3 = fmaf(cv[j], h[n], acc3);
+                            }
+                        }
+                    }
+                    if (kFull) {
+                        float yv = (acc0 + acc1) + (acc2 + acc3) + Dd * uu[k];
+                        if (has_z) yv *= msc::silu_f(zz[k]);
+                        yy[k] = yv;
+                    }
+                }
+            }
+            if (kFull) *reinterpret_cast<float4*>(&s_d[lane][tq]) = make_float4(yy[0], yy[1], yy[2], yy[3]);
+        }
+        if (kFull) {
+            __syncwarp();
+            store_rows<kVec>(p.y, s_d, row0, nrows, p.L, t0, nt, lane);
+        }
+    }
+
+    if (!row_ok) return;
+    if (kFull) {
+        if (p.h_last && seg == p.G - 1) {
+#pragma unroll
+            for (int n = 0; n < kNS; ++n)
+                if (n < N) p.h_last[row * N + n] = h[n];
+        }
+    } else {
+#pragma unroll
+        for (int n = 0; n < kNS; ++n)
+            if (n < N) p.seg_state[((size_t)row * p.G + seg) * N + n] = h[n];
+        p.seg_dsum[(size_t)row * p.G + seg] = dsum;
+    }
+}
+
+// Chains the segment aggregates of every (row, n): carry_0 = h0 (or 0),
+// carry_{g+1} = exp(A sum Delta_g) carry_g + H_g.  Carries overwrite the
+// aggregates in place (each is read before it is overwritten, by one thread).
+__global__ void s6_seg_carry_kernel(const float* __restrict__ A, const float* __restrict__ h0,
+                                    float* seg_state, const float* __restrict__ seg_dsum,
+                                    int64_t rows, int64_t dim, int N, int G) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= rows * N) return;
+    const int64_t row = idx / N;
+    const int n = (int)(idx % N);
+    const int64_t d = row % dim;
+    const float a2 = __ldg(A + d * N + n) * MSC_LOG2E;
+    float h = h0 ? __ldg(h0 + row * N + n) : 0.f;
+    for (int g = 0; g < G; ++g) {
+        const size_t i = ((size_t)row * G + g) * N + n;
+        const float agg = seg_state[i];
+        seg_state[i] = h;
+        if (g + 1 < G) h = fmaf(msc::ex2_approx(a2 * seg_dsum[(size_t)row * G + g]), h, agg);
+    }
+}
+
+template <bool kBF16, bool kVec>
+msc_status launch_rows(const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
+    dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
+    if (mode == kModeFull)
+        s6_fwd_rows_kernel<kBF16, kVec, kModeFull><<<grid, kRows, 0, st>>>(p);
+    else
+        s6_fwd_rows_kernel<kBF16, kVec, kModeAgg><<<grid, kRows, 0, st>>>(p);
+    return msc_host::check_launch("s6_fwd_rows");
+}
+
+msc_status launch_mode(const FwdParams& p, bool bf16, bool vec, int64_t batch, int G, int mode,
+                       cudaStream_t st) {
+    if (bf16) return vec ? launch_rows<true, true>(p, batch, G, mode, st) : launch_rows<true, false>(p, batch, G, mode, st);
+    return vec ? launch_rows<false, true>(p, batch, G, mode, st) : launch_rows<false, false>(p, batch, G, mode, st);
+}
+
+}  // namespace
+
+namespace msc_host {
+
+S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
+    S6Plan plan;
+    const int64_t rows = batch * dim;
+    // Enough rows to keep every SM busy with ~8 resident warps: one pass.
+    const int64_t target = (int64_t)num_sms() * 8 * 32;
+    int64_t G = 1;
+    if (rows < target) G = (target + rows - 1) / rows;
+    const int64_t min_seg = 512;
+    G = std::min<int64_t>(G, std::max<int64_t>(1, seqlen / min_seg));
+    G = std::min<int64_t>(G, 65535);
+    if (G <= 1) {
+        plan.G = 1;
+        plan.seg_len = seqlen;
+        plan.workspace = 0;
+        return plan;
+    }
+    int64_t seg = (seqlen + G - 1) / G;
+    seg = (seg + kT - 1) / kT * kT;
+    G = (seqlen + seg - 1) / seg;
+    plan.G = (int)G;
+    plan.seg_len = seg;
+    plan.workspace = kStatusBytes + (size_t)rows * G * (size_t)dstate * sizeof(float) +
+                     (size_t)rows * G * sizeof(float) + 256;
+    return plan;
+}
+
+msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st) {
+    FwdParams p{};
+    p.u = a.u; p.delta = a.delta; p.z = a.z; p.B = a.B; p.C = a.C;
+    p.A = a.A; p.D = a.D; p.delta_bias = a.delta_bias; p.h0 = a.h0;
+    p.y = a.y; p.h_last = a.h_last;
+    p.dim = a.dim; p.L = a.L; p.N = a.N; p.G = plan.G; p.seg_len = plan.seg_len;
+    // 16-byte vector loads need every row and tile start 16-byte aligned:
+    // bases are checked by the caller; rows start at row * L elements.
+    const bool vec = (a.L % 8) == 0;
+    if (plan.G > 1) {
+        char* ws = static_cast<char*>(a.workspace) + kStatusBytes;
+        p.seg_state = reinterpret_cast<float*>(ws);
+        size_t off = (size_t)(a.batch * a.dim) * plan.G * a.N * sizeof(float);
+        off = (off + 255) / 256 * 256;
+        p.seg_dsum = reinterpret_cast<float*>(ws + off);
+        msc_status s = launch_mode(p, a.bf16, vec, a.batch, plan.G - 1, kModeAgg, st);
+        if (s != MSC_OK) return s;
+        const int64_t total = a.batch * a.dim * a.N;
+        const int threads = 256;
+        s6_seg_carry_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
+            a.A, a.h0, p.seg_state, p.seg_dsum, a.batch * a.dim, a.dim, a.N, plan.G);
+        s = check_launch("s6_seg_carry");
+        if (s != MSC_OK) return s;
+    }
+    return launch_mode(p, a.bf16, vec, a.batch, plan.G, kModeFull, st);
+}
+
+}  // namespace msc_host

@@ -16,3 +16,18 @@ def pytest_configure(config):
 def cuda_available():
     import torch
     return torch.cuda.is_available()
+
+
+def pytest_collection_modifyitems(config, items):
+    """GPU tests are skipped only where no CUDA device is visible at all."""
+    try:
+        import torch
+        have_gpu = torch.cuda.is_available()
+    except Exception:
+        have_gpu = False
+    if have_gpu:
+        return
+    skip = pytest.mark.skip(reason="no CUDA device visible")
+    for item in items:
+        if "gpu" in item.keywords:
+            item.add_marker(skip)

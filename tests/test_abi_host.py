@@ -1,0 +1,117 @@
+"""Host-only checks of the C ABI: the library loads, exports every symbol that
+include/msc.h declares, and rejects bad arguments before launching anything.
+No test here needs a GPU (no compute call reaches a kernel)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import selective_state_space_160_b300 as msc
+from selective_state_space_160_b300 import build as msc_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    msc_build.build()
+    return msc.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "msc.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(msc_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd",
+              "msc_check_device_status", "msc_status_string", "msc_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", msc.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (msc_[a-z0-9_]+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # the python binding declares a signature for every exported entry point
+    assert set(declared_functions()) <= set(msc.SIGNATURES)
+
+
+def test_status_strings(lib):
+    assert msc.msc_status_string(0) == "MSC_OK"
+    assert msc.msc_status_string(4) == "MSC_ERR_TIMEOUT"
+    assert msc.msc_status_string(99) == "MSC_ERR_UNKNOWN"
+
+
+def _fwd(lib, **kw):
+    args = dict(batch=1, dim=4, L=64, N=16, dt=0, u=16, delta=16, A=16, B=16, C=16, D=None, z=None,
+                bias=None, h0=None, y=16, hl=None, ws=None, wsb=0)
+    args.update(kw)
+    return lib.msc_selective_scan_fwd(args["batch"], args["dim"], args["L"], args["N"], args["dt"],
+                                      args["u"], args["delta"], args["A"], args["B"], args["C"],
+                                      args["D"], args["z"], args["bias"], args["h0"], args["y"],
+                                      args["hl"], args["ws"], args["wsb"], None)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    assert _fwd(lib, u=None) == msc.MSC_ERR_INVALID_ARG
+    assert "u must not be NULL" in msc.msc_last_error()
+    assert _fwd(lib, y=None) == msc.MSC_ERR_INVALID_ARG
+    assert _fwd(lib, u=18) == msc.MSC_ERR_INVALID_ARG          # misaligned
+    assert "aligned" in msc.msc_last_error()
+    assert _fwd(lib, L=0) == msc.MSC_ERR_INVALID_ARG
+    assert _fwd(lib, batch=-1) == msc.MSC_ERR_INVALID_ARG
+    assert _fwd(lib, dt=7) == msc.MSC_ERR_INVALID_ARG
+    assert _fwd(lib, N=17) == msc.MSC_ERR_UNSUPPORTED
+    assert _fwd(lib, N=0) == msc.MSC_ERR_UNSUPPORTED
+    assert _fwd(lib, z=20) == msc.MSC_ERR_INVALID_ARG
+
+
+def test_fwd_workspace_query_and_check(lib):
+    # plenty of rows: single pass, no workspace
+    assert msc.msc_selective_scan_fwd_workspace_size(8, 5120, 2048, 16) == 0
+    # few rows and a long sequence: segments need a workspace
+    need = msc.msc_selective_scan_fwd_workspace_size(1, 1536, 1 << 20, 16)
+    assert need > 0
+    assert _fwd(lib, batch=1, dim=1536, L=1 << 20) == msc.MSC_ERR_WORKSPACE
+    assert _fwd(lib, batch=1, dim=1536, L=1 << 20, ws=4096, wsb=need - 1) == msc.MSC_ERR_WORKSPACE
+    assert msc.msc_selective_scan_fwd_workspace_size(0, 4, 4, 4) == 0
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    f = lib.msc_selective_scan_bwd
+    ok = [16] * 5
+    # dD must accompany D
+    st = f(1, 4, 64, 16, 0, *ok, 16, None, None, 16, 16, 16, 16, 16, 16, None, None, None, None, 0, None)
+    assert st == msc.MSC_ERR_INVALID_ARG and "dD" in msc.msc_last_error()
+    st = f(1, 4, 64, 16, 0, *ok, None, 16, None, 16, 16, 16, 16, 16, 16, None, None, None, None, 0, None)
+    assert st == msc.MSC_ERR_INVALID_ARG and "dz" in msc.msc_last_error()
+    st = f(1, 4, 64, 16, 0, *ok, None, None, None, None, 16, 16, 16, 16, 16, None, None, None, None, 0, None)
+    assert st == msc.MSC_ERR_INVALID_ARG and "dy" in msc.msc_last_error()
+
+
+def test_ssd_rejects_bad_arguments(lib):
+    f = lib.msc_ssd_chunked_fwd
+
+    def call(b=1, L=256, H=4, P=64, N=128, G=1, Q=256, dt=1, ws=1024, wsb=1 << 30):
+        return f(b, L, H, P, N, G, Q, dt, 16, 16, 16, 16, 16, None, None, None, 16, None, ws, wsb, None)
+
+    assert call(G=3) == msc.MSC_ERR_INVALID_ARG
+    assert call(P=32) == msc.MSC_ERR_UNSUPPORTED
+    assert call(N=64) == msc.MSC_ERR_UNSUPPORTED
+    assert call(Q=100) == msc.MSC_ERR_UNSUPPORTED
+    assert call(dt=0) == msc.MSC_ERR_UNSUPPORTED
+    assert call(ws=None, wsb=0) == msc.MSC_ERR_WORKSPACE
+    assert call(ws=2048 + 16) == msc.MSC_ERR_INVALID_ARG        # workspace misaligned
+
+
+def test_check_device_status_null_workspace_signature(lib):
+    # only the signature is checked here; calling it needs a CUDA context
+    assert lib.msc_check_device_status.restype == ctypes.c_int

@@ -1,0 +1,131 @@
+"""GPU parity of the S6 forward (through the C ABI) against the CPU oracle.
+
+Tolerances (max |gpu - ref| / (1 + |ref|)): 1e-4 with fp32 inputs, 2e-3 with
+bf16 inputs (the oracle consumes the same bf16-rounded values)."""
+import numpy as np
+import pytest
+
+from oracle import oracle
+from selective_state_space_160_b300.inputs import s6_inputs, s6_inputs_torch
+from helpers import max_rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-4
+TOL_BF16 = 2e-3
+
+
+def _run(inp, bf16, h0=None, return_last_state=False):
+    import selective_state_space_160_b300 as msc
+    dev = {k: to_dev(inp[k], bf16) for k in ("u", "delta", "z", "B", "C")}
+    out = msc.msc_selective_scan_fwd(
+        dev["u"], dev["delta"], to_dev(inp["A"]), dev["B"], dev["C"],
+        to_dev(inp["D"]), dev["z"], to_dev(inp["delta_bias"]),
+        h0=to_dev(h0) if h0 is not None else None, return_last_state=return_last_state)
+    if return_last_state:
+        return out[0].cpu().numpy(), out[1].cpu().numpy()
+    return out.cpu().numpy()
+
+
+def _ref(inp, h0=None, return_last_state=False):
+    return oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                         inp["delta_bias"], h0=h0, return_last_state=return_last_state)
+
+
+def test_tiny_config_fp32():
+    """batch 1, 4 channels, L = 64, N = 16, fp32."""
+    inp = s6_inputs(1, 4, 64, 16, seed=160_000)
+    y = _run(inp, False)
+    assert max_rel_err(y, _ref(inp)) <= TOL_F32
+
+
+@pytest.mark.parametrize("batch,dim,L,N", [
+    (1, 1, 1, 16), (1, 5, 7, 16), (2, 37, 33, 16), (3, 70, 100, 3), (1, 33, 64, 1),
+    (2, 64, 257, 16), (1, 32, 1000, 8), (2, 31, 96, 16)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_shapes(batch, dim, L, N, bf16):
+    inp = s6_inputs(batch, dim, L, N, seed=1000 + batch * 7 + dim + L + N, bf16=bf16)
+    y = _run(inp, bf16)
+    assert max_rel_err(y, _ref(inp)) <= (TOL_BF16 if bf16 else TOL_F32)
+
+
+@pytest.mark.parametrize("with_z,with_D,with_bias", [(False, True, True), (True, False, True),
+                                                     (True, True, False), (False, False, False)])
+def test_optional_inputs(with_z, with_D, with_bias):
+    inp = s6_inputs(2, 40, 72, 16, seed=77, with_z=with_z, with_D=with_D, with_bias=with_bias)
+    y = _run(inp, False)
+    assert max_rel_err(y, _ref(inp)) <= TOL_F32
+
+
+def test_initial_and_final_state():
+    inp = s6_inputs(2, 36, 80, 16, seed=5)
+    h0 = np.random.default_rng(0).standard_normal((2, 36, 16)).astype(np.float32)
+    y, hl = _run(inp, False, h0=h0, return_last_state=True)
+    ry, rh = _ref(inp, h0=h0, return_last_state=True)
+    assert max_rel_err(y, ry) <= TOL_F32
+    assert max_rel_err(hl, rh) <= TOL_F32
+
+
+@pytest.mark.parametrize("L", [4096, 5000, 12345])
+def test_long_sequence_segments(L):
+    """Few rows: the sequence is split into segments chained by carries."""
+    import selective_state_space_160_b300 as msc
+    assert msc.msc_selective_scan_fwd_workspace_size(1, 3, L, 16) > 0
+    inp = s6_inputs(1, 3, L, 16, seed=L)
+    h0 = np.random.default_rng(1).standard_normal((1, 3, 16)).astype(np.float32)
+    y, hl = _run(inp, False, h0=h0, return_last_state=True)
+    ry, rh = _ref(inp, h0=h0, return_last_state=True)
+    assert max_rel_err(y, ry) <= TOL_F32
+    assert max_rel_err(hl, rh) <= TOL_F32
+
+
+def test_long_sequence_segments_bf16_ragged():
+    inp = s6_inputs(2, 5, 6001, 16, seed=9, bf16=True)
+    y = _run(inp, True)
+    assert max_rel_err(y, _ref(inp)) <= TOL_BF16
+
+
+def test_mamba_layer_config_bf16_sampled():
+    """batch 8, D 5120, L 2048, N 16, bf16 inputs, full-size launch; parity on 8
+    sampled channels of every batch entry (the oracle computes those rows)."""
+    inp = s6_inputs(8, 5120, 2048, 16, seed=160_001, bf16=True)
+    y = _run(inp, True)
+    assert np.all(np.isfinite(y))
+    ds = np.array([0, 1, 31, 32, 1000, 2047, 4095, 5119])
+    sub = dict(inp)
+    for k in ("u", "delta", "z"):
+        sub[k] = inp[k][:, ds, :]
+    sub["A"], sub["D"], sub["delta_bias"] = inp["A"][ds], inp["D"][ds], inp["delta_bias"][ds]
+    assert max_rel_err(y[:, ds, :], _ref(sub)) <= TOL_BF16
+
+
+def test_long_sequence_config_fp32_sampled():
+    """batch 1, D 1536, L 2^20, N 16, fp32, full-size launch (segmented); parity
+    on sampled channels, whole-sequence."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    L = 1 << 20
+    inp = s6_inputs_torch(1, 1536, L, 16, seed=160_002, bf16=False)
+    y, hl = msc.msc_selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                       inp["D"], inp["z"], inp["delta_bias"], return_last_state=True)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(y).all())
+    ds = [0, 511, 1024, 1535]
+    host = {k: inp[k].cpu().numpy() for k in ("B", "C", "A", "D", "delta_bias")}
+    for d in ds:
+        sub = {k: inp[k][:, d:d + 1, :].cpu().numpy() for k in ("u", "delta", "z")}
+        sub.update(B=host["B"], C=host["C"], A=host["A"][d:d + 1], D=host["D"][d:d + 1],
+                   delta_bias=host["delta_bias"][d:d + 1])
+        ry, rh = _ref(sub, return_last_state=True)
+        assert max_rel_err(y[:, d:d + 1, :].cpu().numpy(), ry) <= TOL_F32, d
+        assert max_rel_err(hl[:, d:d + 1, :].cpu().numpy(), rh) <= TOL_F32, d
+    del inp, y, hl
+    torch.cuda.empty_cache()
+
+
+def test_repeat_calls_identical():
+    """The forward has no atomics: two calls give bit-identical results."""
+    inp = s6_inputs(2, 64, 300, 16, seed=3, bf16=True)
+    y1 = _run(inp, True)
+    y2 = _run(inp, True)
+    assert np.array_equal(y1, y2)
