@@ -87,10 +87,9 @@ class ClockSampler:
         self.sel = []
         try:
             import torch
-            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-            if uuid and not uuid.startswith("GPU-"):
-                uuid = "GPU-" + uuid
-            self.sel = ["-i", uuid] if uuid else []
+            raw = bytes(torch.cuda.get_device_properties(device_index).uuid.bytes).hex()
+            uuid = "GPU-%s-%s-%s-%s-%s" % (raw[:8], raw[8:12], raw[12:16], raw[16:20], raw[20:32])
+            self.sel = ["-i", uuid]
         except Exception:
             self.sel = []
 
@@ -323,7 +322,7 @@ def cpu_oracle_sample(target_s=12.0, max_rows=None):
     oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["delta_bias"])
     dt = time.perf_counter() - t0
     rate = b * dim * L / dt
-    dim2 = int(max(8, min(512, rate * target_s / (b * L))))
+    dim2 = int(max(8, min(HEADLINE["dim"], rate * target_s / (b * L))))
     if max_rows:
         dim2 = min(dim2, max_rows)
     inp = s6_inputs(b, dim2, L, N, seed=160_001, bf16=True)

@@ -1,19 +1,23 @@
 /*
  * msc.h -- C ABI of libmsc, the B300 (sm_103a) Mamba selective scan.
  *
- * Three operations, as the pages state the problem:
+ * Three operations, as the pages state the problem.  Pages are cited by title:
+ * "Mamba — 选择性状态空间模型" (study note), bqwf survey (the Mamba survey
+ * article on bqwf.cn, whose title did not survive extraction),
+ * "Mamba前世今生全挖掘", "Review: Mamba — Linear-Time Sequence Modeling with
+ * Selective State Spaces", and "Mamba 解密".
  *
- *  - S6 forward.  Selection Delta_t = softplus(delta_t + Delta_bias) ("Mamba: A
- *    Survey" sec. 2.2; "Mamba decoded" sec. 5), exponential-Euler recurrence
- *    h_t = exp(Delta_t A) (.) h_{t-1} + Delta_t B_t u_t ("Mamba decoded" sec. 6.3:
- *    Mamba-1/2 are exponential-Euler), readout y_t = C_t . h_t + D u_t ("Mamba
- *    decoded" sec. 3, D feed-through), gated by silu(z_t) ("Mamba: past and present",
+ *  - S6 forward.  Selection Delta_t = softplus(delta_t + Delta_bias) (bqwf survey sec. 2.2;
+ *    "Mamba 解密" sec. 5), exponential-Euler recurrence
+ *    h_t = exp(Delta_t A) (.) h_{t-1} + Delta_t B_t u_t ("Mamba 解密" sec. 6.3:
+ *    Mamba-1/2 are exponential-Euler), readout y_t = C_t . h_t + D u_t ("Mamba 解密"
+ *    sec. 3, D feed-through), gated by silu(z_t) ("Mamba前世今生全挖掘" sec. 二,
  *    selective SSM + gating).
  *  - S6 backward by recomputation: states are recomputed on chip and never
- *    stored to global memory ("Mamba: A Survey" sec. 2.2, recomputation).
+ *    stored to global memory (bqwf survey sec. 2.2, recomputation).
  *  - Mamba-2 SSD chunked forward: scalar A per head (A_t = alpha_t I), the
- *    semiseparable form Y = M (X . B^T) C with M_ij = a_{j+1}...a_i ("Mamba: A
- *    Survey" sec. 3.2; "Mamba decoded" sec. 6.2), computed by the block
+ *    semiseparable form Y = M (X . B^T) C with M_ij = a_{j+1}...a_i (bqwf
+ *    survey sec. 3.2; "Mamba 解密" sec. 6.2), computed by the block
  *    decomposition on tcgen05 tensor cores.
  *
  * Conventions shared by every entry point
@@ -62,7 +66,9 @@ typedef enum { MSC_F32 = 0, MSC_BF16 = 1 } msc_dtype;
  * Limits: batch, dim, seqlen >= 1; 1 <= dstate <= 16.
  * Long sequences with few rows are split into segments whose carries are
  * combined in the workspace (three launches); otherwise one launch, and the
- * workspace size is 0. */
+ * workspace size is 0.  Rows whose byte stride (seqlen * element size) is a
+ * multiple of 16 are streamed with TMA; other lengths take a plain-load kernel
+ * with identical arithmetic. */
 size_t msc_selective_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
                                              int64_t dstate);
 
@@ -104,7 +110,7 @@ msc_status msc_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, in
  * nheads; chunk in {64, 128, 256}; seqlen >= 1 (ragged last chunk allowed).
  * The result does not depend on `chunk` beyond rounding: it only sets where
  * the chunk states are materialised.  A device-side bounded wait that runs out
- * records MSC_ERR_TIMEOUT in the workspace (msc_check_device_status). */
+ * is reported by msc_check_device_status(). */
 size_t msc_ssd_chunked_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
                                           int64_t headdim, int64_t dstate, int64_t ngroups,
                                           int64_t chunk);
@@ -118,11 +124,13 @@ msc_status msc_ssd_chunked_fwd(int64_t batch, int64_t seqlen, int64_t nheads, in
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------- utilities
- * msc_check_device_status: synchronises `stream`, then reads the status word
- * that device code keeps at the start of `workspace` (the workspace of the last
- * call that used it).  Returns MSC_OK, MSC_ERR_TIMEOUT, or MSC_ERR_CUDA if the
- * stream itself reports an error.  A NULL workspace returns MSC_OK after the sync. */
-msc_status msc_check_device_status(const void* workspace, void* stream);
+ * msc_check_device_status: synchronises `stream`, then reads and clears the
+ * device status words that the library's kernels keep on the current device
+ * (one per kernel module, in device global memory).  A kernel whose bounded
+ * wait on an mbarrier ran out (about one second) records MSC_ERR_TIMEOUT and
+ * the site there, and returns instead of hanging.  Returns MSC_OK,
+ * MSC_ERR_TIMEOUT, or MSC_ERR_CUDA if the stream itself reports an error. */
+msc_status msc_check_device_status(void* stream);
 
 /* Static English name of a status code. */
 const char* msc_status_string(msc_status status);

@@ -7,23 +7,23 @@
  * pages' definitions, one sequential step at a time, with no blocking, fusion or
  * reordering:
  *
- *   Selection (survey article "Mamba" sec. 2.2; translated article sec. 5):
+ *   Selection (bqwf survey sec. 2.2; "Mamba 解密" sec. 5):
  *       Delta_t = softplus(delta_t + Delta_bias)
- *   Exponential-Euler discretisation (translated article sec. 6.3, "Mamba-1 and
- *   Mamba-2 use exponential-Euler"; recurrence of sec. 3/5 with the Euler input):
+ *   Exponential-Euler discretisation ("Mamba 解密" sec. 6.3: Mamba-1 and
+ *   Mamba-2 are exponential-Euler; recurrence of its sec. 3/5 with the Euler input):
  *       abar_{t,n} = exp(Delta_t * A[n])
  *       h_{t,n}    = abar_{t,n} * h_{t-1,n} + Delta_t * B_{t,n} * u_t
- *   Readout with direct feed-through D (translated article sec. 3):
+ *   Readout with direct feed-through D ("Mamba 解密" sec. 3):
  *       y'_t = sum_n C_{t,n} h_{t,n} + D * u_t
- *   Gate (juejin blog: "selective SSM + gating"):  y_t = y'_t * silu(z_t)
+ *   Gate ("Mamba前世今生全挖掘" sec. 二: selective SSM plus gating):  y_t = y'_t * silu(z_t)
  *
- *   SSD (survey article sec. 3.2: scalar A_t = alpha_t I; translated article
+ *   SSD (bqwf survey sec. 3.2: scalar A_t = alpha_t I; "Mamba 解密"
  *   sec. 6.2: M_ij = a_{j+1} ... a_i): per head the state is a P x N matrix
  *       H_t = a_t H_{t-1} + Delta_t x_t B_t^T,   y_t = H_t C_t (+ D x_t)(* silu z_t)
  *   which is the S6 recurrence with channels d = (head, p) sharing Delta and A.
  *
  * The backward is hand-derived from the forward (the pages only say that the
- * gradient recomputes states instead of storing them, survey article sec. 2.2):
+ * gradient recomputes states instead of storing them, bqwf survey sec. 2.2):
  *   g'_t = dy_t * silu(z_t)
  *   dz_t = dy_t * y'_t * sig(z_t) * (1 + z_t (1 - sig(z_t)))
  *   lambda_{t,n} = g'_t C_{t,n} + abar_{t+1,n} lambda_{t+1,n}    (lambda_{L} = 0)

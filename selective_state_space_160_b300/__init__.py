@@ -41,7 +41,7 @@ SIGNATURES = {
     "msc_selective_scan_bwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 9 + [_vp] * 8 + [_vp, _sz, _vp]),
     "msc_ssd_chunked_fwd_workspace_size": (_sz, [_i64] * 7),
     "msc_ssd_chunked_fwd": (ctypes.c_int, [_i64] * 7 + [ctypes.c_int] + [_vp] * 10 + [_vp, _sz, _vp]),
-    "msc_check_device_status": (ctypes.c_int, [_vp, _vp]),
+    "msc_check_device_status": (ctypes.c_int, [_vp]),
     "msc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "msc_last_error": (ctypes.c_char_p, []),
     "msc_version": (ctypes.c_int, []),
@@ -273,8 +273,7 @@ def msc_ssd_chunked_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, chun
     return res
 
 
-def msc_check_device_status(workspace=None, stream=None):
+def msc_check_device_status(stream=None):
     """Synchronise the stream and raise if device code recorded an error
-    (for example a bounded wait that ran out) in `workspace`."""
-    ptr = workspace.data_ptr() if workspace is not None else None
-    _check(load_library().msc_check_device_status(ptr, _stream_ptr(stream)))
+    (a bounded wait that ran out); reading clears the recorded error."""
+    _check(load_library().msc_check_device_status(_stream_ptr(stream)))

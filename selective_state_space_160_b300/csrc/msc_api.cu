@@ -1,11 +1,15 @@
 // msc_api.cu -- extern "C" entry points of libmsc: argument validation,
 // workspace sizing, status reporting; the work itself is in the kernels.
+#include <cudaTypedefs.h>
+
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "msc_common.cuh"
 #include "msc_internal.h"
+#include "msc_tma.cuh"
 
 namespace msc_host {
 
@@ -33,6 +37,43 @@ int num_sms() {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         return 148;
     return n;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) {
+        fail(MSC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    cuuint64_t gd[5];
+    cuuint64_t gs[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) gs[i] = strides_bytes[i];
+    }
+    CUresult r = g_encode(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        fail(MSC_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+        return false;
+    }
+    return true;
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -210,19 +251,21 @@ msc_status msc_ssd_chunked_fwd(int64_t batch, int64_t seqlen, int64_t nheads, in
     return ssd_launch(a, static_cast<cudaStream_t>(stream));
 }
 
-msc_status msc_check_device_status(const void* workspace, void* stream) {
+msc_status msc_check_device_status(void* stream) {
     clear_error();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
-    if (workspace == nullptr) return MSC_OK;
-    unsigned int word[2] = {0, 0};
-    e = cudaMemcpy(word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
-    if (word[0] == MSC_OK) return MSC_OK;
-    if (word[0] == MSC_ERR_TIMEOUT)
-        return fail(MSC_ERR_TIMEOUT, "device-side wait ran out (site %u)", word[1]);
-    return fail((msc_status)word[0], "device status %u (site %u)", word[0], word[1]);
+    unsigned int code = 0, site = 0;
+    msc_status s = s6_fwd_take_status(&code, &site);
+    if (s != MSC_OK) return s;
+    if (code == 0) {
+        s = ssd_take_status(&code, &site);
+        if (s != MSC_OK) return s;
+    }
+    if (code == 0) return MSC_OK;
+    if (code == MSC_ERR_TIMEOUT) return fail(MSC_ERR_TIMEOUT, "device-side wait ran out (site %u)", site);
+    return fail((msc_status)code, "device status %u (site %u)", code, site);
 }
 
 }  // extern "C"

@@ -9,9 +9,6 @@
 
 namespace msc_host {
 
-// Status word kept at the start of any non-empty workspace (device-side errors).
-constexpr size_t kStatusBytes = 256;
-
 struct S6Plan {
     int G = 1;            // segments per row (1 = single launch)
     int64_t seg_len = 0;  // timesteps per segment
@@ -31,6 +28,11 @@ struct S6FwdArgs {
 };
 
 msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t stream);
+
+// Each translation unit with bounded device-side waits keeps its own status
+// word (code, site); these read and clear it.
+msc_status s6_fwd_take_status(unsigned int* code, unsigned int* site);
+msc_status ssd_take_status(unsigned int* code, unsigned int* site);
 
 size_t s6_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
 

@@ -12,13 +12,22 @@
 // registers.  Per (t, n) this costs one MUFU ex2 (exp(Delta A) as
 // ex2(Delta * A log2 e)) and four FP32 ops -- no scan overhead at all.  Rows
 // give the parallelism (b * dim rows); a CTA is one warp owning 32 rows of one
-// batch entry, stepping through time in tiles of 32 steps.  Each tile of
-// u / delta / z (32 rows x 32 steps) and of B / C (N x 32 steps, shared by the
-// warp's rows) is loaded with coalesced 16-byte loads, converted to fp32 and
-// staged in shared memory (row stride padded by 4 floats so the per-lane
-// 16-byte reads are conflict-free, B / C transposed to [t][n] so the per-step
-// read is a broadcast).  y is written back into the delta tile in place and
-// stored with coalesced 16-byte stores.  h never leaves registers.
+// batch entry, stepping through time in tiles of 64-byte rows (32 bf16 or 16
+// fp32 steps).
+//
+// Main kernel (s6_fwd_tma_kernel): one lane issues 3-D TMA tile loads of
+// u / delta / z (32 rows x one tile) and B / C (16 slots x one tile, shared by
+// the warp's rows) into a two-stage shared-memory ring completed on mbarriers,
+// so the next tile streams in while the current one is computed.  Out-of-range
+// rows, slots and steps arrive zero-filled.  Each lane reads its own row with
+// 16-byte loads (64-byte swizzle: conflict-free), computes Delta, Delta*u and
+// D*u for 8 steps at a time, then runs the n loop on packed fp32 pairs
+// (fma.rn.f32x2: two states per issue slot) with B / C converted once per tile
+// into an n-pair-interleaved fp32 layout (each pair is one 64-bit operand, a
+// broadcast read).  y is stored from registers as 32-byte row segments.
+// Rows whose byte stride is not a multiple of 16 cannot be described to TMA;
+// they take the plain-load kernel (s6_fwd_rows_kernel), which stages each tile
+// with coalesced loads and computes the same way in scalar fp32.
 //
 // Few rows and a long sequence (b * dim too small to fill 148 SMs) split each
 // row into G segments: an aggregate pass computes, from a zero state, each
@@ -29,9 +38,11 @@
 // associative parallel scan (study note: Blelloch's work-efficient scan).
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 
 #include "msc_common.cuh"
 #include "msc_internal.h"
+#include "msc_tma.cuh"
 
 namespace {
 
@@ -271,6 +282,299 @@ __global__ void __launch_bounds__(32) s6_fwd_rows_kernel(const FwdParams p) {
     }
 }
 
+
+// --------------------------------------------------------------------------
+// Device status word of this module: (code, site) of the first bounded wait
+// that ran out.  Read and cleared by msc_check_device_status().
+__device__ unsigned int g_s6_fwd_status[2];
+
+__device__ __forceinline__ void record_timeout(unsigned int site) {
+    if (atomicCAS(&g_s6_fwd_status[0], 0u, (unsigned int)MSC_ERR_TIMEOUT) == 0u)
+        g_s6_fwd_status[1] = site;
+}
+
+// Wait for phase `parity` of `bar`, giving up after about one second.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
+    if (msc::mbar_wait(bar, parity, 256)) return true;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    while (true) {
+        if (msc::mbar_try_wait(bar, parity)) return true;
+        uint64_t t1;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+        if (t1 - t0 > 1000000000ull) return false;
+    }
+}
+
+constexpr int kStages = 2;
+constexpr int kRowTile = 2048;               // bytes of one 32-row x 64-byte tile
+constexpr int kBCTile = 1024;                // bytes of one 16-slot x 64-byte tile
+constexpr int kStageBytes = 3 * kRowTile + 2 * kBCTile;
+
+template <bool kBF16, int kMode>
+__global__ void __launch_bounds__(32) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
+                                                        const __grid_constant__ CUtensorMap tm_d,
+                                                        const __grid_constant__ CUtensorMap tm_z,
+                                                        const __grid_constant__ CUtensorMap tm_B,
+                                                        const __grid_constant__ CUtensorMap tm_C,
+                                                        const FwdParams p) {
+    constexpr bool kFull = (kMode == kModeFull);
+    constexpr int kTT = kBF16 ? 32 : 16;  // steps per 64-byte tile row
+    constexpr int kGroups = kTT / 8;
+    __shared__ __align__(1024) uint8_t s_raw[kStages][kStageBytes];
+    __shared__ __align__(16) float s_bc[2][kNS / 2][kTT][2];  // [B|C][n pair][t][n parity]
+    __shared__ __align__(8) uint64_t s_full[kStages];
+
+    const int lane = threadIdx.x;
+    const int64_t b = blockIdx.y;
+    const int64_t d0 = (int64_t)blockIdx.x * kRows;
+    const int nrows = (int)imin64(kRows, p.dim - d0);
+    const bool row_ok = lane < nrows;
+    const int64_t d = row_ok ? d0 + lane : d0;
+    const int64_t row = b * p.dim + d;
+    const int seg = blockIdx.z;
+    const int N = p.N;
+    const bool has_z = kFull && p.z != nullptr;
+
+    uint64_t A2p[kNS / 2], h2[kNS / 2];
+#pragma unroll
+    for (int q = 0; q < kNS / 2; ++q) {
+        float a[2], h[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int n = 2 * q + j;
+            a[j] = (row_ok && n < N) ? __ldg(p.A + d * N + n) * MSC_LOG2E : 0.f;
+            h[j] = 0.f;
+            if (kFull && row_ok && n < N) {
+                if (p.G > 1)
+                    h[j] = p.seg_state[((size_t)row * p.G + seg) * N + n];
+                else if (p.h0)
+                    h[j] = __ldg(p.h0 + row * N + n);
+            }
+        }
+        A2p[q] = msc::pk2(a[0], a[1]);
+        h2[q] = msc::pk2(h[0], h[1]);
+    }
+    const float Dd = (kFull && p.D && row_ok) ? __ldg(p.D + d) : 0.f;
+    const float bias = (p.delta_bias && row_ok) ? __ldg(p.delta_bias + d) : 0.f;
+    float dsum = 0.f;
+
+    const int64_t t_begin = (int64_t)seg * p.seg_len;
+    const int64_t t_end = imin64(p.L, t_begin + p.seg_len);
+    const int ntiles = (int)((t_end - t_begin + kTT - 1) / kTT);
+    const uint32_t tx_bytes = kRowTile * (has_z ? 3 : 2) + kBCTile * (kFull ? 2 : 1);
+
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) msc::mbar_init(&s_full[s], 1);
+        msc::fence_barrier_init();
+        msc::prefetch_tmap(&tm_u);
+        msc::prefetch_tmap(&tm_d);
+        msc::prefetch_tmap(&tm_B);
+        if (has_z) msc::prefetch_tmap(&tm_z);
+        if (kFull) msc::prefetch_tmap(&tm_C);
+    }
+    __syncwarp();
+
+    auto issue = [&](int j) {
+        const int s = j % kStages;
+        const int tj = (int)(t_begin + (int64_t)j * kTT);
+        uint8_t* st = s_raw[s];
+        msc::mbar_arrive_expect_tx(&s_full[s], tx_bytes);
+        msc::tma_load_3d(st, &tm_u, &s_full[s], tj, (int)d0, (int)b);
+        msc::tma_load_3d(st + kRowTile, &tm_d, &s_full[s], tj, (int)d0, (int)b);
+        if (has_z) msc::tma_load_3d(st + 2 * kRowTile, &tm_z, &s_full[s], tj, (int)d0, (int)b);
+        msc::tma_load_3d(st + 3 * kRowTile, &tm_B, &s_full[s], tj, 0, (int)b);
+        if (kFull) msc::tma_load_3d(st + 3 * kRowTile + kBCTile, &tm_C, &s_full[s], tj, 0, (int)b);
+    };
+
+    int issued = 0;
+    if (lane == 0)
+        for (; issued < kStages && issued < ntiles; ++issued) issue(issued);
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+
+    bool failed = false;
+    int i = 0;
+    for (; i < ntiles; ++i) {
+        const int st = i % kStages;
+        if (!wait_phase(&s_full[st], (uint32_t)((i / kStages) & 1))) {
+            if (lane == 0) record_timeout(1);
+            failed = true;
+            break;
+        }
+        const uint8_t* raw = s_raw[st];
+        const int64_t t0 = t_begin + (int64_t)i * kTT;
+        const int nt = (int)imin64(kTT, t_end - t0);
+
+        // B (and C) of this tile -> fp32, n-pair interleaved: s_bc[x][n/2][t][n%2]
+        {
+            const int n = lane >> 1, half = lane & 1;
+#pragma unroll
+            for (int x = 0; x < (kFull ? 2 : 1); ++x) {
+                const uint8_t* src = raw + 3 * kRowTile + x * kBCTile;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(src + msc::sw64(n, 2 * half + c));
+                    if constexpr (kBF16) {
+                        const int tb = 16 * half + 8 * c;
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            s_bc[x][n >> 1][tb + 2 * k][n & 1] = msc::bf16lo(w[k]);
+                            s_bc[x][n >> 1][tb + 2 * k + 1][n & 1] = msc::bf16hi(w[k]);
+                        }
+                    } else {
+                        const int tb = 8 * half + 4 * c;
+                        s_bc[x][n >> 1][tb + 0][n & 1] = __uint_as_float(v.x);
+                        s_bc[x][n >> 1][tb + 1][n & 1] = __uint_as_float(v.y);
+                        s_bc[x][n >> 1][tb + 2][n & 1] = __uint_as_float(v.z);
+                        s_bc[x][n >> 1][tb + 3][n & 1] = __uint_as_float(v.w);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+            if (8 * g >= nt) break;
+            // ---- per-step scalars of this lane's row for steps 8g .. 8g+7
+            float uu[8], dl[8];
+            if constexpr (kBF16) {
+                const uint4 vu = *reinterpret_cast<const uint4*>(raw + msc::sw64(lane, g));
+                const uint4 vd = *reinterpret_cast<const uint4*>(raw + kRowTile + msc::sw64(lane, g));
+                const uint32_t wu[4] = {vu.x, vu.y, vu.z, vu.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uu[2 * k] = msc::bf16lo(wu[k]); uu[2 * k + 1] = msc::bf16hi(wu[k]);
+                    dl[2 * k] = msc::bf16lo(wd[k]); dl[2 * k + 1] = msc::bf16hi(wd[k]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const float4 vu = *reinterpret_cast<const float4*>(raw + msc::sw64(lane, 2 * g + c));
+                    const float4 vd = *reinterpret_cast<const float4*>(raw + kRowTile + msc::sw64(lane, 2 * g + c));
+                    uu[4 * c] = vu.x; uu[4 * c + 1] = vu.y; uu[4 * c + 2] = vu.z; uu[4 * c + 3] = vu.w;
+                    dl[4 * c] = vd.x; dl[4 * c + 1] = vd.y; dl[4 * c + 2] = vd.z; dl[4 * c + 3] = vd.w;
+                }
+            }
+            uint64_t dt2[8], dtu2[8];
+            float du[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float dt = msc::softplus_f(dl[k] + bias);
+                if (8 * g + k >= nt) dt = 0.f;  // steps past the tile end: abar = 1, input 0
+                const float dtu = dt * uu[k];
+                if (!kFull) dsum += dt;
+                dt2[k] = msc::pk2(dt, dt);
+                dtu2[k] = msc::pk2(dtu, dtu);
+                du[k] = Dd * uu[k];
+            }
+            // ---- the scan over n pairs
+            uint64_t acc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] = 0ull;
+#pragma unroll
+            for (int q = 0; q < kNS / 2; ++q) {
+                uint64_t Bp[8], Cp[8];
+                const ulonglong2* bsrc = reinterpret_cast<const ulonglong2*>(&s_bc[0][q][8 * g][0]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const ulonglong2 v = bsrc[k];
+                    Bp[2 * k] = v.x; Bp[2 * k + 1] = v.y;
+                }
+                if (kFull) {
+                    const ulonglong2* csrc = reinterpret_cast<const ulonglong2*>(&s_bc[1][q][8 * g][0]);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const ulonglong2 v = csrc[k];
+                        Cp[2 * k] = v.x; Cp[2 * k + 1] = v.y;
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    float a0, a1;
+                    msc::upk2(msc::mul2(dt2[k], A2p[q]), a0, a1);
+                    const uint64_t a = msc::pk2(msc::ex2_approx(a0), msc::ex2_approx(a1));
+                    h2[q] = msc::fma2(a, h2[q], msc::mul2(dtu2[k], Bp[k]));
+                    if (kFull) acc[k] = msc::fma2(Cp[k], h2[q], acc[k]);
+                }
+            }
+            // ---- readout + skip + gate, store this row's 8 outputs
+            if (kFull) {
+                float yv[8];
+                float zz[8];
+                if (has_z) {
+                    if constexpr (kBF16) {
+                        const uint4 vz = *reinterpret_cast<const uint4*>(raw + 2 * kRowTile + msc::sw64(lane, g));
+                        const uint32_t wz[4] = {vz.x, vz.y, vz.z, vz.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) { zz[2 * k] = msc::bf16lo(wz[k]); zz[2 * k + 1] = msc::bf16hi(wz[k]); }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const float4 vz = *reinterpret_cast<const float4*>(raw + 2 * kRowTile + msc::sw64(lane, 2 * g + c));
+                            zz[4 * c] = vz.x; zz[4 * c + 1] = vz.y; zz[4 * c + 2] = vz.z; zz[4 * c + 3] = vz.w;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    float lo, hi;
+                    msc::upk2(acc[k], lo, hi);
+                    float v = (lo + hi) + du[k];
+                    if (has_z) v *= msc::silu_f(zz[k]);
+                    yv[k] = v;
+                }
+                if (row_ok) {
+                    float* q = p.y + row * p.L + t0 + 8 * g;
+                    const int rem = nt - 8 * g;
+                    if (rem >= 8) {
+                        __stcs(reinterpret_cast<float4*>(q), make_float4(yv[0], yv[1], yv[2], yv[3]));
+                        __stcs(reinterpret_cast<float4*>(q) + 1, make_float4(yv[4], yv[5], yv[6], yv[7]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (k < rem) q[k] = yv[k];
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && issued < ntiles) issue(issued);
+        ++issued;
+        issued = __shfl_sync(0xffffffffu, issued, 0);
+    }
+
+    if (failed) {
+        // drain loads still in flight before the shared memory is released
+        if (lane == 0)
+            for (int j = i; j < issued && j < ntiles; ++j)
+                (void)wait_phase(&s_full[j % kStages], (uint32_t)((j / kStages) & 1));
+        return;
+    }
+    if (!row_ok) return;
+    if (kFull) {
+        if (p.h_last && seg == p.G - 1) {
+#pragma unroll
+            for (int q = 0; q < kNS / 2; ++q) {
+                float h0v, h1v;
+                msc::upk2(h2[q], h0v, h1v);
+                if (2 * q < N) p.h_last[row * N + 2 * q] = h0v;
+                if (2 * q + 1 < N) p.h_last[row * N + 2 * q + 1] = h1v;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < kNS / 2; ++q) {
+            float h0v, h1v;
+            msc::upk2(h2[q], h0v, h1v);
+            if (2 * q < N) p.seg_state[((size_t)row * p.G + seg) * N + 2 * q] = h0v;
+            if (2 * q + 1 < N) p.seg_state[((size_t)row * p.G + seg) * N + 2 * q + 1] = h1v;
+        }
+        p.seg_dsum[(size_t)row * p.G + seg] = dsum;
+    }
+}
+
 // Chains the segment aggregates of every (row, n): carry_0 = h0 (or 0),
 // carry_{g+1} = exp(A sum Delta_g) carry_g + H_g.  Carries overwrite the
 // aggregates in place (each is read before it is overwritten, by one thread).
@@ -302,8 +606,47 @@ msc_status launch_rows(const FwdParams& p, int64_t batch, int G, int mode, cudaS
     return msc_host::check_launch("s6_fwd_rows");
 }
 
-msc_status launch_mode(const FwdParams& p, bool bf16, bool vec, int64_t batch, int G, int mode,
-                       cudaStream_t st) {
+struct FwdMaps {
+    CUtensorMap u, d, z, B, C;
+};
+
+bool make_maps(FwdMaps& m, const FwdParams& p, int64_t batch, bool bf16) {
+    const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const uint64_t es = bf16 ? 2 : 4;
+    const uint32_t tt = bf16 ? 32 : 16;
+    const uint64_t rdims[3] = {(uint64_t)p.L, (uint64_t)p.dim, (uint64_t)batch};
+    const uint64_t rstr[2] = {(uint64_t)p.L * es, (uint64_t)p.dim * p.L * es};
+    const uint32_t rbox[3] = {tt, (uint32_t)kRows, 1};
+    const uint64_t bdims[3] = {(uint64_t)p.L, (uint64_t)p.N, (uint64_t)batch};
+    const uint64_t bstr[2] = {(uint64_t)p.L * es, (uint64_t)p.N * p.L * es};
+    const uint32_t bbox[3] = {tt, (uint32_t)kNS, 1};
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!msc_host::encode_tmap(&m.u, dt, 3, p.u, rdims, rstr, rbox, sw)) return false;
+    if (!msc_host::encode_tmap(&m.d, dt, 3, p.delta, rdims, rstr, rbox, sw)) return false;
+    if (!msc_host::encode_tmap(&m.z, dt, 3, p.z ? p.z : p.u, rdims, rstr, rbox, sw)) return false;
+    if (!msc_host::encode_tmap(&m.B, dt, 3, p.B, bdims, bstr, bbox, sw)) return false;
+    if (!msc_host::encode_tmap(&m.C, dt, 3, p.C, bdims, bstr, bbox, sw)) return false;
+    return true;
+}
+
+template <bool kBF16>
+msc_status launch_tma(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
+    dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
+    if (mode == kModeFull)
+        s6_fwd_tma_kernel<kBF16, kModeFull><<<grid, kRows, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    else
+        s6_fwd_tma_kernel<kBF16, kModeAgg><<<grid, kRows, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    return msc_host::check_launch("s6_fwd_tma");
+}
+
+// TMA needs every row stride to be a multiple of 16 bytes.
+bool tma_ok(const FwdParams& p, bool bf16) {
+    return bf16 ? (p.L % 8 == 0) : (p.L % 4 == 0);
+}
+
+msc_status launch_mode(const FwdParams& p, const FwdMaps* maps, bool bf16, bool vec, int64_t batch, int G,
+                       int mode, cudaStream_t st) {
+    if (maps) return bf16 ? launch_tma<true>(*maps, p, batch, G, mode, st) : launch_tma<false>(*maps, p, batch, G, mode, st);
     if (bf16) return vec ? launch_rows<true, true>(p, batch, G, mode, st) : launch_rows<true, false>(p, batch, G, mode, st);
     return vec ? launch_rows<false, true>(p, batch, G, mode, st) : launch_rows<false, false>(p, batch, G, mode, st);
 }
@@ -333,7 +676,7 @@ S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
     G = (seqlen + seg - 1) / seg;
     plan.G = (int)G;
     plan.seg_len = seg;
-    plan.workspace = kStatusBytes + (size_t)rows * G * (size_t)dstate * sizeof(float) +
+    plan.workspace = (size_t)rows * G * (size_t)dstate * sizeof(float) +
                      (size_t)rows * G * sizeof(float) + 256;
     return plan;
 }
@@ -347,13 +690,19 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
     // 16-byte vector loads need every row and tile start 16-byte aligned:
     // bases are checked by the caller; rows start at row * L elements.
     const bool vec = (a.L % 8) == 0;
+    FwdMaps maps;
+    const FwdMaps* mp = nullptr;
+    if (tma_ok(p, a.bf16) && std::getenv("MSC_S6_FWD_PLAIN") == nullptr) {
+        if (!make_maps(maps, p, a.batch, a.bf16)) return MSC_ERR_CUDA;
+        mp = &maps;
+    }
     if (plan.G > 1) {
-        char* ws = static_cast<char*>(a.workspace) + kStatusBytes;
+        char* ws = static_cast<char*>(a.workspace);
         p.seg_state = reinterpret_cast<float*>(ws);
         size_t off = (size_t)(a.batch * a.dim) * plan.G * a.N * sizeof(float);
         off = (off + 255) / 256 * 256;
         p.seg_dsum = reinterpret_cast<float*>(ws + off);
-        msc_status s = launch_mode(p, a.bf16, vec, a.batch, plan.G - 1, kModeAgg, st);
+        msc_status s = launch_mode(p, mp, a.bf16, vec, a.batch, plan.G - 1, kModeAgg, st);
         if (s != MSC_OK) return s;
         const int64_t total = a.batch * a.dim * a.N;
         const int threads = 256;
@@ -362,7 +711,22 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
         s = check_launch("s6_seg_carry");
         if (s != MSC_OK) return s;
     }
-    return launch_mode(p, a.bf16, vec, a.batch, plan.G, kModeFull, st);
+    return launch_mode(p, mp, a.bf16, vec, a.batch, plan.G, kModeFull, st);
+}
+
+// Reads and clears this module's device status word.
+msc_status s6_fwd_take_status(unsigned int* code, unsigned int* site) {
+    unsigned int w[2] = {0, 0};
+    cudaError_t e = cudaMemcpyFromSymbol(w, g_s6_fwd_status, sizeof(w));
+    if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    if (w[0] != 0) {
+        const unsigned int z[2] = {0, 0};
+        e = cudaMemcpyToSymbol(g_s6_fwd_status, z, sizeof(z));
+        if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+    }
+    *code = w[0];
+    *site = w[1];
+    return MSC_OK;
 }
 
 }  // namespace msc_host

@@ -9,8 +9,9 @@ Recipe (one numpy ``Generator(Philox(seed))`` per problem, draws in this order):
   delta (raw pre-activation) ~ 0.5 * N(0, 1)
   dt ~ log-uniform[1e-3, 1e-1] per channel (per head for SSD);
   delta_bias = log(expm1(dt)), the inverse softplus, so softplus(bias) = dt
-  A[d, n] = -(n + 1)   (S4D-real style initialisation, survey article sec. 2.1,
-                        study note "A uses HiPPO-style initialisation")
+  A[d, n] = -(n + 1)   (S4D-real style initialisation: bqwf survey sec. 2.1 and
+                        the study note "Mamba — 选择性状态空间模型" both name
+                        HiPPO-style initialisation of A)
   A_h ~ -U[1, 16]      (SSD, one scalar per head)
   D = 1
 bf16 inputs are rounded once (round-to-nearest-even) on the host; the GPU gets
