@@ -310,46 +310,54 @@ constexpr int kStages = 2;
 constexpr int kRowTile = 2048;               // bytes of one 32-row x 64-byte tile
 constexpr int kBCTile = 1024;                // bytes of one 16-slot x 64-byte tile
 constexpr int kStageBytes = 3 * kRowTile + 2 * kBCTile;
+constexpr int kTmaThreads = 64;              // two lanes per channel row
 
+// Two lanes share a row: lane parity j owns states n in [8j, 8j + 8) and the
+// per-step work (softplus, gate, store) of steps 4j .. 4j+3 of every 8-step
+// group; the two halves are exchanged with one shuffle each.
 template <bool kBF16, int kMode>
-__global__ void __launch_bounds__(32) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
-                                                        const __grid_constant__ CUtensorMap tm_d,
-                                                        const __grid_constant__ CUtensorMap tm_z,
-                                                        const __grid_constant__ CUtensorMap tm_B,
-                                                        const __grid_constant__ CUtensorMap tm_C,
-                                                        const FwdParams p) {
+__global__ void __launch_bounds__(kTmaThreads) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
+                                                                 const __grid_constant__ CUtensorMap tm_d,
+                                                                 const __grid_constant__ CUtensorMap tm_z,
+                                                                 const __grid_constant__ CUtensorMap tm_B,
+                                                                 const __grid_constant__ CUtensorMap tm_C,
+                                                                 const FwdParams p) {
     constexpr bool kFull = (kMode == kModeFull);
     constexpr int kTT = kBF16 ? 32 : 16;  // steps per 64-byte tile row
     constexpr int kGroups = kTT / 8;
+    constexpr int kPitch = 2 * kTT + 4;   // floats per n-pair row of s_bc (padded: conflict-free stores)
     __shared__ __align__(1024) uint8_t s_raw[kStages][kStageBytes];
-    __shared__ __align__(16) float s_bc[2][kNS / 2][kTT][2];  // [B|C][n pair][t][n parity]
+    __shared__ __align__(16) float s_bc[2][kNS / 2][kPitch];  // [B|C][n pair][t * 2 + n parity]
     __shared__ __align__(8) uint64_t s_full[kStages];
 
-    const int lane = threadIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int r = 16 * (tid >> 5) + (lane >> 1);  // row within the CTA
+    const int j = lane & 1;                       // state half / step half
     const int64_t b = blockIdx.y;
     const int64_t d0 = (int64_t)blockIdx.x * kRows;
     const int nrows = (int)imin64(kRows, p.dim - d0);
-    const bool row_ok = lane < nrows;
-    const int64_t d = row_ok ? d0 + lane : d0;
+    const bool row_ok = r < nrows;
+    const int64_t d = row_ok ? d0 + r : d0;
     const int64_t row = b * p.dim + d;
     const int seg = blockIdx.z;
     const int N = p.N;
     const bool has_z = kFull && p.z != nullptr;
 
-    uint64_t A2p[kNS / 2], h2[kNS / 2];
+    uint64_t A2p[4], h2[4];
 #pragma unroll
-    for (int q = 0; q < kNS / 2; ++q) {
+    for (int q = 0; q < 4; ++q) {
         float a[2], h[2];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int n = 2 * q + j;
-            a[j] = (row_ok && n < N) ? __ldg(p.A + d * N + n) * MSC_LOG2E : 0.f;
-            h[j] = 0.f;
+        for (int e = 0; e < 2; ++e) {
+            const int n = 8 * j + 2 * q + e;
+            a[e] = (row_ok && n < N) ? __ldg(p.A + d * N + n) * MSC_LOG2E : 0.f;
+            h[e] = 0.f;
             if (kFull && row_ok && n < N) {
                 if (p.G > 1)
-                    h[j] = p.seg_state[((size_t)row * p.G + seg) * N + n];
+                    h[e] = p.seg_state[((size_t)row * p.G + seg) * N + n];
                 else if (p.h0)
-                    h[j] = __ldg(p.h0 + row * N + n);
+                    h[e] = __ldg(p.h0 + row * N + n);
             }
         }
         A2p[q] = msc::pk2(a[0], a[1]);
@@ -364,7 +372,7 @@ __global__ void __launch_bounds__(32) s6_fwd_tma_kernel(const __grid_constant__ 
     const int ntiles = (int)((t_end - t_begin + kTT - 1) / kTT);
     const uint32_t tx_bytes = kRowTile * (has_z ? 3 : 2) + kBCTile * (kFull ? 2 : 1);
 
-    if (lane == 0) {
+    if (tid == 0) {
         for (int s = 0; s < kStages; ++s) msc::mbar_init(&s_full[s], 1);
         msc::fence_barrier_init();
         msc::prefetch_tmap(&tm_u);
@@ -373,11 +381,11 @@ __global__ void __launch_bounds__(32) s6_fwd_tma_kernel(const __grid_constant__ 
         if (has_z) msc::prefetch_tmap(&tm_z);
         if (kFull) msc::prefetch_tmap(&tm_C);
     }
-    __syncwarp();
+    __syncthreads();
 
-    auto issue = [&](int j) {
-        const int s = j % kStages;
-        const int tj = (int)(t_begin + (int64_t)j * kTT);
+    auto issue = [&](int jt) {
+        const int s = jt % kStages;
+        const int tj = (int)(t_begin + (int64_t)jt * kTT);
         uint8_t* st = s_raw[s];
         msc::mbar_arrive_expect_tx(&s_full[s], tx_bytes);
         msc::tma_load_3d(st, &tm_u, &s_full[s], tj, (int)d0, (int)b);
@@ -387,17 +395,18 @@ __global__ void __launch_bounds__(32) s6_fwd_tma_kernel(const __grid_constant__ 
         if (kFull) msc::tma_load_3d(st + 3 * kRowTile + kBCTile, &tm_C, &s_full[s], tj, 0, (int)b);
     };
 
-    int issued = 0;
-    if (lane == 0)
-        for (; issued < kStages && issued < ntiles; ++issued) issue(issued);
-    issued = __shfl_sync(0xffffffffu, issued, 0);
+    if (tid == 0)
+        for (int jt = 0; jt < kStages && jt < ntiles; ++jt) issue(jt);
+    int issued = ntiles < kStages ? ntiles : kStages;
 
     bool failed = false;
     int i = 0;
     for (; i < ntiles; ++i) {
         const int st = i % kStages;
-        if (!wait_phase(&s_full[st], (uint32_t)((i / kStages) & 1))) {
-            if (lane == 0) record_timeout(1);
+        const bool ok = wait_phase(&s_full[st], (uint32_t)((i / kStages) & 1));
+        // every thread takes the same branch, so no thread is left at a barrier
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) record_timeout(1);
             failed = true;
             break;
         }
@@ -405,85 +414,85 @@ __global__ void __launch_bounds__(32) s6_fwd_tma_kernel(const __grid_constant__ 
         const int64_t t0 = t_begin + (int64_t)i * kTT;
         const int nt = (int)imin64(kTT, t_end - t0);
 
-        // B (and C) of this tile -> fp32, n-pair interleaved: s_bc[x][n/2][t][n%2]
+        // B (and C) of this tile -> fp32 pairs s_bc[x][q][2t + e] = X[n = 2q + e][t]
         {
-            const int n = lane >> 1, half = lane & 1;
-#pragma unroll
-            for (int x = 0; x < (kFull ? 2 : 1); ++x) {
+            const int x = tid >> 5, q = lane & 7, c = lane >> 3;
+            if (x == 0 || kFull) {
                 const uint8_t* src = raw + 3 * kRowTile + x * kBCTile;
+                const uint4 v0 = *reinterpret_cast<const uint4*>(src + msc::sw64(2 * q, c));
+                const uint4 v1 = *reinterpret_cast<const uint4*>(src + msc::sw64(2 * q + 1, c));
+                float* dst = &s_bc[x][q][0];
+                if constexpr (kBF16) {
+                    const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(src + msc::sw64(n, 2 * half + c));
-                    if constexpr (kBF16) {
-                        const int tb = 16 * half + 8 * c;
-                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            s_bc[x][n >> 1][tb + 2 * k][n & 1] = msc::bf16lo(w[k]);
-                            s_bc[x][n >> 1][tb + 2 * k + 1][n & 1] = msc::bf16hi(w[k]);
-                        }
-                    } else {
-                        const int tb = 8 * half + 4 * c;
-                        s_bc[x][n >> 1][tb + 0][n & 1] = __uint_as_float(v.x);
-                        s_bc[x][n >> 1][tb + 1][n & 1] = __uint_as_float(v.y);
-                        s_bc[x][n >> 1][tb + 2][n & 1] = __uint_as_float(v.z);
-                        s_bc[x][n >> 1][tb + 3][n & 1] = __uint_as_float(v.w);
+                    for (int k = 0; k < 4; ++k) {
+                        *reinterpret_cast<float4*>(dst + 2 * (8 * c + 2 * k)) =
+                            make_float4(msc::bf16lo(w0[k]), msc::bf16lo(w1[k]), msc::bf16hi(w0[k]), msc::bf16hi(w1[k]));
                     }
+                } else {
+                    *reinterpret_cast<float4*>(dst + 2 * (4 * c)) =
+                        make_float4(__uint_as_float(v0.x), __uint_as_float(v1.x), __uint_as_float(v0.y), __uint_as_float(v1.y));
+                    *reinterpret_cast<float4*>(dst + 2 * (4 * c + 2)) =
+                        make_float4(__uint_as_float(v0.z), __uint_as_float(v1.z), __uint_as_float(v0.w), __uint_as_float(v1.w));
                 }
             }
         }
-        __syncwarp();
+        __syncthreads();
 
-#pragma unroll
+#pragma unroll 1
         for (int g = 0; g < kGroups; ++g) {
             if (8 * g >= nt) break;
-            // ---- per-step scalars of this lane's row for steps 8g .. 8g+7
-            float uu[8], dl[8];
+            // ---- this lane's 4 steps (8g + 4j ..): Delta, Delta*u, D*u
+            float uu[4], dl[4];
             if constexpr (kBF16) {
-                const uint4 vu = *reinterpret_cast<const uint4*>(raw + msc::sw64(lane, g));
-                const uint4 vd = *reinterpret_cast<const uint4*>(raw + kRowTile + msc::sw64(lane, g));
-                const uint32_t wu[4] = {vu.x, vu.y, vu.z, vu.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uu[2 * k] = msc::bf16lo(wu[k]); uu[2 * k + 1] = msc::bf16hi(wu[k]);
-                    dl[2 * k] = msc::bf16lo(wd[k]); dl[2 * k + 1] = msc::bf16hi(wd[k]);
-                }
+                const uint2 vu = *reinterpret_cast<const uint2*>(raw + msc::sw64(r, g) + 8 * j);
+                const uint2 vd = *reinterpret_cast<const uint2*>(raw + kRowTile + msc::sw64(r, g) + 8 * j);
+                uu[0] = msc::bf16lo(vu.x); uu[1] = msc::bf16hi(vu.x); uu[2] = msc::bf16lo(vu.y); uu[3] = msc::bf16hi(vu.y);
+                dl[0] = msc::bf16lo(vd.x); dl[1] = msc::bf16hi(vd.x); dl[2] = msc::bf16lo(vd.y); dl[3] = msc::bf16hi(vd.y);
             } else {
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const float4 vu = *reinterpret_cast<const float4*>(raw + msc::sw64(lane, 2 * g + c));
-                    const float4 vd = *reinterpret_cast<const float4*>(raw + kRowTile + msc::sw64(lane, 2 * g + c));
-                    uu[4 * c] = vu.x; uu[4 * c + 1] = vu.y; uu[4 * c + 2] = vu.z; uu[4 * c + 3] = vu.w;
-                    dl[4 * c] = vd.x; dl[4 * c + 1] = vd.y; dl[4 * c + 2] = vd.z; dl[4 * c + 3] = vd.w;
-                }
+                const float4 vu = *reinterpret_cast<const float4*>(raw + msc::sw64(r, 2 * g + j));
+                const float4 vd = *reinterpret_cast<const float4*>(raw + kRowTile + msc::sw64(r, 2 * g + j));
+                uu[0] = vu.x; uu[1] = vu.y; uu[2] = vu.z; uu[3] = vu.w;
+                dl[0] = vd.x; dl[1] = vd.y; dl[2] = vd.z; dl[3] = vd.w;
             }
-            uint64_t dt2[8], dtu2[8];
-            float du[8];
+            float mdt[4], mdtu[4], mdu[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 4; ++k) {
                 float dt = msc::softplus_f(dl[k] + bias);
-                if (8 * g + k >= nt) dt = 0.f;  // steps past the tile end: abar = 1, input 0
-                const float dtu = dt * uu[k];
+                if (8 * g + 4 * j + k >= nt) dt = 0.f;  // past the tile end: abar = 1, input 0
+                mdt[k] = dt;
+                mdtu[k] = dt * uu[k];
+                mdu[k] = Dd * uu[k];
                 if (!kFull) dsum += dt;
-                dt2[k] = msc::pk2(dt, dt);
-                dtu2[k] = msc::pk2(dtu, dtu);
-                du[k] = Dd * uu[k];
             }
-            // ---- the scan over n pairs
+            // ---- exchange halves: every lane gets Delta, Delta*u of all 8 steps
+            uint64_t dt2[8], dtu2[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float odt = __shfl_xor_sync(0xffffffffu, mdt[k], 1);
+                const float odtu = __shfl_xor_sync(0xffffffffu, mdtu[k], 1);
+                const float lo_dt = j ? odt : mdt[k], hi_dt = j ? mdt[k] : odt;
+                const float lo_dtu = j ? odtu : mdtu[k], hi_dtu = j ? mdtu[k] : odtu;
+                dt2[k] = msc::pk2(lo_dt, lo_dt);
+                dt2[k + 4] = msc::pk2(hi_dt, hi_dt);
+                dtu2[k] = msc::pk2(lo_dtu, lo_dtu);
+                dtu2[k + 4] = msc::pk2(hi_dtu, hi_dtu);
+            }
+            // ---- the scan over this lane's 4 n-pairs
             uint64_t acc[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) acc[k] = 0ull;
 #pragma unroll
-            for (int q = 0; q < kNS / 2; ++q) {
+            for (int q = 0; q < 4; ++q) {
                 uint64_t Bp[8], Cp[8];
-                const ulonglong2* bsrc = reinterpret_cast<const ulonglong2*>(&s_bc[0][q][8 * g][0]);
+                const ulonglong2* bsrc = reinterpret_cast<const ulonglong2*>(&s_bc[0][4 * j + q][16 * g]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const ulonglong2 v = bsrc[k];
                     Bp[2 * k] = v.x; Bp[2 * k + 1] = v.y;
                 }
                 if (kFull) {
-                    const ulonglong2* csrc = reinterpret_cast<const ulonglong2*>(&s_bc[1][q][8 * g][0]);
+                    const ulonglong2* csrc = reinterpret_cast<const ulonglong2*>(&s_bc[1][4 * j + q][16 * g]);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const ulonglong2 v = csrc[k];
@@ -499,80 +508,77 @@ __global__ void __launch_bounds__(32) s6_fwd_tma_kernel(const __grid_constant__ 
                     if (kFull) acc[k] = msc::fma2(Cp[k], h2[q], acc[k]);
                 }
             }
-            // ---- readout + skip + gate, store this row's 8 outputs
+            // ---- readout + skip + gate of this lane's 4 steps
             if (kFull) {
-                float yv[8];
-                float zz[8];
-                if (has_z) {
-                    if constexpr (kBF16) {
-                        const uint4 vz = *reinterpret_cast<const uint4*>(raw + 2 * kRowTile + msc::sw64(lane, g));
-                        const uint32_t wz[4] = {vz.x, vz.y, vz.z, vz.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) { zz[2 * k] = msc::bf16lo(wz[k]); zz[2 * k + 1] = msc::bf16hi(wz[k]); }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const float4 vz = *reinterpret_cast<const float4*>(raw + 2 * kRowTile + msc::sw64(lane, 2 * g + c));
-                            zz[4 * c] = vz.x; zz[4 * c + 1] = vz.y; zz[4 * c + 2] = vz.z; zz[4 * c + 3] = vz.w;
-                        }
-                    }
-                }
+                float tot[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     float lo, hi;
                     msc::upk2(acc[k], lo, hi);
-                    float v = (lo + hi) + du[k];
+                    tot[k] = lo + hi;
+                }
+                float zz[4] = {0.f, 0.f, 0.f, 0.f};
+                if (has_z) {
+                    if constexpr (kBF16) {
+                        const uint2 vz = *reinterpret_cast<const uint2*>(raw + 2 * kRowTile + msc::sw64(r, g) + 8 * j);
+                        zz[0] = msc::bf16lo(vz.x); zz[1] = msc::bf16hi(vz.x); zz[2] = msc::bf16lo(vz.y); zz[3] = msc::bf16hi(vz.y);
+                    } else {
+                        const float4 vz = *reinterpret_cast<const float4*>(raw + 2 * kRowTile + msc::sw64(r, 2 * g + j));
+                        zz[0] = vz.x; zz[1] = vz.y; zz[2] = vz.z; zz[3] = vz.w;
+                    }
+                }
+                float yv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float send = j ? tot[k] : tot[k + 4];   // the partner's steps
+                    const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                    float v = (j ? tot[k + 4] : tot[k]) + recv + mdu[k];
                     if (has_z) v *= msc::silu_f(zz[k]);
                     yv[k] = v;
                 }
                 if (row_ok) {
-                    float* q = p.y + row * p.L + t0 + 8 * g;
-                    const int rem = nt - 8 * g;
-                    if (rem >= 8) {
-                        __stcs(reinterpret_cast<float4*>(q), make_float4(yv[0], yv[1], yv[2], yv[3]));
-                        __stcs(reinterpret_cast<float4*>(q) + 1, make_float4(yv[4], yv[5], yv[6], yv[7]));
+                    const int rem = nt - 8 * g - 4 * j;
+                    float* qy = p.y + row * p.L + t0 + 8 * g + 4 * j;
+                    if (rem >= 4) {
+                        __stcs(reinterpret_cast<float4*>(qy), make_float4(yv[0], yv[1], yv[2], yv[3]));
                     } else {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            if (k < rem) q[k] = yv[k];
+                        for (int k = 0; k < 3; ++k)
+                            if (k < rem) qy[k] = yv[k];
                     }
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0 && issued < ntiles) issue(issued);
+        __syncthreads();
+        if (tid == 0 && issued < ntiles) issue(issued);
         ++issued;
-        issued = __shfl_sync(0xffffffffu, issued, 0);
     }
 
     if (failed) {
         // drain loads still in flight before the shared memory is released
-        if (lane == 0)
-            for (int j = i; j < issued && j < ntiles; ++j)
-                (void)wait_phase(&s_full[j % kStages], (uint32_t)((j / kStages) & 1));
+        if (tid == 0)
+            for (int jt = i; jt < issued && jt < ntiles; ++jt)
+                (void)wait_phase(&s_full[jt % kStages], (uint32_t)((jt / kStages) & 1));
         return;
     }
+    if (!kFull) dsum += __shfl_xor_sync(0xffffffffu, dsum, 1);
     if (!row_ok) return;
-    if (kFull) {
-        if (p.h_last && seg == p.G - 1) {
 #pragma unroll
-            for (int q = 0; q < kNS / 2; ++q) {
-                float h0v, h1v;
-                msc::upk2(h2[q], h0v, h1v);
-                if (2 * q < N) p.h_last[row * N + 2 * q] = h0v;
-                if (2 * q + 1 < N) p.h_last[row * N + 2 * q + 1] = h1v;
+    for (int q = 0; q < 4; ++q) {
+        float v0, v1;
+        msc::upk2(h2[q], v0, v1);
+        const int n = 8 * j + 2 * q;
+        if (kFull) {
+            if (p.h_last && seg == p.G - 1) {
+                if (n < N) p.h_last[row * N + n] = v0;
+                if (n + 1 < N) p.h_last[row * N + n + 1] = v1;
             }
+        } else {
+            if (n < N) p.seg_state[((size_t)row * p.G + seg) * N + n] = v0;
+            if (n + 1 < N) p.seg_state[((size_t)row * p.G + seg) * N + n + 1] = v1;
         }
-    } else {
-#pragma unroll
-        for (int q = 0; q < kNS / 2; ++q) {
-            float h0v, h1v;
-            msc::upk2(h2[q], h0v, h1v);
-            if (2 * q < N) p.seg_state[((size_t)row * p.G + seg) * N + 2 * q] = h0v;
-            if (2 * q + 1 < N) p.seg_state[((size_t)row * p.G + seg) * N + 2 * q + 1] = h1v;
-        }
-        p.seg_dsum[(size_t)row * p.G + seg] = dsum;
     }
+    if (!kFull && j == 0) p.seg_dsum[(size_t)row * p.G + seg] = dsum;
 }
 
 // Chains the segment aggregates of every (row, n): carry_0 = h0 (or 0),
@@ -633,9 +639,9 @@ template <bool kBF16>
 msc_status launch_tma(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
     if (mode == kModeFull)
-        s6_fwd_tma_kernel<kBF16, kModeFull><<<grid, kRows, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+        s6_fwd_tma_kernel<kBF16, kModeFull><<<grid, kTmaThreads, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
     else
-        s6_fwd_tma_kernel<kBF16, kModeAgg><<<grid, kRows, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+        s6_fwd_tma_kernel<kBF16, kModeAgg><<<grid, kTmaThreads, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
     return msc_host::check_launch("s6_fwd_tma");
 }
 

@@ -129,3 +129,25 @@ def test_repeat_calls_identical():
     y1 = _run(inp, True)
     y2 = _run(inp, True)
     assert np.array_equal(y1, y2)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_plain_and_tma_paths_agree(bf16, monkeypatch):
+    """Aligned rows stream through TMA; the plain-load kernel (taken for rows
+    whose byte stride is not a multiple of 16) computes the same values."""
+    inp = s6_inputs(2, 40, 256, 16, seed=31, bf16=bf16)
+    y_tma = _run(inp, bf16)
+    monkeypatch.setenv("MSC_S6_FWD_PLAIN", "1")
+    y_plain = _run(inp, bf16)
+    ref = _ref(inp)
+    tol = TOL_BF16 if bf16 else TOL_F32
+    assert max_rel_err(y_tma, ref) <= tol
+    assert max_rel_err(y_plain, ref) <= tol
+    assert max_rel_err(y_tma, y_plain) <= 1e-5
+
+
+def test_device_status_clean_after_runs():
+    import selective_state_space_160_b300 as msc
+    inp = s6_inputs(1, 64, 512, 16, seed=2, bf16=True)
+    _run(inp, True)
+    msc.msc_check_device_status()
