@@ -95,9 +95,9 @@ class ClockSampler:
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100"] + self.sel, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                        "-lms", "100"] + self.sel
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
@@ -109,6 +109,7 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
+        self.err = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -116,6 +117,10 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
             self.t.join(timeout=2)
+            try:
+                self.err = (self.proc.stderr.read() or "").strip()[:300]
+            except Exception:
+                pass
 
     def summary(self):
         sm, mx, reasons = [], [], set()
@@ -133,7 +138,8 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "error": getattr(self, "err", ""), "first_line": self.lines[0] if self.lines else ""}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
 
@@ -326,12 +332,16 @@ def cpu_oracle_sample(target_s=12.0, max_rows=None):
     if max_rows:
         dim2 = min(dim2, max_rows)
     inp = s6_inputs(b, dim2, L, N, seed=160_001, bf16=True)
-    t0 = time.perf_counter()
-    oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["delta_bias"])
-    dt = time.perf_counter() - t0
-    return {"value": b * dim2 * L / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["delta_bias"])
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= 0.8 * target_s or reps >= 50:
+            break
+    return {"value": reps * b * dim2 * L / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "S6 fwd, batch 8 x %d of the 5120 channels x L 2048, N 16, bf16-rounded inputs, "
-                      "double precision, %.1f s" % (dim2, dt)}
+                      "double precision, %d pass(es) in %.1f s" % (dim2, reps, dt)}
 
 
 def run_reference(args):
@@ -400,6 +410,17 @@ def run_ours(args):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        # nvidia-smi needs ~0.1-0.5 s for its first sample, far longer than the
+        # timed region: keep the same step running back to back until samples
+        # arrive, run the timed region, and keep the load on for two more.
+        def load_until(n, limit_s=4.0):
+            t_stop = time.time() + limit_s
+            while len(clk.lines) < n and time.time() < t_stop:
+                for _ in range(20):
+                    step()
+                torch.cuda.synchronize()
+        load_until(2)
+        n0 = len(clk.lines)
         torch.cuda.synchronize()
         start.record(stream)
         for a, e in per:
@@ -408,6 +429,7 @@ def run_ours(args):
             e.record(stream)
         end.record(stream)
         torch.cuda.synchronize()
+        load_until(n0 + 2)
     _barrier(ws)
     total_ms = start.elapsed_time(end)
     kernel_ms = statistics.mean(a.elapsed_time(e) for a, e in per)
@@ -477,7 +499,8 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary(),
+            "clocks": dict(clk.summary(), note="sampled every 100 ms while the step ran back to back "
+                                                 "before, during and after the timed region"),
             "pipe_peaks": {k: {"per_sm_clk": round(v["per_sm_clk"], 2), "ops_per_s": v["ops_per_s"]}
                            for k, v in pipes.items()},
             "legs": legs,

@@ -104,6 +104,53 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t ex2_2(uint64_t x) {
+    float a, b;
+    upk2(x, a, b);
+    float ra, rb;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ra) : "f"(a));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(rb) : "f"(b));
+    return pk2(ra, rb);
+}
+__device__ __forceinline__ uint64_t rcp_2(uint64_t x) {
+    float a, b;
+    upk2(x, a, b);
+    float ra, rb;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(ra) : "f"(a));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rb) : "f"(b));
+    return pk2(ra, rb);
+}
+
+// softplus of two values at once: max(x, 0) + log1p(e^-|x|), log1p(w) =
+// 2 atanh(w / (2 + w)) summed to s^13 (see softplus_f); for x > 20 the log1p
+// term is below half an ulp of x, so the sum rounds to x exactly.
+__device__ __forceinline__ uint64_t softplus_2(uint64_t x) {
+    float x0, x1;
+    upk2(x, x0, x1);
+    const uint64_t w = ex2_2(pk2(-fabsf(x0) * MSC_LOG2E, -fabsf(x1) * MSC_LOG2E));
+    const uint64_t s = mul2(w, rcp_2(add2(w, pk2(2.f, 2.f))));
+    const uint64_t s2 = mul2(s, s);
+    uint64_t p = fma2(s2, pk2(2.f / 13.f, 2.f / 13.f), pk2(2.f / 11.f, 2.f / 11.f));
+    p = fma2(s2, p, pk2(2.f / 9.f, 2.f / 9.f));
+    p = fma2(s2, p, pk2(2.f / 7.f, 2.f / 7.f));
+    p = fma2(s2, p, pk2(2.f / 5.f, 2.f / 5.f));
+    p = fma2(s2, p, pk2(2.f / 3.f, 2.f / 3.f));
+    p = fma2(s2, p, pk2(2.f, 2.f));
+    return fma2(s, p, pk2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)));
+}
+
+// silu of two values: z / (1 + e^-z)
+__device__ __forceinline__ uint64_t silu_2(uint64_t z) {
+    float z0, z1;
+    upk2(z, z0, z1);
+    const uint64_t e = ex2_2(pk2(-z0 * MSC_LOG2E, -z1 * MSC_LOG2E));
+    return mul2(z, rcp_2(add2(e, pk2(1.f, 1.f))));
+}
 
 }  // namespace msc
 

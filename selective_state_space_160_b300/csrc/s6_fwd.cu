@@ -15,16 +15,17 @@
 // batch entry, stepping through time in tiles of 64-byte rows (32 bf16 or 16
 // fp32 steps).
 //
-// Main kernel (s6_fwd_tma_kernel): one lane issues 3-D TMA tile loads of
+// Main kernel (s6_fwd_tma_kernel): one thread issues 3-D TMA tile loads of
 // u / delta / z (32 rows x one tile) and B / C (16 slots x one tile, shared by
 // the warp's rows) into a two-stage shared-memory ring completed on mbarriers,
 // so the next tile streams in while the current one is computed.  Out-of-range
-// rows, slots and steps arrive zero-filled.  Each lane reads its own row with
-// 16-byte loads (64-byte swizzle: conflict-free), computes Delta, Delta*u and
-// D*u for 8 steps at a time, then runs the n loop on packed fp32 pairs
-// (fma.rn.f32x2: two states per issue slot) with B / C converted once per tile
-// into an n-pair-interleaved fp32 layout (each pair is one 64-bit operand, a
-// broadcast read).  y is stored from registers as 32-byte row segments.
+// rows, slots and steps arrive zero-filled.  Two lanes share a row (8 states
+// each); each computes Delta, Delta*u and D*u for half of an 8-step group
+// (softplus on packed pairs) and gathers the other half with shuffles, then
+// runs the n loop on packed fp32 pairs (fma.rn.f32x2: two states per issue
+// slot) with B / C converted once per tile into an n-pair-interleaved fp32
+// layout (each pair is one 64-bit broadcast operand).  The readout partial sums
+// are reduce-scattered between the pair and y is stored from registers.
 // Rows whose byte stride is not a multiple of 16 cannot be described to TMA;
 // they take the plain-load kernel (s6_fwd_rows_kernel), which stages each tile
 // with coalesced loads and computes the same way in scalar fp32.
@@ -310,30 +311,62 @@ constexpr int kStages = 2;
 constexpr int kRowTile = 2048;               // bytes of one 32-row x 64-byte tile
 constexpr int kBCTile = 1024;                // bytes of one 16-slot x 64-byte tile
 constexpr int kStageBytes = 3 * kRowTile + 2 * kBCTile;
-constexpr int kTmaThreads = 64;              // two lanes per channel row
+// Issues the TMA loads of one tile (u, delta, [z], B, [C]) into `st`.
+__device__ __forceinline__ void issue_tile(int, int64_t tj64, uint8_t* st, uint64_t* bar, uint32_t tx_bytes,
+                                           const CUtensorMap* tu, const CUtensorMap* td, const CUtensorMap* tz,
+                                           const CUtensorMap* tb, const CUtensorMap* tc, int64_t d0, int64_t b,
+                                           bool has_z, bool with_c) {
+    const int tj = (int)tj64;
+    msc::mbar_arrive_expect_tx(bar, tx_bytes);
+    msc::tma_load_3d(st, tu, bar, tj, (int)d0, (int)b);
+    msc::tma_load_3d(st + kRowTile, td, bar, tj, (int)d0, (int)b);
+    if (has_z) msc::tma_load_3d(st + 2 * kRowTile, tz, bar, tj, (int)d0, (int)b);
+    msc::tma_load_3d(st + 3 * kRowTile, tb, bar, tj, 0, (int)b);
+    if (with_c) msc::tma_load_3d(st + 3 * kRowTile + kBCTile, tc, bar, tj, 0, (int)b);
+}
 
-// Two lanes share a row: lane parity j owns states n in [8j, 8j + 8) and the
-// per-step work (softplus, gate, store) of steps 4j .. 4j+3 of every 8-step
-// group; the two halves are exchanged with one shuffle each.
-template <bool kBF16, int kMode>
-__global__ void __launch_bounds__(kTmaThreads) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
-                                                                 const __grid_constant__ CUtensorMap tm_d,
-                                                                 const __grid_constant__ CUtensorMap tm_z,
-                                                                 const __grid_constant__ CUtensorMap tm_B,
-                                                                 const __grid_constant__ CUtensorMap tm_C,
-                                                                 const FwdParams p) {
+// One level of the readout reduce-scatter: lanes that differ in bit `kSL` of
+// their group position exchange halves of v[0..kSpan) and keep the half of
+// their side, summed, in v[0..kSpan/2).
+template <int kSL, int kSpan>
+__device__ __forceinline__ void reduce_scatter_level(float* v, int j) {
+    const bool side = (j & kSL) != 0;
+#pragma unroll
+    for (int k = 0; k < kSpan / 2; ++k) {
+        const float send = side ? v[k] : v[k + kSpan / 2];
+        const float keep = side ? v[k + kSpan / 2] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, kSL);
+    }
+}
+
+// kNG lanes share a channel row: lane j of the group owns states
+// n in [j * 16 / kNG, (j + 1) * 16 / kNG) and the per-step work (softplus, gate,
+// store) of steps j * 8 / kNG .. of every 8-step group.  Per-step scalars are
+// gathered from their owner lane with shuffles; the readout partial sums are
+// reduce-scattered back with a shuffle butterfly.
+template <bool kBF16, int kMode, int kNG>
+__global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
+                                                              const __grid_constant__ CUtensorMap tm_d,
+                                                              const __grid_constant__ CUtensorMap tm_z,
+                                                              const __grid_constant__ CUtensorMap tm_B,
+                                                              const __grid_constant__ CUtensorMap tm_C,
+                                                              const FwdParams p) {
     constexpr bool kFull = (kMode == kModeFull);
     constexpr int kTT = kBF16 ? 32 : 16;  // steps per 64-byte tile row
     constexpr int kGroups = kTT / 8;
     constexpr int kPitch = 2 * kTT + 4;   // floats per n-pair row of s_bc (padded: conflict-free stores)
+    constexpr int kES = kBF16 ? 2 : 4;    // bytes per element
+    constexpr int kPPL = 8 / kNG;         // state pairs per lane
+    constexpr int kSPG = 8 / kNG;         // steps per lane per 8-step group
     __shared__ __align__(1024) uint8_t s_raw[kStages][kStageBytes];
     __shared__ __align__(16) float s_bc[2][kNS / 2][kPitch];  // [B|C][n pair][t * 2 + n parity]
     __shared__ __align__(8) uint64_t s_full[kStages];
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
-    const int r = 16 * (tid >> 5) + (lane >> 1);  // row within the CTA
-    const int j = lane & 1;                       // state half / step half
+    const int r = tid / kNG;          // row within the CTA
+    const int j = lane & (kNG - 1);   // position within the row's lane group
+    const int glane0 = lane & ~(kNG - 1);
     const int64_t b = blockIdx.y;
     const int64_t d0 = (int64_t)blockIdx.x * kRows;
     const int nrows = (int)imin64(kRows, p.dim - d0);
@@ -344,13 +377,13 @@ __global__ void __launch_bounds__(kTmaThreads) s6_fwd_tma_kernel(const __grid_co
     const int N = p.N;
     const bool has_z = kFull && p.z != nullptr;
 
-    uint64_t A2p[4], h2[4];
+    uint64_t A2p[kPPL], h2[kPPL];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kPPL; ++q) {
         float a[2], h[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int n = 8 * j + 2 * q + e;
+            const int n = 2 * (kPPL * j + q) + e;
             a[e] = (row_ok && n < N) ? __ldg(p.A + d * N + n) * MSC_LOG2E : 0.f;
             h[e] = 0.f;
             if (kFull && row_ok && n < N) {
@@ -383,20 +416,10 @@ __global__ void __launch_bounds__(kTmaThreads) s6_fwd_tma_kernel(const __grid_co
     }
     __syncthreads();
 
-    auto issue = [&](int jt) {
-        const int s = jt % kStages;
-        const int tj = (int)(t_begin + (int64_t)jt * kTT);
-        uint8_t* st = s_raw[s];
-        msc::mbar_arrive_expect_tx(&s_full[s], tx_bytes);
-        msc::tma_load_3d(st, &tm_u, &s_full[s], tj, (int)d0, (int)b);
-        msc::tma_load_3d(st + kRowTile, &tm_d, &s_full[s], tj, (int)d0, (int)b);
-        if (has_z) msc::tma_load_3d(st + 2 * kRowTile, &tm_z, &s_full[s], tj, (int)d0, (int)b);
-        msc::tma_load_3d(st + 3 * kRowTile, &tm_B, &s_full[s], tj, 0, (int)b);
-        if (kFull) msc::tma_load_3d(st + 3 * kRowTile + kBCTile, &tm_C, &s_full[s], tj, 0, (int)b);
-    };
-
     if (tid == 0)
-        for (int jt = 0; jt < kStages && jt < ntiles; ++jt) issue(jt);
+        for (int jt = 0; jt < kStages && jt < ntiles; ++jt)
+            issue_tile(jt, t_begin + (int64_t)jt * kTT, s_raw[jt % kStages], &s_full[jt % kStages], tx_bytes,
+                       &tm_u, &tm_d, &tm_z, &tm_B, &tm_C, d0, b, has_z, kFull);
     int issued = ntiles < kStages ? ntiles : kStages;
 
     bool failed = false;
@@ -415,7 +438,7 @@ __global__ void __launch_bounds__(kTmaThreads) s6_fwd_tma_kernel(const __grid_co
         const int nt = (int)imin64(kTT, t_end - t0);
 
         // B (and C) of this tile -> fp32 pairs s_bc[x][q][2t + e] = X[n = 2q + e][t]
-        {
+        if (tid < 64) {
             const int x = tid >> 5, q = lane & 7, c = lane >> 3;
             if (x == 0 || kFull) {
                 const uint8_t* src = raw + 3 * kRowTile + x * kBCTile;
@@ -442,115 +465,152 @@ __global__ void __launch_bounds__(kTmaThreads) s6_fwd_tma_kernel(const __grid_co
 #pragma unroll 1
         for (int g = 0; g < kGroups; ++g) {
             if (8 * g >= nt) break;
-            // ---- this lane's 4 steps (8g + 4j ..): Delta, Delta*u, D*u
-            float uu[4], dl[4];
+            const bool partial = 8 * g + 8 > nt;
+            // ---- this lane's kSPG steps: Delta, Delta*u, D*u on packed pairs
+            const uint32_t boff = (uint32_t)(8 * g * kES + j * kSPG * kES);  // byte offset in the row
+            uint64_t u2[kSPG / 2], x2[kSPG / 2];
             if constexpr (kBF16) {
-                const uint2 vu = *reinterpret_cast<const uint2*>(raw + msc::sw64(r, g) + 8 * j);
-                const uint2 vd = *reinterpret_cast<const uint2*>(raw + kRowTile + msc::sw64(r, g) + 8 * j);
-                uu[0] = msc::bf16lo(vu.x); uu[1] = msc::bf16hi(vu.x); uu[2] = msc::bf16lo(vu.y); uu[3] = msc::bf16hi(vu.y);
-                dl[0] = msc::bf16lo(vd.x); dl[1] = msc::bf16hi(vd.x); dl[2] = msc::bf16lo(vd.y); dl[3] = msc::bf16hi(vd.y);
-            } else {
-                const float4 vu = *reinterpret_cast<const float4*>(raw + msc::sw64(r, 2 * g + j));
-                const float4 vd = *reinterpret_cast<const float4*>(raw + kRowTile + msc::sw64(r, 2 * g + j));
-                uu[0] = vu.x; uu[1] = vu.y; uu[2] = vu.z; uu[3] = vu.w;
-                dl[0] = vd.x; dl[1] = vd.y; dl[2] = vd.z; dl[3] = vd.w;
-            }
-            float mdt[4], mdtu[4], mdu[4];
+                const uint8_t* pu = raw + msc::sw64(r, boff >> 4) + (boff & 15);
+                const uint8_t* pd = raw + kRowTile + msc::sw64(r, boff >> 4) + (boff & 15);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float dt = msc::softplus_f(dl[k] + bias);
-                if (8 * g + 4 * j + k >= nt) dt = 0.f;  // past the tile end: abar = 1, input 0
-                mdt[k] = dt;
-                mdtu[k] = dt * uu[k];
-                mdu[k] = Dd * uu[k];
-                if (!kFull) dsum += dt;
-            }
-            // ---- exchange halves: every lane gets Delta, Delta*u of all 8 steps
-            uint64_t dt2[8], dtu2[8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float odt = __shfl_xor_sync(0xffffffffu, mdt[k], 1);
-                const float odtu = __shfl_xor_sync(0xffffffffu, mdtu[k], 1);
-                const float lo_dt = j ? odt : mdt[k], hi_dt = j ? mdt[k] : odt;
-                const float lo_dtu = j ? odtu : mdtu[k], hi_dtu = j ? mdtu[k] : odtu;
-                dt2[k] = msc::pk2(lo_dt, lo_dt);
-                dt2[k + 4] = msc::pk2(hi_dt, hi_dt);
-                dtu2[k] = msc::pk2(lo_dtu, lo_dtu);
-                dtu2[k + 4] = msc::pk2(hi_dtu, hi_dtu);
-            }
-            // ---- the scan over this lane's 4 n-pairs
-            uint64_t acc[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] = 0ull;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint64_t Bp[8], Cp[8];
-                const ulonglong2* bsrc = reinterpret_cast<const ulonglong2*>(&s_bc[0][4 * j + q][16 * g]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const ulonglong2 v = bsrc[k];
-                    Bp[2 * k] = v.x; Bp[2 * k + 1] = v.y;
+                for (int e = 0; e < kSPG / 2; ++e) {
+                    const uint32_t wu = reinterpret_cast<const uint32_t*>(pu)[e];
+                    const uint32_t wd = reinterpret_cast<const uint32_t*>(pd)[e];
+                    u2[e] = msc::pk2(msc::bf16lo(wu), msc::bf16hi(wu));
+                    x2[e] = msc::pk2(msc::bf16lo(wd), msc::bf16hi(wd));
                 }
-                if (kFull) {
-                    const ulonglong2* csrc = reinterpret_cast<const ulonglong2*>(&s_bc[1][4 * j + q][16 * g]);
+            } else {
+                const uint8_t* pu = raw + msc::sw64(r, boff >> 4) + (boff & 15);
+                const uint8_t* pd = raw + kRowTile + msc::sw64(r, boff >> 4) + (boff & 15);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const ulonglong2 v = csrc[k];
-                        Cp[2 * k] = v.x; Cp[2 * k + 1] = v.y;
+                for (int e = 0; e < kSPG / 2; ++e) {
+                    u2[e] = reinterpret_cast<const uint64_t*>(pu)[e];
+                    x2[e] = reinterpret_cast<const uint64_t*>(pd)[e];
+                }
+            }
+            const uint64_t bias2 = msc::pk2(bias, bias);
+            uint64_t mdt2[kSPG / 2], mdtu2[kSPG / 2], mdu2[kSPG / 2];
+#pragma unroll
+            for (int e = 0; e < kSPG / 2; ++e) {
+                uint64_t dt = msc::softplus_2(msc::add2(x2[e], bias2));
+                if (partial) {
+                    float a, c;
+                    msc::upk2(dt, a, c);
+                    const int k0 = 8 * g + j * kSPG + 2 * e;
+                    dt = msc::pk2(k0 < nt ? a : 0.f, k0 + 1 < nt ? c : 0.f);  // past the end: abar = 1, input 0
+                }
+                mdt2[e] = dt;
+                mdtu2[e] = msc::mul2(dt, u2[e]);
+                mdu2[e] = msc::mul2(msc::pk2(Dd, Dd), u2[e]);
+                if (!kFull) {
+                    float a, c;
+                    msc::upk2(dt, a, c);
+                    dsum += a + c;
+                }
+            }
+            // ---- every lane of the group gets Delta, Delta*u of all 8 steps
+            float mdt[kSPG], mdtu[kSPG];
+#pragma unroll
+            for (int e = 0; e < kSPG / 2; ++e) {
+                msc::upk2(mdt2[e], mdt[2 * e], mdt[2 * e + 1]);
+                msc::upk2(mdtu2[e], mdtu[2 * e], mdtu[2 * e + 1]);
+            }
+            float dts[8], dtus[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int src = glane0 | (k / kSPG);
+                dts[k] = __shfl_sync(0xffffffffu, mdt[k % kSPG], src);
+                dtus[k] = __shfl_sync(0xffffffffu, mdtu[k % kSPG], src);
+            }
+            // ---- the scan: 8 steps, kPPL independent state pairs per step
+            uint64_t acc[8];
+            const float* bsrc = &s_bc[0][kPPL * j][16 * g];
+            const float* csrc = &s_bc[1][kPPL * j][16 * g];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                uint64_t Bp[kPPL][2], Cp[kPPL][2];
+#pragma unroll
+                for (int q = 0; q < kPPL; ++q) {
+                    const ulonglong2 vb = *reinterpret_cast<const ulonglong2*>(bsrc + q * kPitch + 4 * kk);
+                    Bp[q][0] = vb.x; Bp[q][1] = vb.y;
+                    if (kFull) {
+                        const ulonglong2 vc = *reinterpret_cast<const ulonglong2*>(csrc + q * kPitch + 4 * kk);
+                        Cp[q][0] = vc.x; Cp[q][1] = vc.y;
                     }
                 }
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    float a0, a1;
-                    msc::upk2(msc::mul2(dt2[k], A2p[q]), a0, a1);
-                    const uint64_t a = msc::pk2(msc::ex2_approx(a0), msc::ex2_approx(a1));
-                    h2[q] = msc::fma2(a, h2[q], msc::mul2(dtu2[k], Bp[k]));
-                    if (kFull) acc[k] = msc::fma2(Cp[k], h2[q], acc[k]);
+                for (int e = 0; e < 2; ++e) {
+                    const int k = 2 * kk + e;
+                    const uint64_t dt2 = msc::pk2(dts[k], dts[k]);
+                    const uint64_t dtu2 = msc::pk2(dtus[k], dtus[k]);
+                    uint64_t acc_a = 0ull, acc_b = 0ull;
+#pragma unroll
+                    for (int q = 0; q < kPPL; ++q) {
+                        const uint64_t a = msc::ex2_2(msc::mul2(dt2, A2p[q]));
+                        h2[q] = msc::fma2(a, h2[q], msc::mul2(dtu2, Bp[q][e]));
+                        if (kFull) {
+                            if (q == 0) acc_a = msc::mul2(Cp[q][e], h2[q]);
+                            else if (q == 1) acc_b = msc::mul2(Cp[q][e], h2[q]);
+                            else if (q % 2 == 0) acc_a = msc::fma2(Cp[q][e], h2[q], acc_a);
+                            else acc_b = msc::fma2(Cp[q][e], h2[q], acc_b);
+                        }
+                    }
+                    if (kFull) acc[k] = (kPPL > 1) ? msc::add2(acc_a, acc_b) : acc_a;
                 }
             }
-            // ---- readout + skip + gate of this lane's 4 steps
+            // ---- readout + skip + gate of this lane's steps
             if (kFull) {
-                float tot[8];
+                float v[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     float lo, hi;
                     msc::upk2(acc[k], lo, hi);
-                    tot[k] = lo + hi;
+                    v[k] = lo + hi;
                 }
-                float zz[4] = {0.f, 0.f, 0.f, 0.f};
+                // reduce-scatter over the group: lane j ends with steps j*kSPG ..
+                reduce_scatter_level<kNG / 2, 8>(v, j);
+                if constexpr (kNG == 4) reduce_scatter_level<1, 4>(v, j);
+                uint64_t y2[kSPG / 2];
+#pragma unroll
+                for (int e = 0; e < kSPG / 2; ++e) y2[e] = msc::add2(msc::pk2(v[2 * e], v[2 * e + 1]), mdu2[e]);
                 if (has_z) {
-                    if constexpr (kBF16) {
-                        const uint2 vz = *reinterpret_cast<const uint2*>(raw + 2 * kRowTile + msc::sw64(r, g) + 8 * j);
-                        zz[0] = msc::bf16lo(vz.x); zz[1] = msc::bf16hi(vz.x); zz[2] = msc::bf16lo(vz.y); zz[3] = msc::bf16hi(vz.y);
-                    } else {
-                        const float4 vz = *reinterpret_cast<const float4*>(raw + 2 * kRowTile + msc::sw64(r, 2 * g + j));
-                        zz[0] = vz.x; zz[1] = vz.y; zz[2] = vz.z; zz[3] = vz.w;
+                    const uint32_t zoff = boff;
+                    const uint8_t* pz = raw + 2 * kRowTile + msc::sw64(r, zoff >> 4) + (zoff & 15);
+#pragma unroll
+                    for (int e = 0; e < kSPG / 2; ++e) {
+                        uint64_t z2;
+                        if constexpr (kBF16) {
+                            const uint32_t wz = reinterpret_cast<const uint32_t*>(pz)[e];
+                            z2 = msc::pk2(msc::bf16lo(wz), msc::bf16hi(wz));
+                        } else {
+                            z2 = reinterpret_cast<const uint64_t*>(pz)[e];
+                        }
+                        y2[e] = msc::mul2(y2[e], msc::silu_2(z2));
                     }
                 }
-                float yv[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float send = j ? tot[k] : tot[k + 4];   // the partner's steps
-                    const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-                    float v = (j ? tot[k + 4] : tot[k]) + recv + mdu[k];
-                    if (has_z) v *= msc::silu_f(zz[k]);
-                    yv[k] = v;
-                }
                 if (row_ok) {
-                    const int rem = nt - 8 * g - 4 * j;
-                    float* qy = p.y + row * p.L + t0 + 8 * g + 4 * j;
-                    if (rem >= 4) {
-                        __stcs(reinterpret_cast<float4*>(qy), make_float4(yv[0], yv[1], yv[2], yv[3]));
+                    const int rem = nt - 8 * g - j * kSPG;
+                    float* qy = p.y + row * p.L + t0 + 8 * g + j * kSPG;
+                    if (rem >= kSPG) {
+                        if constexpr (kSPG == 4)
+                            __stcs(reinterpret_cast<ulonglong2*>(qy), make_ulonglong2(y2[0], y2[1]));
+                        else
+                            __stcs(reinterpret_cast<unsigned long long*>(qy), (unsigned long long)y2[0]);
                     } else {
+                        float vv[kSPG];
 #pragma unroll
-                        for (int k = 0; k < 3; ++k)
-                            if (k < rem) qy[k] = yv[k];
+                        for (int e = 0; e < kSPG / 2; ++e) msc::upk2(y2[e], vv[2 * e], vv[2 * e + 1]);
+#pragma unroll
+                        for (int k = 0; k < kSPG - 1; ++k)
+                            if (k < rem) qy[k] = vv[k];
                     }
                 }
             }
         }
         __syncthreads();
-        if (tid == 0 && issued < ntiles) issue(issued);
+        if (tid == 0 && issued < ntiles)
+            issue_tile(issued, t_begin + (int64_t)issued * kTT, s_raw[issued % kStages], &s_full[issued % kStages],
+                       tx_bytes, &tm_u, &tm_d, &tm_z, &tm_B, &tm_C, d0, b, has_z, kFull);
         ++issued;
     }
 
@@ -561,13 +621,16 @@ __global__ void __launch_bounds__(kTmaThreads) s6_fwd_tma_kernel(const __grid_co
                 (void)wait_phase(&s_full[jt % kStages], (uint32_t)((jt / kStages) & 1));
         return;
     }
-    if (!kFull) dsum += __shfl_xor_sync(0xffffffffu, dsum, 1);
+    if (!kFull) {
+#pragma unroll
+        for (int sl = 1; sl < kNG; sl *= 2) dsum += __shfl_xor_sync(0xffffffffu, dsum, sl);
+    }
     if (!row_ok) return;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kPPL; ++q) {
         float v0, v1;
         msc::upk2(h2[q], v0, v1);
-        const int n = 8 * j + 2 * q;
+        const int n = 2 * (kPPL * j + q);
         if (kFull) {
             if (p.h_last && seg == p.G - 1) {
                 if (n < N) p.h_last[row * N + n] = v0;
@@ -635,14 +698,24 @@ bool make_maps(FwdMaps& m, const FwdParams& p, int64_t batch, bool bf16) {
     return true;
 }
 
-template <bool kBF16>
-msc_status launch_tma(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
+// Lanes per channel row of the TMA kernel.  Two beat four on the batch-8 x
+// 5120 x 2048 workload (0.45 ms vs 0.54 ms): four lanes double the resident
+// warps but add more exchange work than the extra latency hiding recovers.
+constexpr int kLanesPerRow = 2;
+
+template <bool kBF16, int kNG>
+msc_status launch_tma_ng(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
     if (mode == kModeFull)
-        s6_fwd_tma_kernel<kBF16, kModeFull><<<grid, kTmaThreads, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+        s6_fwd_tma_kernel<kBF16, kModeFull, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
     else
-        s6_fwd_tma_kernel<kBF16, kModeAgg><<<grid, kTmaThreads, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+        s6_fwd_tma_kernel<kBF16, kModeAgg, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
     return msc_host::check_launch("s6_fwd_tma");
+}
+
+template <bool kBF16>
+msc_status launch_tma(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
+    return launch_tma_ng<kBF16, kLanesPerRow>(m, p, batch, G, mode, st);
 }
 
 // TMA needs every row stride to be a multiple of 16 bytes.
