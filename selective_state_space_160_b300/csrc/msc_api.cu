@@ -260,6 +260,10 @@ msc_status msc_check_device_status(void* stream) {
     msc_status s = s6_fwd_take_status(&code, &site);
     if (s != MSC_OK) return s;
     if (code == 0) {
+        s = s6_bwd_take_status(&code, &site);
+        if (s != MSC_OK) return s;
+    }
+    if (code == 0) {
         s = ssd_take_status(&code, &site);
         if (s != MSC_OK) return s;
     }

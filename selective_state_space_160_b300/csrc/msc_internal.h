@@ -29,9 +29,14 @@ struct S6FwdArgs {
 
 msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t stream);
 
+// Checkpoint pass used by the backward: writes the state entering every
+// 8-step group of every row to ckpt [batch * dim, ceil(L / 8), 16] (fp32).
+msc_status s6_fwd_checkpoints(const S6FwdArgs& a, float* ckpt, cudaStream_t stream);
+
 // Each translation unit with bounded device-side waits keeps its own status
 // word (code, site); these read and clear it.
 msc_status s6_fwd_take_status(unsigned int* code, unsigned int* site);
+msc_status s6_bwd_take_status(unsigned int* code, unsigned int* site);
 msc_status ssd_take_status(unsigned int* code, unsigned int* site);
 
 size_t s6_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);

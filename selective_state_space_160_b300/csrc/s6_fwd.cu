@@ -52,7 +52,7 @@ constexpr int kT = 32;     // timesteps per staged tile
 constexpr int kNS = 16;    // state slots per lane (dstate <= 16)
 constexpr int kStride = kT + 4;
 
-enum { kModeFull = 0, kModeAgg = 1 };
+enum { kModeFull = 0, kModeAgg = 1, kModeCkpt = 2 };
 
 __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
@@ -70,6 +70,8 @@ struct FwdParams {
     float* h_last;
     float* seg_state;  // [rows, G, N]: aggregates, then carries
     float* seg_dsum;   // [rows, G]
+    float* ckpt;       // [rows, ckpt_groups, 16]: state at every 8-step group start
+    int64_t ckpt_groups;
     int64_t dim, L, seg_len;
     int N, G;
 };
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
                 mdt2[e] = dt;
                 mdtu2[e] = msc::mul2(dt, u2[e]);
                 mdu2[e] = msc::mul2(msc::pk2(Dd, Dd), u2[e]);
-                if (!kFull) {
+                if (kMode == kModeAgg) {
                     float a, c;
                     msc::upk2(dt, a, c);
                     dsum += a + c;
@@ -521,6 +523,14 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
                 const int src = glane0 | (k / kSPG);
                 dts[k] = __shfl_sync(0xffffffffu, mdt[k % kSPG], src);
                 dtus[k] = __shfl_sync(0xffffffffu, mdtu[k % kSPG], src);
+            }
+            if (kMode == kModeCkpt && row_ok) {
+                // state entering this 8-step group, for the recomputing backward
+                float* cp = p.ckpt + ((size_t)row * p.ckpt_groups + (size_t)((t0 + 8 * g) >> 3)) * kNS +
+                            2 * kPPL * j;
+#pragma unroll
+                for (int q = 0; q < kPPL; q += 2)
+                    *reinterpret_cast<ulonglong2*>(cp + 2 * q) = make_ulonglong2(h2[q], h2[q + 1]);
             }
             // ---- the scan: 8 steps, kPPL independent state pairs per step
             uint64_t acc[8];
@@ -621,6 +631,7 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
                 (void)wait_phase(&s_full[jt % kStages], (uint32_t)((jt / kStages) & 1));
         return;
     }
+    if (kMode == kModeCkpt) return;
     if (!kFull) {
 #pragma unroll
         for (int sl = 1; sl < kNG; sl *= 2) dsum += __shfl_xor_sync(0xffffffffu, dsum, sl);
@@ -708,8 +719,10 @@ msc_status launch_tma_ng(const FwdMaps& m, const FwdParams& p, int64_t batch, in
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
     if (mode == kModeFull)
         s6_fwd_tma_kernel<kBF16, kModeFull, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
-    else
+    else if (mode == kModeAgg)
         s6_fwd_tma_kernel<kBF16, kModeAgg, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    else
+        s6_fwd_tma_kernel<kBF16, kModeCkpt, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
     return msc_host::check_launch("s6_fwd_tma");
 }
 
@@ -791,6 +804,24 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
         if (s != MSC_OK) return s;
     }
     return launch_mode(p, mp, a.bf16, vec, a.batch, plan.G, kModeFull, st);
+}
+
+// Checkpoint pass of the backward: the state entering every 8-step group of
+// every row, written to ckpt [batch * dim, ceil(L / 8), 16].  Rows must be
+// TMA-describable (row stride a multiple of 16 bytes).
+msc_status s6_fwd_checkpoints(const S6FwdArgs& a, float* ckpt, cudaStream_t st) {
+    FwdParams p{};
+    p.u = a.u; p.delta = a.delta; p.z = nullptr; p.B = a.B; p.C = a.C;
+    p.A = a.A; p.D = nullptr; p.delta_bias = a.delta_bias; p.h0 = nullptr;
+    p.y = nullptr; p.h_last = nullptr;
+    p.dim = a.dim; p.L = a.L; p.N = a.N; p.G = 1; p.seg_len = a.L;
+    p.ckpt = ckpt;
+    p.ckpt_groups = (a.L + 7) / 8;
+    if (!tma_ok(p, a.bf16)) return fail(MSC_ERR_UNSUPPORTED, "checkpoint pass needs a 16-byte row stride");
+    FwdMaps maps;
+    if (!make_maps(maps, p, a.batch, a.bf16)) return MSC_ERR_CUDA;
+    return a.bf16 ? launch_tma_ng<true, kLanesPerRow>(maps, p, a.batch, 1, kModeCkpt, st)
+                  : launch_tma_ng<false, kLanesPerRow>(maps, p, a.batch, 1, kModeCkpt, st);
 }
 
 // Reads and clears this module's device status word.
