@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmsc.so")
-PROBE_SRC = os.path.join(PKG, "probe", "pipe_peaks.cu")
+PROBE_DIR = os.path.join(PKG, "probe")
 PROBE_LIB = os.path.join(PKG, "libmsc_probe.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -63,12 +63,15 @@ def build(force: bool = False, verbose: bool = False, extra=None) -> str:
 
 
 def build_probe(force: bool = False, verbose: bool = False) -> str:
-    """Build the pipe-throughput probe library used by bench.py."""
-    if not force and os.path.exists(PROBE_LIB) and os.path.getmtime(PROBE_LIB) >= os.path.getmtime(PROBE_SRC):
+    """Build the probe library: pipe-throughput measurement used by bench.py and
+    the tcgen05 building-block check used by the tests."""
+    srcs = sorted(glob.glob(os.path.join(PROBE_DIR, "*.cu")))
+    newest = max(os.path.getmtime(p) for p in srcs + _deps())
+    if not force and os.path.exists(PROBE_LIB) and os.path.getmtime(PROBE_LIB) >= newest:
         return PROBE_LIB
     tmp = PROBE_LIB + ".tmp"
     cmd = [nvcc()] + ARCH + ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-cudart", "static",
-                             "-o", tmp, PROBE_SRC]
+                             "-I", INCLUDE, "-I", CSRC, "-o", tmp] + srcs
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
