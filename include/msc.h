@@ -80,6 +80,32 @@ msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, in
                                   float* y, float* h_last,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* -------------------------------------------- S6 forward without allocation
+ * No counterpart on the pages: an interface for callers that cannot allocate
+ * device memory -- a plugin inside a host framework that owns every device
+ * allocation and exposes no allocator to it, or a latency-critical serving loop
+ * that must not call cudaMalloc on its hot path (cudaMalloc can synchronise the
+ * device).  Same arguments, results and errors as msc_selective_scan_fwd()
+ * without the workspace: the segment scratch of long sequences comes from a
+ * library-owned array of MSC_STATIC_SCRATCH_BYTES in device global memory,
+ * present on every device that loads the library until the process exits.
+ * - A problem whose msc_selective_scan_fwd_workspace_size() exceeds
+ *   MSC_STATIC_SCRATCH_BYTES returns MSC_ERR_WORKSPACE and launches nothing.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current, and caches it; make that
+ *   first call before any stream capture.
+ * - All calls share the one array and its contents persist between calls:
+ *   calls that overlap on the GPU (other streams, other host threads) race.
+ * - Allocates nothing itself (no cudaMalloc / cudaFree). */
+#define MSC_STATIC_SCRATCH_BYTES (4u << 20)
+
+msc_status msc_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                          msc_dtype in_dtype,
+                                          const void* u, const void* delta, const float* A,
+                                          const void* B, const void* C, const float* D,
+                                          const void* z, const float* delta_bias, const float* h0,
+                                          float* y, float* h_last, void* stream);
+
 /* ----------------------------------------------------------------- S6 backward
  * Same shapes and dtype as the forward (zero initial state), plus the upstream
  * gradient dy [batch, dim, seqlen] (in_dtype).  Outputs (fp32, overwritten):

@@ -41,6 +41,7 @@ SIGNATURES = {
     "msc_selective_scan_bwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 9 + [_vp] * 8 + [_vp, _sz, _vp]),
     "msc_ssd_chunked_fwd_workspace_size": (_sz, [_i64] * 7),
     "msc_ssd_chunked_fwd": (ctypes.c_int, [_i64] * 7 + [ctypes.c_int] + [_vp] * 10 + [_vp, _sz, _vp]),
+    "msc_selective_scan_fwd_noalloc": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 11 + [_vp]),
     "msc_check_device_status": (ctypes.c_int, [_vp]),
     "msc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "msc_last_error": (ctypes.c_char_p, []),
