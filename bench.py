@@ -41,7 +41,10 @@ HEADLINE = dict(batch=8, dim=5120, L=2048, N=16)
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch, from one ncu capture,
 # keyed by kernel; valid only while the kernel source hash matches.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/s6_fwd_tma_8x5120x2048_bf16.md: DRAM read 505.2 MB + write 298.3 MB
+    "s6_fwd_rows_kernel": {"src_sha": "b0be9c35fa5e", "bytes_per_launch": 803.5e6},
+}
 
 
 def _sha(path):
