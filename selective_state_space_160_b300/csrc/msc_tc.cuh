@@ -39,13 +39,30 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
     return d;
 }
 
+// Descriptor of an MN-major SW128 tile: 64-element MN blocks of K rows x 128
+// bytes each (the layout TMA writes for a box {64 along MN, K rows} with
+// SWIZZLE_128B); `lbo_bytes` = distance between consecutive 64-wide MN blocks,
+// SBO = 1024 bytes between groups of 8 K rows.  Step K by 16 with +2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr, uint32_t lbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with fp32 accumulation.
-// ab_bf16: operands bf16 (else fp16), both K-major.  M in {64, 128}, N % 16 == 0.
-__host__ __device__ constexpr uint32_t idesc_f16(bool ab_bf16, int M, int N) {
+// ab_bf16: operands bf16 (else fp16).  a_mn / b_mn: operand MN-major (else
+// K-major).  M in {64, 128}, N % 16 == 0.
+__host__ __device__ constexpr uint32_t idesc_f16(bool ab_bf16, int M, int N, bool a_mn = false,
+                                                 bool b_mn = false) {
     return (1u << 4)                                    // D format: f32
          | ((ab_bf16 ? 1u : 0u) << 7)                   // A format
          | ((ab_bf16 ? 1u : 0u) << 10)                  // B format
-         | (0u << 15) | (0u << 16)                      // A, B K-major
+         | ((a_mn ? 1u : 0u) << 15)                     // A major
+         | ((b_mn ? 1u : 0u) << 16)                     // B major
          | ((uint32_t)(N >> 3) << 17)                   // N >> 3, bits 17-22
          | ((uint32_t)(M >> 4) << 24);                  // M >> 4, bits 24-28
 }

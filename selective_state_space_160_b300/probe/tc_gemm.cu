@@ -21,7 +21,7 @@ __device__ unsigned int g_tc_status;
 __global__ void __launch_bounds__(128) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                       const __grid_constant__ CUtensorMap tmB,
                                                       const uint16_t* A, const uint16_t* B, float* D, int K, int N,
-                                                      int bf16, int use_tma) {
+                                                      int bf16, int use_tma, int a_mn, int b_mn) {
     extern __shared__ uint8_t s_dyn[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_dyn) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = base;                     // 128 x K
@@ -45,9 +45,15 @@ __global__ void __launch_bounds__(128) tc_gemm_kernel(const __grid_constant__ CU
         if (tid == 0) {
             const uint32_t bytes = (uint32_t)(128 * K * 2 + N * K * 2);
             msc::mbar_arrive_expect_tx(&bar[1], bytes);
-            for (int kb = 0; kb < K / 64; ++kb) {
-                msc::tma_load_2d(sA + kb * 128 * 128, &tmA, &bar[1], kb * 64, 0);
-                msc::tma_load_2d(sB + kb * N * 128, &tmB, &bar[1], kb * 64, 0);
+            if (a_mn) {  // A given as [K][128]: two 64-wide M blocks of K rows
+                for (int mb = 0; mb < 2; ++mb) msc::tma_load_2d(sA + mb * K * 128, &tmA, &bar[1], mb * 64, 0);
+            } else {
+                for (int kb = 0; kb < K / 64; ++kb) msc::tma_load_2d(sA + kb * 128 * 128, &tmA, &bar[1], kb * 64, 0);
+            }
+            if (b_mn) {  // B given as [K][N]: N / 64 blocks of K rows
+                for (int nb = 0; nb < N / 64; ++nb) msc::tma_load_2d(sB + nb * K * 128, &tmB, &bar[1], nb * 64, 0);
+            } else {
+                for (int kb = 0; kb < K / 64; ++kb) msc::tma_load_2d(sB + kb * N * 128, &tmB, &bar[1], kb * 64, 0);
             }
         }
         bool ok = msc::mbar_wait(&bar[1], 0, 1u << 24);
@@ -67,11 +73,13 @@ __global__ void __launch_bounds__(128) tc_gemm_kernel(const __grid_constant__ CU
     msc::tc_fence_after();
     const uint32_t tmem = *slot;
     if (tid == 0) {
-        const uint32_t idesc = msc::idesc_f16(bf16 != 0, 128, N);
+        const uint32_t idesc = msc::idesc_f16(bf16 != 0, 128, N, a_mn != 0, b_mn != 0);
         for (int k = 0; k < K / 16; ++k) {
-            const uint32_t koff = (uint32_t)((k >> 2) * 0 + (k & 3) * 32);
-            const uint64_t ad = msc::sdesc_sw128(msc::smem_u32(sA + (k >> 2) * 128 * 128) + koff);
-            const uint64_t bd = msc::sdesc_sw128(msc::smem_u32(sB + (k >> 2) * N * 128) + koff);
+            const uint32_t koff = (uint32_t)((k & 3) * 32);
+            const uint64_t ad = a_mn ? msc::sdesc_sw128_mn(msc::smem_u32(sA) + k * 2048, K * 128)
+                                     : msc::sdesc_sw128(msc::smem_u32(sA + (k >> 2) * 128 * 128) + koff);
+            const uint64_t bd = b_mn ? msc::sdesc_sw128_mn(msc::smem_u32(sB) + k * 2048, K * 128)
+                                     : msc::sdesc_sw128(msc::smem_u32(sB + (k >> 2) * N * 128) + koff);
             msc::mma_f16(tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
         }
         msc::mma_commit(&bar[0]);
@@ -94,7 +102,8 @@ __global__ void __launch_bounds__(128) tc_gemm_kernel(const __grid_constant__ CU
     if (warp == 0) msc::tmem_dealloc(tmem, ncols);
 }
 
-bool encode2d(CUtensorMap* m, const void* base, int rows, int K, bool bf16) {
+// 2-D map of a [rows][cols] tensor (cols contiguous) with boxes {64, box_rows}.
+bool encode2d(CUtensorMap* m, const void* base, int rows, int cols, bool bf16) {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void* p = nullptr;
@@ -105,9 +114,9 @@ bool encode2d(CUtensorMap* m, const void* base, int rows, int K, bool bf16) {
             return false;
         fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t str[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)rows};
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t str[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)rows};  // 64 contiguous elements x all rows
     cuuint32_t es[2] = {1, 1};
     return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
               const_cast<void*>(base), dims, str, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -120,19 +129,26 @@ bool encode2d(CUtensorMap* m, const void* base, int rows, int K, bool bf16) {
 extern "C" {
 
 // D[128 x N] = A[128 x K] B[N x K]^T; A, B, D device pointers (16-bit inputs).
-// K in {64, 128}, N in {16 .. 256, multiple of 16}.  Returns 0 on success,
-// -1 for bad arguments, -2 if a bounded wait ran out, else a CUDA error code.
-int msc_probe_tc_gemm(const void* A, const void* B, float* D, int K, int N, int bf16, int use_tma) {
+// K in {64, 128}, N in {16 .. 256, multiple of 16}.  With a_mn (b_mn) the
+// operand is given transposed, [K][128] ([K][N]), and used MN-major (TMA
+// only; N a multiple of 64 for b_mn).  Returns 0 on success, -1 for bad
+// arguments, -2 if a bounded wait ran out, else a CUDA error code.
+int msc_probe_tc_gemm(const void* A, const void* B, float* D, int K, int N, int bf16, int use_tma, int a_mn,
+                      int b_mn) {
     if (!(K == 64 || K == 128) || N < 16 || N > 256 || N % 16) return -1;
+    if ((a_mn || b_mn) && !use_tma) return -1;
+    if (b_mn && N % 64) return -1;
     CUtensorMap ta, tb;
-    if (!encode2d(&ta, A, 128, K, bf16 != 0) || !encode2d(&tb, B, N, K, bf16 != 0)) return -1;
+    const bool ok_a = a_mn ? encode2d(&ta, A, K, 128, bf16 != 0) : encode2d(&ta, A, 128, K, bf16 != 0);
+    const bool ok_b = b_mn ? encode2d(&tb, B, K, N, bf16 != 0) : encode2d(&tb, B, N, K, bf16 != 0);
+    if (!ok_a || !ok_b) return -1;
     const int smem = 1024 + 128 * K * 2 + N * K * 2 + 64;
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
     unsigned int zero = 0;
     cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(zero));
     tc_gemm_kernel<<<1, 128, smem>>>(ta, tb, static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B), D, K,
-                                     N, bf16, use_tma);
+                                     N, bf16, use_tma, a_mn, b_mn);
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return (int)e;
     unsigned int st = 0;
