@@ -12,21 +12,22 @@
 //   S_c[p, n]    = sum_j exp(cs_last - cs_j) Delta_j x_j[p] B_j[n]              (tensor cores)
 //   Hin_{c+1}    = exp(cs_last(c)) Hin_c + S_c                                  (CUDA cores)
 // Four launches: (1) ssd_prep_kernel: Delta and cs; (2) ssd_state_kernel: S_c
-// on tcgen05; (3) ssd_pass_kernel: Hin of every chunk and the final state;
-// (4) ssd_scan_kernel: G = C B^T once per (chunk, row block, head group) into
+// on tcgen05 with the TMA tiles of B and x as MN-major operands; (3)
+// ssd_pass_kernel: Hin of every chunk and the final state; (4)
+// ssd_scan_kernel: G = C B^T once per (chunk, row block, head block) into
 // tensor memory, then per head the masked decay matrix (L . G scaled by Delta)
-// and x are written to shared memory by CUDA cores and Y_diag, Y_off
+// is written to shared memory by CUDA cores, a 64-column quarter at a time
+// while the tensor cores consume the previous quarter, and Y_diag, Y_off
 // accumulate in tensor memory, read back by tcgen05.ld for the epilogue.
 //
-// Precision: G is exact from bf16 C, B with fp32 accumulation.  Every operand
-// the CUDA cores form in fp32 -- the intra-chunk M'[i, j] = G[i, j]
-// exp(cs_i - cs_j) Delta_j, the weighted x of the chunk states and the carried
-// state Hin -- is split into two fp16 terms (hi + lo, ~22 significant bits)
-// and both terms are multiplied on the tensor cores, while C, B and x convert
-// from bf16 to fp16 exactly; every product accumulates in fp32.  A single fp16
-// rounding (11-bit significand) measured up to 6.9e-3 relative error on seeded
-// inputs: Y_diag and Y_off can be large and cancel at chunk boundaries.
-#include <cuda_fp16.h>
+// Precision: C, B and x enter the tensor cores as the bf16 values they are, so
+// G is exact up to fp32 accumulation.  Every operand the CUDA cores form in
+// fp32 -- the intra-chunk M'[i, j] = G[i, j] exp(cs_i - cs_j) Delta_j, the
+// weighted x of the chunk states and the carried state Hin -- is split into two
+// bf16 terms (hi + lo, 16 significant bits) and both terms are multiplied on
+// the tensor cores; every product accumulates in fp32.  A single bf16 rounding
+// of those operands is not enough: Y_diag and Y_off can be large and cancel at
+// chunk boundaries.
 #include <cudaTypedefs.h>
 
 #include <cstdio>
@@ -76,23 +77,12 @@ struct SsdParams {
     float* dt;              // [b, H, Lp]
     float* cs;              // [b, H, Lp]
     float* S;               // [b, nc, H, P, N]
-    uint16_t* Hin;          // [b, nc, H] pairs (hi, lo) of 64 x 128 fp16 K-major SW128 tile images
+    uint16_t* Hin;          // [b, nc, H] pairs (hi, lo) of 64 x 128 bf16 K-major SW128 tile images
     int64_t L, Lp;
-    int H, G, hpg, Q, nc;
+    int batch, H, G, hpg, Q, nc;
 };
 
-// fp32 -> fp16 bit pattern, round to nearest even
-__device__ __forceinline__ uint16_t f2h_bits(float v) {
-    uint16_t r;
-    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(v));
-    return r;
-}
 __device__ __forceinline__ float bf(uint16_t v) { return __uint_as_float(((uint32_t)v) << 16); }
-__device__ __forceinline__ float h2f(uint16_t v) {
-    float r;
-    asm("cvt.f32.f16 %0, %1;" : "=f"(r) : "h"(v));
-    return r;
-}
 
 // ------------------------------------------------------------------ (1) prep
 // One CTA per (chunk, head, batch), one thread per step: Delta and the in-chunk
@@ -126,389 +116,618 @@ __global__ void __launch_bounds__(256) ssd_prep_kernel(const SsdParams p) {
     }
 }
 
+// bf16 pair packing (round to nearest even) and the hi + lo split of a pair
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(a, b);
+    lo = pack_bf16x2(a - msc::bf16lo(hi), b - msc::bf16hi(hi));
+}
+// the same split of a packed fp32 pair, the residual formed by one packed subtract
+__device__ __forceinline__ void split_bf16x2_packed(uint64_t v, uint32_t& hi, uint32_t& lo) {
+    float a, b;
+    msc::upk2(v, a, b);
+    hi = pack_bf16x2(a, b);
+    const uint64_t r = msc::add2(v, msc::pk2(-msc::bf16lo(hi), -msc::bf16hi(hi)));
+    float ra, rb;
+    msc::upk2(r, ra, rb);
+    lo = pack_bf16x2(ra, rb);
+}
+
+// 32-byte streaming store of 8 floats (sm_100+ 256-bit global access); p is
+// 32-byte aligned
+__device__ __forceinline__ void st_cs_v8(float* p, const float* v) {
+    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]),
+                 "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
+
+// cp.async.bulk global -> shared, completion counted on `bar`
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     msc::smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(msc::smem_u32(bar))
+                 : "memory");
+}
+
+constexpr int kHBS = 8;  // heads per CTA of the state kernel
+
 // ------------------------------------------------------ (2) chunk states
-// S_c^T[n, p] = sum_j B_j[n] * (exp(cs_last - cs_j) Delta_j x_j[p]) as a
-// tcgen05 GEMM: M = 128 (n), N = 64 (p), K = Q (j).  A = B^T and B = Xw^T are
-// transposed into K-major SW128 tiles by the CUDA cores.
-__global__ void __launch_bounds__(128) ssd_state_kernel(const SsdParams p) {
+// S_c^T[n, p] = sum_j B_j[n] Xw_j[p], Xw_j = exp(cs_last - cs_j) Delta_j x_j, as
+// a tcgen05 GEMM (M = 128 states, N = 64, K = Q steps) whose operands are the
+// TMA tiles themselves, used MN-major: B [Q j][128 n] as A (two 64-wide n
+// blocks) and x [Q j][64 p], scaled in place by the step weights and split
+// into bf16 hi + lo tiles, as B.  x tiles (with the head's Delta and cs rows)
+// are double-buffered: the load of head h + 1 is issued as soon as the MMAs of
+// head h - 1 have released its buffer, and the epilogue of head h - 1 runs
+// while the MMAs of head h do.
+struct StateSmem {
+    uint8_t* sB;
+    uint8_t* sX;
+    uint8_t* sL;
+    float* s_dc;  // [2 buffers][Delta, cs][256]
+    uint64_t* bars;  // 0: B, 1-2: x buffers, 3-4: MMA of a buffer
+};
+
+__device__ __forceinline__ void state_issue_head(const StateSmem& m, const CUtensorMap* tmX, const SsdParams& p,
+                                                 int h, int s, int c, int b) {
+    const int Q = p.Q;
+    const uint32_t tile = (uint32_t)Q * 128u;
+    const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)c * Q;
+    msc::mbar_arrive_expect_tx(&m.bars[1 + s], tile + 8u * (uint32_t)Q);
+    msc::tma_load_3d(m.sX + s * tile, tmX, &m.bars[1 + s], h * kP, c * Q, b);
+    bulk_g2s(m.s_dc + s * 512, p.dt + dbase, 4u * (uint32_t)Q, &m.bars[1 + s]);
+    bulk_g2s(m.s_dc + s * 512 + 256, p.cs + dbase, 4u * (uint32_t)Q, &m.bars[1 + s]);
+}
+
+__global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ CUtensorMap tmB,
+                                                        const __grid_constant__ CUtensorMap tmX, const SsdParams p) {
     extern __shared__ uint8_t s_dyn[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_dyn) + 1023) & ~uintptr_t(1023));
     const int Q = p.Q;
-    uint8_t* sBt = base;                   // [128 n][Q j] fp16
-    uint8_t* sXw = base + kN * Q * 2;      // [64 p][Q j] fp16, hi term
-    uint8_t* sXl = sXw + kP * Q * 2;       // [64 p][Q j] fp16, lo term
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sXl + kP * Q * 2);
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
-    float* s_w = reinterpret_cast<float*>(slot + 4);  // [Q] weights
+    const uint32_t tile = (uint32_t)Q * 128u;  // bytes of one [Q][64] bf16 tile
+    StateSmem m;
+    m.sB = base;                // 2 tiles (n blocks)
+    m.sX = m.sB + 2 * tile;     // 2 buffers: x, then Xw hi in place
+    m.sL = m.sX + 2 * tile;     // 2 buffers: Xw lo
+    m.s_dc = reinterpret_cast<float*>(m.sL + 2 * tile);
+    m.bars = reinterpret_cast<uint64_t*>(m.s_dc + 1024);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(m.bars + 5);
 
     const int c = blockIdx.x, hb = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h0 = hb * kHB;
+    const int h0 = hb * kHBS;
+    const int nh = min(kHBS, p.H - h0);
     const int g = h0 / p.hpg;
-    const int64_t tc0 = (int64_t)c * Q;
 
     if (warp == 0) {
-        msc::tmem_alloc(slot, 64);
+        msc::tmem_alloc(slot, 128);
         msc::tmem_relinquish();
     }
     if (tid == 0) {
-        msc::mbar_init(bar, 1);
+        for (int k = 0; k < 5; ++k) msc::mbar_init(&m.bars[k], 1);
         msc::fence_barrier_init();
-    }
-    // B^T of this chunk (shared by the group's heads): unit = (j, 8 consecutive n)
-    for (int u = tid; u < Q * (kN / 8); u += 128) {
-        const int j = u >> 4, n0 = (u & 15) * 8;
-        const int64_t t = tc0 + j;
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (t < p.L) raw = __ldg(reinterpret_cast<const uint4*>(p.B + (((int64_t)b * p.L + t) * p.G + g) * kN + n0));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            *reinterpret_cast<uint16_t*>(sBt + msc::sw128_offset(n0 + 2 * e, j, kN)) = f2h_bits(msc::bf16lo(w[e]));
-            *reinterpret_cast<uint16_t*>(sBt + msc::sw128_offset(n0 + 2 * e + 1, j, kN)) = f2h_bits(msc::bf16hi(w[e]));
-        }
+        msc::prefetch_tmap(&tmB);
+        msc::prefetch_tmap(&tmX);
+        msc::mbar_arrive_expect_tx(&m.bars[0], 2 * tile);
+        for (int nb = 0; nb < 2; ++nb) msc::tma_load_3d(m.sB + nb * tile, &tmB, &m.bars[0], g * kN + nb * 64, c * Q, b);
+        for (int it = 0; it < 2 && it < nh; ++it) state_issue_head(m, &tmX, p, h0 + it, it, c, b);
     }
     __syncthreads();
     const uint32_t tmem = *slot;
-    const uint32_t idesc = msc::idesc_f16(false, 128, kP);
-    bool ok = true;
-    const int hend = min(h0 + kHB, p.H);
-    for (int h = h0, it = 0; h < hend; ++h, ++it) {
-        const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
-        const float cs_last = p.cs[dbase + Q - 1];
-        for (int j = tid; j < Q; j += 128) s_w[j] = msc::ex2_approx((cs_last - p.cs[dbase + j]) * MSC_LOG2E) * p.dt[dbase + j];
-        __syncthreads();
-        // Xw^T[p][j] = w_j x_j[p]: unit = (j, 8 consecutive p)
-        for (int u = tid; u < Q * (kP / 8); u += 128) {
-            const int j = u >> 3, p0 = (u & 7) * 8;
-            const int64_t t = tc0 + j;
-            uint4 raw = make_uint4(0, 0, 0, 0);
-            if (t < p.L) raw = __ldg(reinterpret_cast<const uint4*>(p.x + (((int64_t)b * p.L + t) * p.H + h) * kP + p0));
-            const float wj = s_w[j];
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    const uint32_t idesc = msc::idesc_f16(true, 128, kP, true, true);
+    bool ok = wait_phase(&m.bars[0], 0);
+    bool failed = false;
+
+    // S of head hp from accumulator buffer sp: lane = n, column = p; warps w and
+    // w + 4 read lanes 32 (w % 4) .. and split the 64 columns
+    auto epilogue = [&](int hp, int sp) {
+        const int lq = warp & 3, c0 = 32 * (warp >> 2);
+        float* dst = p.S + ((((size_t)b * p.nc + c) * p.H + hp) * kP) * kN + (32 * lq + lane);
+        float v[32];
+        msc::tmem_ld16(tmem + 64 * sp + ((uint32_t)(32 * lq) << 16) + (uint32_t)c0, v);
+        msc::tmem_ld16(tmem + 64 * sp + ((uint32_t)(32 * lq) << 16) + (uint32_t)(c0 + 16), v + 16);
+        msc::tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-#pragma unroll
-                for (int f = 0; f < 2; ++f) {
-                    const float v = wj * (f ? msc::bf16hi(w[e]) : msc::bf16lo(w[e]));
-                    const uint16_t hb = f2h_bits(v);
-                    const uint32_t off = msc::sw128_offset(p0 + 2 * e + f, j, kP);
-                    *reinterpret_cast<uint16_t*>(sXw + off) = hb;
-                    *reinterpret_cast<uint16_t*>(sXl + off) = f2h_bits(v - h2f(hb));
-                }
+        for (int i = 0; i < 32; ++i) __stcs(dst + (size_t)(c0 + i) * kN, v[i]);
+        msc::tc_fence_before();
+    };
+
+    for (int it = 0; it < nh; ++it) {
+        const int s = it & 1;
+        if (it >= 1) {
+            // MMAs of head it - 1 done: its x buffer takes head it + 1
+            ok = wait_phase(&m.bars[3 + (s ^ 1)], (uint32_t)(((it - 1) >> 1) & 1)) && ok;
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) record_timeout(20);
+                failed = true;
+                break;
             }
+            if (tid == 0 && it + 1 < nh) state_issue_head(m, &tmX, p, h0 + it + 1, s ^ 1, c, b);
         }
-        msc::fence_proxy_async_smem();
-        __syncthreads();
-        msc::tc_fence_after();
-        if (tid == 0) {
-            for (int k = 0; k < Q / 16; ++k) {
-                const uint32_t koff = (uint32_t)((k & 3) * 32);
-                const uint64_t ad = msc::sdesc_sw128(msc::smem_u32(sBt + (k >> 2) * kN * 128) + koff);
-                const uint64_t bh = msc::sdesc_sw128(msc::smem_u32(sXw + (k >> 2) * kP * 128) + koff);
-                const uint64_t bl = msc::sdesc_sw128(msc::smem_u32(sXl + (k >> 2) * kP * 128) + koff);
-                msc::mma_f16(tmem, ad, bh, idesc, k > 0 ? 1u : 0u);
-                msc::mma_f16(tmem, ad, bl, idesc, 1u);
-            }
-            msc::mma_commit(bar);
-        }
-        const bool w_ok = wait_phase(bar, (uint32_t)(it & 1));
-        if (__syncthreads_or(!w_ok)) {
-            if (tid == 0) record_timeout(20);
-            ok = false;
+        ok = wait_phase(&m.bars[1 + s], (uint32_t)((it >> 1) & 1)) && ok;
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) record_timeout(21);
+            failed = true;
             break;
         }
-        msc::tc_fence_after();
-        // thread = state n (TMEM lane); 64 columns = p
-        float* dst = p.S + ((((size_t)b * p.nc + c) * p.H + h) * kP) * kN + (32 * warp + lane);
+        // Xw = w_j x_j, split into hi (in place) and lo; row j of the tile is
+        // 128 bytes (64 p), the swizzle only permutes chunks within the row
+        {
+            uint8_t* xs = m.sX + s * tile;
+            uint8_t* ls = m.sL + s * tile;
+            const float* s_dt = m.s_dc + s * 512;
+            const float* s_cs = s_dt + 256;
+            const float cs_last = s_cs[Q - 1];
+            for (int u = tid; u < Q * 8; u += 256) {
+                const int j = u >> 3;
+                const float wj = msc::ex2_approx((cs_last - s_cs[j]) * MSC_LOG2E) * s_dt[j];
+                uint4 v = *reinterpret_cast<const uint4*>(xs + u * 16);
+                uint32_t w[4] = {v.x, v.y, v.z, v.w}, hi[4], lo[4];
+                const uint64_t wj2 = msc::pk2(wj, wj);
 #pragma unroll
-        for (int c16 = 0; c16 < kP; c16 += 16) {
-            float v[16];
-            msc::tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c16, v);
-            msc::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) dst[(size_t)(c16 + i) * kN] = v[i];
-        }
-        msc::tc_fence_before();
-        __syncthreads();
-    }
-    (void)ok;
-    msc::tc_fence_before();
-    __syncthreads();
-    if (warp == 0) msc::tmem_dealloc(tmem, 64);
-}
-
-// ------------------------------------------------------------ (3) state pass
-// One thread per (b, h, p, n): Hin of every chunk (fp16 tile images for the
-// scan kernel's tensor cores) and the final state.
-__global__ void __launch_bounds__(256) ssd_pass_kernel(const SsdParams p) {
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t total = (int64_t)gridDim.y * p.H * kP * kN;  // gridDim.y = batch
-    (void)total;
-    const int b = blockIdx.y;
-    if (idx >= (int64_t)p.H * kP * kN) return;
-    const int n = (int)(idx % kN);
-    const int pp = (int)((idx / kN) % kP);
-    const int h = (int)(idx / (kN * kP));
-    float run = 0.f;
-    const size_t dbase = ((size_t)b * p.H + h) * p.Lp;
-    for (int c = 0; c < p.nc; ++c) {
-        // hi image, then lo image (the rounding residual), 16 KB each
-        uint8_t* tile = reinterpret_cast<uint8_t*>(p.Hin + (((size_t)b * p.nc + c) * p.H + h) * (2 * kP * kN));
-        const uint16_t hb = f2h_bits(run);
-        *reinterpret_cast<uint16_t*>(tile + msc::sw128_offset(pp, n, kP)) = hb;
-        *reinterpret_cast<uint16_t*>(tile + kP * kN * 2 + msc::sw128_offset(pp, n, kP)) = f2h_bits(run - h2f(hb));
-        const float decay = msc::ex2_approx(p.cs[dbase + (size_t)c * p.Q + p.Q - 1] * MSC_LOG2E);
-        run = fmaf(decay, run, p.S[((((size_t)b * p.nc + c) * p.H + h) * kP + pp) * kN + n]);
-    }
-    if (p.final_state) p.final_state[(((size_t)b * p.H + h) * kP + pp) * kN + n] = run;
-}
-
-// ------------------------------------------------------------ (4) chunk scan
-struct ScanMaps {
-    CUtensorMap C, B;
-};
-
-// Releases the block's tensor memory (every thread calls it once, at the end).
-__device__ __forceinline__ void scan_finish(uint32_t tmem, int warp) {
-    msc::tc_fence_before();
-    __syncthreads();
-    if (warp == 0) msc::tmem_dealloc(tmem, 512);
-}
-
-// CTA = (chunk c, row block ib of 128 rows, head block, batch b); 256 threads.
-// Warps w and w + 4 share TMEM lanes 32 (w % 4) .. (rows) and split columns.
-__global__ void __launch_bounds__(256) ssd_scan_kernel(const __grid_constant__ CUtensorMap tmC,
-                                                       const __grid_constant__ CUtensorMap tmB, const SsdParams p) {
-    extern __shared__ uint8_t s_dyn[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_dyn) + 1023) & ~uintptr_t(1023));
-    const int Q = p.Q;
-    const int c = blockIdx.x / ((Q + 127) / 128), ib = blockIdx.x % ((Q + 127) / 128);
-    const int hb = blockIdx.y, b = blockIdx.z;
-    const int Qi = min(Q, (ib + 1) * 128);      // columns j of this row block: [0, Qi)
-    const int rows_valid = min(128, Q - ib * 128);
-    uint8_t* sC = base;                          // [128 i][128 n]  (2 x 16 KB)
-    uint8_t* sBM = sC + 32768;                   // B [Q j][128 n] for G, then M'_hi [128 i][Qi j]
-    uint8_t* sML = sBM + 65536;                  // M'_lo [128 i][Qi j]
-    uint8_t* sXd = sML + 65536;                  // x [64 p][Qi j] fp16
-    uint8_t* sH = sXd + 32768;                   // Hin [64 p][128 n] fp16: hi tile, then lo tile
-    float* s_w = reinterpret_cast<float*>(sH + 32768);  // log2(Delta_j) - cs_j log2(e)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_w + 256);  // 0: loads, 1: G, 2: Hin, 3: head MMAs
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 4);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int i_loc = 32 * quarter + lane;        // row of this thread within the block
-    const int i_chk = ib * 128 + i_loc;           // row within the chunk
-    const int h0 = hb * kHB;
-    const int g = h0 / p.hpg;
-    const int64_t tc0 = (int64_t)c * Q;
-    const uint32_t tG = 0, tYd = 256, tYo = 320;
-
-    if (warp == 0) {
-        msc::tmem_alloc(slot, 512);
-        msc::tmem_relinquish();
-    }
-    if (tid == 0) {
-        for (int k = 0; k < 4; ++k) msc::mbar_init(&bars[k], 1);
-        msc::fence_barrier_init();
-        msc::prefetch_tmap(&tmC);
-        msc::prefetch_tmap(&tmB);
-        // C rows of this block and B rows [0, Qi) of the chunk, 128-byte swizzled, K = n in 2 blocks
-        // (the B box is Q rows: the G GEMM of this block uses its first Qi)
-        const uint32_t bytes = 2u * 128u * 128u + 2u * (uint32_t)Q * 128u;
-        msc::mbar_arrive_expect_tx(&bars[0], bytes);
-        for (int kb = 0; kb < 2; ++kb) {
-            msc::tma_load_3d(sC + kb * 16384, &tmC, &bars[0], g * kN + kb * 64, (int)(tc0 + ib * 128), b);
-            msc::tma_load_3d(sBM + kb * Q * 128, &tmB, &bars[0], g * kN + kb * 64, (int)tc0, b);
-        }
-    }
-    __syncthreads();
-    const uint32_t tmem = *slot;
-    bool ok = wait_phase(&bars[0], 0);
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) record_timeout(40);
-        scan_finish(tmem, warp);
-        return;
-    }
-    msc::tc_fence_after();
-    // G = C B^T (M = 128, N = Qi, K = 128), bf16 operands
-    if (tid == 0) {
-        const uint32_t idesc = msc::idesc_f16(true, 128, Qi);
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t koff = (uint32_t)((k & 3) * 32);
-            const uint64_t ad = msc::sdesc_sw128(msc::smem_u32(sC + (k >> 2) * 16384) + koff);
-            const uint64_t bd = msc::sdesc_sw128(msc::smem_u32(sBM + (k >> 2) * Q * 128) + koff);
-            msc::mma_f16(tmem + tG, ad, bd, idesc, k > 0 ? 1u : 0u);
-        }
-        msc::mma_commit(&bars[1]);
-    }
-    ok = wait_phase(&bars[1], 0);
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) record_timeout(41);
-        scan_finish(tmem, warp);
-        return;
-    }
-    msc::tc_fence_after();
-    // C tile bf16 -> fp16 in place (the swizzle is a pure permutation of 2-byte slots)
-    for (int u = tid; u < 128 * 128 / 8; u += 256) {
-        uint4* q = reinterpret_cast<uint4*>(sC) + u;
-        uint4 v = *q;
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) w[e] = msc::pack_half2(msc::bf16lo(w[e]), msc::bf16hi(w[e]));
-        *q = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-
-    {
-        const int hend = min(h0 + kHB, p.H);
-        for (int h = h0, it = 0; h < hend; ++h, ++it) {
-            const uint32_t par = (uint32_t)(it & 1);
-            if (tid == 0) {
-                msc::mbar_arrive_expect_tx(&bars[2], 32768u);
-                const uint16_t* src = p.Hin + (((size_t)b * p.nc + c) * p.H + h) * (2 * kP * kN);
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                        msc::smem_u32(sH)),
-                    "l"(src), "r"(32768), "r"(msc::smem_u32(&bars[2]))
-                    : "memory");
-            }
-            const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
-            for (int j = tid; j < Qi; j += 256) {
-                const float dtj = p.dt[dbase + j];
-                s_w[j] = (dtj > 0.f ? __log2f(dtj) : -INFINITY) - p.cs[dbase + j] * MSC_LOG2E;
-            }
-            const float cs_i = p.cs[dbase + (i_chk < Qi ? i_chk : 0)];
-            // x of the chunk, transposed to [p][j] fp16 (exact): unit = (j, 8 consecutive p)
-            for (int u = tid; u < Qi * 8; u += 256) {
-                const int j = u >> 3, p0 = (u & 7) * 8;
-                const int64_t t = tc0 + j;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (t < p.L) v = __ldg(reinterpret_cast<const uint4*>(p.x + (((int64_t)b * p.L + t) * p.H + h) * kP + p0));
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    *reinterpret_cast<uint16_t*>(sXd + msc::sw128_offset(p0 + 2 * e, j, kP)) = f2h_bits(msc::bf16lo(w[e]));
-                    *reinterpret_cast<uint16_t*>(sXd + msc::sw128_offset(p0 + 2 * e + 1, j, kP)) = f2h_bits(msc::bf16hi(w[e]));
-                }
-            }
-            __syncthreads();  // s_w complete
-            // M'[i][j] = G[i][j] exp(cs_i - cs_j) Delta_j for j <= i, else 0, as fp16 hi + lo;
-            // this thread: row i_loc, columns [half * Qi / 2, (half + 1) * Qi / 2)
-            {
-                const float csi = cs_i * MSC_LOG2E;
-                const int j0 = half * (Qi / 2), j1 = j0 + Qi / 2;
-                for (int jc = j0; jc < j1; jc += 16) {
-                    float gv[16];
-                    msc::tmem_ld16(tmem + tG + ((uint32_t)(32 * quarter) << 16) + (uint32_t)jc, gv);
-                    msc::tmem_ld_wait();
-                    uint32_t ph[8], pl[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int ja = jc + 2 * e, jb = ja + 1;
-                        const float va = (ja <= i_chk) ? gv[2 * e] * msc::ex2_approx(csi + s_w[ja]) : 0.f;
-                        const float vb = (jb <= i_chk) ? gv[2 * e + 1] * msc::ex2_approx(csi + s_w[jb]) : 0.f;
-                        ph[e] = msc::pack_half2(va, vb);
-                        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&ph[e]));
-                        pl[e] = msc::pack_half2(va - hf.x, vb - hf.y);
-                    }
-                    const uint32_t o0 = msc::sw128_offset(i_loc, jc, 128), o1 = msc::sw128_offset(i_loc, jc + 8, 128);
-                    *reinterpret_cast<uint4*>(sBM + o0) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                    *reinterpret_cast<uint4*>(sBM + o1) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
-                    *reinterpret_cast<uint4*>(sML + o0) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-                    *reinterpret_cast<uint4*>(sML + o1) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
-                }
-            }
-            ok = wait_phase(&bars[2], par);
-            if (__syncthreads_or(!ok)) {
-                if (tid == 0) record_timeout(42);
-                break;
+                for (int e = 0; e < 4; ++e)
+                    split_bf16x2_packed(msc::mul2(wj2, msc::pk2(msc::bf16lo(w[e]), msc::bf16hi(w[e]))), hi[e], lo[e]);
+                *reinterpret_cast<uint4*>(xs + u * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(ls + u * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
             msc::fence_proxy_async_smem();
             msc::tc_fence_before();
             __syncthreads();
             msc::tc_fence_after();
             if (tid == 0) {
-                const uint32_t id64 = msc::idesc_f16(false, 128, kP);
-                for (int k = 0; k < Qi / 16; ++k) {
-                    const uint32_t koff = (uint32_t)((k & 3) * 32);
-                    const uint64_t bd = msc::sdesc_sw128(msc::smem_u32(sXd + (k >> 2) * kP * 128) + koff);
-                    const uint64_t adh = msc::sdesc_sw128(msc::smem_u32(sBM + (k >> 2) * 16384) + koff);
-                    const uint64_t adl = msc::sdesc_sw128(msc::smem_u32(sML + (k >> 2) * 16384) + koff);
-                    msc::mma_f16(tmem + tYd, adh, bd, id64, k > 0 ? 1u : 0u);
-                    msc::mma_f16(tmem + tYd, adl, bd, id64, 1u);
+                const uint32_t aB = msc::smem_u32(m.sB), aX = msc::smem_u32(xs), aL = msc::smem_u32(ls);
+                for (int k = 0; k < Q / 16; ++k) {
+                    const uint64_t ad = msc::sdesc_sw128_mn(aB + k * 2048, tile);
+                    msc::mma_f16(tmem + 64 * s, ad, msc::sdesc_sw128_mn(aX + k * 2048, tile), idesc, k > 0 ? 1u : 0u);
+                    msc::mma_f16(tmem + 64 * s, ad, msc::sdesc_sw128_mn(aL + k * 2048, tile), idesc, 1u);
                 }
-                for (int k = 0; k < kN / 16; ++k) {
-                    const uint32_t koff = (uint32_t)((k & 3) * 32);
-                    const uint64_t ad = msc::sdesc_sw128(msc::smem_u32(sC + (k >> 2) * 16384) + koff);
-                    const uint64_t bh = msc::sdesc_sw128(msc::smem_u32(sH + (k >> 2) * kP * 128) + koff);
-                    const uint64_t bl = msc::sdesc_sw128(msc::smem_u32(sH + 16384 + (k >> 2) * kP * 128) + koff);
-                    msc::mma_f16(tmem + tYo, ad, bh, id64, k > 0 ? 1u : 0u);
-                    msc::mma_f16(tmem + tYo, ad, bl, id64, 1u);
-                }
-                msc::mma_commit(&bars[3]);
+                msc::mma_commit(&m.bars[3 + s]);
             }
-            ok = wait_phase(&bars[3], par);
-            if (__syncthreads_or(!ok)) {
-                if (tid == 0) record_timeout(43);
-                break;
-            }
+        }
+        if (it >= 1) epilogue(h0 + it - 1, s ^ 1);  // its MMAs were waited for above
+    }
+    if (!failed && nh > 0) {
+        const int it = nh - 1;
+        ok = wait_phase(&m.bars[3 + (it & 1)], (uint32_t)((it >> 1) & 1));
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) record_timeout(22);
+        } else {
             msc::tc_fence_after();
-            // epilogue: row i_loc, columns p in [32 half, 32 half + 32)
-            {
-                const int64_t t = tc0 + i_chk;
-                const bool store = (i_loc < rows_valid) && (t < p.L);
-                const float e_i = msc::ex2_approx(cs_i * MSC_LOG2E);
-                const float Dh = p.D ? p.D[h] : 0.f;
-                float* yrow = p.y + (((int64_t)b * p.L + t) * p.H + h) * kP;
-                const uint16_t* zrow = p.z ? p.z + (((int64_t)b * p.L + t) * p.H + h) * kP : nullptr;
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int pc = 32 * half + 16 * cc;
-                    float yd[16], yo[16];
-                    msc::tmem_ld16(tmem + tYd + ((uint32_t)(32 * quarter) << 16) + (uint32_t)pc, yd);
-                    msc::tmem_ld16(tmem + tYo + ((uint32_t)(32 * quarter) << 16) + (uint32_t)pc, yo);
-                    msc::tmem_ld_wait();
-                    if (store) {
-                        const uint16_t* xrow = p.x + (((int64_t)b * p.L + t) * p.H + h) * kP;
-                        const uint4 xv0 = __ldg(reinterpret_cast<const uint4*>(xrow + pc));
-                        const uint4 xv1 = __ldg(reinterpret_cast<const uint4*>(xrow + pc + 8));
-                        const uint32_t xw[8] = {xv0.x, xv0.y, xv0.z, xv0.w, xv1.x, xv1.y, xv1.z, xv1.w};
-                        float out[16];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            out[2 * e] = fmaf(e_i, yo[2 * e], yd[2 * e]) + Dh * msc::bf16lo(xw[e]);
-                            out[2 * e + 1] = fmaf(e_i, yo[2 * e + 1], yd[2 * e + 1]) + Dh * msc::bf16hi(xw[e]);
-                        }
-                        if (zrow) {
-                            const uint4 zv0 = __ldg(reinterpret_cast<const uint4*>(zrow + pc));
-                            const uint4 zv1 = __ldg(reinterpret_cast<const uint4*>(zrow + pc + 8));
-                            const uint32_t zw[8] = {zv0.x, zv0.y, zv0.z, zv0.w, zv1.x, zv1.y, zv1.z, zv1.w};
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                out[2 * e] *= msc::silu_f(msc::bf16lo(zw[e]));
-                                out[2 * e + 1] *= msc::silu_f(msc::bf16hi(zw[e]));
-                            }
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            __stcs(reinterpret_cast<float4*>(yrow + pc) + e,
-                                   make_float4(out[4 * e], out[4 * e + 1], out[4 * e + 2], out[4 * e + 3]));
-                    }
-                }
-            }
-            msc::tc_fence_before();
-            __syncthreads();
+            epilogue(h0 + it, it & 1);
         }
     }
-    scan_finish(tmem, warp);
+    msc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) msc::tmem_dealloc(tmem, 128);
+}
+
+// ------------------------------------------------------------ (3) state pass
+// One thread per (b, h, p, 8 consecutive n): Hin of every chunk as bf16 hi + lo
+// tile images (K-major [64 p][128 n], 128-byte swizzle: one 16-byte chunk per
+// thread and chunk) for the scan kernel's tensor cores, and the final state.
+// The chunk states are loaded eight chunks ahead of the dependent chain.
+__global__ void __launch_bounds__(256) ssd_pass_kernel(const SsdParams p) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int b = blockIdx.y;
+    constexpr int kN8 = kN / 8;
+    if (idx >= (int64_t)p.H * kP * kN8) return;
+    const int n0 = (int)(idx % kN8) * 8;
+    const int pp = (int)((idx / kN8) % kP);
+    const int h = (int)(idx / (kN8 * kP));
+    const size_t dbase = ((size_t)b * p.H + h) * p.Lp;
+    const uint32_t off = msc::sw128_offset(pp, n0, kP);
+    float run[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) run[e] = 0.f;
+    for (int c0 = 0; c0 < p.nc; c0 += 8) {
+        float4 sv[8][2];
+        float dv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int c = c0 + k;
+            if (c < p.nc) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    p.S + ((((size_t)b * p.nc + c) * p.H + h) * kP + pp) * kN + n0);
+                sv[k][0] = __ldcs(src);
+                sv[k][1] = __ldcs(src + 1);
+                dv[k] = p.cs[dbase + (size_t)c * p.Q + p.Q - 1];
+            } else {
+                sv[k][0] = sv[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                dv[k] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int c = c0 + k;
+            if (c >= p.nc) break;
+            uint8_t* tile = reinterpret_cast<uint8_t*>(p.Hin + (((size_t)b * p.nc + c) * p.H + h) * (2 * kP * kN));
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_bf16x2(run[2 * e], run[2 * e + 1], hi[e], lo[e]);
+            *reinterpret_cast<uint4*>(tile + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(tile + kP * kN * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            const float a = msc::ex2_approx(dv[k] * MSC_LOG2E);
+            const float s8[8] = {sv[k][0].x, sv[k][0].y, sv[k][0].z, sv[k][0].w,
+                                 sv[k][1].x, sv[k][1].y, sv[k][1].z, sv[k][1].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) run[e] = fmaf(a, run[e], s8[e]);
+        }
+    }
+    if (p.final_state) {
+        float4* dst = reinterpret_cast<float4*>(p.final_state + (((size_t)b * p.H + h) * kP + pp) * kN + n0);
+        dst[0] = make_float4(run[0], run[1], run[2], run[3]);
+        dst[1] = make_float4(run[4], run[5], run[6], run[7]);
+    }
+}
+
+// ------------------------------------------------------------ (4) chunk scan
+struct ScanMaps {
+    CUtensorMap C, B, xs, xq;
+};
+
+constexpr int kScanCompute = 16;                       // warps forming M' and running the epilogue
+constexpr int kWarpLoad = kScanCompute;                // warp streaming x, Delta, cs and Hin
+constexpr int kWarpMma = kScanCompute + 1;             // warp issuing the tensor-core MMAs
+constexpr int kScanThreads = (kScanCompute + 2) * 32;
+
+// Bounded wait that also gives up as soon as another role of the block has
+// set *abort (so that one timeout does not cascade into many).
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const volatile uint32_t* abort) {
+    if (msc::mbar_wait(bar, parity, 256)) return true;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    while (true) {
+        if (msc::mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        uint64_t t1;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+        if (t1 - t0 > 1000000000ull) return false;
+    }
+}
+
+// CTA = (chunk c, row block ib of 128 rows, block of kHB heads, batch b), in
+// three roles that hand work over through mbarriers:
+//  * load warp: streams, one head ahead, the x tile with the head's Delta and
+//    cs rows (double-buffered) and the Hin hi + lo images (reloaded as soon as
+//    the head's Y_off MMAs have read them);
+//  * MMA warp: G = C B^T once (bf16 K-major TMA tiles, into tensor memory),
+//    then per head Y_off = C Hin^T and Y_diag = M' x, one 64-column quarter of
+//    M' at a time, into one of two accumulator pairs;
+//  * 16 compute warps: warp w owns rows 32 (w % 4) + lane (its TMEM lanes) and
+//    16 columns of every quarter.  They form M'[i, j] = G[i, j] exp(cs_i -
+//    cs_j) Delta_j for j <= i, plus D on the diagonal so that D x_i comes out
+//    of the same product, split into bf16 hi + lo, into two alternating
+//    quarter buffers; blocks above the diagonal are written as zeros without
+//    arithmetic.  The epilogue of head h (y = Y_diag + exp(cs_i) Y_off, times
+//    silu(z)) runs after the quarters of head h + 1 have been handed over, so
+//    the tensor cores are never waited for.
+__global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_constant__ CUtensorMap tmC,
+                                                                   const __grid_constant__ CUtensorMap tmB,
+                                                                   const __grid_constant__ CUtensorMap tmX,
+                                                                   const SsdParams p) {
+    extern __shared__ uint8_t s_dyn[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_dyn) + 1023) & ~uintptr_t(1023));
+    const int Q = p.Q;
+    const int nib = (Q + 127) / 128;
+    const int c = blockIdx.x / nib, ib = blockIdx.x % nib;
+    const int hb = blockIdx.y, b = blockIdx.z;
+    const int Qi = min(Q, (ib + 1) * 128);       // columns j of this row block: [0, Qi)
+    const int rows_valid = min(128, Q - ib * 128);
+    const int xrows = min(Q, 128);               // rows of one x box
+    const int nq = Qi / 64;
+    uint8_t* sC = base;                          // [2 kb][128 i][128 B], K-major
+    uint8_t* sBM = sC + 32768;                   // B [2 kb][Q j][128 B] for G, then 2 x (hi, lo) quarter buffers
+    uint8_t* sX = sBM + 65536;                   // 2 x: x [Qi j][64 p], MN-major
+    uint8_t* sH = sX + 65536;                    // Hin hi [2 kb][64 p][128 B], then lo
+    float* s_dc = reinterpret_cast<float*>(sH + 32768);  // [2 buffers][Delta, cs][256]
+    float* s_w = s_dc + 1024;                    // per compute warp: log2(Delta_j) - cs_j log2(e), 64 columns
+    float* s_D = s_w + kScanCompute * 64;        // D of the block's heads
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_D + 64);
+    // 0 C+B loaded, 1 G done, 2-3 x full, 4 Hin full, 5 Y_off done, 6-7 quarter built (16 arrivals),
+    // 8-9 quarter consumed, 10-11 x free, 12-13 head done, 14-15 accumulator free (16 arrivals), 16 drain
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 17);
+    volatile uint32_t* abort = slot + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h0 = hb * kHB;
+    const int nh = min(kHB, p.H - h0);
+    const int g = h0 / p.hpg;
+    const int64_t tc0 = (int64_t)c * Q;
+    const uint32_t tG = 0;
+    const uint32_t xbytes = (uint32_t)Qi * 128u;
+
+    if (warp == 0) {
+        msc::tmem_alloc(slot, 512);
+        msc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int k = 0; k < 17; ++k) msc::mbar_init(&bars[k], (k == 6 || k == 7 || k == 14 || k == 15) ? kScanCompute : 1);
+        msc::fence_barrier_init();
+        *abort = 0u;
+    }
+    if (tid < kHB) s_D[tid] = (p.D && tid < nh) ? p.D[h0 + tid] : 0.f;
+    __syncthreads();
+    const uint32_t tmem = *slot;
+
+    if (warp == kWarpLoad) {
+        // ---------------------------------------------------------- loads
+        if (lane == 0) {
+            msc::prefetch_tmap(&tmC);
+            msc::prefetch_tmap(&tmB);
+            msc::prefetch_tmap(&tmX);
+            msc::mbar_arrive_expect_tx(&bars[0], 2u * 128u * 128u + 2u * (uint32_t)Q * 128u);
+            for (int kb = 0; kb < 2; ++kb) {
+                msc::tma_load_3d(sC + kb * 16384, &tmC, &bars[0], g * kN + kb * 64, (int)(tc0 + ib * 128), b);
+                msc::tma_load_3d(sBM + kb * Q * 128, &tmB, &bars[0], g * kN + kb * 64, (int)tc0, b);
+            }
+        }
+        bool pok = true;
+        int nx0 = 0, nx1 = 0, nhin = 0;
+        for (int it = 0; it < nh; ++it) {
+            const int s = it & 1, h = h0 + it;
+            if (it >= 2) {
+                pok = __all_sync(0xffffffffu, wait_or_abort(&bars[10 + s], (uint32_t)(((it - 2) >> 1) & 1), abort));
+                if (!pok) break;
+            }
+            if (lane == 0) {
+                const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
+                msc::mbar_arrive_expect_tx(&bars[2 + s], xbytes + 8u * (uint32_t)Qi);
+                for (int r = 0; r < Qi; r += xrows)
+                    msc::tma_load_3d(sX + s * 32768 + r * 128, &tmX, &bars[2 + s], h * kP, (int)(tc0 + r), b);
+                bulk_g2s(s_dc + s * 512, p.dt + dbase, 4u * (uint32_t)Qi, &bars[2 + s]);
+                bulk_g2s(s_dc + s * 512 + 256, p.cs + dbase, 4u * (uint32_t)Qi, &bars[2 + s]);
+            }
+            if (s == 0) ++nx0; else ++nx1;
+            if (it >= 1) {
+                pok = __all_sync(0xffffffffu, wait_or_abort(&bars[5], (uint32_t)((it - 1) & 1), abort));
+                if (!pok) break;
+            }
+            if (lane == 0) {
+                msc::mbar_arrive_expect_tx(&bars[4], 32768u);
+                bulk_g2s(sH, p.Hin + (((size_t)b * p.nc + c) * p.H + h) * (2 * kP * kN), 32768u, &bars[4]);
+            }
+            ++nhin;
+        }
+        if (!pok && lane == 0) {
+            record_timeout(50);
+            *abort = 1u;
+        }
+        // every load issued lands before the block ends (they have all been
+        // consumed already unless the block gives up)
+        bool dok = true;
+        if (nx0 > 0) dok = wait_phase(&bars[2], (uint32_t)((nx0 - 1) & 1)) && dok;
+        if (nx1 > 0) dok = wait_phase(&bars[3], (uint32_t)((nx1 - 1) & 1)) && dok;
+        if (nhin > 0) dok = wait_phase(&bars[4], (uint32_t)((nhin - 1) & 1)) && dok;
+        if (!dok && lane == 0) record_timeout(51);
+    } else if (warp == kWarpMma) {
+        // ---------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            const uint32_t id64 = msc::idesc_f16(true, 128, kP);                // A, B K-major
+            const uint32_t id64x = msc::idesc_f16(true, 128, kP, false, true);  // B MN-major (x)
+            bool mok = wait_or_abort(&bars[0], 0, abort);
+            if (mok) {
+                msc::tc_fence_after();
+                const uint32_t idesc = msc::idesc_f16(true, 128, Qi);
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t koff = (uint32_t)((k & 3) * 32);
+                    const uint64_t ad = msc::sdesc_sw128(msc::smem_u32(sC + (k >> 2) * 16384) + koff);
+                    const uint64_t bd = msc::sdesc_sw128(msc::smem_u32(sBM + (k >> 2) * Q * 128) + koff);
+                    msc::mma_f16(tmem + tG, ad, bd, idesc, k > 0 ? 1u : 0u);
+                }
+                msc::mma_commit(&bars[1]);
+            }
+            for (int it = 0; it < nh && mok; ++it) {
+                const int s = it & 1;
+                const uint32_t tYd = 256u + 128u * (uint32_t)s, tYo = tYd + 64u;
+                mok = wait_or_abort(&bars[2 + s], (uint32_t)((it >> 1) & 1), abort) &&
+                      wait_or_abort(&bars[4], (uint32_t)(it & 1), abort);
+                if (mok && it >= 2) mok = wait_or_abort(&bars[14 + s], (uint32_t)(((it - 2) >> 1) & 1), abort);
+                if (!mok) break;
+                msc::tc_fence_after();
+                const uint32_t aC = msc::smem_u32(sC), aH = msc::smem_u32(sH);
+                for (int k = 0; k < kN / 16; ++k) {
+                    const uint32_t koff = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
+                    const uint32_t hoff = (uint32_t)((k >> 2) * kP * 128 + (k & 3) * 32);
+                    msc::mma_f16(tmem + tYo, msc::sdesc_sw128(aC + koff), msc::sdesc_sw128(aH + hoff), id64,
+                                 k > 0 ? 1u : 0u);
+                    msc::mma_f16(tmem + tYo, msc::sdesc_sw128(aC + koff), msc::sdesc_sw128(aH + 16384 + hoff), id64, 1u);
+                }
+                msc::mma_commit(&bars[5]);
+                const uint32_t aX = msc::smem_u32(sX + s * 32768);
+                for (int q = 0; q < nq; ++q) {
+                    const int u = it * nq + q, bq = u & 1;
+                    mok = wait_or_abort(&bars[6 + bq], (uint32_t)((u >> 1) & 1), abort);
+                    if (!mok) break;
+                    msc::tc_fence_after();
+                    const uint32_t aHi = msc::smem_u32(sBM + bq * 32768), aLo = aHi + 16384u;
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t bd = msc::sdesc_sw128_mn(aX + (uint32_t)(64 * q + 16 * k) * 128u, 32768u);
+                        msc::mma_f16(tmem + tYd, msc::sdesc_sw128(aHi + k * 32), bd, id64x, (q > 0 || k > 0) ? 1u : 0u);
+                        msc::mma_f16(tmem + tYd, msc::sdesc_sw128(aLo + k * 32), bd, id64x, 1u);
+                    }
+                    msc::mma_commit(&bars[8 + bq]);
+                }
+                if (!mok) break;
+                msc::mma_commit(&bars[10 + s]);
+                msc::mma_commit(&bars[12 + s]);
+            }
+            if (!mok) {
+                record_timeout(46);
+                *abort = 1u;
+            }
+            // every MMA issued completes before the tensor memory is released
+            msc::mma_commit(&bars[16]);
+            if (!wait_phase(&bars[16], 0)) record_timeout(47);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ M' quarters and epilogue
+        const int lq = warp & 3, cslot = warp >> 2;
+        const int i_loc = 32 * lq + lane;
+        const int i_chk = ib * 128 + i_loc;
+        const int row_lo = ib * 128 + 32 * lq;     // first row of this warp
+        const uint32_t lane_off = (uint32_t)(32 * lq) << 16;
+        float* my_w = s_w + warp * 64;
+        bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[1], 0, abort));
+        msc::tc_fence_after();
+        float csi_prev = 0.f;
+        uint4 z_prev[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        // y of head hp (row scale csi_prev, gate z_prev); `release` hands the
+        // accumulator pair back to the MMA warp once it has been read
+        auto epilogue = [&](int hp, bool release) -> bool {
+            const int sp = hp & 1;
+            if (!__all_sync(0xffffffffu, wait_or_abort(&bars[12 + sp], (uint32_t)((hp >> 1) & 1), abort)))
+                return false;
+            msc::tc_fence_after();
+            float yd[16], yo[16];
+            const uint32_t tYd = 256u + 128u * (uint32_t)sp;
+            msc::tmem_ld16(tmem + tYd + lane_off + (uint32_t)(16 * cslot), yd);
+            msc::tmem_ld16(tmem + tYd + 64u + lane_off + (uint32_t)(16 * cslot), yo);
+            msc::tmem_ld_wait();
+            msc::tc_fence_before();
+            __syncwarp();
+            if (release && lane == 0) msc::mbar_arrive(&bars[14 + sp]);
+            const int64_t t = tc0 + i_chk;
+            if (i_loc < rows_valid && t < p.L) {
+                const float e_i = msc::ex2_approx(csi_prev);
+                float out[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) out[e] = fmaf(e_i, yo[e], yd[e]);
+                if (p.z) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint32_t zw[4] = {z_prev[e].x, z_prev[e].y, z_prev[e].z, z_prev[e].w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            out[8 * e + 2 * k] *= msc::silu_f(msc::bf16lo(zw[k]));
+                            out[8 * e + 2 * k + 1] *= msc::silu_f(msc::bf16hi(zw[k]));
+                        }
+                    }
+                }
+                float* yrow = p.y + (((int64_t)b * p.L + t) * p.H + h0 + hp) * kP + 16 * cslot;
+                st_cs_v8(yrow, out);
+                st_cs_v8(yrow + 8, out + 8);
+            }
+            return true;
+        };
+        for (int it = 0; it <= nh && ok; ++it) {
+            if (it < nh) {
+                const int s = it & 1;
+                ok = __all_sync(0xffffffffu, wait_or_abort(&bars[2 + s], (uint32_t)((it >> 1) & 1), abort));
+                if (!ok) break;
+                const float* s_dt = s_dc + s * 512;
+                const float* s_cs = s_dt + 256;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int idx = lane + 32 * r;
+                    const int j = 64 * (idx >> 4) + 16 * cslot + (idx & 15);
+                    float wv = 0.f;
+                    if (j < Qi) {
+                        const float dtj = s_dt[j];
+                        wv = (dtj > 0.f ? __log2f(dtj) : -INFINITY) - s_cs[j] * MSC_LOG2E;
+                    }
+                    my_w[idx] = wv;
+                }
+                const float csi = s_cs[i_chk < Qi ? i_chk : 0] * MSC_LOG2E;
+                const float Dh = s_D[it];
+                __syncwarp();
+                for (int q = 0; q < nq; ++q) {
+                    // quarter u alternates between buffers u % 2; before refilling
+                    // one, wait for the MMAs of its previous use (u - 2)
+                    const int u = it * nq + q, bq = u & 1;
+                    if (u >= 2) {
+                        ok = __all_sync(0xffffffffu,
+                                        wait_or_abort(&bars[8 + bq], (uint32_t)(((u >> 1) - 1) & 1), abort));
+                        if (!ok) break;
+                    }
+                    const int j0 = 64 * q + 16 * cslot;
+                    uint32_t ph[8], pl[8];
+                    if (j0 > row_lo + 31 || row_lo >= Qi) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ph[e] = pl[e] = 0u;
+                    } else {
+                        float gv[16];
+                        msc::tmem_ld16(tmem + tG + lane_off + (uint32_t)j0, gv);
+                        float wv[16];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 w4 = reinterpret_cast<const float4*>(my_w + 16 * q)[e];
+                            wv[4 * e] = w4.x; wv[4 * e + 1] = w4.y; wv[4 * e + 2] = w4.z; wv[4 * e + 3] = w4.w;
+                        }
+                        msc::tmem_ld_wait();
+                        if (j0 + 15 <= row_lo) {
+                            // every column at or below every row of the warp: packed
+                            // pair arithmetic, no masks
+                            const uint64_t csi2 = msc::pk2(csi, csi);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const uint64_t v = msc::mul2(msc::ex2_2(msc::add2(csi2, msc::pk2(wv[2 * e], wv[2 * e + 1]))),
+                                                             msc::pk2(gv[2 * e], gv[2 * e + 1]));
+                                split_bf16x2_packed(v, ph[e], pl[e]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int ja = j0 + 2 * e, jb = ja + 1;
+                                float va = (ja <= i_chk) ? gv[2 * e] * msc::ex2_approx(csi + wv[2 * e]) : 0.f;
+                                float vb = (jb <= i_chk) ? gv[2 * e + 1] * msc::ex2_approx(csi + wv[2 * e + 1]) : 0.f;
+                                if (ja == i_chk) va += Dh;
+                                if (jb == i_chk) vb += Dh;
+                                split_bf16x2(va, vb, ph[e], pl[e]);
+                            }
+                        }
+                    }
+                    uint8_t* bh = sBM + bq * 32768;
+                    const uint32_t o0 = msc::sw128_offset(i_loc, 16 * cslot, 128);
+                    const uint32_t o1 = msc::sw128_offset(i_loc, 16 * cslot + 8, 128);
+                    *reinterpret_cast<uint4*>(bh + o0) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                    *reinterpret_cast<uint4*>(bh + o1) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+                    *reinterpret_cast<uint4*>(bh + 16384 + o0) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+                    *reinterpret_cast<uint4*>(bh + 16384 + o1) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+                    msc::fence_proxy_async_smem();
+                    msc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) msc::mbar_arrive(&bars[6 + bq]);
+                }
+                if (!ok) break;
+                // epilogue of head it - 1, then keep this head's row scale and gate
+                if (it >= 1) {
+                    ok = epilogue(it - 1, true);
+                    if (!ok) break;
+                }
+                csi_prev = csi;
+                {
+                    const int64_t t = tc0 + i_chk;
+                    if (p.z && i_loc < rows_valid && t < p.L) {
+                        const uint4* zrow = reinterpret_cast<const uint4*>(
+                            p.z + (((int64_t)b * p.L + t) * p.H + h0 + it) * kP + 16 * cslot);
+                        z_prev[0] = __ldcs(zrow);
+                        z_prev[1] = __ldcs(zrow + 1);
+                    }
+                }
+            } else {
+                ok = epilogue(nh - 1, false);  // the last head
+            }
+        }
+        if (!ok && lane == 0) {
+            record_timeout(42);
+            *abort = 1u;
+        }
+    }
+    msc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) msc::tmem_dealloc(tmem, 512);
 }
 
 size_t a256(size_t x) { return (x + 255) / 256 * 256; }
 
-constexpr int kScanSmem = 1024 + 32768 + 65536 + 65536 + 32768 + 32768 + 1024 + 64;
+constexpr int kScanSmem = 1024 + 32768 + 65536 + 65536 + 32768 + 4096 + 4096 + 256 + 17 * 8 + 8;
 
-int state_smem(int Q) { return 1024 + kN * Q * 2 + 2 * kP * Q * 2 + 64 + Q * 4; }
+int state_smem(int Q) { return 1024 + 6 * Q * 128 + 4096 + 64; }
 
 }  // namespace
 
@@ -531,7 +750,7 @@ msc_status ssd_launch(const SsdArgs& a, cudaStream_t st) {
     p.C = static_cast<const uint16_t*>(a.C);
     p.z = static_cast<const uint16_t*>(a.z);
     p.A = a.A; p.D = a.D; p.bias = a.delta_bias; p.y = a.y; p.final_state = a.final_state;
-    p.L = a.L; p.H = (int)a.H; p.G = (int)a.G; p.hpg = (int)(a.H / a.G); p.Q = (int)a.Q;
+    p.L = a.L; p.batch = (int)a.batch; p.H = (int)a.H; p.G = (int)a.G; p.hpg = (int)(a.H / a.G); p.Q = (int)a.Q;
     p.nc = (int)((a.L + a.Q - 1) / a.Q);
     p.Lp = (int64_t)p.nc * a.Q;
     if (p.hpg % kHB != 0 && p.G != 1) return fail(MSC_ERR_UNSUPPORTED, "heads per group must be a multiple of %d", kHB);
@@ -545,43 +764,50 @@ msc_status ssd_launch(const SsdArgs& a, cudaStream_t st) {
     ssd_prep_kernel<<<dim3(p.nc, p.H, (unsigned)a.batch), 256, 0, st>>>(p);
     msc_status s = check_launch("ssd_prep");
     if (s != MSC_OK) return s;
+    // tensor maps: x [b, L, H * P] and B, C [b, L, G * N], boxes of 64 elements
+    ScanMaps m;
+    {
+        const uint64_t bcd[3] = {(uint64_t)(a.G * kN), (uint64_t)a.L, (uint64_t)a.batch};
+        const uint64_t bcs[2] = {(uint64_t)(a.G * kN * 2), (uint64_t)(a.L * a.G * kN * 2)};
+        const uint32_t cbox[3] = {64, 128, 1};
+        const uint32_t qbox[3] = {64, (uint32_t)p.Q, 1};
+        const uint32_t sbox[3] = {64, (uint32_t)std::min(p.Q, 128), 1};
+        const uint64_t xd[3] = {(uint64_t)(a.H * kP), (uint64_t)a.L, (uint64_t)a.batch};
+        const uint64_t xs[2] = {(uint64_t)(a.H * kP * 2), (uint64_t)(a.L * a.H * kP * 2)};
+        if (!encode_tmap(&m.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.C, bcd, bcs, cbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&m.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.B, bcd, bcs, qbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&m.xq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.x, xd, xs, qbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&m.xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.x, xd, xs, sbox, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MSC_ERR_CUDA;
+    }
     // (2) chunk states
     {
-        const int smem = state_smem(p.Q);
-        static int configured = 0;
-        if (configured < smem) {
+        static bool configured = false;
+        if (!configured) {
             cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_state smem attribute: %s", cudaGetErrorString(e));
-            configured = smem;
+            configured = true;
         }
-        ssd_state_kernel<<<dim3(p.nc, (p.H + kHB - 1) / kHB, (unsigned)a.batch), 128, smem, st>>>(p);
+        ssd_state_kernel<<<dim3(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch), 256, state_smem(p.Q), st>>>(m.B, m.xq, p);
         if ((s = check_launch("ssd_state")) != MSC_OK) return s;
     }
     // (3) inter-chunk state pass
     {
         const int64_t per_b = (int64_t)p.H * kP * kN;
-        ssd_pass_kernel<<<dim3((unsigned)((per_b + 255) / 256), (unsigned)a.batch), 256, 0, st>>>(p);
+        ssd_pass_kernel<<<dim3((unsigned)((per_b / 8 + 255) / 256), (unsigned)a.batch), 256, 0, st>>>(p);
         if ((s = check_launch("ssd_pass")) != MSC_OK) return s;
     }
     // (4) chunk scan
     {
-        ScanMaps m;
-        const uint64_t bcd[3] = {(uint64_t)(a.G * kN), (uint64_t)a.L, (uint64_t)a.batch};
-        const uint64_t bcs[2] = {(uint64_t)(a.G * kN * 2), (uint64_t)(a.L * a.G * kN * 2)};
-        const uint32_t cbox[3] = {64, 128, 1};
-        const uint32_t bbox[3] = {64, (uint32_t)(p.Q < 256 ? p.Q : 256), 1};
         const int nib = (p.Q + 127) / 128;
-        // the B box is the whole chunk (Q rows); a row block uses its first Qi
-        if (!encode_tmap(&m.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.C, bcd, bcs, cbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_tmap(&m.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.B, bcd, bcs, bbox, CU_TENSOR_MAP_SWIZZLE_128B))
-            return MSC_ERR_CUDA;
         static bool configured = false;
         if (!configured) {
             cudaError_t e = cudaFuncSetAttribute(ssd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
             if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_scan smem attribute: %s", cudaGetErrorString(e));
             configured = true;
         }
-        ssd_scan_kernel<<<dim3(p.nc * nib, (p.H + kHB - 1) / kHB, (unsigned)a.batch), 256, kScanSmem, st>>>(m.C, m.B, p);
+        ssd_scan_kernel<<<dim3(p.nc * nib, (p.H + kHB - 1) / kHB, (unsigned)a.batch), kScanThreads, kScanSmem, st>>>(
+            m.C, m.B, m.xs, p);
         if ((s = check_launch("ssd_scan")) != MSC_OK) return s;
     }
     return MSC_OK;
