@@ -127,6 +127,27 @@ msc_status msc_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, in
                                   float* dD, float* dz, float* ddelta_bias,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------ S6 decode step
+ * One token of the same recurrence for every channel row, the state carried
+ * from call to call ("Mamba — 选择性状态空间模型", 实践案例 1: what happens when
+ * one token is read -- the fixed-size state h is updated once and read out;
+ * 核心要点: training runs the parallel scan, inference runs this step-by-step
+ * recurrence).  Per row (b, d), with Delta = softplus(delta + Delta_bias[d]):
+ *   state[n] <- exp(Delta A[d, n]) state[n] + Delta B[b, n] u
+ *   y = (sum_n C[b, n] state[n] + D[d] u) * silu(z)
+ * Shapes: u, delta, z, y: [batch, dim]; B, C: [batch, dstate]; A: [dim, dstate];
+ * D, delta_bias: [dim]; state: [batch, dim, dstate] fp32, read and overwritten
+ * in place.  Same limits as the forward (dstate 1..16); no workspace.  Calling
+ * it seqlen times on tokens t = 0.. reproduces msc_selective_scan_fwd with
+ * h0 = the initial state, up to fp32 rounding.  A state row of 16 states is
+ * moved with one 32-byte load and store per thread (two threads per row).
+ */
+msc_status msc_selective_state_update(int64_t batch, int64_t dim, int64_t dstate, msc_dtype in_dtype,
+                                      const void* u, const void* delta, const float* A,
+                                      const void* B, const void* C, const float* D,
+                                      const void* z, const float* delta_bias,
+                                      float* state, float* y, void* stream);
+
 /* ------------------------------------------------------------- SSD chunked fwd
  * Shapes: x, z: [batch, seqlen, nheads, headdim]; delta: [batch, seqlen, nheads];
  * A, D, delta_bias: [nheads] fp32; B, C: [batch, seqlen, ngroups, dstate];

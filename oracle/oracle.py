@@ -96,6 +96,18 @@ def s6_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None,
     return (y, h_last) if return_last_state else y
 
 
+def s6_step(u, delta, A, B, C, D=None, z=None, delta_bias=None, state=None):
+    """One decode step ("Mamba — 选择性状态空间模型", 实践案例 1: one token updates the
+    fixed-size state once and is read out): the forward recurrence over a
+    single step from `state`.  u, delta, z: [batch, dim]; B, C: [batch, N];
+    state: [batch, dim, N] (zero if None).  Returns (y [batch, dim], new state)."""
+    u, delta, B, C = map(_f64, (u, delta, B, C))
+    z = None if z is None else _f64(z)[:, :, None]
+    y, h = s6_fwd(u[:, :, None], delta[:, :, None], A, B[:, :, None], C[:, :, None], D, z, delta_bias,
+                  state, return_last_state=True)
+    return y[:, :, 0], h
+
+
 def s6_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, dy=None):
     """S6 backward (zero initial state).  Returns a dict of float64 grads:
     du, ddelta, dA, dB, dC, and dD / dz / ddelta_bias when the input is present."""

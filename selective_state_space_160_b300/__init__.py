@@ -15,7 +15,7 @@ import threading
 
 __all__ = [
     "load_library", "library_path",
-    "msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd",
+    "msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd", "msc_selective_state_update",
     "msc_selective_scan_fwd_workspace_size", "msc_selective_scan_bwd_workspace_size",
     "msc_ssd_chunked_fwd_workspace_size", "msc_check_device_status", "msc_status_string",
     "msc_last_error", "MscError", "MSC_F32", "MSC_BF16",
@@ -42,6 +42,7 @@ SIGNATURES = {
     "msc_ssd_chunked_fwd_workspace_size": (_sz, [_i64] * 7),
     "msc_ssd_chunked_fwd": (ctypes.c_int, [_i64] * 7 + [ctypes.c_int] + [_vp] * 10 + [_vp, _sz, _vp]),
     "msc_selective_scan_fwd_noalloc": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 11 + [_vp]),
+    "msc_selective_state_update": (ctypes.c_int, [_i64] * 3 + [ctypes.c_int] + [_vp] * 10 + [_vp]),
     "msc_check_device_status": (ctypes.c_int, [_vp]),
     "msc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "msc_last_error": (ctypes.c_char_p, []),
@@ -190,6 +191,37 @@ def msc_selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h
                                     ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream))
     _check(st)
     return (y, h_last) if return_last_state else y
+
+
+def msc_selective_state_update(u, delta, A, B, C, D=None, z=None, delta_bias=None, state=None,
+                               y=None, stream=None):
+    """S6 decode step: one token per row.  u, delta, z: [batch, dim] (fp32 or
+    bf16, all the same); B, C: [batch, N] (same dtype); A: [dim, N] fp32;
+    D, delta_bias: [dim] fp32; state: [batch, dim, N] fp32, updated in place.
+    Returns y [batch, dim] fp32."""
+    torch = _torch()
+    lib = load_library()
+    if state is None:
+        raise ValueError("state is required (it is read and updated in place)")
+    batch, dim = u.shape
+    N = A.shape[1]
+    dt = _in_dtype(u)
+    tdt = u.dtype
+    args = [
+        _dev_ptr(u, "u"), _dev_ptr(delta, "delta", tdt, (batch, dim)),
+        _dev_ptr(A, "A", torch.float32, (dim, N)),
+        _dev_ptr(B, "B", tdt, (batch, N)), _dev_ptr(C, "C", tdt, (batch, N)),
+        _dev_ptr(D, "D", torch.float32, (dim,), optional=True),
+        _dev_ptr(z, "z", tdt, (batch, dim), optional=True),
+        _dev_ptr(delta_bias, "delta_bias", torch.float32, (dim,), optional=True),
+        _dev_ptr(state, "state", torch.float32, (batch, dim, N)),
+    ]
+    if y is None:
+        y = torch.empty((batch, dim), dtype=torch.float32, device=u.device)
+    st = lib.msc_selective_state_update(batch, dim, N, dt, *args, _dev_ptr(y, "y", torch.float32, (batch, dim)),
+                                        _stream_ptr(stream))
+    _check(st)
+    return y
 
 
 def msc_selective_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, dy=None,

@@ -165,6 +165,23 @@ msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, in
     return s6_fwd_launch(a, plan, static_cast<cudaStream_t>(stream));
 }
 
+msc_status msc_selective_state_update(int64_t batch, int64_t dim, int64_t dstate, msc_dtype in_dtype,
+                                      const void* u, const void* delta, const float* A, const void* B,
+                                      const void* C, const float* D, const void* z, const float* delta_bias,
+                                      float* state, float* y, void* stream) {
+    clear_error();
+    msc_status s = check_s6_dims(batch, dim, 1, dstate, in_dtype);
+    if (s != MSC_OK) return s;
+    MSC_PTR(u, "u"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A"); MSC_PTR(B, "B");
+    MSC_PTR(C, "C"); MSC_PTR(state, "state"); MSC_PTR(y, "y");
+    MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z"); MSC_OPT_PTR(delta_bias, "delta_bias");
+    S6StepArgs a{};
+    a.batch = batch; a.dim = dim; a.N = (int)dstate; a.bf16 = in_dtype == MSC_BF16;
+    a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C;
+    a.A = A; a.D = D; a.delta_bias = delta_bias; a.state = state; a.y = y;
+    return s6_step_launch(a, static_cast<cudaStream_t>(stream));
+}
+
 size_t msc_selective_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
                                              int64_t dstate) {
     if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > 16) return 0;

@@ -53,6 +53,18 @@ struct S6BwdArgs {
 
 msc_status s6_bwd_launch(const S6BwdArgs& a, cudaStream_t stream);
 
+// Decode step: one token per row, state [batch * dim, N] updated in place.
+struct S6StepArgs {
+    int64_t batch, dim;
+    int N;
+    bool bf16;
+    const void *u, *delta, *z, *B, *C;
+    const float *A, *D, *delta_bias;
+    float *state, *y;
+};
+
+msc_status s6_step_launch(const S6StepArgs& a, cudaStream_t stream);
+
 struct SsdArgs {
     int64_t batch, L, H, P, N, G, Q;
     const void *x, *delta, *B, *C, *z;

@@ -115,3 +115,19 @@ def test_ssd_rejects_bad_arguments(lib):
 def test_check_device_status_null_workspace_signature(lib):
     # only the signature is checked here; calling it needs a CUDA context
     assert lib.msc_check_device_status.restype == ctypes.c_int
+
+
+def test_step_rejects_bad_arguments(lib):
+    f = lib.msc_selective_state_update
+
+    def call(batch=2, dim=4, N=16, dt=1, u=16, state=16, y=16, z=None):
+        return f(batch, dim, N, dt, u, 16, 16, 16, 16, None, z, None, state, y, None)
+
+    assert call(state=None) == msc.MSC_ERR_INVALID_ARG
+    assert "state must not be NULL" in msc.msc_last_error()
+    assert call(y=None) == msc.MSC_ERR_INVALID_ARG
+    assert call(u=24) == msc.MSC_ERR_INVALID_ARG                 # misaligned
+    assert call(z=40) == msc.MSC_ERR_INVALID_ARG
+    assert call(N=17) == msc.MSC_ERR_UNSUPPORTED
+    assert call(dim=0) == msc.MSC_ERR_INVALID_ARG
+    assert call(dt=5) == msc.MSC_ERR_INVALID_ARG

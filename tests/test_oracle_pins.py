@@ -377,6 +377,37 @@ def test_p8_study_note_three_steps():
     np.testing.assert_allclose(y[0, 0], [1.0 * h0, 3.0 * h1, 2.0 * h2], rtol=1e-14, atol=1e-15)
 
 
+# ----------------------------------------------------------------------------- P9
+@pytest.mark.parametrize("with_z,with_D,with_bias", [(True, True, True), (False, False, False)])
+def test_p9_decode_steps_equal_scan(with_z, with_D, with_bias):
+    """The decode-step oracle run token by token from a state equals the scan
+    over the same tokens from that state (recurrent mode = scan mode)."""
+    inp = s6_inputs(2, 5, 9, 16, seed=41, with_z=with_z, with_D=with_D, with_bias=with_bias)
+    rng = np.random.default_rng(5)
+    h0 = rng.standard_normal((2, 5, 16))
+    y_scan, h_scan = oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                   inp["delta_bias"], h0=h0, return_last_state=True)
+    h = h0
+    ys = []
+    for t in range(9):
+        zt = None if inp["z"] is None else inp["z"][:, :, t]
+        y, h = oracle.s6_step(inp["u"][:, :, t], inp["delta"][:, :, t], inp["A"], inp["B"][:, :, t],
+                              inp["C"][:, :, t], inp["D"], zt, inp["delta_bias"], h)
+        ys.append(y)
+    np.testing.assert_allclose(np.stack(ys, axis=2), y_scan, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(h, h_scan, rtol=1e-12, atol=1e-13)
+
+
+def test_p9_decode_step_from_zero_is_first_scan_step():
+    inp = s6_inputs(1, 3, 4, 8, seed=42)
+    y_scan = oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                           inp["delta_bias"])
+    y, h = oracle.s6_step(inp["u"][:, :, 0], inp["delta"][:, :, 0], inp["A"], inp["B"][:, :, 0],
+                          inp["C"][:, :, 0], inp["D"], inp["z"][:, :, 0], inp["delta_bias"])
+    np.testing.assert_allclose(y, y_scan[:, :, 0], rtol=1e-13, atol=1e-14)
+    assert h.shape == (1, 3, 8)
+
+
 # ------------------------------------------------------------------ planted mistakes
 MUTATIONS = [
     # (description, original text, mutated text)
