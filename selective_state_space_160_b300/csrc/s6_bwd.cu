@@ -40,7 +40,10 @@ constexpr int kStages = 2;
 constexpr int kRowTile = 2048;  // 32 rows x 64 bytes
 constexpr int kBCTile = 1024;   // 16 slots x 64 bytes
 constexpr int kStageBytes = 4 * kRowTile + 2 * kBCTile;
-constexpr int kRedPitch = 34;   // floats per (x, k, n) row of the reduction buffer
+// dB / dC reduction buffer s_red[x][k][row][n]: 16 floats per row, rows 16.. shifted by
+// 16 floats so that the two row halves summed side by side use different banks
+constexpr int kRedBlock = 32 * 16 + 32;  // floats per (x, k) block
+__host__ __device__ constexpr int red_row(int r) { return r * 16 + (r >= 16 ? 16 : 0); }
 
 __device__ unsigned int g_s6_bwd_status[2];
 
@@ -132,13 +135,13 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
     constexpr int kES = kBF16 ? 2 : 4;
     // dynamic shared memory, carved at a 1024-byte aligned base (TMA swizzle atoms)
     extern __shared__ uint8_t s_dyn[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_dyn) + 1023) & ~uintptr_t(1023));
+    // (offset from s_dyn itself, so the compiler keeps shared-memory accesses)
+    uint8_t* base = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);
     uint8_t (*s_raw)[kStageBytes] = reinterpret_cast<uint8_t (*)[kStageBytes]>(base);
     float (*s_bc)[8][kPitch] = reinterpret_cast<float (*)[8][kPitch]>(base + kStages * kStageBytes);
-    float (*s_red)[8][16][kRedPitch] =
-        reinterpret_cast<float (*)[8][16][kRedPitch]>(base + kStages * kStageBytes + 2 * 8 * kPitch * 4);
-    uint64_t* s_full = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes + 2 * 8 * kPitch * 4 +
-                                                   2 * 8 * 16 * kRedPitch * 4);
+    float* s_red = reinterpret_cast<float*>(base + kStages * kStageBytes + 2 * 8 * kPitch * 4);
+    float* s_sum = s_red + 2 * 8 * kRedBlock;  // [x][n][k] row sums of one group
+    uint64_t* s_full = reinterpret_cast<uint64_t*>(s_sum + 2 * 16 * 8);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -299,6 +302,7 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
                 const uint64_t dtu2 = msc::pk2(dtus[k], dtus[k]);
                 const uint64_t gp2 = msc::pk2(gps[k], gps[k]);
                 uint64_t ysum = 0ull;
+                uint64_t dc[2];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const uint64_t Bq = *reinterpret_cast<const uint64_t*>(bsrc + q * kPitch + 2 * k);
@@ -309,12 +313,10 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
                     h[q] = msc::fma2(a, h[q], msc::mul2(dtu2, Bq));
                     ysum = q == 0 ? msc::mul2(Cq, h[q]) : msc::fma2(Cq, h[q], ysum);
                     // dC_{t,n} contribution of this row: g'_t h_{t,n}
-                    float c0, c1;
-                    msc::upk2(msc::mul2(gp2, h[q]), c0, c1);
-                    const int n = 4 * j + 2 * q;
-                    s_red[1][k][n][r] = c0;
-                    s_red[1][k][n + 1][r] = c1;
+                    dc[q] = msc::mul2(gp2, h[q]);
                 }
+                *reinterpret_cast<ulonglong2*>(s_red + (8 + k) * kRedBlock + red_row(r) + 4 * j) =
+                    make_ulonglong2(dc[0], dc[1]);
                 float lo, hi;
                 msc::upk2(ysum, lo, hi);
                 yp[k] = lo + hi;
@@ -327,6 +329,7 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
                 const uint64_t dtu2 = msc::pk2(dtus[k], dtus[k]);
                 const uint64_t gp2 = msc::pk2(gps[k], gps[k]);
                 uint64_t t1 = 0ull, t2 = 0ull;
+                uint64_t db[2];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const uint64_t Bq = *reinterpret_cast<const uint64_t*>(bsrc + q * kPitch + 2 * k);
@@ -339,12 +342,10 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
                     t2 = q == 0 ? msc::mul2(lq, Ap[q]) : msc::fma2(lq, Ap[q], t2);
                     dA2[q] = msc::fma2(lq, dt2, dA2[q]);
                     // dB_{t,n} contribution of this row: lambda_{t,n} Delta_t u_t
-                    float c0, c1;
-                    msc::upk2(msc::mul2(lam[q], dtu2), c0, c1);
-                    const int n = 4 * j + 2 * q;
-                    s_red[0][k][n][r] = c0;
-                    s_red[0][k][n + 1][r] = c1;
+                    db[q] = msc::mul2(lam[q], dtu2);
                 }
+                *reinterpret_cast<ulonglong2*>(s_red + k * kRedBlock + red_row(r) + 4 * j) =
+                    make_ulonglong2(db[0], db[1]);
                 float lo, hi;
                 msc::upk2(t1, lo, hi);
                 s1[k] = lo + hi;
@@ -374,29 +375,35 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
                 if (has_z) *reinterpret_cast<float2*>(p.dz + off) = make_float2(o_dz[0], o_dz[1]);
             }
             __syncthreads();
-            // ---- dB, dC of this group: sum the CTA's rows, one vector add per 4 steps
+            // ---- dB, dC of this group: sum the CTA's 32 rows (thread = (x, k, 4 states, row half)),
+            // transpose through s_sum, one vector add per 4 steps
             {
-                const int half = tid & 1;           // rows 16 * half ..
-                const int item = tid >> 1;          // (x, n, kq)
-                const int x = item >> 5, n = (item >> 1) & 15, kq = item & 1;
-                float acc4[4];
+                const int half = tid & 1, n4 = (tid >> 1) & 3, k = (tid >> 3) & 7, x = tid >> 6;
+                const float* src = s_red + (8 * x + k) * kRedBlock + red_row(16 * half) + 4 * n4;
+                uint64_t a01 = 0ull, a23 = 0ull;
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const float* src = &s_red[x][4 * kq + k4][n][16 * half];
-                    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                    for (int rr = 0; rr < 16; rr += 2) {
-                        const float2 v = *reinterpret_cast<const float2*>(src + rr);
-                        a0 += v.x;
-                        a1 += v.y;
-                    }
-                    acc4[k4] = a0 + a1;
+                for (int rr = 0; rr < 16; ++rr) {
+                    const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + 16 * rr);
+                    a01 = msc::add2(a01, v.x);
+                    a23 = msc::add2(a23, v.y);
                 }
+                float s4[4];
+                msc::upk2(a01, s4[0], s4[1]);
+                msc::upk2(a23, s4[2], s4[3]);
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) acc4[k4] += __shfl_xor_sync(0xffffffffu, acc4[k4], 1);
-                if (half == 0 && n < N) {
+                for (int e = 0; e < 4; ++e) s4[e] += __shfl_xor_sync(0xffffffffu, s4[e], 1);
+                if (half == 0) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s_sum[(16 * x + 4 * n4 + e) * 8 + k] = s4[e];
+                }
+            }
+            __syncthreads();
+            if (tid < 64) {
+                const int x = tid >> 5, n = (tid >> 1) & 15, kq = tid & 1;
+                const float4 v = *reinterpret_cast<const float4*>(s_sum + (16 * x + n) * 8 + 4 * kq);
+                if (n < N) {
                     float* dst = (x == 0 ? p.dB : p.dC) + ((size_t)b * N + n) * p.L + tg + 4 * kq;
-                    red_add_v4(dst, acc4[0], acc4[1], acc4[2], acc4[3]);
+                    red_add_v4(dst, v.x, v.y, v.z, v.w);
                 }
             }
             __syncthreads();
@@ -433,8 +440,8 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
 
 template <bool kBF16>
 constexpr int bwd_smem_bytes() {
-    return 1024 + kStages * kStageBytes + 2 * 8 * (2 * (kBF16 ? 32 : 16) + 4) * 4 + 2 * 8 * 16 * kRedPitch * 4 +
-           kStages * 8;
+    return 1024 + kStages * kStageBytes + 2 * 8 * (2 * (kBF16 ? 32 : 16) + 4) * 4 + 2 * 8 * kRedBlock * 4 +
+           2 * 16 * 8 * 4 + kStages * 8;
 }
 
 template <bool kBF16>

@@ -172,7 +172,7 @@ struct StateSmem {
     uint64_t* bars;  // 0: B, 1-2: x buffers, 3-4: MMA of a buffer
 };
 
-__device__ __forceinline__ void state_issue_head(const StateSmem& m, const CUtensorMap* tmX, const SsdParams& p,
+__device__ __forceinline__ void state_issue_head(const StateSmem m, const CUtensorMap* tmX, const SsdParams& p,
                                                  int h, int s, int c, int b) {
     const int Q = p.Q;
     const uint32_t tile = (uint32_t)Q * 128u;
@@ -186,7 +186,7 @@ __device__ __forceinline__ void state_issue_head(const StateSmem& m, const CUten
 __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ CUtensorMap tmB,
                                                         const __grid_constant__ CUtensorMap tmX, const SsdParams p) {
     extern __shared__ uint8_t s_dyn[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_dyn) + 1023) & ~uintptr_t(1023));
+    uint8_t* base = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);  // 1024-aligned, still a shared address
     const int Q = p.Q;
     const uint32_t tile = (uint32_t)Q * 128u;  // bytes of one [Q][64] bf16 tile
     StateSmem m;
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
                                                                    const __grid_constant__ CUtensorMap tmX,
                                                                    const SsdParams p) {
     extern __shared__ uint8_t s_dyn[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_dyn) + 1023) & ~uintptr_t(1023));
+    uint8_t* base = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);  // 1024-aligned, still a shared address
     const int Q = p.Q;
     const int nib = (Q + 127) / 128;
     const int c = blockIdx.x / nib, ib = blockIdx.x % nib;
