@@ -296,8 +296,19 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
             float yp[8];
             const float* bsrc = &s_bc[0][2 * j][16 * g];
             const float* csrc = &s_bc[1][2 * j][16 * g];
+            // B, C pairs of steps (k, k + 1), k even, of state pair q: one 16-byte load each
+            uint64_t Bk[2][2], Ck[2][2];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
+                if ((k & 1) == 0) {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const ulonglong2 vb = *reinterpret_cast<const ulonglong2*>(bsrc + q * kPitch + 2 * k);
+                        const ulonglong2 vc = *reinterpret_cast<const ulonglong2*>(csrc + q * kPitch + 2 * k);
+                        Bk[0][q] = vb.x; Bk[1][q] = vb.y;
+                        Ck[0][q] = vc.x; Ck[1][q] = vc.y;
+                    }
+                }
                 const uint64_t dt2 = msc::pk2(dts[k], dts[k]);
                 const uint64_t dtu2 = msc::pk2(dtus[k], dtus[k]);
                 const uint64_t gp2 = msc::pk2(gps[k], gps[k]);
@@ -305,8 +316,8 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
                 uint64_t dc[2];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const uint64_t Bq = *reinterpret_cast<const uint64_t*>(bsrc + q * kPitch + 2 * k);
-                    const uint64_t Cq = *reinterpret_cast<const uint64_t*>(csrc + q * kPitch + 2 * k);
+                    const uint64_t Bq = Bk[k & 1][q];
+                    const uint64_t Cq = Ck[k & 1][q];
                     const uint64_t a = msc::ex2_2(msc::mul2(dt2, A2p[q]));
                     ah[k][q] = a;
                     hp[k][q] = h[q];
@@ -325,6 +336,15 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
             float s1[8], s2[8];
 #pragma unroll
             for (int k = 7; k >= 0; --k) {
+                if (k & 1) {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const ulonglong2 vb = *reinterpret_cast<const ulonglong2*>(bsrc + q * kPitch + 2 * (k - 1));
+                        const ulonglong2 vc = *reinterpret_cast<const ulonglong2*>(csrc + q * kPitch + 2 * (k - 1));
+                        Bk[0][q] = vb.x; Bk[1][q] = vb.y;
+                        Ck[0][q] = vc.x; Ck[1][q] = vc.y;
+                    }
+                }
                 const uint64_t dt2 = msc::pk2(dts[k], dts[k]);
                 const uint64_t dtu2 = msc::pk2(dtus[k], dtus[k]);
                 const uint64_t gp2 = msc::pk2(gps[k], gps[k]);
@@ -332,8 +352,8 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
                 uint64_t db[2];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const uint64_t Bq = *reinterpret_cast<const uint64_t*>(bsrc + q * kPitch + 2 * k);
-                    const uint64_t Cq = *reinterpret_cast<const uint64_t*>(csrc + q * kPitch + 2 * k);
+                    const uint64_t Bq = Bk[k & 1][q];
+                    const uint64_t Cq = Ck[k & 1][q];
                     const uint64_t anext = (k < 7) ? ah[k + 1][q] : a_carry[q];
                     lam[q] = msc::fma2(anext, lam[q], msc::mul2(gp2, Cq));
                     const uint64_t qh = msc::mul2(ah[k][q], hp[k][q]);  // abar_t h_{t-1}
