@@ -330,6 +330,35 @@ def leg_decode(peaks, pipes, steps=20, warmup=3):
     return res
 
 
+def leg_conv1d(peaks, pipes, steps=10, warmup=3):
+    """Causal conv1d (K 4) + SiLU front end, batch 8 x D 5120 x L 2048, bf16 in
+    and out (168 MB in, 168 MB out per call: larger than L2)."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    batch, dim, L, K = 8, 5120, 2048, 4
+    g = torch.Generator(device="cuda").manual_seed(160_006)
+    x = torch.randn((batch, dim, L), device="cuda", generator=g).to(torch.bfloat16)
+    w = torch.randn((dim, K), device="cuda", generator=g) / 2.0
+    bias = 0.1 * torch.randn(dim, device="cuda", generator=g)
+    out = torch.empty((batch, dim, L), dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def fn():
+        msc.msc_causal_conv1d_fwd(x, w, bias, out=out)
+    ms = statistics.median(time_launches(fn, steps, warmup, st))
+    el = batch * dim * L
+    nbytes = el * 4 + dim * (K + 1) * 4
+    t = ms * 1e-3
+    ach = nbytes / t / 1e9
+    res = {"workload": "causal conv1d K 4 + SiLU, batch 8, D 5120, L 2048, bf16 in / bf16 out",
+           "elements_per_s": el / t, "ms": ms,
+           "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": nbytes}}
+    del x, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def leg_ssd(peaks, pipes, steps=5, warmup=2):
     import torch
     import selective_state_space_160_b300 as msc
@@ -533,7 +562,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         for name in args.legs.split(","):
             try:
-                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "decode": leg_decode}[name]
+                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "decode": leg_decode, "conv1d": leg_conv1d}[name]
                 legs[name] = fn(peaks, pipes)
             except Exception as ex:  # report, do not hide: a failing leg is printed as such
                 legs[name] = {"error": "%s: %s" % (type(ex).__name__, ex)}
@@ -574,7 +603,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="fwd_long,bwd,ssd,decode")
+    ap.add_argument("--legs", default="fwd_long,bwd,ssd,decode,conv1d")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)

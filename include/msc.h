@@ -148,6 +148,34 @@ msc_status msc_selective_state_update(int64_t batch, int64_t dim, int64_t dstate
                                       const void* z, const float* delta_bias,
                                       float* state, float* y, void* stream);
 
+/* ------------------------------------------------ causal conv1d front end
+ * The short causal convolution that gives the selective SSM its local context
+ * in every Mamba block (bqwf survey sec. 3.1: causal 1-D convolution, then the
+ * selective SSM), depthwise per channel, followed by SiLU:
+ *   out[b, d, t] = silu(bias[d] + sum_{k < width} w[d, k] x[b, d, t - (width - 1) + k])
+ * with x = 0 before t = 0 (width 1..8; 4 in Mamba).  Shapes: x, out
+ * [batch, dim, seqlen]; weight [dim, width] fp32; bias [dim] fp32 or NULL.
+ * `silu` = 0 skips the activation.  x is fp32 or bf16 (in_dtype); out is
+ * fp32 or bf16 (out_dtype; bf16 rounds to nearest even), so the result can be
+ * passed to msc_selective_scan_fwd as u.  No workspace.
+ */
+msc_status msc_causal_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t width,
+                                 msc_dtype in_dtype, msc_dtype out_dtype, const void* x,
+                                 const float* weight, const float* bias, int silu, void* out,
+                                 void* stream);
+
+/* Decode step of the same convolution (study note "Mamba — 选择性状态空间模型",
+ * 踩过的坑: with no attention cache, the convolution still keeps the last
+ * few inputs).  conv_state [batch, dim, width - 1] fp32 holds the previous
+ * width - 1 inputs, oldest first; it is read, shifted by one and written back
+ * with x appended.  x, out: [batch, dim].  Calling it seqlen times reproduces
+ * msc_causal_conv1d_fwd from a zero state.
+ */
+msc_status msc_causal_conv1d_update(int64_t batch, int64_t dim, int64_t width, msc_dtype in_dtype,
+                                    msc_dtype out_dtype, const void* x, const float* weight,
+                                    const float* bias, int silu, float* conv_state, void* out,
+                                    void* stream);
+
 /* ------------------------------------------------------------- SSD chunked fwd
  * Shapes: x, z: [batch, seqlen, nheads, headdim]; delta: [batch, seqlen, nheads];
  * A, D, delta_bias: [nheads] fp32; B, C: [batch, seqlen, ngroups, dstate];

@@ -108,6 +108,41 @@ def s6_step(u, delta, A, B, C, D=None, z=None, delta_bias=None, state=None):
     return y[:, :, 0], h
 
 
+def _silu(v):
+    return v / (1.0 + np.exp(-v))
+
+
+def causal_conv1d(x, weight, bias=None, silu=True):
+    """Causal depthwise conv1d front end of the Mamba block (bqwf survey sec. 3.1:
+    a causal 1-D convolution for local context before the selective SSM):
+    out[b, d, t] = act(bias[d] + sum_k weight[d, k] x[b, d, t - (K - 1) + k]),
+    x = 0 before t = 0, act = silu or identity.  x: [batch, dim, L];
+    weight: [dim, K]; bias: [dim]."""
+    x = _f64(x)
+    w = _f64(weight)
+    batch, dim, L = x.shape
+    K = w.shape[1]
+    xp = np.concatenate([np.zeros((batch, dim, K - 1)), x], axis=2)
+    out = np.zeros((batch, dim, L)) if bias is None else np.broadcast_to(_f64(bias)[None, :, None],
+                                                                          (batch, dim, L)).copy()
+    for k in range(K):
+        out += w[None, :, k, None] * xp[:, :, k:k + L]
+    return _silu(out) if silu else out
+
+
+def causal_conv1d_update(x, conv_state, weight, bias=None, silu=True):
+    """Decode step of causal_conv1d (study note "Mamba — 选择性状态空间模型",
+    踩过的坑: the convolution keeps the last few inputs).  x: [batch, dim];
+    conv_state: [batch, dim, K - 1], oldest first.  Returns (out, new state)."""
+    x = _f64(x)
+    w = _f64(weight)
+    window = np.concatenate([_f64(conv_state), x[:, :, None]], axis=2)
+    out = np.einsum("bdk,dk->bd", window, w)
+    if bias is not None:
+        out = out + _f64(bias)[None, :]
+    return (_silu(out) if silu else out), window[:, :, 1:]
+
+
 def s6_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, dy=None):
     """S6 backward (zero initial state).  Returns a dict of float64 grads:
     du, ddelta, dA, dB, dC, and dD / dz / ddelta_bias when the input is present."""

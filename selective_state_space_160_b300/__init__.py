@@ -16,6 +16,7 @@ import threading
 __all__ = [
     "load_library", "library_path",
     "msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd", "msc_selective_state_update",
+    "msc_causal_conv1d_fwd", "msc_causal_conv1d_update",
     "msc_selective_scan_fwd_workspace_size", "msc_selective_scan_bwd_workspace_size",
     "msc_ssd_chunked_fwd_workspace_size", "msc_check_device_status", "msc_status_string",
     "msc_last_error", "MscError", "MSC_F32", "MSC_BF16",
@@ -43,6 +44,8 @@ SIGNATURES = {
     "msc_ssd_chunked_fwd": (ctypes.c_int, [_i64] * 7 + [ctypes.c_int] + [_vp] * 10 + [_vp, _sz, _vp]),
     "msc_selective_scan_fwd_noalloc": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 11 + [_vp]),
     "msc_selective_state_update": (ctypes.c_int, [_i64] * 3 + [ctypes.c_int] + [_vp] * 10 + [_vp]),
+    "msc_causal_conv1d_fwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] * 2 + [_vp] * 3 + [ctypes.c_int] + [_vp, _vp]),
+    "msc_causal_conv1d_update": (ctypes.c_int, [_i64] * 3 + [ctypes.c_int] * 2 + [_vp] * 3 + [ctypes.c_int] + [_vp] * 3),
     "msc_check_device_status": (ctypes.c_int, [_vp]),
     "msc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "msc_last_error": (ctypes.c_char_p, []),
@@ -222,6 +225,54 @@ def msc_selective_state_update(u, delta, A, B, C, D=None, z=None, delta_bias=Non
                                         _stream_ptr(stream))
     _check(st)
     return y
+
+
+def _dtype_code(dtype):
+    torch = _torch()
+    if dtype == torch.float32:
+        return MSC_F32
+    if dtype == torch.bfloat16:
+        return MSC_BF16
+    raise ValueError("dtype must be torch.float32 or torch.bfloat16 (got %s)" % dtype)
+
+
+def msc_causal_conv1d_fwd(x, weight, bias=None, silu=True, out_dtype=None, out=None, stream=None):
+    """Causal depthwise conv1d (+ SiLU).  x: [batch, dim, L] fp32 or bf16;
+    weight: [dim, K] fp32; bias: [dim] fp32.  Returns out [batch, dim, L] in
+    out_dtype (default: x's dtype), ready to be the scan's u."""
+    torch = _torch()
+    lib = load_library()
+    batch, dim, L = x.shape
+    K = weight.shape[1]
+    out_dtype = x.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((batch, dim, L), dtype=out_dtype, device=x.device)
+    st = lib.msc_causal_conv1d_fwd(batch, dim, L, K, _in_dtype(x), _dtype_code(out.dtype), _dev_ptr(x, "x"),
+                                   _dev_ptr(weight, "weight", torch.float32, (dim, K)),
+                                   _dev_ptr(bias, "bias", torch.float32, (dim,), optional=True), int(bool(silu)),
+                                   _dev_ptr(out, "out", out.dtype, (batch, dim, L)), _stream_ptr(stream))
+    _check(st)
+    return out
+
+
+def msc_causal_conv1d_update(x, conv_state, weight, bias=None, silu=True, out_dtype=None, out=None, stream=None):
+    """Decode step of the causal conv1d.  x: [batch, dim]; conv_state:
+    [batch, dim, K - 1] fp32, updated in place.  Returns out [batch, dim]."""
+    torch = _torch()
+    lib = load_library()
+    batch, dim = x.shape
+    K = weight.shape[1]
+    out_dtype = x.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((batch, dim), dtype=out_dtype, device=x.device)
+    state_ptr = _dev_ptr(conv_state, "conv_state", torch.float32, (batch, dim, K - 1), optional=(K == 1))
+    st = lib.msc_causal_conv1d_update(batch, dim, K, _in_dtype(x), _dtype_code(out.dtype), _dev_ptr(x, "x"),
+                                      _dev_ptr(weight, "weight", torch.float32, (dim, K)),
+                                      _dev_ptr(bias, "bias", torch.float32, (dim,), optional=True),
+                                      int(bool(silu)), state_ptr, _dev_ptr(out, "out", out.dtype, (batch, dim)),
+                                      _stream_ptr(stream))
+    _check(st)
+    return out
 
 
 def msc_selective_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, dy=None,

@@ -182,6 +182,49 @@ msc_status msc_selective_state_update(int64_t batch, int64_t dim, int64_t dstate
     return s6_step_launch(a, static_cast<cudaStream_t>(stream));
 }
 
+static msc_status check_conv_dims(int64_t batch, int64_t dim, int64_t seqlen, int64_t width, msc_dtype in_dt,
+                                  msc_dtype out_dt) {
+    MSC_REQUIRE(batch >= 1 && dim >= 1 && seqlen >= 1, "batch, dim and seqlen must be >= 1 (got %lld, %lld, %lld)",
+                (long long)batch, (long long)dim, (long long)seqlen);
+    MSC_REQUIRE(in_dt == MSC_F32 || in_dt == MSC_BF16, "in_dtype must be MSC_F32 or MSC_BF16");
+    MSC_REQUIRE(out_dt == MSC_F32 || out_dt == MSC_BF16, "out_dtype must be MSC_F32 or MSC_BF16");
+    if (width < 1 || width > 8) return fail(MSC_ERR_UNSUPPORTED, "width must be in [1, 8] (got %lld)", (long long)width);
+    MSC_REQUIRE(batch * dim <= ((int64_t)1 << 40) && seqlen <= ((int64_t)1 << 40) / (batch * dim) * ((int64_t)1 << 20),
+                "batch * dim * seqlen too large");
+    return MSC_OK;
+}
+
+msc_status msc_causal_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t width, msc_dtype in_dtype,
+                                 msc_dtype out_dtype, const void* x, const float* weight, const float* bias, int silu,
+                                 void* out, void* stream) {
+    clear_error();
+    msc_status s = check_conv_dims(batch, dim, seqlen, width, in_dtype, out_dtype);
+    if (s != MSC_OK) return s;
+    MSC_PTR(x, "x"); MSC_PTR(weight, "weight"); MSC_PTR(out, "out");
+    MSC_OPT_PTR(bias, "bias");
+    Conv1dArgs a{};
+    a.batch = batch; a.dim = dim; a.L = seqlen; a.K = (int)width; a.silu = silu != 0;
+    a.in_bf16 = in_dtype == MSC_BF16; a.out_bf16 = out_dtype == MSC_BF16;
+    a.x = x; a.weight = weight; a.bias = bias; a.out = out;
+    return conv1d_fwd_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+msc_status msc_causal_conv1d_update(int64_t batch, int64_t dim, int64_t width, msc_dtype in_dtype,
+                                    msc_dtype out_dtype, const void* x, const float* weight, const float* bias,
+                                    int silu, float* conv_state, void* out, void* stream) {
+    clear_error();
+    msc_status s = check_conv_dims(batch, dim, 1, width, in_dtype, out_dtype);
+    if (s != MSC_OK) return s;
+    MSC_PTR(x, "x"); MSC_PTR(weight, "weight"); MSC_PTR(out, "out");
+    MSC_OPT_PTR(bias, "bias");
+    if (width > 1) MSC_PTR(conv_state, "conv_state");
+    Conv1dArgs a{};
+    a.batch = batch; a.dim = dim; a.L = 1; a.K = (int)width; a.silu = silu != 0;
+    a.in_bf16 = in_dtype == MSC_BF16; a.out_bf16 = out_dtype == MSC_BF16;
+    a.x = x; a.weight = weight; a.bias = bias; a.out = out; a.state = conv_state;
+    return conv1d_update_launch(a, static_cast<cudaStream_t>(stream));
+}
+
 size_t msc_selective_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
                                              int64_t dstate) {
     if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > 16) return 0;

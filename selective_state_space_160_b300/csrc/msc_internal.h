@@ -65,6 +65,20 @@ struct S6StepArgs {
 
 msc_status s6_step_launch(const S6StepArgs& a, cudaStream_t stream);
 
+// Causal depthwise conv1d (+ SiLU) front end and its decode step.
+struct Conv1dArgs {
+    int64_t batch, dim, L;
+    int K, silu;
+    bool in_bf16, out_bf16;
+    const void* x;
+    const float *weight, *bias;
+    float* state;
+    void* out;
+};
+
+msc_status conv1d_fwd_launch(const Conv1dArgs& a, cudaStream_t stream);
+msc_status conv1d_update_launch(const Conv1dArgs& a, cudaStream_t stream);
+
 struct SsdArgs {
     int64_t batch, L, H, P, N, G, Q;
     const void *x, *delta, *B, *C, *z;

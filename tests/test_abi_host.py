@@ -131,3 +131,20 @@ def test_step_rejects_bad_arguments(lib):
     assert call(N=17) == msc.MSC_ERR_UNSUPPORTED
     assert call(dim=0) == msc.MSC_ERR_INVALID_ARG
     assert call(dt=5) == msc.MSC_ERR_INVALID_ARG
+
+
+def test_conv1d_rejects_bad_arguments(lib):
+    f = lib.msc_causal_conv1d_fwd
+
+    def call(batch=1, dim=4, L=16, K=4, idt=1, odt=1, x=16, w=16, out=16):
+        return f(batch, dim, L, K, idt, odt, x, w, None, 1, out, None)
+
+    assert call(x=None) == msc.MSC_ERR_INVALID_ARG
+    assert call(K=9) == msc.MSC_ERR_UNSUPPORTED
+    assert call(K=0) == msc.MSC_ERR_UNSUPPORTED
+    assert call(odt=3) == msc.MSC_ERR_INVALID_ARG
+    assert call(L=0) == msc.MSC_ERR_INVALID_ARG
+    assert call(out=24) == msc.MSC_ERR_INVALID_ARG
+    g = lib.msc_causal_conv1d_update
+    assert g(1, 4, 4, 1, 1, 16, 16, None, 1, None, 16, None) == msc.MSC_ERR_INVALID_ARG   # state required
+    assert "conv_state" in msc.msc_last_error()

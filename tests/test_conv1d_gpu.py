@@ -1,0 +1,113 @@
+"""GPU parity of the causal conv1d front end and its decode step (through the C
+ABI) against the oracle.
+
+Tolerances: with an fp32 output max |gpu - ref| / (1 + |ref|) <= 1e-4.  A bf16
+output is a quantised value (8 significant bits, up to 2^-8 relative rounding
+error), so both sides take the same quantisation: the GPU value must equal the
+oracle's value rounded to bf16, or its neighbour one bf16 ulp away when the
+fp32 result before rounding lies within rounding distance of a boundary.  The
+oracle consumes the same bf16-rounded inputs."""
+import numpy as np
+import pytest
+
+from oracle import oracle
+from selective_state_space_160_b300.inputs import bf16_round
+from helpers import max_rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _data(batch, dim, L, K, seed, bf16):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((batch, dim, L)).astype(np.float32)
+    if bf16:
+        x = bf16_round(x)
+    w = (rng.standard_normal((dim, K)) / np.sqrt(K)).astype(np.float32)
+    bias = (0.1 * rng.standard_normal(dim)).astype(np.float32)
+    return x, w, bias
+
+
+def _out_np(t):
+    return t.float().cpu().numpy()
+
+
+def bf16_match(got, ref):
+    """Largest |got - bf16(ref)| in units of one bf16 ulp at |ref| (<= 1 passes)."""
+    r = bf16_round(np.asarray(ref, np.float32)).astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -120))) - 7)
+    return float(np.max(np.abs(np.asarray(got, np.float64) - r) / ulp))
+
+
+@pytest.mark.parametrize("batch,dim,L,K", [(1, 4, 64, 4), (2, 37, 100, 4), (3, 5, 7, 3), (1, 70, 1, 4),
+                                           (2, 16, 256, 8), (1, 9, 33, 1), (2, 12, 40, 2)])
+@pytest.mark.parametrize("in_bf16,out_bf16", [(False, False), (True, False), (True, True)])
+def test_forward_shapes(batch, dim, L, K, in_bf16, out_bf16):
+    import torch
+    import selective_state_space_160_b300 as msc
+    x, w, bias = _data(batch, dim, L, K, 900 + batch + dim + L + K, in_bf16)
+    out = msc.msc_causal_conv1d_fwd(to_dev(x, in_bf16), to_dev(w), to_dev(bias),
+                                    out_dtype=torch.bfloat16 if out_bf16 else torch.float32)
+    ref = oracle.causal_conv1d(x, w, bias)
+    if out_bf16:
+        assert bf16_match(_out_np(out), ref) <= 1.0
+    else:
+        assert max_rel_err(_out_np(out), ref) <= 1e-4
+
+
+@pytest.mark.parametrize("silu,with_bias", [(False, True), (True, False), (False, False)])
+def test_forward_options(silu, with_bias):
+    import selective_state_space_160_b300 as msc
+    x, w, bias = _data(2, 24, 64, 4, 950, False)
+    b = bias if with_bias else None
+    out = msc.msc_causal_conv1d_fwd(to_dev(x), to_dev(w), to_dev(b), silu=silu)
+    assert max_rel_err(_out_np(out), oracle.causal_conv1d(x, w, b, silu=silu)) <= 1e-4
+
+
+@pytest.mark.parametrize("K", [4, 1, 6])
+def test_update_chain_matches_forward(K):
+    """Decode steps from a zero state reproduce the sequence convolution and
+    leave the last K - 1 inputs in the state."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    x, w, bias = _data(2, 33, 20, K, 960 + K, True)
+    state = torch.zeros((2, 33, K - 1), dtype=torch.float32, device="cuda")
+    outs = []
+    for t in range(20):
+        o = msc.msc_causal_conv1d_update(to_dev(np.ascontiguousarray(x[:, :, t]), True), state, to_dev(w),
+                                         to_dev(bias), out_dtype=torch.float32)
+        outs.append(_out_np(o))
+    ref = oracle.causal_conv1d(x, w, bias)
+    assert max_rel_err(np.stack(outs, axis=2), ref) <= 1e-4
+    if K > 1:
+        np.testing.assert_array_equal(state.cpu().numpy(), x[:, :, 20 - (K - 1):])
+
+
+def test_feeds_the_scan():
+    """conv1d (bf16 out) -> S6 forward equals the oracle chain on the same values."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    from selective_state_space_160_b300.inputs import s6_inputs
+    inp = s6_inputs(2, 32, 128, 16, seed=970, bf16=True)
+    x, w, bias = _data(2, 32, 128, 4, 971, True)
+    u = msc.msc_causal_conv1d_fwd(to_dev(x, True), to_dev(w), to_dev(bias), out_dtype=torch.bfloat16)
+    dev = {k: to_dev(inp[k], True) for k in ("delta", "z", "B", "C")}
+    y = msc.msc_selective_scan_fwd(u, dev["delta"], to_dev(inp["A"]), dev["B"], dev["C"], to_dev(inp["D"]),
+                                   dev["z"], to_dev(inp["delta_bias"]))
+    u_ref = _out_np(u)                       # the bf16 values the scan consumed
+    assert bf16_match(u_ref, oracle.causal_conv1d(x, w, bias)) <= 1.0
+    ref = oracle.s6_fwd(u_ref, inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["delta_bias"])
+    assert max_rel_err(y.cpu().numpy(), ref) <= 2e-3
+
+
+def test_conv_config_full_size_sampled():
+    """batch 8 x D 5120 x L 2048, K 4, bf16 in and out: the launch the bench
+    times.  Channels 0, 1, 2047 and 5119 of every batch entry are checked."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    x, w, bias = _data(8, 5120, 2048, 4, 160_006, True)
+    out = msc.msc_causal_conv1d_fwd(to_dev(x, True), to_dev(w), to_dev(bias), out_dtype=torch.bfloat16)
+    got = _out_np(out)
+    ds = [0, 1, 2047, 5119]
+    ref = oracle.causal_conv1d(x[:, ds], w[ds], bias[ds])
+    assert bf16_match(got[:, ds], ref) <= 1.0
+    assert np.all(np.isfinite(got))

@@ -408,6 +408,51 @@ def test_p9_decode_step_from_zero_is_first_scan_step():
     assert h.shape == (1, 3, 8)
 
 
+# ---------------------------------------------------------------------------- P10
+@pytest.mark.parametrize("K", [1, 3, 4, 8])
+def test_p10_conv1d_is_numpy_convolve(K):
+    """Without the activation the causal conv of every channel is numpy's full
+    convolution with the reversed kernel, first L outputs, plus the bias."""
+    rng = np.random.default_rng(60 + K)
+    x = rng.standard_normal((2, 3, 37))
+    w = rng.standard_normal((3, K))
+    bias = rng.standard_normal(3)
+    out = oracle.causal_conv1d(x, w, bias, silu=False)
+    for b in range(2):
+        for d in range(3):
+            ref = np.convolve(x[b, d], w[d][::-1])[:37] + bias[d]
+            np.testing.assert_allclose(out[b, d], ref, rtol=1e-13, atol=1e-13)
+
+
+def test_p10_conv1d_causal_and_silu():
+    rng = np.random.default_rng(70)
+    x = rng.standard_normal((1, 4, 20))
+    w = rng.standard_normal((4, 4))
+    y0 = oracle.causal_conv1d(x, w)
+    x2 = x.copy()
+    x2[:, :, 11] += 5.0
+    y1 = oracle.causal_conv1d(x2, w)
+    np.testing.assert_array_equal(y0[:, :, :11], y1[:, :, :11])       # no output before the change moves
+    assert np.all(y0[:, :, 11] != y1[:, :, 11])
+    pre = oracle.causal_conv1d(x, w, silu=False)
+    np.testing.assert_allclose(y0, pre * 0.5 * (1.0 + np.tanh(0.5 * pre)), rtol=1e-13, atol=1e-15)
+
+
+def test_p10_conv1d_update_chain_equals_sequence():
+    rng = np.random.default_rng(71)
+    x = rng.standard_normal((2, 5, 12))
+    w = rng.standard_normal((5, 4))
+    bias = rng.standard_normal(5)
+    ref = oracle.causal_conv1d(x, w, bias)
+    state = np.zeros((2, 5, 3))
+    outs = []
+    for t in range(12):
+        o, state = oracle.causal_conv1d_update(x[:, :, t], state, w, bias)
+        outs.append(o)
+    np.testing.assert_allclose(np.stack(outs, axis=2), ref, rtol=1e-13, atol=1e-14)
+    np.testing.assert_array_equal(state, x[:, :, -3:])
+
+
 # ------------------------------------------------------------------ planted mistakes
 MUTATIONS = [
     # (description, original text, mutated text)
