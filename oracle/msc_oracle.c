@@ -145,6 +145,81 @@ int oracle_s6_fwd(int64_t batch, int64_t dim, int64_t L, int64_t N,
  * Per-row outputs: du, ddelta, dz [L]; dA_row [N]; *dD_row, *dbias_row.
  * Contributions to the channel-shared grads are ADDED into dB_acc, dC_acc [N, L].
  * hs: scratch (L + 1) * N doubles; lam: scratch N doubles. */
+/* S6 forward with another discretisation of the input term; decay, readout,
+ * skip and gate as in oracle_s6_fwd_row.
+ *  disc 1, zero-order hold ("Mamba 解密" sec. 3 and sec. 5): with the input held
+ *    constant over the step, B-bar = (Delta A)^-1 (exp(Delta A) - 1) Delta B, so the
+ *    input term is expm1(Delta A_n) / A_n * B_n u (Delta B_n u when A_n = 0).
+ *  disc 2, exponential-trapezoidal ("Mamba 解密" sec. 6.3):
+ *    h_t = Abar_t h_{t-1} + 1/2 (Bbar_t x_t + Abar_t Bbar_{t-1} x_{t-1}),
+ *    read with Bbar_t x_t = Delta_t B_t u_t (the exponential-Euler input term of
+ *    sec. 6.3) and no input term before t = 0.
+ * eprev: N doubles of scratch. */
+void oracle_s6_fwd_disc_row(int disc, int64_t L, int64_t N,
+                            const double* u, const double* delta, const double* A,
+                            const double* B, const double* C,
+                            double D, const double* z, double bias,
+                            const double* h0, double* y, double* h_last, double* h, double* eprev) {
+    for (int64_t n = 0; n < N; ++n) {
+        h[n] = h0 ? h0[n] : 0.0;
+        eprev[n] = 0.0;
+    }
+    for (int64_t t = 0; t < L; ++t) {
+        double dt = softplus_d(delta[t] + bias);
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double abar = exp(dt * A[n]);
+            double bu = B[n * L + t] * u[t];
+            double in;
+            if (disc == 1) {
+                in = (A[n] != 0.0 ? expm1(dt * A[n]) / A[n] : dt) * bu;
+            } else {
+                double e = dt * bu;
+                in = 0.5 * (e + abar * eprev[n]);
+                eprev[n] = e;
+            }
+            h[n] = abar * h[n] + in;
+            acc += C[n * L + t] * h[n];
+        }
+        acc += D * u[t];
+        if (z) acc *= z[t] * sigmoid_d(z[t]);
+        y[t] = acc;
+    }
+    if (h_last)
+        for (int64_t n = 0; n < N; ++n) h_last[n] = h[n];
+}
+
+int oracle_s6_fwd_disc(int disc, int64_t batch, int64_t dim, int64_t L, int64_t N,
+                       const double* u, const double* delta, const double* A,
+                       const double* B, const double* C, const double* D,
+                       const double* z, const double* delta_bias, const double* h0,
+                       double* y, double* h_last) {
+    if (disc != 1 && disc != 2) return 2;
+    int64_t rows = batch * dim;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* h = (double*)malloc(sizeof(double) * (size_t)(2 * (N > 0 ? N : 1)));
+        if (!h) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < rows; ++r) {
+                int64_t b = r / dim, d = r % dim;
+                oracle_s6_fwd_disc_row(disc, L, N, u + r * L, delta + r * L, A + d * N,
+                                       B + b * N * L, C + b * N * L,
+                                       D ? D[d] : 0.0, z ? z + r * L : NULL,
+                                       delta_bias ? delta_bias[d] : 0.0,
+                                       h0 ? h0 + r * N : NULL, y + r * L,
+                                       h_last ? h_last + r * N : NULL, h, h + N);
+            }
+            free(h);
+        }
+    }
+    return err;
+}
+
 void oracle_s6_bwd_row(int64_t L, int64_t N,
                        const double* u, const double* delta, const double* A,
                        const double* B, const double* C,

@@ -48,6 +48,8 @@ def _load():
             lib.oracle_s6_fwd.restype = ctypes.c_int
             lib.oracle_s6_bwd.argtypes = [_i64] * 4 + [_dp] * 17
             lib.oracle_s6_bwd.restype = ctypes.c_int
+            lib.oracle_s6_fwd_disc.argtypes = [ctypes.c_int] + [_i64] * 4 + [_dp] * 11
+            lib.oracle_s6_fwd_disc.restype = ctypes.c_int
             lib.oracle_ssd_fwd.argtypes = [_i64] * 6 + [_dp] * 10
             lib.oracle_ssd_fwd.restype = ctypes.c_int
             lib.oracle_num_threads.restype = ctypes.c_int
@@ -93,6 +95,33 @@ def s6_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None,
                                _ptr(y), _ptr(h_last))
     if rc:
         raise MemoryError("oracle_s6_fwd failed")
+    return (y, h_last) if return_last_state else y
+
+
+DISC_EULER, DISC_ZOH, DISC_TRAPEZOID = 0, 1, 2
+
+
+def s6_fwd_disc(disc, u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None,
+                return_last_state=False):
+    """S6 forward with the input term discretised by zero-order hold (disc 1,
+    "Mamba 解密" sec. 3 / sec. 5) or by the exponential-trapezoidal rule (disc 2,
+    "Mamba 解密" sec. 6.3); disc 0 is the exponential-Euler s6_fwd.  Same
+    shapes and results as s6_fwd."""
+    if disc == DISC_EULER:
+        return s6_fwd(u, delta, A, B, C, D, z, delta_bias, h0, return_last_state)
+    u, delta, A, B, C = map(_f64, (u, delta, A, B, C))
+    D, z, delta_bias, h0 = map(_f64, (D, z, delta_bias, h0))
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    assert delta.shape == u.shape and A.shape == (dim, N)
+    assert B.shape == (batch, N, L) and C.shape == (batch, N, L)
+    y = np.empty((batch, dim, L), np.float64)
+    h_last = np.empty((batch, dim, N), np.float64)
+    rc = _load().oracle_s6_fwd_disc(int(disc), batch, dim, L, N, _ptr(u), _ptr(delta), _ptr(A), _ptr(B),
+                                    _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0), _ptr(y),
+                                    _ptr(h_last))
+    if rc:
+        raise ValueError("oracle_s6_fwd_disc failed (%d)" % rc)
     return (y, h_last) if return_last_state else y
 
 

@@ -453,6 +453,85 @@ def test_p10_conv1d_update_chain_equals_sequence():
     np.testing.assert_array_equal(state, x[:, :, -3:])
 
 
+# ---------------------------------------------------------------------------- P11
+def _delta_for(dt):
+    """pre-activation delta whose softplus is dt (bias 0)"""
+    return np.log(np.expm1(np.asarray(dt, np.float64)))
+
+
+def test_p11_zoh_is_the_exact_held_input_step():
+    """Zero-order hold: with u, B held over each step, the discrete state equals
+    the continuous system dh/ds = A h + B u integrated by scipy's ODE solver."""
+    from scipy.integrate import solve_ivp
+    rng = np.random.default_rng(80)
+    N, L = 3, 5
+    A = np.array([[-0.5, -2.0, -7.0]])
+    dts = rng.uniform(0.05, 0.4, L)
+    u = rng.standard_normal(L)
+    B = rng.standard_normal((N, L))
+    C = rng.standard_normal((N, L))
+    h0 = rng.standard_normal(N)
+    y, hl = oracle.s6_fwd_disc(oracle.DISC_ZOH, u[None, None], _delta_for(dts)[None, None], A, B[None],
+                               C[None], h0=h0[None, None], return_last_state=True)
+    h = h0.copy()
+    for t in range(L):
+        sol = solve_ivp(lambda s, v: A[0] * v + B[:, t] * u[t], (0.0, dts[t]), h, rtol=1e-12, atol=1e-14,
+                        method="DOP853")
+        h = sol.y[:, -1]
+        assert abs(y[0, 0, t] - np.dot(C[:, t], h)) <= 1e-9 * (1 + abs(y[0, 0, t]))
+    np.testing.assert_allclose(hl[0, 0], h, rtol=1e-9, atol=1e-12)
+
+
+def test_p11_zoh_tends_to_euler_as_a_vanishes():
+    inp = s6_inputs(1, 3, 20, 4, seed=81)
+    A = np.full((3, 4), -1e-9)
+    args = (inp["u"], inp["delta"], A, inp["B"], inp["C"], inp["D"], inp["z"], inp["delta_bias"])
+    np.testing.assert_allclose(oracle.s6_fwd_disc(oracle.DISC_ZOH, *args), oracle.s6_fwd(*args),
+                               rtol=1e-7, atol=1e-9)
+
+
+# ---------------------------------------------------------------------------- P12
+def _order_study(disc, steps):
+    """error at s = 2 of the discretised dh/ds = -1.3 h + 0.7 (1 - cos s), h(0) = 0,
+    sampled at s_t = t * 2 / steps (the input vanishes before s = 0)"""
+    from scipy.integrate import solve_ivp
+    exact = solve_ivp(lambda s, v: -1.3 * v + 0.7 * (1 - np.cos(s)), (0.0, 2.0), [0.0], rtol=1e-13,
+                      atol=1e-15, method="DOP853").y[0, -1]
+    errs = []
+    for T in steps:
+        dt = 2.0 / T
+        s_t = dt * np.arange(T + 1)
+        L = T + 1
+        y = oracle.s6_fwd_disc(disc, (1 - np.cos(s_t))[None, None], np.full((1, 1, L), _delta_for(dt)),
+                               np.array([[-1.3]]), np.full((1, 1, L), 0.7), np.ones((1, 1, L)))
+        errs.append(abs(y[0, 0, -1] - exact))
+    return errs
+
+
+def test_p12_trapezoid_is_second_order_euler_first_order():
+    """The exponential-trapezoidal input rule (Mamba 解密 sec. 6.3) converges with
+    order 2 in the step, the exponential-Euler rule with order 1."""
+    steps = (50, 100, 200, 400)
+    et = _order_study(oracle.DISC_TRAPEZOID, steps)
+    ee = _order_study(oracle.DISC_EULER, steps)
+    for a, b in zip(et, et[1:]):
+        assert 3.7 < a / b < 4.3, et
+    for a, b in zip(ee, ee[1:]):
+        assert 1.8 < a / b < 2.2, ee
+    assert et[-1] < ee[-1] / 100
+
+
+def test_p12_trapezoid_constant_input_steady_state():
+    """Constant Delta, B, u: the trapezoidal state tends to the fixed point
+    h* = (1/2) Delta B u (1 + abar) / (1 - abar)."""
+    dt, A, Bv, uv, L = 0.1, -2.0, 0.6, 1.5, 400
+    y, hl = oracle.s6_fwd_disc(oracle.DISC_TRAPEZOID, np.full((1, 1, L), uv), np.full((1, 1, L), _delta_for(dt)),
+                               np.array([[A]]), np.full((1, 1, L), Bv), np.ones((1, 1, L)),
+                               return_last_state=True)
+    ab = np.exp(dt * A)
+    assert abs(hl[0, 0, 0] - 0.5 * dt * Bv * uv * (1 + ab) / (1 - ab)) < 1e-12
+
+
 # ------------------------------------------------------------------ planted mistakes
 MUTATIONS = [
     # (description, original text, mutated text)
@@ -470,6 +549,11 @@ MUTATIONS = [
      "dA_row[n] += l * dt * abar * hs[(t + 1) * N + n];"),
     ("ssd: decay index off by one", "double hv = a * H[p * N + n] + dt * xp * B[t * sb + n];",
      "double hv = a * H[p * N + n] + dt * xp * B[(t > 0 ? t - 1 : t) * sb + n];"),
+    ("zoh: divided by Delta A instead of A", "in = (A[n] != 0.0 ? expm1(dt * A[n]) / A[n] : dt) * bu;",
+     "in = (A[n] != 0.0 ? expm1(dt * A[n]) / (dt * A[n]) : dt) * bu;"),
+    ("trapezoid: previous term without decay", "in = 0.5 * (e + abar * eprev[n]);",
+     "in = 0.5 * (e + eprev[n]);"),
+    ("trapezoid: no halving", "in = 0.5 * (e + abar * eprev[n]);", "in = e + abar * eprev[n];"),
 ]
 
 
@@ -489,7 +573,10 @@ def test_planted_mistakes(tmp_path, desc, orig, mut, monkeypatch):
     caught = False
     for pin in (lambda: test_p1_closed_form(True, True, True),
                 lambda: test_p5_finite_differences_full(),
-                lambda: test_p4_ssd_materialised_and_s6_equivalence()):
+                lambda: test_p4_ssd_materialised_and_s6_equivalence(),
+                lambda: test_p11_zoh_is_the_exact_held_input_step(),
+                lambda: test_p12_trapezoid_is_second_order_euler_first_order(),
+                lambda: test_p12_trapezoid_constant_input_steady_state()):
         try:
             pin()
         except AssertionError:
