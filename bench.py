@@ -255,6 +255,33 @@ def leg_fwd_long(peaks, pipes, steps=3, warmup=1):
     return res
 
 
+def leg_disc(peaks, pipes, steps=10, warmup=3):
+    """The headline forward (batch 8, D 5120, L 2048, N 16, bf16) with the
+    zero-order-hold and exponential-trapezoidal input terms.  FP32 work per
+    (element, state): ZOH 12 (decay argument, series and direct phi, input term,
+    recurrence, readout), trapezoid 5 (one extra add), Euler 4."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    batch, dim, L, N = 8, 5120, 2048, 16
+    inp = s6_fwd_workload(batch, dim, L, N, True, 160_001)
+    y = torch.empty((batch, dim, L), dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+    el = batch * dim * L
+    nbytes = el * 10 + 2 * batch * N * L * 2
+    res = {}
+    for name, disc, ops in (("zoh", msc.MSC_DISC_ZOH, 12.0), ("trapezoid", msc.MSC_DISC_TRAPEZOID, 5.0)):
+        def fn():
+            msc.msc_selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                       inp["z"], inp["delta_bias"], y=y, disc=disc)
+        ms = statistics.median(time_launches(fn, steps, warmup, st))
+        res[name] = {"workload": "S6 fwd %s, batch 8, D 5120, L 2048, N 16, bf16 in / fp32 y" % name,
+                     "elements_per_s": el / (ms * 1e-3), "ms": ms,
+                     "roofline": roofline_s6(el, N, nbytes, ms, peaks, pipes, fp32_per_elem_n=ops)}
+    del inp, y
+    torch.cuda.empty_cache()
+    return res
+
+
 def leg_bwd(peaks, pipes, steps=5, warmup=2):
     import torch
     import selective_state_space_160_b300 as msc
@@ -562,7 +589,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         for name in args.legs.split(","):
             try:
-                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "decode": leg_decode, "conv1d": leg_conv1d}[name]
+                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "decode": leg_decode, "conv1d": leg_conv1d, "disc": leg_disc}[name]
                 legs[name] = fn(peaks, pipes)
             except Exception as ex:  # report, do not hide: a failing leg is printed as such
                 legs[name] = {"error": "%s: %s" % (type(ex).__name__, ex)}
@@ -603,7 +630,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="fwd_long,bwd,ssd,decode,conv1d")
+    ap.add_argument("--legs", default="fwd_long,bwd,ssd,decode,conv1d,disc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)

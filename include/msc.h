@@ -80,6 +80,31 @@ msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, in
                                   float* y, float* h_last,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* --------------------------------------- S6 forward, other discretisations
+ * The same forward with the input term of h_t = abar_t h_{t-1} + b_t chosen by
+ * `disc` (abar_t = exp(Delta_t A) in every form):
+ *  - MSC_DISC_EULER: b_t = Delta_t B_t u_t, exactly msc_selective_scan_fwd
+ *    ("Mamba 解密" sec. 6.3: Mamba-1/2 are exponential-Euler);
+ *  - MSC_DISC_ZOH: zero-order hold, b_t = (Delta_t A)^-1 (exp(Delta_t A) - 1)
+ *    Delta_t B_t u_t ("Mamba 解密" sec. 3 and sec. 5);
+ *  - MSC_DISC_TRAPEZOID: exponential-trapezoidal (Mamba-3, "Mamba 解密" sec. 6.3),
+ *    b_t = 1/2 (Delta_t B_t u_t + abar_t Delta_{t-1} B_{t-1} u_{t-1}), with no
+ *    input term before t = 0 (h0, if given, is the state only).
+ * Arguments, workspace (msc_selective_scan_fwd_workspace_size) and errors as
+ * msc_selective_scan_fwd.  The ZOH and trapezoidal forms need 16-byte row
+ * strides (seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) and return
+ * MSC_ERR_UNSUPPORTED otherwise; no backward is provided for them.
+ */
+typedef enum { MSC_DISC_EULER = 0, MSC_DISC_ZOH = 1, MSC_DISC_TRAPEZOID = 2 } msc_discretization;
+
+msc_status msc_selective_scan_fwd_ex(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                     msc_dtype in_dtype, msc_discretization disc,
+                                     const void* u, const void* delta, const float* A,
+                                     const void* B, const void* C, const float* D,
+                                     const void* z, const float* delta_bias, const float* h0,
+                                     float* y, float* h_last,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* -------------------------------------------- S6 forward without allocation
  * No counterpart on the pages: an interface for callers that cannot allocate
  * device memory -- a plugin inside a host framework that owns every device

@@ -16,7 +16,8 @@ import threading
 __all__ = [
     "load_library", "library_path",
     "msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd", "msc_selective_state_update",
-    "msc_causal_conv1d_fwd", "msc_causal_conv1d_update",
+    "msc_causal_conv1d_fwd", "msc_causal_conv1d_update", "msc_selective_scan_fwd_ex",
+    "MSC_DISC_EULER", "MSC_DISC_ZOH", "MSC_DISC_TRAPEZOID",
     "msc_selective_scan_fwd_workspace_size", "msc_selective_scan_bwd_workspace_size",
     "msc_ssd_chunked_fwd_workspace_size", "msc_check_device_status", "msc_status_string",
     "msc_last_error", "MscError", "MSC_F32", "MSC_BF16",
@@ -29,6 +30,7 @@ _lib = None
 
 MSC_OK, MSC_ERR_INVALID_ARG, MSC_ERR_UNSUPPORTED, MSC_ERR_CUDA, MSC_ERR_TIMEOUT, MSC_ERR_WORKSPACE = range(6)
 MSC_F32, MSC_BF16 = 0, 1
+MSC_DISC_EULER, MSC_DISC_ZOH, MSC_DISC_TRAPEZOID = 0, 1, 2
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -42,6 +44,7 @@ SIGNATURES = {
     "msc_selective_scan_bwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 9 + [_vp] * 8 + [_vp, _sz, _vp]),
     "msc_ssd_chunked_fwd_workspace_size": (_sz, [_i64] * 7),
     "msc_ssd_chunked_fwd": (ctypes.c_int, [_i64] * 7 + [ctypes.c_int] + [_vp] * 10 + [_vp, _sz, _vp]),
+    "msc_selective_scan_fwd_ex": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] * 2 + [_vp] * 11 + [_vp, _sz, _vp]),
     "msc_selective_scan_fwd_noalloc": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 11 + [_vp]),
     "msc_selective_state_update": (ctypes.c_int, [_i64] * 3 + [ctypes.c_int] + [_vp] * 10 + [_vp]),
     "msc_causal_conv1d_fwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] * 2 + [_vp] * 3 + [ctypes.c_int] + [_vp, _vp]),
@@ -164,10 +167,12 @@ def msc_selective_scan_bwd_workspace_size(batch, dim, seqlen, dstate) -> int:
 
 
 def msc_selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None,
-                           return_last_state=False, y=None, workspace=None, stream=None):
+                           return_last_state=False, y=None, workspace=None, stream=None, disc=MSC_DISC_EULER):
     """S6 forward.  u, delta, z: [batch, dim, L] (fp32 or bf16, all the same);
     B, C: [batch, N, L] (same dtype); A: [dim, N] fp32; D, delta_bias: [dim] fp32;
-    h0: [batch, dim, N] fp32.  Returns y [batch, dim, L] fp32 (and h_last)."""
+    h0: [batch, dim, N] fp32.  Returns y [batch, dim, L] fp32 (and h_last).
+    disc: MSC_DISC_EULER (msc_selective_scan_fwd), MSC_DISC_ZOH or
+    MSC_DISC_TRAPEZOID (msc_selective_scan_fwd_ex)."""
     torch = _torch()
     lib = load_library()
     batch, dim, L = u.shape
@@ -188,10 +193,12 @@ def msc_selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h
     h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device) if return_last_state else None
     nbytes = msc_selective_scan_fwd_workspace_size(batch, dim, L, N)
     ws, wsb = _workspace(nbytes, u.device, workspace)
-    st = lib.msc_selective_scan_fwd(batch, dim, L, N, dt, *args,
-                                    _dev_ptr(y, "y", torch.float32, (batch, dim, L)),
-                                    _dev_ptr(h_last, "h_last", optional=True),
-                                    ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream))
+    tail = (_dev_ptr(y, "y", torch.float32, (batch, dim, L)), _dev_ptr(h_last, "h_last", optional=True),
+            ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream))
+    if disc == MSC_DISC_EULER:
+        st = lib.msc_selective_scan_fwd(batch, dim, L, N, dt, *args, *tail)
+    else:
+        st = lib.msc_selective_scan_fwd_ex(batch, dim, L, N, dt, int(disc), *args, *tail)
     _check(st)
     return (y, h_last) if return_last_state else y
 

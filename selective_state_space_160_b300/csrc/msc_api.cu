@@ -137,15 +137,17 @@ size_t msc_selective_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t
     return s6_fwd_plan(batch, dim, seqlen, dstate).workspace;
 }
 
-msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
-                                  msc_dtype in_dtype, const void* u, const void* delta,
-                                  const float* A, const void* B, const void* C, const float* D,
-                                  const void* z, const float* delta_bias, const float* h0,
-                                  float* y, float* h_last, void* workspace,
-                                  size_t workspace_bytes, void* stream) {
+msc_status msc_selective_scan_fwd_ex(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                     msc_dtype in_dtype, msc_discretization disc, const void* u,
+                                     const void* delta, const float* A, const void* B, const void* C,
+                                     const float* D, const void* z, const float* delta_bias, const float* h0,
+                                     float* y, float* h_last, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
     clear_error();
     msc_status s = check_s6_dims(batch, dim, seqlen, dstate, in_dtype);
     if (s != MSC_OK) return s;
+    MSC_REQUIRE(disc == MSC_DISC_EULER || disc == MSC_DISC_ZOH || disc == MSC_DISC_TRAPEZOID,
+                "disc must be MSC_DISC_EULER, MSC_DISC_ZOH or MSC_DISC_TRAPEZOID");
     MSC_PTR(u, "u"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A"); MSC_PTR(B, "B");
     MSC_PTR(C, "C"); MSC_PTR(y, "y");
     MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z"); MSC_OPT_PTR(delta_bias, "delta_bias");
@@ -162,6 +164,7 @@ msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, in
     a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C;
     a.A = A; a.D = D; a.delta_bias = delta_bias; a.h0 = h0; a.y = y; a.h_last = h_last;
     a.workspace = workspace;
+    a.disc = (int)disc;
     return s6_fwd_launch(a, plan, static_cast<cudaStream_t>(stream));
 }
 
@@ -223,6 +226,16 @@ msc_status msc_causal_conv1d_update(int64_t batch, int64_t dim, int64_t width, m
     a.in_bf16 = in_dtype == MSC_BF16; a.out_bf16 = out_dtype == MSC_BF16;
     a.x = x; a.weight = weight; a.bias = bias; a.out = out; a.state = conv_state;
     return conv1d_update_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                  msc_dtype in_dtype, const void* u, const void* delta,
+                                  const float* A, const void* B, const void* C, const float* D,
+                                  const void* z, const float* delta_bias, const float* h0,
+                                  float* y, float* h_last, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    return msc_selective_scan_fwd_ex(batch, dim, seqlen, dstate, in_dtype, MSC_DISC_EULER, u, delta, A, B, C, D,
+                                     z, delta_bias, h0, y, h_last, workspace, workspace_bytes, stream);
 }
 
 size_t msc_selective_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,

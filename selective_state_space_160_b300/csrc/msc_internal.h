@@ -25,6 +25,7 @@ struct S6FwdArgs {
     const float *A, *D, *delta_bias, *h0;
     float *y, *h_last;
     void* workspace;
+    int disc = 0;  // msc_discretization
 };
 
 msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t stream);

@@ -53,6 +53,8 @@ constexpr int kNS = 16;    // state slots per lane (dstate <= 16)
 constexpr int kStride = kT + 4;
 
 enum { kModeFull = 0, kModeAgg = 1, kModeCkpt = 2 };
+// input-term discretisation (values of msc_discretization)
+enum { kDiscEuler = 0, kDiscZoh = 1, kDiscTrap = 2 };
 
 __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
@@ -346,7 +348,18 @@ __device__ __forceinline__ void reduce_scatter_level(float* v, int j) {
 // store) of steps j * 8 / kNG .. of every 8-step group.  Per-step scalars are
 // gathered from their owner lane with shuffles; the readout partial sums are
 // reduce-scattered back with a shuffle butterfly.
-template <bool kBF16, int kMode, int kNG>
+//
+// kDisc selects the input term b_t of h_t = abar_t h_{t-1} + b_t:
+//  - exponential Euler: b = Delta B u;
+//  - zero-order hold ("Mamba 解密" sec. 3 / sec. 5): b = phi(Delta A) Delta B u with
+//    phi(x) = expm1(x) / x, taken from its series 1 + x/2 + x^2/6 + x^3/24 when
+//    |x| < 0.03 (truncation < 1e-8) and from (abar - 1) (1/A) (1/Delta) otherwise
+//    (the rounding of abar then costs < 1e-5 relative); 1/A per state is set up
+//    once and 1/Delta is one reciprocal per step shared by the row's states;
+//  - exponential-trapezoidal ("Mamba 解密" sec. 6.3): b_t = e_t + abar_t e_{t-1}
+//    with e_t = Delta_t B_t u_t / 2, carried per state in registers; a segment's
+//    first step rebuilds e_{t0-1} from the inputs at t0 - 1 (none before t = 0).
+template <bool kBF16, int kMode, int kNG, int kDisc = kDiscEuler>
 __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                                                               const __grid_constant__ CUtensorMap tm_d,
                                                               const __grid_constant__ CUtensorMap tm_z,
@@ -403,6 +416,38 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
     float dsum = 0.f;
 
     const int64_t t_begin = (int64_t)seg * p.seg_len;
+    // zero-order hold: 1/A per state (0 where A = 0: the series branch covers it)
+    uint64_t invA2[kDisc == kDiscZoh ? kPPL : 1];
+    // trapezoid: half input term of the previous step, per state
+    uint64_t ep2[kDisc == kDiscTrap ? kPPL : 1];
+    if constexpr (kDisc == kDiscZoh) {
+#pragma unroll
+        for (int q = 0; q < kPPL; ++q) {
+            float a0, a1;
+            msc::upk2(A2p[q], a0, a1);
+            a0 *= MSC_LN2;
+            a1 *= MSC_LN2;
+            invA2[q] = msc::pk2(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
+        }
+    }
+    if constexpr (kDisc == kDiscTrap) {
+        float eu = 0.f;
+        if (row_ok && t_begin > 0) {
+            const int64_t tp = t_begin - 1;
+            const float dtp = msc::softplus_f(msc::ld_elem<kBF16>(p.delta, row * p.L + tp) + bias);
+            eu = 0.5f * dtp * msc::ld_elem<kBF16>(p.u, row * p.L + tp);
+        }
+#pragma unroll
+        for (int q = 0; q < kPPL; ++q) {
+            float e[2] = {0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int n = 2 * (kPPL * j + q) + k;
+                if (eu != 0.f && n < N) e[k] = eu * msc::ld_elem<kBF16>(p.B, (b * N + n) * p.L + t_begin - 1);
+            }
+            ep2[q] = msc::pk2(e[0], e[1]);
+        }
+    }
     const int64_t t_end = imin64(p.L, t_begin + p.seg_len);
     const int ntiles = (int)((t_end - t_begin + kTT - 1) / kTT);
     const uint32_t tx_bytes = kRowTile * (has_z ? 3 : 2) + kBCTile * (kFull ? 2 : 1);
@@ -503,6 +548,7 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
                 }
                 mdt2[e] = dt;
                 mdtu2[e] = msc::mul2(dt, u2[e]);
+                if constexpr (kDisc == kDiscTrap) mdtu2[e] = msc::mul2(mdtu2[e], msc::pk2(0.5f, 0.5f));
                 mdu2[e] = msc::mul2(msc::pk2(Dd, Dd), u2[e]);
                 if (kMode == kModeAgg) {
                     float a, c;
@@ -554,10 +600,39 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
                     const uint64_t dt2 = msc::pk2(dts[k], dts[k]);
                     const uint64_t dtu2 = msc::pk2(dtus[k], dtus[k]);
                     uint64_t acc_a = 0ull, acc_b = 0ull;
+                    float rdt = 0.f;
+                    if constexpr (kDisc == kDiscZoh) rdt = dts[k] > 0.f ? msc::rcp_approx(dts[k]) : 0.f;
+                    if constexpr (kDisc == kDiscTrap) {
+                        // the first step past the end drops the previous input term
+                        if (partial && k == nt - 8 * g) {
+#pragma unroll
+                            for (int q = 0; q < kPPL; ++q) ep2[q] = 0ull;
+                        }
+                    }
 #pragma unroll
                     for (int q = 0; q < kPPL; ++q) {
-                        const uint64_t a = msc::ex2_2(msc::mul2(dt2, A2p[q]));
-                        h2[q] = msc::fma2(a, h2[q], msc::mul2(dtu2, Bp[q][e]));
+                        const uint64_t arg = msc::mul2(dt2, A2p[q]);
+                        const uint64_t a = msc::ex2_2(arg);
+                        if constexpr (kDisc == kDiscEuler) {
+                            h2[q] = msc::fma2(a, h2[q], msc::mul2(dtu2, Bp[q][e]));
+                        } else if constexpr (kDisc == kDiscZoh) {
+                            const uint64_t x = msc::mul2(arg, msc::pk2(MSC_LN2, MSC_LN2));  // Delta A
+                            uint64_t ps = msc::fma2(x, msc::pk2(1.f / 24.f, 1.f / 24.f), msc::pk2(1.f / 6.f, 1.f / 6.f));
+                            ps = msc::fma2(x, ps, msc::pk2(0.5f, 0.5f));
+                            ps = msc::fma2(x, ps, msc::pk2(1.f, 1.f));
+                            const uint64_t pd = msc::mul2(msc::mul2(msc::add2(a, msc::pk2(-1.f, -1.f)), invA2[q]),
+                                                          msc::pk2(rdt, rdt));
+                            float x0, x1, s0, s1, d0, d1;
+                            msc::upk2(x, x0, x1);
+                            msc::upk2(ps, s0, s1);
+                            msc::upk2(pd, d0, d1);
+                            const uint64_t phi = msc::pk2(fabsf(x0) < 0.03f ? s0 : d0, fabsf(x1) < 0.03f ? s1 : d1);
+                            h2[q] = msc::fma2(a, h2[q], msc::mul2(phi, msc::mul2(dtu2, Bp[q][e])));
+                        } else {
+                            const uint64_t e2 = msc::mul2(dtu2, Bp[q][e]);  // half the Euler term
+                            h2[q] = msc::fma2(a, msc::add2(h2[q], ep2[q]), e2);
+                            ep2[q] = e2;
+                        }
                         if (kFull) {
                             if (q == 0) acc_a = msc::mul2(Cp[q][e], h2[q]);
                             else if (q == 1) acc_b = msc::mul2(Cp[q][e], h2[q]);
@@ -714,20 +789,25 @@ bool make_maps(FwdMaps& m, const FwdParams& p, int64_t batch, bool bf16) {
 // warps but add more exchange work than the extra latency hiding recovers.
 constexpr int kLanesPerRow = 2;
 
-template <bool kBF16, int kNG>
+template <bool kBF16, int kNG, int kDisc = kDiscEuler>
 msc_status launch_tma_ng(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
     if (mode == kModeFull)
-        s6_fwd_tma_kernel<kBF16, kModeFull, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+        s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
     else if (mode == kModeAgg)
-        s6_fwd_tma_kernel<kBF16, kModeAgg, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
-    else
+        s6_fwd_tma_kernel<kBF16, kModeAgg, kNG, kDisc><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    else if (kDisc == kDiscEuler)
         s6_fwd_tma_kernel<kBF16, kModeCkpt, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    else
+        return msc_host::fail(MSC_ERR_UNSUPPORTED, "checkpoints are kept for the exponential-Euler form only");
     return msc_host::check_launch("s6_fwd_tma");
 }
 
 template <bool kBF16>
-msc_status launch_tma(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
+msc_status launch_tma(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, int disc,
+                      cudaStream_t st) {
+    if (disc == kDiscZoh) return launch_tma_ng<kBF16, kLanesPerRow, kDiscZoh>(m, p, batch, G, mode, st);
+    if (disc == kDiscTrap) return launch_tma_ng<kBF16, kLanesPerRow, kDiscTrap>(m, p, batch, G, mode, st);
     return launch_tma_ng<kBF16, kLanesPerRow>(m, p, batch, G, mode, st);
 }
 
@@ -737,8 +817,14 @@ bool tma_ok(const FwdParams& p, bool bf16) {
 }
 
 msc_status launch_mode(const FwdParams& p, const FwdMaps* maps, bool bf16, bool vec, int64_t batch, int G,
-                       int mode, cudaStream_t st) {
-    if (maps) return bf16 ? launch_tma<true>(*maps, p, batch, G, mode, st) : launch_tma<false>(*maps, p, batch, G, mode, st);
+                       int mode, int disc, cudaStream_t st) {
+    if (maps)
+        return bf16 ? launch_tma<true>(*maps, p, batch, G, mode, disc, st)
+                    : launch_tma<false>(*maps, p, batch, G, mode, disc, st);
+    if (disc != kDiscEuler)
+        return msc_host::fail(MSC_ERR_UNSUPPORTED,
+                              "the zero-order-hold and trapezoidal forms need 16-byte row strides "
+                              "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32)");
     if (bf16) return vec ? launch_rows<true, true>(p, batch, G, mode, st) : launch_rows<true, false>(p, batch, G, mode, st);
     return vec ? launch_rows<false, true>(p, batch, G, mode, st) : launch_rows<false, false>(p, batch, G, mode, st);
 }
@@ -794,7 +880,7 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
         size_t off = (size_t)(a.batch * a.dim) * plan.G * a.N * sizeof(float);
         off = (off + 255) / 256 * 256;
         p.seg_dsum = reinterpret_cast<float*>(ws + off);
-        msc_status s = launch_mode(p, mp, a.bf16, vec, a.batch, plan.G - 1, kModeAgg, st);
+        msc_status s = launch_mode(p, mp, a.bf16, vec, a.batch, plan.G - 1, kModeAgg, a.disc, st);
         if (s != MSC_OK) return s;
         const int64_t total = a.batch * a.dim * a.N;
         const int threads = 256;
@@ -803,7 +889,7 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
         s = check_launch("s6_seg_carry");
         if (s != MSC_OK) return s;
     }
-    return launch_mode(p, mp, a.bf16, vec, a.batch, plan.G, kModeFull, st);
+    return launch_mode(p, mp, a.bf16, vec, a.batch, plan.G, kModeFull, a.disc, st);
 }
 
 // Checkpoint pass of the backward: the state entering every 8-step group of

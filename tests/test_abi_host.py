@@ -148,3 +148,15 @@ def test_conv1d_rejects_bad_arguments(lib):
     g = lib.msc_causal_conv1d_update
     assert g(1, 4, 4, 1, 1, 16, 16, None, 1, None, 16, None) == msc.MSC_ERR_INVALID_ARG   # state required
     assert "conv_state" in msc.msc_last_error()
+
+
+def test_fwd_ex_rejects_bad_arguments(lib):
+    f = lib.msc_selective_scan_fwd_ex
+
+    def call(L=64, dt=1, disc=1):
+        return f(1, 4, L, 16, dt, disc, 16, 16, 16, 16, 16, None, None, None, None, 16, None, None, 0, None)
+
+    assert call(disc=7) == msc.MSC_ERR_INVALID_ARG
+    assert "disc" in msc.msc_last_error()
+    assert call(L=63, disc=msc.MSC_DISC_ZOH) == msc.MSC_ERR_UNSUPPORTED        # bf16 rows not 16-byte strided
+    assert call(L=66, dt=0, disc=msc.MSC_DISC_TRAPEZOID) == msc.MSC_ERR_UNSUPPORTED
