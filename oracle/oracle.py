@@ -214,3 +214,47 @@ def ssd_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, return_final_sta
     if rc:
         raise ValueError("oracle_ssd_fwd failed (rc=%d)" % rc)
     return (y, fs) if return_final_state else y
+
+
+def ssd_bwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, dy=None):
+    """SSD backward (zero initial state).  The SSD is the S6 scan with channels
+    d = (head, p), Delta and A shared by a head's P channels and B, C shared by
+    a group's heads (bqwf survey sec. 3.2: scalar A_t = alpha_t I); so each
+    gradient is the S6 backward of that problem, summed over the channels that
+    share the parameter: dx = du; ddelta[h] = sum_p ddelta(h, p); dA[h] =
+    sum_{p,n} dA(h, p, n); dD, ddelta_bias likewise; dB, dC per group.
+    Shapes as ssd_fwd; returns a dict dx, ddelta, dA, dB, dC and, when the input
+    is given, dD, dz, ddelta_bias."""
+    x, delta, A, B, C, dy = map(_f64, (x, delta, A, B, C, dy))
+    D, z, delta_bias = map(_f64, (D, z, delta_bias))
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    hpg = H // G
+    out = {"dx": np.empty_like(x), "ddelta": np.empty((batch, L, H)), "dA": np.empty(H),
+           "dB": np.empty_like(B), "dC": np.empty_like(C),
+           "dD": np.empty(H) if D is not None else None, "dz": np.empty_like(x) if z is not None else None,
+           "ddelta_bias": np.empty(H) if delta_bias is not None else None}
+    for g in range(G):
+        heads = list(range(g * hpg, (g + 1) * hpg))
+        u = np.concatenate([x[:, :, h, :].transpose(0, 2, 1) for h in heads], axis=1)
+        dl = np.concatenate([np.repeat(delta[:, None, :, h], P, axis=1) for h in heads], axis=1)
+        dyy = np.concatenate([dy[:, :, h, :].transpose(0, 2, 1) for h in heads], axis=1)
+        zz = None if z is None else np.concatenate([z[:, :, h, :].transpose(0, 2, 1) for h in heads], axis=1)
+        A6 = np.concatenate([np.full((P, N), A[h]) for h in heads], axis=0)
+        D6 = None if D is None else np.concatenate([np.full(P, D[h]) for h in heads])
+        b6 = None if delta_bias is None else np.concatenate([np.full(P, delta_bias[h]) for h in heads])
+        r = s6_bwd(u, dl, A6, B[:, :, g, :].transpose(0, 2, 1), C[:, :, g, :].transpose(0, 2, 1), D6, zz, b6, dyy)
+        out["dB"][:, :, g, :] = r["dB"].transpose(0, 2, 1)
+        out["dC"][:, :, g, :] = r["dC"].transpose(0, 2, 1)
+        for i, h in enumerate(heads):
+            sl = slice(i * P, (i + 1) * P)
+            out["dx"][:, :, h, :] = r["du"][:, sl, :].transpose(0, 2, 1)
+            out["ddelta"][:, :, h] = r["ddelta"][:, sl, :].sum(axis=1)
+            out["dA"][h] = r["dA"][sl].sum()
+            if D is not None:
+                out["dD"][h] = r["dD"][sl].sum()
+            if z is not None:
+                out["dz"][:, :, h, :] = r["dz"][:, sl, :].transpose(0, 2, 1)
+            if delta_bias is not None:
+                out["ddelta_bias"][h] = r["ddelta_bias"][sl].sum()
+    return out

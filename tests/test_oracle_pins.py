@@ -532,6 +532,31 @@ def test_p12_trapezoid_constant_input_steady_state():
     assert abs(hl[0, 0, 0] - 0.5 * dt * Bv * uv * (1 + ab) / (1 - ab)) < 1e-12
 
 
+# ---------------------------------------------------------------------------- P13
+def test_p13_ssd_backward_finite_differences():
+    """The SSD backward (built on the S6 backward through the channel mapping
+    of P4) against central finite differences of <dy, y> of the SSD forward
+    oracle, for every entry of every input (2 groups, all optional inputs)."""
+    inp = ssd_inputs(1, 7, 4, 2, 3, ngroups=2, seed=91, bf16=False, with_z=True)
+    dy = np.random.default_rng(92).standard_normal(inp["x"].shape)
+    keys = ("x", "delta", "A", "B", "C", "D", "z", "delta_bias")
+    base = {k: np.array(inp[k], dtype=np.float64) for k in keys}
+    g = oracle.ssd_bwd(*(base[k] for k in keys), dy=dy)
+
+    def loss(v):
+        return float((oracle.ssd_fwd(*(v[k] for k in keys)) * dy).sum())
+
+    names = {"x": "dx", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "z": "dz",
+             "delta_bias": "ddelta_bias"}
+    eps = 1e-6
+    for k in keys:
+        for idx in np.ndindex(base[k].shape):
+            vp = dict(base); vp[k] = base[k].copy(); vp[k][idx] += eps
+            vm = dict(base); vm[k] = base[k].copy(); vm[k][idx] -= eps
+            fd = (loss(vp) - loss(vm)) / (2 * eps)
+            assert abs(g[names[k]][idx] - fd) <= 1e-6 * max(1.0, abs(fd)), (k, idx, g[names[k]][idx], fd)
+
+
 # ------------------------------------------------------------------ planted mistakes
 MUTATIONS = [
     # (description, original text, mutated text)
