@@ -426,6 +426,70 @@ def leg_ssd(peaks, pipes, steps=5, warmup=2):
     return res
 
 
+def ssd_bwd_macs(b, L, H, G, Q, P=64, N=128, T=64):
+    """Multiply-adds the SSD backward's fp32 tile products execute (per launch):
+    the chunk states, G = C B^T, U, dG, dC / dB from dG, dx and its state terms,
+    and the cross-head state parts of dB, dC.  Masked halves of diagonal tiles
+    are counted, as the kernels compute them."""
+    nc, nb = -(-L // Q), Q // T
+    ntri = nb * (nb + 1) // 2
+    hpg = H // G
+    m = b * nc * H * P * N * Q                          # chunk states (recomputed)
+    m += b * nc * G * ntri * T * T * N                  # G = C B^T
+    m += b * nc * H * P * N * Q                         # U
+    m += b * nc * G * ntri * hpg * T * T * P            # dG over the group's heads
+    m += b * nc * G * ntri * 2 * T * T * N              # dC, dB from dG
+    m += b * nc * H * (ntri * T * T * P + nb * 2 * T * P * N)   # dx: Y_diag and state terms
+    m += b * nc * nb * H * 2 * T * N * P                # state parts of dB, dC
+    return m
+
+
+def leg_ssd_bwd(peaks, pipes, steps=5, warmup=2):
+    import torch
+    import selective_state_space_160_b300 as msc
+    from selective_state_space_160_b300.inputs import ssd_inputs, bf16_bits
+    b, L, H, P, N, Q = 4, 4096, 80, 64, 128, 256
+    inp = ssd_inputs(b, L, H, P, N, 1, seed=160_006, bf16=True, with_dy=True)
+
+    def dev(a, bf):
+        if a is None:
+            return None
+        if bf:
+            return torch.from_numpy(bf16_bits(a).view(np.int16).copy()).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+    d = {k: dev(v, k in ("x", "delta", "B", "C", "z", "dy")) for k, v in inp.items()}
+    nbytes_ws = msc.msc_ssd_chunked_bwd_workspace_size(b, L, H, P, N, 1, Q, False)
+    ws = torch.empty(nbytes_ws + 1024, dtype=torch.uint8, device="cuda")
+    off = (-ws.data_ptr()) % 1024
+    ws = ws[off:off + nbytes_ws]
+    st = torch.cuda.current_stream()
+
+    def fn():
+        msc.msc_ssd_chunked_bwd(d["x"], d["delta"], d["A"], d["B"], d["C"], d["dy"], d["D"], None,
+                                d["delta_bias"], chunk=Q, workspace=ws)
+    ms = statistics.median(time_launches(fn, steps, warmup, st))
+    el = b * L * H * P
+    t = ms * 1e-3
+    macs = ssd_bwd_macs(b, L, H, 1, Q, P, N)
+    nst = b * (L // Q) * H * P * N * 4
+    # inputs x, dy, delta, B, C (bf16) read; dx, ddelta, dB, dC (fp32) written;
+    # S, Hin, U/dS written once and read back
+    nbytes = 2 * el * 2 + b * L * H * 2 + 2 * b * L * N * 2 + el * 4 + b * L * H * 4 + 2 * b * L * N * 4 + 6 * nst
+    alu = {"achieved": macs / t / 1e9, "peak": pipes["ffma"]["ops_per_s"] / 1e9, "unit": "GFMA/s"}
+    hbm = {"achieved": nbytes / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    for v in (alu, hbm):
+        v["frac"] = v["achieved"] / v["peak"]
+    sel = alu if alu["frac"] >= hbm["frac"] else hbm
+    res = {"workload": "SSD bwd batch 4, heads 80, P 64, N 128, L 4096, chunk 256, bf16 in / fp32 grads",
+           "elements_per_s": el / t, "ms": ms,
+           "roofline": {"bound": "alu" if sel is alu else "hbm", "achieved": sel["achieved"], "peak": sel["peak"],
+                        "unit": sel["unit"], "frac": sel["frac"], "traffic": None, "macs": macs,
+                        "terms": {"alu_fp32_fma": alu, "hbm": hbm}}}
+    del d, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- reference arm
 def cpu_oracle_sample(target_s=12.0, max_rows=None):
     """Time the CPU oracle on a bounded sample of the headline workload:
@@ -589,7 +653,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         for name in args.legs.split(","):
             try:
-                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "decode": leg_decode, "conv1d": leg_conv1d, "disc": leg_disc}[name]
+                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "ssd_bwd": leg_ssd_bwd, "decode": leg_decode, "conv1d": leg_conv1d, "disc": leg_disc}[name]
                 legs[name] = fn(peaks, pipes)
             except Exception as ex:  # report, do not hide: a failing leg is printed as such
                 legs[name] = {"error": "%s: %s" % (type(ex).__name__, ex)}
@@ -630,7 +694,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="fwd_long,bwd,ssd,decode,conv1d,disc")
+    ap.add_argument("--legs", default="fwd_long,bwd,ssd,ssd_bwd,decode,conv1d,disc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)

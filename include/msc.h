@@ -223,6 +223,34 @@ msc_status msc_ssd_chunked_fwd(int64_t batch, int64_t seqlen, int64_t nheads, in
                                const float* delta_bias, float* y, float* final_state,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------- SSD chunked bwd
+ * Gradients of msc_ssd_chunked_fwd (zero initial state; final_state is not an
+ * output here), derived from the same chunk decomposition (bqwf survey sec. 3.2:
+ * scalar A_t = alpha_t I; "Mamba 解密" sec. 6.2: the SSD as the masked matrix
+ * Y = M (X . B^T) C).  Inputs as the forward, plus dy [batch, seqlen, nheads,
+ * headdim] bf16.  Outputs (fp32, overwritten): dx [batch, seqlen, nheads,
+ * headdim]; ddelta [batch, seqlen, nheads]; dA [nheads]; dB, dC [batch, seqlen,
+ * ngroups, dstate]; dD [nheads] (required iff D != NULL); dz like dx (required
+ * iff z != NULL); ddelta_bias [nheads] (required iff delta_bias != NULL).
+ * Limits as the forward, and nheads / ngroups a multiple of 16 when ngroups > 1.
+ * With z the pre-gate output is recomputed by the forward into the workspace
+ * (has_z selects the larger workspace).  dB, dC, dA, dD, ddelta_bias and the
+ * cumulative-sum gradients are fp32 atomic sums: their low bits depend on the
+ * order in which blocks finish. */
+size_t msc_ssd_chunked_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
+                                          int64_t headdim, int64_t dstate, int64_t ngroups,
+                                          int64_t chunk, int has_z);
+
+msc_status msc_ssd_chunked_bwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                               int64_t dstate, int64_t ngroups, int64_t chunk,
+                               msc_dtype in_dtype,
+                               const void* x, const void* delta, const float* A,
+                               const void* B, const void* C, const float* D, const void* z,
+                               const float* delta_bias, const void* dy, float* dx, float* ddelta,
+                               float* dA, float* dB, float* dC, float* dD, float* dz,
+                               float* ddelta_bias, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
 /* ------------------------------------------------------------------- utilities
  * msc_check_device_status: synchronises `stream`, then reads and clears the
  * device status words that the library's kernels keep on the current device

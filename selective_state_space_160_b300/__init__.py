@@ -15,7 +15,8 @@ import threading
 
 __all__ = [
     "load_library", "library_path",
-    "msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd", "msc_selective_state_update",
+    "msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd", "msc_ssd_chunked_bwd",
+    "msc_selective_state_update", "msc_ssd_chunked_bwd_workspace_size",
     "msc_causal_conv1d_fwd", "msc_causal_conv1d_update", "msc_selective_scan_fwd_ex",
     "MSC_DISC_EULER", "MSC_DISC_ZOH", "MSC_DISC_TRAPEZOID",
     "msc_selective_scan_fwd_workspace_size", "msc_selective_scan_bwd_workspace_size",
@@ -44,6 +45,8 @@ SIGNATURES = {
     "msc_selective_scan_bwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 9 + [_vp] * 8 + [_vp, _sz, _vp]),
     "msc_ssd_chunked_fwd_workspace_size": (_sz, [_i64] * 7),
     "msc_ssd_chunked_fwd": (ctypes.c_int, [_i64] * 7 + [ctypes.c_int] + [_vp] * 10 + [_vp, _sz, _vp]),
+    "msc_ssd_chunked_bwd_workspace_size": (_sz, [_i64] * 7 + [ctypes.c_int]),
+    "msc_ssd_chunked_bwd": (ctypes.c_int, [_i64] * 7 + [ctypes.c_int] + [_vp] * 8 + [_vp] * 9 + [_vp, _sz, _vp]),
     "msc_selective_scan_fwd_ex": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] * 2 + [_vp] * 11 + [_vp, _sz, _vp]),
     "msc_selective_scan_fwd_noalloc": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 11 + [_vp]),
     "msc_selective_state_update": (ctypes.c_int, [_i64] * 3 + [ctypes.c_int] + [_vp] * 10 + [_vp]),
@@ -362,6 +365,53 @@ def msc_ssd_chunked_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, chun
     if return_workspace:
         return res, ws
     return res
+
+
+def msc_ssd_chunked_bwd_workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups, chunk,
+                                       has_z) -> int:
+    return int(load_library().msc_ssd_chunked_bwd_workspace_size(batch, seqlen, nheads, headdim,
+                                                                 dstate, ngroups, chunk, int(bool(has_z))))
+
+
+def msc_ssd_chunked_bwd(x, delta, A, B, C, dy, D=None, z=None, delta_bias=None, chunk=256,
+                        workspace=None, stream=None):
+    """SSD backward (zero initial state).  Inputs as msc_ssd_chunked_fwd plus
+    dy [batch, L, heads, P] bf16.  Returns a dict of fp32 gradients dx, ddelta,
+    dA, dB, dC and, for the optional inputs given, dD, dz, ddelta_bias."""
+    torch = _torch()
+    lib = load_library()
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dt = _in_dtype(x)
+    tdt = x.dtype
+    f32 = torch.float32
+    dev = x.device
+    g = {"dx": torch.empty((batch, L, H, P), dtype=f32, device=dev),
+         "ddelta": torch.empty((batch, L, H), dtype=f32, device=dev),
+         "dA": torch.empty((H,), dtype=f32, device=dev),
+         "dB": torch.empty((batch, L, G, N), dtype=f32, device=dev),
+         "dC": torch.empty((batch, L, G, N), dtype=f32, device=dev),
+         "dD": torch.empty((H,), dtype=f32, device=dev) if D is not None else None,
+         "dz": torch.empty((batch, L, H, P), dtype=f32, device=dev) if z is not None else None,
+         "ddelta_bias": torch.empty((H,), dtype=f32, device=dev) if delta_bias is not None else None}
+    nbytes = msc_ssd_chunked_bwd_workspace_size(batch, L, H, P, N, G, chunk, z is not None)
+    ws, wsb = _workspace(nbytes, dev, workspace)
+    st = lib.msc_ssd_chunked_bwd(
+        batch, L, H, P, N, G, chunk, dt,
+        _dev_ptr(x, "x"), _dev_ptr(delta, "delta", tdt, (batch, L, H)),
+        _dev_ptr(A, "A", f32, (H,)),
+        _dev_ptr(B, "B", tdt, (batch, L, G, N)), _dev_ptr(C, "C", tdt, (batch, L, G, N)),
+        _dev_ptr(D, "D", f32, (H,), optional=True),
+        _dev_ptr(z, "z", tdt, (batch, L, H, P), optional=True),
+        _dev_ptr(delta_bias, "delta_bias", f32, (H,), optional=True),
+        _dev_ptr(dy, "dy", tdt, (batch, L, H, P)),
+        _dev_ptr(g["dx"], "dx"), _dev_ptr(g["ddelta"], "ddelta"), _dev_ptr(g["dA"], "dA"),
+        _dev_ptr(g["dB"], "dB"), _dev_ptr(g["dC"], "dC"),
+        _dev_ptr(g["dD"], "dD", optional=True), _dev_ptr(g["dz"], "dz", optional=True),
+        _dev_ptr(g["ddelta_bias"], "ddelta_bias", optional=True),
+        ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream))
+    _check(st)
+    return {k: v for k, v in g.items() if v is not None}
 
 
 def msc_check_device_status(stream=None):

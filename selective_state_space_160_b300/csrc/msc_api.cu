@@ -324,6 +324,62 @@ msc_status msc_ssd_chunked_fwd(int64_t batch, int64_t seqlen, int64_t nheads, in
     return ssd_launch(a, static_cast<cudaStream_t>(stream));
 }
 
+size_t msc_ssd_chunked_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
+                                          int64_t headdim, int64_t dstate, int64_t ngroups,
+                                          int64_t chunk, int has_z) {
+    if (batch < 1 || seqlen < 1 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1 ||
+        nheads % ngroups != 0 || chunk < 1)
+        return 0;
+    return ssd_bwd_workspace(batch, seqlen, nheads, ngroups, chunk, has_z != 0);
+}
+
+msc_status msc_ssd_chunked_bwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                               int64_t dstate, int64_t ngroups, int64_t chunk, msc_dtype in_dtype,
+                               const void* x, const void* delta, const float* A, const void* B,
+                               const void* C, const float* D, const void* z,
+                               const float* delta_bias, const void* dy, float* dx, float* ddelta,
+                               float* dA, float* dB, float* dC, float* dD, float* dz,
+                               float* ddelta_bias, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+    clear_error();
+    MSC_REQUIRE(batch >= 1 && seqlen >= 1 && nheads >= 1 && headdim >= 1 && dstate >= 1 && ngroups >= 1,
+                "all sizes must be >= 1");
+    MSC_REQUIRE(nheads % ngroups == 0, "ngroups (%lld) must divide nheads (%lld)", (long long)ngroups,
+                (long long)nheads);
+    MSC_REQUIRE(in_dtype == MSC_F32 || in_dtype == MSC_BF16, "in_dtype must be MSC_F32 or MSC_BF16");
+    if (in_dtype != MSC_BF16) return fail(MSC_ERR_UNSUPPORTED, "SSD supports bf16 inputs only");
+    if (headdim != 64 || dstate != 128)
+        return fail(MSC_ERR_UNSUPPORTED, "SSD supports headdim 64 and dstate 128 (got %lld, %lld)",
+                    (long long)headdim, (long long)dstate);
+    if (chunk != 64 && chunk != 128 && chunk != 256)
+        return fail(MSC_ERR_UNSUPPORTED, "chunk must be 64, 128 or 256 (got %lld)", (long long)chunk);
+    if (batch > 65535 || nheads > 65535) return fail(MSC_ERR_UNSUPPORTED, "batch and nheads must be <= 65535");
+    if (ngroups != 1 && (nheads / ngroups) % 16 != 0)
+        return fail(MSC_ERR_UNSUPPORTED, "heads per group must be a multiple of 16 when ngroups > 1");
+    MSC_REQUIRE(seqlen <= ((int64_t)1 << 31), "seqlen too large");
+    MSC_PTR(x, "x"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A"); MSC_PTR(B, "B"); MSC_PTR(C, "C");
+    MSC_PTR(dy, "dy"); MSC_PTR(dx, "dx"); MSC_PTR(ddelta, "ddelta"); MSC_PTR(dA, "dA");
+    MSC_PTR(dB, "dB"); MSC_PTR(dC, "dC");
+    MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z"); MSC_OPT_PTR(delta_bias, "delta_bias");
+    MSC_REQUIRE((D == nullptr) == (dD == nullptr), "dD must be given exactly when D is");
+    MSC_REQUIRE((z == nullptr) == (dz == nullptr), "dz must be given exactly when z is");
+    MSC_REQUIRE((delta_bias == nullptr) == (ddelta_bias == nullptr),
+                "ddelta_bias must be given exactly when delta_bias is");
+    const size_t need = ssd_bwd_workspace(batch, seqlen, nheads, ngroups, chunk, z != nullptr);
+    if (workspace == nullptr || workspace_bytes < need)
+        return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    MSC_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 1023u) == 0, "workspace must be 1024-byte aligned");
+    SsdBwdArgs a{};
+    a.f.batch = batch; a.f.L = seqlen; a.f.H = nheads; a.f.P = headdim; a.f.N = dstate; a.f.G = ngroups;
+    a.f.Q = chunk;
+    a.f.x = x; a.f.delta = delta; a.f.B = B; a.f.C = C; a.f.z = z; a.f.A = A; a.f.D = D;
+    a.f.delta_bias = delta_bias;
+    a.dy = dy; a.dx = dx; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dz = dz;
+    a.ddelta_bias = ddelta_bias; a.workspace = workspace;
+    return ssd_bwd_launch(a, static_cast<cudaStream_t>(stream));
+}
+
 msc_status msc_check_device_status(void* stream) {
     clear_error();
     cudaStream_t st = static_cast<cudaStream_t>(stream);

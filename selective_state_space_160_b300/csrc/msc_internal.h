@@ -91,5 +91,20 @@ struct SsdArgs {
 size_t ssd_workspace(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, int64_t G,
                      int64_t Q);
 msc_status ssd_launch(const SsdArgs& a, cudaStream_t stream);
+// For the backward: Delta and in-chunk cumsum cs [b, H, nc * Q], chunk states
+// S and the state entering every chunk Hin32 [b, nc, H, P, N] (all fp32).
+msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* Hin32, cudaStream_t stream);
+
+// SSD backward: the forward's inputs in f (y, final_state, workspace unused),
+// the upstream gradient dy (bf16, shaped like x) and fp32 gradients.
+struct SsdBwdArgs {
+    SsdArgs f;
+    const void* dy;
+    float *dx, *ddelta, *dA, *dB, *dC, *dD, *dz, *ddelta_bias;
+    void* workspace;
+};
+
+size_t ssd_bwd_workspace(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t Q, bool has_z);
+msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t stream);
 
 }  // namespace msc_host

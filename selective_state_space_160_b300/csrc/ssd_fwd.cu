@@ -364,6 +364,34 @@ __global__ void __launch_bounds__(256) ssd_pass_kernel(const SsdParams p) {
     }
 }
 
+// fp32 variant of the state pass for the backward: Hin32[b, c, h, p, n], the
+// state entering every chunk, one thread per (b, h, p, 8 consecutive n).
+__global__ void __launch_bounds__(256) ssd_pass32_kernel(const SsdParams p, float* Hin32) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int b = blockIdx.y;
+    constexpr int kN8 = kN / 8;
+    if (idx >= (int64_t)p.H * kP * kN8) return;
+    const int n0 = (int)(idx % kN8) * 8;
+    const int pp = (int)((idx / kN8) % kP);
+    const int h = (int)(idx / (kN8 * kP));
+    const size_t dbase = ((size_t)b * p.H + h) * p.Lp;
+    float run[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) run[e] = 0.f;
+    for (int c = 0; c < p.nc; ++c) {
+        const size_t o = ((((size_t)b * p.nc + c) * p.H + h) * kP + pp) * kN + n0;
+        float4* dst = reinterpret_cast<float4*>(Hin32 + o);
+        dst[0] = make_float4(run[0], run[1], run[2], run[3]);
+        dst[1] = make_float4(run[4], run[5], run[6], run[7]);
+        const float4* src = reinterpret_cast<const float4*>(p.S + o);
+        const float4 s0 = src[0], s1 = src[1];
+        const float a = msc::ex2_approx(p.cs[dbase + (size_t)c * p.Q + p.Q - 1] * MSC_LOG2E);
+        const float s8[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) run[e] = fmaf(a, run[e], s8[e]);
+    }
+}
+
 // ------------------------------------------------------------ (4) chunk scan
 struct ScanMaps {
     CUtensorMap C, B, xs, xq;
@@ -811,6 +839,47 @@ msc_status ssd_launch(const SsdArgs& a, cudaStream_t st) {
         if ((s = check_launch("ssd_scan")) != MSC_OK) return s;
     }
     return MSC_OK;
+}
+
+msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* Hin32, cudaStream_t st) {
+    SsdParams p{};
+    p.x = static_cast<const uint16_t*>(a.x);
+    p.delta = static_cast<const uint16_t*>(a.delta);
+    p.B = static_cast<const uint16_t*>(a.B);
+    p.C = static_cast<const uint16_t*>(a.C);
+    p.A = a.A; p.bias = a.delta_bias;
+    p.L = a.L; p.batch = (int)a.batch; p.H = (int)a.H; p.G = (int)a.G; p.hpg = (int)(a.H / a.G); p.Q = (int)a.Q;
+    p.nc = (int)((a.L + a.Q - 1) / a.Q);
+    p.Lp = (int64_t)p.nc * a.Q;
+    if (p.hpg % kHBS != 0 && p.G != 1) return fail(MSC_ERR_UNSUPPORTED, "heads per group must be a multiple of %d", kHBS);
+    p.dt = dt; p.cs = cs; p.S = S;
+    ssd_prep_kernel<<<dim3(p.nc, p.H, (unsigned)a.batch), 256, 0, st>>>(p);
+    msc_status s = check_launch("ssd_prep");
+    if (s != MSC_OK) return s;
+    CUtensorMap mB, mX;
+    {
+        const uint64_t bcd[3] = {(uint64_t)(a.G * kN), (uint64_t)a.L, (uint64_t)a.batch};
+        const uint64_t bcs[2] = {(uint64_t)(a.G * kN * 2), (uint64_t)(a.L * a.G * kN * 2)};
+        const uint32_t qbox[3] = {64, (uint32_t)p.Q, 1};
+        const uint64_t xd[3] = {(uint64_t)(a.H * kP), (uint64_t)a.L, (uint64_t)a.batch};
+        const uint64_t xs[2] = {(uint64_t)(a.H * kP * 2), (uint64_t)(a.L * a.H * kP * 2)};
+        if (!encode_tmap(&mB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.B, bcd, bcs, qbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&mX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.x, xd, xs, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MSC_ERR_CUDA;
+    }
+    {
+        static bool configured = false;
+        if (!configured) {
+            cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
+            if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_state smem attribute: %s", cudaGetErrorString(e));
+            configured = true;
+        }
+        ssd_state_kernel<<<dim3(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch), 256, state_smem(p.Q), st>>>(mB, mX, p);
+        if ((s = check_launch("ssd_state")) != MSC_OK) return s;
+    }
+    const int64_t per_b = (int64_t)p.H * kP * kN;
+    ssd_pass32_kernel<<<dim3((unsigned)((per_b / 8 + 255) / 256), (unsigned)a.batch), 256, 0, st>>>(p, Hin32);
+    return check_launch("ssd_pass32");
 }
 
 msc_status ssd_take_status(unsigned int* code, unsigned int* site) {

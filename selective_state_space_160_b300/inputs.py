@@ -72,8 +72,9 @@ def s6_inputs(batch, dim, seqlen, dstate, seed=SEED_BASE, bf16=False, with_z=Tru
 
 
 def ssd_inputs(batch, seqlen, nheads, headdim, dstate, ngroups=1, seed=SEED_BASE,
-               bf16=True, with_z=False, with_D=True, with_bias=True):
-    """Inputs of one SSD (scalar-A, multi-head) problem as float32 numpy arrays."""
+               bf16=True, with_z=False, with_D=True, with_bias=True, with_dy=False):
+    """Inputs of one SSD (scalar-A, multi-head) problem as float32 numpy arrays
+    (with_dy: also an upstream gradient dy shaped like x, drawn last)."""
     g = _rng(seed)
     rnd = bf16_round if bf16 else (lambda a: a)
     out = {}
@@ -87,6 +88,8 @@ def ssd_inputs(batch, seqlen, nheads, headdim, dstate, ngroups=1, seed=SEED_BASE
     out["delta_bias"] = np.log(np.expm1(dt)).astype(np.float32) if with_bias else None
     out["A"] = (-g.uniform(1.0, 16.0, size=nheads)).astype(np.float32)
     out["D"] = np.ones(nheads, np.float32) if with_D else None
+    if with_dy:
+        out["dy"] = rnd(_normal(g, (batch, seqlen, nheads, headdim)))
     return out
 
 

@@ -160,3 +160,29 @@ def test_fwd_ex_rejects_bad_arguments(lib):
     assert "disc" in msc.msc_last_error()
     assert call(L=63, disc=msc.MSC_DISC_ZOH) == msc.MSC_ERR_UNSUPPORTED        # bf16 rows not 16-byte strided
     assert call(L=66, dt=0, disc=msc.MSC_DISC_TRAPEZOID) == msc.MSC_ERR_UNSUPPORTED
+
+
+def test_ssd_bwd_rejects_bad_arguments(lib):
+    f = lib.msc_ssd_chunked_bwd
+
+    def call(b=1, L=256, H=4, P=64, N=128, G=1, Q=256, dt=1, D=None, z=None, bias=None, dy=16,
+             dD=None, dz=None, dbias=None, ws=1024, wsb=1 << 30):
+        return f(b, L, H, P, N, G, Q, dt, 16, 16, 16, 16, 16, D, z, bias, dy, 16, 16, 16, 16, 16,
+                 dD, dz, dbias, ws, wsb, None)
+
+    assert call(G=3) == msc.MSC_ERR_INVALID_ARG
+    assert call(P=32) == msc.MSC_ERR_UNSUPPORTED
+    assert call(Q=100) == msc.MSC_ERR_UNSUPPORTED
+    assert call(dt=0) == msc.MSC_ERR_UNSUPPORTED
+    assert call(H=24, G=2) == msc.MSC_ERR_UNSUPPORTED          # 12 heads per group
+    assert call(dy=None) == msc.MSC_ERR_INVALID_ARG and "dy" in msc.msc_last_error()
+    assert call(D=16) == msc.MSC_ERR_INVALID_ARG and "dD" in msc.msc_last_error()
+    assert call(z=16) == msc.MSC_ERR_INVALID_ARG and "dz" in msc.msc_last_error()
+    assert call(bias=16) == msc.MSC_ERR_INVALID_ARG and "ddelta_bias" in msc.msc_last_error()
+    assert call(ws=None, wsb=0) == msc.MSC_ERR_WORKSPACE
+    assert call(ws=2048 + 16) == msc.MSC_ERR_INVALID_ARG        # workspace misaligned
+    # the gate needs room for the recomputed pre-gate output and the forward's workspace
+    no_z = msc.msc_ssd_chunked_bwd_workspace_size(2, 1000, 8, 64, 128, 1, 256, False)
+    with_z = msc.msc_ssd_chunked_bwd_workspace_size(2, 1000, 8, 64, 128, 1, 256, True)
+    assert 0 < no_z < with_z
+    assert call(z=16, dz=16, wsb=no_z, L=1000, b=2, H=8) == msc.MSC_ERR_WORKSPACE
