@@ -396,6 +396,10 @@ msc_status msc_check_device_status(void* stream) {
         s = ssd_take_status(&code, &site);
         if (s != MSC_OK) return s;
     }
+    if (code == 0) {
+        s = ssd_bwd_take_status(&code, &site);
+        if (s != MSC_OK) return s;
+    }
     if (code == 0) return MSC_OK;
     if (code == MSC_ERR_TIMEOUT) return fail(MSC_ERR_TIMEOUT, "device-side wait ran out (site %u)", site);
     return fail((msc_status)code, "device status %u (site %u)", code, site);

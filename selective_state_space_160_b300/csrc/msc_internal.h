@@ -39,6 +39,7 @@ msc_status s6_fwd_checkpoints(const S6FwdArgs& a, float* ckpt, cudaStream_t stre
 msc_status s6_fwd_take_status(unsigned int* code, unsigned int* site);
 msc_status s6_bwd_take_status(unsigned int* code, unsigned int* site);
 msc_status ssd_take_status(unsigned int* code, unsigned int* site);
+msc_status ssd_bwd_take_status(unsigned int* code, unsigned int* site);
 
 size_t s6_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
 
@@ -92,8 +93,11 @@ size_t ssd_workspace(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, 
                      int64_t Q);
 msc_status ssd_launch(const SsdArgs& a, cudaStream_t stream);
 // For the backward: Delta and in-chunk cumsum cs [b, H, nc * Q], chunk states
-// S and the state entering every chunk Hin32 [b, nc, H, P, N] (all fp32).
-msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* Hin32, cudaStream_t stream);
+// S and the state entering every chunk Hin32 [b, nc, H, P, N] (all fp32), and
+// the same states as bf16 hi + lo tile images Himg [b, nc, H][2][64 x 128]
+// (K-major, 128-byte swizzle) for the tensor cores.
+msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* Hin32, uint16_t* Himg,
+                      cudaStream_t stream);
 
 // SSD backward: the forward's inputs in f (y, final_state, workspace unused),
 // the upstream gradient dy (bf16, shaped like x) and fp32 gradients.

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "msc_common.cuh"
 #include "msc_tma.cuh"
 
 namespace msc {
@@ -124,6 +125,31 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
+}
+
+// fp32 pair -> packed bf16x2 (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two-term bf16 split of an fp32 pair: hi = bf16(v), lo = bf16(v - hi), so that
+// hi + lo carries 16 significant bits; tensor-core products of fp32 operands
+// are formed as hi*hi + hi*lo + lo*hi with fp32 accumulation.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(a, b);
+    lo = pack_bf16x2(a - bf16lo(hi), b - bf16hi(hi));
+}
+// the same split of a packed fp32 pair, the residual formed by one packed subtract
+__device__ __forceinline__ void split_bf16x2_packed(uint64_t v, uint32_t& hi, uint32_t& lo) {
+    float a, b;
+    upk2(v, a, b);
+    hi = pack_bf16x2(a, b);
+    const uint64_t r = add2(v, pk2(-bf16lo(hi), -bf16hi(hi)));
+    float ra, rb;
+    upk2(r, ra, rb);
+    lo = pack_bf16x2(ra, rb);
 }
 
 // fp32 pair -> packed fp16x2 (round to nearest even)

@@ -47,18 +47,6 @@ __host__ __device__ constexpr int red_row(int r) { return r * 16 + (r >= 16 ? 16
 
 __device__ unsigned int g_s6_bwd_status[2];
 
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
-    if (msc::mbar_wait(bar, parity, 256)) return true;
-    uint64_t t0;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    while (true) {
-        if (msc::mbar_try_wait(bar, parity)) return true;
-        uint64_t t1;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
-        if (t1 - t0 > 1000000000ull) return false;
-    }
-}
-
 struct BwdParams {
     const float* A;
     const float* D;
@@ -214,7 +202,7 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
     int c = 0;
     for (; c < ntiles; ++c) {
         const int st = c % kStages;
-        const bool ok = wait_phase(&s_full[st], (uint32_t)((c / kStages) & 1));
+        const bool ok = msc::wait_bounded(&s_full[st], (uint32_t)((c / kStages) & 1));
         if (__syncthreads_or(!ok)) {
             if (tid == 0 && atomicCAS(&g_s6_bwd_status[0], 0u, (unsigned int)MSC_ERR_TIMEOUT) == 0u)
                 g_s6_bwd_status[1] = 2;
@@ -435,7 +423,7 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
     if (failed) {
         if (tid == 0)
             for (int cc = c; cc < issued && cc < ntiles; ++cc)
-                (void)wait_phase(&s_full[cc % kStages], (uint32_t)((cc / kStages) & 1));
+                (void)msc::wait_bounded(&s_full[cc % kStages], (uint32_t)((cc / kStages) & 1));
         return;
     }
     // per-channel sums: dA over this row's states, dD and dbias over its steps

@@ -298,19 +298,6 @@ __device__ __forceinline__ void record_timeout(unsigned int site) {
         g_s6_fwd_status[1] = site;
 }
 
-// Wait for phase `parity` of `bar`, giving up after about one second.
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
-    if (msc::mbar_wait(bar, parity, 256)) return true;
-    uint64_t t0;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    while (true) {
-        if (msc::mbar_try_wait(bar, parity)) return true;
-        uint64_t t1;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
-        if (t1 - t0 > 1000000000ull) return false;
-    }
-}
-
 constexpr int kStages = 2;
 constexpr int kRowTile = 2048;               // bytes of one 32-row x 64-byte tile
 constexpr int kBCTile = 1024;                // bytes of one 16-slot x 64-byte tile
@@ -473,7 +460,7 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
     int i = 0;
     for (; i < ntiles; ++i) {
         const int st = i % kStages;
-        const bool ok = wait_phase(&s_full[st], (uint32_t)((i / kStages) & 1));
+        const bool ok = msc::wait_bounded(&s_full[st], (uint32_t)((i / kStages) & 1));
         // every thread takes the same branch, so no thread is left at a barrier
         if (__syncthreads_or(!ok)) {
             if (tid == 0) record_timeout(1);
@@ -703,7 +690,7 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
         // drain loads still in flight before the shared memory is released
         if (tid == 0)
             for (int jt = i; jt < issued && jt < ntiles; ++jt)
-                (void)wait_phase(&s_full[jt % kStages], (uint32_t)((jt / kStages) & 1));
+                (void)msc::wait_bounded(&s_full[jt % kStages], (uint32_t)((jt / kStages) & 1));
         return;
     }
     if (kMode == kModeCkpt) return;

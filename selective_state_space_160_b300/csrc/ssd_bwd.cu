@@ -23,15 +23,16 @@
 // The oracle checks the same gradients through the S6 backward (its pins include
 // finite differences of the SSD forward).
 //
-// Kernels (every contraction is a 64-row tile of fp32 FMAs staged through
-// shared memory; cross-head sums are accumulated inside one CTA per group):
+// Kernels (cross-head sums are accumulated inside one CTA per group; dx runs
+// on tcgen05 with fp32 operands split into bf16 hi + lo, the other products
+// are 64-row tiles of fp32 FMAs staged through shared memory):
 //   ssd_gdz_kernel      dz, dD
 //   ssd_gmat_kernel     G = C B^T per (chunk, group), lower block triangle
 //   ssd_u_kernel        U_c per (chunk, head)
 //   ssd_rpass_kernel    reverse state pass: dS_c in place of U_c, dcs_last
 //   ssd_dg_kernel       dG per (chunk, group, 64 x 64 tile) over its heads; dDelta, dcs of Y_diag
 //   ssd_dbc_kernel      dC, dB from dG
-//   ssd_dx_kernel       dx per (chunk, head, 64 steps); dDelta, dcs of the state and Y_off terms
+//   ssd_dx_tc_kernel    dx per (chunk, head, 128 steps); dDelta, dcs of the state and Y_off terms
 //   ssd_dbcs_kernel     state parts of dB, dC per (chunk, group, 64 steps, 16 heads)
 //   ssd_dcs_kernel      cs -> Delta, A; ddelta, dbias
 #include <cuda_runtime.h>
@@ -40,6 +41,8 @@
 
 #include "msc_common.cuh"
 #include "msc_internal.h"
+#include "msc_tc.cuh"
+#include "msc_tma.cuh"
 
 namespace {
 
@@ -49,6 +52,12 @@ constexpr int kT = 64;       // tile rows / steps per block
 constexpr int kKS = 32;      // K slab of a tile product
 constexpr int kHBlk = 16;    // heads per CTA of the cross-head state kernel
 
+__device__ unsigned int g_ssdb_status[2];
+
+__device__ __forceinline__ void record_timeout(unsigned int site) {
+    if (atomicCAS(&g_ssdb_status[0], 0u, (unsigned int)MSC_ERR_TIMEOUT) == 0u) g_ssdb_status[1] = site;
+}
+
 struct SsdBwdParams {
     const uint16_t *x, *delta, *B, *C, *z, *dy;  // bf16
     const float *A, *D, *bias;
@@ -56,6 +65,8 @@ struct SsdBwdParams {
     const float *dt, *cs;                        // [b, H, Lp]
     const float* Hin;                            // [b, nc, H, P, N]
     float* U;                                    // [b, nc, H, P, N]: U_c, then dS_c
+    uint16_t* dSimg;                             // [b, nc, H] (hi, lo) bf16 images of dS_c, K-major [64 p][128 n] SW128
+    const uint16_t* Himg;                        // the same images of Hin
     float *Gm, *dG;                              // [b, nc, Gr, Q, Q]
     float *dcs, *dDelta;                         // [b, H, Lp] accumulators
     float *dx, *ddelta, *dA, *dB, *dC, *dD, *dz, *dbias;
@@ -232,6 +243,15 @@ __global__ void __launch_bounds__(256) ssd_rpass_kernel(const SsdBwdParams p) {
         const float4 hb = reinterpret_cast<const float4*>(p.Hin + o)[1];
         u4[0] = make_float4(dh[0], dh[1], dh[2], dh[3]);
         u4[1] = make_float4(dh[4], dh[5], dh[6], dh[7]);
+        {
+            uint8_t* tile = reinterpret_cast<uint8_t*>(p.dSimg) + (((size_t)b * p.nc + c) * p.H + h) * 32768;
+            const uint32_t off = msc::sw128_offset(pp, n0, kP);
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) msc::split_bf16x2(dh[2 * e], dh[2 * e + 1], hi[e], lo[e]);
+            *reinterpret_cast<uint4*>(tile + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(tile + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
         const float a = msc::ex2_approx(p.cs[dbase + (size_t)c * p.Q + p.Q - 1] * MSC_LOG2E);
         float part = ha.x * dh[0] + ha.y * dh[1] + ha.z * dh[2] + ha.w * dh[3] + hb.x * dh[4] + hb.y * dh[5] +
                      hb.z * dh[6] + hb.w * dh[7];
@@ -396,112 +416,291 @@ __global__ void __launch_bounds__(256) ssd_dbc_kernel(const SsdBwdParams p) {
     }
 }
 
-// ------------------------------------------------------------------ dx and the state terms of dDelta, dcs
-// CTA = (chunk * nb + jb, head, batch), 64 steps j x 64 channels p:
-//   acc1[j][p] = sum_{i >= j} E_ij G_ij g_i[p]       (Y_diag, K = i over blocks ib >= jb)
-//   acc2[j][p] = (dS B_j)[p]                        (K = N)
-//   acc3[j][p] = (Hin C_j)[p]                       (K = N)
-//   dx_j = Delta_j acc1 + w_j acc2 + D g_j;  dw_j = x_j . acc2;  v_j = exp(cs_j) g_j . acc3.
-__global__ void __launch_bounds__(256) ssd_dx_kernel(const SsdBwdParams p) {
-    __shared__ float As[kT][kT + 1];
-    __shared__ float Bs[kT][kT + 4];
-    __shared__ float s_cs[kT + 1], s_dt[kT];
-    __shared__ float s_red[8];
-    const int nb = p.Q / kT;
-    const int c = blockIdx.x / nb, jb = blockIdx.x % nb;
+// ------------------------------------------------------------------ dx on tcgen05
+// CTA = (chunk * nmb + row block mb of 128 steps j, head, batch); 8 operand /
+// epilogue warps, one load warp, one MMA warp.  Three accumulators in tensor
+// memory, M = 128 rows j, N = 64 channels p, all fp32:
+//   acc1 = sum_{i >= j} (E_ij G_ij) g_i[p]  A: E o G formed by CUDA cores, split hi + lo;
+//                                          B: g tile [64 i][64 p], MN-major (dy itself, or
+//                                          dy silu(z) split hi + lo)
+//   acc2 = B_j . dS[p, :]                  A: B tile by TMA (exact bf16); B: dS hi, lo images
+//   acc3 = C_j . Hin[p, :]                 A: C tile by TMA; B: Hin hi, lo images
+// The operands stream through a ring of four 48 KB stages, one K slab of 64
+// each: A hi [128][64] | A lo | B hi [64][64] | B lo (bf16, 128-byte swizzle).
+// Slabs 0-1 feed acc2 (n blocks 0, 1), 2-3 acc3, then one per 64 steps i >= j0.
+// Epilogue (thread = row j, half of the p columns):
+//   dx_j = Delta_j acc1 + w_j acc2 + D g_j;  dw_j = x_j . acc2;  v_j = exp(cs_j) g_j . acc3
+constexpr int kDxStages = 4;
+constexpr uint32_t kDxStage = 49152;
+constexpr int kDxOpWarps = 8;
+constexpr int kDxWarpLoad = kDxOpWarps, kDxWarpMma = kDxOpWarps + 1;
+constexpr int kDxThreads = (kDxOpWarps + 2) * 32;
+constexpr size_t kDxSmem = 1024 + kDxStages * kDxStage + (256 + 256 + 512) * 4 + 16 * 8 + 16;
+
+__global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_constant__ CUtensorMap tmB,
+                                                                  const __grid_constant__ CUtensorMap tmC,
+                                                                  const __grid_constant__ CUtensorMap tmDy,
+                                                                  const __grid_constant__ CUtensorMap tmZ,
+                                                                  const SsdBwdParams p) {
+    extern __shared__ uint8_t s_dyn[];
+    uint8_t* stages = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);
+    float* s_csl = reinterpret_cast<float*>(stages + kDxStages * kDxStage);  // cs log2(e) of the chunk
+    float* s_dt = s_csl + 256;
+    float* s_part = s_dt + 256;                                                // [dw, v][2 halves][128 rows]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_part + 512);
+    // 0-3 stage loaded (TMA), 4-7 stage built (8 warps), 8-9 free (MMA), 12 done, 13 drain
+    uint64_t *tfull = bars, *full = bars + 4, *empty = bars + 8, *done = bars + 12, *drain = bars + 13;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 14);
+    volatile uint32_t* abort = slot + 1;
+
+    const int Q = p.Q;
+    const int nmb = (Q + 127) / 128;
+    const int c = blockIdx.x / nmb, mb = blockIdx.x % nmb;
     const int h = blockIdx.y, b = blockIdx.z, g = h / p.hpg;
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int64_t t0 = (int64_t)c * p.Q;
-    const int jloc0 = jb * kT;
-    const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)t0;
-    const float* Gt = p.Gm + (((size_t)b * p.nc + c) * p.Gr + g) * p.Q * p.Q;
-    const size_t so = (((size_t)b * p.nc + c) * p.H + h) * kP * kN;
-    if (tid < kT) {
-        s_cs[tid] = p.cs[dbase + jloc0 + tid];
-        s_dt[tid] = p.dt[dbase + jloc0 + tid];
+    const int j0 = 128 * mb;
+    const int rows_valid = min(128, Q - j0);
+    const int ns = 4 + (Q - j0) / 64;
+    const int64_t tc0 = (int64_t)c * Q;
+    const bool has_z = p.z != nullptr;
+    const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
+    const size_t img = (((size_t)b * p.nc + c) * p.H + h) * 32768;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (warp == 0) {
+        msc::tmem_alloc(slot, 256);
+        msc::tmem_relinquish();
     }
-    if (tid == 0) s_cs[kT] = p.cs[dbase + p.Q - 1];
-    float acc1[4][4], acc2[4][4], acc3[4][4];
-    zero_acc(acc1);
-    zero_acc(acc2);
-    zero_acc(acc3);
-    for (int ib = jb; ib < nb; ++ib) {
-        __syncthreads();
-        const int iloc0 = ib * kT;
-        for (int e = tid; e < kT * kT; e += 256) {
-            const int r = e / kT, k = e % kT;  // r: i, k: j (coalesced along j)
-            const float csi = p.cs[dbase + iloc0 + r];
-            const float v = (iloc0 + r >= jloc0 + k)
-                                ? Gt[(size_t)(iloc0 + r) * p.Q + jloc0 + k] *
-                                      msc::ex2_approx((csi - s_cs[k]) * MSC_LOG2E)
-                                : 0.f;
-            As[k][r] = v;
-            Bs[r][k] = gval(p, b, t0 + iloc0 + r, h, k);
+    if (tid == 32) {
+        for (int k = 0; k < 4; ++k) {
+            msc::mbar_init(&tfull[k], 1);
+            msc::mbar_init(&full[k], kDxOpWarps);
+            msc::mbar_init(&empty[k], 1);
         }
-        __syncthreads();
-        tile_fma<4>(&As[0][0], kT + 1, &Bs[0][0], kT + 4, kT, acc1, tid);
+        msc::mbar_init(done, 1);
+        msc::mbar_init(drain, 1);
+        slot[1] = 0u;
+        msc::fence_barrier_init();
     }
-    // state terms: K = N in two halves of 64
-    for (int side = 0; side < 2; ++side) {
-        for (int k0 = 0; k0 < kN; k0 += kT) {
-            __syncthreads();
-            const float* M = side ? p.Hin + so : p.U + so;  // U holds dS after the reverse pass
-            for (int e = tid; e < kT * kT; e += 256) {
-                const int r = e / kT, k = e % kT;
-                As[r][k] = bval(side ? p.C : p.B, p, b, t0 + jloc0 + r, g, k0 + k);
-                Bs[k][r] = M[(size_t)r * kN + k0 + k];  // r: p
-            }
-            __syncthreads();
-            if (side)
-                tile_fma<4>(&As[0][0], kT + 1, &Bs[0][0], kT + 4, kT, acc3, tid);
-            else
-                tile_fma<4>(&As[0][0], kT + 1, &Bs[0][0], kT + 4, kT, acc2, tid);
-        }
+    if (tid < Q) {
+        s_csl[tid] = p.cs[dbase + tid] * MSC_LOG2E;
+        s_dt[tid] = p.dt[dbase + tid];
     }
-    const float Dh = p.D ? p.D[h] : 0.f;
-    const float cl = s_cs[kT];
-    float lastp = 0.f;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int jl = ty * 4 + r;
-        const int64_t t = t0 + jloc0 + jl;
-        const float dtj = s_dt[jl];
-        const float ej = msc::ex2_approx((cl - s_cs[jl]) * MSC_LOG2E);
-        const float wj = ej * dtj;
-        float dw = 0.f, v = 0.f;
-        float dxv[4];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const int pp = tx * 4 + cc;
-            const float gv = gval(p, b, t, h, pp);
-            dxv[cc] = dtj * acc1[r][cc] + wj * acc2[r][cc] + Dh * gv;
-            dw = fmaf(xval(p, b, t, h, pp), acc2[r][cc], dw);
-            v = fmaf(gv, acc3[r][cc], v);
-        }
-        if (t < p.L)
-            *reinterpret_cast<float4*>(p.dx + (((size_t)b * p.L + t) * p.H + h) * kP + tx * 4) =
-                make_float4(dxv[0], dxv[1], dxv[2], dxv[3]);
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) {
-            dw += __shfl_xor_sync(0xffffffffu, dw, off);
-            v += __shfl_xor_sync(0xffffffffu, v, off);
-        }
-        if (tx == 0 && t < p.L) {
-            const float ecs = msc::ex2_approx(s_cs[jl] * MSC_LOG2E);
-            atomicAdd(p.dDelta + dbase + jloc0 + jl, ej * dw);
-            atomicAdd(p.dcs + dbase + jloc0 + jl, ecs * v - wj * dw);
-            lastp += wj * dw;
-        }
-    }
-    // dcs_last += sum_j w_j dw_j over the block
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lastp += __shfl_xor_sync(0xffffffffu, lastp, off);
-    if ((tid & 31) == 0) s_red[tid >> 5] = lastp;
+    msc::tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
-        float s = 0.f;
-        for (int w = 0; w < 8; ++w) s += s_red[w];
-        if (s != 0.f) atomicAdd(p.dcs + dbase + p.Q - 1, s);
+    msc::tc_fence_after();
+    const uint32_t tmem = *slot;
+
+    if (warp == kDxWarpLoad) {
+        // ------------------------------------------------------------ loads
+        if (lane == 0) {
+            msc::prefetch_tmap(&tmB);
+            msc::prefetch_tmap(&tmC);
+            msc::prefetch_tmap(&tmDy);
+            if (has_z) msc::prefetch_tmap(&tmZ);
+            int issued = 0;
+            for (int s = 0; s < ns; ++s) {
+                const int st = s & 3, use = s >> 2;
+                if (use > 0 && !msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort)) {
+                    record_timeout(101);
+                    *abort = 1u;
+                    break;
+                }
+                uint8_t* sg = stages + st * kDxStage;
+                if (s < 4) {
+                    const int which = s >> 1, kb = s & 1;
+                    const uint8_t* im = reinterpret_cast<const uint8_t*>(which ? p.Himg : p.dSimg) + img;
+                    msc::mbar_arrive_expect_tx(&tfull[st], 32768u);
+                    msc::tma_load_3d(sg, which ? &tmC : &tmB, &tfull[st], g * kN + 64 * kb, (int)(tc0 + j0), b);
+                    msc::bulk_g2s(sg + 32768, im + 8192 * kb, 8192u, &tfull[st]);
+                    msc::bulk_g2s(sg + 40960, im + 16384 + 8192 * kb, 8192u, &tfull[st]);
+                } else {
+                    const int i0 = j0 + 64 * (s - 4);
+                    msc::mbar_arrive_expect_tx(&tfull[st], has_z ? 16384u : 8192u);
+                    msc::tma_load_3d(sg + 32768, &tmDy, &tfull[st], h * kP, (int)(tc0 + i0), b);
+                    if (has_z) msc::tma_load_3d(sg + 40960, &tmZ, &tfull[st], h * kP, (int)(tc0 + i0), b);
+                }
+                ++issued;
+            }
+            // no copy may still be landing when the block exits
+            for (int st = 0; st < 4 && st < issued; ++st)
+                if (!msc::wait_bounded(&tfull[st], (uint32_t)(((issued - 1 - st) >> 2) & 1))) record_timeout(102);
+        }
+        __syncwarp();
+    } else if (warp == kDxWarpMma) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t idK = msc::idesc_f16(true, 128, kP);
+            const uint32_t idX = msc::idesc_f16(true, 128, kP, false, true);
+            bool ok = true;
+            for (int s = 0; s < ns && ok; ++s) {
+                const int st = s & 3, use = s >> 2;
+                ok = msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort) &&
+                     msc::wait_bounded(&full[st], (uint32_t)(use & 1), abort);
+                if (!ok) break;
+                msc::tc_fence_after();
+                const uint32_t a = msc::smem_u32(stages + st * kDxStage);
+                if (s < 4) {
+                    const uint32_t acc = tmem + (s < 2 ? 64u : 128u);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad = msc::sdesc_sw128(a + 32 * k);
+                        msc::mma_f16(acc, ad, msc::sdesc_sw128(a + 32768 + 32 * k), idK, ((s & 1) || k) ? 1u : 0u);
+                        msc::mma_f16(acc, ad, msc::sdesc_sw128(a + 40960 + 32 * k), idK, 1u);
+                    }
+                } else {
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t bh = msc::sdesc_sw128_mn(a + 32768 + 2048 * k, 8192u);
+                        const uint64_t ah = msc::sdesc_sw128(a + 32 * k);
+                        msc::mma_f16(tmem, ah, bh, idX, (s > 4 || k) ? 1u : 0u);
+                        msc::mma_f16(tmem, msc::sdesc_sw128(a + 16384 + 32 * k), bh, idX, 1u);
+                        if (has_z) msc::mma_f16(tmem, ah, msc::sdesc_sw128_mn(a + 40960 + 2048 * k, 8192u), idX, 1u);
+                    }
+                }
+                msc::mma_commit(&empty[st]);
+            }
+            if (ok) {
+                msc::mma_commit(done);
+            } else {
+                record_timeout(103);
+                *abort = 1u;
+            }
+            // every MMA issued completes before the tensor memory is released
+            msc::mma_commit(drain);
+            if (!msc::wait_bounded(drain, 0)) record_timeout(104);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ operands, then epilogue
+        const float* Gt = p.Gm + (((size_t)b * p.nc + c) * p.Gr + g) * (size_t)Q * Q;
+        bool ok = true;
+        for (int s = 0; s < ns; ++s) {
+            const int st = s & 3, use = s >> 2;
+            uint8_t* sg = stages + st * kDxStage;
+            if (s >= 4) {
+                if (use > 0) ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort));
+                if (!ok) break;
+                // A = (E o G)^T of this slab: rows j (128), K = 64 steps i from i0
+                const int i0 = j0 + 64 * (s - 4);
+#pragma unroll 1
+                for (int r = 0; r < 4; ++r) {
+                    const int e = tid + 256 * r;
+                    const int row = e & 127, kc = e >> 7;
+                    const int j = j0 + row, ib = i0 + 8 * kc;
+                    uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+                    if (row < rows_valid && ib + 7 >= j) {
+                        const float csj = s_csl[j];
+                        float v[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int i = ib + q;
+                            v[q] = 0.f;
+                            if (i >= j) v[q] = Gt[(size_t)i * Q + j] * msc::ex2_approx(s_csl[i] - csj);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) msc::split_bf16x2(v[2 * q], v[2 * q + 1], hi[q], lo[q]);
+                    }
+                    const uint32_t off = msc::sw128_offset(row, 8 * kc, 128);
+                    *reinterpret_cast<uint4*>(sg + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(sg + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                if (has_z) {
+                    // g = dy silu(z) in place: hi over dy, lo over z
+                    ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort));
+                    if (!ok) break;
+#pragma unroll 1
+                    for (int u = tid; u < 512; u += 256) {
+                        uint4* ph = reinterpret_cast<uint4*>(sg + 32768 + 16 * u);
+                        uint4* pl = reinterpret_cast<uint4*>(sg + 40960 + 16 * u);
+                        const uint4 dv = *ph, zv = *pl;
+                        const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w}, zw[4] = {zv.x, zv.y, zv.z, zv.w};
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            msc::split_bf16x2(msc::bf16lo(dw[q]) * msc::silu_f(msc::bf16lo(zw[q])),
+                                              msc::bf16hi(dw[q]) * msc::silu_f(msc::bf16hi(zw[q])), hi[q], lo[q]);
+                        *ph = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *pl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+            }
+            msc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) msc::mbar_arrive(&full[st]);
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(105);
+            *abort = 1u;
+        }
+        // ---------------------------------------------------------- epilogue
+        ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(done, 0, abort));
+        msc::tc_fence_after();
+        const int lq = warp & 3, half = warp >> 2;
+        const int row = 32 * lq + lane, j = j0 + row;
+        const int64_t t = tc0 + j;
+        const bool valid = ok && row < rows_valid && t < p.L;
+        float dw = 0.f, v = 0.f, ej = 0.f, wj = 0.f, ecs = 0.f;
+        if (ok) {
+            const uint32_t ta = tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)(32 * half);
+            float a1[32], a2[32], a3[32];
+            msc::tmem_ld16(ta, a1);
+            msc::tmem_ld16(ta + 16, a1 + 16);
+            msc::tmem_ld16(ta + 64, a2);
+            msc::tmem_ld16(ta + 80, a2 + 16);
+            msc::tmem_ld16(ta + 128, a3);
+            msc::tmem_ld16(ta + 144, a3 + 16);
+            msc::tmem_ld_wait();
+            if (valid) {
+                const size_t o = (((size_t)b * p.L + t) * p.H + h) * kP + 32 * half;
+                const float dtj = s_dt[j];
+                ej = msc::ex2_approx(s_csl[Q - 1] - s_csl[j]);
+                wj = ej * dtj;
+                ecs = msc::ex2_approx(s_csl[j]);
+                const float Dh = p.D ? p.D[h] : 0.f;
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    const uint4 dv = *reinterpret_cast<const uint4*>(p.dy + o + 8 * q8);
+                    const uint4 xv = *reinterpret_cast<const uint4*>(p.x + o + 8 * q8);
+                    uint4 zv = make_uint4(0u, 0u, 0u, 0u);
+                    if (has_z) zv = *reinterpret_cast<const uint4*>(p.z + o + 8 * q8);
+                    const uint32_t dwd[4] = {dv.x, dv.y, dv.z, dv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+                    float out[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int q = 8 * q8 + e;
+                        const float dyv = (e & 1) ? msc::bf16hi(dwd[e >> 1]) : msc::bf16lo(dwd[e >> 1]);
+                        const float xvv = (e & 1) ? msc::bf16hi(xw[e >> 1]) : msc::bf16lo(xw[e >> 1]);
+                        const float gv = has_z ? dyv * msc::silu_f((e & 1) ? msc::bf16hi(zw[e >> 1]) : msc::bf16lo(zw[e >> 1]))
+                                               : dyv;
+                        out[e] = dtj * a1[q] + wj * a2[q] + Dh * gv;
+                        dw = fmaf(xvv, a2[q], dw);
+                        v = fmaf(gv, a3[q], v);
+                    }
+                    msc::st_cs_v8(p.dx + o + 8 * q8, out);
+                }
+            }
+        }
+        s_part[128 * half + row] = dw;
+        s_part[256 + 128 * half + row] = v;
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (half == 0) {
+            float lastp = 0.f;
+            if (valid) {
+                const float dwt = dw + s_part[128 + row];
+                const float vt = v + s_part[384 + row];
+                atomicAdd(p.dDelta + dbase + j, ej * dwt);
+                atomicAdd(p.dcs + dbase + j, ecs * vt - wj * dwt);
+                lastp = wj * dwt;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) lastp += __shfl_xor_sync(0xffffffffu, lastp, off);
+            if (lane == 0 && lastp != 0.f) atomicAdd(p.dcs + dbase + Q - 1, lastp);
+        }
+        msc::tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        msc::tc_fence_after();
+        msc::tmem_dealloc(tmem, 256);
     }
 }
 
@@ -631,7 +830,7 @@ size_t ssd_bwd_workspace(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t
     const int64_t nc = (L + Q - 1) / Q, Lp = nc * Q;
     size_t s = 1024;
     s += 4 * a256((size_t)batch * H * Lp * 4);            // dt, cs, dcs, dDelta
-    s += 3 * a256((size_t)batch * nc * H * kP * kN * 4);  // S, Hin, U / dS
+    s += 5 * a256((size_t)batch * nc * H * kP * kN * 4);  // S, Hin, U / dS, and the Hin, dS bf16 hi + lo images
     s += 2 * a256((size_t)batch * nc * G * Q * Q * 4);    // G, dG
     if (has_z) {
         s += a256((size_t)batch * L * H * kP * 4);         // pre-gate output
@@ -666,6 +865,9 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
     float* S = reinterpret_cast<float*>(ws); ws += a256(nst);
     float* Hin = reinterpret_cast<float*>(ws); ws += a256(nst);
     p.U = reinterpret_cast<float*>(ws); ws += a256(nst);
+    uint16_t* Himg = reinterpret_cast<uint16_t*>(ws); ws += a256(nst);
+    p.dSimg = reinterpret_cast<uint16_t*>(ws); ws += a256(nst);
+    p.Himg = Himg;
     p.Gm = reinterpret_cast<float*>(ws); ws += a256(ngm);
     p.dG = reinterpret_cast<float*>(ws); ws += a256(ngm);
     p.dt = dt; p.cs = cs; p.Hin = Hin;
@@ -677,7 +879,7 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
         if ((s = ssd_launch(fa, st)) != MSC_OK) return s;
         p.ypre = ypre;
     }
-    if ((s = ssd_states(f, dt, cs, S, Hin, st)) != MSC_OK) return s;
+    if ((s = ssd_states(f, dt, cs, S, Hin, Himg, st)) != MSC_OK) return s;
     cudaError_t e = cudaMemsetAsync(p.dcs, 0, 2 * a256(nrow), st);  // dcs and dDelta are adjacent
     if (e == cudaSuccess) e = cudaMemsetAsync(p.dA, 0, (size_t)f.H * 4, st);
     if (e == cudaSuccess && p.dD) e = cudaMemsetAsync(p.dD, 0, (size_t)f.H * 4, st);
@@ -697,13 +899,49 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
     if ((s = check_launch("ssd_dg")) != MSC_OK) return s;
     ssd_dbc_kernel<<<dim3(2 * nb, nc, BG), 256, 0, st>>>(p);
     if ((s = check_launch("ssd_dbc")) != MSC_OK) return s;
-    ssd_dx_kernel<<<dim3(nc * nb, H, B), 256, 0, st>>>(p);
-    if ((s = check_launch("ssd_dx")) != MSC_OK) return s;
+    {
+        // B, C as [128 steps][64 n] boxes; dy, z as [64 steps][64 p] boxes (bf16, 128-byte swizzle)
+        CUtensorMap mB, mC, mDy, mZ;
+        const uint64_t bcd[3] = {(uint64_t)(f.G * kN), (uint64_t)f.L, (uint64_t)f.batch};
+        const uint64_t bcs[2] = {(uint64_t)(f.G * kN * 2), (uint64_t)(f.L * f.G * kN * 2)};
+        const uint64_t xd[3] = {(uint64_t)(f.H * kP), (uint64_t)f.L, (uint64_t)f.batch};
+        const uint64_t xs[2] = {(uint64_t)(f.H * kP * 2), (uint64_t)(f.L * f.H * kP * 2)};
+        const uint32_t box128[3] = {64, 128, 1}, box64[3] = {64, 64, 1};
+        if (!encode_tmap(&mB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, f.B, bcd, bcs, box128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&mC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, f.C, bcd, bcs, box128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&mDy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.dy, xd, xs, box64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&mZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, f.z ? f.z : a.dy, xd, xs, box64,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return MSC_ERR_CUDA;
+        static bool configured = false;
+        if (!configured) {
+            cudaError_t e2 = cudaFuncSetAttribute(ssd_dx_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmem);
+            if (e2 != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_dx_tc smem attribute: %s", cudaGetErrorString(e2));
+            configured = true;
+        }
+        const unsigned nmb = (unsigned)((f.Q + 127) / 128);
+        ssd_dx_tc_kernel<<<dim3(nc * nmb, H, B), kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, p);
+        if ((s = check_launch("ssd_dx_tc")) != MSC_OK) return s;
+    }
     const unsigned nhb = (unsigned)((p.hpg + kHBlk - 1) / kHBlk);
     ssd_dbcs_kernel<<<dim3(nc * nb, (unsigned)f.G * nhb, B), 256, 0, st>>>(p);
     if ((s = check_launch("ssd_dbcs")) != MSC_OK) return s;
     ssd_dcs_kernel<<<dim3(nc, H, B), 256, 0, st>>>(p);
     return check_launch("ssd_dcs");
+}
+
+msc_status ssd_bwd_take_status(unsigned int* code, unsigned int* site) {
+    unsigned int w[2] = {0, 0};
+    cudaError_t e = cudaMemcpyFromSymbol(w, g_ssdb_status, sizeof(w));
+    if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    if (w[0] != 0) {
+        const unsigned int zz[2] = {0, 0};
+        e = cudaMemcpyToSymbol(g_ssdb_status, zz, sizeof(zz));
+        if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+    }
+    *code = w[0];
+    *site = w[1];
+    return MSC_OK;
 }
 
 }  // namespace msc_host

@@ -44,23 +44,16 @@ constexpr int kP = 64;    // head dimension
 constexpr int kN = 128;   // state size
 constexpr int kHB = 16;   // heads per CTA of the state and scan kernels
 
+using msc::bulk_g2s;
+using msc::pack_bf16x2;
+using msc::split_bf16x2;
+using msc::split_bf16x2_packed;
+using msc::st_cs_v8;
+
 __device__ unsigned int g_ssd_status[2];
 
 __device__ __forceinline__ void record_timeout(unsigned int site) {
     if (atomicCAS(&g_ssd_status[0], 0u, (unsigned int)MSC_ERR_TIMEOUT) == 0u) g_ssd_status[1] = site;
-}
-
-// Wait for phase `parity` of `bar`, giving up after about one second.
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
-    if (msc::mbar_wait(bar, parity, 256)) return true;
-    uint64_t t0;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    while (true) {
-        if (msc::mbar_try_wait(bar, parity)) return true;
-        uint64_t t1;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
-        if (t1 - t0 > 1000000000ull) return false;
-    }
 }
 
 struct SsdParams {
@@ -116,42 +109,8 @@ __global__ void __launch_bounds__(256) ssd_prep_kernel(const SsdParams p) {
     }
 }
 
-// bf16 pair packing (round to nearest even) and the hi + lo split of a pair
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
-    hi = pack_bf16x2(a, b);
-    lo = pack_bf16x2(a - msc::bf16lo(hi), b - msc::bf16hi(hi));
-}
-// the same split of a packed fp32 pair, the residual formed by one packed subtract
-__device__ __forceinline__ void split_bf16x2_packed(uint64_t v, uint32_t& hi, uint32_t& lo) {
-    float a, b;
-    msc::upk2(v, a, b);
-    hi = pack_bf16x2(a, b);
-    const uint64_t r = msc::add2(v, msc::pk2(-msc::bf16lo(hi), -msc::bf16hi(hi)));
-    float ra, rb;
-    msc::upk2(r, ra, rb);
-    lo = pack_bf16x2(ra, rb);
-}
 
-// 32-byte streaming store of 8 floats (sm_100+ 256-bit global access); p is
-// 32-byte aligned
-__device__ __forceinline__ void st_cs_v8(float* p, const float* v) {
-    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]),
-                 "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
-                 : "memory");
-}
 
-// cp.async.bulk global -> shared, completion counted on `bar`
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     msc::smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(msc::smem_u32(bar))
-                 : "memory");
-}
 
 constexpr int kHBS = 8;  // heads per CTA of the state kernel
 
@@ -219,7 +178,7 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
     __syncthreads();
     const uint32_t tmem = *slot;
     const uint32_t idesc = msc::idesc_f16(true, 128, kP, true, true);
-    bool ok = wait_phase(&m.bars[0], 0);
+    bool ok = msc::wait_bounded(&m.bars[0], 0);
     bool failed = false;
 
     // S of head hp from accumulator buffer sp: lane = n, column = p; warps w and
@@ -240,7 +199,7 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
         const int s = it & 1;
         if (it >= 1) {
             // MMAs of head it - 1 done: its x buffer takes head it + 1
-            ok = wait_phase(&m.bars[3 + (s ^ 1)], (uint32_t)(((it - 1) >> 1) & 1)) && ok;
+            ok = msc::wait_bounded(&m.bars[3 + (s ^ 1)], (uint32_t)(((it - 1) >> 1) & 1)) && ok;
             if (__syncthreads_or(!ok)) {
                 if (tid == 0) record_timeout(20);
                 failed = true;
@@ -248,7 +207,7 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
             }
             if (tid == 0 && it + 1 < nh) state_issue_head(m, &tmX, p, h0 + it + 1, s ^ 1, c, b);
         }
-        ok = wait_phase(&m.bars[1 + s], (uint32_t)((it >> 1) & 1)) && ok;
+        ok = msc::wait_bounded(&m.bars[1 + s], (uint32_t)((it >> 1) & 1)) && ok;
         if (__syncthreads_or(!ok)) {
             if (tid == 0) record_timeout(21);
             failed = true;
@@ -292,7 +251,7 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
     }
     if (!failed && nh > 0) {
         const int it = nh - 1;
-        ok = wait_phase(&m.bars[3 + (it & 1)], (uint32_t)((it >> 1) & 1));
+        ok = msc::wait_bounded(&m.bars[3 + (it & 1)], (uint32_t)((it >> 1) & 1));
         if (__syncthreads_or(!ok)) {
             if (tid == 0) record_timeout(22);
         } else {
@@ -402,20 +361,6 @@ constexpr int kWarpLoad = kScanCompute;                // warp streaming x, Delt
 constexpr int kWarpMma = kScanCompute + 1;             // warp issuing the tensor-core MMAs
 constexpr int kScanThreads = (kScanCompute + 2) * 32;
 
-// Bounded wait that also gives up as soon as another role of the block has
-// set *abort (so that one timeout does not cascade into many).
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const volatile uint32_t* abort) {
-    if (msc::mbar_wait(bar, parity, 256)) return true;
-    uint64_t t0;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    while (true) {
-        if (msc::mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        uint64_t t1;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
-        if (t1 - t0 > 1000000000ull) return false;
-    }
-}
 
 // CTA = (chunk c, row block ib of 128 rows, block of kHB heads, batch b), in
 // three roles that hand work over through mbarriers:
@@ -498,7 +443,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         for (int it = 0; it < nh; ++it) {
             const int s = it & 1, h = h0 + it;
             if (it >= 2) {
-                pok = __all_sync(0xffffffffu, wait_or_abort(&bars[10 + s], (uint32_t)(((it - 2) >> 1) & 1), abort));
+                pok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[10 + s], (uint32_t)(((it - 2) >> 1) & 1), abort));
                 if (!pok) break;
             }
             if (lane == 0) {
@@ -511,7 +456,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
             }
             if (s == 0) ++nx0; else ++nx1;
             if (it >= 1) {
-                pok = __all_sync(0xffffffffu, wait_or_abort(&bars[5], (uint32_t)((it - 1) & 1), abort));
+                pok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[5], (uint32_t)((it - 1) & 1), abort));
                 if (!pok) break;
             }
             if (lane == 0) {
@@ -527,16 +472,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         // every load issued lands before the block ends (they have all been
         // consumed already unless the block gives up)
         bool dok = true;
-        if (nx0 > 0) dok = wait_phase(&bars[2], (uint32_t)((nx0 - 1) & 1)) && dok;
-        if (nx1 > 0) dok = wait_phase(&bars[3], (uint32_t)((nx1 - 1) & 1)) && dok;
-        if (nhin > 0) dok = wait_phase(&bars[4], (uint32_t)((nhin - 1) & 1)) && dok;
+        if (nx0 > 0) dok = msc::wait_bounded(&bars[2], (uint32_t)((nx0 - 1) & 1)) && dok;
+        if (nx1 > 0) dok = msc::wait_bounded(&bars[3], (uint32_t)((nx1 - 1) & 1)) && dok;
+        if (nhin > 0) dok = msc::wait_bounded(&bars[4], (uint32_t)((nhin - 1) & 1)) && dok;
         if (!dok && lane == 0) record_timeout(51);
     } else if (warp == kWarpMma) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t id64 = msc::idesc_f16(true, 128, kP);                // A, B K-major
             const uint32_t id64x = msc::idesc_f16(true, 128, kP, false, true);  // B MN-major (x)
-            bool mok = wait_or_abort(&bars[0], 0, abort);
+            bool mok = msc::wait_bounded(&bars[0], 0, abort);
             if (mok) {
                 msc::tc_fence_after();
                 const uint32_t idesc = msc::idesc_f16(true, 128, Qi);
@@ -551,9 +496,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
             for (int it = 0; it < nh && mok; ++it) {
                 const int s = it & 1;
                 const uint32_t tYd = 256u + 128u * (uint32_t)s, tYo = tYd + 64u;
-                mok = wait_or_abort(&bars[2 + s], (uint32_t)((it >> 1) & 1), abort) &&
-                      wait_or_abort(&bars[4], (uint32_t)(it & 1), abort);
-                if (mok && it >= 2) mok = wait_or_abort(&bars[14 + s], (uint32_t)(((it - 2) >> 1) & 1), abort);
+                mok = msc::wait_bounded(&bars[2 + s], (uint32_t)((it >> 1) & 1), abort) &&
+                      msc::wait_bounded(&bars[4], (uint32_t)(it & 1), abort);
+                if (mok && it >= 2) mok = msc::wait_bounded(&bars[14 + s], (uint32_t)(((it - 2) >> 1) & 1), abort);
                 if (!mok) break;
                 msc::tc_fence_after();
                 const uint32_t aC = msc::smem_u32(sC), aH = msc::smem_u32(sH);
@@ -568,7 +513,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
                 const uint32_t aX = msc::smem_u32(sX + s * 32768);
                 for (int q = 0; q < nq; ++q) {
                     const int u = it * nq + q, bq = u & 1;
-                    mok = wait_or_abort(&bars[6 + bq], (uint32_t)((u >> 1) & 1), abort);
+                    mok = msc::wait_bounded(&bars[6 + bq], (uint32_t)((u >> 1) & 1), abort);
                     if (!mok) break;
                     msc::tc_fence_after();
                     const uint32_t aHi = msc::smem_u32(sBM + bq * 32768), aLo = aHi + 16384u;
@@ -589,7 +534,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
             }
             // every MMA issued completes before the tensor memory is released
             msc::mma_commit(&bars[16]);
-            if (!wait_phase(&bars[16], 0)) record_timeout(47);
+            if (!msc::wait_bounded(&bars[16], 0)) record_timeout(47);
         }
         __syncwarp();
     } else {
@@ -600,7 +545,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         const int row_lo = ib * 128 + 32 * lq;     // first row of this warp
         const uint32_t lane_off = (uint32_t)(32 * lq) << 16;
         float* my_w = s_w + warp * 64;
-        bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[1], 0, abort));
+        bool ok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[1], 0, abort));
         msc::tc_fence_after();
         float csi_prev = 0.f;
         uint4 z_prev[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
@@ -608,7 +553,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         // accumulator pair back to the MMA warp once it has been read
         auto epilogue = [&](int hp, bool release) -> bool {
             const int sp = hp & 1;
-            if (!__all_sync(0xffffffffu, wait_or_abort(&bars[12 + sp], (uint32_t)((hp >> 1) & 1), abort)))
+            if (!__all_sync(0xffffffffu, msc::wait_bounded(&bars[12 + sp], (uint32_t)((hp >> 1) & 1), abort)))
                 return false;
             msc::tc_fence_after();
             float yd[16], yo[16];
@@ -645,7 +590,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         for (int it = 0; it <= nh && ok; ++it) {
             if (it < nh) {
                 const int s = it & 1;
-                ok = __all_sync(0xffffffffu, wait_or_abort(&bars[2 + s], (uint32_t)((it >> 1) & 1), abort));
+                ok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[2 + s], (uint32_t)((it >> 1) & 1), abort));
                 if (!ok) break;
                 const float* s_dt = s_dc + s * 512;
                 const float* s_cs = s_dt + 256;
@@ -669,7 +614,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
                     const int u = it * nq + q, bq = u & 1;
                     if (u >= 2) {
                         ok = __all_sync(0xffffffffu,
-                                        wait_or_abort(&bars[8 + bq], (uint32_t)(((u >> 1) - 1) & 1), abort));
+                                        msc::wait_bounded(&bars[8 + bq], (uint32_t)(((u >> 1) - 1) & 1), abort));
                         if (!ok) break;
                     }
                     const int j0 = 64 * q + 16 * cslot;
@@ -841,7 +786,8 @@ msc_status ssd_launch(const SsdArgs& a, cudaStream_t st) {
     return MSC_OK;
 }
 
-msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* Hin32, cudaStream_t st) {
+msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* Hin32, uint16_t* Himg,
+                      cudaStream_t st) {
     SsdParams p{};
     p.x = static_cast<const uint16_t*>(a.x);
     p.delta = static_cast<const uint16_t*>(a.delta);
@@ -879,7 +825,11 @@ msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* H
     }
     const int64_t per_b = (int64_t)p.H * kP * kN;
     ssd_pass32_kernel<<<dim3((unsigned)((per_b / 8 + 255) / 256), (unsigned)a.batch), 256, 0, st>>>(p, Hin32);
-    return check_launch("ssd_pass32");
+    if ((s = check_launch("ssd_pass32")) != MSC_OK) return s;
+    p.Hin = Himg;
+    p.final_state = nullptr;
+    ssd_pass_kernel<<<dim3((unsigned)((per_b / 8 + 255) / 256), (unsigned)a.batch), 256, 0, st>>>(p);
+    return check_launch("ssd_pass");
 }
 
 msc_status ssd_take_status(unsigned int* code, unsigned int* site) {
