@@ -1,4 +1,4 @@
-// ssd_bwd.cu -- Mamba-2 SSD chunked backward on sm_103a (fp32 CUDA-core GEMM tiles).
+// ssd_bwd.cu -- Mamba-2 SSD chunked backward on sm_103a (tcgen05 for the large products).
 //
 // The pages give the SSD forward (bqwf survey sec. 3.2: scalar A_t = alpha_t I;
 // "Mamba 解密" sec. 6.2: Y = M (X . B^T) C, M_ij = a_{j+1} ... a_i); the backward is
@@ -23,17 +23,18 @@
 // The oracle checks the same gradients through the S6 backward (its pins include
 // finite differences of the SSD forward).
 //
-// Kernels (cross-head sums are accumulated inside one CTA per group; dx runs
-// on tcgen05 with fp32 operands split into bf16 hi + lo, the other products
-// are 64-row tiles of fp32 FMAs staged through shared memory):
+// Kernels (cross-head sums are accumulated inside one CTA per group; U, dG, dx
+// and the state parts of dB, dC run on tcgen05 with fp32 operands split into
+// bf16 hi + lo; G = C B^T and dC, dB from dG are 64-row tiles of fp32 FMAs
+// staged through shared memory):
 //   ssd_gdz_kernel      dz, dD
 //   ssd_gmat_kernel     G = C B^T per (chunk, group), lower block triangle
-//   ssd_u_kernel        U_c per (chunk, head)
+//   ssd_ugrad           U_c per (chunk, head): the forward's chunk-state kernel on dy, C
 //   ssd_rpass_kernel    reverse state pass: dS_c in place of U_c, dcs_last
-//   ssd_dg_kernel       dG per (chunk, group, 64 x 64 tile) over its heads; dDelta, dcs of Y_diag
+//   ssd_dg_tc_kernel    dG per (chunk, group, 128 x 128 tile) over its heads; dDelta, dcs of Y_diag
 //   ssd_dbc_kernel      dC, dB from dG
 //   ssd_dx_tc_kernel    dx per (chunk, head, 128 steps); dDelta, dcs of the state and Y_off terms
-//   ssd_dbcs_kernel     state parts of dB, dC per (chunk, group, 64 steps, 16 heads)
+//   ssd_dbcs_tc_kernel  state parts of dB, dC per (chunk, group, 128 steps, 16 heads)
 //   ssd_dcs_kernel      cs -> Delta, A; ddelta, dbias
 #include <cuda_runtime.h>
 
@@ -76,16 +77,6 @@ struct SsdBwdParams {
 
 __device__ __forceinline__ float bfv(uint16_t v) { return __uint_as_float(((uint32_t)v) << 16); }
 
-// g = dy * silu(z) (dy without a gate) at step t of row (b, h), channel pp; 0 past the end
-__device__ __forceinline__ float gval(const SsdBwdParams& p, int b, int64_t t, int h, int pp) {
-    if (t >= p.L) return 0.f;
-    const size_t o = (((size_t)b * p.L + t) * p.H + h) * kP + pp;
-    const float d = bfv(p.dy[o]);
-    return p.z ? d * msc::silu_f(bfv(p.z[o])) : d;
-}
-__device__ __forceinline__ float xval(const SsdBwdParams& p, int b, int64_t t, int h, int pp) {
-    return t < p.L ? bfv(p.x[(((size_t)b * p.L + t) * p.H + h) * kP + pp]) : 0.f;
-}
 __device__ __forceinline__ float bval(const uint16_t* M, const SsdBwdParams& p, int b, int64_t t, int g, int n) {
     return t < p.L ? bfv(M[(((size_t)b * p.L + t) * p.Gr + g) * kN + n]) : 0.f;
 }
@@ -185,40 +176,6 @@ __global__ void __launch_bounds__(256) ssd_gmat_kernel(const SsdBwdParams p) {
             dst[(size_t)(ib * kT + ty * 4 + r) * p.Q + jb * kT + tx * 4 + cc] = acc[r][cc];
 }
 
-// ------------------------------------------------------------------ U_c
-// CTA = (chunk, head, batch): U[p][n] = sum_i exp(cs_i) g_i[p] C_i[n] (64 x 128, K = Q).
-__global__ void __launch_bounds__(256) ssd_u_kernel(const SsdBwdParams p) {
-    __shared__ float As[kP][kKS + 1];
-    __shared__ float Bs[kKS][kN + 4];
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int g = h / p.hpg;
-    const int tid = threadIdx.x;
-    const int64_t t0 = (int64_t)c * p.Q;
-    const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)t0;
-    float acc[4][8];
-    zero_acc(acc);
-    for (int k0 = 0; k0 < p.Q; k0 += kKS) {
-        for (int e = tid; e < kP * kKS; e += 256) {
-            const int pp = e / kKS, k = e % kKS;
-            const float ecs = msc::ex2_approx(p.cs[dbase + k0 + k] * MSC_LOG2E);
-            As[pp][k] = ecs * gval(p, b, t0 + k0 + k, h, pp);
-        }
-        for (int e = tid; e < kKS * kN; e += 256) {
-            const int k = e / kN, n = e % kN;
-            Bs[k][n] = bval(p.C, p, b, t0 + k0 + k, g, n);
-        }
-        __syncthreads();
-        tile_fma<8>(&As[0][0], kKS + 1, &Bs[0][0], kN + 4, kKS, acc, tid);
-        __syncthreads();
-    }
-    const int ty = tid >> 4, tx = tid & 15;
-    float* dst = p.U + (((size_t)b * p.nc + c) * p.H + h) * kP * kN;
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) dst[(size_t)(ty * 4 + r) * kN + tx * 8 + cc] = acc[r][cc];
-}
-
 // ------------------------------------------------------------------ reverse state pass
 // Thread = (b, h, p, 8 consecutive n); 1024 threads per head, so every CTA of 256
 // belongs to one head.  Walking chunks last to first: dS_c = dH_{c+1} replaces
@@ -271,103 +228,292 @@ __global__ void __launch_bounds__(256) ssd_rpass_kernel(const SsdBwdParams p) {
     }
 }
 
-// ------------------------------------------------------------------ dG and the Y_diag terms
-// CTA = (64 x 64 tile (ib, jb), jb <= ib, chunk, batch * Gr), looping over the
-// group's heads: R = g_I x_J^T (K = P), then per element (i >= j)
-//   dG += E Delta_j R,   dDelta_j += E G R,   T = E G Delta_j R -> dcs_i += T, dcs_j -= T.
-__global__ void __launch_bounds__(256) ssd_dg_kernel(const SsdBwdParams p) {
-    __shared__ float As[kT][kKS + 1];
-    __shared__ float Bs[kKS][kT + 4];
-    __shared__ float s_cs[2][kT], s_dt[kT];
-    __shared__ float s_col[2][16][kT];
+// ------------------------------------------------------------------ dG on tcgen05
+// CTA = (128 x 128 tile (ib, jb), jb <= ib, chunk, batch * Gr), looping over the
+// group's heads.  Per head the tensor cores form R = g_I x_J^T (M = 128 steps i,
+// N = 128 steps j, K = P; g is dy, or dy silu(z) split hi + lo) into one of two
+// tensor-memory buffers; the CUDA cores then take, per element with i >= j,
+//   er = E_ij R_ij,  dG_ij += er Delta_j,  p1 = er G_ij,
+//   dcs_i += sum_j Delta_j p1,  dDelta_j += sum_i p1,  dcs_j -= Delta_j sum_i p1,
+// with the dG accumulators in registers (thread = row i, 64 columns j) and G
+// in shared memory,
+// while the MMAs of the next head run.  Column sums: a butterfly over the 32
+// lanes of a warp, then the four row quarters through shared memory.
+constexpr int kDgStages = 3;
+constexpr uint32_t kDgStage = 49152;           // A hi [128][64] | A lo (z) | B = x [128][64]
+constexpr int kDgOpWarps = 8;
+constexpr int kDgWarpLoad = kDgOpWarps, kDgWarpMma = kDgOpWarps + 1;
+constexpr int kDgThreads = (kDgOpWarps + 2) * 32;
+constexpr int kDgGld = 129;                    // row stride (floats) of the G tile in shared memory
+constexpr size_t kDgSmem = 1024 + kDgStages * kDgStage + (2 * 128 * 3 + 2 * 4 * 64 + 2 * 128 + 128 * kDgGld) * 4 + 16 * 8 + 16;
+
+// v[0..15] of every lane -> sum over the warp's 32 lanes of v[lane >> 1]
+__device__ __forceinline__ float warp_colsum16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const bool up = lane & 16;
+        const float send = up ? v[c] : v[c + 8];
+        const float keep = up ? v[c + 8] : v[c];
+        v[c] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const bool up = lane & 8;
+        const float send = up ? v[c] : v[c + 4];
+        const float keep = up ? v[c + 4] : v[c];
+        v[c] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const bool up = lane & 4;
+        const float send = up ? v[c] : v[c + 2];
+        const float keep = up ? v[c + 2] : v[c];
+        v[c] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    {
+        const bool up = lane & 2;
+        const float send = up ? v[0] : v[1];
+        const float keep = up ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+__global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                  const __grid_constant__ CUtensorMap tmDy,
+                                                                  const __grid_constant__ CUtensorMap tmZ,
+                                                                  const SsdBwdParams p) {
+    extern __shared__ uint8_t s_dyn[];
+    uint8_t* stages = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);
+    float* s_ci = reinterpret_cast<float*>(stages + kDgStages * kDgStage);  // [2 heads][128] cs_i log2(e)
+    float* s_cj = s_ci + 256;                                              // [2][128] cs_j log2(e)
+    float* s_dj = s_cj + 256;                                              // [2][128] Delta_j
+    float* s_col = s_dj + 256;                                             // [2 halves][4 quarters][64]
+    float* s_row = s_col + 512;                                            // [2 halves][128]
+    float* s_G = s_row + 256;                                              // [128 i][kDgGld] G of the tile
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_G + 128 * kDgGld);
+    // 0-2 stage loaded, 3-5 stage built, 6-8 stage free, 9-10 R ready, 11-12 R read, 13 drain
+    uint64_t *tfull = bars, *full = bars + 3, *empty = bars + 6, *rfull = bars + 9, *rfree = bars + 11,
+             *drain = bars + 13;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 14);
+    volatile uint32_t* abort = slot + 1;
+
+    const int Q = p.Q;
+    const int nt = (Q + 127) / 128;
     int ib = 0, rem = blockIdx.x;
     while (rem > ib) { rem -= ib + 1; ++ib; }
     const int jb = rem;
+    (void)nt;
     const int c = blockIdx.y, b = blockIdx.z / p.Gr, g = blockIdx.z % p.Gr;
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int64_t t0 = (int64_t)c * p.Q;
-    const int iloc0 = ib * kT, jloc0 = jb * kT;
-    const float* Gt = p.Gm + (((size_t)b * p.nc + c) * p.Gr + g) * p.Q * p.Q;
-    float Gv[4][4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) Gv[r][cc] = Gt[(size_t)(iloc0 + ty * 4 + r) * p.Q + jloc0 + tx * 4 + cc];
-    float dg[4][4];
-    zero_acc(dg);
-    for (int hh = 0; hh < p.hpg; ++hh) {
-        const int h = g * p.hpg + hh;
-        const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)t0;
-        float R[4][4];
-        zero_acc(R);
-        for (int k0 = 0; k0 < kP; k0 += kKS) {
-            for (int e = tid; e < kT * kKS; e += 256) {
-                const int r = e / kKS, k = e % kKS;
-                As[r][k] = gval(p, b, t0 + iloc0 + r, h, k0 + k);
-                Bs[k][r] = xval(p, b, t0 + jloc0 + r, h, k0 + k);
-            }
-            if (k0 == 0 && tid < kT) {
-                s_cs[0][tid] = p.cs[dbase + iloc0 + tid];
-                s_cs[1][tid] = p.cs[dbase + jloc0 + tid];
-                s_dt[tid] = p.dt[dbase + jloc0 + tid];
-            }
-            __syncthreads();
-            tile_fma<4>(&As[0][0], kKS + 1, &Bs[0][0], kT + 4, kKS, R, tid);
-            __syncthreads();
-        }
-        float rowT[4] = {0.f, 0.f, 0.f, 0.f}, colT[4] = {0.f, 0.f, 0.f, 0.f}, colD[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int il = ty * 4 + r;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int jl = tx * 4 + cc;
-                if (iloc0 + il < jloc0 + jl) continue;
-                const float E = msc::ex2_approx((s_cs[0][il] - s_cs[1][jl]) * MSC_LOG2E);
-                const float er = E * R[r][cc];
-                dg[r][cc] = fmaf(er, s_dt[jl], dg[r][cc]);
-                const float egr = er * Gv[r][cc];
-                const float T = egr * s_dt[jl];
-                rowT[r] += T;
-                colT[cc] += T;
-                colD[cc] += egr;
-            }
-        }
-        // row sums over the 16 threads of a row group (lanes tx of one ty)
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) rowT[r] += __shfl_xor_sync(0xffffffffu, rowT[r], off);
-        if (tx == 0) {
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                if (rowT[r] != 0.f) atomicAdd(p.dcs + dbase + iloc0 + ty * 4 + r, rowT[r]);
-        }
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            s_col[0][ty][tx * 4 + cc] = colT[cc];
-            s_col[1][ty][tx * 4 + cc] = colD[cc];
-        }
-        __syncthreads();
-        if (tid < 2 * kT) {
-            const int q = tid / kT, jl = tid % kT;
-            float sum = 0.f;
-            for (int yy = 0; yy < 16; ++yy) sum += s_col[q][yy][jl];
-            if (sum != 0.f) {
-                if (q == 0)
-                    atomicAdd(p.dcs + dbase + jloc0 + jl, -sum);
-                else
-                    atomicAdd(p.dDelta + dbase + jloc0 + jl, sum);
-            }
-        }
-        __syncthreads();
+    const int rv = min(128, Q);                  // valid rows / columns of a tile (Q = 64: half)
+    const int nh = p.hpg;
+    const int64_t tc0 = (int64_t)c * Q;
+    const bool has_z = p.z != nullptr;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (warp == 0) {
+        msc::tmem_alloc(slot, 256);
+        msc::tmem_relinquish();
     }
-    float* dst = p.dG + (((size_t)b * p.nc + c) * p.Gr + g) * p.Q * p.Q;
+    if (tid == 32) {
+        for (int k = 0; k < kDgStages; ++k) {
+            msc::mbar_init(&tfull[k], 1);
+            msc::mbar_init(&full[k], kDgOpWarps);
+            msc::mbar_init(&empty[k], 1);
+        }
+        for (int k = 0; k < 2; ++k) {
+            msc::mbar_init(&rfull[k], 1);
+            msc::mbar_init(&rfree[k], kDgOpWarps);
+        }
+        msc::mbar_init(drain, 1);
+        slot[1] = 0u;
+        msc::fence_barrier_init();
+    }
+    msc::tc_fence_before();
+    __syncthreads();
+    msc::tc_fence_after();
+    const uint32_t tmem = *slot;
+
+    if (warp == kDgWarpLoad) {
+        if (lane == 0) {
+            msc::prefetch_tmap(&tmX);
+            msc::prefetch_tmap(&tmDy);
+            if (has_z) msc::prefetch_tmap(&tmZ);
+            int issued = 0;
+            for (int hh = 0; hh < nh; ++hh) {
+                const int st = hh % kDgStages, use = hh / kDgStages;
+                if (use > 0 && !msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort)) {
+                    record_timeout(121);
+                    *abort = 1u;
+                    break;
+                }
+                const int h = g * p.hpg + hh;
+                uint8_t* sg = stages + st * kDgStage;
+                msc::mbar_arrive_expect_tx(&tfull[st], has_z ? 49152u : 32768u);
+                msc::tma_load_3d(sg, &tmDy, &tfull[st], h * kP, (int)(tc0 + 128 * ib), b);
+                if (has_z) msc::tma_load_3d(sg + 16384, &tmZ, &tfull[st], h * kP, (int)(tc0 + 128 * ib), b);
+                msc::tma_load_3d(sg + 32768, &tmX, &tfull[st], h * kP, (int)(tc0 + 128 * jb), b);
+                ++issued;
+            }
+            for (int st = 0; st < kDgStages && st < issued; ++st)
+                if (!msc::wait_bounded(&tfull[st], (uint32_t)(((issued - 1 - st) / kDgStages) & 1))) record_timeout(122);
+        }
+        __syncwarp();
+    } else if (warp == kDgWarpMma) {
+        if (lane == 0) {
+            const uint32_t idK = msc::idesc_f16(true, 128, 128);
+            bool ok = true;
+            for (int hh = 0; hh < nh && ok; ++hh) {
+                const int st = hh % kDgStages, use = hh / kDgStages, rb = hh & 1;
+                ok = msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort) &&
+                     msc::wait_bounded(&full[st], (uint32_t)(use & 1), abort);
+                if (ok && hh >= 2) ok = msc::wait_bounded(&rfree[rb], (uint32_t)(((hh - 2) >> 1) & 1), abort);
+                if (!ok) break;
+                msc::tc_fence_after();
+                const uint32_t a = msc::smem_u32(stages + st * kDgStage);
+                const uint32_t acc = tmem + 128u * (uint32_t)rb;
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t bd = msc::sdesc_sw128(a + 32768 + 32 * k);
+                    msc::mma_f16(acc, msc::sdesc_sw128(a + 32 * k), bd, idK, k ? 1u : 0u);
+                    if (has_z) msc::mma_f16(acc, msc::sdesc_sw128(a + 16384 + 32 * k), bd, idK, 1u);
+                }
+                msc::mma_commit(&empty[st]);
+                msc::mma_commit(&rfull[rb]);
+            }
+            if (!ok) {
+                record_timeout(123);
+                *abort = 1u;
+            }
+            msc::mma_commit(drain);
+            if (!msc::wait_bounded(drain, 0)) record_timeout(124);
+        }
+        __syncwarp();
+    } else {
+        const int lq = warp & 3, half = warp >> 2;
+        const int row = 32 * lq + lane;              // i within the tile
+        const int il = 128 * ib + row;               // i within the chunk
+        const bool row_ok = row < rv;
+        const float* Gt = p.Gm + (((size_t)b * p.nc + c) * p.Gr + g) * (size_t)Q * Q;
+        float dgacc[64];
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+        for (int k = 0; k < 64; ++k) dgacc[k] = 0.f;
+        // G of the tile (entries above the diagonal are never used: set to 0)
+#pragma unroll 4
+        for (int e = tid; e < 128 * 128; e += 256) {
+            const int r = e >> 7, jj = e & 127;
+            const int ir = 128 * ib + r;
+            s_G[r * kDgGld + jj] = (r < rv && jj < rv && ir >= 128 * jb + jj) ? Gt[(size_t)ir * Q + 128 * jb + jj] : 0.f;
+        }
+        bool ok = true;
+        auto produce = [&](int hh) {
+            const int st = hh % kDgStages, use = hh / kDgStages;
+            if (has_z) {
+                ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort));
+                if (ok) {
+                    uint8_t* sg = stages + st * kDgStage;
+#pragma unroll 1
+                    for (int u = tid; u < 1024; u += 256) {
+                        uint4* ph = reinterpret_cast<uint4*>(sg + 16 * u);
+                        uint4* pl = reinterpret_cast<uint4*>(sg + 16384 + 16 * u);
+                        const uint4 dv = *ph, zv = *pl;
+                        const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w}, zw[4] = {zv.x, zv.y, zv.z, zv.w};
+                        uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-            dst[(size_t)(iloc0 + ty * 4 + r) * p.Q + jloc0 + tx * 4 + cc] = dg[r][cc];
+                        for (int q = 0; q < 4; ++q)
+                            msc::split_bf16x2(msc::bf16lo(dw[q]) * msc::silu_f(msc::bf16lo(zw[q])),
+                                              msc::bf16hi(dw[q]) * msc::silu_f(msc::bf16hi(zw[q])), hi[q], lo[q]);
+                        *ph = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *pl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                    msc::fence_proxy_async_smem();
+                }
+            }
+            __syncwarp();
+            if (lane == 0) msc::mbar_arrive(&full[st]);
+        };
+        auto epilogue = [&](int hh) {
+            const int buf = hh & 1;
+            const int h = g * p.hpg + hh;
+            const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
+            // this head's cs and Delta rows; the other buffer may still be read by
+            // the tail of the previous head, this one was last read two heads ago
+            if (tid < 128) {
+                const bool on = tid < rv;
+                s_ci[128 * buf + tid] = on ? p.cs[dbase + 128 * ib + tid] * MSC_LOG2E : 0.f;
+                s_cj[128 * buf + tid] = on ? p.cs[dbase + 128 * jb + tid] * MSC_LOG2E : 0.f;
+                s_dj[128 * buf + tid] = on ? p.dt[dbase + 128 * jb + tid] : 0.f;
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&rfull[buf], (uint32_t)((hh >> 1) & 1), abort));
+            msc::tc_fence_after();
+            float rowt = 0.f;
+            const float csi = s_ci[128 * buf + row];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float r[16], col[16];
+                if (ok) {
+                    msc::tmem_ld16(tmem + 128u * (uint32_t)buf + ((uint32_t)(32 * lq) << 16) + (uint32_t)(64 * half + 16 * q), r);
+                    msc::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int k = 16 * q + e, jj = 64 * half + k;
+                    const bool m = row_ok && jj < rv && il >= 128 * jb + jj;
+                    const float dj = s_dj[128 * buf + jj];
+                    const float er = m ? msc::ex2_approx(csi - s_cj[128 * buf + jj]) * r[e] : 0.f;
+                    dgacc[k] = fmaf(er, dj, dgacc[k]);
+                    const float p1 = er * s_G[row * kDgGld + jj];
+                    rowt = fmaf(p1, dj, rowt);
+                    col[e] = p1;
+                }
+                const float cs_ = warp_colsum16(col, lane);
+                if ((lane & 1) == 0) s_col[256 * half + 64 * lq + 16 * q + (lane >> 1)] = cs_;
+            }
+            msc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) msc::mbar_arrive(&rfree[buf]);
+            s_row[128 * half + row] = rowt;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (tid < 128) {
+                const int jj = tid, hf = jj >> 6, k = jj & 63;
+                const float cd = s_col[256 * hf + k] + s_col[256 * hf + 64 + k] + s_col[256 * hf + 128 + k] +
+                                 s_col[256 * hf + 192 + k];
+                if (jj < rv && cd != 0.f) {
+                    atomicAdd(p.dDelta + dbase + 128 * jb + jj, cd);
+                    atomicAdd(p.dcs + dbase + 128 * jb + jj, -s_dj[128 * buf + jj] * cd);
+                }
+            } else {
+                const int r2 = tid - 128;
+                const float rt = s_row[r2] + s_row[128 + r2];
+                if (r2 < rv && rt != 0.f) atomicAdd(p.dcs + dbase + 128 * ib + r2, rt);
+            }
+        };
+        for (int hh = 0; hh <= nh; ++hh) {
+            if (hh < nh) produce(hh);
+            if (hh >= 1) epilogue(hh - 1);
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(125);
+            *abort = 1u;
+        }
+        if (row_ok) {
+            float* dst = p.dG + (((size_t)b * p.nc + c) * p.Gr + g) * (size_t)Q * Q + (size_t)il * Q + 128 * jb + 64 * half;
+            if (64 * half < rv) {
+#pragma unroll
+                for (int k = 0; k < 64; k += 4)
+                    *reinterpret_cast<float4*>(dst + k) = make_float4(dgacc[k], dgacc[k + 1], dgacc[k + 2], dgacc[k + 3]);
+            }
+        }
+        msc::tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        msc::tc_fence_after();
+        msc::tmem_dealloc(tmem, 256);
+    }
 }
 
 // ------------------------------------------------------------------ dC, dB from dG
@@ -704,66 +850,218 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
     }
 }
 
-// ------------------------------------------------------------------ state parts of dB, dC
-// CTA = (chunk * nb + jb, group * nhb + head block, batch), 64 steps x 128 n, summing
-// over up to kHBlk heads of the group (K = heads x P):
-//   dB_j += sum_h w_j^h x_j^h . dS_h,     dC_i += sum_h exp(cs_i^h) g_i^h . Hin_h
-__global__ void __launch_bounds__(256) ssd_dbcs_kernel(const SsdBwdParams p) {
-    __shared__ float As[kT][kKS + 1];
-    __shared__ float Bs[kKS][kN + 4];
-    __shared__ float s_w[kT], s_e[kT];
-    const int nb = p.Q / kT;
+// ------------------------------------------------------------------ state parts of dB, dC on tcgen05
+// CTA = (chunk * nmb + row block mb of 128 steps, group * nhb + block of up to
+// kHBlk heads, batch).  Two accumulators in tensor memory, M = 128 steps,
+// N = 128 states, summed over the block's heads (K = heads x P):
+//   accB[j, n] += sum_p (w_j x_j[p]) dS_h[p, n]        (dB_j += sum_h w_j x_j . dS_h)
+//   accC[i, n] += sum_p (exp(cs_i) g_i[p]) Hin_h[p, n]  (dC_i += sum_h exp(cs_i) g_i . Hin_h)
+// Per head two slabs through a ring of three 64 KB stages: A hi [128][64 p] |
+// A lo | B hi [64 p][128 n] | B lo.  A is the TMA tile of x (or dy, with z
+// landing in the A lo slot), scaled per row (and gated) and split in place; B
+// is the head's dS or Hin image used MN-major (N = n, K = p), which is the same
+// bytes as the K-major [64 p][128 n] image.  The sums are added to dB, dC
+// (which already hold the dG terms) with vector reductions.
+constexpr int kSbStages = 3;
+constexpr uint32_t kSbStage = 65536;
+constexpr int kSbOpWarps = 8;
+constexpr int kSbWarpLoad = kSbOpWarps, kSbWarpMma = kSbOpWarps + 1;
+constexpr int kSbThreads = (kSbOpWarps + 2) * 32;
+constexpr size_t kSbSmem = 1024 + kSbStages * kSbStage + 16 * 8 + 16;
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                    const __grid_constant__ CUtensorMap tmDy,
+                                                                    const __grid_constant__ CUtensorMap tmZ,
+                                                                    const SsdBwdParams p) {
+    extern __shared__ uint8_t s_dyn[];
+    uint8_t* stages = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stages + kSbStages * kSbStage);
+    // 0-2 stage loaded (TMA), 3-5 stage built (8 warps), 6-8 free (MMA), 9 done, 10 drain
+    uint64_t *tfull = bars, *full = bars + 3, *empty = bars + 6, *done = bars + 9, *drain = bars + 10;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 11);
+    volatile uint32_t* abort = slot + 1;
+
+    const int Q = p.Q;
+    const int nmb = (Q + 127) / 128;
     const int nhb = (p.hpg + kHBlk - 1) / kHBlk;
-    const int c = blockIdx.x / nb, jb = blockIdx.x % nb;
+    const int c = blockIdx.x / nmb, mb = blockIdx.x % nmb;
     const int g = blockIdx.y / nhb, hb = blockIdx.y % nhb;
     const int b = blockIdx.z;
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int64_t t0 = (int64_t)c * p.Q + jb * kT;
-    float accB[4][8], accC[4][8];
-    zero_acc(accB);
-    zero_acc(accC);
-    const int h_end = min(p.hpg, (hb + 1) * kHBlk);
-    for (int hh = hb * kHBlk; hh < h_end; ++hh) {
-        const int h = g * p.hpg + hh;
-        const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)c * p.Q;
-        const size_t so = (((size_t)b * p.nc + c) * p.H + h) * kP * kN;
-        __syncthreads();
-        if (tid < kT) {
-            const float csj = p.cs[dbase + jb * kT + tid];
-            const float cl = p.cs[dbase + p.Q - 1];
-            s_w[tid] = msc::ex2_approx((cl - csj) * MSC_LOG2E) * p.dt[dbase + jb * kT + tid];
-            s_e[tid] = msc::ex2_approx(csj * MSC_LOG2E);
+    const int j0 = 128 * mb;
+    const int rows_valid = min(128, Q - j0);
+    const int hh0 = hb * kHBlk;
+    const int nh = min(kHBlk, p.hpg - hh0);
+    const int ns = 2 * nh;                       // slab 2 k: dB term of head k, 2 k + 1: dC term
+    const int64_t tc0 = (int64_t)c * Q;
+    const bool has_z = p.z != nullptr;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (warp == 0) {
+        msc::tmem_alloc(slot, 256);
+        msc::tmem_relinquish();
+    }
+    if (tid == 32) {
+        for (int k = 0; k < kSbStages; ++k) {
+            msc::mbar_init(&tfull[k], 1);
+            msc::mbar_init(&full[k], kSbOpWarps);
+            msc::mbar_init(&empty[k], 1);
         }
-        for (int side = 0; side < 2; ++side) {
-            const float* M = side ? p.Hin + so : p.U + so;
-            for (int k0 = 0; k0 < kP; k0 += kKS) {
-                __syncthreads();
-                for (int e = tid; e < kT * kKS; e += 256) {
-                    const int r = e / kKS, k = e % kKS;
-                    As[r][k] = side ? s_e[r] * gval(p, b, t0 + r, h, k0 + k) : s_w[r] * xval(p, b, t0 + r, h, k0 + k);
+        msc::mbar_init(done, 1);
+        msc::mbar_init(drain, 1);
+        slot[1] = 0u;
+        msc::fence_barrier_init();
+    }
+    msc::tc_fence_before();
+    __syncthreads();
+    msc::tc_fence_after();
+    const uint32_t tmem = *slot;
+
+    if (warp == kSbWarpLoad) {
+        if (lane == 0) {
+            msc::prefetch_tmap(&tmX);
+            msc::prefetch_tmap(&tmDy);
+            if (has_z) msc::prefetch_tmap(&tmZ);
+            int issued = 0;
+            for (int s = 0; s < ns; ++s) {
+                const int st = s % kSbStages, use = s / kSbStages;
+                if (use > 0 && !msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort)) {
+                    record_timeout(111);
+                    *abort = 1u;
+                    break;
                 }
-                for (int e = tid; e < kKS * kN; e += 256) {
-                    const int k = e / kN, n = e % kN;
-                    Bs[k][n] = M[(size_t)(k0 + k) * kN + n];
+                const int h = g * p.hpg + hh0 + (s >> 1);
+                const bool cterm = s & 1;
+                uint8_t* sg = stages + st * kSbStage;
+                const uint8_t* im = reinterpret_cast<const uint8_t*>(cterm ? p.Himg : p.dSimg) +
+                                    (((size_t)b * p.nc + c) * p.H + h) * 32768;
+                msc::mbar_arrive_expect_tx(&tfull[st], (cterm && has_z) ? 65536u : 49152u);
+                msc::tma_load_3d(sg, cterm ? &tmDy : &tmX, &tfull[st], h * kP, (int)(tc0 + j0), b);
+                if (cterm && has_z) msc::tma_load_3d(sg + 16384, &tmZ, &tfull[st], h * kP, (int)(tc0 + j0), b);
+                msc::bulk_g2s(sg + 32768, im, 32768u, &tfull[st]);
+                ++issued;
+            }
+            for (int st = 0; st < kSbStages && st < issued; ++st)
+                if (!msc::wait_bounded(&tfull[st], (uint32_t)(((issued - 1 - st) / kSbStages) & 1))) record_timeout(112);
+        }
+        __syncwarp();
+    } else if (warp == kSbWarpMma) {
+        if (lane == 0) {
+            const uint32_t idX = msc::idesc_f16(true, 128, kN, false, true);
+            bool ok = true;
+            for (int s = 0; s < ns && ok; ++s) {
+                const int st = s % kSbStages, use = s / kSbStages;
+                ok = msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort) &&
+                     msc::wait_bounded(&full[st], (uint32_t)(use & 1), abort);
+                if (!ok) break;
+                msc::tc_fence_after();
+                const uint32_t a = msc::smem_u32(stages + st * kSbStage);
+                const uint32_t acc = tmem + ((s & 1) ? 128u : 0u);
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t ah = msc::sdesc_sw128(a + 32 * k), al = msc::sdesc_sw128(a + 16384 + 32 * k);
+                    const uint64_t bh = msc::sdesc_sw128_mn(a + 32768 + 2048 * k, 8192u);
+                    const uint64_t bl = msc::sdesc_sw128_mn(a + 49152 + 2048 * k, 8192u);
+                    msc::mma_f16(acc, ah, bh, idX, (s > 1 || k) ? 1u : 0u);
+                    msc::mma_f16(acc, ah, bl, idX, 1u);
+                    msc::mma_f16(acc, al, bh, idX, 1u);
                 }
-                __syncthreads();
-                if (side)
-                    tile_fma<8>(&As[0][0], kKS + 1, &Bs[0][0], kN + 4, kKS, accC, tid);
-                else
-                    tile_fma<8>(&As[0][0], kKS + 1, &Bs[0][0], kN + 4, kKS, accB, tid);
+                msc::mma_commit(&empty[st]);
+            }
+            if (ok) {
+                msc::mma_commit(done);
+            } else {
+                record_timeout(113);
+                *abort = 1u;
+            }
+            msc::mma_commit(drain);
+            if (!msc::wait_bounded(drain, 0)) record_timeout(114);
+        }
+        __syncwarp();
+    } else {
+        bool ok = true;
+        for (int s = 0; s < ns; ++s) {
+            const int st = s % kSbStages, use = s / kSbStages;
+            const int h = g * p.hpg + hh0 + (s >> 1);
+            const bool cterm = s & 1;
+            uint8_t* sg = stages + st * kSbStage;
+            ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort));
+            if (!ok) break;
+            const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
+            const float csl_last = p.cs[dbase + Q - 1] * MSC_LOG2E;
+            // 1024 chunks of 16 bytes (8 p of one row) per tile, 4 per thread
+#pragma unroll 1
+            for (int r = 0; r < 4; ++r) {
+                const int u = tid + 256 * r;
+                const int row = u >> 3;
+                float wr = 0.f;
+                if (row < rows_valid) {
+                    const float csl = p.cs[dbase + j0 + row] * MSC_LOG2E;
+                    wr = cterm ? msc::ex2_approx(csl) : msc::ex2_approx(csl_last - csl) * p.dt[dbase + j0 + row];
+                }
+                uint4* ph = reinterpret_cast<uint4*>(sg + 16 * u);
+                uint4* pl = reinterpret_cast<uint4*>(sg + 16384 + 16 * u);
+                const uint4 xv = *ph;
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                uint32_t zw[4] = {0u, 0u, 0u, 0u};
+                if (cterm && has_z) {
+                    const uint4 zv = *pl;
+                    zw[0] = zv.x; zw[1] = zv.y; zw[2] = zv.z; zw[3] = zv.w;
+                }
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float a0 = msc::bf16lo(xw[q]) * wr, a1 = msc::bf16hi(xw[q]) * wr;
+                    if (cterm && has_z) {
+                        a0 *= msc::silu_f(msc::bf16lo(zw[q]));
+                        a1 *= msc::silu_f(msc::bf16hi(zw[q]));
+                    }
+                    msc::split_bf16x2(a0, a1, hi[q], lo[q]);
+                }
+                *ph = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *pl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            msc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) msc::mbar_arrive(&full[st]);
+            // the next use of this stage is loaded only after these MMAs (empty), so no wait here
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(115);
+            *abort = 1u;
+        }
+        ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(done, 0, abort));
+        msc::tc_fence_after();
+        if (ok) {
+            const int lq = warp & 3, half = warp >> 2;
+            const int row = 32 * lq + lane;
+            const int64_t t = tc0 + j0 + row;
+            const bool valid = row < rows_valid && t < p.L;
+            const size_t o = (((size_t)b * p.L + t) * p.Gr + g) * kN + 64 * half;
+#pragma unroll 1
+            for (int term = 0; term < 2; ++term) {
+                float* dst = (term ? p.dC : p.dB) + o;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float v[16];
+                    msc::tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)(128 * term + 64 * half + 16 * q), v);
+                    msc::tmem_ld_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) red_add_v4(dst + 16 * q + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
+                    }
+                }
             }
         }
+        msc::tc_fence_before();
     }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int64_t t = t0 + ty * 4 + r;
-        if (t >= p.L) continue;
-        const size_t o = (((size_t)b * p.L + t) * p.Gr + g) * kN + tx * 8;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            atomicAdd(p.dB + o + cc, accB[r][cc]);
-            atomicAdd(p.dC + o + cc, accC[r][cc]);
-        }
+    __syncthreads();
+    if (warp == 0) {
+        msc::tc_fence_after();
+        msc::tmem_dealloc(tmem, 256);
     }
 }
 
@@ -887,45 +1185,54 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd bwd memset: %s", cudaGetErrorString(e));
     const unsigned nb = (unsigned)(f.Q / kT), ntri = nb * (nb + 1) / 2;
     const unsigned B = (unsigned)f.batch, H = (unsigned)f.H, nc = (unsigned)p.nc, BG = (unsigned)(f.batch * f.G);
-    ssd_gdz_kernel<<<dim3((unsigned)((f.L + 63) / 64), H, B), 256, 0, st>>>(p);
-    if ((s = check_launch("ssd_gdz")) != MSC_OK) return s;
-    ssd_gmat_kernel<<<dim3(ntri, nc, BG), 256, 0, st>>>(p);
-    if ((s = check_launch("ssd_gmat")) != MSC_OK) return s;
-    ssd_u_kernel<<<dim3(nc, H, B), 256, 0, st>>>(p);
-    if ((s = check_launch("ssd_u")) != MSC_OK) return s;
-    ssd_rpass_kernel<<<dim3(H * (kP * kN / 8) / 256, B), 256, 0, st>>>(p);
-    if ((s = check_launch("ssd_rpass")) != MSC_OK) return s;
-    ssd_dg_kernel<<<dim3(ntri, nc, BG), 256, 0, st>>>(p);
-    if ((s = check_launch("ssd_dg")) != MSC_OK) return s;
-    ssd_dbc_kernel<<<dim3(2 * nb, nc, BG), 256, 0, st>>>(p);
-    if ((s = check_launch("ssd_dbc")) != MSC_OK) return s;
+    // B, C as [128 steps][64 n] boxes; x, dy, z as [64 steps][64 p] and [128 steps][64 p] boxes
+    // (bf16, 128-byte swizzle)
+    CUtensorMap mB, mC, mDy, mZ, mX128, mDy128, mZ128;
     {
-        // B, C as [128 steps][64 n] boxes; dy, z as [64 steps][64 p] boxes (bf16, 128-byte swizzle)
-        CUtensorMap mB, mC, mDy, mZ;
         const uint64_t bcd[3] = {(uint64_t)(f.G * kN), (uint64_t)f.L, (uint64_t)f.batch};
         const uint64_t bcs[2] = {(uint64_t)(f.G * kN * 2), (uint64_t)(f.L * f.G * kN * 2)};
         const uint64_t xd[3] = {(uint64_t)(f.H * kP), (uint64_t)f.L, (uint64_t)f.batch};
         const uint64_t xs[2] = {(uint64_t)(f.H * kP * 2), (uint64_t)(f.L * f.H * kP * 2)};
         const uint32_t box128[3] = {64, 128, 1}, box64[3] = {64, 64, 1};
+        const void* zsrc = f.z ? f.z : a.dy;  // unused without a gate
         if (!encode_tmap(&mB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, f.B, bcd, bcs, box128, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_tmap(&mC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, f.C, bcd, bcs, box128, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_tmap(&mDy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.dy, xd, xs, box64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_tmap(&mZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, f.z ? f.z : a.dy, xd, xs, box64,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
+            !encode_tmap(&mZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, zsrc, xd, xs, box64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&mX128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, f.x, xd, xs, box128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&mDy128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.dy, xd, xs, box128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&mZ128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, zsrc, xd, xs, box128, CU_TENSOR_MAP_SWIZZLE_128B))
             return MSC_ERR_CUDA;
         static bool configured = false;
         if (!configured) {
             cudaError_t e2 = cudaFuncSetAttribute(ssd_dx_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmem);
-            if (e2 != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_dx_tc smem attribute: %s", cudaGetErrorString(e2));
+            if (e2 == cudaSuccess)
+                e2 = cudaFuncSetAttribute(ssd_dbcs_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSbSmem);
+            if (e2 == cudaSuccess)
+                e2 = cudaFuncSetAttribute(ssd_dg_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDgSmem);
+            if (e2 != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd bwd smem attribute: %s", cudaGetErrorString(e2));
             configured = true;
         }
-        const unsigned nmb = (unsigned)((f.Q + 127) / 128);
+    }
+    const unsigned nmb = (unsigned)((f.Q + 127) / 128), ntri128 = nmb * (nmb + 1) / 2;
+    ssd_gdz_kernel<<<dim3((unsigned)((f.L + 63) / 64), H, B), 256, 0, st>>>(p);
+    if ((s = check_launch("ssd_gdz")) != MSC_OK) return s;
+    ssd_gmat_kernel<<<dim3(ntri, nc, BG), 256, 0, st>>>(p);
+    if ((s = check_launch("ssd_gmat")) != MSC_OK) return s;
+    if ((s = ssd_ugrad(f, a.dy, cs, p.U, st)) != MSC_OK) return s;
+    ssd_rpass_kernel<<<dim3(H * (kP * kN / 8) / 256, B), 256, 0, st>>>(p);
+    if ((s = check_launch("ssd_rpass")) != MSC_OK) return s;
+    ssd_dg_tc_kernel<<<dim3(ntri128, nc, BG), kDgThreads, kDgSmem, st>>>(mX128, mDy128, mZ128, p);
+    if ((s = check_launch("ssd_dg_tc")) != MSC_OK) return s;
+    ssd_dbc_kernel<<<dim3(2 * nb, nc, BG), 256, 0, st>>>(p);
+    if ((s = check_launch("ssd_dbc")) != MSC_OK) return s;
+    {
         ssd_dx_tc_kernel<<<dim3(nc * nmb, H, B), kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, p);
         if ((s = check_launch("ssd_dx_tc")) != MSC_OK) return s;
+        const unsigned nhb = (unsigned)((p.hpg + kHBlk - 1) / kHBlk);
+        ssd_dbcs_tc_kernel<<<dim3(nc * nmb, (unsigned)f.G * nhb, B), kSbThreads, kSbSmem, st>>>(mX128, mDy128, mZ128, p);
+        if ((s = check_launch("ssd_dbcs_tc")) != MSC_OK) return s;
     }
-    const unsigned nhb = (unsigned)((p.hpg + kHBlk - 1) / kHBlk);
-    ssd_dbcs_kernel<<<dim3(nc * nb, (unsigned)f.G * nhb, B), 256, 0, st>>>(p);
-    if ((s = check_launch("ssd_dbcs")) != MSC_OK) return s;
     ssd_dcs_kernel<<<dim3(nc, H, B), 256, 0, st>>>(p);
     return check_launch("ssd_dcs");
 }

@@ -131,19 +131,27 @@ struct StateSmem {
     uint64_t* bars;  // 0: B, 1-2: x buffers, 3-4: MMA of a buffer
 };
 
-__device__ __forceinline__ void state_issue_head(const StateSmem m, const CUtensorMap* tmX, const SsdParams& p,
-                                                 int h, int s, int c, int b) {
+__device__ __forceinline__ void state_issue_head(const StateSmem m, const CUtensorMap* tmX, const CUtensorMap* tmZ,
+                                                 const SsdParams& p, int h, int s, int c, int b) {
     const int Q = p.Q;
     const uint32_t tile = (uint32_t)Q * 128u;
     const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)c * Q;
-    msc::mbar_arrive_expect_tx(&m.bars[1 + s], tile + 8u * (uint32_t)Q);
+    msc::mbar_arrive_expect_tx(&m.bars[1 + s], (tmZ ? 2u : 1u) * tile + 8u * (uint32_t)Q);
     msc::tma_load_3d(m.sX + s * tile, tmX, &m.bars[1 + s], h * kP, c * Q, b);
+    if (tmZ) msc::tma_load_3d(m.sL + s * tile, tmZ, &m.bars[1 + s], h * kP, c * Q, b);
     bulk_g2s(m.s_dc + s * 512, p.dt + dbase, 4u * (uint32_t)Q, &m.bars[1 + s]);
     bulk_g2s(m.s_dc + s * 512 + 256, p.cs + dbase, 4u * (uint32_t)Q, &m.bars[1 + s]);
 }
 
+// kMode 0: the chunk states above.  The same product with other operands gives
+// the backward's U_c^T[n, p] = sum_i C_i[n] exp(cs_i) g_i[p] (the gradient that
+// reaches the state entering chunk c from the chunk's own outputs): tmB maps C,
+// tmX maps dy, and with kMode 2 tmZ maps z, which lands in the lo buffer and
+// gates g = dy silu(z) before the split; the result goes to p.S.
+template <int kMode>
 __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ CUtensorMap tmB,
-                                                        const __grid_constant__ CUtensorMap tmX, const SsdParams p) {
+                                                        const __grid_constant__ CUtensorMap tmX,
+                                                        const __grid_constant__ CUtensorMap tmZ, const SsdParams p) {
     extern __shared__ uint8_t s_dyn[];
     uint8_t* base = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);  // 1024-aligned, still a shared address
     const int Q = p.Q;
@@ -173,7 +181,8 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
         msc::prefetch_tmap(&tmX);
         msc::mbar_arrive_expect_tx(&m.bars[0], 2 * tile);
         for (int nb = 0; nb < 2; ++nb) msc::tma_load_3d(m.sB + nb * tile, &tmB, &m.bars[0], g * kN + nb * 64, c * Q, b);
-        for (int it = 0; it < 2 && it < nh; ++it) state_issue_head(m, &tmX, p, h0 + it, it, c, b);
+        if (kMode == 2) msc::prefetch_tmap(&tmZ);
+        for (int it = 0; it < 2 && it < nh; ++it) state_issue_head(m, &tmX, kMode == 2 ? &tmZ : nullptr, p, h0 + it, it, c, b);
     }
     __syncthreads();
     const uint32_t tmem = *slot;
@@ -205,7 +214,8 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
                 failed = true;
                 break;
             }
-            if (tid == 0 && it + 1 < nh) state_issue_head(m, &tmX, p, h0 + it + 1, s ^ 1, c, b);
+            if (tid == 0 && it + 1 < nh)
+                state_issue_head(m, &tmX, kMode == 2 ? &tmZ : nullptr, p, h0 + it + 1, s ^ 1, c, b);
         }
         ok = msc::wait_bounded(&m.bars[1 + s], (uint32_t)((it >> 1) & 1)) && ok;
         if (__syncthreads_or(!ok)) {
@@ -223,13 +233,24 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
             const float cs_last = s_cs[Q - 1];
             for (int u = tid; u < Q * 8; u += 256) {
                 const int j = u >> 3;
-                const float wj = msc::ex2_approx((cs_last - s_cs[j]) * MSC_LOG2E) * s_dt[j];
+                const float wj = kMode == 0 ? msc::ex2_approx((cs_last - s_cs[j]) * MSC_LOG2E) * s_dt[j]
+                                            : msc::ex2_approx(s_cs[j] * MSC_LOG2E);
                 uint4 v = *reinterpret_cast<const uint4*>(xs + u * 16);
                 uint32_t w[4] = {v.x, v.y, v.z, v.w}, hi[4], lo[4];
                 const uint64_t wj2 = msc::pk2(wj, wj);
+                if (kMode == 2) {
+                    const uint4 zv = *reinterpret_cast<const uint4*>(ls + u * 16);
+                    const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    split_bf16x2_packed(msc::mul2(wj2, msc::pk2(msc::bf16lo(w[e]), msc::bf16hi(w[e]))), hi[e], lo[e]);
+                    for (int e = 0; e < 4; ++e)
+                        split_bf16x2_packed(msc::mul2(msc::mul2(wj2, msc::pk2(msc::bf16lo(w[e]), msc::bf16hi(w[e]))),
+                                                      msc::silu_2(msc::pk2(msc::bf16lo(zw[e]), msc::bf16hi(zw[e])))),
+                                            hi[e], lo[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        split_bf16x2_packed(msc::mul2(wj2, msc::pk2(msc::bf16lo(w[e]), msc::bf16hi(w[e]))), hi[e], lo[e]);
+                }
                 *reinterpret_cast<uint4*>(xs + u * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4*>(ls + u * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
@@ -757,11 +778,12 @@ msc_status ssd_launch(const SsdArgs& a, cudaStream_t st) {
     {
         static bool configured = false;
         if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
+            cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_state smem attribute: %s", cudaGetErrorString(e));
             configured = true;
         }
-        ssd_state_kernel<<<dim3(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch), 256, state_smem(p.Q), st>>>(m.B, m.xq, p);
+        ssd_state_kernel<0><<<dim3(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch), 256, state_smem(p.Q), st>>>(
+            m.B, m.xq, m.xq, p);
         if ((s = check_launch("ssd_state")) != MSC_OK) return s;
     }
     // (3) inter-chunk state pass
@@ -816,11 +838,16 @@ msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* H
     {
         static bool configured = false;
         if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
+            cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(ssd_state_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(ssd_state_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_state smem attribute: %s", cudaGetErrorString(e));
             configured = true;
         }
-        ssd_state_kernel<<<dim3(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch), 256, state_smem(p.Q), st>>>(mB, mX, p);
+        ssd_state_kernel<0><<<dim3(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch), 256, state_smem(p.Q), st>>>(
+            mB, mX, mX, p);
         if ((s = check_launch("ssd_state")) != MSC_OK) return s;
     }
     const int64_t per_b = (int64_t)p.H * kP * kN;
@@ -830,6 +857,33 @@ msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* H
     p.final_state = nullptr;
     ssd_pass_kernel<<<dim3((unsigned)((per_b / 8 + 255) / 256), (unsigned)a.batch), 256, 0, st>>>(p);
     return check_launch("ssd_pass");
+}
+
+msc_status ssd_ugrad(const SsdArgs& a, const void* dy, const float* cs, float* U, cudaStream_t st) {
+    SsdParams p{};
+    p.L = a.L; p.batch = (int)a.batch; p.H = (int)a.H; p.G = (int)a.G; p.hpg = (int)(a.H / a.G); p.Q = (int)a.Q;
+    p.nc = (int)((a.L + a.Q - 1) / a.Q);
+    p.Lp = (int64_t)p.nc * a.Q;
+    if (p.hpg % kHBS != 0 && p.G != 1) return fail(MSC_ERR_UNSUPPORTED, "heads per group must be a multiple of %d", kHBS);
+    p.cs = const_cast<float*>(cs);
+    p.dt = const_cast<float*>(cs);  // read into shared memory with cs; unused by the U weights
+    p.S = U;
+    CUtensorMap mC, mDy, mZ;
+    const uint64_t bcd[3] = {(uint64_t)(a.G * kN), (uint64_t)a.L, (uint64_t)a.batch};
+    const uint64_t bcs[2] = {(uint64_t)(a.G * kN * 2), (uint64_t)(a.L * a.G * kN * 2)};
+    const uint32_t qbox[3] = {64, (uint32_t)p.Q, 1};
+    const uint64_t xd[3] = {(uint64_t)(a.H * kP), (uint64_t)a.L, (uint64_t)a.batch};
+    const uint64_t xs[2] = {(uint64_t)(a.H * kP * 2), (uint64_t)(a.L * a.H * kP * 2)};
+    if (!encode_tmap(&mC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.C, bcd, bcs, qbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap(&mDy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dy, xd, xs, qbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap(&mZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.z ? a.z : dy, xd, xs, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MSC_ERR_CUDA;
+    const dim3 grid(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch);
+    if (a.z)
+        ssd_state_kernel<2><<<grid, 256, state_smem(p.Q), st>>>(mC, mDy, mZ, p);
+    else
+        ssd_state_kernel<1><<<grid, 256, state_smem(p.Q), st>>>(mC, mDy, mZ, p);
+    return check_launch("ssd_ugrad");
 }
 
 msc_status ssd_take_status(unsigned int* code, unsigned int* site) {
