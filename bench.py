@@ -386,11 +386,14 @@ def leg_conv1d(peaks, pipes, steps=10, warmup=3):
     return res
 
 
+SSD_BATCH = 4  # batch of the SSD legs (--ssd-batch; 1 for a profiling-size run)
+
+
 def leg_ssd(peaks, pipes, steps=5, warmup=2):
     import torch
     import selective_state_space_160_b300 as msc
     from selective_state_space_160_b300.inputs import ssd_inputs, bf16_bits
-    b, L, H, P, N, Q = 4, 4096, 80, 64, 128, 256
+    b, L, H, P, N, Q = SSD_BATCH, 4096, 80, 64, 128, 256
     inp = ssd_inputs(b, L, H, P, N, 1, seed=160_004, bf16=True)
 
     def dev(a, bf):
@@ -417,7 +420,7 @@ def leg_ssd(peaks, pipes, steps=5, warmup=2):
     ten["frac"] = ten["achieved"] / ten["peak"]
     bound = "hbm" if hbm["frac"] >= ten["frac"] else "tensor"
     sel = hbm if bound == "hbm" else ten
-    res = {"workload": "SSD fwd batch 4, heads 80, P 64, N 128, L 4096, chunk 256, bf16", "elements_per_s": el / t,
+    res = {"workload": "SSD fwd batch %d, heads 80, P 64, N 128, L 4096, chunk 256, bf16" % b, "elements_per_s": el / t,
            "ms": ms, "roofline": {"bound": bound, "achieved": sel["achieved"], "peak": sel["peak"],
                                   "unit": sel["unit"], "frac": sel["frac"], "traffic": None,
                                   "terms": {"hbm": hbm, "tensor": ten}}}
@@ -448,7 +451,7 @@ def leg_ssd_bwd(peaks, pipes, steps=5, warmup=2):
     import torch
     import selective_state_space_160_b300 as msc
     from selective_state_space_160_b300.inputs import ssd_inputs, bf16_bits
-    b, L, H, P, N, Q = 4, 4096, 80, 64, 128, 256
+    b, L, H, P, N, Q = SSD_BATCH, 4096, 80, 64, 128, 256
     inp = ssd_inputs(b, L, H, P, N, 1, seed=160_006, bf16=True, with_dy=True)
 
     def dev(a, bf):
@@ -480,7 +483,7 @@ def leg_ssd_bwd(peaks, pipes, steps=5, warmup=2):
     for v in (alu, hbm):
         v["frac"] = v["achieved"] / v["peak"]
     sel = alu if alu["frac"] >= hbm["frac"] else hbm
-    res = {"workload": "SSD bwd batch 4, heads 80, P 64, N 128, L 4096, chunk 256, bf16 in / fp32 grads",
+    res = {"workload": "SSD bwd batch %d, heads 80, P 64, N 128, L 4096, chunk 256, bf16 in / fp32 grads" % b,
            "elements_per_s": el / t, "ms": ms,
            "roofline": {"bound": "alu" if sel is alu else "hbm", "achieved": sel["achieved"], "peak": sel["peak"],
                         "unit": sel["unit"], "frac": sel["frac"], "traffic": None, "macs": macs,
@@ -697,7 +700,10 @@ def main(argv=None):
     ap.add_argument("--legs", default="fwd_long,bwd,ssd,ssd_bwd,decode,conv1d,disc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ssd-batch", type=int, default=4, help="batch of the SSD legs (4 = the timed workload)")
     args = ap.parse_args(argv)
+    global SSD_BATCH
+    SSD_BATCH = args.ssd_batch
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

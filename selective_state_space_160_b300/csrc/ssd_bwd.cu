@@ -27,17 +27,17 @@
 // and the state parts of dB, dC run on tcgen05 with fp32 operands split into
 // bf16 hi + lo; G = C B^T and dC, dB from dG are 64-row tiles of fp32 FMAs
 // staged through shared memory):
-//   ssd_gdz_kernel      dz, dD
 //   ssd_gmat_kernel     G = C B^T per (chunk, group), lower block triangle
 //   ssd_ugrad           U_c per (chunk, head): the forward's chunk-state kernel on dy, C
-//   ssd_rpass_kernel    reverse state pass: dS_c in place of U_c, dcs_last
+//   ssd_rpass_kernel    reverse state pass: dS_c (bf16 hi + lo images), dcs_last
 //   ssd_dg_tc_kernel    dG per (chunk, group, 128 x 128 tile) over its heads; dDelta, dcs of Y_diag
 //   ssd_dbc_kernel      dC, dB from dG
-//   ssd_dx_tc_kernel    dx per (chunk, head, 128 steps); dDelta, dcs of the state and Y_off terms
+//   ssd_dx_tc_kernel    dx, dz, dD per (chunk, head, 128 steps); dDelta, dcs of the state and Y_off terms
 //   ssd_dbcs_tc_kernel  state parts of dB, dC per (chunk, group, 128 steps, 16 heads)
 //   ssd_dcs_kernel      cs -> Delta, A; ddelta, dbias
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 
 #include "msc_common.cuh"
@@ -65,7 +65,7 @@ struct SsdBwdParams {
     const float* ypre;                           // [b, L, H, P] pre-gate output (z given)
     const float *dt, *cs;                        // [b, H, Lp]
     const float* Hin;                            // [b, nc, H, P, N]
-    float* U;                                    // [b, nc, H, P, N]: U_c, then dS_c
+    const float* U;                              // [b, nc, H, P, N]: U_c
     uint16_t* dSimg;                             // [b, nc, H] (hi, lo) bf16 images of dS_c, K-major [64 p][128 n] SW128
     const uint16_t* Himg;                        // the same images of Hin
     float *Gm, *dG;                              // [b, nc, Gr, Q, Q]
@@ -73,12 +73,19 @@ struct SsdBwdParams {
     float *dx, *ddelta, *dA, *dB, *dC, *dD, *dz, *dbias;
     int64_t L, Lp;
     int batch, H, Gr, hpg, Q, nc;
+    int dg_hpb;                                  // heads per CTA of the dG kernel
 };
 
 __device__ __forceinline__ float bfv(uint16_t v) { return __uint_as_float(((uint32_t)v) << 16); }
 
 __device__ __forceinline__ float bval(const uint16_t* M, const SsdBwdParams& p, int b, int64_t t, int g, int n) {
     return t < p.L ? bfv(M[(((size_t)b * p.L + t) * p.Gr + g) * kN + n]) : 0.f;
+}
+
+// vector reduction into global memory (16-byte aligned)
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
 }
 
 // acc[r][c] += sum_{k < K} As[(ty * 4 + r) * lda + k] * Bs[k * ldb + tx * TC + c]:
@@ -107,41 +114,6 @@ __device__ __forceinline__ void zero_acc(float (&acc)[4][TC]) {
     for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int c = 0; c < TC; ++c) acc[r][c] = 0.f;
-}
-
-// ------------------------------------------------------------------ gate, dz, dD
-// CTA = (64 steps, head, batch); thread = (step, 16 channels).
-__global__ void __launch_bounds__(256) ssd_gdz_kernel(const SsdBwdParams p) {
-    __shared__ float s_red[8];
-    const int b = blockIdx.z, h = blockIdx.y;
-    const int tid = threadIdx.x;
-    const int64_t t = (int64_t)blockIdx.x * 64 + (tid >> 2);
-    const int p0 = (tid & 3) * 16;
-    float dd = 0.f;
-    if (t < p.L) {
-#pragma unroll 4
-        for (int e = 0; e < 16; ++e) {
-            const size_t o = (((size_t)b * p.L + t) * p.H + h) * kP + p0 + e;
-            const float dyv = bfv(p.dy[o]);
-            float gv = dyv;
-            if (p.z) {
-                const float zv = bfv(p.z[o]);
-                const float sg = msc::sigmoid_f(zv);
-                gv = dyv * zv * sg;
-                p.dz[o] = dyv * p.ypre[o] * sg * (1.f + zv * (1.f - sg));
-            }
-            dd = fmaf(gv, bfv(p.x[o]), dd);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
-    if ((tid & 31) == 0) s_red[tid >> 5] = dd;
-    __syncthreads();
-    if (tid == 0 && p.dD) {
-        float s = 0.f;
-        for (int w = 0; w < 8; ++w) s += s_red[w];
-        atomicAdd(p.dD + h, s);
-    }
 }
 
 // ------------------------------------------------------------------ G = C B^T
@@ -177,75 +149,91 @@ __global__ void __launch_bounds__(256) ssd_gmat_kernel(const SsdBwdParams p) {
 }
 
 // ------------------------------------------------------------------ reverse state pass
-// Thread = (b, h, p, 8 consecutive n); 1024 threads per head, so every CTA of 256
-// belongs to one head.  Walking chunks last to first: dS_c = dH_{c+1} replaces
-// U_c, dH_c = U_c + exp(cs_last) dH_{c+1}, and dcs_last(c) += exp(cs_last) <Hin_c, dH_{c+1}>.
+// Thread = (b, h, p, 8 consecutive n).  Walking chunks last to first: dS_c =
+// dH_{c+1} (written as bf16 hi + lo tile images for the tensor cores),
+// dH_c = U_c + exp(cs_last) dH_{c+1}, and dcs_last(c) += exp(cs_last) <Hin_c, dH_{c+1}>
+// (a warp sum, then one atomic per warp).  U and Hin of four chunks are loaded
+// ahead of the dependent chain.
+constexpr int kRpAhead = 4;
+
 __global__ void __launch_bounds__(256) ssd_rpass_kernel(const SsdBwdParams p) {
-    __shared__ float s_red[8];
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int b = blockIdx.y;
+    const int lane = threadIdx.x & 31;
     constexpr int kN8 = kN / 8;
     const int n0 = (int)(idx % kN8) * 8;
     const int pp = (int)((idx / kN8) % kP);
     const int h = (int)(idx / (kN8 * kP));
     const size_t dbase = ((size_t)b * p.H + h) * p.Lp;
+    const uint32_t off = msc::sw128_offset(pp, n0, kP);
     float dh[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) dh[e] = 0.f;
-    for (int c = p.nc - 1; c >= 0; --c) {
-        const size_t o = ((((size_t)b * p.nc + c) * p.H + h) * kP + pp) * kN + n0;
-        float4* u4 = reinterpret_cast<float4*>(p.U + o);
-        const float4 ua = u4[0], ub = u4[1];
-        const float4 ha = reinterpret_cast<const float4*>(p.Hin + o)[0];
-        const float4 hb = reinterpret_cast<const float4*>(p.Hin + o)[1];
-        u4[0] = make_float4(dh[0], dh[1], dh[2], dh[3]);
-        u4[1] = make_float4(dh[4], dh[5], dh[6], dh[7]);
-        {
-            uint8_t* tile = reinterpret_cast<uint8_t*>(p.dSimg) + (((size_t)b * p.nc + c) * p.H + h) * 32768;
-            const uint32_t off = msc::sw128_offset(pp, n0, kP);
-            uint32_t hi[4], lo[4];
+    for (int ctop = p.nc - 1; ctop >= 0; ctop -= kRpAhead) {
+        float4 uv[kRpAhead][2], hv[kRpAhead][2];
+        float av[kRpAhead];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) msc::split_bf16x2(dh[2 * e], dh[2 * e + 1], hi[e], lo[e]);
-            *reinterpret_cast<uint4*>(tile + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(tile + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int k = 0; k < kRpAhead; ++k) {
+            const int c = ctop - k;
+            if (c >= 0) {
+                const size_t o = ((((size_t)b * p.nc + c) * p.H + h) * kP + pp) * kN + n0;
+                const float4* u4 = reinterpret_cast<const float4*>(p.U + o);
+                const float4* h4 = reinterpret_cast<const float4*>(p.Hin + o);
+                uv[k][0] = __ldcs(u4);
+                uv[k][1] = __ldcs(u4 + 1);
+                hv[k][0] = __ldcs(h4);
+                hv[k][1] = __ldcs(h4 + 1);
+                av[k] = p.cs[dbase + (size_t)c * p.Q + p.Q - 1];
+            }
         }
-        const float a = msc::ex2_approx(p.cs[dbase + (size_t)c * p.Q + p.Q - 1] * MSC_LOG2E);
-        float part = ha.x * dh[0] + ha.y * dh[1] + ha.z * dh[2] + ha.w * dh[3] + hb.x * dh[4] + hb.y * dh[5] +
-                     hb.z * dh[6] + hb.w * dh[7];
-        const float u8[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) dh[e] = fmaf(a, dh[e], u8[e]);
+        for (int k = 0; k < kRpAhead; ++k) {
+            const int c = ctop - k;
+            if (c < 0) break;
+            {
+                uint8_t* tile = reinterpret_cast<uint8_t*>(p.dSimg) + (((size_t)b * p.nc + c) * p.H + h) * 32768;
+                uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = part;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float sum = 0.f;
-            for (int w = 0; w < 8; ++w) sum += s_red[w];
-            if (sum != 0.f) atomicAdd(p.dcs + dbase + (size_t)c * p.Q + p.Q - 1, a * sum);
+                for (int e = 0; e < 4; ++e) msc::split_bf16x2(dh[2 * e], dh[2 * e + 1], hi[e], lo[e]);
+                *reinterpret_cast<uint4*>(tile + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(tile + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            const float a = msc::ex2_approx(av[k] * MSC_LOG2E);
+            const float h8[8] = {hv[k][0].x, hv[k][0].y, hv[k][0].z, hv[k][0].w,
+                                 hv[k][1].x, hv[k][1].y, hv[k][1].z, hv[k][1].w};
+            const float u8[8] = {uv[k][0].x, uv[k][0].y, uv[k][0].z, uv[k][0].w,
+                                 uv[k][1].x, uv[k][1].y, uv[k][1].z, uv[k][1].w};
+            float part = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                part = fmaf(h8[e], dh[e], part);
+                dh[e] = fmaf(a, dh[e], u8[e]);
+            }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+            if (lane == 0 && part != 0.f) atomicAdd(p.dcs + dbase + (size_t)c * p.Q + p.Q - 1, a * part);
         }
-        __syncthreads();
     }
 }
 
 // ------------------------------------------------------------------ dG on tcgen05
-// CTA = (128 x 128 tile (ib, jb), jb <= ib, chunk, batch * Gr), looping over the
-// group's heads.  Per head the tensor cores form R = g_I x_J^T (M = 128 steps i,
-// N = 128 steps j, K = P; g is dy, or dy silu(z) split hi + lo) into one of two
-// tensor-memory buffers; the CUDA cores then take, per element with i >= j,
+// CTA = (128 x 128 tile (ib, jb) with jb <= ib, and a block of the group's heads;
+// chunk; batch * Gr).  Per head the tensor cores form R = g_I x_J^T (M = 128
+// steps i, N = 128 steps j, K = P; g is dy, or dy silu(z) split hi + lo) into one
+// of two tensor-memory buffers; the CUDA cores then take, per element with i >= j,
 //   er = E_ij R_ij,  dG_ij += er Delta_j,  p1 = er G_ij,
 //   dcs_i += sum_j Delta_j p1,  dDelta_j += sum_i p1,  dcs_j -= Delta_j sum_i p1,
-// with the dG accumulators in registers (thread = row i, 64 columns j) and G
-// in shared memory,
-// while the MMAs of the next head run.  Column sums: a butterfly over the 32
-// lanes of a warp, then the four row quarters through shared memory.
+// with the dG accumulators in registers (thread = row i, 64 columns j) and G in
+// shared memory, while the MMAs of the next head run.  Column sums: a butterfly
+// over the 32 lanes of a warp, then the four row quarters through shared memory.
+// The head blocks of a tile add their dG with vector reductions (dG starts at 0).
 constexpr int kDgStages = 3;
 constexpr uint32_t kDgStage = 49152;           // A hi [128][64] | A lo (z) | B = x [128][64]
 constexpr int kDgOpWarps = 8;
 constexpr int kDgWarpLoad = kDgOpWarps, kDgWarpMma = kDgOpWarps + 1;
 constexpr int kDgThreads = (kDgOpWarps + 2) * 32;
-constexpr int kDgGld = 129;                    // row stride (floats) of the G tile in shared memory
-constexpr size_t kDgSmem = 1024 + kDgStages * kDgStage + (2 * 128 * 3 + 2 * 4 * 64 + 2 * 128 + 128 * kDgGld) * 4 + 16 * 8 + 16;
+constexpr int kDgGld = 132;                    // row stride (floats) of the G tile: 16-byte rows
+constexpr size_t kDgSmem = 1024 + kDgStages * kDgStage + (3 * 128 * 3 + 2 * 4 * 64 + 2 * 128 + 128 * kDgGld) * 4 + 20 * 8 + 16;
 
 // v[0..15] of every lane -> sum over the warp's 32 lanes of v[lane >> 1]
 __device__ __forceinline__ float warp_colsum16(float (&v)[16], int lane) {
@@ -285,30 +273,35 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
                                                                   const SsdBwdParams p) {
     extern __shared__ uint8_t s_dyn[];
     uint8_t* stages = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);
-    float* s_ci = reinterpret_cast<float*>(stages + kDgStages * kDgStage);  // [2 heads][128] cs_i log2(e)
-    float* s_cj = s_ci + 256;                                              // [2][128] cs_j log2(e)
-    float* s_dj = s_cj + 256;                                              // [2][128] Delta_j
-    float* s_col = s_dj + 256;                                             // [2 halves][4 quarters][64]
+    // cs of the tile's rows i and columns j and Delta of its columns, per head, in
+    // a ring of three (bulk copies with the head's tiles)
+    float* s_ci = reinterpret_cast<float*>(stages + kDgStages * kDgStage);  // [3][128]
+    float* s_cj = s_ci + 384;                                              // [3][128]
+    float* s_dj = s_cj + 384;                                              // [3][128]
+    float* s_col = s_dj + 384;                                             // [2 halves][4 quarters][64]
     float* s_row = s_col + 512;                                            // [2 halves][128]
     float* s_G = s_row + 256;                                              // [128 i][kDgGld] G of the tile
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_G + 128 * kDgGld);
-    // 0-2 stage loaded, 3-5 stage built, 6-8 stage free, 9-10 R ready, 11-12 R read, 13 drain
+    // 0-2 stage loaded, 3-5 stage built, 6-8 stage free, 9-10 R ready, 11-12 R read, 13 drain,
+    // 14-16 the head's cs / Delta rows read
     uint64_t *tfull = bars, *full = bars + 3, *empty = bars + 6, *rfull = bars + 9, *rfree = bars + 11,
-             *drain = bars + 13;
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 14);
+             *drain = bars + 13, *cfree = bars + 14;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 17);
     volatile uint32_t* abort = slot + 1;
 
     const int Q = p.Q;
-    const int nt = (Q + 127) / 128;
-    int ib = 0, rem = blockIdx.x;
+    const int nhb = (p.hpg + p.dg_hpb - 1) / p.dg_hpb;
+    const int tile = blockIdx.x / nhb, hb = blockIdx.x % nhb;
+    int ib = 0, rem = tile;
     while (rem > ib) { rem -= ib + 1; ++ib; }
     const int jb = rem;
-    (void)nt;
     const int c = blockIdx.y, b = blockIdx.z / p.Gr, g = blockIdx.z % p.Gr;
     const int rv = min(128, Q);                  // valid rows / columns of a tile (Q = 64: half)
-    const int nh = p.hpg;
+    const int hh0 = hb * p.dg_hpb;
+    const int nh = min(p.dg_hpb, p.hpg - hh0);
     const int64_t tc0 = (int64_t)c * Q;
     const bool has_z = p.z != nullptr;
+    const bool diag_tile = ib == jb;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (warp == 0) {
@@ -325,10 +318,12 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             msc::mbar_init(&rfull[k], 1);
             msc::mbar_init(&rfree[k], kDgOpWarps);
         }
+        for (int k = 0; k < 3; ++k) msc::mbar_init(&cfree[k], kDgOpWarps);
         msc::mbar_init(drain, 1);
         slot[1] = 0u;
         msc::fence_barrier_init();
     }
+    for (int e = tid; e < 3 * 384; e += kDgThreads) s_ci[e] = 0.f;  // rows past a short chunk stay 0
     msc::tc_fence_before();
     __syncthreads();
     msc::tc_fence_after();
@@ -342,14 +337,20 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             int issued = 0;
             for (int hh = 0; hh < nh; ++hh) {
                 const int st = hh % kDgStages, use = hh / kDgStages;
-                if (use > 0 && !msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort)) {
+                if (use > 0 && !(msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort) &&
+                                 msc::wait_bounded(&cfree[st], (uint32_t)((use - 1) & 1), abort))) {
                     record_timeout(121);
                     *abort = 1u;
                     break;
                 }
-                const int h = g * p.hpg + hh;
+                const int h = g * p.hpg + hh0 + hh;
+                const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
                 uint8_t* sg = stages + st * kDgStage;
-                msc::mbar_arrive_expect_tx(&tfull[st], has_z ? 49152u : 32768u);
+                const uint32_t rb4 = 4u * (uint32_t)rv;
+                msc::mbar_arrive_expect_tx(&tfull[st], (has_z ? 49152u : 32768u) + 3u * rb4);
+                msc::bulk_g2s(s_ci + 128 * st, p.cs + dbase + 128 * ib, rb4, &tfull[st]);
+                msc::bulk_g2s(s_cj + 128 * st, p.cs + dbase + 128 * jb, rb4, &tfull[st]);
+                msc::bulk_g2s(s_dj + 128 * st, p.dt + dbase + 128 * jb, rb4, &tfull[st]);
                 msc::tma_load_3d(sg, &tmDy, &tfull[st], h * kP, (int)(tc0 + 128 * ib), b);
                 if (has_z) msc::tma_load_3d(sg + 16384, &tmZ, &tfull[st], h * kP, (int)(tc0 + 128 * ib), b);
                 msc::tma_load_3d(sg + 32768, &tmX, &tfull[st], h * kP, (int)(tc0 + 128 * jb), b);
@@ -432,49 +433,68 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             if (lane == 0) msc::mbar_arrive(&full[st]);
         };
         auto epilogue = [&](int hh) {
-            const int buf = hh & 1;
-            const int h = g * p.hpg + hh;
+            const int buf = hh & 1, cb = hh % 3;
+            const int h = g * p.hpg + hh0 + hh;
             const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
-            // this head's cs and Delta rows; the other buffer may still be read by
-            // the tail of the previous head, this one was last read two heads ago
-            if (tid < 128) {
-                const bool on = tid < rv;
-                s_ci[128 * buf + tid] = on ? p.cs[dbase + 128 * ib + tid] * MSC_LOG2E : 0.f;
-                s_cj[128 * buf + tid] = on ? p.cs[dbase + 128 * jb + tid] * MSC_LOG2E : 0.f;
-                s_dj[128 * buf + tid] = on ? p.dt[dbase + 128 * jb + tid] : 0.f;
-            }
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&rfull[buf], (uint32_t)((hh >> 1) & 1), abort));
+            ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&rfull[buf], (uint32_t)((hh >> 1) & 1), abort) &&
+                                                   msc::wait_bounded(&tfull[cb], (uint32_t)((hh / 3) & 1), abort));
             msc::tc_fence_after();
-            float rowt = 0.f;
-            const float csi = s_ci[128 * buf + row];
+            // the diagonal T_ii would enter dcs_i once as +T and once as -T: it is
+            // left out of both sums (exactly zero), which keeps the large diagonal
+            // terms of a fast-decaying chunk from cancelling in fp32; its dDelta
+            // share goes in separately
+            float rowt = 0.f, pdiag = 0.f;
+            const float csi = s_ci[128 * cb + row];
+            const float* cjp = s_cj + 128 * cb;
+            const float* djp = s_dj + 128 * cb;
+            const float* gp = s_G + row * kDgGld;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                float r[16], col[16];
-                if (ok) {
-                    msc::tmem_ld16(tmem + 128u * (uint32_t)buf + ((uint32_t)(32 * lq) << 16) + (uint32_t)(64 * half + 16 * q), r);
-                    msc::tmem_ld_wait();
-                } else {
+                const int c0 = 64 * half + 16 * q;
+                // warp-uniform: every element of the chunk lies above the diagonal or
+                // outside a short chunk
+                const bool skip = (diag_tile && c0 > 32 * lq + 31) || c0 >= rv || 32 * lq >= rv;
+                float cs_ = 0.f;
+                if (!skip) {
+                    float r[16], col[16];
+                    if (ok) {
+                        msc::tmem_ld16(tmem + 128u * (uint32_t)buf + ((uint32_t)(32 * lq) << 16) + (uint32_t)c0, r);
+                        msc::tmem_ld_wait();
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) r[e] = 0.f;
-                }
+                        for (int e = 0; e < 16; ++e) r[e] = 0.f;
+                    }
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int k = 16 * q + e, jj = 64 * half + k;
-                    const bool m = row_ok && jj < rv && il >= 128 * jb + jj;
-                    const float dj = s_dj[128 * buf + jj];
-                    const float er = m ? msc::ex2_approx(csi - s_cj[128 * buf + jj]) * r[e] : 0.f;
-                    dgacc[k] = fmaf(er, dj, dgacc[k]);
-                    const float p1 = er * s_G[row * kDgGld + jj];
-                    rowt = fmaf(p1, dj, rowt);
-                    col[e] = p1;
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        const float4 cj4 = *reinterpret_cast<const float4*>(cjp + c0 + 4 * e4);
+                        const float4 dj4 = *reinterpret_cast<const float4*>(djp + c0 + 4 * e4);
+                        const float4 g4 = *reinterpret_cast<const float4*>(gp + c0 + 4 * e4);
+                        const float cj[4] = {cj4.x, cj4.y, cj4.z, cj4.w};
+                        const float dj[4] = {dj4.x, dj4.y, dj4.z, dj4.w};
+                        const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int e = 4 * e4 + t, jj = c0 + e;
+                            const bool m = row_ok && jj < rv && (!diag_tile || row >= jj);
+                            // the difference first: |cs| reaches thousands in a fast-decaying chunk
+                            const float er = m ? msc::ex2_approx((csi - cj[t]) * MSC_LOG2E) * r[e] : 0.f;
+                            dgacc[16 * q + e] = fmaf(er, dj[t], dgacc[16 * q + e]);
+                            const float p1 = er * gv[t];
+                            const bool dg_ = diag_tile && row == jj;
+                            rowt = dg_ ? rowt : fmaf(p1, dj[t], rowt);
+                            col[e] = dg_ ? 0.f : p1;
+                            pdiag = dg_ ? p1 : pdiag;
+                        }
+                    }
+                    cs_ = warp_colsum16(col, lane);
                 }
-                const float cs_ = warp_colsum16(col, lane);
                 if ((lane & 1) == 0) s_col[256 * half + 64 * lq + 16 * q + (lane >> 1)] = cs_;
             }
             msc::tc_fence_before();
             __syncwarp();
             if (lane == 0) msc::mbar_arrive(&rfree[buf]);
+            if (pdiag != 0.f) atomicAdd(p.dDelta + dbase + il, pdiag);
             s_row[128 * half + row] = rowt;
             asm volatile("bar.sync 1, 256;" ::: "memory");
             if (tid < 128) {
@@ -483,13 +503,15 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
                                  s_col[256 * hf + 192 + k];
                 if (jj < rv && cd != 0.f) {
                     atomicAdd(p.dDelta + dbase + 128 * jb + jj, cd);
-                    atomicAdd(p.dcs + dbase + 128 * jb + jj, -s_dj[128 * buf + jj] * cd);
+                    atomicAdd(p.dcs + dbase + 128 * jb + jj, -djp[jj] * cd);
                 }
             } else {
                 const int r2 = tid - 128;
                 const float rt = s_row[r2] + s_row[128 + r2];
                 if (r2 < rv && rt != 0.f) atomicAdd(p.dcs + dbase + 128 * ib + r2, rt);
             }
+            __syncwarp();
+            if (lane == 0) msc::mbar_arrive(&cfree[cb]);
         };
         for (int hh = 0; hh <= nh; ++hh) {
             if (hh < nh) produce(hh);
@@ -499,13 +521,10 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             if (lane == 0) record_timeout(125);
             *abort = 1u;
         }
-        if (row_ok) {
+        if (row_ok && 64 * half < rv) {
             float* dst = p.dG + (((size_t)b * p.nc + c) * p.Gr + g) * (size_t)Q * Q + (size_t)il * Q + 128 * jb + 64 * half;
-            if (64 * half < rv) {
 #pragma unroll
-                for (int k = 0; k < 64; k += 4)
-                    *reinterpret_cast<float4*>(dst + k) = make_float4(dgacc[k], dgacc[k + 1], dgacc[k + 2], dgacc[k + 3]);
-            }
+            for (int k = 0; k < 64; k += 4) red_add_v4(dst + k, dgacc[k], dgacc[k + 1], dgacc[k + 2], dgacc[k + 3]);
         }
         msc::tc_fence_before();
     }
@@ -573,9 +592,12 @@ __global__ void __launch_bounds__(256) ssd_dbc_kernel(const SsdBwdParams p) {
 //   acc3 = C_j . Hin[p, :]                 A: C tile by TMA; B: Hin hi, lo images
 // The operands stream through a ring of four 48 KB stages, one K slab of 64
 // each: A hi [128][64] | A lo | B hi [64][64] | B lo (bf16, 128-byte swizzle).
-// Slabs 0-1 feed acc2 (n blocks 0, 1), 2-3 acc3, then one per 64 steps i >= j0.
+// The first na slabs feed acc1, one per 64 steps i >= j0 (formed by the CUDA
+// cores while the later tiles load), then four by TMA: acc2 (n blocks 0, 1),
+// acc3 (n blocks 0, 1).
 // Epilogue (thread = row j, half of the p columns):
 //   dx_j = Delta_j acc1 + w_j acc2 + D g_j;  dw_j = x_j . acc2;  v_j = exp(cs_j) g_j . acc3
+// and, since it reads dy, x and z of the row anyway, the gate's dz and dD.
 constexpr int kDxStages = 4;
 constexpr uint32_t kDxStage = 49152;
 constexpr int kDxOpWarps = 8;
@@ -590,8 +612,8 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                                                                   const SsdBwdParams p) {
     extern __shared__ uint8_t s_dyn[];
     uint8_t* stages = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);
-    float* s_csl = reinterpret_cast<float*>(stages + kDxStages * kDxStage);  // cs log2(e) of the chunk
-    float* s_dt = s_csl + 256;
+    float* s_cs = reinterpret_cast<float*>(stages + kDxStages * kDxStage);   // cs of the chunk
+    float* s_dt = s_cs + 256;
     float* s_part = s_dt + 256;                                                // [dw, v][2 halves][128 rows]
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_part + 512);
     // 0-3 stage loaded (TMA), 4-7 stage built (8 warps), 8-9 free (MMA), 12 done, 13 drain
@@ -605,7 +627,8 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
     const int h = blockIdx.y, b = blockIdx.z, g = h / p.hpg;
     const int j0 = 128 * mb;
     const int rows_valid = min(128, Q - j0);
-    const int ns = 4 + (Q - j0) / 64;
+    const int na = (Q - j0) / 64;                // acc1 slabs
+    const int ns = na + 4;
     const int64_t tc0 = (int64_t)c * Q;
     const bool has_z = p.z != nullptr;
     const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
@@ -628,7 +651,7 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
         msc::fence_barrier_init();
     }
     if (tid < Q) {
-        s_csl[tid] = p.cs[dbase + tid] * MSC_LOG2E;
+        s_cs[tid] = p.cs[dbase + tid];
         s_dt[tid] = p.dt[dbase + tid];
     }
     msc::tc_fence_before();
@@ -652,15 +675,15 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                     break;
                 }
                 uint8_t* sg = stages + st * kDxStage;
-                if (s < 4) {
-                    const int which = s >> 1, kb = s & 1;
+                if (s >= na) {
+                    const int which = (s - na) >> 1, kb = (s - na) & 1;
                     const uint8_t* im = reinterpret_cast<const uint8_t*>(which ? p.Himg : p.dSimg) + img;
                     msc::mbar_arrive_expect_tx(&tfull[st], 32768u);
                     msc::tma_load_3d(sg, which ? &tmC : &tmB, &tfull[st], g * kN + 64 * kb, (int)(tc0 + j0), b);
                     msc::bulk_g2s(sg + 32768, im + 8192 * kb, 8192u, &tfull[st]);
                     msc::bulk_g2s(sg + 40960, im + 16384 + 8192 * kb, 8192u, &tfull[st]);
                 } else {
-                    const int i0 = j0 + 64 * (s - 4);
+                    const int i0 = j0 + 64 * s;
                     msc::mbar_arrive_expect_tx(&tfull[st], has_z ? 16384u : 8192u);
                     msc::tma_load_3d(sg + 32768, &tmDy, &tfull[st], h * kP, (int)(tc0 + i0), b);
                     if (has_z) msc::tma_load_3d(sg + 40960, &tmZ, &tfull[st], h * kP, (int)(tc0 + i0), b);
@@ -685,18 +708,19 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                 if (!ok) break;
                 msc::tc_fence_after();
                 const uint32_t a = msc::smem_u32(stages + st * kDxStage);
-                if (s < 4) {
-                    const uint32_t acc = tmem + (s < 2 ? 64u : 128u);
+                if (s >= na) {
+                    const int si = s - na;
+                    const uint32_t acc = tmem + (si < 2 ? 64u : 128u);
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t ad = msc::sdesc_sw128(a + 32 * k);
-                        msc::mma_f16(acc, ad, msc::sdesc_sw128(a + 32768 + 32 * k), idK, ((s & 1) || k) ? 1u : 0u);
+                        msc::mma_f16(acc, ad, msc::sdesc_sw128(a + 32768 + 32 * k), idK, ((si & 1) || k) ? 1u : 0u);
                         msc::mma_f16(acc, ad, msc::sdesc_sw128(a + 40960 + 32 * k), idK, 1u);
                     }
                 } else {
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t bh = msc::sdesc_sw128_mn(a + 32768 + 2048 * k, 8192u);
                         const uint64_t ah = msc::sdesc_sw128(a + 32 * k);
-                        msc::mma_f16(tmem, ah, bh, idX, (s > 4 || k) ? 1u : 0u);
+                        msc::mma_f16(tmem, ah, bh, idX, (s > 0 || k) ? 1u : 0u);
                         msc::mma_f16(tmem, msc::sdesc_sw128(a + 16384 + 32 * k), bh, idX, 1u);
                         if (has_z) msc::mma_f16(tmem, ah, msc::sdesc_sw128_mn(a + 40960 + 2048 * k, 8192u), idX, 1u);
                     }
@@ -721,28 +745,38 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
         for (int s = 0; s < ns; ++s) {
             const int st = s & 3, use = s >> 2;
             uint8_t* sg = stages + st * kDxStage;
-            if (s >= 4) {
-                if (use > 0) ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort));
-                if (!ok) break;
+            // every slab: the stage's previous MMAs are done before this use is
+            // announced (a full barrier may not run a phase ahead of its consumer)
+            if (use > 0) ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort));
+            if (!ok) break;
+            if (s < na) {
                 // A = (E o G)^T of this slab: rows j (128), K = 64 steps i from i0
-                const int i0 = j0 + 64 * (s - 4);
-#pragma unroll 1
+                const int i0 = j0 + 64 * s;
+                // thread: row (tid & 127), chunks kc = tid / 128 + 2 r of 8 steps; the 32
+                // loads of G are issued before any is used
+                const int row = tid & 127, j = j0 + row;
+                const bool row_on = row < rows_valid;
+                const float csj = s_cs[row_on ? j : 0];
+                float v[4][8];
+#pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const int e = tid + 256 * r;
-                    const int row = e & 127, kc = e >> 7;
-                    const int j = j0 + row, ib = i0 + 8 * kc;
+                    const int ib = i0 + 8 * ((tid >> 7) + 2 * r);
+                    const float* gcol = Gt + (size_t)ib * Q + j;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[r][q] = (row_on && ib + q >= j) ? gcol[q * Q] : 0.f;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int kc = (tid >> 7) + 2 * r, ib = i0 + 8 * kc;
                     uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
-                    if (row < rows_valid && ib + 7 >= j) {
-                        const float csj = s_csl[j];
-                        float v[8];
+                    if (row_on && ib + 7 >= j) {  // else the whole chunk lies above the diagonal
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             const int i = ib + q;
-                            v[q] = 0.f;
-                            if (i >= j) v[q] = Gt[(size_t)i * Q + j] * msc::ex2_approx(s_csl[i] - csj);
+                            v[r][q] = i >= j ? v[r][q] * msc::ex2_approx((s_cs[i] - csj) * MSC_LOG2E) : 0.f;
                         }
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) msc::split_bf16x2(v[2 * q], v[2 * q + 1], hi[q], lo[q]);
+                        for (int q = 0; q < 4; ++q) msc::split_bf16x2(v[r][2 * q], v[r][2 * q + 1], hi[q], lo[q]);
                     }
                     const uint32_t off = msc::sw128_offset(row, 8 * kc, 128);
                     *reinterpret_cast<uint4*>(sg + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -783,7 +817,7 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
         const int row = 32 * lq + lane, j = j0 + row;
         const int64_t t = tc0 + j;
         const bool valid = ok && row < rows_valid && t < p.L;
-        float dw = 0.f, v = 0.f, ej = 0.f, wj = 0.f, ecs = 0.f;
+        float dw = 0.f, v = 0.f, ej = 0.f, wj = 0.f, ecs = 0.f, dd = 0.f;
         if (ok) {
             const uint32_t ta = tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)(32 * half);
             float a1[32], a2[32], a3[32];
@@ -797,9 +831,9 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
             if (valid) {
                 const size_t o = (((size_t)b * p.L + t) * p.H + h) * kP + 32 * half;
                 const float dtj = s_dt[j];
-                ej = msc::ex2_approx(s_csl[Q - 1] - s_csl[j]);
+                ej = msc::ex2_approx((s_cs[Q - 1] - s_cs[j]) * MSC_LOG2E);
                 wj = ej * dtj;
-                ecs = msc::ex2_approx(s_csl[j]);
+                ecs = msc::ex2_approx(s_cs[j] * MSC_LOG2E);
                 const float Dh = p.D ? p.D[h] : 0.f;
 #pragma unroll
                 for (int q8 = 0; q8 < 4; ++q8) {
@@ -809,24 +843,43 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                     if (has_z) zv = *reinterpret_cast<const uint4*>(p.z + o + 8 * q8);
                     const uint32_t dwd[4] = {dv.x, dv.y, dv.z, dv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
                     const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
-                    float out[8];
+                    float yp[8];
+                    if (has_z) {
+                        const float4 y0 = *reinterpret_cast<const float4*>(p.ypre + o + 8 * q8);
+                        const float4 y1 = *reinterpret_cast<const float4*>(p.ypre + o + 8 * q8 + 4);
+                        yp[0] = y0.x; yp[1] = y0.y; yp[2] = y0.z; yp[3] = y0.w;
+                        yp[4] = y1.x; yp[5] = y1.y; yp[6] = y1.z; yp[7] = y1.w;
+                    }
+                    float out[8], dzo[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int q = 8 * q8 + e;
                         const float dyv = (e & 1) ? msc::bf16hi(dwd[e >> 1]) : msc::bf16lo(dwd[e >> 1]);
                         const float xvv = (e & 1) ? msc::bf16hi(xw[e >> 1]) : msc::bf16lo(xw[e >> 1]);
-                        const float gv = has_z ? dyv * msc::silu_f((e & 1) ? msc::bf16hi(zw[e >> 1]) : msc::bf16lo(zw[e >> 1]))
-                                               : dyv;
+                        float gv = dyv;
+                        if (has_z) {
+                            // gate: g = dy silu(z), dz = dy y_pre silu'(z)
+                            const float zz = (e & 1) ? msc::bf16hi(zw[e >> 1]) : msc::bf16lo(zw[e >> 1]);
+                            const float sg = msc::sigmoid_f(zz);
+                            gv = dyv * zz * sg;
+                            dzo[e] = dyv * yp[e] * sg * (1.f + zz * (1.f - sg));
+                        }
                         out[e] = dtj * a1[q] + wj * a2[q] + Dh * gv;
                         dw = fmaf(xvv, a2[q], dw);
                         v = fmaf(gv, a3[q], v);
+                        dd = fmaf(gv, xvv, dd);
                     }
                     msc::st_cs_v8(p.dx + o + 8 * q8, out);
+                    if (has_z) msc::st_cs_v8(p.dz + o + 8 * q8, dzo);
                 }
             }
         }
         s_part[128 * half + row] = dw;
         s_part[256 + 128 * half + row] = v;
+        // dD = sum g . x over steps and channels of the head
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
+        if (lane == 0 && p.dD && dd != 0.f) atomicAdd(p.dD + h, dd);
         asm volatile("bar.sync 1, 256;" ::: "memory");
         if (half == 0) {
             float lastp = 0.f;
@@ -834,8 +887,11 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                 const float dwt = dw + s_part[128 + row];
                 const float vt = v + s_part[384 + row];
                 atomicAdd(p.dDelta + dbase + j, ej * dwt);
-                atomicAdd(p.dcs + dbase + j, ecs * vt - wj * dwt);
-                lastp = wj * dwt;
+                // w_j dw_j goes to dcs_last and out of dcs_j: for j = last the two
+                // cancel exactly and are left out
+                const bool last = j == Q - 1;
+                atomicAdd(p.dcs + dbase + j, ecs * vt - (last ? 0.f : wj * dwt));
+                lastp = last ? 0.f : wj * dwt;
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) lastp += __shfl_xor_sync(0xffffffffu, lastp, off);
@@ -867,12 +923,7 @@ constexpr uint32_t kSbStage = 65536;
 constexpr int kSbOpWarps = 8;
 constexpr int kSbWarpLoad = kSbOpWarps, kSbWarpMma = kSbOpWarps + 1;
 constexpr int kSbThreads = (kSbOpWarps + 2) * 32;
-constexpr size_t kSbSmem = 1024 + kSbStages * kSbStage + 16 * 8 + 16;
-
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
+constexpr size_t kSbSmem = 1024 + kSbStages * kSbStage + kSbStages * 384 * 4 + 16 * 8 + 16;
 
 __global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                     const __grid_constant__ CUtensorMap tmDy,
@@ -880,7 +931,8 @@ __global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid
                                                                     const SsdBwdParams p) {
     extern __shared__ uint8_t s_dyn[];
     uint8_t* stages = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(stages + kSbStages * kSbStage);
+    float* s_cw = reinterpret_cast<float*>(stages + kSbStages * kSbStage);  // per stage: cs [256], Delta [128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_cw + kSbStages * 384);
     // 0-2 stage loaded (TMA), 3-5 stage built (8 warps), 6-8 free (MMA), 9 done, 10 drain
     uint64_t *tfull = bars, *full = bars + 3, *empty = bars + 6, *done = bars + 9, *drain = bars + 10;
     uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 11);
@@ -939,7 +991,10 @@ __global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid
                 uint8_t* sg = stages + st * kSbStage;
                 const uint8_t* im = reinterpret_cast<const uint8_t*>(cterm ? p.Himg : p.dSimg) +
                                     (((size_t)b * p.nc + c) * p.H + h) * 32768;
-                msc::mbar_arrive_expect_tx(&tfull[st], (cterm && has_z) ? 65536u : 49152u);
+                const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
+                msc::mbar_arrive_expect_tx(&tfull[st], ((cterm && has_z) ? 65536u : 49152u) + 4u * (uint32_t)(Q + rows_valid));
+                msc::bulk_g2s(s_cw + 384 * st, p.cs + dbase, 4u * (uint32_t)Q, &tfull[st]);
+                msc::bulk_g2s(s_cw + 384 * st + 256, p.dt + dbase + j0, 4u * (uint32_t)rows_valid, &tfull[st]);
                 msc::tma_load_3d(sg, cterm ? &tmDy : &tmX, &tfull[st], h * kP, (int)(tc0 + j0), b);
                 if (cterm && has_z) msc::tma_load_3d(sg + 16384, &tmZ, &tfull[st], h * kP, (int)(tc0 + j0), b);
                 msc::bulk_g2s(sg + 32768, im, 32768u, &tfull[st]);
@@ -985,22 +1040,21 @@ __global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid
         bool ok = true;
         for (int s = 0; s < ns; ++s) {
             const int st = s % kSbStages, use = s / kSbStages;
-            const int h = g * p.hpg + hh0 + (s >> 1);
             const bool cterm = s & 1;
             uint8_t* sg = stages + st * kSbStage;
             ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort));
             if (!ok) break;
-            const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
-            const float csl_last = p.cs[dbase + Q - 1] * MSC_LOG2E;
+            const float* scs = s_cw + 384 * st;
+            const float cs_last = scs[Q - 1];
             // 1024 chunks of 16 bytes (8 p of one row) per tile, 4 per thread
-#pragma unroll 1
+#pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int u = tid + 256 * r;
                 const int row = u >> 3;
                 float wr = 0.f;
                 if (row < rows_valid) {
-                    const float csl = p.cs[dbase + j0 + row] * MSC_LOG2E;
-                    wr = cterm ? msc::ex2_approx(csl) : msc::ex2_approx(csl_last - csl) * p.dt[dbase + j0 + row];
+                    const float csr = scs[j0 + row];
+                    wr = cterm ? msc::ex2_approx(csr * MSC_LOG2E) : msc::ex2_approx((cs_last - csr) * MSC_LOG2E) * scs[256 + row];
                 }
                 uint4* ph = reinterpret_cast<uint4*>(sg + 16 * u);
                 uint4* pl = reinterpret_cast<uint4*>(sg + 16384 + 16 * u);
@@ -1162,7 +1216,8 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
     p.dDelta = reinterpret_cast<float*>(ws); ws += a256(nrow);
     float* S = reinterpret_cast<float*>(ws); ws += a256(nst);
     float* Hin = reinterpret_cast<float*>(ws); ws += a256(nst);
-    p.U = reinterpret_cast<float*>(ws); ws += a256(nst);
+    float* U = reinterpret_cast<float*>(ws); ws += a256(nst);
+    p.U = U;
     uint16_t* Himg = reinterpret_cast<uint16_t*>(ws); ws += a256(nst);
     p.dSimg = reinterpret_cast<uint16_t*>(ws); ws += a256(nst);
     p.Himg = Himg;
@@ -1215,14 +1270,21 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
         }
     }
     const unsigned nmb = (unsigned)((f.Q + 127) / 128), ntri128 = nmb * (nmb + 1) / 2;
-    ssd_gdz_kernel<<<dim3((unsigned)((f.L + 63) / 64), H, B), 256, 0, st>>>(p);
-    if ((s = check_launch("ssd_gdz")) != MSC_OK) return s;
     ssd_gmat_kernel<<<dim3(ntri, nc, BG), 256, 0, st>>>(p);
     if ((s = check_launch("ssd_gmat")) != MSC_OK) return s;
-    if ((s = ssd_ugrad(f, a.dy, cs, p.U, st)) != MSC_OK) return s;
+    if ((s = ssd_ugrad(f, a.dy, cs, U, st)) != MSC_OK) return s;
     ssd_rpass_kernel<<<dim3(H * (kP * kN / 8) / 256, B), 256, 0, st>>>(p);
     if ((s = check_launch("ssd_rpass")) != MSC_OK) return s;
-    ssd_dg_tc_kernel<<<dim3(ntri128, nc, BG), kDgThreads, kDgSmem, st>>>(mX128, mDy128, mZ128, p);
+    {
+        // enough head blocks per tile to give every SM about two CTAs
+        const int tiles = (int)(ntri128 * nc * BG);
+        const int want = std::max(1, std::min(p.hpg, (2 * 148 + tiles - 1) / tiles));
+        p.dg_hpb = (p.hpg + want - 1) / want;
+        const unsigned nhb = (unsigned)((p.hpg + p.dg_hpb - 1) / p.dg_hpb);
+        e = cudaMemsetAsync(p.dG, 0, ngm, st);
+        if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd bwd memset: %s", cudaGetErrorString(e));
+        ssd_dg_tc_kernel<<<dim3(ntri128 * nhb, nc, BG), kDgThreads, kDgSmem, st>>>(mX128, mDy128, mZ128, p);
+    }
     if ((s = check_launch("ssd_dg_tc")) != MSC_OK) return s;
     ssd_dbc_kernel<<<dim3(2 * nb, nc, BG), 256, 0, st>>>(p);
     if ((s = check_launch("ssd_dbc")) != MSC_OK) return s;
