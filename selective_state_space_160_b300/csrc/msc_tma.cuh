@@ -47,6 +47,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, but a thread whose phase is not complete is suspended until it
+// completes or about `hint_ns` nanoseconds pass, instead of returning at once
+// (a waiting warp then takes no issue slots from the warps it waits for).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait on phase `parity`: returns false if it did not complete within
 // `max_iters` polls (each poll may suspend the warp for a short while).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iters) {
@@ -58,13 +73,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 // Wait for phase `parity` of `bar`, giving up after about one second (by the
 // global timer), or as soon as *abort becomes non-zero when abort is given, so
 // that one role's timeout does not cascade through the others of the block.
+// sleep_ns > 0: after a few polls the waiting thread is suspended between tests
+// (for roles that wait long, such as an MMA issuer or an epilogue); 0 keeps
+// polling (for short waits inside a tight pipeline).
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
-                                             const volatile uint32_t* abort = nullptr) {
-    if (mbar_wait(bar, parity, 256)) return true;
+                                             const volatile uint32_t* abort = nullptr, uint32_t sleep_ns = 0) {
+    if (mbar_wait(bar, parity, sleep_ns ? 4u : 256u)) return true;
     uint64_t t0;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (sleep_ns ? mbar_try_wait_sleep(bar, parity, sleep_ns) : mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
         uint64_t t1;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));

@@ -47,6 +47,8 @@
 
 namespace {
 
+constexpr uint32_t kSleepNs = 20000;  // suspend hint of the blocks' mbarrier waits
+
 constexpr int kP = 64;
 constexpr int kN = 128;
 constexpr int kT = 64;       // tile rows / steps per block
@@ -337,8 +339,8 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             int issued = 0;
             for (int hh = 0; hh < nh; ++hh) {
                 const int st = hh % kDgStages, use = hh / kDgStages;
-                if (use > 0 && !(msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort) &&
-                                 msc::wait_bounded(&cfree[st], (uint32_t)((use - 1) & 1), abort))) {
+                if (use > 0 && !(msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort, kSleepNs) &&
+                                 msc::wait_bounded(&cfree[st], (uint32_t)((use - 1) & 1), abort, kSleepNs))) {
                     record_timeout(121);
                     *abort = 1u;
                     break;
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
                 ++issued;
             }
             for (int st = 0; st < kDgStages && st < issued; ++st)
-                if (!msc::wait_bounded(&tfull[st], (uint32_t)(((issued - 1 - st) / kDgStages) & 1))) record_timeout(122);
+                if (!msc::wait_bounded(&tfull[st], (uint32_t)(((issued - 1 - st) / kDgStages) & 1), nullptr, kSleepNs)) record_timeout(122);
         }
         __syncwarp();
     } else if (warp == kDgWarpMma) {
@@ -366,9 +368,9 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             bool ok = true;
             for (int hh = 0; hh < nh && ok; ++hh) {
                 const int st = hh % kDgStages, use = hh / kDgStages, rb = hh & 1;
-                ok = msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort) &&
-                     msc::wait_bounded(&full[st], (uint32_t)(use & 1), abort);
-                if (ok && hh >= 2) ok = msc::wait_bounded(&rfree[rb], (uint32_t)(((hh - 2) >> 1) & 1), abort);
+                ok = msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort, kSleepNs) &&
+                     msc::wait_bounded(&full[st], (uint32_t)(use & 1), abort, kSleepNs);
+                if (ok && hh >= 2) ok = msc::wait_bounded(&rfree[rb], (uint32_t)(((hh - 2) >> 1) & 1), abort, kSleepNs);
                 if (!ok) break;
                 msc::tc_fence_after();
                 const uint32_t a = msc::smem_u32(stages + st * kDgStage);
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
                 *abort = 1u;
             }
             msc::mma_commit(drain);
-            if (!msc::wait_bounded(drain, 0)) record_timeout(124);
+            if (!msc::wait_bounded(drain, 0, nullptr, kSleepNs)) record_timeout(124);
         }
         __syncwarp();
     } else {
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
         auto produce = [&](int hh) {
             const int st = hh % kDgStages, use = hh / kDgStages;
             if (has_z) {
-                ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort));
+                ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort, kSleepNs));
                 if (ok) {
                     uint8_t* sg = stages + st * kDgStage;
 #pragma unroll 1
@@ -437,8 +439,8 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             const int h = g * p.hpg + hh0 + hh;
             const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&rfull[buf], (uint32_t)((hh >> 1) & 1), abort) &&
-                                                   msc::wait_bounded(&tfull[cb], (uint32_t)((hh / 3) & 1), abort));
+            ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&rfull[buf], (uint32_t)((hh >> 1) & 1), abort, kSleepNs) &&
+                                                   msc::wait_bounded(&tfull[cb], (uint32_t)((hh / 3) & 1), abort, kSleepNs));
             msc::tc_fence_after();
             // the diagonal T_ii would enter dcs_i once as +T and once as -T: it is
             // left out of both sums (exactly zero), which keeps the large diagonal
@@ -582,77 +584,88 @@ __global__ void __launch_bounds__(256) ssd_dbc_kernel(const SsdBwdParams p) {
 }
 
 // ------------------------------------------------------------------ dx on tcgen05
-// CTA = (chunk * nmb + row block mb of 128 steps j, head, batch); 8 operand /
-// epilogue warps, one load warp, one MMA warp.  Three accumulators in tensor
-// memory, M = 128 rows j, N = 64 channels p, all fp32:
+// CTA = (chunk * nmb + row block mb of 128 steps j, block of kDxHB heads, batch),
+// persistent over its heads: 16 operand / epilogue warps, one load warp, one MMA
+// warp (the chunk length is a template parameter, so that the strided shared
+// memory reads take immediate offsets).  Per head three accumulators in tensor
+// memory (two buffers, so that the epilogue of one head runs while the MMAs of
+// the next do), M = 128 rows j, N = 64 channels p, all fp32:
 //   acc1 = sum_{i >= j} (E_ij G_ij) g_i[p]  A: E o G formed by CUDA cores, split hi + lo;
 //                                          B: g tile [64 i][64 p], MN-major (dy itself, or
 //                                          dy silu(z) split hi + lo)
 //   acc2 = B_j . dS[p, :]                  A: B tile by TMA (exact bf16); B: dS hi, lo images
 //   acc3 = C_j . Hin[p, :]                 A: C tile by TMA; B: Hin hi, lo images
-// The operands stream through a ring of four 48 KB stages, one K slab of 64
-// each: A hi [128][64] | A lo | B hi [64][64] | B lo (bf16, 128-byte swizzle).
-// The first na slabs feed acc1, one per 64 steps i >= j0 (formed by the CUDA
-// cores while the later tiles load), then four by TMA: acc2 (n blocks 0, 1),
-// acc3 (n blocks 0, 1).
-// Epilogue (thread = row j, half of the p columns):
+// The operands stream through a ring of two 80 KB stages, one K slab of 64
+// each: A hi [128][64] | A lo | B hi [64][64] | B lo (bf16, 128-byte swizzle) |
+// G [64 i][128 j] (fp32, by TMA, read by the CUDA cores forming A).  Per head the
+// first na slabs feed acc1, one per 64 steps i >= j0, then four by TMA: acc2
+// (n blocks 0, 1), acc3 (n blocks 0, 1).  The head's cs and Delta rows come by
+// bulk copy into a ring of three.
+// Epilogue (thread = row j, a quarter of the p columns):
 //   dx_j = Delta_j acc1 + w_j acc2 + D g_j;  dw_j = x_j . acc2;  v_j = exp(cs_j) g_j . acc3
 // and, since it reads dy, x and z of the row anyway, the gate's dz and dD.
-constexpr int kDxStages = 4;
-constexpr uint32_t kDxStage = 49152;
-constexpr int kDxOpWarps = 8;
+constexpr int kDxStages = 2;
+constexpr uint32_t kDxStage = 81920;           // A hi | A lo | B hi | B lo | G [64 i][128 j] fp32
+constexpr int kDxOpWarps = 16;
 constexpr int kDxWarpLoad = kDxOpWarps, kDxWarpMma = kDxOpWarps + 1;
 constexpr int kDxThreads = (kDxOpWarps + 2) * 32;
-constexpr size_t kDxSmem = 1024 + kDxStages * kDxStage + (256 + 256 + 512) * 4 + 16 * 8 + 16;
+constexpr int kDxHB = 8;                       // heads per CTA
+constexpr size_t kDxSmem = 1024 + kDxStages * kDxStage + (3 * 512 + 1024) * 4 + 24 * 8 + 16;
 
+template <int kQ>
 __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_constant__ CUtensorMap tmB,
                                                                   const __grid_constant__ CUtensorMap tmC,
                                                                   const __grid_constant__ CUtensorMap tmDy,
                                                                   const __grid_constant__ CUtensorMap tmZ,
+                                                                  const __grid_constant__ CUtensorMap tmG,
                                                                   const SsdBwdParams p) {
     extern __shared__ uint8_t s_dyn[];
     uint8_t* stages = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);
-    float* s_cs = reinterpret_cast<float*>(stages + kDxStages * kDxStage);   // cs of the chunk
-    float* s_dt = s_cs + 256;
-    float* s_part = s_dt + 256;                                                // [dw, v][2 halves][128 rows]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_part + 512);
-    // 0-3 stage loaded (TMA), 4-7 stage built (8 warps), 8-9 free (MMA), 12 done, 13 drain
-    uint64_t *tfull = bars, *full = bars + 4, *empty = bars + 8, *done = bars + 12, *drain = bars + 13;
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 14);
+    float* s_rows = reinterpret_cast<float*>(stages + kDxStages * kDxStage);  // [3][cs 256 | Delta 256]
+    float* s_part = s_rows + 3 * 512;                                          // [dw, v][4 quarters][128 rows]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_part + 1024);
+    // 0-1 stage loaded (TMA), 2-3 stage built (16 warps), 4-5 stage free (MMA), 6-8 rows loaded,
+    // 9-11 rows free (16 warps), 12-13 accumulators ready, 14-15 accumulators free (16 warps), 16 drain
+    uint64_t *tfull = bars, *full = bars + 2, *empty = bars + 4, *rfull = bars + 6, *rfree = bars + 9,
+             *afull = bars + 12, *afree = bars + 14, *drain = bars + 16;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 17);
     volatile uint32_t* abort = slot + 1;
 
-    const int Q = p.Q;
-    const int nmb = (Q + 127) / 128;
+    constexpr int Q = kQ;
+    constexpr int nmb = (Q + 127) / 128;
+    constexpr int kGW = Q < 128 ? Q : 128;       // columns j of a G slab
     const int c = blockIdx.x / nmb, mb = blockIdx.x % nmb;
-    const int h = blockIdx.y, b = blockIdx.z, g = h / p.hpg;
+    const int hb = blockIdx.y, b = blockIdx.z;
     const int j0 = 128 * mb;
     const int rows_valid = min(128, Q - j0);
-    const int na = (Q - j0) / 64;                // acc1 slabs
-    const int ns = na + 4;
+    const int na = (Q - j0) / 64;                // acc1 slabs per head
+    const int ns = na + 4;                       // slabs per head
+    const int nh = min(kDxHB, p.H - hb * kDxHB);
     const int64_t tc0 = (int64_t)c * Q;
     const bool has_z = p.z != nullptr;
-    const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
-    const size_t img = (((size_t)b * p.nc + c) * p.H + h) * 32768;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (warp == 0) {
-        msc::tmem_alloc(slot, 256);
+        msc::tmem_alloc(slot, 512);
         msc::tmem_relinquish();
     }
     if (tid == 32) {
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kDxStages; ++k) {
             msc::mbar_init(&tfull[k], 1);
             msc::mbar_init(&full[k], kDxOpWarps);
             msc::mbar_init(&empty[k], 1);
         }
-        msc::mbar_init(done, 1);
+        for (int k = 0; k < 3; ++k) {
+            msc::mbar_init(&rfull[k], 1);
+            msc::mbar_init(&rfree[k], kDxOpWarps);
+        }
+        for (int k = 0; k < 2; ++k) {
+            msc::mbar_init(&afull[k], 1);
+            msc::mbar_init(&afree[k], kDxOpWarps);
+        }
         msc::mbar_init(drain, 1);
         slot[1] = 0u;
         msc::fence_barrier_init();
-    }
-    if (tid < Q) {
-        s_cs[tid] = p.cs[dbase + tid];
-        s_dt[tid] = p.dt[dbase + tid];
     }
     msc::tc_fence_before();
     __syncthreads();
@@ -665,34 +678,59 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
             msc::prefetch_tmap(&tmB);
             msc::prefetch_tmap(&tmC);
             msc::prefetch_tmap(&tmDy);
+            msc::prefetch_tmap(&tmG);
             if (has_z) msc::prefetch_tmap(&tmZ);
-            int issued = 0;
-            for (int s = 0; s < ns; ++s) {
-                const int st = s & 3, use = s >> 2;
-                if (use > 0 && !msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort)) {
-                    record_timeout(101);
-                    *abort = 1u;
+            int issued = 0, rissued = 0;
+            bool ok = true;
+            for (int hh = 0; hh < nh && ok; ++hh) {
+                const int h = hb * kDxHB + hh, g = h / p.hpg;
+                const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
+                const size_t img = (((size_t)b * p.nc + c) * p.H + h) * 32768;
+                const int grow = ((b * p.nc + c) * p.Gr + g) * Q;  // first row of the chunk's G (2-D view)
+                const int rb = hh % 3;
+                if (hh >= 3 && !msc::wait_bounded(&rfree[rb], (uint32_t)(((hh - 3) / 3) & 1), abort, kSleepNs)) {
+                    ok = false;
                     break;
                 }
-                uint8_t* sg = stages + st * kDxStage;
-                if (s >= na) {
-                    const int which = (s - na) >> 1, kb = (s - na) & 1;
-                    const uint8_t* im = reinterpret_cast<const uint8_t*>(which ? p.Himg : p.dSimg) + img;
-                    msc::mbar_arrive_expect_tx(&tfull[st], 32768u);
-                    msc::tma_load_3d(sg, which ? &tmC : &tmB, &tfull[st], g * kN + 64 * kb, (int)(tc0 + j0), b);
-                    msc::bulk_g2s(sg + 32768, im + 8192 * kb, 8192u, &tfull[st]);
-                    msc::bulk_g2s(sg + 40960, im + 16384 + 8192 * kb, 8192u, &tfull[st]);
-                } else {
-                    const int i0 = j0 + 64 * s;
-                    msc::mbar_arrive_expect_tx(&tfull[st], has_z ? 16384u : 8192u);
-                    msc::tma_load_3d(sg + 32768, &tmDy, &tfull[st], h * kP, (int)(tc0 + i0), b);
-                    if (has_z) msc::tma_load_3d(sg + 40960, &tmZ, &tfull[st], h * kP, (int)(tc0 + i0), b);
+                msc::mbar_arrive_expect_tx(&rfull[rb], 8u * (uint32_t)Q);
+                msc::bulk_g2s(s_rows + 512 * rb, p.cs + dbase, 4u * (uint32_t)Q, &rfull[rb]);
+                msc::bulk_g2s(s_rows + 512 * rb + 256, p.dt + dbase, 4u * (uint32_t)Q, &rfull[rb]);
+                ++rissued;
+                for (int s = 0; s < ns; ++s) {
+                    const int u = hh * ns + s, st = u % kDxStages, use = u / kDxStages;
+                    if (use > 0 && !msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort, kSleepNs)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sg = stages + st * kDxStage;
+                    if (s >= na) {
+                        const int which = (s - na) >> 1, kb = (s - na) & 1;
+                        const uint8_t* im = reinterpret_cast<const uint8_t*>(which ? p.Himg : p.dSimg) + img;
+                        msc::mbar_arrive_expect_tx(&tfull[st], 32768u);
+                        msc::tma_load_3d(sg, which ? &tmC : &tmB, &tfull[st], g * kN + 64 * kb, (int)(tc0 + j0), b);
+                        msc::bulk_g2s(sg + 32768, im + 8192 * kb, 8192u, &tfull[st]);
+                        msc::bulk_g2s(sg + 40960, im + 16384 + 8192 * kb, 8192u, &tfull[st]);
+                    } else {
+                        const int i0 = j0 + 64 * s;
+                        msc::mbar_arrive_expect_tx(&tfull[st], (has_z ? 16384u : 8192u) + 256u * kGW);
+                        msc::tma_load_2d(sg + 49152, &tmG, &tfull[st], j0, grow + i0);
+                        msc::tma_load_3d(sg + 32768, &tmDy, &tfull[st], h * kP, (int)(tc0 + i0), b);
+                        if (has_z) msc::tma_load_3d(sg + 40960, &tmZ, &tfull[st], h * kP, (int)(tc0 + i0), b);
+                    }
+                    ++issued;
                 }
-                ++issued;
+            }
+            if (!ok) {
+                record_timeout(101);
+                *abort = 1u;
             }
             // no copy may still be landing when the block exits
-            for (int st = 0; st < 4 && st < issued; ++st)
-                if (!msc::wait_bounded(&tfull[st], (uint32_t)(((issued - 1 - st) >> 2) & 1))) record_timeout(102);
+            for (int st = 0; st < kDxStages && st < issued; ++st)
+                if (!msc::wait_bounded(&tfull[st], (uint32_t)(((issued - 1 - st) / kDxStages) & 1), nullptr, kSleepNs))
+                    record_timeout(102);
+            for (int rb = 0; rb < 3 && rb < rissued; ++rb)
+                if (!msc::wait_bounded(&rfull[rb], (uint32_t)(((rissued - 1 - rb) / 3) & 1), nullptr, kSleepNs))
+                    record_timeout(102);
         }
         __syncwarp();
     } else if (warp == kDxWarpMma) {
@@ -701,95 +739,99 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
             const uint32_t idK = msc::idesc_f16(true, 128, kP);
             const uint32_t idX = msc::idesc_f16(true, 128, kP, false, true);
             bool ok = true;
-            for (int s = 0; s < ns && ok; ++s) {
-                const int st = s & 3, use = s >> 2;
-                ok = msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort) &&
-                     msc::wait_bounded(&full[st], (uint32_t)(use & 1), abort);
-                if (!ok) break;
-                msc::tc_fence_after();
-                const uint32_t a = msc::smem_u32(stages + st * kDxStage);
-                if (s >= na) {
-                    const int si = s - na;
-                    const uint32_t acc = tmem + (si < 2 ? 64u : 128u);
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t ad = msc::sdesc_sw128(a + 32 * k);
-                        msc::mma_f16(acc, ad, msc::sdesc_sw128(a + 32768 + 32 * k), idK, ((si & 1) || k) ? 1u : 0u);
-                        msc::mma_f16(acc, ad, msc::sdesc_sw128(a + 40960 + 32 * k), idK, 1u);
+            for (int hh = 0; hh < nh && ok; ++hh) {
+                const int ab = hh & 1;
+                const uint32_t acc1 = tmem + 256u * (uint32_t)ab;
+                if (hh >= 2) ok = msc::wait_bounded(&afree[ab], (uint32_t)(((hh - 2) >> 1) & 1), abort, kSleepNs);
+                for (int s = 0; s < ns && ok; ++s) {
+                    const int u = hh * ns + s, st = u % kDxStages, use = u / kDxStages;
+                    ok = msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort, kSleepNs) &&
+                         msc::wait_bounded(&full[st], (uint32_t)(use & 1), abort, kSleepNs);
+                    if (!ok) break;
+                    msc::tc_fence_after();
+                    const uint32_t a = msc::smem_u32(stages + st * kDxStage);
+                    if (s >= na) {
+                        const int si = s - na;
+                        const uint32_t acc = acc1 + (si < 2 ? 64u : 128u);
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t ad = msc::sdesc_sw128(a + 32 * k);
+                            msc::mma_f16(acc, ad, msc::sdesc_sw128(a + 32768 + 32 * k), idK, ((si & 1) || k) ? 1u : 0u);
+                            msc::mma_f16(acc, ad, msc::sdesc_sw128(a + 40960 + 32 * k), idK, 1u);
+                        }
+                    } else {
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t bh = msc::sdesc_sw128_mn(a + 32768 + 2048 * k, 8192u);
+                            const uint64_t ah = msc::sdesc_sw128(a + 32 * k);
+                            msc::mma_f16(acc1, ah, bh, idX, (s > 0 || k) ? 1u : 0u);
+                            msc::mma_f16(acc1, msc::sdesc_sw128(a + 16384 + 32 * k), bh, idX, 1u);
+                            if (has_z) msc::mma_f16(acc1, ah, msc::sdesc_sw128_mn(a + 40960 + 2048 * k, 8192u), idX, 1u);
+                        }
                     }
-                } else {
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t bh = msc::sdesc_sw128_mn(a + 32768 + 2048 * k, 8192u);
-                        const uint64_t ah = msc::sdesc_sw128(a + 32 * k);
-                        msc::mma_f16(tmem, ah, bh, idX, (s > 0 || k) ? 1u : 0u);
-                        msc::mma_f16(tmem, msc::sdesc_sw128(a + 16384 + 32 * k), bh, idX, 1u);
-                        if (has_z) msc::mma_f16(tmem, ah, msc::sdesc_sw128_mn(a + 40960 + 2048 * k, 8192u), idX, 1u);
-                    }
+                    msc::mma_commit(&empty[st]);
                 }
-                msc::mma_commit(&empty[st]);
+                if (ok) msc::mma_commit(&afull[ab]);
             }
-            if (ok) {
-                msc::mma_commit(done);
-            } else {
+            if (!ok) {
                 record_timeout(103);
                 *abort = 1u;
             }
             // every MMA issued completes before the tensor memory is released
             msc::mma_commit(drain);
-            if (!msc::wait_bounded(drain, 0)) record_timeout(104);
+            if (!msc::wait_bounded(drain, 0, nullptr, kSleepNs)) record_timeout(104);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ operands, then epilogue
-        const float* Gt = p.Gm + (((size_t)b * p.nc + c) * p.Gr + g) * (size_t)Q * Q;
         bool ok = true;
-        for (int s = 0; s < ns; ++s) {
-            const int st = s & 3, use = s >> 2;
-            uint8_t* sg = stages + st * kDxStage;
-            // every slab: the stage's previous MMAs are done before this use is
-            // announced (a full barrier may not run a phase ahead of its consumer)
-            if (use > 0) ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort));
-            if (!ok) break;
-            if (s < na) {
-                // A = (E o G)^T of this slab: rows j (128), K = 64 steps i from i0
-                const int i0 = j0 + 64 * s;
-                // thread: row (tid & 127), chunks kc = tid / 128 + 2 r of 8 steps; the 32
-                // loads of G are issued before any is used
-                const int row = tid & 127, j = j0 + row;
-                const bool row_on = row < rows_valid;
-                const float csj = s_cs[row_on ? j : 0];
-                float v[4][8];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int ib = i0 + 8 * ((tid >> 7) + 2 * r);
-                    const float* gcol = Gt + (size_t)ib * Q + j;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) v[r][q] = (row_on && ib + q >= j) ? gcol[q * Q] : 0.f;
-                }
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int kc = (tid >> 7) + 2 * r, ib = i0 + 8 * kc;
-                    uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
-                    if (row_on && ib + 7 >= j) {  // else the whole chunk lies above the diagonal
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int i = ib + q;
-                            v[r][q] = i >= j ? v[r][q] * msc::ex2_approx((s_cs[i] - csj) * MSC_LOG2E) : 0.f;
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) msc::split_bf16x2(v[r][2 * q], v[r][2 * q + 1], hi[q], lo[q]);
-                    }
-                    const uint32_t off = msc::sw128_offset(row, 8 * kc, 128);
-                    *reinterpret_cast<uint4*>(sg + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(sg + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
-                if (has_z) {
-                    // g = dy silu(z) in place: hi over dy, lo over z
-                    ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort));
+        auto fail_here = [&]() {
+            if (lane == 0) record_timeout(105);
+            *abort = 1u;
+        };
+        auto produce_head = [&](int hh) {
+            const int rb = hh % 3;
+            ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&rfull[rb], (uint32_t)((hh / 3) & 1), abort, kSleepNs));
+            const float* s_cs = s_rows + 512 * rb;
+            for (int s = 0; s < ns && ok; ++s) {
+                const int u = hh * ns + s, st = u % kDxStages, use = u / kDxStages;
+                uint8_t* sg = stages + st * kDxStage;
+                // every slab: the stage's previous MMAs are done before this use is
+                // announced (a full barrier may not run a phase ahead of its consumer)
+                if (use > 0) ok = __all_sync(0xffffffffu, msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort, kSleepNs));
+                if (!ok) break;
+                if (s < na) {
+                    // A = (E o G)^T of this slab: rows j (128), K = 64 steps i from i0; G and
+                    // the g tile arrive by TMA
+                    ok = __all_sync(0xffffffffu, msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort, kSleepNs));
                     if (!ok) break;
-#pragma unroll 1
-                    for (int u = tid; u < 512; u += 256) {
-                        uint4* ph = reinterpret_cast<uint4*>(sg + 32768 + 16 * u);
-                        uint4* pl = reinterpret_cast<uint4*>(sg + 40960 + 16 * u);
+                    const int i0 = j0 + 64 * s;
+                    const float* sG = reinterpret_cast<const float*>(sg + 49152);
+                    // thread: row (tid & 127), chunks kc = tid / 128 + 4 r of 8 steps
+                    const int row = tid & 127, j = j0 + row;
+                    const bool row_on = row < rows_valid;
+                    const float csj = s_cs[row_on ? j : 0];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int kc = (tid >> 7) + 4 * r, ib = i0 + 8 * kc;
+                        uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+                        if (row_on && ib + 7 >= j) {  // else the whole chunk lies above the diagonal
+                            float v[8];
+                            const float* gcol = sG + (ib - i0) * kGW + row;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const int i = ib + q;
+                                v[q] = i >= j ? gcol[q * kGW] * msc::ex2_approx((s_cs[i] - csj) * MSC_LOG2E) : 0.f;
+                            }
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) msc::split_bf16x2(v[2 * q], v[2 * q + 1], hi[q], lo[q]);
+                        }
+                        const uint32_t off = msc::sw128_offset(row, 8 * kc, 128);
+                        *reinterpret_cast<uint4*>(sg + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4*>(sg + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                    if (has_z) {
+                        // g = dy silu(z) in place: hi over dy, lo over z (one 16-byte chunk per thread)
+                        uint4* ph = reinterpret_cast<uint4*>(sg + 32768 + 16 * tid);
+                        uint4* pl = reinterpret_cast<uint4*>(sg + 40960 + 16 * tid);
                         const uint4 dv = *ph, zv = *pl;
                         const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w}, zw[4] = {zv.x, zv.y, zv.z, zv.w};
                         uint32_t hi[4], lo[4];
@@ -801,42 +843,46 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                         *pl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
                 }
+                msc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) msc::mbar_arrive(&full[st]);
             }
-            msc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) msc::mbar_arrive(&full[st]);
-        }
-        if (!ok) {
-            if (lane == 0) record_timeout(105);
-            *abort = 1u;
-        }
-        // ---------------------------------------------------------- epilogue
-        ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(done, 0, abort));
-        msc::tc_fence_after();
-        const int lq = warp & 3, half = warp >> 2;
+            if (!ok) fail_here();
+        };
+        // warp w: TMEM lanes 32 (w % 4) .. (rows j), columns 16 (w / 4) .. of each accumulator
+        const int lq = warp & 3, cq = warp >> 2;
         const int row = 32 * lq + lane, j = j0 + row;
         const int64_t t = tc0 + j;
-        const bool valid = ok && row < rows_valid && t < p.L;
-        float dw = 0.f, v = 0.f, ej = 0.f, wj = 0.f, ecs = 0.f, dd = 0.f;
-        if (ok) {
-            const uint32_t ta = tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)(32 * half);
-            float a1[32], a2[32], a3[32];
-            msc::tmem_ld16(ta, a1);
-            msc::tmem_ld16(ta + 16, a1 + 16);
-            msc::tmem_ld16(ta + 64, a2);
-            msc::tmem_ld16(ta + 80, a2 + 16);
-            msc::tmem_ld16(ta + 128, a3);
-            msc::tmem_ld16(ta + 144, a3 + 16);
-            msc::tmem_ld_wait();
+        auto epilogue_head = [&](int hh) {
+            const int ab = hh & 1, rb = hh % 3;
+            const int h = hb * kDxHB + hh;
+            const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
+            const float* s_cs = s_rows + 512 * rb;
+            const float* s_dt = s_cs + 256;
+            ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&afull[ab], (uint32_t)((hh >> 1) & 1), abort, kSleepNs));
+            msc::tc_fence_after();
+            const bool valid = ok && row < rows_valid && t < p.L;
+            float dw = 0.f, v = 0.f, ej = 0.f, wj = 0.f, ecs = 0.f, dd = 0.f;
+            float a1[16], a2[16], a3[16];
+            if (ok) {
+                const uint32_t ta = tmem + 256u * (uint32_t)ab + ((uint32_t)(32 * lq) << 16) + (uint32_t)(16 * cq);
+                msc::tmem_ld16(ta, a1);
+                msc::tmem_ld16(ta + 64, a2);
+                msc::tmem_ld16(ta + 128, a3);
+                msc::tmem_ld_wait();
+            }
+            msc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) msc::mbar_arrive(&afree[ab]);  // the next head but one may write this buffer
             if (valid) {
-                const size_t o = (((size_t)b * p.L + t) * p.H + h) * kP + 32 * half;
+                const size_t o = (((size_t)b * p.L + t) * p.H + h) * kP + 16 * cq;
                 const float dtj = s_dt[j];
                 ej = msc::ex2_approx((s_cs[Q - 1] - s_cs[j]) * MSC_LOG2E);
                 wj = ej * dtj;
                 ecs = msc::ex2_approx(s_cs[j] * MSC_LOG2E);
                 const float Dh = p.D ? p.D[h] : 0.f;
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
+                for (int q8 = 0; q8 < 2; ++q8) {
                     const uint4 dv = *reinterpret_cast<const uint4*>(p.dy + o + 8 * q8);
                     const uint4 xv = *reinterpret_cast<const uint4*>(p.x + o + 8 * q8);
                     uint4 zv = make_uint4(0u, 0u, 0u, 0u);
@@ -873,36 +919,44 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                     if (has_z) msc::st_cs_v8(p.dz + o + 8 * q8, dzo);
                 }
             }
-        }
-        s_part[128 * half + row] = dw;
-        s_part[256 + 128 * half + row] = v;
-        // dD = sum g . x over steps and channels of the head
+            s_part[128 * cq + row] = dw;
+            s_part[512 + 128 * cq + row] = v;
+            // dD = sum g . x over steps and channels of the head
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
-        if (lane == 0 && p.dD && dd != 0.f) atomicAdd(p.dD + h, dd);
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (half == 0) {
-            float lastp = 0.f;
-            if (valid) {
-                const float dwt = dw + s_part[128 + row];
-                const float vt = v + s_part[384 + row];
-                atomicAdd(p.dDelta + dbase + j, ej * dwt);
-                // w_j dw_j goes to dcs_last and out of dcs_j: for j = last the two
-                // cancel exactly and are left out
-                const bool last = j == Q - 1;
-                atomicAdd(p.dcs + dbase + j, ecs * vt - (last ? 0.f : wj * dwt));
-                lastp = last ? 0.f : wj * dwt;
+            for (int off = 16; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
+            if (lane == 0 && p.dD && dd != 0.f) atomicAdd(p.dD + h, dd);
+            asm volatile("bar.sync 1, 512;" ::: "memory");
+            if (cq == 0) {
+                float lastp = 0.f;
+                if (valid) {
+                    const float dwt = dw + s_part[128 + row] + s_part[256 + row] + s_part[384 + row];
+                    const float vt = v + s_part[640 + row] + s_part[768 + row] + s_part[896 + row];
+                    atomicAdd(p.dDelta + dbase + j, ej * dwt);
+                    // w_j dw_j goes to dcs_last and out of dcs_j: for j = last the two
+                    // cancel exactly and are left out
+                    const bool last = j == Q - 1;
+                    atomicAdd(p.dcs + dbase + j, ecs * vt - (last ? 0.f : wj * dwt));
+                    lastp = last ? 0.f : wj * dwt;
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) lastp += __shfl_xor_sync(0xffffffffu, lastp, off);
+                if (lane == 0 && lastp != 0.f) atomicAdd(p.dcs + dbase + Q - 1, lastp);
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) lastp += __shfl_xor_sync(0xffffffffu, lastp, off);
-            if (lane == 0 && lastp != 0.f) atomicAdd(p.dcs + dbase + Q - 1, lastp);
+            asm volatile("bar.sync 1, 512;" ::: "memory");  // s_part is rewritten by the next head
+            __syncwarp();
+            if (lane == 0) msc::mbar_arrive(&rfree[rb]);
+        };
+        for (int hh = 0; hh <= nh; ++hh) {
+            if (hh < nh) produce_head(hh);
+            if (hh >= 1) epilogue_head(hh - 1);
         }
+        if (!ok) fail_here();
         msc::tc_fence_before();
     }
     __syncthreads();
     if (warp == 0) {
         msc::tc_fence_after();
-        msc::tmem_dealloc(tmem, 256);
+        msc::tmem_dealloc(tmem, 512);
     }
 }
 
@@ -981,7 +1035,7 @@ __global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid
             int issued = 0;
             for (int s = 0; s < ns; ++s) {
                 const int st = s % kSbStages, use = s / kSbStages;
-                if (use > 0 && !msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort)) {
+                if (use > 0 && !msc::wait_bounded(&empty[st], (uint32_t)((use - 1) & 1), abort, kSleepNs)) {
                     record_timeout(111);
                     *abort = 1u;
                     break;
@@ -1001,7 +1055,7 @@ __global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid
                 ++issued;
             }
             for (int st = 0; st < kSbStages && st < issued; ++st)
-                if (!msc::wait_bounded(&tfull[st], (uint32_t)(((issued - 1 - st) / kSbStages) & 1))) record_timeout(112);
+                if (!msc::wait_bounded(&tfull[st], (uint32_t)(((issued - 1 - st) / kSbStages) & 1), nullptr, kSleepNs)) record_timeout(112);
         }
         __syncwarp();
     } else if (warp == kSbWarpMma) {
@@ -1010,8 +1064,8 @@ __global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid
             bool ok = true;
             for (int s = 0; s < ns && ok; ++s) {
                 const int st = s % kSbStages, use = s / kSbStages;
-                ok = msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort) &&
-                     msc::wait_bounded(&full[st], (uint32_t)(use & 1), abort);
+                ok = msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort, kSleepNs) &&
+                     msc::wait_bounded(&full[st], (uint32_t)(use & 1), abort, kSleepNs);
                 if (!ok) break;
                 msc::tc_fence_after();
                 const uint32_t a = msc::smem_u32(stages + st * kSbStage);
@@ -1033,7 +1087,7 @@ __global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid
                 *abort = 1u;
             }
             msc::mma_commit(drain);
-            if (!msc::wait_bounded(drain, 0)) record_timeout(114);
+            if (!msc::wait_bounded(drain, 0, nullptr, kSleepNs)) record_timeout(114);
         }
         __syncwarp();
     } else {
@@ -1042,7 +1096,7 @@ __global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid
             const int st = s % kSbStages, use = s / kSbStages;
             const bool cterm = s & 1;
             uint8_t* sg = stages + st * kSbStage;
-            ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort));
+            ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&tfull[st], (uint32_t)(use & 1), abort, kSleepNs));
             if (!ok) break;
             const float* scs = s_cw + 384 * st;
             const float cs_last = scs[Q - 1];
@@ -1087,7 +1141,7 @@ __global__ void __launch_bounds__(kSbThreads, 1) ssd_dbcs_tc_kernel(const __grid
             if (lane == 0) record_timeout(115);
             *abort = 1u;
         }
-        ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(done, 0, abort));
+        ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(done, 0, abort, kSleepNs));
         msc::tc_fence_after();
         if (ok) {
             const int lq = warp & 3, half = warp >> 2;
@@ -1242,7 +1296,7 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
     const unsigned B = (unsigned)f.batch, H = (unsigned)f.H, nc = (unsigned)p.nc, BG = (unsigned)(f.batch * f.G);
     // B, C as [128 steps][64 n] boxes; x, dy, z as [64 steps][64 p] and [128 steps][64 p] boxes
     // (bf16, 128-byte swizzle)
-    CUtensorMap mB, mC, mDy, mZ, mX128, mDy128, mZ128;
+    CUtensorMap mB, mC, mDy, mZ, mX128, mDy128, mZ128, mG;
     {
         const uint64_t bcd[3] = {(uint64_t)(f.G * kN), (uint64_t)f.L, (uint64_t)f.batch};
         const uint64_t bcs[2] = {(uint64_t)(f.G * kN * 2), (uint64_t)(f.L * f.G * kN * 2)};
@@ -1258,9 +1312,19 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
             !encode_tmap(&mDy128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.dy, xd, xs, box128, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_tmap(&mZ128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, zsrc, xd, xs, box128, CU_TENSOR_MAP_SWIZZLE_128B))
             return MSC_ERR_CUDA;
+        // G as rows of Q fp32, [64 i][min(Q, 128) j] boxes
+        const uint64_t gd[2] = {(uint64_t)f.Q, (uint64_t)(f.batch * p.nc * f.G * f.Q)};
+        const uint64_t gs[1] = {(uint64_t)(f.Q * 4)};
+        const uint32_t gbox[2] = {(uint32_t)std::min<int64_t>(f.Q, 128), 64};
+        if (!encode_tmap(&mG, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.Gm, gd, gs, gbox, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return MSC_ERR_CUDA;
         static bool configured = false;
         if (!configured) {
-            cudaError_t e2 = cudaFuncSetAttribute(ssd_dx_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmem);
+            cudaError_t e2 = cudaFuncSetAttribute(ssd_dx_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmem);
+            if (e2 == cudaSuccess)
+                e2 = cudaFuncSetAttribute(ssd_dx_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmem);
+            if (e2 == cudaSuccess)
+                e2 = cudaFuncSetAttribute(ssd_dx_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmem);
             if (e2 == cudaSuccess)
                 e2 = cudaFuncSetAttribute(ssd_dbcs_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSbSmem);
             if (e2 == cudaSuccess)
@@ -1289,7 +1353,13 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
     ssd_dbc_kernel<<<dim3(2 * nb, nc, BG), 256, 0, st>>>(p);
     if ((s = check_launch("ssd_dbc")) != MSC_OK) return s;
     {
-        ssd_dx_tc_kernel<<<dim3(nc * nmb, H, B), kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, p);
+        const dim3 gdx(nc * nmb, (H + kDxHB - 1) / kDxHB, B);
+        if (f.Q == 64)
+            ssd_dx_tc_kernel<64><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, p);
+        else if (f.Q == 128)
+            ssd_dx_tc_kernel<128><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, p);
+        else
+            ssd_dx_tc_kernel<256><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, p);
         if ((s = check_launch("ssd_dx_tc")) != MSC_OK) return s;
         const unsigned nhb = (unsigned)((p.hpg + kHBlk - 1) / kHBlk);
         ssd_dbcs_tc_kernel<<<dim3(nc * nmb, (unsigned)f.G * nhb, B), kSbThreads, kSbSmem, st>>>(mX128, mDy128, mZ128, p);

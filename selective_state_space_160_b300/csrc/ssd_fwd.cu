@@ -40,6 +40,8 @@
 
 namespace {
 
+constexpr uint32_t kSleepNs = 20000;  // suspend hint of the blocks' mbarrier waits
+
 constexpr int kP = 64;    // head dimension
 constexpr int kN = 128;   // state size
 constexpr int kHB = 16;   // heads per CTA of the state and scan kernels
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
     __syncthreads();
     const uint32_t tmem = *slot;
     const uint32_t idesc = msc::idesc_f16(true, 128, kP, true, true);
-    bool ok = msc::wait_bounded(&m.bars[0], 0);
+    bool ok = msc::wait_bounded(&m.bars[0], 0, nullptr, kSleepNs);
     bool failed = false;
 
     // S of head hp from accumulator buffer sp: lane = n, column = p; warps w and
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
         const int s = it & 1;
         if (it >= 1) {
             // MMAs of head it - 1 done: its x buffer takes head it + 1
-            ok = msc::wait_bounded(&m.bars[3 + (s ^ 1)], (uint32_t)(((it - 1) >> 1) & 1)) && ok;
+            ok = msc::wait_bounded(&m.bars[3 + (s ^ 1)], (uint32_t)(((it - 1) >> 1) & 1), nullptr, kSleepNs) && ok;
             if (__syncthreads_or(!ok)) {
                 if (tid == 0) record_timeout(20);
                 failed = true;
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
             if (tid == 0 && it + 1 < nh)
                 state_issue_head(m, &tmX, kMode == 2 ? &tmZ : nullptr, p, h0 + it + 1, s ^ 1, c, b);
         }
-        ok = msc::wait_bounded(&m.bars[1 + s], (uint32_t)((it >> 1) & 1)) && ok;
+        ok = msc::wait_bounded(&m.bars[1 + s], (uint32_t)((it >> 1) & 1), nullptr, kSleepNs) && ok;
         if (__syncthreads_or(!ok)) {
             if (tid == 0) record_timeout(21);
             failed = true;
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
     }
     if (!failed && nh > 0) {
         const int it = nh - 1;
-        ok = msc::wait_bounded(&m.bars[3 + (it & 1)], (uint32_t)((it >> 1) & 1));
+        ok = msc::wait_bounded(&m.bars[3 + (it & 1)], (uint32_t)((it >> 1) & 1), nullptr, kSleepNs);
         if (__syncthreads_or(!ok)) {
             if (tid == 0) record_timeout(22);
         } else {
@@ -464,7 +466,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         for (int it = 0; it < nh; ++it) {
             const int s = it & 1, h = h0 + it;
             if (it >= 2) {
-                pok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[10 + s], (uint32_t)(((it - 2) >> 1) & 1), abort));
+                pok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[10 + s], (uint32_t)(((it - 2) >> 1) & 1), abort, kSleepNs));
                 if (!pok) break;
             }
             if (lane == 0) {
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
             }
             if (s == 0) ++nx0; else ++nx1;
             if (it >= 1) {
-                pok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[5], (uint32_t)((it - 1) & 1), abort));
+                pok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[5], (uint32_t)((it - 1) & 1), abort, kSleepNs));
                 if (!pok) break;
             }
             if (lane == 0) {
@@ -493,16 +495,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         // every load issued lands before the block ends (they have all been
         // consumed already unless the block gives up)
         bool dok = true;
-        if (nx0 > 0) dok = msc::wait_bounded(&bars[2], (uint32_t)((nx0 - 1) & 1)) && dok;
-        if (nx1 > 0) dok = msc::wait_bounded(&bars[3], (uint32_t)((nx1 - 1) & 1)) && dok;
-        if (nhin > 0) dok = msc::wait_bounded(&bars[4], (uint32_t)((nhin - 1) & 1)) && dok;
+        if (nx0 > 0) dok = msc::wait_bounded(&bars[2], (uint32_t)((nx0 - 1) & 1), nullptr, kSleepNs) && dok;
+        if (nx1 > 0) dok = msc::wait_bounded(&bars[3], (uint32_t)((nx1 - 1) & 1), nullptr, kSleepNs) && dok;
+        if (nhin > 0) dok = msc::wait_bounded(&bars[4], (uint32_t)((nhin - 1) & 1), nullptr, kSleepNs) && dok;
         if (!dok && lane == 0) record_timeout(51);
     } else if (warp == kWarpMma) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t id64 = msc::idesc_f16(true, 128, kP);                // A, B K-major
             const uint32_t id64x = msc::idesc_f16(true, 128, kP, false, true);  // B MN-major (x)
-            bool mok = msc::wait_bounded(&bars[0], 0, abort);
+            bool mok = msc::wait_bounded(&bars[0], 0, abort, kSleepNs);
             if (mok) {
                 msc::tc_fence_after();
                 const uint32_t idesc = msc::idesc_f16(true, 128, Qi);
@@ -517,9 +519,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
             for (int it = 0; it < nh && mok; ++it) {
                 const int s = it & 1;
                 const uint32_t tYd = 256u + 128u * (uint32_t)s, tYo = tYd + 64u;
-                mok = msc::wait_bounded(&bars[2 + s], (uint32_t)((it >> 1) & 1), abort) &&
-                      msc::wait_bounded(&bars[4], (uint32_t)(it & 1), abort);
-                if (mok && it >= 2) mok = msc::wait_bounded(&bars[14 + s], (uint32_t)(((it - 2) >> 1) & 1), abort);
+                mok = msc::wait_bounded(&bars[2 + s], (uint32_t)((it >> 1) & 1), abort, kSleepNs) &&
+                      msc::wait_bounded(&bars[4], (uint32_t)(it & 1), abort, kSleepNs);
+                if (mok && it >= 2) mok = msc::wait_bounded(&bars[14 + s], (uint32_t)(((it - 2) >> 1) & 1), abort, kSleepNs);
                 if (!mok) break;
                 msc::tc_fence_after();
                 const uint32_t aC = msc::smem_u32(sC), aH = msc::smem_u32(sH);
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
                 const uint32_t aX = msc::smem_u32(sX + s * 32768);
                 for (int q = 0; q < nq; ++q) {
                     const int u = it * nq + q, bq = u & 1;
-                    mok = msc::wait_bounded(&bars[6 + bq], (uint32_t)((u >> 1) & 1), abort);
+                    mok = msc::wait_bounded(&bars[6 + bq], (uint32_t)((u >> 1) & 1), abort, kSleepNs);
                     if (!mok) break;
                     msc::tc_fence_after();
                     const uint32_t aHi = msc::smem_u32(sBM + bq * 32768), aLo = aHi + 16384u;
@@ -555,7 +557,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
             }
             // every MMA issued completes before the tensor memory is released
             msc::mma_commit(&bars[16]);
-            if (!msc::wait_bounded(&bars[16], 0)) record_timeout(47);
+            if (!msc::wait_bounded(&bars[16], 0, nullptr, kSleepNs)) record_timeout(47);
         }
         __syncwarp();
     } else {
@@ -566,7 +568,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         const int row_lo = ib * 128 + 32 * lq;     // first row of this warp
         const uint32_t lane_off = (uint32_t)(32 * lq) << 16;
         float* my_w = s_w + warp * 64;
-        bool ok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[1], 0, abort));
+        bool ok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[1], 0, abort, kSleepNs));
         msc::tc_fence_after();
         float csi_prev = 0.f;
         uint4 z_prev[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
@@ -574,7 +576,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         // accumulator pair back to the MMA warp once it has been read
         auto epilogue = [&](int hp, bool release) -> bool {
             const int sp = hp & 1;
-            if (!__all_sync(0xffffffffu, msc::wait_bounded(&bars[12 + sp], (uint32_t)((hp >> 1) & 1), abort)))
+            if (!__all_sync(0xffffffffu, msc::wait_bounded(&bars[12 + sp], (uint32_t)((hp >> 1) & 1), abort, kSleepNs)))
                 return false;
             msc::tc_fence_after();
             float yd[16], yo[16];
@@ -611,7 +613,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         for (int it = 0; it <= nh && ok; ++it) {
             if (it < nh) {
                 const int s = it & 1;
-                ok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[2 + s], (uint32_t)((it >> 1) & 1), abort));
+                ok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[2 + s], (uint32_t)((it >> 1) & 1), abort, kSleepNs));
                 if (!ok) break;
                 const float* s_dt = s_dc + s * 512;
                 const float* s_cs = s_dt + 256;
@@ -635,7 +637,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
                     const int u = it * nq + q, bq = u & 1;
                     if (u >= 2) {
                         ok = __all_sync(0xffffffffu,
-                                        msc::wait_bounded(&bars[8 + bq], (uint32_t)(((u >> 1) - 1) & 1), abort));
+                                        msc::wait_bounded(&bars[8 + bq], (uint32_t)(((u >> 1) - 1) & 1), abort, kSleepNs));
                         if (!ok) break;
                     }
                     const int j0 = 64 * q + 16 * cslot;
