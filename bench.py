@@ -430,10 +430,11 @@ def leg_ssd(peaks, pipes, steps=5, warmup=2):
 
 
 def ssd_bwd_macs(b, L, H, G, Q, P=64, N=128, T=64):
-    """Multiply-adds the SSD backward's fp32 tile products execute (per launch):
-    the chunk states, G = C B^T, U, dG, dC / dB from dG, dx and its state terms,
-    and the cross-head state parts of dB, dC.  Masked halves of diagonal tiles
-    are counted, as the kernels compute them."""
+    """Multiply-adds of the SSD backward's products per launch (the algorithmic
+    count, one pass per product whatever the operand split): the chunk states,
+    G = C B^T, U, dG, dC / dB from dG, dx and its state terms, and the
+    cross-head state parts of dB, dC.  Masked halves of diagonal 64 x 64 tiles
+    are counted."""
     nc, nb = -(-L // Q), Q // T
     ntri = nb * (nb + 1) // 2
     hpg = H // G
@@ -478,16 +479,18 @@ def leg_ssd_bwd(peaks, pipes, steps=5, warmup=2):
     # inputs x, dy, delta, B, C (bf16) read; dx, ddelta, dB, dC (fp32) written;
     # S, Hin, U/dS written once and read back
     nbytes = 2 * el * 2 + b * L * H * 2 + 2 * b * L * N * 2 + el * 4 + b * L * H * 4 + 2 * b * L * N * 4 + 6 * nst
-    alu = {"achieved": macs / t / 1e9, "peak": pipes["ffma"]["ops_per_s"] / 1e9, "unit": "GFMA/s"}
+    # the products run on tcgen05 (bf16 operands, fp32 operands as hi + lo pairs):
+    # algorithmic flops = 2 x the multiply-adds above, against the dense bf16 peak
+    ten = {"achieved": 2.0 * macs / t / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     hbm = {"achieved": nbytes / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    for v in (alu, hbm):
+    for v in (ten, hbm):
         v["frac"] = v["achieved"] / v["peak"]
-    sel = alu if alu["frac"] >= hbm["frac"] else hbm
+    sel = ten if ten["frac"] >= hbm["frac"] else hbm
     res = {"workload": "SSD bwd batch %d, heads 80, P 64, N 128, L 4096, chunk 256, bf16 in / fp32 grads" % b,
            "elements_per_s": el / t, "ms": ms,
-           "roofline": {"bound": "alu" if sel is alu else "hbm", "achieved": sel["achieved"], "peak": sel["peak"],
+           "roofline": {"bound": "tensor" if sel is ten else "hbm", "achieved": sel["achieved"], "peak": sel["peak"],
                         "unit": sel["unit"], "frac": sel["frac"], "traffic": None, "macs": macs,
-                        "terms": {"alu_fp32_fma": alu, "hbm": hbm}}}
+                        "terms": {"tensor": ten, "hbm": hbm}}}
     del d, ws
     torch.cuda.empty_cache()
     return res
