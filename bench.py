@@ -386,6 +386,42 @@ def leg_conv1d(peaks, pipes, steps=10, warmup=3):
     return res
 
 
+def leg_conv_scan(peaks, pipes, steps=5, warmup=2):
+    """The Mamba block's front end and scan at the headline shape (batch 8, D
+    5120, L 2048, N 16, bf16, conv width 4): fused (u formed inside the scan)
+    against two launches (conv1d with bf16 u, then the scan)."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    batch, dim, L, N, K = 8, 5120, 2048, 16, 4
+    inp = s6_fwd_workload(batch, dim, L, N, True, 160_007)
+    g = torch.Generator(device="cuda").manual_seed(160_008)
+    w = torch.randn((dim, K), device="cuda", generator=g) / 2.0
+    cb = 0.1 * torch.randn(dim, device="cuda", generator=g)
+    y = torch.empty((batch, dim, L), dtype=torch.float32, device="cuda")
+    u = torch.empty((batch, dim, L), dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def fused():
+        msc.msc_selective_scan_fwd_conv(inp["u"], w, cb, inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                        inp["z"], inp["delta_bias"], y=y)
+
+    def two():
+        msc.msc_causal_conv1d_fwd(inp["u"], w, cb, out=u)
+        msc.msc_selective_scan_fwd(u, inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                   inp["delta_bias"], y=y)
+    ms = statistics.median(time_launches(fused, steps, warmup, st))
+    ms2 = statistics.median(time_launches(two, steps, warmup, st))
+    el = batch * dim * L
+    # x, delta, z (bf16) in, y (fp32) out, B and C per batch entry
+    nbytes = el * (3 * 2 + 4) + 2 * batch * N * L * 2 + dim * (N + K + 3) * 4
+    res = {"workload": "conv1d K 4 + SiLU fused into the S6 fwd, batch 8, D 5120, L 2048, N 16, bf16",
+           "elements_per_s": el / (ms * 1e-3), "ms": ms, "two_launch_ms": ms2,
+           "roofline": roofline_s6(el, N, nbytes, ms, peaks, pipes)}
+    del inp, y, u
+    torch.cuda.empty_cache()
+    return res
+
+
 SSD_BATCH = 4  # batch of the SSD legs (--ssd-batch; 1 for a profiling-size run)
 
 
@@ -659,7 +695,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         for name in args.legs.split(","):
             try:
-                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "ssd_bwd": leg_ssd_bwd, "decode": leg_decode, "conv1d": leg_conv1d, "disc": leg_disc}[name]
+                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "ssd_bwd": leg_ssd_bwd, "decode": leg_decode, "conv1d": leg_conv1d, "conv_scan": leg_conv_scan, "disc": leg_disc}[name]
                 legs[name] = fn(peaks, pipes)
             except Exception as ex:  # report, do not hide: a failing leg is printed as such
                 legs[name] = {"error": "%s: %s" % (type(ex).__name__, ex)}
@@ -700,7 +736,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="fwd_long,bwd,ssd,ssd_bwd,decode,conv1d,disc")
+    ap.add_argument("--legs", default="fwd_long,bwd,ssd,ssd_bwd,decode,conv1d,conv_scan,disc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ssd-batch", type=int, default=4, help="batch of the SSD legs (4 = the timed workload)")

@@ -131,6 +131,27 @@ msc_status msc_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t se
                                           const void* z, const float* delta_bias, const float* h0,
                                           float* y, float* h_last, void* stream);
 
+/* ------------------------------- S6 forward with the conv1d front end fused
+ * The Mamba block's causal depthwise conv1d + SiLU (bqwf survey sec. 3.1: the
+ * convolution gives local context before the selective SSM), formed inside the
+ * scan so that its output u never goes through memory:
+ *   u[b, d, t] = silu(conv_bias[d] + sum_{k < width} conv_weight[d, k] x[b, d, t - (width - 1) + k])
+ * (x = 0 before t = 0), then exactly msc_selective_scan_fwd on u.  x: [batch,
+ * dim, seqlen] in in_dtype; conv_weight [dim, width] fp32 (width 1..4);
+ * conv_bias [dim] fp32 or NULL; the other arguments, the workspace
+ * (msc_selective_scan_fwd_workspace_size) and the errors as
+ * msc_selective_scan_fwd.  u is kept in fp32 (not rounded to in_dtype), so
+ * the result equals msc_causal_conv1d_fwd (fp32 out) followed by
+ * msc_selective_scan_fwd with fp32 u up to rounding.  Needs 16-byte row
+ * strides (seqlen a multiple of 8 with bf16 inputs, of 4 with fp32), else
+ * MSC_ERR_UNSUPPORTED; exponential-Euler form only; no backward. */
+msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                       int64_t conv_width, msc_dtype in_dtype, const void* x,
+                                       const float* conv_weight, const float* conv_bias, const void* delta,
+                                       const float* A, const void* B, const void* C, const float* D,
+                                       const void* z, const float* delta_bias, const float* h0, float* y,
+                                       float* h_last, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ----------------------------------------------------------------- S6 backward
  * Same shapes and dtype as the forward (zero initial state), plus the upstream
  * gradient dy [batch, dim, seqlen] (in_dtype).  Outputs (fp32, overwritten):

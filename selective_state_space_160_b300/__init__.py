@@ -18,6 +18,7 @@ __all__ = [
     "msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd", "msc_ssd_chunked_bwd",
     "msc_selective_state_update", "msc_ssd_chunked_bwd_workspace_size",
     "msc_causal_conv1d_fwd", "msc_causal_conv1d_update", "msc_selective_scan_fwd_ex",
+    "msc_selective_scan_fwd_conv",
     "MSC_DISC_EULER", "MSC_DISC_ZOH", "MSC_DISC_TRAPEZOID",
     "msc_selective_scan_fwd_workspace_size", "msc_selective_scan_bwd_workspace_size",
     "msc_ssd_chunked_fwd_workspace_size", "msc_check_device_status", "msc_status_string",
@@ -48,6 +49,7 @@ SIGNATURES = {
     "msc_ssd_chunked_bwd_workspace_size": (_sz, [_i64] * 7 + [ctypes.c_int]),
     "msc_ssd_chunked_bwd": (ctypes.c_int, [_i64] * 7 + [ctypes.c_int] + [_vp] * 8 + [_vp] * 9 + [_vp, _sz, _vp]),
     "msc_selective_scan_fwd_ex": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] * 2 + [_vp] * 11 + [_vp, _sz, _vp]),
+    "msc_selective_scan_fwd_conv": (ctypes.c_int, [_i64] * 5 + [ctypes.c_int] + [_vp] * 13 + [_vp, _sz, _vp]),
     "msc_selective_scan_fwd_noalloc": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 11 + [_vp]),
     "msc_selective_state_update": (ctypes.c_int, [_i64] * 3 + [ctypes.c_int] + [_vp] * 10 + [_vp]),
     "msc_causal_conv1d_fwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] * 2 + [_vp] * 3 + [ctypes.c_int] + [_vp, _vp]),
@@ -202,6 +204,42 @@ def msc_selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h
         st = lib.msc_selective_scan_fwd(batch, dim, L, N, dt, *args, *tail)
     else:
         st = lib.msc_selective_scan_fwd_ex(batch, dim, L, N, dt, int(disc), *args, *tail)
+    _check(st)
+    return (y, h_last) if return_last_state else y
+
+
+def msc_selective_scan_fwd_conv(x, conv_weight, conv_bias, delta, A, B, C, D=None, z=None, delta_bias=None,
+                                h0=None, return_last_state=False, y=None, workspace=None, stream=None):
+    """S6 forward with the causal conv1d + SiLU front end fused: u =
+    silu(conv_bias + causal depthwise conv of x with conv_weight [dim, width])
+    is formed inside the scan.  x, delta, z: [batch, dim, L] (fp32 or bf16, all
+    the same); conv_weight [dim, width <= 4] fp32; conv_bias [dim] fp32 or None;
+    the rest as msc_selective_scan_fwd.  Returns y (and h_last)."""
+    torch = _torch()
+    lib = load_library()
+    batch, dim, L = x.shape
+    N = A.shape[1]
+    K = conv_weight.shape[1]
+    dt = _in_dtype(x)
+    tdt = x.dtype
+    if y is None:
+        y = torch.empty((batch, dim, L), dtype=torch.float32, device=x.device)
+    h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=x.device) if return_last_state else None
+    nbytes = msc_selective_scan_fwd_workspace_size(batch, dim, L, N)
+    ws, wsb = _workspace(nbytes, x.device, workspace)
+    st = lib.msc_selective_scan_fwd_conv(
+        batch, dim, L, N, K, dt, _dev_ptr(x, "x"),
+        _dev_ptr(conv_weight, "conv_weight", torch.float32, (dim, K)),
+        _dev_ptr(conv_bias, "conv_bias", torch.float32, (dim,), optional=True),
+        _dev_ptr(delta, "delta", tdt, (batch, dim, L)),
+        _dev_ptr(A, "A", torch.float32, (dim, N)),
+        _dev_ptr(B, "B", tdt, (batch, N, L)), _dev_ptr(C, "C", tdt, (batch, N, L)),
+        _dev_ptr(D, "D", torch.float32, (dim,), optional=True),
+        _dev_ptr(z, "z", tdt, (batch, dim, L), optional=True),
+        _dev_ptr(delta_bias, "delta_bias", torch.float32, (dim,), optional=True),
+        _dev_ptr(h0, "h0", torch.float32, (batch, dim, N), optional=True),
+        _dev_ptr(y, "y", torch.float32, (batch, dim, L)), _dev_ptr(h_last, "h_last", optional=True),
+        ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream))
     _check(st)
     return (y, h_last) if return_last_state else y
 

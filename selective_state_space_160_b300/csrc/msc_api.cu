@@ -168,6 +168,40 @@ msc_status msc_selective_scan_fwd_ex(int64_t batch, int64_t dim, int64_t seqlen,
     return s6_fwd_launch(a, plan, static_cast<cudaStream_t>(stream));
 }
 
+msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                       int64_t conv_width, msc_dtype in_dtype, const void* x,
+                                       const float* conv_weight, const float* conv_bias, const void* delta,
+                                       const float* A, const void* B, const void* C, const float* D,
+                                       const void* z, const float* delta_bias, const float* h0, float* y,
+                                       float* h_last, void* workspace, size_t workspace_bytes, void* stream) {
+    clear_error();
+    msc_status s = check_s6_dims(batch, dim, seqlen, dstate, in_dtype);
+    if (s != MSC_OK) return s;
+    if (conv_width < 1 || conv_width > 4)
+        return fail(MSC_ERR_UNSUPPORTED, "conv_width must be 1..4 (got %lld)", (long long)conv_width);
+    MSC_PTR(x, "x"); MSC_PTR(conv_weight, "conv_weight"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A");
+    MSC_PTR(B, "B"); MSC_PTR(C, "C"); MSC_PTR(y, "y");
+    MSC_OPT_PTR(conv_bias, "conv_bias"); MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z");
+    MSC_OPT_PTR(delta_bias, "delta_bias"); MSC_OPT_PTR(h0, "h0"); MSC_OPT_PTR(h_last, "h_last");
+    if (seqlen % (in_dtype == MSC_BF16 ? 8 : 4) != 0)
+        return fail(MSC_ERR_UNSUPPORTED, "the fused conv front end needs seqlen a multiple of %d (got %lld)",
+                    in_dtype == MSC_BF16 ? 8 : 4, (long long)seqlen);
+    S6Plan plan = s6_fwd_plan(batch, dim, seqlen, dstate);
+    if (plan.workspace > 0) {
+        if (workspace == nullptr || workspace_bytes < plan.workspace)
+            return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", plan.workspace,
+                        workspace ? workspace_bytes : (size_t)0);
+        MSC_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "workspace must be 256-byte aligned");
+    }
+    S6FwdArgs a{};
+    a.batch = batch; a.dim = dim; a.L = seqlen; a.N = (int)dstate; a.bf16 = in_dtype == MSC_BF16;
+    a.u = x; a.delta = delta; a.z = z; a.B = B; a.C = C;
+    a.A = A; a.D = D; a.delta_bias = delta_bias; a.h0 = h0; a.y = y; a.h_last = h_last;
+    a.workspace = workspace;
+    a.conv_w = conv_weight; a.conv_b = conv_bias; a.conv_k = (int)conv_width;
+    return s6_fwd_launch(a, plan, static_cast<cudaStream_t>(stream));
+}
+
 msc_status msc_selective_state_update(int64_t batch, int64_t dim, int64_t dstate, msc_dtype in_dtype,
                                       const void* u, const void* delta, const float* A, const void* B,
                                       const void* C, const float* D, const void* z, const float* delta_bias,

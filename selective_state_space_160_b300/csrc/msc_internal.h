@@ -26,6 +26,10 @@ struct S6FwdArgs {
     float *y, *h_last;
     void* workspace;
     int disc = 0;  // msc_discretization
+    // fused causal conv1d + SiLU front end: u holds its input x when conv_w is set
+    const float* conv_w = nullptr;  // [dim, conv_k]
+    const float* conv_b = nullptr;  // [dim] or null
+    int conv_k = 0;
 };
 
 msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t stream);

@@ -74,6 +74,9 @@ struct FwdParams {
     float* seg_dsum;   // [rows, G]
     float* ckpt;       // [rows, ckpt_groups, 16]: state at every 8-step group start
     int64_t ckpt_groups;
+    const float* conv_w;  // fused front end: [dim, conv_k] causal conv taps (u then holds its input x)
+    const float* conv_b;  // [dim] or null
+    int conv_k;
     int64_t dim, L, seg_len;
     int N, G;
 };
@@ -346,7 +349,14 @@ __device__ __forceinline__ void reduce_scatter_level(float* v, int j) {
 //  - exponential-trapezoidal ("Mamba 解密" sec. 6.3): b_t = e_t + abar_t e_{t-1}
 //    with e_t = Delta_t B_t u_t / 2, carried per state in registers; a segment's
 //    first step rebuilds e_{t0-1} from the inputs at t0 - 1 (none before t = 0).
-template <bool kBF16, int kMode, int kNG, int kDisc = kDiscEuler>
+// kConv: the u tiles hold the input x of the causal conv1d + SiLU front end, and
+// every lane forms u_t = silu(b + sum_k w_k x_{t-K+1+k}) for its own four steps
+// of each 8-step group: it loads its x as packed pairs and takes the three steps
+// before from its partner lane (the partner's steps of this group, or of the
+// previous group, which the second lane keeps in registers across groups and
+// tiles; at a segment start they are read from memory), so u never goes
+// through HBM.
+template <bool kBF16, int kMode, int kNG, int kDisc = kDiscEuler, bool kConv = false>
 __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                                                               const __grid_constant__ CUtensorMap tm_d,
                                                               const __grid_constant__ CUtensorMap tm_z,
@@ -403,6 +413,28 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
     float dsum = 0.f;
 
     const int64_t t_begin = (int64_t)seg * p.seg_len;
+    // fused conv: taps right-aligned in a 4-tap window (cw[m] multiplies x_{t-3+m}),
+    // as packed pairs; xprev = x of the three steps before this lane's group (kept by
+    // the second lane of the row: its last three steps)
+    static_assert(!kConv || kNG == 2, "the fused conv front end runs with two lanes per row");
+    uint64_t cw2[4];
+    uint64_t cb2 = 0ull;
+    float xprev[3] = {0.f, 0.f, 0.f};
+    if constexpr (kConv) {
+        const int K = p.conv_k;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float w = (row_ok && m + K >= 4) ? __ldg(p.conv_w + d * K + (m + K - 4)) : 0.f;
+            cw2[m] = msc::pk2(w, w);
+        }
+        const float cb = (row_ok && p.conv_b) ? __ldg(p.conv_b + d) : 0.f;
+        cb2 = msc::pk2(cb, cb);
+#pragma unroll
+        for (int m = 0; m < 3; ++m) {
+            const int64_t tp = t_begin - 3 + m;
+            xprev[m] = (j == 1 && row_ok && tp >= 0) ? msc::ld_elem<kBF16>(p.u, row * p.L + tp) : 0.f;
+        }
+    }
     // zero-order hold: 1/A per state (0 where A = 0: the series branch covers it)
     uint64_t invA2[kDisc == kDiscZoh ? kPPL : 1];
     // trapezoid: half input term of the previous step, per state
@@ -503,7 +535,45 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
             // ---- this lane's kSPG steps: Delta, Delta*u, D*u on packed pairs
             const uint32_t boff = (uint32_t)(8 * g * kES + j * kSPG * kES);  // byte offset in the row
             uint64_t u2[kSPG / 2], x2[kSPG / 2];
-            if constexpr (kBF16) {
+            if constexpr (kConv) {
+                // x of this lane's four steps, and of the three before them
+                const uint8_t* px = raw + msc::sw64(r, boff >> 4) + (boff & 15);
+                const uint8_t* pd = raw + kRowTile + msc::sw64(r, boff >> 4) + (boff & 15);
+                float xw[7];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    if constexpr (kBF16) {
+                        const uint32_t wx = reinterpret_cast<const uint32_t*>(px)[e];
+                        const uint32_t wd = reinterpret_cast<const uint32_t*>(pd)[e];
+                        xw[3 + 2 * e] = msc::bf16lo(wx);
+                        xw[4 + 2 * e] = msc::bf16hi(wx);
+                        x2[e] = msc::pk2(msc::bf16lo(wd), msc::bf16hi(wd));
+                    } else {
+                        const float2 fx = reinterpret_cast<const float2*>(px)[e];
+                        xw[3 + 2 * e] = fx.x;
+                        xw[4 + 2 * e] = fx.y;
+                        x2[e] = reinterpret_cast<const uint64_t*>(pd)[e];
+                    }
+                }
+                // lane 0 of the row sends its steps 1..3 (lane 1's predecessors), lane 1
+                // its previous group's steps 1..3 (lane 0's predecessors)
+#pragma unroll
+                for (int m = 0; m < 3; ++m) {
+                    const float send = j == 0 ? xw[4 + m] : xprev[m];
+                    xw[m] = __shfl_xor_sync(0xffffffffu, send, 1);
+                }
+                if (j == 1) {
+#pragma unroll
+                    for (int m = 0; m < 3; ++m) xprev[m] = xw[4 + m];
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    uint64_t acc = cb2;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) acc = msc::fma2(cw2[m], msc::pk2(xw[2 * e + m], xw[2 * e + 1 + m]), acc);
+                    u2[e] = msc::silu_2(acc);
+                }
+            } else if constexpr (kBF16) {
                 const uint8_t* pu = raw + msc::sw64(r, boff >> 4) + (boff & 15);
                 const uint8_t* pd = raw + kRowTile + msc::sw64(r, boff >> 4) + (boff & 15);
 #pragma unroll
@@ -776,14 +846,14 @@ bool make_maps(FwdMaps& m, const FwdParams& p, int64_t batch, bool bf16) {
 // warps but add more exchange work than the extra latency hiding recovers.
 constexpr int kLanesPerRow = 2;
 
-template <bool kBF16, int kNG, int kDisc = kDiscEuler>
+template <bool kBF16, int kNG, int kDisc = kDiscEuler, bool kConv = false>
 msc_status launch_tma_ng(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
     if (mode == kModeFull)
-        s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+        s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc, kConv><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
     else if (mode == kModeAgg)
-        s6_fwd_tma_kernel<kBF16, kModeAgg, kNG, kDisc><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
-    else if (kDisc == kDiscEuler)
+        s6_fwd_tma_kernel<kBF16, kModeAgg, kNG, kDisc, kConv><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    else if (kDisc == kDiscEuler && !kConv)
         s6_fwd_tma_kernel<kBF16, kModeCkpt, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
     else
         return msc_host::fail(MSC_ERR_UNSUPPORTED, "checkpoints are kept for the exponential-Euler form only");
@@ -793,6 +863,11 @@ msc_status launch_tma_ng(const FwdMaps& m, const FwdParams& p, int64_t batch, in
 template <bool kBF16>
 msc_status launch_tma(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, int disc,
                       cudaStream_t st) {
+    if (p.conv_w) {
+        if (disc != kDiscEuler)
+            return msc_host::fail(MSC_ERR_UNSUPPORTED, "the fused conv front end runs with the exponential-Euler form");
+        return launch_tma_ng<kBF16, kLanesPerRow, kDiscEuler, true>(m, p, batch, G, mode, st);
+    }
     if (disc == kDiscZoh) return launch_tma_ng<kBF16, kLanesPerRow, kDiscZoh>(m, p, batch, G, mode, st);
     if (disc == kDiscTrap) return launch_tma_ng<kBF16, kLanesPerRow, kDiscTrap>(m, p, batch, G, mode, st);
     return launch_tma_ng<kBF16, kLanesPerRow>(m, p, batch, G, mode, st);
@@ -808,6 +883,10 @@ msc_status launch_mode(const FwdParams& p, const FwdMaps* maps, bool bf16, bool 
     if (maps)
         return bf16 ? launch_tma<true>(*maps, p, batch, G, mode, disc, st)
                     : launch_tma<false>(*maps, p, batch, G, mode, disc, st);
+    if (p.conv_w)
+        return msc_host::fail(MSC_ERR_UNSUPPORTED,
+                              "the fused conv front end needs 16-byte row strides "
+                              "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32)");
     if (disc != kDiscEuler)
         return msc_host::fail(MSC_ERR_UNSUPPORTED,
                               "the zero-order-hold and trapezoidal forms need 16-byte row strides "
@@ -852,6 +931,7 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
     p.A = a.A; p.D = a.D; p.delta_bias = a.delta_bias; p.h0 = a.h0;
     p.y = a.y; p.h_last = a.h_last;
     p.dim = a.dim; p.L = a.L; p.N = a.N; p.G = plan.G; p.seg_len = plan.seg_len;
+    p.conv_w = a.conv_w; p.conv_b = a.conv_b; p.conv_k = a.conv_k;
     // 16-byte vector loads need every row and tile start 16-byte aligned:
     // bases are checked by the caller; rows start at row * L elements.
     const bool vec = (a.L % 8) == 0;

@@ -123,3 +123,12 @@ def s6_inputs_torch(batch, dim, seqlen, dstate, seed=SEED_BASE, bf16=False, devi
     if with_dy:
         out["dy"] = normal((batch, dim, seqlen))
     return out
+
+
+def conv_taps(dim, width, seed=SEED_BASE):
+    """Causal conv1d front-end parameters: weight [dim, width] with unit-variance
+    outputs for unit-variance inputs, and a small bias [dim] (float32)."""
+    g = _rng(seed)
+    w = (_normal(g, (dim, width)) / np.float32(np.sqrt(width))).astype(np.float32)
+    b = _normal(g, (dim,), 0.1)
+    return w, b

@@ -186,3 +186,28 @@ def test_ssd_bwd_rejects_bad_arguments(lib):
     with_z = msc.msc_ssd_chunked_bwd_workspace_size(2, 1000, 8, 64, 128, 1, 256, True)
     assert 0 < no_z < with_z
     assert call(z=16, dz=16, wsb=no_z, L=1000, b=2, H=8) == msc.MSC_ERR_WORKSPACE
+
+
+def test_signatures_match_header_argument_counts():
+    """Every binding signature has as many arguments as the header declares."""
+    src = open(os.path.join(ROOT, "include", "msc.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for name in declared_functions():
+        m = re.search(r"\b%s\s*\(([^)]*)\)" % name, src)
+        params = m.group(1).strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(msc.SIGNATURES[name][1]) == n, name
+
+
+def test_fwd_conv_rejects_bad_arguments(lib):
+    f = lib.msc_selective_scan_fwd_conv
+
+    def call(K=4, L=64, dt=1, x=16, w=16, N=16):
+        return f(1, 4, L, N, K, dt, x, w, None, 16, 16, 16, 16, None, None, None, None, 16, None, None, 0, None)
+
+    assert call(K=0) == msc.MSC_ERR_UNSUPPORTED
+    assert call(K=5) == msc.MSC_ERR_UNSUPPORTED
+    assert call(x=None) == msc.MSC_ERR_INVALID_ARG and "x" in msc.msc_last_error()
+    assert call(w=None) == msc.MSC_ERR_INVALID_ARG and "conv_weight" in msc.msc_last_error()
+    assert call(L=100) == msc.MSC_ERR_UNSUPPORTED                # bf16 rows need seqlen % 8 == 0
+    assert call(N=17) == msc.MSC_ERR_UNSUPPORTED
