@@ -42,8 +42,9 @@ HEADLINE = dict(batch=8, dim=5120, L=2048, N=16)
 # dram__bytes_read.sum + dram__bytes_write.sum per launch, from one ncu capture,
 # keyed by kernel; valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
-    # profiles/s6_fwd_tma_8x5120x2048_bf16.md: DRAM read 505.2 MB + write 298.3 MB
-    "s6_fwd_rows_kernel": {"src_sha": "b0be9c35fa5e", "bytes_per_launch": 803.5e6},
+    # profiles/s6_fwd_tma_8x5120x2048_bf16.md: DRAM read 505.2 MB + write 298.6 MB per launch,
+    # taken from the source whose hash is src_sha (any later change makes the traffic null)
+    "s6_fwd_tma_kernel": {"src_sha": "0500199e411e", "bytes_per_launch": 803.84e6},
 }
 
 
@@ -687,7 +688,7 @@ def run_ours(args):
 
     src = os.path.join(ROOT, "selective_state_space_160_b300", "csrc", "s6_fwd.cu")
     nbytes = el * (2 + 2 + 2 + 4) + 2 * b * N * L * 2
-    roof = roofline_s6(el, N, nbytes, kernel_ms, peaks, pipes, kernel="s6_fwd_rows_kernel", src=src)
+    roof = roofline_s6(el, N, nbytes, kernel_ms, peaks, pipes, kernel="s6_fwd_tma_kernel", src=src)
 
     legs = {}
     if rank == 0 and args.legs != "none":
