@@ -172,6 +172,33 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, silu=True):
     return (_silu(out) if silu else out), window[:, :, 1:]
 
 
+def causal_conv1d_bwd(x, weight, bias=None, dout=None, silu=True):
+    """Gradients of causal_conv1d for an upstream gradient dout [batch, dim, L]
+    (the chain rule through its definition): with pre the pre-activation and
+    g = dout * silu'(pre) (g = dout without the activation),
+      dx[b, d, s]  = sum_k weight[d, k] g[b, d, s + (K - 1) - k]   (terms past L are 0)
+      dweight[d, k] = sum_{b, t} g[b, d, t] x[b, d, t - (K - 1) + k]
+      dbias[d]     = sum_{b, t} g[b, d, t].
+    Returns (dx, dweight, dbias) in float64."""
+    x = _f64(x)
+    w = _f64(weight)
+    g = _f64(dout)
+    batch, dim, L = x.shape
+    K = w.shape[1]
+    if silu:
+        pre = causal_conv1d(x, w, bias, silu=False)
+        sg = 1.0 / (1.0 + np.exp(-pre))
+        g = g * sg * (1.0 + pre * (1.0 - sg))
+    xp = np.concatenate([np.zeros((batch, dim, K - 1)), x], axis=2)
+    gp = np.concatenate([g, np.zeros((batch, dim, K - 1))], axis=2)
+    dx = np.zeros((batch, dim, L))
+    dw = np.zeros((dim, K))
+    for k in range(K):
+        dx += w[None, :, k, None] * gp[:, :, K - 1 - k:K - 1 - k + L]
+        dw[:, k] = np.einsum("bdt,bdt->d", g, xp[:, :, k:k + L])
+    return dx, dw, g.sum(axis=(0, 2))
+
+
 def s6_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, dy=None):
     """S6 backward (zero initial state).  Returns a dict of float64 grads:
     du, ddelta, dA, dB, dC, and dD / dz / ddelta_bias when the input is present."""

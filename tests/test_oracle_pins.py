@@ -453,6 +453,33 @@ def test_p10_conv1d_update_chain_equals_sequence():
     np.testing.assert_array_equal(state, x[:, :, -3:])
 
 
+@pytest.mark.parametrize("K,silu", [(4, True), (3, False), (1, True)])
+def test_p10_conv1d_backward_finite_differences(K, silu):
+    """The conv backward against central finite differences of <dout, out> of
+    the conv oracle, for every entry of x, the weights and the bias."""
+    rng = np.random.default_rng(72 + K)
+    x = rng.standard_normal((2, 3, 9))
+    w = rng.standard_normal((3, K))
+    bias = rng.standard_normal(3)
+    dout = rng.standard_normal((2, 3, 9))
+    dx, dw, db = oracle.causal_conv1d_bwd(x, w, bias, dout, silu=silu)
+    h = 1e-6
+
+    def loss(x_, w_, b_):
+        return float((oracle.causal_conv1d(x_, w_, b_, silu=silu) * dout).sum())
+    for arr, grad in ((x, dx), (w, dw), (bias, db)):
+        num = np.empty_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = loss(x, w, bias)
+            arr[idx] = old - h
+            lm = loss(x, w, bias)
+            arr[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-7)
+
+
 # ---------------------------------------------------------------------------- P11
 def _delta_for(dt):
     """pre-activation delta whose softplus is dt (bias 0)"""
@@ -609,3 +636,26 @@ def test_planted_mistakes(tmp_path, desc, orig, mut, monkeypatch):
             break
     monkeypatch.setattr(oracle, "_lib", None)
     assert caught, "no pin caught: " + desc
+
+
+PY_MUTATIONS = [
+    # (description, function, original text, mutated text) in oracle.py
+    ("conv bwd: taps not reversed", "causal_conv1d_bwd", "gp[:, :, K - 1 - k:K - 1 - k + L]", "gp[:, :, k:k + L]"),
+    ("conv bwd: silu derivative without its second term", "causal_conv1d_bwd",
+     "g = g * sg * (1.0 + pre * (1.0 - sg))", "g = g * sg"),
+]
+
+
+@pytest.mark.parametrize("desc,fn,orig,mut", PY_MUTATIONS, ids=[m[0] for m in PY_MUTATIONS])
+def test_planted_mistakes_python(desc, fn, orig, mut, monkeypatch):
+    """Plant each mistake in a copy of a Python oracle function and check that
+    its pin fails."""
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(getattr(oracle, fn)))
+    assert orig in src, desc
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(orig, mut, 1), "<planted>", "exec"), ns)
+    monkeypatch.setattr(oracle, fn, ns[fn])
+    with pytest.raises(AssertionError):
+        test_p10_conv1d_backward_finite_differences(4, True)
