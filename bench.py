@@ -387,6 +387,35 @@ def leg_conv1d(peaks, pipes, steps=10, warmup=3):
     return res
 
 
+def leg_conv1d_bwd(peaks, pipes, steps=10, warmup=3):
+    """Backward of the causal conv1d (K 4) + SiLU, batch 8 x D 5120 x L 2048:
+    x bf16 and dout fp32 in, dx fp32 out (the pre-activation is recomputed)."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    batch, dim, L, K = 8, 5120, 2048, 4
+    g = torch.Generator(device="cuda").manual_seed(160_009)
+    x = torch.randn((batch, dim, L), device="cuda", generator=g).to(torch.bfloat16)
+    w = torch.randn((dim, K), device="cuda", generator=g) / 2.0
+    bias = 0.1 * torch.randn(dim, device="cuda", generator=g)
+    dout = torch.randn((batch, dim, L), device="cuda", generator=g)
+    st = torch.cuda.current_stream()
+
+    def fn():
+        msc.msc_causal_conv1d_bwd(x, w, dout, bias)
+    ms = statistics.median(time_launches(fn, steps, warmup, st))
+    el = batch * dim * L
+    nbytes = el * (2 + 4 + 4) + dim * (K + 1) * 4 * 2
+    t = ms * 1e-3
+    ach = nbytes / t / 1e9
+    res = {"workload": "causal conv1d K 4 + SiLU backward, batch 8, D 5120, L 2048, bf16 x, fp32 dout / dx",
+           "elements_per_s": el / t, "ms": ms,
+           "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": nbytes}}
+    del x, dout
+    torch.cuda.empty_cache()
+    return res
+
+
 def leg_conv_scan(peaks, pipes, steps=5, warmup=2):
     """The Mamba block's front end and scan at the headline shape (batch 8, D
     5120, L 2048, N 16, bf16, conv width 4): fused (u formed inside the scan)
@@ -696,7 +725,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         for name in args.legs.split(","):
             try:
-                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "ssd_bwd": leg_ssd_bwd, "decode": leg_decode, "conv1d": leg_conv1d, "conv_scan": leg_conv_scan, "disc": leg_disc}[name]
+                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "ssd_bwd": leg_ssd_bwd, "decode": leg_decode, "conv1d": leg_conv1d, "conv1d_bwd": leg_conv1d_bwd, "conv_scan": leg_conv_scan, "disc": leg_disc}[name]
                 legs[name] = fn(peaks, pipes)
             except Exception as ex:  # report, do not hide: a failing leg is printed as such
                 legs[name] = {"error": "%s: %s" % (type(ex).__name__, ex)}
@@ -737,7 +766,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="fwd_long,bwd,ssd,ssd_bwd,decode,conv1d,conv_scan,disc")
+    ap.add_argument("--legs", default="fwd_long,bwd,ssd,ssd_bwd,decode,conv1d,conv1d_bwd,conv_scan,disc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ssd-batch", type=int, default=4, help="batch of the SSD legs (4 = the timed workload)")

@@ -210,6 +210,20 @@ msc_status msc_causal_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int
                                  const float* weight, const float* bias, int silu, void* out,
                                  void* stream);
 
+/* Backward of msc_causal_conv1d_fwd for an upstream gradient dout (the chain
+ * rule through its definition): with pre the pre-activation and g = dout *
+ * silu'(pre) (g = dout when silu = 0),
+ *   dx[b, d, s]   = sum_k weight[d, k] g[b, d, s + (width - 1) - k]
+ *   dweight[d, k] = sum_{b, t} g[b, d, t] x[b, d, t - (width - 1) + k]
+ *   dbias[d]      = sum_{b, t} g[b, d, t]
+ * x, weight, bias, silu as the forward (x in in_dtype); dout, dx [batch, dim,
+ * seqlen] fp32 (dout is what msc_selective_scan_bwd returns as du); dweight
+ * [dim, width] and dbias [dim] fp32 (dbias may be NULL), overwritten.  The sums
+ * over batch and steps use fp32 atomics.  No workspace. */
+msc_status msc_causal_conv1d_bwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t width, msc_dtype in_dtype,
+                                 const void* x, const float* weight, const float* bias, int silu,
+                                 const float* dout, float* dx, float* dweight, float* dbias, void* stream);
+
 /* Decode step of the same convolution (study note "Mamba — 选择性状态空间模型",
  * 踩过的坑: with no attention cache, the convolution still keeps the last
  * few inputs).  conv_state [batch, dim, width - 1] fp32 holds the previous

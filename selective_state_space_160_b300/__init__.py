@@ -18,7 +18,7 @@ __all__ = [
     "msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd", "msc_ssd_chunked_bwd",
     "msc_selective_state_update", "msc_ssd_chunked_bwd_workspace_size",
     "msc_causal_conv1d_fwd", "msc_causal_conv1d_update", "msc_selective_scan_fwd_ex",
-    "msc_selective_scan_fwd_conv",
+    "msc_selective_scan_fwd_conv", "msc_causal_conv1d_bwd",
     "MSC_DISC_EULER", "MSC_DISC_ZOH", "MSC_DISC_TRAPEZOID",
     "msc_selective_scan_fwd_workspace_size", "msc_selective_scan_bwd_workspace_size",
     "msc_ssd_chunked_fwd_workspace_size", "msc_check_device_status", "msc_status_string",
@@ -54,6 +54,7 @@ SIGNATURES = {
     "msc_selective_state_update": (ctypes.c_int, [_i64] * 3 + [ctypes.c_int] + [_vp] * 10 + [_vp]),
     "msc_causal_conv1d_fwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] * 2 + [_vp] * 3 + [ctypes.c_int] + [_vp, _vp]),
     "msc_causal_conv1d_update": (ctypes.c_int, [_i64] * 3 + [ctypes.c_int] * 2 + [_vp] * 3 + [ctypes.c_int] + [_vp] * 3),
+    "msc_causal_conv1d_bwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 3 + [ctypes.c_int] + [_vp] * 5),
     "msc_check_device_status": (ctypes.c_int, [_vp]),
     "msc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "msc_last_error": (ctypes.c_char_p, []),
@@ -301,6 +302,27 @@ def msc_causal_conv1d_fwd(x, weight, bias=None, silu=True, out_dtype=None, out=N
                                    _dev_ptr(out, "out", out.dtype, (batch, dim, L)), _stream_ptr(stream))
     _check(st)
     return out
+
+
+def msc_causal_conv1d_bwd(x, weight, dout, bias=None, silu=True, with_dbias=True, stream=None):
+    """Backward of msc_causal_conv1d_fwd.  x: [batch, dim, L] fp32 or bf16;
+    weight [dim, K], bias [dim] fp32 (the forward's); dout [batch, dim, L] fp32.
+    Returns (dx [batch, dim, L], dweight [dim, K], dbias [dim] or None), fp32."""
+    torch = _torch()
+    lib = load_library()
+    batch, dim, L = x.shape
+    K = weight.shape[1]
+    f32 = torch.float32
+    dx = torch.empty((batch, dim, L), dtype=f32, device=x.device)
+    dw = torch.empty((dim, K), dtype=f32, device=x.device)
+    db = torch.empty((dim,), dtype=f32, device=x.device) if with_dbias else None
+    st = lib.msc_causal_conv1d_bwd(batch, dim, L, K, _in_dtype(x), _dev_ptr(x, "x"),
+                                   _dev_ptr(weight, "weight", f32, (dim, K)),
+                                   _dev_ptr(bias, "bias", f32, (dim,), optional=True), int(bool(silu)),
+                                   _dev_ptr(dout, "dout", f32, (batch, dim, L)), _dev_ptr(dx, "dx"),
+                                   _dev_ptr(dw, "dweight"), _dev_ptr(db, "dbias", optional=True), _stream_ptr(stream))
+    _check(st)
+    return dx, dw, db
 
 
 def msc_causal_conv1d_update(x, conv_state, weight, bias=None, silu=True, out_dtype=None, out=None, stream=None):

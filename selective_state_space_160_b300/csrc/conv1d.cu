@@ -3,9 +3,9 @@
 // What it computes (bqwf survey sec. 3.1: each Mamba block runs a causal 1-D
 // convolution for local context before the selective SSM):
 //   out[b, d, t] = silu(bias[d] + sum_{k < K} w[d, k] x[b, d, t - (K - 1) + k]),  x = 0 before t = 0
-// and its decode step, which keeps the last K - 1 inputs of every row (study
+// its decode step, which keeps the last K - 1 inputs of every row (study
 // note "Mamba — 选择性状态空间模型", 踩过的坑: the convolution still keeps the
-// last few inputs when there is no attention cache).
+// last few inputs when there is no attention cache), and its backward.
 //
 // Design.  Both are bound by HBM: per element the sequence kernel reads x once
 // (2 or 4 bytes) and writes out once; the K <= 8 weights of a channel and its
@@ -142,6 +142,136 @@ __global__ void __launch_bounds__(256) conv1d_update_kernel(const ConvParams p) 
     }
 }
 
+// Backward, one thread per 16 consecutive steps of a row (the forward's tiling):
+// with pre the pre-activation and g = dout silu'(pre) (dout without the
+// activation), dx[s] = sum_k w[k] g[s + K - 1 - k], dw[k] += sum_t g[t] x[t - K + 1 + k],
+// db += sum_t g[t].  The thread recomputes pre over its 16 steps and the 8 after
+// (an 8-step halo of x before them), so it needs x of steps t0 - 8 .. t0 + 24
+// and dout of t0 .. t0 + 24.  dw and db: a butterfly over the warp when all 32
+// lanes hold chunks of one row, else per-thread atomics.
+// kW: the tap window (4 when K <= 4, as in Mamba, else 8), weights right-aligned.
+template <bool kInBF16, bool kVec, int kW>
+__global__ void __launch_bounds__(256) conv1d_bwd_kernel(const ConvParams p, const float* dout, float* dx,
+                                                         float* dw, float* db) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool live = idx < p.rows * p.nchunks;
+    const int64_t row = live ? idx / p.nchunks : 0;
+    const int64_t c = live ? idx - row * p.nchunks : 0;
+    const int64_t d = row % p.dim;
+    const int64_t t0 = 16 * c;
+    const int K = p.K;
+    const int lane = threadIdx.x & 31;
+    // xv[i] = x[t0 - 8 + i] (i < 32), gv[i] = dout[t0 + i] (i < 24), 0 outside [0, L)
+    float xv[32], gv[24];
+    const bool vec = kVec && live && t0 + 24 <= p.L;
+    if (vec) {
+        if (c > 0) msc::ld8<kInBF16>(p.x, row * p.L + t0 - 8, xv);
+        else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xv[i] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            msc::ld8<kInBF16>(p.x, row * p.L + t0 + 8 * q, xv + 8 + 8 * q);
+            msc::ld8<false>(dout, row * p.L + t0 + 8 * q, gv + 8 * q);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int64_t t = t0 - 8 + i;
+            xv[i] = (live && t >= 0 && t < p.L) ? msc::ld_elem<kInBF16>(p.x, row * p.L + t) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 24; ++i) {
+            const int64_t t = t0 + i;
+            gv[i] = (live && t < p.L) ? dout[row * p.L + t] : 0.f;
+        }
+    }
+    float ws[kW];
+#pragma unroll
+    for (int m = 0; m < kW; ++m) ws[m] = (live && m + K >= kW) ? __ldg(p.w + d * K + (m + K - kW)) : 0.f;
+    const float b0 = (live && p.bias) ? __ldg(p.bias + d) : 0.f;
+    // g over steps t0 .. t0 + 15 + kW - 1
+    // (pre[t0 + i] = sum_m ws[m] x[t0 + i - kW + 1 + m] = sum_m ws[m] xv[i + 9 - kW + m])
+    constexpr int kG = 16 + kW - 1;
+    if (p.silu) {
+#pragma unroll
+        for (int i = 0; i < kG; ++i) {
+            float pre = b0;
+#pragma unroll
+            for (int m = 0; m < kW; ++m) pre = fmaf(ws[m], xv[i + 9 - kW + m], pre);
+            const float sg = msc::sigmoid_f(pre);
+            gv[i] *= sg * (1.f + pre * (1.f - sg));
+        }
+    }
+    // dx[t0 + s] = sum_m ws[m] g[t0 + s + kW - 1 - m]
+    if (live) {
+        float o[16];
+#pragma unroll
+        for (int s2 = 0; s2 < 16; ++s2) {
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < kW; ++m) acc = fmaf(ws[m], gv[s2 + kW - 1 - m], acc);
+            o[s2] = acc;
+        }
+        if (kVec && t0 + 16 <= p.L) {
+            float4* q = reinterpret_cast<float4*>(dx + row * p.L + t0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) q[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+        } else {
+#pragma unroll
+            for (int s2 = 0; s2 < 16; ++s2)
+                if (t0 + s2 < p.L) dx[row * p.L + t0 + s2] = o[s2];
+        }
+    }
+    // partial dw (tap m of the window) and db over this thread's own steps
+    float part[kW + 1];
+#pragma unroll
+    for (int m = 0; m <= kW; ++m) part[m] = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < 16; ++s2) {
+        const float gg = (t0 + s2 < p.L) ? gv[s2] : 0.f;
+#pragma unroll
+        for (int m = 0; m < kW; ++m) part[m] = fmaf(gg, xv[s2 + 9 - kW + m], part[m]);
+        part[kW] += gg;
+    }
+    const int64_t row0 = __shfl_sync(0xffffffffu, row, 0);
+    const bool one_row = __all_sync(0xffffffffu, live && row == row0);
+    if (one_row) {
+#pragma unroll
+        for (int m = 0; m <= kW; ++m)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) part[m] += __shfl_xor_sync(0xffffffffu, part[m], off);
+        if (lane != 0) return;
+    } else if (!live) {
+        return;
+    }
+#pragma unroll
+    for (int m = 0; m < kW; ++m)
+        if (m + K >= kW) atomicAdd(dw + d * K + (m + K - kW), part[m]);
+    if (db) atomicAdd(db + d, part[kW]);
+}
+
+template <bool kIn>
+msc_status launch_bwd(const ConvParams& p, bool vec, const float* dout, float* dx, float* dw, float* db,
+                      cudaStream_t st) {
+    const int64_t n = p.rows * p.nchunks;
+    const int64_t blocks = (n + 255) / 256;
+    if (blocks > 0x7FFFFFFF) return msc_host::fail(MSC_ERR_UNSUPPORTED, "problem too large for one launch");
+    if (p.K <= 4) {
+        if (vec)
+            conv1d_bwd_kernel<kIn, true, 4><<<(unsigned)blocks, 256, 0, st>>>(p, dout, dx, dw, db);
+        else
+            conv1d_bwd_kernel<kIn, false, 4><<<(unsigned)blocks, 256, 0, st>>>(p, dout, dx, dw, db);
+    } else {
+        if (vec)
+            conv1d_bwd_kernel<kIn, true, 8><<<(unsigned)blocks, 256, 0, st>>>(p, dout, dx, dw, db);
+        else
+            conv1d_bwd_kernel<kIn, false, 8><<<(unsigned)blocks, 256, 0, st>>>(p, dout, dx, dw, db);
+    }
+    return msc_host::check_launch("conv1d_bwd");
+}
+
 template <bool kIn, bool kOut>
 msc_status launch_fwd(const ConvParams& p, bool vec, cudaStream_t st) {
     const int64_t n = p.rows * p.nchunks;
@@ -175,6 +305,20 @@ msc_status conv1d_fwd_launch(const Conv1dArgs& a, cudaStream_t st) {
     if (a.in_bf16)
         return a.out_bf16 ? launch_fwd<true, true>(p, vec, st) : launch_fwd<true, false>(p, vec, st);
     return a.out_bf16 ? launch_fwd<false, true>(p, vec, st) : launch_fwd<false, false>(p, vec, st);
+}
+
+msc_status conv1d_bwd_launch(const Conv1dArgs& a, const float* dout, float* dx, float* dweight, float* dbias,
+                             cudaStream_t st) {
+    ConvParams p{};
+    p.x = a.x; p.w = a.weight; p.bias = a.bias;
+    p.rows = a.batch * a.dim; p.dim = a.dim; p.L = a.L; p.nchunks = (a.L + 15) / 16;
+    p.K = a.K; p.silu = a.silu;
+    cudaError_t e = cudaMemsetAsync(dweight, 0, (size_t)a.dim * a.K * sizeof(float), st);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, (size_t)a.dim * sizeof(float), st);
+    if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "conv1d bwd memset: %s", cudaGetErrorString(e));
+    const bool vec = (a.L % 8) == 0;
+    return a.in_bf16 ? launch_bwd<true>(p, vec, dout, dx, dweight, dbias, st)
+                     : launch_bwd<false>(p, vec, dout, dx, dweight, dbias, st);
 }
 
 msc_status conv1d_update_launch(const Conv1dArgs& a, cudaStream_t st) {

@@ -246,6 +246,22 @@ msc_status msc_causal_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int
     return conv1d_fwd_launch(a, static_cast<cudaStream_t>(stream));
 }
 
+msc_status msc_causal_conv1d_bwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t width, msc_dtype in_dtype,
+                                 const void* x, const float* weight, const float* bias, int silu, const float* dout,
+                                 float* dx, float* dweight, float* dbias, void* stream) {
+    clear_error();
+    msc_status s = check_conv_dims(batch, dim, seqlen, width, in_dtype, MSC_F32);
+    if (s != MSC_OK) return s;
+    MSC_PTR(x, "x"); MSC_PTR(weight, "weight"); MSC_PTR(dout, "dout"); MSC_PTR(dx, "dx");
+    MSC_PTR(dweight, "dweight");
+    MSC_OPT_PTR(bias, "bias"); MSC_OPT_PTR(dbias, "dbias");
+    Conv1dArgs a{};
+    a.batch = batch; a.dim = dim; a.L = seqlen; a.K = (int)width; a.silu = silu != 0;
+    a.in_bf16 = in_dtype == MSC_BF16; a.out_bf16 = false;
+    a.x = x; a.weight = weight; a.bias = bias;
+    return conv1d_bwd_launch(a, dout, dx, dweight, dbias, static_cast<cudaStream_t>(stream));
+}
+
 msc_status msc_causal_conv1d_update(int64_t batch, int64_t dim, int64_t width, msc_dtype in_dtype,
                                     msc_dtype out_dtype, const void* x, const float* weight, const float* bias,
                                     int silu, float* conv_state, void* out, void* stream) {

@@ -84,6 +84,9 @@ struct Conv1dArgs {
 
 msc_status conv1d_fwd_launch(const Conv1dArgs& a, cudaStream_t stream);
 msc_status conv1d_update_launch(const Conv1dArgs& a, cudaStream_t stream);
+// dout, dx: [batch, dim, L] fp32; dweight [dim, K], dbias [dim] (may be null) fp32, overwritten.
+msc_status conv1d_bwd_launch(const Conv1dArgs& a, const float* dout, float* dx, float* dweight, float* dbias,
+                             cudaStream_t stream);
 
 struct SsdArgs {
     int64_t batch, L, H, P, N, G, Q;

@@ -111,3 +111,60 @@ def test_conv_config_full_size_sampled():
     ref = oracle.causal_conv1d(x[:, ds], w[ds], bias[ds])
     assert bf16_match(got[:, ds], ref) <= 1.0
     assert np.all(np.isfinite(got))
+
+
+# ----------------------------------------------------------------------------- backward
+TOL_BWD = 1e-4
+
+
+def _bwd(x, w, bias, dout, bf16, silu=True, with_dbias=True):
+    import selective_state_space_160_b300 as msc
+    dx, dw, db = msc.msc_causal_conv1d_bwd(to_dev(x, bf16), to_dev(w), to_dev(dout), to_dev(bias), silu=silu,
+                                           with_dbias=with_dbias)
+    return dx.cpu().numpy(), dw.cpu().numpy(), (None if db is None else db.cpu().numpy())
+
+
+@pytest.mark.parametrize("batch,dim,L,K,bf16,silu", [
+    (1, 4, 64, 4, False, True), (2, 37, 96, 4, True, True), (2, 5, 100, 3, False, True),
+    (1, 3, 17, 8, False, False), (3, 8, 2048, 4, True, True), (1, 6, 1, 2, True, True),
+    (2, 33, 999, 1, False, True)])
+def test_bwd_shapes(batch, dim, L, K, bf16, silu):
+    x, w, bias = _data(batch, dim, L, K, 5000 + L + K, bf16)
+    dout = np.random.default_rng(5100 + L).standard_normal((batch, dim, L)).astype(np.float32)
+    dx, dw, db = _bwd(x, w, bias, dout, bf16, silu)
+    rdx, rdw, rdb = oracle.causal_conv1d_bwd(x, w, bias, dout, silu=silu)
+    assert max_rel_err(dx, rdx) <= TOL_BWD
+    # dw and db sum batch x L terms: relative to the sum of their magnitudes
+    scale = 1.0 + np.abs(dout).sum() / dim
+    assert np.max(np.abs(dw - rdw)) / scale <= TOL_BWD
+    assert np.max(np.abs(db - rdb)) / scale <= TOL_BWD
+
+
+def test_bwd_no_bias_and_no_dbias():
+    x, w, _ = _data(2, 16, 256, 4, 5200, False)
+    dout = np.random.default_rng(5201).standard_normal((2, 16, 256)).astype(np.float32)
+    dx, dw, db = _bwd(x, w, None, dout, False, with_dbias=False)
+    rdx, rdw, _ = oracle.causal_conv1d_bwd(x, w, None, dout)
+    assert db is None
+    assert max_rel_err(dx, rdx) <= TOL_BWD
+    assert max_rel_err(dw, rdw) <= 1e-3
+
+
+def test_bwd_through_scan_chain():
+    """conv -> scan -> loss: the scan's du fed to the conv backward equals the
+    oracle's chain (conv oracle, S6 backward oracle, conv backward oracle)."""
+    import selective_state_space_160_b300 as msc
+    from selective_state_space_160_b300.inputs import s6_inputs, conv_taps
+    inp = s6_inputs(2, 24, 128, 16, seed=5300, with_dy=True)
+    w, cb = conv_taps(24, 4, seed=5301)
+    u = msc.msc_causal_conv1d_fwd(to_dev(inp["u"]), to_dev(w), to_dev(cb))
+    g = msc.msc_selective_scan_bwd(u, to_dev(inp["delta"]), to_dev(inp["A"]), to_dev(inp["B"]), to_dev(inp["C"]),
+                                   to_dev(inp["D"]), to_dev(inp["z"]), to_dev(inp["delta_bias"]), to_dev(inp["dy"]))
+    dx, dw, db = msc.msc_causal_conv1d_bwd(to_dev(inp["u"]), to_dev(w), g["du"], to_dev(cb))
+    ru = oracle.causal_conv1d(inp["u"], w, cb)
+    rg = oracle.s6_bwd(ru, inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["delta_bias"],
+                       inp["dy"])
+    rdx, rdw, rdb = oracle.causal_conv1d_bwd(inp["u"], w, cb, rg["du"])
+    assert max_rel_err(dx.cpu().numpy(), rdx) <= 1e-3
+    assert max_rel_err(dw.cpu().numpy(), rdw) <= 1e-3
+    assert max_rel_err(db.cpu().numpy(), rdb) <= 1e-3
