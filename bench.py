@@ -162,13 +162,21 @@ def _barrier(ws):
 
 
 def _max_over_ranks(x, ws):
+    """Largest x over the ranks (the slowest rank's time)."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_step, steps, ws, max_ms):
+    """Units all ranks processed (weak scaling: each rank its own units) over
+    the slowest rank's time."""
+    return units_per_step * steps * ws / (max_ms * 1e-3)
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -683,7 +691,7 @@ def run_ours(args):
     kernel_ms = statistics.mean(a.elapsed_time(e) for a, e in per)
     total_ms = _max_over_ranks(total_ms, ws)
     el = b * dim * L
-    value = el * args.steps * ws / (total_ms * 1e-3)
+    value = whole_job_rate(el, args.steps, ws, total_ms)
 
     # end to end through the public API with host buffers: H2D of this step's
     # inputs from pinned memory, the call, D2H of y
@@ -712,7 +720,7 @@ def run_ours(args):
     e2.record(stream)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(s2.elapsed_time(e2), ws)
-    e2e_value = el * e2e_steps * ws / (e2e_ms * 1e-3)
+    e2e_value = whole_job_rate(el, e2e_steps, ws, e2e_ms)
     del host, dev_in, yh
 
     src = os.path.join(ROOT, "selective_state_space_160_b300", "csrc", "s6_fwd.cu")
