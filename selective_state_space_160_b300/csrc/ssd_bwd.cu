@@ -610,7 +610,8 @@ constexpr int kDxOpWarps = 16;
 constexpr int kDxWarpLoad = kDxOpWarps, kDxWarpMma = kDxOpWarps + 1;
 constexpr int kDxThreads = (kDxOpWarps + 2) * 32;
 constexpr int kDxHB = 8;                       // heads per CTA
-constexpr size_t kDxSmem = 1024 + kDxStages * kDxStage + (3 * 512 + 1024) * 4 + 24 * 8 + 16;
+constexpr uint32_t kDxEpi = 32768;             // the epilogue's dy and x tiles [128 j][64 p] (no gate)
+constexpr size_t kDxSmem = 1024 + kDxStages * kDxStage + kDxEpi + (3 * 512 + 1024) * 4 + 24 * 8 + 16;
 
 template <int kQ>
 __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_constant__ CUtensorMap tmB,
@@ -618,17 +619,21 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                                                                   const __grid_constant__ CUtensorMap tmDy,
                                                                   const __grid_constant__ CUtensorMap tmZ,
                                                                   const __grid_constant__ CUtensorMap tmG,
+                                                                  const __grid_constant__ CUtensorMap tmDyE,
+                                                                  const __grid_constant__ CUtensorMap tmXE,
                                                                   const SsdBwdParams p) {
     extern __shared__ uint8_t s_dyn[];
     uint8_t* stages = s_dyn + ((1024u - (msc::smem_u32(s_dyn) & 1023u)) & 1023u);
-    float* s_rows = reinterpret_cast<float*>(stages + kDxStages * kDxStage);  // [3][cs 256 | Delta 256]
+    uint8_t* s_epi = stages + kDxStages * kDxStage;                            // dy | x tiles of the head
+    float* s_rows = reinterpret_cast<float*>(s_epi + kDxEpi);                  // [3][cs 256 | Delta 256]
     float* s_part = s_rows + 3 * 512;                                          // [dw, v][4 quarters][128 rows]
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_part + 1024);
     // 0-1 stage loaded (TMA), 2-3 stage built (16 warps), 4-5 stage free (MMA), 6-8 rows loaded,
-    // 9-11 rows free (16 warps), 12-13 accumulators ready, 14-15 accumulators free (16 warps), 16 drain
+    // 9-11 rows free (16 warps), 12-13 accumulators ready, 14-15 accumulators free (16 warps), 16 drain,
+    // 17 epilogue tiles loaded, 18 epilogue tiles read (16 warps)
     uint64_t *tfull = bars, *full = bars + 2, *empty = bars + 4, *rfull = bars + 6, *rfree = bars + 9,
-             *afull = bars + 12, *afree = bars + 14, *drain = bars + 16;
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 17);
+             *afull = bars + 12, *afree = bars + 14, *drain = bars + 16, *efull = bars + 17, *efree = bars + 18;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 19);
     volatile uint32_t* abort = slot + 1;
 
     constexpr int Q = kQ;
@@ -664,6 +669,8 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
             msc::mbar_init(&afree[k], kDxOpWarps);
         }
         msc::mbar_init(drain, 1);
+        msc::mbar_init(efull, 1);
+        msc::mbar_init(efree, kDxOpWarps);
         slot[1] = 0u;
         msc::fence_barrier_init();
     }
@@ -680,7 +687,11 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
             msc::prefetch_tmap(&tmDy);
             msc::prefetch_tmap(&tmG);
             if (has_z) msc::prefetch_tmap(&tmZ);
-            int issued = 0, rissued = 0;
+            else {
+                msc::prefetch_tmap(&tmDyE);
+                msc::prefetch_tmap(&tmXE);
+            }
+            int issued = 0, rissued = 0, eissued = 0;
             bool ok = true;
             for (int hh = 0; hh < nh && ok; ++hh) {
                 const int h = hb * kDxHB + hh, g = h / p.hpg;
@@ -719,6 +730,19 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                     }
                     ++issued;
                 }
+                if (!ok) break;
+                // the epilogue's dy and x rows of this head (one buffer: after the
+                // previous head's epilogue has read it)
+                if (!has_z) {
+                    if (hh >= 1 && !msc::wait_bounded(efree, (uint32_t)((hh - 1) & 1), abort, kSleepNs)) {
+                        ok = false;
+                        break;
+                    }
+                    msc::mbar_arrive_expect_tx(efull, kDxEpi);
+                    msc::tma_load_3d(s_epi, &tmDyE, efull, h * kP, (int)(tc0 + j0), b);
+                    msc::tma_load_3d(s_epi + 16384, &tmXE, efull, h * kP, (int)(tc0 + j0), b);
+                    ++eissued;
+                }
             }
             if (!ok) {
                 record_timeout(101);
@@ -731,6 +755,8 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
             for (int rb = 0; rb < 3 && rb < rissued; ++rb)
                 if (!msc::wait_bounded(&rfull[rb], (uint32_t)(((rissued - 1 - rb) / 3) & 1), nullptr, kSleepNs))
                     record_timeout(102);
+            if (eissued > 0 && !msc::wait_bounded(efull, (uint32_t)((eissued - 1) & 1), nullptr, kSleepNs))
+                record_timeout(102);
         }
         __syncwarp();
     } else if (warp == kDxWarpMma) {
@@ -874,6 +900,7 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
             msc::tc_fence_before();
             __syncwarp();
             if (lane == 0) msc::mbar_arrive(&afree[ab]);  // the next head but one may write this buffer
+            if (!has_z) ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(efull, (uint32_t)(hh & 1), abort, kSleepNs));
             if (valid) {
                 const size_t o = (((size_t)b * p.L + t) * p.H + h) * kP + 16 * cq;
                 const float dtj = s_dt[j];
@@ -883,8 +910,15 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                 const float Dh = p.D ? p.D[h] : 0.f;
 #pragma unroll
                 for (int q8 = 0; q8 < 2; ++q8) {
-                    const uint4 dv = *reinterpret_cast<const uint4*>(p.dy + o + 8 * q8);
-                    const uint4 xv = *reinterpret_cast<const uint4*>(p.x + o + 8 * q8);
+                    uint4 dv, xv;
+                    if (has_z) {
+                        dv = *reinterpret_cast<const uint4*>(p.dy + o + 8 * q8);
+                        xv = *reinterpret_cast<const uint4*>(p.x + o + 8 * q8);
+                    } else {
+                        const uint32_t eo = msc::sw128_offset(row, 16 * cq + 8 * q8, 128);
+                        dv = *reinterpret_cast<const uint4*>(s_epi + eo);
+                        xv = *reinterpret_cast<const uint4*>(s_epi + 16384 + eo);
+                    }
                     uint4 zv = make_uint4(0u, 0u, 0u, 0u);
                     if (has_z) zv = *reinterpret_cast<const uint4*>(p.z + o + 8 * q8);
                     const uint32_t dwd[4] = {dv.x, dv.y, dv.z, dv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -918,6 +952,10 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                     msc::st_cs_v8(p.dx + o + 8 * q8, out);
                     if (has_z) msc::st_cs_v8(p.dz + o + 8 * q8, dzo);
                 }
+            }
+            if (!has_z) {
+                __syncwarp();
+                if (lane == 0) msc::mbar_arrive(efree);   // the next head's tiles may land
             }
             s_part[128 * cq + row] = dw;
             s_part[512 + 128 * cq + row] = v;
@@ -1355,11 +1393,11 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
     {
         const dim3 gdx(nc * nmb, (H + kDxHB - 1) / kDxHB, B);
         if (f.Q == 64)
-            ssd_dx_tc_kernel<64><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, p);
+            ssd_dx_tc_kernel<64><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, mDy128, mX128, p);
         else if (f.Q == 128)
-            ssd_dx_tc_kernel<128><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, p);
+            ssd_dx_tc_kernel<128><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, mDy128, mX128, p);
         else
-            ssd_dx_tc_kernel<256><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, p);
+            ssd_dx_tc_kernel<256><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, mDy128, mX128, p);
         if ((s = check_launch("ssd_dx_tc")) != MSC_OK) return s;
         const unsigned nhb = (unsigned)((p.hpg + kHBlk - 1) / kHBlk);
         ssd_dbcs_tc_kernel<<<dim3(nc * nmb, (unsigned)f.G * nhb, B), kSbThreads, kSbSmem, st>>>(mX128, mDy128, mZ128, p);
