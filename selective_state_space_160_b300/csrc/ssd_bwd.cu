@@ -467,6 +467,37 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
 #pragma unroll
                         for (int e = 0; e < 16; ++e) r[e] = 0.f;
                     }
+                    // warp-uniform: every row of the warp lies below every column of the
+                    // chunk (no mask, no diagonal element): two columns per packed op
+                    const bool dense = (!diag_tile || c0 + 15 < 32 * lq) && rv == 128;
+                    if (dense) {
+                        const uint64_t csi2 = msc::pk2(csi, csi);
+                        uint64_t rowt2 = 0ull;
+#pragma unroll
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            const ulonglong2 cj4 = *reinterpret_cast<const ulonglong2*>(cjp + c0 + 4 * e4);
+                            const ulonglong2 dj4 = *reinterpret_cast<const ulonglong2*>(djp + c0 + 4 * e4);
+                            const ulonglong2 g4 = *reinterpret_cast<const ulonglong2*>(gp + c0 + 4 * e4);
+#pragma unroll
+                            for (int tp = 0; tp < 2; ++tp) {
+                                const int e = 4 * e4 + 2 * tp, k = 16 * q + e;
+                                const uint64_t cj2 = tp ? cj4.y : cj4.x, dj2 = tp ? dj4.y : dj4.x;
+                                const uint64_t g2 = tp ? g4.y : g4.x;
+                                // the difference first (exact), then the scale
+                                const uint64_t diff2 = msc::fma2(cj2, msc::pk2(-1.f, -1.f), csi2);
+                                const uint64_t e2 = msc::ex2_2(msc::mul2(diff2, msc::pk2(MSC_LOG2E, MSC_LOG2E)));
+                                const uint64_t er2 = msc::mul2(e2, msc::pk2(r[e], r[e + 1]));
+                                uint64_t dg2 = msc::fma2(er2, dj2, msc::pk2(dgacc[k], dgacc[k + 1]));
+                                msc::upk2(dg2, dgacc[k], dgacc[k + 1]);
+                                const uint64_t p12 = msc::mul2(er2, g2);
+                                rowt2 = msc::fma2(p12, dj2, rowt2);
+                                msc::upk2(p12, col[e], col[e + 1]);
+                            }
+                        }
+                        float ra, rb;
+                        msc::upk2(rowt2, ra, rb);
+                        rowt += ra + rb;
+                    } else {
 #pragma unroll
                     for (int e4 = 0; e4 < 4; ++e4) {
                         const float4 cj4 = *reinterpret_cast<const float4*>(cjp + c0 + 4 * e4);
@@ -488,6 +519,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
                             col[e] = dg_ ? 0.f : p1;
                             pdiag = dg_ ? p1 : pdiag;
                         }
+                    }
                     }
                     cs_ = warp_colsum16(col, lane);
                 }
