@@ -73,6 +73,7 @@ struct SsdParams {
     float* cs;              // [b, H, Lp]
     float* S;               // [b, nc, H, P, N]
     uint16_t* Hin;          // [b, nc, H] pairs (hi, lo) of 64 x 128 bf16 K-major SW128 tile images
+    float* Hin32;           // [b, nc, H, P, N] fp32 copy of the same states, or null
     int64_t L, Lp;
     int batch, H, G, hpg, Q, nc;
 };
@@ -288,7 +289,8 @@ __global__ void __launch_bounds__(256) ssd_state_kernel(const __grid_constant__ 
 }
 
 // ------------------------------------------------------------ (3) state pass
-// One thread per (b, h, p, 8 consecutive n): Hin of every chunk as bf16 hi + lo
+// One thread per (b, h, p, 8 consecutive n): Hin of every chunk (also in fp32
+// when Hin32 is set, for the backward) as bf16 hi + lo
 // tile images (K-major [64 p][128 n], 128-byte swizzle: one 16-byte chunk per
 // thread and chunk) for the scan kernel's tensor cores, and the final state.
 // The chunk states are loaded eight chunks ahead of the dependent chain.
@@ -327,6 +329,11 @@ __global__ void __launch_bounds__(256) ssd_pass_kernel(const SsdParams p) {
             const int c = c0 + k;
             if (c >= p.nc) break;
             uint8_t* tile = reinterpret_cast<uint8_t*>(p.Hin + (((size_t)b * p.nc + c) * p.H + h) * (2 * kP * kN));
+            if (p.Hin32) {
+                float4* dst = reinterpret_cast<float4*>(p.Hin32 + ((((size_t)b * p.nc + c) * p.H + h) * kP + pp) * kN + n0);
+                dst[0] = make_float4(run[0], run[1], run[2], run[3]);
+                dst[1] = make_float4(run[4], run[5], run[6], run[7]);
+            }
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) split_bf16x2(run[2 * e], run[2 * e + 1], hi[e], lo[e]);
@@ -343,34 +350,6 @@ __global__ void __launch_bounds__(256) ssd_pass_kernel(const SsdParams p) {
         float4* dst = reinterpret_cast<float4*>(p.final_state + (((size_t)b * p.H + h) * kP + pp) * kN + n0);
         dst[0] = make_float4(run[0], run[1], run[2], run[3]);
         dst[1] = make_float4(run[4], run[5], run[6], run[7]);
-    }
-}
-
-// fp32 variant of the state pass for the backward: Hin32[b, c, h, p, n], the
-// state entering every chunk, one thread per (b, h, p, 8 consecutive n).
-__global__ void __launch_bounds__(256) ssd_pass32_kernel(const SsdParams p, float* Hin32) {
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int b = blockIdx.y;
-    constexpr int kN8 = kN / 8;
-    if (idx >= (int64_t)p.H * kP * kN8) return;
-    const int n0 = (int)(idx % kN8) * 8;
-    const int pp = (int)((idx / kN8) % kP);
-    const int h = (int)(idx / (kN8 * kP));
-    const size_t dbase = ((size_t)b * p.H + h) * p.Lp;
-    float run[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) run[e] = 0.f;
-    for (int c = 0; c < p.nc; ++c) {
-        const size_t o = ((((size_t)b * p.nc + c) * p.H + h) * kP + pp) * kN + n0;
-        float4* dst = reinterpret_cast<float4*>(Hin32 + o);
-        dst[0] = make_float4(run[0], run[1], run[2], run[3]);
-        dst[1] = make_float4(run[4], run[5], run[6], run[7]);
-        const float4* src = reinterpret_cast<const float4*>(p.S + o);
-        const float4 s0 = src[0], s1 = src[1];
-        const float a = msc::ex2_approx(p.cs[dbase + (size_t)c * p.Q + p.Q - 1] * MSC_LOG2E);
-        const float s8[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) run[e] = fmaf(a, run[e], s8[e]);
     }
 }
 
@@ -852,10 +831,10 @@ msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* H
             mB, mX, mX, p);
         if ((s = check_launch("ssd_state")) != MSC_OK) return s;
     }
+    // one pass writes the states entering every chunk in fp32 and as the images
     const int64_t per_b = (int64_t)p.H * kP * kN;
-    ssd_pass32_kernel<<<dim3((unsigned)((per_b / 8 + 255) / 256), (unsigned)a.batch), 256, 0, st>>>(p, Hin32);
-    if ((s = check_launch("ssd_pass32")) != MSC_OK) return s;
     p.Hin = Himg;
+    p.Hin32 = Hin32;
     p.final_state = nullptr;
     ssd_pass_kernel<<<dim3((unsigned)((per_b / 8 + 255) / 256), (unsigned)a.batch), 256, 0, st>>>(p);
     return check_launch("ssd_pass");
