@@ -17,7 +17,7 @@
 // entering every 8-step group (1/8 of the states, fp32) to the workspace.
 // (2) This kernel walks each row backwards: TMA streams the tiles of u, delta,
 // z, dy, B, C in reverse order into a two-stage ring; for each 8-step group it
-// reloads the checkpoint, recomputes the 8 steps forward keeping abar and
+// takes the checkpoint (loaded one group ahead), recomputes the 8 steps forward keeping abar and
 // h_{t-1} in registers, then runs the adjoint backwards through them.  Four
 // lanes share a row (4 states each) so the two 8-step histories fit in
 // registers.  dB and dC, sums over all channels of a batch entry, are first
@@ -198,6 +198,12 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
         for (int c = 0; c < kStages && c < ntiles; ++c) issue(c);
     int issued = ntiles < kStages ? ntiles : kStages;
 
+    // groups are walked last to first (p.L is a multiple of 8): the checkpoint of
+    // the next group is loaded one group ahead of its use
+    const float* ck = p.ckpt + (size_t)row * p.ckpt_groups * 16 + 4 * j;
+    float4 hv_next = row_ok ? __ldg(reinterpret_cast<const float4*>(ck + (size_t)((p.L - 8) >> 3) * 16))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+
     bool failed = false;
     int c = 0;
     for (; c < ntiles; ++c) {
@@ -274,9 +280,8 @@ __global__ void __launch_bounds__(kThreads) s6_bwd_kernel(const __grid_constant_
             // ---- recompute the group forward from its checkpoint
             uint64_t h[2];
             {
-                const float4 hv = row_ok ? __ldg(reinterpret_cast<const float4*>(
-                                               p.ckpt + ((size_t)row * p.ckpt_groups + (size_t)(tg >> 3)) * 16 + 4 * j))
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 hv = hv_next;
+                if (row_ok && tg >= 8) hv_next = __ldg(reinterpret_cast<const float4*>(ck + (size_t)((tg - 8) >> 3) * 16));
                 h[0] = msc::pk2(hv.x, hv.y);
                 h[1] = msc::pk2(hv.z, hv.w);
             }
