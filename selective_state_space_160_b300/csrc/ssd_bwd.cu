@@ -645,7 +645,7 @@ constexpr int kDxHB = 8;                       // heads per CTA
 constexpr uint32_t kDxEpi = 32768;             // the epilogue's dy and x tiles [128 j][64 p] (no gate)
 constexpr size_t kDxSmem = 1024 + kDxStages * kDxStage + kDxEpi + (3 * 512 + 1024) * 4 + 24 * 8 + 16;
 
-template <int kQ>
+template <int kQ, bool kZ>
 __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_constant__ CUtensorMap tmB,
                                                                   const __grid_constant__ CUtensorMap tmC,
                                                                   const __grid_constant__ CUtensorMap tmDy,
@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
     const int ns = na + 4;                       // slabs per head
     const int nh = min(kDxHB, p.H - hb * kDxHB);
     const int64_t tc0 = (int64_t)c * Q;
-    const bool has_z = p.z != nullptr;
+    constexpr bool has_z = kZ;  // a gate: g = dy silu(z), dz
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (warp == 0) {
@@ -917,6 +917,7 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
             const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
             const float* s_cs = s_rows + 512 * rb;
             const float* s_dt = s_cs + 256;
+            const float Dh = p.D ? __ldg(p.D + h) : 0.f;  // issued before the waits
             ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&afull[ab], (uint32_t)((hh >> 1) & 1), abort, kSleepNs));
             msc::tc_fence_after();
             const bool valid = ok && row < rows_valid && t < p.L;
@@ -939,7 +940,6 @@ __global__ void __launch_bounds__(kDxThreads, 1) ssd_dx_tc_kernel(const __grid_c
                 ej = msc::ex2_approx((s_cs[Q - 1] - s_cs[j]) * MSC_LOG2E);
                 wj = ej * dtj;
                 ecs = msc::ex2_approx(s_cs[j] * MSC_LOG2E);
-                const float Dh = p.D ? p.D[h] : 0.f;
 #pragma unroll
                 for (int q8 = 0; q8 < 2; ++q8) {
                     uint4 dv, xv;
@@ -1390,11 +1390,11 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
             return MSC_ERR_CUDA;
         static bool configured = false;
         if (!configured) {
-            cudaError_t e2 = cudaFuncSetAttribute(ssd_dx_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmem);
-            if (e2 == cudaSuccess)
-                e2 = cudaFuncSetAttribute(ssd_dx_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmem);
-            if (e2 == cudaSuccess)
-                e2 = cudaFuncSetAttribute(ssd_dx_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmem);
+            cudaError_t e2 = cudaSuccess;
+            for (const void* k : {(const void*)ssd_dx_tc_kernel<64, false>, (const void*)ssd_dx_tc_kernel<64, true>,
+                                  (const void*)ssd_dx_tc_kernel<128, false>, (const void*)ssd_dx_tc_kernel<128, true>,
+                                  (const void*)ssd_dx_tc_kernel<256, false>, (const void*)ssd_dx_tc_kernel<256, true>})
+                if (e2 == cudaSuccess) e2 = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDxSmem);
             if (e2 == cudaSuccess)
                 e2 = cudaFuncSetAttribute(ssd_dbcs_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSbSmem);
             if (e2 == cudaSuccess)
@@ -1424,12 +1424,14 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
     if ((s = check_launch("ssd_dbc")) != MSC_OK) return s;
     {
         const dim3 gdx(nc * nmb, (H + kDxHB - 1) / kDxHB, B);
+        auto dx = [&](auto kern) { kern<<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, mDy128, mX128, p); };
+        const bool z = f.z != nullptr;
         if (f.Q == 64)
-            ssd_dx_tc_kernel<64><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, mDy128, mX128, p);
+            z ? dx(ssd_dx_tc_kernel<64, true>) : dx(ssd_dx_tc_kernel<64, false>);
         else if (f.Q == 128)
-            ssd_dx_tc_kernel<128><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, mDy128, mX128, p);
+            z ? dx(ssd_dx_tc_kernel<128, true>) : dx(ssd_dx_tc_kernel<128, false>);
         else
-            ssd_dx_tc_kernel<256><<<gdx, kDxThreads, kDxSmem, st>>>(mB, mC, mDy, mZ, mG, mDy128, mX128, p);
+            z ? dx(ssd_dx_tc_kernel<256, true>) : dx(ssd_dx_tc_kernel<256, false>);
         if ((s = check_launch("ssd_dx_tc")) != MSC_OK) return s;
         const unsigned nhb = (unsigned)((p.hpg + kHBlk - 1) / kHBlk);
         ssd_dbcs_tc_kernel<<<dim3(nc * nmb, (unsigned)f.G * nhb, B), kSbThreads, kSbSmem, st>>>(mX128, mDy128, mZ128, p);
