@@ -80,8 +80,21 @@ struct SsdBwdParams {
 
 __device__ __forceinline__ float bfv(uint16_t v) { return __uint_as_float(((uint32_t)v) << 16); }
 
-__device__ __forceinline__ float bval(const uint16_t* M, const SsdBwdParams& p, int b, int64_t t, int g, int n) {
-    return t < p.L ? bfv(M[(((size_t)b * p.L + t) * p.Gr + g) * kN + n]) : 0.f;
+// B or C of step t, group g, states n0 .. n0 + 7 (n0 a multiple of 8): one 16-byte load
+__device__ __forceinline__ void bval8(const uint16_t* M, const SsdBwdParams& p, int b, int64_t t, int g, int n0,
+                                      float* v) {
+    if (t >= p.L) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+        return;
+    }
+    const uint4 w = *reinterpret_cast<const uint4*>(M + (((size_t)b * p.L + t) * p.Gr + g) * kN + n0);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        v[2 * e] = msc::bf16lo(ww[e]);
+        v[2 * e + 1] = msc::bf16hi(ww[e]);
+    }
 }
 
 // vector reduction into global memory (16-byte aligned)
@@ -132,10 +145,17 @@ __global__ void __launch_bounds__(256) ssd_gmat_kernel(const SsdBwdParams p) {
     float acc[4][4];
     zero_acc(acc);
     for (int k0 = 0; k0 < kN; k0 += kKS) {
-        for (int e = tid; e < kT * kKS; e += 256) {
-            const int r = e / kKS, k = e % kKS;
-            As[r][k] = bval(p.C, p, b, t0 + ib * kT + r, g, k0 + k);
-            Bs[k][r] = bval(p.B, p, b, t0 + jb * kT + r, g, k0 + k);
+        {
+            // 64 rows x 4 chunks of 8 states: one chunk of C and one of B per thread
+            const int r = tid >> 2, ch = tid & 3;
+            float vc[8], vb[8];
+            bval8(p.C, p, b, t0 + ib * kT + r, g, k0 + 8 * ch, vc);
+            bval8(p.B, p, b, t0 + jb * kT + r, g, k0 + 8 * ch, vb);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                As[r][8 * ch + e] = vc[e];
+                Bs[8 * ch + e][r] = vb[e];
+            }
         }
         __syncthreads();
         tile_fma<4>(&As[0][0], kKS + 1, &Bs[0][0], kT + 4, kKS, acc, tid);
@@ -595,9 +615,13 @@ __global__ void __launch_bounds__(256) ssd_dbc_kernel(const SsdBwdParams p) {
                 As[k][r] = dGt[(size_t)(ob * kT + r) * p.Q + kb * kT + k];
         }
         for (int k0 = 0; k0 < kT; k0 += kKS) {
-            for (int e = tid; e < kKS * kN; e += 256) {
-                const int k = e / kN, n = e % kN;
-                Bs[k][n] = bval(side ? p.C : p.B, p, b, t0 + ob * kT + k0 + k, g, n);
+#pragma unroll
+            for (int e = tid; e < kKS * kN / 8; e += 256) {  // 32 rows x 16 chunks of 8 states
+                const int k = e >> 4, ch = e & 15;
+                float v[8];
+                bval8(side ? p.C : p.B, p, b, t0 + ob * kT + k0 + k, g, 8 * ch, v);
+                *reinterpret_cast<float4*>(&Bs[k][8 * ch]) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(&Bs[k][8 * ch + 4]) = make_float4(v[4], v[5], v[6], v[7]);
             }
             __syncthreads();
             tile_fma<8>(&As[0][k0], kT + 1, &Bs[0][0], kN + 4, kKS, acc, tid);
