@@ -255,7 +255,7 @@ constexpr int kDgOpWarps = 8;
 constexpr int kDgWarpLoad = kDgOpWarps, kDgWarpMma = kDgOpWarps + 1;
 constexpr int kDgThreads = (kDgOpWarps + 2) * 32;
 constexpr int kDgGld = 132;                    // row stride (floats) of the G tile: 16-byte rows
-constexpr size_t kDgSmem = 1024 + kDgStages * kDgStage + (3 * 128 * 3 + 2 * 4 * 64 + 2 * 128 + 128 * kDgGld) * 4 + 20 * 8 + 16;
+constexpr size_t kDgSmem = 1024 + kDgStages * kDgStage + (3 * 128 * 3 + 2 * (2 * 4 * 64 + 2 * 128) + 128 * kDgGld) * 4 + 20 * 8 + 16;
 
 // v[0..15] of every lane -> sum over the warp's 32 lanes of v[lane >> 1]
 __device__ __forceinline__ float warp_colsum16(float (&v)[16], int lane) {
@@ -300,9 +300,11 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
     float* s_ci = reinterpret_cast<float*>(stages + kDgStages * kDgStage);  // [3][128]
     float* s_cj = s_ci + 384;                                              // [3][128]
     float* s_dj = s_cj + 384;                                              // [3][128]
-    float* s_col = s_dj + 384;                                             // [2 halves][4 quarters][64]
-    float* s_row = s_col + 512;                                            // [2 halves][128]
-    float* s_G = s_row + 256;                                              // [128 i][kDgGld] G of the tile
+    // column and row sums exchanged between warps, by head parity (a buffer is
+    // rewritten two heads later, after every warp has passed the barrier between)
+    float* s_col = s_dj + 384;                                             // [2][2 halves][4 quarters][64]
+    float* s_row = s_col + 1024;                                           // [2][2 halves][128]
+    float* s_G = s_row + 512;                                              // [128 i][kDgGld] G of the tile
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_G + 128 * kDgGld);
     // 0-2 stage loaded, 3-5 stage built, 6-8 stage free, 9-10 R ready, 11-12 R read, 13 drain,
     // 14-16 the head's cs / Delta rows read
@@ -427,6 +429,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             const int ir = 128 * ib + r;
             s_G[r * kDgGld + jj] = (r < rv && jj < rv && ir >= 128 * jb + jj) ? Gt[(size_t)ir * Q + 128 * jb + jj] : 0.f;
         }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
         bool ok = true;
         auto produce = [&](int hh) {
             const int st = hh % kDgStages, use = hh / kDgStages;
@@ -458,7 +461,8 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             const int buf = hh & 1, cb = hh % 3;
             const int h = g * p.hpg + hh0 + hh;
             const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
-            asm volatile("bar.sync 1, 256;" ::: "memory");
+            float* s_colh = s_col + 512 * buf;
+            float* s_rowh = s_row + 256 * buf;
             ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&rfull[buf], (uint32_t)((hh >> 1) & 1), abort, kSleepNs) &&
                                                    msc::wait_bounded(&tfull[cb], (uint32_t)((hh / 3) & 1), abort, kSleepNs));
             msc::tc_fence_after();
@@ -543,25 +547,25 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
                     }
                     cs_ = warp_colsum16(col, lane);
                 }
-                if ((lane & 1) == 0) s_col[256 * half + 64 * lq + 16 * q + (lane >> 1)] = cs_;
+                if ((lane & 1) == 0) s_colh[256 * half + 64 * lq + 16 * q + (lane >> 1)] = cs_;
             }
             msc::tc_fence_before();
             __syncwarp();
             if (lane == 0) msc::mbar_arrive(&rfree[buf]);
             if (pdiag != 0.f) atomicAdd(p.dDelta + dbase + il, pdiag);
-            s_row[128 * half + row] = rowt;
+            s_rowh[128 * half + row] = rowt;
             asm volatile("bar.sync 1, 256;" ::: "memory");
             if (tid < 128) {
                 const int jj = tid, hf = jj >> 6, k = jj & 63;
-                const float cd = s_col[256 * hf + k] + s_col[256 * hf + 64 + k] + s_col[256 * hf + 128 + k] +
-                                 s_col[256 * hf + 192 + k];
+                const float cd = s_colh[256 * hf + k] + s_colh[256 * hf + 64 + k] + s_colh[256 * hf + 128 + k] +
+                                 s_colh[256 * hf + 192 + k];
                 if (jj < rv && cd != 0.f) {
                     atomicAdd(p.dDelta + dbase + 128 * jb + jj, cd);
                     atomicAdd(p.dcs + dbase + 128 * jb + jj, -djp[jj] * cd);
                 }
             } else {
                 const int r2 = tid - 128;
-                const float rt = s_row[r2] + s_row[128 + r2];
+                const float rt = s_rowh[r2] + s_rowh[128 + r2];
                 if (r2 < rv && rt != 0.f) atomicAdd(p.dcs + dbase + 128 * ib + r2, rt);
             }
             __syncwarp();
