@@ -245,17 +245,17 @@ __global__ void __launch_bounds__(256) ssd_rpass_kernel(const SsdBwdParams p) {
 // of two tensor-memory buffers; the CUDA cores then take, per element with i >= j,
 //   er = E_ij R_ij,  dG_ij += er Delta_j,  p1 = er G_ij,
 //   dcs_i += sum_j Delta_j p1,  dDelta_j += sum_i p1,  dcs_j -= Delta_j sum_i p1,
-// with the dG accumulators in registers (thread = row i, 64 columns j) and G in
-// shared memory, while the MMAs of the next head run.  Column sums: a butterfly
+// with the dG accumulators in registers (thread = row i, 32 columns j; 16
+// warps) and G in shared memory, while the MMAs of the next head run.  Column sums: a butterfly
 // over the 32 lanes of a warp, then the four row quarters through shared memory.
 // The head blocks of a tile add their dG with vector reductions (dG starts at 0).
 constexpr int kDgStages = 3;
 constexpr uint32_t kDgStage = 49152;           // A hi [128][64] | A lo (z) | B = x [128][64]
-constexpr int kDgOpWarps = 8;
+constexpr int kDgOpWarps = 16;
 constexpr int kDgWarpLoad = kDgOpWarps, kDgWarpMma = kDgOpWarps + 1;
 constexpr int kDgThreads = (kDgOpWarps + 2) * 32;
 constexpr int kDgGld = 132;                    // row stride (floats) of the G tile: 16-byte rows
-constexpr size_t kDgSmem = 1024 + kDgStages * kDgStage + (3 * 128 * 3 + 2 * (2 * 4 * 64 + 2 * 128) + 128 * kDgGld) * 4 + 20 * 8 + 16;
+constexpr size_t kDgSmem = 1024 + kDgStages * kDgStage + (3 * 128 * 3 + 2 * (4 * 4 * 32 + 4 * 128) + 128 * kDgGld) * 4 + 20 * 8 + 16;
 
 // v[0..15] of every lane -> sum over the warp's 32 lanes of v[lane >> 1]
 __device__ __forceinline__ float warp_colsum16(float (&v)[16], int lane) {
@@ -302,9 +302,9 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
     float* s_dj = s_cj + 384;                                              // [3][128]
     // column and row sums exchanged between warps, by head parity (a buffer is
     // rewritten two heads later, after every warp has passed the barrier between)
-    float* s_col = s_dj + 384;                                             // [2][2 halves][4 quarters][64]
-    float* s_row = s_col + 1024;                                           // [2][2 halves][128]
-    float* s_G = s_row + 512;                                              // [128 i][kDgGld] G of the tile
+    float* s_col = s_dj + 384;                                             // [2][4 col quarters][4 row quarters][32]
+    float* s_row = s_col + 1024;                                           // [2][4 col quarters][128]
+    float* s_G = s_row + 1024;                                             // [128 i][kDgGld] G of the tile
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_G + 128 * kDgGld);
     // 0-2 stage loaded, 3-5 stage built, 6-8 stage free, 9-10 R ready, 11-12 R read, 13 drain,
     // 14-16 the head's cs / Delta rows read
@@ -414,22 +414,22 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
         }
         __syncwarp();
     } else {
-        const int lq = warp & 3, half = warp >> 2;
+        const int lq = warp & 3, cq = warp >> 2;     // row quarter (TMEM lanes), column quarter
         const int row = 32 * lq + lane;              // i within the tile
         const int il = 128 * ib + row;               // i within the chunk
         const bool row_ok = row < rv;
         const float* Gt = p.Gm + (((size_t)b * p.nc + c) * p.Gr + g) * (size_t)Q * Q;
-        float dgacc[64];
+        float dgacc[32];
 #pragma unroll
-        for (int k = 0; k < 64; ++k) dgacc[k] = 0.f;
+        for (int k = 0; k < 32; ++k) dgacc[k] = 0.f;
         // G of the tile (entries above the diagonal are never used: set to 0)
 #pragma unroll 4
-        for (int e = tid; e < 128 * 128; e += 256) {
+        for (int e = tid; e < 128 * 128; e += 32 * kDgOpWarps) {
             const int r = e >> 7, jj = e & 127;
             const int ir = 128 * ib + r;
             s_G[r * kDgGld + jj] = (r < rv && jj < rv && ir >= 128 * jb + jj) ? Gt[(size_t)ir * Q + 128 * jb + jj] : 0.f;
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        asm volatile("bar.sync 1, 512;" ::: "memory");
         bool ok = true;
         auto produce = [&](int hh) {
             const int st = hh % kDgStages, use = hh / kDgStages;
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
                 if (ok) {
                     uint8_t* sg = stages + st * kDgStage;
 #pragma unroll 1
-                    for (int u = tid; u < 1024; u += 256) {
+                    for (int u = tid; u < 1024; u += 32 * kDgOpWarps) {
                         uint4* ph = reinterpret_cast<uint4*>(sg + 16 * u);
                         uint4* pl = reinterpret_cast<uint4*>(sg + 16384 + 16 * u);
                         const uint4 dv = *ph, zv = *pl;
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             const int h = g * p.hpg + hh0 + hh;
             const size_t dbase = ((size_t)b * p.H + h) * p.Lp + (size_t)tc0;
             float* s_colh = s_col + 512 * buf;
-            float* s_rowh = s_row + 256 * buf;
+            float* s_rowh = s_row + 512 * buf;
             ok = ok && __all_sync(0xffffffffu, msc::wait_bounded(&rfull[buf], (uint32_t)((hh >> 1) & 1), abort, kSleepNs) &&
                                                    msc::wait_bounded(&tfull[cb], (uint32_t)((hh / 3) & 1), abort, kSleepNs));
             msc::tc_fence_after();
@@ -476,8 +476,8 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             const float* djp = s_dj + 128 * cb;
             const float* gp = s_G + row * kDgGld;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int c0 = 64 * half + 16 * q;
+            for (int q = 0; q < 2; ++q) {
+                const int c0 = 32 * cq + 16 * q;
                 // warp-uniform: every element of the chunk lies above the diagonal or
                 // outside a short chunk
                 const bool skip = (diag_tile && c0 > 32 * lq + 31) || c0 >= rv || 32 * lq >= rv;
@@ -547,25 +547,25 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
                     }
                     cs_ = warp_colsum16(col, lane);
                 }
-                if ((lane & 1) == 0) s_colh[256 * half + 64 * lq + 16 * q + (lane >> 1)] = cs_;
+                if ((lane & 1) == 0) s_colh[128 * cq + 32 * lq + 16 * q + (lane >> 1)] = cs_;
             }
             msc::tc_fence_before();
             __syncwarp();
             if (lane == 0) msc::mbar_arrive(&rfree[buf]);
             if (pdiag != 0.f) atomicAdd(p.dDelta + dbase + il, pdiag);
-            s_rowh[128 * half + row] = rowt;
-            asm volatile("bar.sync 1, 256;" ::: "memory");
+            s_rowh[128 * cq + row] = rowt;
+            asm volatile("bar.sync 1, 512;" ::: "memory");
             if (tid < 128) {
-                const int jj = tid, hf = jj >> 6, k = jj & 63;
-                const float cd = s_colh[256 * hf + k] + s_colh[256 * hf + 64 + k] + s_colh[256 * hf + 128 + k] +
-                                 s_colh[256 * hf + 192 + k];
+                const int jj = tid, cf = jj >> 5, k = jj & 31;
+                const float cd = s_colh[128 * cf + k] + s_colh[128 * cf + 32 + k] + s_colh[128 * cf + 64 + k] +
+                                 s_colh[128 * cf + 96 + k];
                 if (jj < rv && cd != 0.f) {
                     atomicAdd(p.dDelta + dbase + 128 * jb + jj, cd);
                     atomicAdd(p.dcs + dbase + 128 * jb + jj, -djp[jj] * cd);
                 }
-            } else {
+            } else if (tid < 256) {
                 const int r2 = tid - 128;
-                const float rt = s_rowh[r2] + s_rowh[128 + r2];
+                const float rt = s_rowh[r2] + s_rowh[128 + r2] + s_rowh[256 + r2] + s_rowh[384 + r2];
                 if (r2 < rv && rt != 0.f) atomicAdd(p.dcs + dbase + 128 * ib + r2, rt);
             }
             __syncwarp();
@@ -579,10 +579,10 @@ __global__ void __launch_bounds__(kDgThreads, 1) ssd_dg_tc_kernel(const __grid_c
             if (lane == 0) record_timeout(125);
             *abort = 1u;
         }
-        if (row_ok && 64 * half < rv) {
-            float* dst = p.dG + (((size_t)b * p.nc + c) * p.Gr + g) * (size_t)Q * Q + (size_t)il * Q + 128 * jb + 64 * half;
+        if (row_ok && 32 * cq < rv) {
+            float* dst = p.dG + (((size_t)b * p.nc + c) * p.Gr + g) * (size_t)Q * Q + (size_t)il * Q + 128 * jb + 32 * cq;
 #pragma unroll
-            for (int k = 0; k < 64; k += 4) red_add_v4(dst + k, dgacc[k], dgacc[k + 1], dgacc[k + 2], dgacc[k + 3]);
+            for (int k = 0; k < 32; k += 4) red_add_v4(dst + k, dgacc[k], dgacc[k + 1], dgacc[k + 2], dgacc[k + 3]);
         }
         msc::tc_fence_before();
     }
