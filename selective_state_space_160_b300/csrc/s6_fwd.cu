@@ -937,6 +937,9 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
     const bool vec = (a.L % 8) == 0;
     FwdMaps maps;
     const FwdMaps* mp = nullptr;
+    // MSC_S6_FWD_PLAIN (any value) sends rows that TMA could take to the
+    // plain-load kernel as well, so that the two paths can be compared on the
+    // same inputs; it changes which kernel runs, not what it computes.
     if (tma_ok(p, a.bf16) && std::getenv("MSC_S6_FWD_PLAIN") == nullptr) {
         if (!make_maps(maps, p, a.batch, a.bf16)) return MSC_ERR_CUDA;
         mp = &maps;
