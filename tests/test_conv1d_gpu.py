@@ -168,3 +168,19 @@ def test_bwd_through_scan_chain():
     assert max_rel_err(dx.cpu().numpy(), rdx) <= 1e-3
     assert max_rel_err(dw.cpu().numpy(), rdw) <= 1e-3
     assert max_rel_err(db.cpu().numpy(), rdb) <= 1e-3
+
+
+def test_bwd_config_full_size_sampled():
+    """batch 8 x D 5120 x L 2048, K 4, bf16 x, fp32 dout: the launch the bench
+    times.  dx, dweight and dbias of channels 0, 1, 2047 and 5119 (every batch
+    entry and step) against the oracle on those channels."""
+    x, w, bias = _data(8, 5120, 2048, 4, 160_010, True)
+    dout = np.random.default_rng(160_011).standard_normal((8, 5120, 2048)).astype(np.float32)
+    dx, dw, db = _bwd(x, w, bias, dout, True)
+    assert np.all(np.isfinite(dx))
+    ds = [0, 1, 2047, 5119]
+    rdx, rdw, rdb = oracle.causal_conv1d_bwd(x[:, ds], w[ds], bias[ds], dout[:, ds])
+    assert max_rel_err(dx[:, ds], rdx) <= TOL_BWD
+    scale = 1.0 + np.abs(dout[:, ds]).sum() / len(ds)
+    assert np.max(np.abs(dw[ds] - rdw)) / scale <= TOL_BWD
+    assert np.max(np.abs(db[ds] - rdb)) / scale <= TOL_BWD

@@ -85,9 +85,9 @@ def test_equals_two_launches_fp32():
 
 
 def test_mamba_layer_size_sampled_rows():
-    """batch 2 of the Mamba-2.8B layer shape (D 5120, L 2048, N 16, bf16, K 4):
-    the full launch, oracle on every 37th channel."""
-    inp = s6_inputs(2, 5120, 2048, 16, seed=4500, bf16=True)
+    """The launch the bench times (batch 8, D 5120, L 2048, N 16, bf16, K 4),
+    oracle on every 37th channel of every batch entry."""
+    inp = s6_inputs(8, 5120, 2048, 16, seed=4500, bf16=True)
     w, cb = conv_taps(5120, 4, seed=4501)
     y = _run(inp, w, cb, True)
     assert np.all(np.isfinite(y))
