@@ -94,6 +94,9 @@ struct SsdArgs {
     const float *A, *D, *delta_bias;
     float *y, *final_state;
     void* workspace;
+    // optional, for the backward: the state entering every chunk in fp32
+    // [b, nc, H, P, N], written by the forward's state pass
+    float* Hin32 = nullptr;
 };
 
 size_t ssd_workspace(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, int64_t G,

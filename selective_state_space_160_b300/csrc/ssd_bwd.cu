@@ -1336,10 +1336,7 @@ size_t ssd_bwd_workspace(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t
     s += 4 * a256((size_t)batch * H * Lp * 4);            // dt, cs, dcs, dDelta
     s += 5 * a256((size_t)batch * nc * H * kP * kN * 4);  // S, Hin, U / dS, and the Hin, dS bf16 hi + lo images
     s += 2 * a256((size_t)batch * nc * G * Q * Q * 4);    // G, dG
-    if (has_z) {
-        s += a256((size_t)batch * L * H * kP * 4);         // pre-gate output
-        s += a256(ssd_workspace(batch, L, H, kP, kN, G, Q));
-    }
+    if (has_z) s += a256((size_t)batch * L * H * kP * 4);  // pre-gate output
     return s;
 }
 
@@ -1361,16 +1358,20 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
     const size_t nrow = (size_t)f.batch * f.H * p.Lp * 4;
     const size_t nst = (size_t)f.batch * p.nc * f.H * kP * kN * 4;
     const size_t ngm = (size_t)f.batch * p.nc * f.G * f.Q * f.Q * 4;
-    char* ws = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(a.workspace) + 1023) & ~uintptr_t(1023));
+    // the first four buffers are laid out as the forward's workspace (Delta, cs,
+    // chunk states, state images), so that with a gate the forward run that
+    // gives y_pre also leaves the states the backward needs
+    char* base = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(a.workspace) + 1023) & ~uintptr_t(1023));
+    char* ws = base;
     float* dt = reinterpret_cast<float*>(ws); ws += a256(nrow);
     float* cs = reinterpret_cast<float*>(ws); ws += a256(nrow);
+    float* S = reinterpret_cast<float*>(ws); ws += a256(nst);
+    uint16_t* Himg = reinterpret_cast<uint16_t*>(ws); ws += a256(nst);
     p.dcs = reinterpret_cast<float*>(ws); ws += a256(nrow);
     p.dDelta = reinterpret_cast<float*>(ws); ws += a256(nrow);
-    float* S = reinterpret_cast<float*>(ws); ws += a256(nst);
     float* Hin = reinterpret_cast<float*>(ws); ws += a256(nst);
     float* U = reinterpret_cast<float*>(ws); ws += a256(nst);
     p.U = U;
-    uint16_t* Himg = reinterpret_cast<uint16_t*>(ws); ws += a256(nst);
     p.dSimg = reinterpret_cast<uint16_t*>(ws); ws += a256(nst);
     p.Himg = Himg;
     p.Gm = reinterpret_cast<float*>(ws); ws += a256(ngm);
@@ -1378,13 +1379,15 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
     p.dt = dt; p.cs = cs; p.Hin = Hin;
     msc_status s;
     if (f.z) {
+        // the forward without the gate: y_pre, and Delta, cs, S, Hin in this workspace
         float* ypre = reinterpret_cast<float*>(ws); ws += a256((size_t)f.batch * f.L * f.H * kP * 4);
         SsdArgs fa = f;
-        fa.z = nullptr; fa.y = ypre; fa.final_state = nullptr; fa.workspace = ws;
+        fa.z = nullptr; fa.y = ypre; fa.final_state = nullptr; fa.workspace = base; fa.Hin32 = Hin;
         if ((s = ssd_launch(fa, st)) != MSC_OK) return s;
         p.ypre = ypre;
+    } else if ((s = ssd_states(f, dt, cs, S, Hin, Himg, st)) != MSC_OK) {
+        return s;
     }
-    if ((s = ssd_states(f, dt, cs, S, Hin, Himg, st)) != MSC_OK) return s;
     cudaError_t e = cudaMemsetAsync(p.dcs, 0, 2 * a256(nrow), st);  // dcs and dDelta are adjacent
     if (e == cudaSuccess) e = cudaMemsetAsync(p.dA, 0, (size_t)f.H * 4, st);
     if (e == cudaSuccess && p.dD) e = cudaMemsetAsync(p.dD, 0, (size_t)f.H * 4, st);

@@ -725,6 +725,7 @@ msc_status ssd_launch(const SsdArgs& a, cudaStream_t st) {
     p.C = static_cast<const uint16_t*>(a.C);
     p.z = static_cast<const uint16_t*>(a.z);
     p.A = a.A; p.D = a.D; p.bias = a.delta_bias; p.y = a.y; p.final_state = a.final_state;
+    p.Hin32 = a.Hin32;
     p.L = a.L; p.batch = (int)a.batch; p.H = (int)a.H; p.G = (int)a.G; p.hpg = (int)(a.H / a.G); p.Q = (int)a.Q;
     p.nc = (int)((a.L + a.Q - 1) / a.Q);
     p.Lp = (int64_t)p.nc * a.Q;
