@@ -110,7 +110,7 @@ msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* H
                       cudaStream_t stream);
 // U_c [b, nc, H, P, N] = sum over the chunk of exp(cs_i) g_i (x) C_i, g = dy
 // (times silu(z) when a.z is set), on the chunk-state tensor-core kernel; cs from
-// ssd_states.  Call ssd_states first (it configures that kernel).
+// ssd_states or from the forward's workspace.
 msc_status ssd_ugrad(const SsdArgs& a, const void* dy, const float* cs, float* U, cudaStream_t stream);
 
 // SSD backward: the forward's inputs in f (y, final_state, workspace unused),

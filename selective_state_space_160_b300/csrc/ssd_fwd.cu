@@ -860,6 +860,16 @@ msc_status ssd_ugrad(const SsdArgs& a, const void* dy, const float* cs, float* U
         !encode_tmap(&mDy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dy, xd, xs, qbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tmap(&mZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.z ? a.z : dy, xd, xs, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
         return MSC_ERR_CUDA;
+    {
+        static bool configured = false;
+        if (!configured) {
+            cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(ssd_state_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
+            if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_state smem attribute: %s", cudaGetErrorString(e));
+            configured = true;
+        }
+    }
     const dim3 grid(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch);
     if (a.z)
         ssd_state_kernel<2><<<grid, 256, state_smem(p.Q), st>>>(mC, mDy, mZ, p);

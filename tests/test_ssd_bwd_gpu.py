@@ -128,3 +128,32 @@ def test_ssd_config_full_size_sampled_heads():
     assert all(np.all(np.isfinite(v)) for v in full.values())
     for k in ("dx", "dz"):
         assert np.array_equal(full[k][:, :, hs, :], g[k][:, :, hs, :]), k
+
+
+def test_gated_backward_first_in_a_fresh_process():
+    """The gated backward as the first SSD call of a process (it takes a path
+    that no earlier call has configured), checked against the oracle."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = """
+import sys
+sys.path.insert(0, %r); sys.path.insert(0, %r)
+import numpy as np
+from oracle import oracle
+from selective_state_space_160_b300.inputs import ssd_inputs
+from helpers import max_rel_err, to_dev
+import selective_state_space_160_b300 as msc
+inp = ssd_inputs(1, 300, 2, 64, 128, 1, seed=3700, bf16=True, with_z=True, with_dy=True)
+dev = {k: to_dev(inp[k], True) for k in ("x", "delta", "B", "C", "z", "dy")}
+g = msc.msc_ssd_chunked_bwd(dev["x"], dev["delta"], to_dev(inp["A"]), dev["B"], dev["C"], dev["dy"],
+                            to_dev(inp["D"]), dev["z"], to_dev(inp["delta_bias"]), chunk=128)
+r = oracle.ssd_bwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                   inp["delta_bias"], inp["dy"])
+e = max(max_rel_err(v.cpu().numpy(), r[k]) for k, v in g.items())
+print("ERR", e)
+sys.exit(0 if e <= 2e-3 else 1)
+""" % (root, os.path.join(root, "tests"))
+    res = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stdout[-2000:] + res.stderr[-2000:]
