@@ -95,4 +95,11 @@ void clear_error();
 // Checks cudaGetLastError() after a launch; returns MSC_OK or MSC_ERR_CUDA.
 msc_status check_launch(const char* what);
 int num_sms();
+// This thread's current device as one bit (devices 0..63), for launch sites
+// that set a kernel attribute once per device.
+inline uint64_t device_bit() {
+    int d = 0;
+    cudaGetDevice(&d);
+    return 1ull << (d & 63);
+}
 }  // namespace msc_host

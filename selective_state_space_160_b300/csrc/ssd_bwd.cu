@@ -1419,8 +1419,8 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
         const uint32_t gbox[2] = {(uint32_t)std::min<int64_t>(f.Q, 128), 64};
         if (!encode_tmap(&mG, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.Gm, gd, gs, gbox, CU_TENSOR_MAP_SWIZZLE_NONE))
             return MSC_ERR_CUDA;
-        static bool configured = false;
-        if (!configured) {
+        static uint64_t configured = 0;  // one bit per device on which the attribute is set
+        if (!(configured & msc_host::device_bit())) {
             cudaError_t e2 = cudaSuccess;
             for (const void* k : {(const void*)ssd_dx_tc_kernel<64, false>, (const void*)ssd_dx_tc_kernel<64, true>,
                                   (const void*)ssd_dx_tc_kernel<128, false>, (const void*)ssd_dx_tc_kernel<128, true>,
@@ -1431,7 +1431,7 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
             if (e2 == cudaSuccess)
                 e2 = cudaFuncSetAttribute(ssd_dg_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDgSmem);
             if (e2 != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd bwd smem attribute: %s", cudaGetErrorString(e2));
-            configured = true;
+            configured |= msc_host::device_bit();
         }
     }
     const unsigned nmb = (unsigned)((f.Q + 127) / 128), ntri128 = nmb * (nmb + 1) / 2;

@@ -758,11 +758,11 @@ msc_status ssd_launch(const SsdArgs& a, cudaStream_t st) {
     }
     // (2) chunk states
     {
-        static bool configured = false;
-        if (!configured) {
+        static uint64_t configured = 0;  // one bit per device on which the attribute is set
+        if (!(configured & msc_host::device_bit())) {
             cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_state smem attribute: %s", cudaGetErrorString(e));
-            configured = true;
+            configured |= msc_host::device_bit();
         }
         ssd_state_kernel<0><<<dim3(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch), 256, state_smem(p.Q), st>>>(
             m.B, m.xq, m.xq, p);
@@ -777,11 +777,11 @@ msc_status ssd_launch(const SsdArgs& a, cudaStream_t st) {
     // (4) chunk scan
     {
         const int nib = (p.Q + 127) / 128;
-        static bool configured = false;
-        if (!configured) {
+        static uint64_t configured = 0;  // one bit per device on which the attribute is set
+        if (!(configured & msc_host::device_bit())) {
             cudaError_t e = cudaFuncSetAttribute(ssd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
             if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_scan smem attribute: %s", cudaGetErrorString(e));
-            configured = true;
+            configured |= msc_host::device_bit();
         }
         ssd_scan_kernel<<<dim3(p.nc * nib, (p.H + kHB - 1) / kHB, (unsigned)a.batch), kScanThreads, kScanSmem, st>>>(
             m.C, m.B, m.xs, p);
@@ -818,15 +818,15 @@ msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* H
             return MSC_ERR_CUDA;
     }
     {
-        static bool configured = false;
-        if (!configured) {
+        static uint64_t configured = 0;  // one bit per device on which the attribute is set
+        if (!(configured & msc_host::device_bit())) {
             cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(ssd_state_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(ssd_state_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_state smem attribute: %s", cudaGetErrorString(e));
-            configured = true;
+            configured |= msc_host::device_bit();
         }
         ssd_state_kernel<0><<<dim3(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch), 256, state_smem(p.Q), st>>>(
             mB, mX, mX, p);
@@ -861,13 +861,13 @@ msc_status ssd_ugrad(const SsdArgs& a, const void* dy, const float* cs, float* U
         !encode_tmap(&mZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.z ? a.z : dy, xd, xs, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
         return MSC_ERR_CUDA;
     {
-        static bool configured = false;
-        if (!configured) {
+        static uint64_t configured = 0;  // one bit per device on which the attribute is set
+        if (!(configured & msc_host::device_bit())) {
             cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(ssd_state_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_state smem attribute: %s", cudaGetErrorString(e));
-            configured = true;
+            configured |= msc_host::device_bit();
         }
     }
     const dim3 grid(p.nc, (p.H + kHBS - 1) / kHBS, (unsigned)a.batch);
