@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include "msc_common.cuh"
+#include "msc_tma.cuh"
 #include "msc_internal.h"
 
 namespace {
@@ -114,6 +115,149 @@ __global__ void __launch_bounds__(256) conv1d_fwd_kernel(const ConvParams p) {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             if (t0 + i < p.L) store1<kOutBF16>(p.out, row * p.L + t0 + i, o[i]);
+    }
+}
+
+// K <= 4 (the width Mamba uses) and L % 8 == 0: a persistent kernel whose
+// warps walk units of one row's 512 consecutive steps, lane l taking steps
+// 16 l .. 16 l + 15 of the unit.  The three inputs before a lane's first step
+// are the last three of the lane before it (a shuffle); a unit's first lane
+// loads them.  The first lane also prefetches, into L2 with one bulk request,
+// the unit the warp takes two sweeps later, so DRAM reads run ahead of the
+// loads without holding registers.  Taps are right-aligned in a 4-tap window;
+// output pairs use packed f32x2 arithmetic.
+constexpr int kUnitSteps = 512;
+constexpr int kPrefetchAhead = 2;  // units (sweeps of the grid) prefetched ahead
+
+// Position of a unit: row, 512-step segment, channel.
+struct UnitPos {
+    int64_t row, d;
+    int seg;
+};
+
+__device__ __forceinline__ void advance(UnitPos& q, int64_t sq, int sr, int64_t sqd, int nseg, int64_t dim) {
+    q.row += sq;
+    q.d += sqd;
+    q.seg += sr;
+    if (q.seg >= nseg) { q.seg -= nseg; ++q.row; ++q.d; }
+    if (q.d >= dim) q.d -= dim;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// One unit's inputs (512 steps, or the row's rest) into L2.
+template <int kES>
+__device__ __forceinline__ void prefetch_unit(const void* x, const UnitPos& q, int64_t L) {
+    const int64_t s0 = (int64_t)q.seg * kUnitSteps;
+    const int64_t n = L - s0 < kUnitSteps ? L - s0 : kUnitSteps;
+    prefetch_l2(reinterpret_cast<const uint8_t*>(x) + (q.row * L + s0) * kES, (uint32_t)(n * kES));
+}
+
+template <bool kInBF16, bool kOutBF16>
+__global__ void __launch_bounds__(256) conv1d_fwd_w4_kernel(const ConvParams p, int64_t units, int nseg) {
+    constexpr int kES = kInBF16 ? 2 : 4;
+    const int lane = threadIdx.x & 31;
+    const int64_t wstep = (int64_t)gridDim.x * (blockDim.x >> 5);  // units per sweep of the grid
+    int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (u >= units) return;  // warp-uniform
+    const int64_t sq = wstep / nseg;
+    const int sr = (int)(wstep - sq * nseg);
+    const int64_t sqd = sq % p.dim;
+    UnitPos cur;
+    cur.row = u / nseg;
+    cur.seg = (int)(u - cur.row * nseg);
+    cur.d = cur.row % p.dim;
+    // the unit prefetched next: kPrefetchAhead sweeps ahead of the current one
+    UnitPos pf = cur;
+    int64_t upf = u;
+    for (int k = 0; k <= kPrefetchAhead; ++k) {
+        if (k > 0) { advance(pf, sq, sr, sqd, nseg, p.dim); upf += wstep; }
+        if (lane == 0 && upf < units) prefetch_unit<kES>(p.x, pf, p.L);
+    }
+
+    for (; u < units; u += wstep, advance(cur, sq, sr, sqd, nseg, p.dim)) {
+        advance(pf, sq, sr, sqd, nseg, p.dim);
+        upf += wstep;
+        if (lane == 0 && upf < units) prefetch_unit<kES>(p.x, pf, p.L);
+
+        const int64_t t0 = (int64_t)cur.seg * kUnitSteps + 16 * lane;
+        const int nv = t0 >= p.L ? 0 : (p.L - t0 >= 16 ? 16 : (int)(p.L - t0));
+        const int64_t base = cur.row * p.L + t0;
+        // xs[0..3) = x[t0 - 3 .. t0), xs[3..19) = x[t0 .. t0 + 16)
+        float xs[19];
+        if constexpr (kInBF16) {
+            const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.x) + base);
+            const uint4 a = nv > 0 ? __ldg(q) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 b = nv > 8 ? __ldg(q + 1) : make_uint4(0u, 0u, 0u, 0u);
+            // x[t0 - 4 .. t0) as two bf16 pairs (8-byte aligned: t0 is a multiple of 16)
+            const uint2 hv = (lane == 0 && t0 > 0)
+                                 ? __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.x) + base - 4))
+                                 : make_uint2(0u, 0u);
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                xs[3 + 2 * k] = msc::bf16lo(w[k]);
+                xs[4 + 2 * k] = msc::bf16hi(w[k]);
+            }
+            const uint32_t s6 = __shfl_up_sync(0xffffffffu, w[6], 1);
+            const uint32_t s7 = __shfl_up_sync(0xffffffffu, w[7], 1);
+            const uint32_t h0 = lane == 0 ? hv.x : s6, h1 = lane == 0 ? hv.y : s7;
+            xs[0] = msc::bf16hi(h0);
+            xs[1] = msc::bf16lo(h1);
+            xs[2] = msc::bf16hi(h1);
+        } else {
+            const float4* q = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.x) + base);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 v = nv > 4 * e ? __ldg(q + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xs[3 + 4 * e] = v.x; xs[4 + 4 * e] = v.y; xs[5 + 4 * e] = v.z; xs[6 + 4 * e] = v.w;
+            }
+            // x[t0 - 4 .. t0) (16-byte aligned); the last three are the halo
+            const float4 hv = (lane == 0 && t0 > 0) ? __ldg(q - 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float hl[3] = {hv.y, hv.z, hv.w};
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                const float s = __shfl_up_sync(0xffffffffu, xs[16 + m], 1);
+                xs[m] = lane == 0 ? hl[m] : s;
+            }
+        }
+        if (t0 == 0) xs[0] = xs[1] = xs[2] = 0.f;
+        uint64_t w2[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float w = (m + p.K >= 4) ? __ldg(p.w + cur.d * p.K + (m + p.K - 4)) : 0.f;
+            w2[m] = msc::pk2(w, w);
+        }
+        const float bv = p.bias ? __ldg(p.bias + cur.d) : 0.f;
+        const uint64_t b2 = msc::pk2(bv, bv);
+        // output t0 + i = sum_m w4[m] x[t0 + i - 3 + m] = sum_m w4[m] xs[i + m]
+        uint32_t ob[8];
+        uint64_t of[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            uint64_t acc = b2;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) acc = msc::fma2(w2[m], msc::pk2(xs[i + m], xs[i + 1 + m]), acc);
+            if (p.silu) acc = msc::silu_2(acc);
+            float lo, hi;
+            msc::upk2(acc, lo, hi);
+            if constexpr (kOutBF16) ob[i / 2] = pack_bf16x2_rn(lo, hi);
+            else of[i / 2] = acc;
+        }
+        if (nv > 0) {
+            if constexpr (kOutBF16) {
+                uint4* q = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + base);
+                q[0] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+                if (nv > 8) q[1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
+            } else {
+                ulonglong2* q = reinterpret_cast<ulonglong2*>(reinterpret_cast<float*>(p.out) + base);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (nv > 4 * e) q[e] = make_ulonglong2(of[2 * e], of[2 * e + 1]);
+            }
+        }
     }
 }
 
@@ -274,6 +418,28 @@ msc_status launch_bwd(const ConvParams& p, bool vec, const float* dout, float* d
 
 template <bool kIn, bool kOut>
 msc_status launch_fwd(const ConvParams& p, bool vec, cudaStream_t st) {
+    if (vec && p.K <= 4) {
+        const int nseg = (int)((p.L + kUnitSteps - 1) / kUnitSteps);
+        const int64_t units = p.rows * nseg;
+        if (units == 0) return MSC_OK;
+        // resident CTAs per SM, once per device
+        static int per_sm[64] = {0};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int& occ = per_sm[dev & 63];
+        if (occ == 0) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, conv1d_fwd_w4_kernel<kIn, kOut>, 256, 0) !=
+                    cudaSuccess || n < 1)
+                n = 1;
+            occ = n;
+        }
+        const int64_t want = (units + 7) / 8;
+        const int64_t cap = (int64_t)msc_host::num_sms() * occ;
+        const unsigned blocks = (unsigned)(want < cap ? want : cap);
+        conv1d_fwd_w4_kernel<kIn, kOut><<<blocks, 256, 0, st>>>(p, units, nseg);
+        return msc_host::check_launch("conv1d_fwd");
+    }
     const int64_t n = p.rows * p.nchunks;
     const int64_t blocks = (n + 255) / 256;
     if (blocks > 0x7FFFFFFF) return msc_host::fail(MSC_ERR_UNSUPPORTED, "problem too large for one launch");
