@@ -42,6 +42,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 
 __device__ __forceinline__ float finish(float acc, int silu) { return silu ? msc::silu_f(acc) : acc; }
 
+// silu'(x) = s (1 + x (1 - s)), s = sigmoid(x)
+__device__ __forceinline__ float dsilu_f(float x) {
+    const float sg = msc::sigmoid_f(x);
+    return sg * (1.f + x * (1.f - sg));
+}
+__device__ __forceinline__ uint64_t dsilu_2(uint64_t x) {
+    float x0, x1;
+    msc::upk2(x, x0, x1);
+    const uint64_t e = msc::ex2_2(msc::pk2(-x0 * MSC_LOG2E, -x1 * MSC_LOG2E));
+    const uint64_t sg = msc::rcp_2(msc::add2(e, msc::pk2(1.f, 1.f)));
+    const uint64_t one_m = msc::fma2(sg, msc::pk2(-1.f, -1.f), msc::pk2(1.f, 1.f));
+    return msc::mul2(sg, msc::fma2(x, one_m, msc::pk2(1.f, 1.f)));
+}
+
 template <bool kOutBF16>
 __device__ __forceinline__ void store1(void* out, int64_t i, float v) {
     if constexpr (kOutBF16) {
@@ -396,9 +410,233 @@ __global__ void __launch_bounds__(256) conv1d_bwd_kernel(const ConvParams p, con
     if (db) atomicAdd(db + d, part[kW]);
 }
 
+// Backward for K <= 4 and L % 8 == 0.  A warp takes whole rows, one 512-step
+// segment after another, lane l taking steps 16 l .. 16 l + 15 of a segment
+// (the forward's tiling).  With pre the pre-activation and g = dout silu'(pre)
+// (dout without the activation):
+//   dx[s] = sum_m w4[m] g[s + 3 - m],  dw4[m] += sum_t g[t] x[t - 3 + m],  db += sum_t g[t]
+// (w4: the taps right-aligned in a 4-tap window).  A lane's three inputs before
+// its first step come from the lane before it, the three g after its last step
+// from the lane after it (shuffles); the segment's first lane loads its halo, the
+// last lane loads the three inputs and output gradients after the segment and
+// forms their g itself.  dw and db accumulate in registers over the row and are
+// reduced over the warp once per row.  Lane 0 prefetches into L2, with bulk
+// requests, the segment the warp takes two segments later (x and dout).
+// Issues the L2 prefetch of segment (pf_row, pf_seg) of x and dout (lane 0) and
+// moves the cursor to the warp's next segment.
+template <int kES>
+__device__ __forceinline__ void bwd_prefetch(const void* x, const float* dout, int64_t rows, int64_t L, int nseg,
+                                             int64_t nwarps, int lane, int64_t& pf_row, int& pf_seg) {
+    if (lane == 0 && pf_row < rows) {
+        const int64_t s0 = (int64_t)pf_seg * kUnitSteps;
+        const int64_t n = L - s0 < kUnitSteps ? L - s0 : kUnitSteps;
+        prefetch_l2(reinterpret_cast<const uint8_t*>(x) + (pf_row * L + s0) * kES, (uint32_t)(n * kES));
+        prefetch_l2(dout + pf_row * L + s0, (uint32_t)(n * 4));
+    }
+    if (++pf_seg == nseg) {
+        pf_seg = 0;
+        pf_row += nwarps;
+    }
+}
+
+template <bool kInBF16>
+__global__ void __launch_bounds__(256) conv1d_bwd_w4_kernel(const ConvParams p, const float* __restrict__ dout,
+                                                            float* __restrict__ dx, float* dw, float* db, int nseg) {
+    constexpr int kES = kInBF16 ? 2 : 4;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= p.rows) return;  // warp-uniform
+    const int64_t L = p.L;
+    // prefetch cursor, two segments ahead of the one being computed
+    int64_t pf_row = row;
+    int pf_seg = 0;
+    bwd_prefetch<kES>(p.x, dout, p.rows, L, nseg, nwarps, lane, pf_row, pf_seg);
+    bwd_prefetch<kES>(p.x, dout, p.rows, L, nseg, nwarps, lane, pf_row, pf_seg);
+
+    for (; row < p.rows; row += nwarps) {
+        const int64_t d = row % p.dim;
+        float ws[4];
+        uint64_t w2[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            ws[m] = (m + p.K >= 4) ? __ldg(p.w + d * p.K + (m + p.K - 4)) : 0.f;
+            w2[m] = msc::pk2(ws[m], ws[m]);
+        }
+        const float bv = p.bias ? __ldg(p.bias + d) : 0.f;
+        const uint64_t b2 = msc::pk2(bv, bv);
+        uint64_t dw2[4] = {0ull, 0ull, 0ull, 0ull};
+        uint64_t db2 = 0ull;
+        for (int seg = 0; seg < nseg; ++seg) {
+            bwd_prefetch<kES>(p.x, dout, p.rows, L, nseg, nwarps, lane, pf_row, pf_seg);
+            const int64_t t0 = (int64_t)seg * kUnitSteps + 16 * lane;
+            const int nv = t0 >= L ? 0 : (L - t0 >= 16 ? 16 : (int)(L - t0));
+            const int64_t base = row * L + t0;
+            // xs[0..3) = x[t0 - 3 .. t0), xs[3..19) = x[t0 .. t0 + 16), xs[19..22) = x[t0 + 16 .. t0 + 19)
+            float xs[22];
+            float gv[16];
+            // x after the lane's steps, and dout there (the last lane of the segment)
+            const bool tail = lane == 31 && t0 + 16 < L;
+            float xt[3] = {0.f, 0.f, 0.f}, gt[3] = {0.f, 0.f, 0.f};
+            if constexpr (kInBF16) {
+                const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.x) + base);
+                const uint4 a = nv > 0 ? __ldg(q) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 b = nv > 8 ? __ldg(q + 1) : make_uint4(0u, 0u, 0u, 0u);
+                const uint2 hv = (lane == 0 && t0 > 0)
+                                     ? __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.x) + base - 4))
+                                     : make_uint2(0u, 0u);
+                const uint2 tv = tail ? __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.x) + base + 16))
+                                      : make_uint2(0u, 0u);
+                const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    xs[3 + 2 * k] = msc::bf16lo(w[k]);
+                    xs[4 + 2 * k] = msc::bf16hi(w[k]);
+                }
+                const uint32_t s6 = __shfl_up_sync(0xffffffffu, w[6], 1);
+                const uint32_t s7 = __shfl_up_sync(0xffffffffu, w[7], 1);
+                const uint32_t h0 = lane == 0 ? hv.x : s6, h1 = lane == 0 ? hv.y : s7;
+                xs[0] = msc::bf16hi(h0);
+                xs[1] = msc::bf16lo(h1);
+                xs[2] = msc::bf16hi(h1);
+                xt[0] = msc::bf16lo(tv.x);
+                xt[1] = msc::bf16hi(tv.x);
+                xt[2] = msc::bf16lo(tv.y);
+            } else {
+                const float4* q = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.x) + base);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 v = nv > 4 * e ? __ldg(q + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    xs[3 + 4 * e] = v.x; xs[4 + 4 * e] = v.y; xs[5 + 4 * e] = v.z; xs[6 + 4 * e] = v.w;
+                }
+                const float4 hv = (lane == 0 && t0 > 0) ? __ldg(q - 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 tv = tail ? __ldg(q + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float hl[3] = {hv.y, hv.z, hv.w};
+#pragma unroll
+                for (int m = 0; m < 3; ++m) {
+                    const float sv = __shfl_up_sync(0xffffffffu, xs[16 + m], 1);
+                    xs[m] = lane == 0 ? hl[m] : sv;
+                }
+                xt[0] = tv.x; xt[1] = tv.y; xt[2] = tv.z;
+            }
+            if (t0 == 0) xs[0] = xs[1] = xs[2] = 0.f;
+            {
+                const float4* q = reinterpret_cast<const float4*>(dout + base);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 v = nv > 4 * e ? __ldg(q + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    gv[4 * e] = v.x; gv[4 * e + 1] = v.y; gv[4 * e + 2] = v.z; gv[4 * e + 3] = v.w;
+                }
+                const float4 tg = tail ? __ldg(q + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                gt[0] = tg.x; gt[1] = tg.y; gt[2] = tg.z;
+            }
+            // the inputs after the lane's steps (used by the last lane only)
+            xs[19] = xt[0]; xs[20] = xt[1]; xs[21] = xt[2];
+            // g over the lane's 16 steps (pairs), and over the three after it on the last lane
+            // (pre[t0 + i] = sum_m w4[m] xs[i + m])
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                uint64_t pre = b2;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) pre = msc::fma2(w2[m], msc::pk2(xs[i + m], xs[i + 1 + m]), pre);
+                uint64_t g = msc::pk2(gv[i], gv[i + 1]);
+                if (p.silu) g = msc::mul2(g, dsilu_2(pre));
+                msc::upk2(g, gv[i], gv[i + 1]);
+            }
+            float ga[3];
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                float pre = bv;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) pre = fmaf(ws[m], xs[16 + j + m], pre);
+                const float gl = p.silu ? gt[j] * dsilu_f(pre) : gt[j];
+                const float sv = __shfl_down_sync(0xffffffffu, gv[j], 1);
+                ga[j] = lane == 31 ? gl : sv;
+            }
+            // past the row end g is 0 (dout there is not read)
+            if (nv < 16) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (i >= nv) gv[i] = 0.f;
+            }
+            if (t0 + 16 >= L) ga[0] = ga[1] = ga[2] = 0.f;
+            // dx[t0 + s] = sum_m w4[m] g[t0 + s + 3 - m]; g index k = s + 3 - m in 0 .. 18
+            float gg[19];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) gg[i] = gv[i];
+            gg[16] = ga[0]; gg[17] = ga[1]; gg[18] = ga[2];
+            uint64_t o[8];
+#pragma unroll
+            for (int s2 = 0; s2 < 16; s2 += 2) {
+                uint64_t acc = 0ull;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) acc = msc::fma2(w2[m], msc::pk2(gg[s2 + 3 - m], gg[s2 + 4 - m]), acc);
+                o[s2 / 2] = acc;
+            }
+            if (nv > 0) {
+                ulonglong2* q = reinterpret_cast<ulonglong2*>(dx + base);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (nv > 4 * e) q[e] = make_ulonglong2(o[2 * e], o[2 * e + 1]);
+            }
+            // dw4[m] += g[t0 + s] x[t0 + s - 3 + m] = gv[s] xs[s + m]; db += g
+#pragma unroll
+            for (int s2 = 0; s2 < 16; s2 += 2) {
+                const uint64_t g2 = msc::pk2(gv[s2], gv[s2 + 1]);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) dw2[m] = msc::fma2(g2, msc::pk2(xs[s2 + m], xs[s2 + 1 + m]), dw2[m]);
+                db2 = msc::add2(db2, g2);
+            }
+        }
+        // the row's dw and db: sum the pair halves, then over the warp
+        float part[5];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            float lo, hi;
+            msc::upk2(dw2[m], lo, hi);
+            part[m] = lo + hi;
+        }
+        {
+            float lo, hi;
+            msc::upk2(db2, lo, hi);
+            part[4] = lo + hi;
+        }
+#pragma unroll
+        for (int m = 0; m < 5; ++m)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) part[m] += __shfl_xor_sync(0xffffffffu, part[m], off);
+        if (lane == 0) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                if (m + p.K >= 4) atomicAdd(dw + d * p.K + (m + p.K - 4), part[m]);
+            if (db) atomicAdd(db + d, part[4]);
+        }
+    }
+}
+
 template <bool kIn>
 msc_status launch_bwd(const ConvParams& p, bool vec, const float* dout, float* dx, float* dw, float* db,
                       cudaStream_t st) {
+    if (vec && p.K <= 4) {
+        if (p.rows == 0) return MSC_OK;
+        const int nseg = (int)((p.L + kUnitSteps - 1) / kUnitSteps);
+        static int per_sm[64] = {0};  // resident CTAs per SM, once per device
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int& occ = per_sm[dev & 63];
+        if (occ == 0) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, conv1d_bwd_w4_kernel<kIn>, 256, 0) != cudaSuccess ||
+                n < 1)
+                n = 1;
+            occ = n;
+        }
+        const int64_t want = (p.rows + 7) / 8;
+        const int64_t cap = (int64_t)msc_host::num_sms() * occ;
+        const unsigned blocks = (unsigned)(want < cap ? want : cap);
+        conv1d_bwd_w4_kernel<kIn><<<blocks, 256, 0, st>>>(p, dout, dx, dw, db, nseg);
+        return msc_host::check_launch("conv1d_bwd");
+    }
     const int64_t n = p.rows * p.nchunks;
     const int64_t blocks = (n + 255) / 256;
     if (blocks > 0x7FFFFFFF) return msc_host::fail(MSC_ERR_UNSUPPORTED, "problem too large for one launch");

@@ -151,7 +151,8 @@ def _bwd(x, w, bias, dout, bf16, silu=True, with_dbias=True):
 @pytest.mark.parametrize("batch,dim,L,K,bf16,silu", [
     (1, 4, 64, 4, False, True), (2, 37, 96, 4, True, True), (2, 5, 100, 3, False, True),
     (1, 3, 17, 8, False, False), (3, 8, 2048, 4, True, True), (1, 6, 1, 2, True, True),
-    (2, 33, 999, 1, False, True)])
+    (2, 33, 999, 1, False, True), (2, 30, 1048, 4, False, True), (1, 5, 520, 3, True, False),
+    (4, 700, 1024, 2, True, True)])
 def test_bwd_shapes(batch, dim, L, K, bf16, silu):
     x, w, bias = _data(batch, dim, L, K, 5000 + L + K, bf16)
     dout = np.random.default_rng(5100 + L).standard_normal((batch, dim, L)).astype(np.float32)
