@@ -45,7 +45,17 @@ NCU_TRAFFIC = {
     # profiles/s6_fwd_tma_8x5120x2048_bf16.md: DRAM read 505.2 MB + write 298.6 MB per launch,
     # taken from the source whose hash is src_sha (any later change makes the traffic null)
     "s6_fwd_tma_kernel": {"src_sha": "e554ecadd6f4", "bytes_per_launch": 803.84e6},
+    # profiles/conv1d_8x5120x2048_bf16.md: mean of 13 launches, read 170.6 MB + write 122.5 MB
+    "conv1d_fwd_w4_kernel": {"src_sha": "ed63d8777b5a", "bytes_per_launch": 293.1e6},
+    # profiles/conv1d_bwd_8x5120x2048_bf16.md: mean of 3 launches, read 504.5 MB + write 296.8 MB
+    "conv1d_bwd_w4_kernel": {"src_sha": "ed63d8777b5a", "bytes_per_launch": 801.4e6},
 }
+
+
+def _ncu_traffic(kernel, src):
+    """The committed ncu DRAM traffic of `kernel`, or None once its source has changed."""
+    e = NCU_TRAFFIC.get(kernel)
+    return e["bytes_per_launch"] if e and os.path.exists(src) and e["src_sha"] == _sha(src) else None
 
 
 def _sha(path):
@@ -389,7 +399,9 @@ def leg_conv1d(peaks, pipes, steps=10, warmup=3):
     res = {"workload": "causal conv1d K 4 + SiLU, batch 8, D 5120, L 2048, bf16 in / bf16 out",
            "elements_per_s": el / t, "ms": ms,
            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": nbytes}}
+                        "frac": ach / peaks["hbm_gbs"],
+                        "traffic": _ncu_traffic("conv1d_fwd_w4_kernel", os.path.join(ROOT, "selective_state_space_160_b300", "csrc", "conv1d.cu")),
+                        "algorithmic_bytes": nbytes}}
     del x, out
     torch.cuda.empty_cache()
     return res
@@ -418,7 +430,9 @@ def leg_conv1d_bwd(peaks, pipes, steps=10, warmup=3):
     res = {"workload": "causal conv1d K 4 + SiLU backward, batch 8, D 5120, L 2048, bf16 x, fp32 dout / dx",
            "elements_per_s": el / t, "ms": ms,
            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": nbytes}}
+                        "frac": ach / peaks["hbm_gbs"],
+                        "traffic": _ncu_traffic("conv1d_bwd_w4_kernel", os.path.join(ROOT, "selective_state_space_160_b300", "csrc", "conv1d.cu")),
+                        "algorithmic_bytes": nbytes}}
     del x, dout
     torch.cuda.empty_cache()
     return res

@@ -40,8 +40,9 @@ __global__ void __launch_bounds__(256) pipe_kernel(float* sink, unsigned long lo
             } else if (kOp == 2) {
                 asm volatile("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(xv[c]) : "l"(av), "l"(bv));
             } else {
-                // rcp(x) of x in [0.5, 2] stays in [0.5, 2]
-                asm volatile("rcp.approx.ftz.f32 %0, %0;" : "+f"(x[c]));
+                // x <- rcp(x + 1): x in [0.5, 1] stays in [0.5, 0.67]; the add keeps
+                // the chain from being an involution (rcp of rcp) that folds away
+                asm volatile("add.f32 %0, %0, 0f3F800000;\n\trcp.approx.ftz.f32 %0, %0;" : "+f"(x[c]));
             }
         }
     }
