@@ -238,9 +238,7 @@ def roofline_s6(elements, N, bytes_per_launch, ms, peaks, pipes, exps_per_elem_n
         v["frac"] = v["achieved"] / v["peak"]
     bound = max(terms, key=lambda k: terms[k]["frac"])
     sel = terms[bound]
-    traffic = None
-    if kernel and src and kernel in NCU_TRAFFIC and NCU_TRAFFIC[kernel]["src_sha"] == _sha(src):
-        traffic = NCU_TRAFFIC[kernel]["bytes_per_launch"]
+    traffic = _ncu_traffic(kernel, src) if kernel and src else None
     out = {"bound": "hbm" if bound == "hbm" else "alu", "achieved": sel["achieved"], "peak": sel["peak"],
            "unit": sel["unit"], "frac": sel["frac"], "traffic": traffic,
            "algorithmic_bytes": bytes_per_launch, "kernel_ms": ms,
