@@ -620,19 +620,19 @@ msc_status launch_bwd(const ConvParams& p, bool vec, const float* dout, float* d
     if (vec && p.K <= 4) {
         if (p.rows == 0) return MSC_OK;
         const int nseg = (int)((p.L + kUnitSteps - 1) / kUnitSteps);
-        static int per_sm[64] = {0};  // resident CTAs per SM, once per device
+        static std::atomic<int> per_sm[64];  // resident CTAs per SM, once per device (0: not yet)
         int dev = 0;
         cudaGetDevice(&dev);
-        int& occ = per_sm[dev & 63];
-        if (occ == 0) {
+        std::atomic<int>& occ = per_sm[dev & 63];
+        if (occ.load() == 0) {
             int n = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, conv1d_bwd_w4_kernel<kIn>, 256, 0) != cudaSuccess ||
                 n < 1)
                 n = 1;
-            occ = n;
+            occ.store(n);
         }
         const int64_t want = (p.rows + 7) / 8;
-        const int64_t cap = (int64_t)msc_host::num_sms() * occ;
+        const int64_t cap = (int64_t)msc_host::num_sms() * occ.load();
         const unsigned blocks = (unsigned)(want < cap ? want : cap);
         conv1d_bwd_w4_kernel<kIn><<<blocks, 256, 0, st>>>(p, dout, dx, dw, db, nseg);
         return msc_host::check_launch("conv1d_bwd");
@@ -660,20 +660,19 @@ msc_status launch_fwd(const ConvParams& p, bool vec, cudaStream_t st) {
         const int nseg = (int)((p.L + kUnitSteps - 1) / kUnitSteps);
         const int64_t units = p.rows * nseg;
         if (units == 0) return MSC_OK;
-        // resident CTAs per SM, once per device
-        static int per_sm[64] = {0};
+        static std::atomic<int> per_sm[64];  // resident CTAs per SM, once per device (0: not yet)
         int dev = 0;
         cudaGetDevice(&dev);
-        int& occ = per_sm[dev & 63];
-        if (occ == 0) {
+        std::atomic<int>& occ = per_sm[dev & 63];
+        if (occ.load() == 0) {
             int n = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, conv1d_fwd_w4_kernel<kIn, kOut>, 256, 0) !=
                     cudaSuccess || n < 1)
                 n = 1;
-            occ = n;
+            occ.store(n);
         }
         const int64_t want = (units + 7) / 8;
-        const int64_t cap = (int64_t)msc_host::num_sms() * occ;
+        const int64_t cap = (int64_t)msc_host::num_sms() * occ.load();
         const unsigned blocks = (unsigned)(want < cap ? want : cap);
         conv1d_fwd_w4_kernel<kIn, kOut><<<blocks, 256, 0, st>>>(p, units, nseg);
         return msc_host::check_launch("conv1d_fwd");

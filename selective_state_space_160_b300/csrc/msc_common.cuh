@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "msc.h"
 
 #define MSC_LOG2E 1.4426950408889634f

@@ -460,7 +460,7 @@ constexpr int bwd_smem_bytes() {
 template <bool kBF16>
 msc_status launch_bwd(const CUtensorMap* maps, const BwdParams& p, int64_t batch, cudaStream_t st) {
     constexpr int smem = bwd_smem_bytes<kBF16>();
-    static uint64_t configured = 0;  // the attribute, set once per device (per instantiation)
+    static std::atomic<uint64_t> configured{0};  // the attribute, set once per device (per instantiation)
     if (!(configured & msc_host::device_bit())) {
         cudaError_t e = cudaFuncSetAttribute(s6_bwd_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return msc_host::fail(MSC_ERR_CUDA, "s6_bwd smem attribute: %s", cudaGetErrorString(e));

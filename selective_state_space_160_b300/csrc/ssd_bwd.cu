@@ -1419,7 +1419,7 @@ msc_status ssd_bwd_launch(const SsdBwdArgs& a, cudaStream_t st) {
         const uint32_t gbox[2] = {(uint32_t)std::min<int64_t>(f.Q, 128), 64};
         if (!encode_tmap(&mG, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.Gm, gd, gs, gbox, CU_TENSOR_MAP_SWIZZLE_NONE))
             return MSC_ERR_CUDA;
-        static uint64_t configured = 0;  // one bit per device on which the attribute is set
+        static std::atomic<uint64_t> configured{0};  // one bit per device on which the attribute is set
         if (!(configured & msc_host::device_bit())) {
             cudaError_t e2 = cudaSuccess;
             for (const void* k : {(const void*)ssd_dx_tc_kernel<64, false>, (const void*)ssd_dx_tc_kernel<64, true>,

@@ -758,7 +758,7 @@ msc_status ssd_launch(const SsdArgs& a, cudaStream_t st) {
     }
     // (2) chunk states
     {
-        static uint64_t configured = 0;  // one bit per device on which the attribute is set
+        static std::atomic<uint64_t> configured{0};  // one bit per device on which the attribute is set
         if (!(configured & msc_host::device_bit())) {
             cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_state smem attribute: %s", cudaGetErrorString(e));
@@ -777,7 +777,7 @@ msc_status ssd_launch(const SsdArgs& a, cudaStream_t st) {
     // (4) chunk scan
     {
         const int nib = (p.Q + 127) / 128;
-        static uint64_t configured = 0;  // one bit per device on which the attribute is set
+        static std::atomic<uint64_t> configured{0};  // one bit per device on which the attribute is set
         if (!(configured & msc_host::device_bit())) {
             cudaError_t e = cudaFuncSetAttribute(ssd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
             if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "ssd_scan smem attribute: %s", cudaGetErrorString(e));
@@ -818,7 +818,7 @@ msc_status ssd_states(const SsdArgs& a, float* dt, float* cs, float* S, float* H
             return MSC_ERR_CUDA;
     }
     {
-        static uint64_t configured = 0;  // one bit per device on which the attribute is set
+        static std::atomic<uint64_t> configured{0};  // one bit per device on which the attribute is set
         if (!(configured & msc_host::device_bit())) {
             cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e == cudaSuccess)
@@ -861,7 +861,7 @@ msc_status ssd_ugrad(const SsdArgs& a, const void* dy, const float* cs, float* U
         !encode_tmap(&mZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.z ? a.z : dy, xd, xs, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
         return MSC_ERR_CUDA;
     {
-        static uint64_t configured = 0;  // one bit per device on which the attribute is set
+        static std::atomic<uint64_t> configured{0};  // one bit per device on which the attribute is set
         if (!(configured & msc_host::device_bit())) {
             cudaError_t e = cudaFuncSetAttribute(ssd_state_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(256));
             if (e == cudaSuccess)
