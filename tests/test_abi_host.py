@@ -211,3 +211,20 @@ def test_fwd_conv_rejects_bad_arguments(lib):
     assert call(w=None) == msc.MSC_ERR_INVALID_ARG and "conv_weight" in msc.msc_last_error()
     assert call(L=100) == msc.MSC_ERR_UNSUPPORTED                # bf16 rows need seqlen % 8 == 0
     assert call(N=17) == msc.MSC_ERR_UNSUPPORTED
+
+
+def test_conv1d_bwd_rejects_bad_arguments(lib):
+    f = lib.msc_causal_conv1d_bwd
+
+    def call(batch=1, dim=4, L=16, K=4, idt=1, x=16, w=16, dout=16, dx=16, dw=16, db=None):
+        return f(batch, dim, L, K, idt, x, w, None, 1, dout, dx, dw, db, None)
+
+    assert call(dout=None) == msc.MSC_ERR_INVALID_ARG and "dout" in msc.msc_last_error()
+    assert call(dx=None) == msc.MSC_ERR_INVALID_ARG and "dx" in msc.msc_last_error()
+    assert call(dw=None) == msc.MSC_ERR_INVALID_ARG and "dweight" in msc.msc_last_error()
+    assert call(x=None) == msc.MSC_ERR_INVALID_ARG
+    assert call(dx=24) == msc.MSC_ERR_INVALID_ARG               # dx misaligned
+    assert call(db=40) == msc.MSC_ERR_INVALID_ARG               # dbias misaligned
+    assert call(K=9) == msc.MSC_ERR_UNSUPPORTED
+    assert call(idt=3) == msc.MSC_ERR_INVALID_ARG
+    assert call(batch=0) == msc.MSC_ERR_INVALID_ARG
