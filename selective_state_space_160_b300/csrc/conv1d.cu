@@ -9,12 +9,15 @@
 //
 // Design.  Both are bound by HBM: per element the sequence kernel reads x once
 // (2 or 4 bytes) and writes out once; the K <= 8 weights of a channel and its
-// bias are read through L1.  One thread produces 16 consecutive outputs of a
-// row: it loads its own two 8-step chunks and the chunk before them (the
+// bias are read through L1.  For K <= 4 (Mamba's width) and L % 8 == 0 the
+// forward and backward are persistent kernels whose warps walk 512-step units
+// of a row, lane l taking 16 consecutive steps: halos and look-ahead pass
+// between neighbouring lanes by shuffle, one lane per warp prefetches the unit
+// two ahead into L2 with a bulk request, and the taps run on packed f32x2
+// arithmetic.  Other widths and lengths take one thread per 16 consecutive
+// outputs: it loads its own two 8-step chunks and the chunk before them (the
 // K - 1 halo inputs; the neighbouring thread loads the same chunk, so that
-// load hits L1), so a warp reads and writes whole contiguous row segments with
-// three 16-byte (bf16) loads in flight per thread.  Rows whose length is not a
-// multiple of 8 take element-wise accesses.
+// load hits L1), with element-wise accesses where L is not a multiple of 8.
 #include <cuda_runtime.h>
 
 #include "msc_common.cuh"
