@@ -92,8 +92,9 @@ msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, in
  *    input term before t = 0 (h0, if given, is the state only).
  * Arguments, workspace (msc_selective_scan_fwd_workspace_size) and errors as
  * msc_selective_scan_fwd.  The ZOH and trapezoidal forms need 16-byte row
- * strides (seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) and return
- * MSC_ERR_UNSUPPORTED otherwise; no backward is provided for them.
+ * strides (seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) and seqlen,
+ * dim below 2^31 (their TMA tile coordinates are 32-bit), and
+ * return MSC_ERR_UNSUPPORTED otherwise; no backward is provided for them.
  */
 typedef enum { MSC_DISC_EULER = 0, MSC_DISC_ZOH = 1, MSC_DISC_TRAPEZOID = 2 } msc_discretization;
 
@@ -143,8 +144,9 @@ msc_status msc_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t se
  * msc_selective_scan_fwd.  u is kept in fp32 (not rounded to in_dtype), so
  * the result equals msc_causal_conv1d_fwd (fp32 out) followed by
  * msc_selective_scan_fwd with fp32 u up to rounding.  Needs 16-byte row
- * strides (seqlen a multiple of 8 with bf16 inputs, of 4 with fp32), else
- * MSC_ERR_UNSUPPORTED; exponential-Euler form only; no backward. */
+ * strides (seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) and seqlen,
+ * dim below 2^31, else MSC_ERR_UNSUPPORTED; exponential-Euler form only; no
+ * backward. */
 msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                        int64_t conv_width, msc_dtype in_dtype, const void* x,
                                        const float* conv_weight, const float* conv_bias, const void* delta,
@@ -160,7 +162,8 @@ msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqle
  * ddelta_bias [dim] (required iff delta_bias != NULL).
  * The forward states are recomputed chunk by chunk on chip; dB, dC, dA, dD and
  * ddelta_bias are sums accumulated with fp32 atomics, so their low bits depend
- * on the order in which blocks finish. */
+ * on the order in which blocks finish.  seqlen (rounded up to a 16-byte row)
+ * and dim must be below 2^31, else MSC_ERR_UNSUPPORTED. */
 size_t msc_selective_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
                                              int64_t dstate);
 

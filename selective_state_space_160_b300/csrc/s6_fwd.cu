@@ -874,7 +874,12 @@ msc_status launch_tma(const FwdMaps& m, const FwdParams& p, int64_t batch, int G
 }
 
 // TMA needs every row stride to be a multiple of 16 bytes.
+// The TMA path needs 16-byte row strides, and its tile coordinates (step, row)
+// are signed 32-bit: longer rows or more channels take the plain-load kernel,
+// whose indices are 64-bit.
 bool tma_ok(const FwdParams& p, bool bf16) {
+    constexpr int64_t kMaxCoord = ((int64_t)1 << 31) - 64;
+    if (p.L > kMaxCoord || p.dim > kMaxCoord) return false;
     return bf16 ? (p.L % 8 == 0) : (p.L % 4 == 0);
 }
 
@@ -886,11 +891,13 @@ msc_status launch_mode(const FwdParams& p, const FwdMaps* maps, bool bf16, bool 
     if (p.conv_w)
         return msc_host::fail(MSC_ERR_UNSUPPORTED,
                               "the fused conv front end needs 16-byte row strides "
-                              "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32)");
+                              "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) "
+                              "and seqlen, dim below 2^31");
     if (disc != kDiscEuler)
         return msc_host::fail(MSC_ERR_UNSUPPORTED,
                               "the zero-order-hold and trapezoidal forms need 16-byte row strides "
-                              "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32)");
+                              "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) "
+                              "and seqlen, dim below 2^31");
     if (bf16) return vec ? launch_rows<true, true>(p, batch, G, mode, st) : launch_rows<true, false>(p, batch, G, mode, st);
     return vec ? launch_rows<false, true>(p, batch, G, mode, st) : launch_rows<false, false>(p, batch, G, mode, st);
 }
@@ -973,7 +980,8 @@ msc_status s6_fwd_checkpoints(const S6FwdArgs& a, float* ckpt, cudaStream_t st) 
     p.dim = a.dim; p.L = a.L; p.N = a.N; p.G = 1; p.seg_len = a.L;
     p.ckpt = ckpt;
     p.ckpt_groups = (a.L + 7) / 8;
-    if (!tma_ok(p, a.bf16)) return fail(MSC_ERR_UNSUPPORTED, "checkpoint pass needs a 16-byte row stride");
+    if (!tma_ok(p, a.bf16))
+        return fail(MSC_ERR_UNSUPPORTED, "checkpoint pass needs a 16-byte row stride and seqlen, dim below 2^31");
     FwdMaps maps;
     if (!make_maps(maps, p, a.batch, a.bf16)) return MSC_ERR_CUDA;
     return a.bf16 ? launch_tma_ng<true, kLanesPerRow>(maps, p, a.batch, 1, kModeCkpt, st)

@@ -160,6 +160,11 @@ def test_fwd_ex_rejects_bad_arguments(lib):
     assert "disc" in msc.msc_last_error()
     assert call(L=63, disc=msc.MSC_DISC_ZOH) == msc.MSC_ERR_UNSUPPORTED        # bf16 rows not 16-byte strided
     assert call(L=66, dt=0, disc=msc.MSC_DISC_TRAPEZOID) == msc.MSC_ERR_UNSUPPORTED
+    # rows of 2^31 steps do not fit the 32-bit TMA coordinates: refused before any launch
+    big = 1 << 31
+    ws = msc.msc_selective_scan_fwd_workspace_size(1, 4, big, 16)
+    r = f(1, 4, big, 16, 1, msc.MSC_DISC_ZOH, 16, 16, 16, 16, 16, None, None, None, None, 16, None, 4096, ws, None)
+    assert r == msc.MSC_ERR_UNSUPPORTED and "2^31" in msc.msc_last_error()
 
 
 def test_ssd_bwd_rejects_bad_arguments(lib):
