@@ -531,6 +531,10 @@ msc_status s6_bwd_launch(const S6BwdArgs& a0, cudaStream_t st) {
     const int64_t rows = a.batch * a.dim;
     const int64_t L = a.L;
     const int64_t Lp = padded_len(L, a.bf16);
+    // the tiles' TMA coordinates (step, row) are signed 32-bit: refuse before any device work
+    constexpr int64_t kMaxCoord = ((int64_t)1 << 31) - 64;
+    if (Lp > kMaxCoord || a.dim > kMaxCoord)
+        return fail(MSC_ERR_UNSUPPORTED, "the backward needs seqlen and dim below 2^31");
     const size_t es = a.bf16 ? 2 : 4;
     char* ws = static_cast<char*>(a.workspace);
     float* ckpt = reinterpret_cast<float*>(ws);

@@ -95,6 +95,11 @@ def test_bwd_rejects_bad_arguments(lib):
     assert st == msc.MSC_ERR_INVALID_ARG and "dz" in msc.msc_last_error()
     st = f(1, 4, 64, 16, 0, *ok, None, None, None, None, 16, 16, 16, 16, 16, None, None, None, None, 0, None)
     assert st == msc.MSC_ERR_INVALID_ARG and "dy" in msc.msc_last_error()
+    # rows of 2^31 steps do not fit the 32-bit TMA coordinates: refused before any device work
+    big = 1 << 31
+    ws = msc.msc_selective_scan_bwd_workspace_size(1, 4, big, 16)
+    st = f(1, 4, big, 16, 1, *ok, None, None, None, 16, 16, 16, 16, 16, 16, None, None, None, 4096, ws, None)
+    assert st == msc.MSC_ERR_UNSUPPORTED and "2^31" in msc.msc_last_error()
 
 
 def test_ssd_rejects_bad_arguments(lib):
