@@ -639,15 +639,23 @@ def test_planted_mistakes(tmp_path, desc, orig, mut, monkeypatch):
 
 
 PY_MUTATIONS = [
-    # (description, function, original text, mutated text) in oracle.py
-    ("conv bwd: taps not reversed", "causal_conv1d_bwd", "gp[:, :, K - 1 - k:K - 1 - k + L]", "gp[:, :, k:k + L]"),
+    # (description, function, original text, mutated text, pin) in oracle.py
+    ("conv bwd: taps not reversed", "causal_conv1d_bwd", "gp[:, :, K - 1 - k:K - 1 - k + L]", "gp[:, :, k:k + L]",
+     "p10"),
     ("conv bwd: silu derivative without its second term", "causal_conv1d_bwd",
-     "g = g * sg * (1.0 + pre * (1.0 - sg))", "g = g * sg"),
+     "g = g * sg * (1.0 + pre * (1.0 - sg))", "g = g * sg", "p10"),
+    ("ssd bwd: B of the first group for every group", "ssd_bwd",
+     "B[:, :, g, :].transpose(0, 2, 1), C[:, :, g, :]", "B[:, :, 0, :].transpose(0, 2, 1), C[:, :, g, :]", "p13"),
+    ("ssd bwd: ddelta from one channel of the head", "ssd_bwd",
+     'r["ddelta"][:, sl, :].sum(axis=1)', 'r["ddelta"][:, i * P, :]', "p13"),
+    ("ssd bwd: dA from one channel of the head", "ssd_bwd", 'r["dA"][sl].sum()', 'r["dA"][sl][0].sum()', "p13"),
+    ("ssd bwd: dx of the group's first head for every head", "ssd_bwd",
+     'r["du"][:, sl, :]', 'r["du"][:, :P, :]', "p13"),
 ]
 
 
-@pytest.mark.parametrize("desc,fn,orig,mut", PY_MUTATIONS, ids=[m[0] for m in PY_MUTATIONS])
-def test_planted_mistakes_python(desc, fn, orig, mut, monkeypatch):
+@pytest.mark.parametrize("desc,fn,orig,mut,pin", PY_MUTATIONS, ids=[m[0] for m in PY_MUTATIONS])
+def test_planted_mistakes_python(desc, fn, orig, mut, pin, monkeypatch):
     """Plant each mistake in a copy of a Python oracle function and check that
     its pin fails."""
     import inspect
@@ -658,4 +666,7 @@ def test_planted_mistakes_python(desc, fn, orig, mut, monkeypatch):
     exec(compile(src.replace(orig, mut, 1), "<planted>", "exec"), ns)
     monkeypatch.setattr(oracle, fn, ns[fn])
     with pytest.raises(AssertionError):
-        test_p10_conv1d_backward_finite_differences(4, True)
+        if pin == "p10":
+            test_p10_conv1d_backward_finite_differences(4, True)
+        else:
+            test_p13_ssd_backward_finite_differences()
