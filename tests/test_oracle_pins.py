@@ -651,7 +651,20 @@ PY_MUTATIONS = [
     ("ssd bwd: dA from one channel of the head", "ssd_bwd", 'r["dA"][sl].sum()', 'r["dA"][sl][0].sum()', "p13"),
     ("ssd bwd: dx of the group's first head for every head", "ssd_bwd",
      'r["du"][:, sl, :]', 'r["du"][:, :P, :]', "p13"),
+    ("conv: taps in reverse order", "causal_conv1d", "out += w[None, :, k, None] * xp[:, :, k:k + L]",
+     "out += w[None, :, K - 1 - k, None] * xp[:, :, k:k + L]", "p10_fwd"),
+    ("conv decode step: state not shifted", "causal_conv1d_update", "window[:, :, 1:]", "window[:, :, :-1]",
+     "p10_update"),
+    ("decode step: gate dropped", "s6_step", "z = None if z is None else _f64(z)[:, :, None]", "z = None", "p9"),
 ]
+
+PY_PINS = {
+    "p9": lambda: test_p9_decode_steps_equal_scan(True, True, True),
+    "p10": lambda: test_p10_conv1d_backward_finite_differences(4, True),
+    "p10_fwd": lambda: test_p10_conv1d_is_numpy_convolve(4),
+    "p10_update": lambda: test_p10_conv1d_update_chain_equals_sequence(),
+    "p13": lambda: test_p13_ssd_backward_finite_differences(),
+}
 
 
 @pytest.mark.parametrize("desc,fn,orig,mut,pin", PY_MUTATIONS, ids=[m[0] for m in PY_MUTATIONS])
@@ -666,7 +679,4 @@ def test_planted_mistakes_python(desc, fn, orig, mut, pin, monkeypatch):
     exec(compile(src.replace(orig, mut, 1), "<planted>", "exec"), ns)
     monkeypatch.setattr(oracle, fn, ns[fn])
     with pytest.raises(AssertionError):
-        if pin == "p10":
-            test_p10_conv1d_backward_finite_differences(4, True)
-        else:
-            test_p13_ssd_backward_finite_differences()
+        PY_PINS[pin]()
