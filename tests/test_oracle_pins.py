@@ -606,6 +606,14 @@ MUTATIONS = [
     ("trapezoid: previous term without decay", "in = 0.5 * (e + abar * eprev[n]);",
      "in = 0.5 * (e + eprev[n]);"),
     ("trapezoid: no halving", "in = 0.5 * (e + abar * eprev[n]);", "in = e + abar * eprev[n];"),
+    ("softplus: wrong sign inside log1p", "return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));",
+     "return (x > 0.0 ? x : 0.0) + log1p(exp(fabs(x)));"),
+    ("fwd: Delta_bias not added", "double dt = softplus_d(delta[t] + bias);\n        double acc = 0.0;",
+     "double dt = softplus_d(delta[t]);\n        double acc = 0.0;"),
+    ("bwd: ddelta without the softplus derivative", "ddelta[t] = dDelta * sigmoid_d(x);",
+     "ddelta[t] = dDelta;"),
+    ("bwd: dDelta without the decay term", "dDelta += l * (B[n * L + t] * u[t] + A[n] * abar * hprev);",
+     "dDelta += l * B[n * L + t] * u[t];"),
 ]
 
 
