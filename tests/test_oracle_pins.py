@@ -614,6 +614,9 @@ MUTATIONS = [
      "ddelta[t] = dDelta;"),
     ("bwd: dDelta without the decay term", "dDelta += l * (B[n * L + t] * u[t] + A[n] * abar * hprev);",
      "dDelta += l * B[n * L + t] * u[t];"),
+    ("ssd: heads mapped to groups round-robin", "g = h / hpg;", "g = h % ngroups;"),
+    ("ssd: every channel of a head driven by its first", "dt * xp * B[t * sb + n]", "dt * x[t * sx] * B[t * sb + n]"),
+    ("ssd: D feed-through dropped", "acc += D * xp;\n            if (z) {", "if (z) {"),
 ]
 
 
