@@ -238,3 +238,20 @@ def test_conv1d_bwd_rejects_bad_arguments(lib):
     assert call(K=9) == msc.MSC_ERR_UNSUPPORTED
     assert call(idt=3) == msc.MSC_ERR_INVALID_ARG
     assert call(batch=0) == msc.MSC_ERR_INVALID_ARG
+
+
+def test_binding_has_no_cpu_path(monkeypatch):
+    """The product path refuses host tensors (no CPU fallback) and raises when
+    the library has not been built."""
+    import torch
+    x = torch.zeros((1, 4, 16))
+    A = torch.zeros((4, 16))
+    Bm = torch.zeros((1, 16, 16))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        msc.msc_selective_scan_fwd(x, x, A, Bm, Bm)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        msc.msc_causal_conv1d_fwd(x, torch.zeros((4, 4)))
+    monkeypatch.setattr(msc, "_LIB_PATH", os.path.join(ROOT, "no_such_dir", "libmsc.so"))
+    monkeypatch.setattr(msc, "_lib", None)
+    with pytest.raises(RuntimeError, match="not found"):
+        msc.load_library()
