@@ -2,7 +2,8 @@
 """Benchmark of the Mamba selective scan on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--legs fwd_long,bwd,ssd|none]
+                    [--legs fwd_long,bwd,ssd,ssd_bwd,decode,conv1d,conv1d_bwd,conv_scan,disc|none]
+                    [--no-cpu-baseline]
 
 One step = one S6 forward of the Mamba-2.8B-layer workload (batch 8, d_inner
 5120, L 2048, N 16, bf16 u/delta/z/B/C, fp32 state and output, z-gate, D and
@@ -12,10 +13,13 @@ resident in HBM (503 MB of inputs + 336 MB of output per step, larger than the
 126 MB L2, so no L2 flush is needed between steps).
 
 Printed on rank 0: one JSON line with value, roofline (live CUDA-event timing of
-the kernel against HBM / SFU / FP32 peaks), e2e (host buffers through the public
-API), the CPU oracle baseline, clocks sampled during the timed region, and
-`legs` (the long-sequence forward, the backward and the SSD chunked forward,
-each timed the same way).  Under torchrun (N > 1) every rank runs an
+the kernel against HBM / SFU / FP32 peaks, with the committed ncu DRAM traffic
+of the kernel while its source is unchanged), e2e (host buffers through the
+public API), the CPU oracle baseline, clocks sampled during the timed region,
+and `legs` (the long-sequence forward, the backward, the SSD chunked forward
+and backward, the decode step, the conv1d front end forward and backward, the
+front end fused into the scan, and the ZOH / trapezoidal forms, each timed the
+same way with its own roofline).  Under torchrun (N > 1) every rank runs an
 independent replica (weak scaling, no collective in the data path).
 """
 from __future__ import annotations
