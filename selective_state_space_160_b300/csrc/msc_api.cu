@@ -153,17 +153,17 @@ msc_status msc_selective_scan_fwd_ex(int64_t batch, int64_t dim, int64_t seqlen,
     MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z"); MSC_OPT_PTR(delta_bias, "delta_bias");
     MSC_OPT_PTR(h0, "h0"); MSC_OPT_PTR(h_last, "h_last");
     S6Plan plan = s6_fwd_plan(batch, dim, seqlen, dstate);
-    if (plan.workspace > 0) {
-        if (workspace == nullptr || workspace_bytes < plan.workspace)
-            return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", plan.workspace,
-                        workspace ? workspace_bytes : (size_t)0);
+    if (plan.workspace_required && (workspace == nullptr || workspace_bytes < plan.workspace))
+        return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", plan.workspace,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (workspace != nullptr)
         MSC_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "workspace must be 256-byte aligned");
-    }
     S6FwdArgs a{};
     a.batch = batch; a.dim = dim; a.L = seqlen; a.N = (int)dstate; a.bf16 = in_dtype == MSC_BF16;
     a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C;
     a.A = A; a.D = D; a.delta_bias = delta_bias; a.h0 = h0; a.y = y; a.h_last = h_last;
     a.workspace = workspace;
+    a.workspace_bytes = workspace ? workspace_bytes : 0;
     a.disc = (int)disc;
     return s6_fwd_launch(a, plan, static_cast<cudaStream_t>(stream));
 }
@@ -187,17 +187,17 @@ msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqle
         return fail(MSC_ERR_UNSUPPORTED, "the fused conv front end needs seqlen a multiple of %d (got %lld)",
                     in_dtype == MSC_BF16 ? 8 : 4, (long long)seqlen);
     S6Plan plan = s6_fwd_plan(batch, dim, seqlen, dstate);
-    if (plan.workspace > 0) {
-        if (workspace == nullptr || workspace_bytes < plan.workspace)
-            return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", plan.workspace,
-                        workspace ? workspace_bytes : (size_t)0);
+    if (plan.workspace_required && (workspace == nullptr || workspace_bytes < plan.workspace))
+        return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", plan.workspace,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (workspace != nullptr)
         MSC_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "workspace must be 256-byte aligned");
-    }
     S6FwdArgs a{};
     a.batch = batch; a.dim = dim; a.L = seqlen; a.N = (int)dstate; a.bf16 = in_dtype == MSC_BF16;
     a.u = x; a.delta = delta; a.z = z; a.B = B; a.C = C;
     a.A = A; a.D = D; a.delta_bias = delta_bias; a.h0 = h0; a.y = y; a.h_last = h_last;
     a.workspace = workspace;
+    a.workspace_bytes = workspace ? workspace_bytes : 0;
     a.conv_w = conv_weight; a.conv_b = conv_bias; a.conv_k = (int)conv_width;
     return s6_fwd_launch(a, plan, static_cast<cudaStream_t>(stream));
 }

@@ -10,9 +10,13 @@
 namespace msc_host {
 
 struct S6Plan {
-    int G = 1;            // segments per row (1 = single launch)
+    int G = 1;            // independent segments per row (1: no segment pass)
     int64_t seg_len = 0;  // timesteps per segment
-    size_t workspace = 0; // bytes
+    int chunks = 1;       // chained chunks per row block (1: one item per row block)
+    int64_t chunk = 0;    // timesteps per chained chunk
+    size_t workspace = 0; // bytes the plan uses
+    bool workspace_required = false;  // segmented plans cannot run without it
+    size_t seg_state_off = 0, seg_dsum_off = 0, ctrl_off = 0, ctrl_bytes = 0, chain_state_off = 0, bc_off = 0;
 };
 
 S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
@@ -25,6 +29,7 @@ struct S6FwdArgs {
     const float *A, *D, *delta_bias, *h0;
     float *y, *h_last;
     void* workspace;
+    size_t workspace_bytes = 0;
     int disc = 0;  // msc_discretization
     // fused causal conv1d + SiLU front end: u holds its input x when conv_w is set
     const float* conv_w = nullptr;  // [dim, conv_k]

@@ -21,6 +21,7 @@
 
 #include "msc.h"
 #include "msc_common.cuh"
+#include "msc_internal.h"
 
 namespace {
 
@@ -38,7 +39,13 @@ extern "C" msc_status msc_selective_scan_fwd_noalloc(int64_t batch, int64_t dim,
                                                      const void* z, const float* delta_bias, const float* h0,
                                                      float* y, float* h_last, void* stream) {
     msc_host::clear_error();
-    const size_t need = msc_selective_scan_fwd_workspace_size(batch, dim, seqlen, dstate);
+    // Only the segment scratch of long sequences with few rows is required; the
+    // chained schedule's scratch is used when it fits and skipped when not.
+    size_t need = 0;
+    if (batch >= 1 && dim >= 1 && seqlen >= 1 && dstate >= 1 && dstate <= 16) {
+        const msc_host::S6Plan plan = msc_host::s6_fwd_plan(batch, dim, seqlen, dstate);
+        if (plan.workspace_required) need = plan.workspace;
+    }
     if (need > (size_t)MSC_STATIC_SCRATCH_BYTES)
         return msc_host::fail(MSC_ERR_WORKSPACE,
                               "this problem needs %zu bytes of scratch; the allocation-free entry point has %u",

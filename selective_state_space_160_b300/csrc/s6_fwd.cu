@@ -11,9 +11,9 @@
 // one lane owns one channel row and keeps all N (<= 16) fp32 states in
 // registers.  Per (t, n) this costs one MUFU ex2 (exp(Delta A) as
 // ex2(Delta * A log2 e)) and four FP32 ops -- no scan overhead at all.  Rows
-// give the parallelism (b * dim rows); a CTA is one warp owning 32 rows of one
-// batch entry, stepping through time in tiles of 64-byte rows (32 bf16 or 16
-// fp32 steps).
+// give the parallelism (b * dim rows); a CTA is 32 rows of one batch entry
+// (two lanes per row: 64 threads), stepping through time in tiles of 64-byte
+// rows (32 bf16 or 16 fp32 steps).
 //
 // Main kernel (s6_fwd_tma_kernel): one thread issues 3-D TMA tile loads of
 // u / delta / z (32 rows x one tile) and B / C (16 slots x one tile, shared by
@@ -30,6 +30,15 @@
 // they take the plain-load kernel (s6_fwd_rows_kernel), which stages each tile
 // with coalesced loads and computes the same way in scalar fp32.
 //
+// Enough rows to fill the GPU: the 32-row blocks run on persistent CTAs (at
+// most one per row block) that take (row block, chunk) items in chunk-major
+// order from a ticket counter.  Chunk c of a block starts from the state chunk
+// c - 1 left in the workspace, once that chunk's flag (release / acquire, a
+// bounded wait) says it is there; the predecessor was taken a full round of
+// tickets earlier, so it is normally finished.  A block's chunks thus run on
+// different SMs, which evens out the load that a fixed grid leaves uneven
+// (1280 blocks on 148 SMs: some schedulers hold five warps, the average 4.3).
+//
 // Few rows and a long sequence (b * dim too small to fill 148 SMs) split each
 // row into G segments: an aggregate pass computes, from a zero state, each
 // segment's end state and sum of Delta (segment decay exp(A sum Delta)); a tiny
@@ -38,6 +47,7 @@
 // the scan composition (a, b) o (a', b') = (a a', a' b + b') of the
 // associative parallel scan (study note: Blelloch's work-efficient scan).
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 
@@ -79,6 +89,15 @@ struct FwdParams {
     int conv_k;
     int64_t dim, L, seg_len;
     int N, G;
+    // chained schedule (full pass only): persistent CTAs take (row block, chunk)
+    // items from a ticket counter; chunk q > 0 starts from the state chunk q - 1
+    // left in chain_state once flags[block] says q chunks are done
+    unsigned long long* ctr;  // ticket counter (null: one item per CTA from blockIdx)
+    unsigned* flags;          // [chains] finished chunks per row block
+    float* chain_state;       // [batch * dim, 16]
+    unsigned* abort_word;     // set by a CTA whose wait ran out, so that the others stop waiting
+    int64_t chunk, nblk, chains, total_items;
+    int chained;
 };
 
 // Stage a [kRows x kT] tile of a [rows, L] tensor (rows d0.. of batch entry b),
@@ -301,6 +320,25 @@ __device__ __forceinline__ void record_timeout(unsigned int site) {
         g_s6_fwd_status[1] = site;
 }
 
+// Wait until *flag >= target (acquire), about one second at most by the global
+// timer; gives up early once another CTA of the launch has given up.
+__device__ __forceinline__ bool wait_flag_geq(const unsigned* flag, unsigned target, const volatile unsigned* abort) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v >= target) return true;
+        if (i >= 16) {
+            uint64_t t1;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+            if (i == 16) t0 = t1;
+            else if (t1 - t0 > 1000000000ull) return false;
+            if (abort && *abort != 0u) return false;
+            __nanosleep(128);
+        }
+    }
+}
+
 constexpr int kStages = 2;
 constexpr int kRowTile = 2048;               // bytes of one 32-row x 64-byte tile
 constexpr int kBCTile = 1024;                // bytes of one 16-slot x 64-byte tile
@@ -379,15 +417,62 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
     const int r = tid / kNG;          // row within the CTA
     const int j = lane & (kNG - 1);   // position within the row's lane group
     const int glane0 = lane & ~(kNG - 1);
-    const int64_t b = blockIdx.y;
-    const int64_t d0 = (int64_t)blockIdx.x * kRows;
+    const int N = p.N;
+    const bool has_z = kFull && p.z != nullptr;
+    __shared__ long long s_ticket;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) msc::mbar_init(&s_full[s], 1);
+        msc::fence_barrier_init();
+        msc::prefetch_tmap(&tm_u);
+        msc::prefetch_tmap(&tm_d);
+        msc::prefetch_tmap(&tm_B);
+        if (has_z) msc::prefetch_tmap(&tm_z);
+        if (kFull) msc::prefetch_tmap(&tm_C);
+    }
+    __syncthreads();
+
+    // Items: one per CTA from blockIdx (row block, batch entry, segment), or,
+    // with a ticket counter, (row block, chunk) items taken in order until none
+    // are left.  tbase counts the tiles earlier items took through the stage ring.
+    uint32_t tbase = 0;
+    for (;;) {
+    int64_t b, d0, chain = 0, t_begin, t_end;
+    int seg;
+    if (p.ctr) {
+        if (tid == 0) s_ticket = (long long)atomicAdd(p.ctr, 1ull);
+        __syncthreads();
+        const long long item = s_ticket;
+        if (item >= p.total_items) break;
+        chain = item % p.chains;
+        seg = (int)(item / p.chains);
+        b = chain / p.nblk;
+        d0 = (chain % p.nblk) * kRows;
+        t_begin = (int64_t)seg * p.chunk;
+        t_end = imin64(p.L, t_begin + p.chunk);
+    } else {
+        b = blockIdx.y;
+        d0 = (int64_t)blockIdx.x * kRows;
+        seg = blockIdx.z;
+        t_begin = (int64_t)seg * p.seg_len;
+        t_end = imin64(p.L, t_begin + p.seg_len);
+    }
+    const bool chained_in = p.ctr && p.chained && seg > 0;  // starts from the previous chunk's state
+    if (chained_in) {
+        bool ok = true;
+        if (tid == 0) ok = wait_flag_geq(&p.flags[chain], (unsigned)seg, p.abort_word);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                record_timeout(3);
+                atomicExch(p.abort_word, 1u);
+            }
+            return;
+        }
+    }
     const int nrows = (int)imin64(kRows, p.dim - d0);
     const bool row_ok = r < nrows;
     const int64_t d = row_ok ? d0 + r : d0;
     const int64_t row = b * p.dim + d;
-    const int seg = blockIdx.z;
-    const int N = p.N;
-    const bool has_z = kFull && p.z != nullptr;
 
     uint64_t A2p[kPPL], h2[kPPL];
 #pragma unroll
@@ -399,9 +484,11 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
             a[e] = (row_ok && n < N) ? __ldg(p.A + d * N + n) * MSC_LOG2E : 0.f;
             h[e] = 0.f;
             if (kFull && row_ok && n < N) {
-                if (p.G > 1)
+                if (chained_in)
+                    h[e] = __ldcg(p.chain_state + row * 16 + n);
+                else if (p.G > 1)
                     h[e] = p.seg_state[((size_t)row * p.G + seg) * N + n];
-                else if (p.h0)
+                else if (p.h0 && seg == 0)
                     h[e] = __ldg(p.h0 + row * N + n);
             }
         }
@@ -412,7 +499,6 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
     const float bias = (p.delta_bias && row_ok) ? __ldg(p.delta_bias + d) : 0.f;
     float dsum = 0.f;
 
-    const int64_t t_begin = (int64_t)seg * p.seg_len;
     // fused conv: taps right-aligned in a 4-tap window (cw[m] multiplies x_{t-3+m}),
     // as packed pairs; xprev = x of the three steps before this lane's group (kept by
     // the second lane of the row: its last three steps)
@@ -467,32 +553,20 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
             ep2[q] = msc::pk2(e[0], e[1]);
         }
     }
-    const int64_t t_end = imin64(p.L, t_begin + p.seg_len);
     const int ntiles = (int)((t_end - t_begin + kTT - 1) / kTT);
     const uint32_t tx_bytes = kRowTile * (has_z ? 3 : 2) + kBCTile * (kFull ? 2 : 1);
 
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) msc::mbar_init(&s_full[s], 1);
-        msc::fence_barrier_init();
-        msc::prefetch_tmap(&tm_u);
-        msc::prefetch_tmap(&tm_d);
-        msc::prefetch_tmap(&tm_B);
-        if (has_z) msc::prefetch_tmap(&tm_z);
-        if (kFull) msc::prefetch_tmap(&tm_C);
-    }
-    __syncthreads();
-
     if (tid == 0)
         for (int jt = 0; jt < kStages && jt < ntiles; ++jt)
-            issue_tile(jt, t_begin + (int64_t)jt * kTT, s_raw[jt % kStages], &s_full[jt % kStages], tx_bytes,
-                       &tm_u, &tm_d, &tm_z, &tm_B, &tm_C, d0, b, has_z, kFull);
+            issue_tile(jt, t_begin + (int64_t)jt * kTT, s_raw[(tbase + jt) % kStages], &s_full[(tbase + jt) % kStages],
+                       tx_bytes, &tm_u, &tm_d, &tm_z, &tm_B, &tm_C, d0, b, has_z, kFull);
     int issued = ntiles < kStages ? ntiles : kStages;
 
     bool failed = false;
     int i = 0;
     for (; i < ntiles; ++i) {
-        const int st = i % kStages;
-        const bool ok = msc::wait_bounded(&s_full[st], (uint32_t)((i / kStages) & 1));
+        const int st = (tbase + i) % kStages;
+        const bool ok = msc::wait_bounded(&s_full[st], (uint32_t)(((tbase + i) / kStages) & 1), p.abort_word);
         // every thread takes the same branch, so no thread is left at a barrier
         if (__syncthreads_or(!ok)) {
             if (tid == 0) record_timeout(1);
@@ -624,8 +698,13 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int src = glane0 | (k / kSPG);
-                dts[k] = __shfl_sync(0xffffffffu, mdt[k % kSPG], src);
-                dtus[k] = __shfl_sync(0xffffffffu, mdtu[k % kSPG], src);
+                if constexpr (kNG == 1) {
+                    dts[k] = mdt[k];
+                    dtus[k] = mdtu[k];
+                } else {
+                    dts[k] = __shfl_sync(0xffffffffu, mdt[k % kSPG], src);
+                    dtus[k] = __shfl_sync(0xffffffffu, mdtu[k % kSPG], src);
+                }
             }
             if (kMode == kModeCkpt && row_ok) {
                 // state entering this 8-step group, for the recomputing backward
@@ -710,7 +789,7 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
                     v[k] = lo + hi;
                 }
                 // reduce-scatter over the group: lane j ends with steps j*kSPG ..
-                reduce_scatter_level<kNG / 2, 8>(v, j);
+                if constexpr (kNG > 1) reduce_scatter_level<kNG / 2, 8>(v, j);
                 if constexpr (kNG == 4) reduce_scatter_level<1, 4>(v, j);
                 uint64_t y2[kSPG / 2];
 #pragma unroll
@@ -750,17 +829,21 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
             }
         }
         __syncthreads();
-        if (tid == 0 && issued < ntiles)
-            issue_tile(issued, t_begin + (int64_t)issued * kTT, s_raw[issued % kStages], &s_full[issued % kStages],
-                       tx_bytes, &tm_u, &tm_d, &tm_z, &tm_B, &tm_C, d0, b, has_z, kFull);
+        if (tid == 0 && issued < ntiles) {
+            const uint32_t si = (tbase + issued) % kStages;
+            issue_tile(issued, t_begin + (int64_t)issued * kTT, s_raw[si], &s_full[si], tx_bytes, &tm_u, &tm_d,
+                       &tm_z, &tm_B, &tm_C, d0, b, has_z, kFull);
+        }
         ++issued;
     }
 
     if (failed) {
         // drain loads still in flight before the shared memory is released
-        if (tid == 0)
+        if (tid == 0) {
+            if (p.abort_word) atomicExch(p.abort_word, 1u);
             for (int jt = i; jt < issued && jt < ntiles; ++jt)
-                (void)msc::wait_bounded(&s_full[jt % kStages], (uint32_t)((jt / kStages) & 1));
+                (void)msc::wait_bounded(&s_full[(tbase + jt) % kStages], (uint32_t)(((tbase + jt) / kStages) & 1));
+        }
         return;
     }
     if (kMode == kModeCkpt) return;
@@ -768,23 +851,36 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
 #pragma unroll
         for (int sl = 1; sl < kNG; sl *= 2) dsum += __shfl_xor_sync(0xffffffffu, dsum, sl);
     }
-    if (!row_ok) return;
+    // a chained chunk that is not the row's last hands its state to the next chunk
+    const bool publish = kFull && p.ctr && p.chained && t_end < p.L;
+    if (row_ok) {
 #pragma unroll
-    for (int q = 0; q < kPPL; ++q) {
-        float v0, v1;
-        msc::upk2(h2[q], v0, v1);
-        const int n = 2 * (kPPL * j + q);
-        if (kFull) {
-            if (p.h_last && seg == p.G - 1) {
-                if (n < N) p.h_last[row * N + n] = v0;
-                if (n + 1 < N) p.h_last[row * N + n + 1] = v1;
+        for (int q = 0; q < kPPL; ++q) {
+            float v0, v1;
+            msc::upk2(h2[q], v0, v1);
+            const int n = 2 * (kPPL * j + q);
+            if (kFull) {
+                if (publish) {
+                    *reinterpret_cast<uint64_t*>(p.chain_state + row * 16 + n) = h2[q];
+                } else if (p.h_last && t_end == p.L) {
+                    if (n < N) p.h_last[row * N + n] = v0;
+                    if (n + 1 < N) p.h_last[row * N + n + 1] = v1;
+                }
+            } else {
+                if (n < N) p.seg_state[((size_t)row * p.G + seg) * N + n] = v0;
+                if (n + 1 < N) p.seg_state[((size_t)row * p.G + seg) * N + n + 1] = v1;
             }
-        } else {
-            if (n < N) p.seg_state[((size_t)row * p.G + seg) * N + n] = v0;
-            if (n + 1 < N) p.seg_state[((size_t)row * p.G + seg) * N + n + 1] = v1;
         }
+        if (!kFull && j == 0) p.seg_dsum[(size_t)row * p.G + seg] = dsum;
     }
-    if (!kFull && j == 0) p.seg_dsum[(size_t)row * p.G + seg] = dsum;
+    if (!p.ctr) break;
+    tbase += (uint32_t)ntiles;
+    __syncthreads();  // this item's state is stored (and s_ticket may be rewritten)
+    if (tid == 0 && publish) {
+        __threadfence();
+        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&p.flags[chain]), "r"((unsigned)(seg + 1)) : "memory");
+    }
+    }  // items
 }
 
 // Chains the segment aggregates of every (row, n): carry_0 = h0 (or 0),
@@ -802,9 +898,14 @@ __global__ void s6_seg_carry_kernel(const float* __restrict__ A, const float* __
     float h = h0 ? __ldg(h0 + row * N + n) : 0.f;
     for (int g = 0; g < G; ++g) {
         const size_t i = ((size_t)row * G + g) * N + n;
-        const float agg = seg_state[i];
-        seg_state[i] = h;
-        if (g + 1 < G) h = fmaf(msc::ex2_approx(a2 * seg_dsum[(size_t)row * G + g]), h, agg);
+        // the aggregate pass writes segments 0 .. G-2; the last slot only receives its carry
+        if (g + 1 < G) {
+            const float agg = seg_state[i];
+            seg_state[i] = h;
+            h = fmaf(msc::ex2_approx(a2 * seg_dsum[(size_t)row * G + g]), h, agg);
+        } else {
+            seg_state[i] = h;
+        }
     }
 }
 
@@ -846,10 +947,34 @@ bool make_maps(FwdMaps& m, const FwdParams& p, int64_t batch, bool bf16) {
 // warps but add more exchange work than the extra latency hiding recovers.
 constexpr int kLanesPerRow = 2;
 
+// Resident CTAs per SM of a kernel instance, once per device.
+template <typename K>
+int resident_ctas(K kernel, int threads) {
+    static std::atomic<uint64_t> known{0};
+    static std::atomic<int> per_sm[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = msc_host::device_bit();
+    if (!(known.load() & bit)) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
+        per_sm[dev & 63] = n;
+        known |= bit;
+    }
+    return per_sm[dev & 63].load();
+}
+
 template <bool kBF16, int kNG, int kDisc = kDiscEuler, bool kConv = false>
 msc_status launch_tma_ng(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
-    if (mode == kModeFull)
+    if (mode == kModeFull && p.ctr) {
+        // persistent: at most one CTA per row block, so that the chunk before a
+        // ticket's chunk was taken a full round earlier and is normally done
+        auto kern = s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc, kConv>;
+        const int64_t slots = (int64_t)resident_ctas(kern, 32 * kNG) * msc_host::num_sms();
+        const int64_t n = std::min<int64_t>(slots, std::min<int64_t>(p.chains, p.total_items));
+        kern<<<(unsigned)n, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    } else if (mode == kModeFull)
         s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc, kConv><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
     else if (mode == kModeAgg)
         s6_fwd_tma_kernel<kBF16, kModeAgg, kNG, kDisc, kConv><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
@@ -866,7 +991,7 @@ msc_status launch_tma(const FwdMaps& m, const FwdParams& p, int64_t batch, int G
     if (p.conv_w) {
         if (disc != kDiscEuler)
             return msc_host::fail(MSC_ERR_UNSUPPORTED, "the fused conv front end runs with the exponential-Euler form");
-        return launch_tma_ng<kBF16, kLanesPerRow, kDiscEuler, true>(m, p, batch, G, mode, st);
+        return launch_tma_ng<kBF16, 2, kDiscEuler, true>(m, p, batch, G, mode, st);
     }
     if (disc == kDiscZoh) return launch_tma_ng<kBF16, kLanesPerRow, kDiscZoh>(m, p, batch, G, mode, st);
     if (disc == kDiscTrap) return launch_tma_ng<kBF16, kLanesPerRow, kDiscTrap>(m, p, batch, G, mode, st);
@@ -906,29 +1031,78 @@ msc_status launch_mode(const FwdParams& p, const FwdMaps* maps, bool bf16, bool 
 
 namespace msc_host {
 
+namespace {
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+// Work plan of the forward.  A CTA of the two-lane kernel runs 32 channel rows
+// ("row block"); about ten are resident per SM (64 threads, 96 registers,
+// 21 KB of shared memory).
+//  - Enough row blocks to fill the GPU: one pass.  Sequences of 512 steps or
+//    more are cut into chained chunks (at least 256 steps, at most 4 per row)
+//    taken by persistent CTAs in order, so that a row block's work moves
+//    between SMs at chunk boundaries and the SMs that hold more warps do not
+//    set the time.  Its workspace (ticket counter, flags, the state handed from
+//    chunk to chunk) is optional: without it the pass runs one CTA per row block.
+//  - Few row blocks and a long sequence: independent segments (aggregate pass,
+//    carry pass, full pass), the number chosen by the cost of the busiest CTA
+//    in steps, the aggregate pass counted at 3/4 of the full pass per step.
+//    Its workspace is required.
 S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
+    // Chunks per row and their least length: each item restarts the CTA's TMA
+    // pipeline (a few microseconds), so that 4 chunks of 512 steps balance the
+    // batch-8 x 5120 x 2048 workload as well as 8 of 256 (0.412 vs 0.414 ms on a
+    // B300) and better than 16 of 128 (0.443 ms).
+    constexpr int64_t kMaxChunks = 4, kMinChunk = 256;
     S6Plan plan;
     const int64_t rows = batch * dim;
-    // Enough rows to keep every SM busy with ~8 resident warps: one pass.
-    const int64_t target = (int64_t)num_sms() * 8 * 32;
-    int64_t G = 1;
-    if (rows < target) G = (target + rows - 1) / rows;
-    const int64_t min_seg = 512;
-    G = std::min<int64_t>(G, std::max<int64_t>(1, seqlen / min_seg));
-    G = std::min<int64_t>(G, 65535);
-    if (G <= 1) {
-        plan.G = 1;
-        plan.seg_len = seqlen;
-        plan.workspace = 0;
+    const int64_t chains = batch * cdiv64(dim, kRows);
+    const int64_t W = 10 * (int64_t)num_sms();
+    plan.G = 1;
+    plan.seg_len = seqlen;
+    plan.chunks = 1;
+    plan.chunk = seqlen;
+    if (chains * 2 >= W) {
+        if (seqlen >= 512) {
+            const int64_t chunk = std::max<int64_t>(kMinChunk, cdiv64(cdiv64(seqlen, kMaxChunks), kT) * kT);
+            plan.chunk = chunk;
+            plan.chunks = (int)cdiv64(seqlen, chunk);
+        }
+        if (plan.chunks > 1) {
+            plan.ctrl_off = 0;
+            plan.ctrl_bytes = align256(256 + (size_t)chains * sizeof(unsigned));
+            plan.chain_state_off = plan.ctrl_bytes;
+            plan.workspace = plan.chain_state_off + (size_t)rows * 16 * sizeof(float);
+            plan.workspace_required = false;
+        }
         return plan;
     }
-    int64_t seg = (seqlen + G - 1) / G;
-    seg = (seg + kT - 1) / kT * kT;
-    G = (seqlen + seg - 1) / seg;
-    plan.G = (int)G;
-    plan.seg_len = seg;
-    plan.workspace = (size_t)rows * G * (size_t)dstate * sizeof(float) +
-                     (size_t)rows * G * sizeof(float) + 256;
+    const double ovh = 16.0;  // steps' worth of per-CTA start-up
+    double best = (double)cdiv64(chains, W) * ((double)seqlen + ovh);
+    int bestG = 1;
+    int64_t best_seg = seqlen;
+    const int64_t max_G = std::min<int64_t>({(int64_t)65535, seqlen / 256, 64 * W / chains + 1});
+    for (int64_t G = 2; G <= max_G; ++G) {
+        const int64_t seg = cdiv64(cdiv64(seqlen, G), kT) * kT;
+        const int64_t Gc = cdiv64(seqlen, seg);
+        if (Gc < 2) continue;
+        const double per = (double)seg + ovh;
+        const double cost = 0.75 * (double)cdiv64(chains * (Gc - 1), W) * per + (double)cdiv64(chains * Gc, W) * per;
+        if (cost < best) {
+            best = cost;
+            bestG = (int)Gc;
+            best_seg = seg;
+        }
+    }
+    if (bestG > 1) {
+        plan.G = bestG;
+        plan.seg_len = best_seg;
+        plan.seg_state_off = 0;
+        plan.seg_dsum_off = align256((size_t)rows * bestG * (size_t)dstate * sizeof(float));
+        plan.workspace = plan.seg_dsum_off + (size_t)rows * bestG * sizeof(float);
+        plan.workspace_required = true;
+    }
     return plan;
 }
 
@@ -939,6 +1113,7 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
     p.y = a.y; p.h_last = a.h_last;
     p.dim = a.dim; p.L = a.L; p.N = a.N; p.G = plan.G; p.seg_len = plan.seg_len;
     p.conv_w = a.conv_w; p.conv_b = a.conv_b; p.conv_k = a.conv_k;
+    char* ws = static_cast<char*>(a.workspace);
     // 16-byte vector loads need every row and tile start 16-byte aligned:
     // bases are checked by the caller; rows start at row * L elements.
     const bool vec = (a.L % 8) == 0;
@@ -952,11 +1127,8 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
         mp = &maps;
     }
     if (plan.G > 1) {
-        char* ws = static_cast<char*>(a.workspace);
-        p.seg_state = reinterpret_cast<float*>(ws);
-        size_t off = (size_t)(a.batch * a.dim) * plan.G * a.N * sizeof(float);
-        off = (off + 255) / 256 * 256;
-        p.seg_dsum = reinterpret_cast<float*>(ws + off);
+        p.seg_state = reinterpret_cast<float*>(ws + plan.seg_state_off);
+        p.seg_dsum = reinterpret_cast<float*>(ws + plan.seg_dsum_off);
         msc_status s = launch_mode(p, mp, a.bf16, vec, a.batch, plan.G - 1, kModeAgg, a.disc, st);
         if (s != MSC_OK) return s;
         const int64_t total = a.batch * a.dim * a.N;
@@ -965,6 +1137,21 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
             a.A, a.h0, p.seg_state, p.seg_dsum, a.batch * a.dim, a.dim, a.N, plan.G);
         s = check_launch("s6_seg_carry");
         if (s != MSC_OK) return s;
+    } else if (plan.chunks > 1 && mp && ws && a.workspace_bytes >= plan.workspace) {
+        // chained chunks on persistent CTAs (TMA path only); the control block
+        // (ticket counter at 0, abort word at 16, flags from 256) starts at zero
+        unsigned char* ctrl = reinterpret_cast<unsigned char*>(ws + plan.ctrl_off);
+        const cudaError_t e = cudaMemsetAsync(ctrl, 0, plan.ctrl_bytes, st);
+        if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "workspace clear: %s", cudaGetErrorString(e));
+        p.ctr = reinterpret_cast<unsigned long long*>(ctrl);
+        p.abort_word = reinterpret_cast<unsigned*>(ctrl + 16);
+        p.flags = reinterpret_cast<unsigned*>(ctrl + 256);
+        p.chain_state = reinterpret_cast<float*>(ws + plan.chain_state_off);
+        p.chunk = plan.chunk;
+        p.nblk = cdiv64(a.dim, kRows);
+        p.chains = a.batch * p.nblk;
+        p.total_items = p.chains * plan.chunks;
+        p.chained = 1;
     }
     return launch_mode(p, mp, a.bf16, vec, a.batch, plan.G, kModeFull, a.disc, st);
 }
@@ -984,8 +1171,8 @@ msc_status s6_fwd_checkpoints(const S6FwdArgs& a, float* ckpt, cudaStream_t st) 
         return fail(MSC_ERR_UNSUPPORTED, "checkpoint pass needs a 16-byte row stride and seqlen, dim below 2^31");
     FwdMaps maps;
     if (!make_maps(maps, p, a.batch, a.bf16)) return MSC_ERR_CUDA;
-    return a.bf16 ? launch_tma_ng<true, kLanesPerRow>(maps, p, a.batch, 1, kModeCkpt, st)
-                  : launch_tma_ng<false, kLanesPerRow>(maps, p, a.batch, 1, kModeCkpt, st);
+    return a.bf16 ? launch_tma_ng<true, 2>(maps, p, a.batch, 1, kModeCkpt, st)
+                  : launch_tma_ng<false, 2>(maps, p, a.batch, 1, kModeCkpt, st);
 }
 
 // Reads and clears this module's device status word.

@@ -75,8 +75,13 @@ def test_fwd_rejects_bad_arguments(lib):
 
 
 def test_fwd_workspace_query_and_check(lib):
-    # plenty of rows: single pass, no workspace
-    assert msc.msc_selective_scan_fwd_workspace_size(8, 5120, 2048, 16) == 0
+    # plenty of rows: the chained schedule's state hand-over (optional: without it
+    # one CTA per row block) -- 40960 rows x 16 states x 4 B, plus a 256-byte
+    # control block and one 4-byte flag per 32-row block
+    need = msc.msc_selective_scan_fwd_workspace_size(8, 5120, 2048, 16)
+    assert 40960 * 16 * 4 + 256 + 1280 * 4 <= need <= 40960 * 16 * 4 + 256 + 1280 * 4 + 256
+    # a short sequence with one row block: one item, no workspace
+    assert msc.msc_selective_scan_fwd_workspace_size(1, 64, 256, 16) == 0
     # few rows and a long sequence: segments need a workspace
     need = msc.msc_selective_scan_fwd_workspace_size(1, 1536, 1 << 20, 16)
     assert need > 0
