@@ -12,14 +12,15 @@ kernel launch.  Metric: elements (batch * D * L) per second.  Inputs are
 resident in HBM (503 MB of inputs + 336 MB of output per step, larger than the
 126 MB L2, so no L2 flush is needed between steps).
 
-Printed on rank 0: one JSON line with value, roofline (live CUDA-event timing of
-the kernel against HBM / SFU / FP32 peaks, with the committed ncu DRAM traffic
-of the kernel while its source is unchanged), e2e (host buffers through the
-public API), the CPU oracle baseline, clocks sampled during the timed region,
-and `legs` (the long-sequence forward, the backward, the SSD chunked forward
-and backward, the decode step, the conv1d front end forward and backward, the
-front end fused into the scan, and the ZOH / trapezoidal forms, each timed the
-same way with its own roofline).  Under torchrun (N > 1) every rank runs an
+Printed on rank 0: first one JSON line per leg ({"leg": name, ...}: the
+long-sequence forward, the backward, the SSD chunked forward and backward, the
+decode step, the conv1d front end forward and backward, the front end fused
+into the scan, and the ZOH / trapezoidal forms, each timed the same way with
+its own roofline), then the headline line, last: value, roofline (live
+CUDA-event timing of the kernel against HBM / SFU / FP32 peaks, with the
+committed ncu DRAM traffic of the kernel while its source is unchanged), e2e
+(host buffers through the public API), the CPU oracle baseline, clocks sampled
+during the timed region, and a summary of the legs (ms, bound, fraction).  Under torchrun (N > 1) every rank runs an
 independent replica (weak scaling, no collective in the data path).
 """
 from __future__ import annotations
@@ -86,7 +87,7 @@ def _pipe_peaks():
     """Measured MUFU ex2 / FFMA / FFMA2 throughput of this GPU (probe library)."""
     import ctypes
     from selective_state_space_160_b300 import build as b
-    lib = ctypes.CDLL(b.build_probe())
+    lib = ctypes.CDLL(b.build_pipe_peaks())
     res = (ctypes.c_float * 16)()
     rc = lib.msc_probe_pipe_peaks(res, 4096)
     if rc != 0:
@@ -240,7 +241,7 @@ def roofline_s6(elements, N, bytes_per_launch, ms, peaks, pipes, exps_per_elem_n
     terms = {
         "hbm": {"achieved": hbm, "peak": peaks["hbm_gbs"], "unit": "GB/s"},
         "sfu": {"achieved": exps / t / 1e9, "peak": pipes["ex2"]["ops_per_s"] / 1e9, "unit": "Gex2/s"},
-        "fp32": {"achieved": fp32 / t / 1e9, "peak": pipes["ffma2"]["ops_per_s"] / 1e9, "unit": "Gflop32/s"},
+        "fp32": {"achieved": fp32 / t / 1e9, "peak": pipes["ffma2"]["ops_per_s"] / 1e9, "unit": "G fp32 lane-ops/s"},
     }
     for v in terms.values():
         v["frac"] = v["achieved"] / v["peak"]
@@ -253,6 +254,23 @@ def roofline_s6(elements, N, bytes_per_launch, ms, peaks, pipes, exps_per_elem_n
            "terms": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                      for k, v in terms.items()},
            "hbm_frac_nominal_8tbs": hbm / 8000.0, "peak_source": peaks["source"]}
+    return out
+
+
+def _leg_summary(res):
+    """ms, rate and roofline fraction of a leg (the full record is its own line)."""
+    if "error" in res:
+        return {"error": res["error"]}
+    out = {}
+    for k, v in res.items():
+        if isinstance(v, dict) and "roofline" in v:  # legs with sub-workloads
+            out[k] = _leg_summary(v)
+    if "ms" in res:
+        out["ms"] = round(res["ms"], 4)
+    roof = res.get("roofline")
+    if roof:
+        out["bound"] = roof.get("bound")
+        out["frac"] = round(roof.get("frac", 0.0), 4)
     return out
 
 
@@ -570,9 +588,11 @@ def leg_ssd_bwd(peaks, pipes, steps=5, warmup=2):
     t = ms * 1e-3
     macs = ssd_bwd_macs(b, L, H, 1, Q, P, N)
     nst = b * (L // Q) * H * P * N * 4
-    # inputs x, dy, delta, B, C (bf16) read; dx, ddelta, dB, dC (fp32) written;
-    # S, Hin, U/dS written once and read back
-    nbytes = 2 * el * 2 + b * L * H * 2 + 2 * b * L * N * 2 + el * 4 + b * L * H * 4 + 2 * b * L * N * 4 + 6 * nst
+    # algorithmic: inputs x, dy, delta, B, C (bf16) read once; dx, ddelta, dB, dC
+    # (fp32) written once.  The chunk states S, Hin and U/dS that the kernels write
+    # to the workspace and read back are scratch traffic, reported apart.
+    nbytes = 2 * el * 2 + b * L * H * 2 + 2 * b * L * N * 2 + el * 4 + b * L * H * 4 + 2 * b * L * N * 4
+    scratch = 6 * nst
     # the products run on tcgen05 (bf16 operands, fp32 operands as hi + lo pairs):
     # algorithmic flops = 2 x the multiply-adds above, against the dense bf16 peak
     ten = {"achieved": 2.0 * macs / t / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
@@ -584,6 +604,7 @@ def leg_ssd_bwd(peaks, pipes, steps=5, warmup=2):
            "elements_per_s": el / t, "ms": ms,
            "roofline": {"bound": "tensor" if sel is ten else "hbm", "achieved": sel["achieved"], "peak": sel["peak"],
                         "unit": sel["unit"], "frac": sel["frac"], "traffic": None, "macs": macs,
+                        "algorithmic_bytes": nbytes, "workspace_bytes_moved": scratch,
                         "terms": {"tensor": ten, "hbm": hbm}}}
     del d, ws
     torch.cuda.empty_cache()
@@ -673,11 +694,18 @@ def run_ours(args):
     inp = s6_fwd_workload(b, dim, L, N, True, 160_001 + 1000 * rank)
     y = torch.empty((b, dim, L), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
-    launches_per_step = 1 if msc.msc_selective_scan_fwd_workspace_size(b, dim, L, N) == 0 else 3
+    # the chained schedule's workspace (ticket counter, flags, hand-over states),
+    # allocated once; each call clears its control block with one memset and
+    # launches one kernel
+    wsz = msc.msc_selective_scan_fwd_workspace_size(b, dim, L, N)
+    ws_buf = torch.empty(wsz + 256, dtype=torch.uint8, device="cuda")
+    ws_off = (-ws_buf.data_ptr()) % 256
+    fwd_ws = ws_buf[ws_off:ws_off + wsz]
+    launches_per_step = 1
 
     def step():
         msc.msc_selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
-                                   inp["z"], inp["delta_bias"], y=y)
+                                   inp["z"], inp["delta_bias"], y=y, workspace=fwd_ws)
 
     for _ in range(args.warmup):
         step()
@@ -713,20 +741,24 @@ def run_ours(args):
     el = b * dim * L
     value = whole_job_rate(el, args.steps, ws, total_ms)
 
-    # end to end through the public API with host buffers: H2D of this step's
-    # inputs from pinned memory, the call, D2H of y
+    # end to end through the C ABI with HOST buffers (msc_selective_scan_fwd_host):
+    # every step uploads its inputs from pinned memory, scans and downloads y,
+    # two batch entries at a time on three streams so that the copies overlap
+    # the scan; the device staging is allocated once
     host = {k: (inp[k].cpu().pin_memory() if inp[k] is not None else None) for k in ("u", "delta", "z", "B", "C")}
-    dev_in = {k: torch.empty_like(inp[k]) for k in host}
     yh = torch.empty((b, dim, L), dtype=torch.float32).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = yh.numel() * 4
+    e2e_chunk = 2
+    lib = msc.load_library()
+    st_bytes = lib.msc_selective_scan_fwd_host_staging_size(b, dim, L, N, 1, 1, e2e_chunk)
+    st_buf = torch.empty(st_bytes + 256, dtype=torch.uint8, device="cuda")
+    st_off = (-st_buf.data_ptr()) % 256
+    staging = st_buf[st_off:st_off + st_bytes]
 
     def e2e_step():
-        for k in host:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        msc.msc_selective_scan_fwd(dev_in["u"], dev_in["delta"], inp["A"], dev_in["B"], dev_in["C"], inp["D"],
-                                   dev_in["z"], inp["delta_bias"], y=y)
-        yh.copy_(y, non_blocking=True)
+        msc.msc_selective_scan_fwd_host(host["u"], host["delta"], inp["A"], host["B"], host["C"], inp["D"],
+                                        host["z"], inp["delta_bias"], y=yh, chunk_batch=e2e_chunk, staging=staging)
 
     e2e_steps = max(2, min(args.steps, 10))
     for _ in range(2):
@@ -741,7 +773,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(s2.elapsed_time(e2), ws)
     e2e_value = whole_job_rate(el, e2e_steps, ws, e2e_ms)
-    del host, dev_in, yh
+    del host, yh, staging, st_buf
 
     src = os.path.join(ROOT, "selective_state_space_160_b300", "csrc", "s6_fwd.cu")
     nbytes = el * (2 + 2 + 2 + 4) + 2 * b * N * L * 2
@@ -757,6 +789,8 @@ def run_ours(args):
                 legs[name] = fn(peaks, pipes)
             except Exception as ex:  # report, do not hide: a failing leg is printed as such
                 legs[name] = {"error": "%s: %s" % (type(ex).__name__, ex)}
+            # each leg on its own line, before the headline line
+            print(json.dumps({"leg": name, **legs[name]}), flush=True)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -773,13 +807,16 @@ def run_ours(args):
                        "l2": "inputs (503 MB) + outputs (336 MB) per step exceed the 126 MB L2; no flush"},
             "roofline": roof,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "msc_selective_scan_fwd_host (C ABI, pinned host buffers, 2 batch entries per chunk, "
+                            "upload / scan / download overlapped on three streams)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": dict(clk.summary(), note="sampled every 100 ms while the step ran back to back "
                                                  "before, during and after the timed region"),
             "pipe_peaks": {k: {"per_sm_clk": round(v["per_sm_clk"], 2), "ops_per_s": v["ops_per_s"]}
                            for k, v in pipes.items()},
-            "legs": legs,
+            # one line per leg is printed above; here only the summary
+            "legs": {k: _leg_summary(v) for k, v in legs.items()},
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -1,4 +1,4 @@
-// pipe_peaks.cu -- measurement probe, not part of the libmsc boundary.
+// bench_pipe_peaks.cu -- measurement probe for bench.py, not part of libmsc.
 //
 // Measures the per-SM throughput of the pipes the S6 scan is bound by, on the
 // GPU it runs on: MUFU ex2 (ex2.approx.ftz.f32), MUFU rcp, FP32 FFMA and the

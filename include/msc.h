@@ -13,8 +13,10 @@
  *    Mamba-1/2 are exponential-Euler), readout y_t = C_t . h_t + D u_t ("Mamba 解密"
  *    sec. 3, D feed-through), gated by silu(z_t) ("Mamba前世今生全挖掘" sec. 二,
  *    selective SSM + gating).
- *  - S6 backward by recomputation: states are recomputed on chip and never
- *    stored to global memory (bqwf survey sec. 2.2, recomputation).
+ *  - S6 backward by recomputation (bqwf survey sec. 2.2): a forward pass keeps
+ *    the fp32 state entering every 8-step group of every row in the workspace
+ *    (1/8 of h), and the reverse pass recomputes the steps in between in
+ *    registers; no other state is stored.
  *  - Mamba-2 SSD chunked forward: scalar A per head (A_t = alpha_t I), the
  *    semiseparable form Y = M (X . B^T) C with M_ij = a_{j+1}...a_i (bqwf
  *    survey sec. 3.2; "Mamba 解密" sec. 6.2), computed by the block
@@ -64,11 +66,19 @@ typedef enum { MSC_F32 = 0, MSC_BF16 = 1 } msc_dtype;
  * Optional (may be NULL): D (no feed-through), z (no gate), delta_bias (0),
  * h0 (zero initial state), h_last (final state not returned).
  * Limits: batch, dim, seqlen >= 1; 1 <= dstate <= 16.
- * Long sequences with few rows are split into segments whose carries are
- * combined in the workspace (three launches); otherwise one launch, and the
- * workspace size is 0.  Rows whose byte stride (seqlen * element size) is a
- * multiple of 16 are streamed with TMA; other lengths take a plain-load kernel
- * with identical arithmetic. */
+ * Workspace (256-byte aligned, size from msc_selective_scan_fwd_workspace_size):
+ *  - long sequences with few rows are split into segments whose carries are
+ *    combined in the workspace (three launches); there it is REQUIRED and a
+ *    smaller one returns MSC_ERR_WORKSPACE;
+ *  - otherwise one pass; for sequences of 512 steps or more the workspace lets
+ *    persistent CTAs hand each 32-row block's state from one time chunk to the
+ *    next (a ticket counter, per-block flags and the states, cleared by the
+ *    call itself), which balances the load across SMs.  There it is OPTIONAL:
+ *    with NULL or a smaller one the pass runs one CTA per row block.
+ *  - a workspace must not be shared by calls that overlap on the GPU.
+ * Rows whose byte stride (seqlen * element size) is a multiple of 16 are
+ * streamed with TMA; other lengths take a plain-load kernel with identical
+ * arithmetic. */
 size_t msc_selective_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
                                              int64_t dstate);
 
@@ -115,8 +125,10 @@ msc_status msc_selective_scan_fwd_ex(int64_t batch, int64_t dim, int64_t seqlen,
  * without the workspace: the segment scratch of long sequences comes from a
  * library-owned array of MSC_STATIC_SCRATCH_BYTES in device global memory,
  * present on every device that loads the library until the process exits.
- * - A problem whose msc_selective_scan_fwd_workspace_size() exceeds
- *   MSC_STATIC_SCRATCH_BYTES returns MSC_ERR_WORKSPACE and launches nothing.
+ * - A problem whose REQUIRED workspace (the segment scratch of long sequences
+ *   with few rows, see msc_selective_scan_fwd) exceeds MSC_STATIC_SCRATCH_BYTES
+ *   returns MSC_ERR_WORKSPACE and launches nothing; the optional load-balancing
+ *   scratch is used when it fits in the array and left out when it does not.
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current, and caches it; make that
  *   first call before any stream capture.
@@ -131,6 +143,30 @@ msc_status msc_selective_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t se
                                           const void* B, const void* C, const float* D,
                                           const void* z, const float* delta_bias, const float* h0,
                                           float* y, float* h_last, void* stream);
+
+/* ------------------------------------------- S6 forward from host memory
+ * The forward of msc_selective_scan_fwd for inputs and outputs that live in
+ * HOST memory: u, delta, z (optional), B, C and y are host pointers (pinned
+ * memory lets the copies overlap the scan; pageable memory works but
+ * serialises); A, D, delta_bias are device pointers as in
+ * msc_selective_scan_fwd (zero initial state, no final state).  The batch runs
+ * in chunks of chunk_batch entries through a three-stream pipeline: the upload
+ * of chunk i + 1, the scan of chunk i on `stream` and the download of chunk
+ * i - 1 proceed together.  staging: caller-owned device memory, 256-byte
+ * aligned, of msc_selective_scan_fwd_host_staging_size(...) bytes (two chunk
+ * slots and the forward's workspace); the library allocates nothing (it keeps
+ * two CUDA streams per device for the copies).  The call returns once the work
+ * is queued; `stream` waits for the last download, so synchronising it makes
+ * y complete.  Rows are independent, so y equals msc_selective_scan_fwd over
+ * the whole batch whenever both take the same segment plan. */
+size_t msc_selective_scan_fwd_host_staging_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                                msc_dtype in_dtype, int has_z, int64_t chunk_batch);
+
+msc_status msc_selective_scan_fwd_host(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                       msc_dtype in_dtype, const void* u, const void* delta, const float* A,
+                                       const void* B, const void* C, const float* D, const void* z,
+                                       const float* delta_bias, float* y, int64_t chunk_batch, void* staging,
+                                       size_t staging_bytes, void* stream);
 
 /* ------------------------------- S6 forward with the conv1d front end fused
  * The Mamba block's causal depthwise conv1d + SiLU (bqwf survey sec. 3.1: the
@@ -160,7 +196,8 @@ msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqle
  * du, ddelta: [batch, dim, seqlen]; dA: [dim, dstate]; dB, dC: [batch, dstate, seqlen];
  * dD [dim] (required iff D != NULL); dz [batch, dim, seqlen] (required iff z != NULL);
  * ddelta_bias [dim] (required iff delta_bias != NULL).
- * The forward states are recomputed chunk by chunk on chip; dB, dC, dA, dD and
+ * The forward states are recomputed from checkpoints kept every 8 steps in the
+ * workspace (16 fp32 per row and group: 8 bytes per element); dB, dC, dA, dD and
  * ddelta_bias are sums accumulated with fp32 atomics, so their low bits depend
  * on the order in which blocks finish.  seqlen (rounded up to a 16-byte row)
  * and dim must be below 2^31, else MSC_ERR_UNSUPPORTED. */

@@ -18,7 +18,7 @@ __all__ = [
     "msc_selective_scan_fwd", "msc_selective_scan_bwd", "msc_ssd_chunked_fwd", "msc_ssd_chunked_bwd",
     "msc_selective_state_update", "msc_ssd_chunked_bwd_workspace_size",
     "msc_causal_conv1d_fwd", "msc_causal_conv1d_update", "msc_selective_scan_fwd_ex",
-    "msc_selective_scan_fwd_conv", "msc_causal_conv1d_bwd",
+    "msc_selective_scan_fwd_conv", "msc_causal_conv1d_bwd", "msc_selective_scan_fwd_host",
     "MSC_DISC_EULER", "MSC_DISC_ZOH", "MSC_DISC_TRAPEZOID",
     "msc_selective_scan_fwd_workspace_size", "msc_selective_scan_bwd_workspace_size",
     "msc_ssd_chunked_fwd_workspace_size", "msc_check_device_status", "msc_status_string",
@@ -51,6 +51,8 @@ SIGNATURES = {
     "msc_selective_scan_fwd_ex": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] * 2 + [_vp] * 11 + [_vp, _sz, _vp]),
     "msc_selective_scan_fwd_conv": (ctypes.c_int, [_i64] * 5 + [ctypes.c_int] + [_vp] * 13 + [_vp, _sz, _vp]),
     "msc_selective_scan_fwd_noalloc": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 11 + [_vp]),
+    "msc_selective_scan_fwd_host_staging_size": (_sz, [_i64] * 4 + [ctypes.c_int] * 2 + [_i64]),
+    "msc_selective_scan_fwd_host": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 9 + [_i64, _vp, _sz, _vp]),
     "msc_selective_state_update": (ctypes.c_int, [_i64] * 3 + [ctypes.c_int] + [_vp] * 10 + [_vp]),
     "msc_causal_conv1d_fwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] * 2 + [_vp] * 3 + [ctypes.c_int] + [_vp, _vp]),
     "msc_causal_conv1d_update": (ctypes.c_int, [_i64] * 3 + [ctypes.c_int] * 2 + [_vp] * 3 + [ctypes.c_int] + [_vp] * 3),
@@ -207,6 +209,56 @@ def msc_selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, h
         st = lib.msc_selective_scan_fwd_ex(batch, dim, L, N, dt, int(disc), *args, *tail)
     _check(st)
     return (y, h_last) if return_last_state else y
+
+
+def _host_ptr(t, name, dtype=None, shape=None, optional=False):
+    torch = _torch()
+    if t is None:
+        if optional:
+            return None
+        raise ValueError("%s is required" % name)
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError("%s must be a host (CPU) tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s (got %s)" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s (got %s)" % (name, tuple(shape), tuple(t.shape)))
+    return t.data_ptr()
+
+
+def msc_selective_scan_fwd_host(u, delta, A, B, C, D=None, z=None, delta_bias=None, y=None, chunk_batch=2,
+                                staging=None, stream=None):
+    """S6 forward from and to host memory.  u, delta, z [batch, dim, L] and
+    B, C [batch, N, L] are CPU tensors (pinned for overlap), A [dim, N], D and
+    delta_bias [dim] CUDA fp32 tensors.  y: CPU fp32 [batch, dim, L] (made
+    pinned when None).  The copies of chunk_batch batch entries at a time
+    overlap the scan.  Returns y, which is complete once the stream has been
+    synchronised (the call itself does not wait)."""
+    torch = _torch()
+    lib = load_library()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dt = _in_dtype(u)
+    tdt = u.dtype
+    device = A.device
+    if y is None:
+        y = torch.empty((batch, dim, L), dtype=torch.float32).pin_memory()
+    args = [
+        _host_ptr(u, "u"), _host_ptr(delta, "delta", tdt, (batch, dim, L)),
+        _dev_ptr(A, "A", torch.float32, (dim, N)),
+        _host_ptr(B, "B", tdt, (batch, N, L)), _host_ptr(C, "C", tdt, (batch, N, L)),
+        _dev_ptr(D, "D", torch.float32, (dim,), optional=True),
+        _host_ptr(z, "z", tdt, (batch, dim, L), optional=True),
+        _dev_ptr(delta_bias, "delta_bias", torch.float32, (dim,), optional=True),
+        _host_ptr(y, "y", torch.float32, (batch, dim, L)),
+    ]
+    nbytes = lib.msc_selective_scan_fwd_host_staging_size(batch, dim, L, N, dt, int(z is not None), chunk_batch)
+    ws, wsb = _workspace(nbytes, device, staging, align=256)
+    _check(lib.msc_selective_scan_fwd_host(batch, dim, L, N, dt, *args, chunk_batch,
+                                           ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream)))
+    return y
 
 
 def msc_selective_scan_fwd_conv(x, conv_weight, conv_bias, delta, A, B, C, D=None, z=None, delta_bias=None,

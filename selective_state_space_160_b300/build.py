@@ -20,8 +20,13 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmsc.so")
-PROBE_DIR = os.path.join(PKG, "probe")
-PROBE_LIB = os.path.join(PKG, "libmsc_probe.so")
+# Not part of the library: the tests' device fixtures (a one-CTA tcgen05 GEMM
+# that checks the descriptors, a bounded wait that nothing completes) and the
+# bench's pipe-throughput probe, each built into its own in-tree library.
+FIXTURE_DIR = os.path.join(ROOT, "tests", "fixtures")
+FIXTURE_LIB = os.path.join(FIXTURE_DIR, "libmsc_fixtures.so")
+PIPE_PEAKS_SRC = os.path.join(ROOT, "bench_pipe_peaks.cu")
+PIPE_PEAKS_LIB = os.path.join(ROOT, "libmsc_pipe_peaks.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
@@ -62,25 +67,33 @@ def build(force: bool = False, verbose: bool = False, extra=None) -> str:
     return LIB
 
 
-def build_probe(force: bool = False, verbose: bool = False) -> str:
-    """Build the probe library: pipe-throughput measurement used by bench.py and
-    the tcgen05 building-block check used by the tests."""
-    srcs = sorted(glob.glob(os.path.join(PROBE_DIR, "*.cu")))
+def _build_side(srcs, lib, verbose=False, force=False):
     newest = max(os.path.getmtime(p) for p in srcs + _deps())
-    if not force and os.path.exists(PROBE_LIB) and os.path.getmtime(PROBE_LIB) >= newest:
-        return PROBE_LIB
-    tmp = PROBE_LIB + ".tmp"
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= newest:
+        return lib
+    tmp = lib + ".tmp"
     cmd = [nvcc()] + ARCH + ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-cudart", "static",
                              "-I", INCLUDE, "-I", CSRC, "-o", tmp] + srcs
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
-    os.replace(tmp, PROBE_LIB)
-    return PROBE_LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_fixtures(force: bool = False, verbose: bool = False) -> str:
+    """Build the tests' device fixtures (tests/fixtures/*.cu)."""
+    return _build_side(sorted(glob.glob(os.path.join(FIXTURE_DIR, "*.cu"))), FIXTURE_LIB, verbose, force)
+
+
+def build_pipe_peaks(force: bool = False, verbose: bool = False) -> str:
+    """Build the bench's MUFU / FFMA throughput probe (bench_pipe_peaks.cu)."""
+    return _build_side([PIPE_PEAKS_SRC], PIPE_PEAKS_LIB, verbose, force)
 
 
 def build_all(force: bool = False, verbose: bool = False):
-    return build(force=force, verbose=verbose), build_probe(force=force, verbose=verbose)
+    return (build(force=force, verbose=verbose), build_fixtures(force=force, verbose=verbose),
+            build_pipe_peaks(force=force, verbose=verbose))
 
 
 def main(argv=None):
@@ -91,7 +104,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     extra = ["-Xptxas", "-v"] if args.ptxas_info else None
     print(build(force=args.force or args.ptxas_info, verbose=args.verbose, extra=extra))
-    print(build_probe(force=args.force, verbose=args.verbose))
+    print(build_fixtures(force=args.force, verbose=args.verbose))
+    print(build_pipe_peaks(force=args.force, verbose=args.verbose))
 
 
 if __name__ == "__main__":

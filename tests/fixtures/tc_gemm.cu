@@ -1,4 +1,4 @@
-// tc_gemm.cu -- building-block check, not part of the libmsc boundary.
+// tc_gemm.cu -- test fixture (tcgen05 building blocks), not part of libmsc.
 //
 // One CTA computes D[128 x N] = A[128 x K] * B[N x K]^T with tcgen05.mma
 // (kind::f16, fp32 accumulate in tensor memory) from K-major 128-byte-swizzled

@@ -260,3 +260,22 @@ def test_binding_has_no_cpu_path(monkeypatch):
     monkeypatch.setattr(msc, "_lib", None)
     with pytest.raises(RuntimeError, match="not found"):
         msc.load_library()
+
+
+def test_fwd_host_rejects_bad_arguments(lib):
+    f = lib.msc_selective_scan_fwd_host
+
+    def call(batch=2, L=64, dt=1, u=16, y=16, chunk=1, st=4096, stb=1 << 30):
+        return f(batch, 4, L, 16, dt, u, 16, 16, 16, 16, None, None, None, y, chunk, st, stb, None)
+
+    assert call(u=None) == msc.MSC_ERR_INVALID_ARG
+    assert call(y=None) == msc.MSC_ERR_INVALID_ARG
+    assert call(chunk=0) == msc.MSC_ERR_INVALID_ARG
+    assert call(dt=5) == msc.MSC_ERR_INVALID_ARG
+    assert call(st=None) == msc.MSC_ERR_WORKSPACE
+    assert call(stb=16) == msc.MSC_ERR_WORKSPACE
+    assert call(st=4096 + 16) == msc.MSC_ERR_INVALID_ARG           # staging misaligned
+    one = lib.msc_selective_scan_fwd_host_staging_size(8, 4, 64, 16, 1, 1, 1)
+    two = lib.msc_selective_scan_fwd_host_staging_size(8, 4, 64, 16, 1, 1, 2)
+    assert 0 < one < two
+    assert lib.msc_selective_scan_fwd_host_staging_size(8, 4, 64, 16, 1, 1, 0) == 0

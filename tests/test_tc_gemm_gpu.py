@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 
 def _lib():
     from selective_state_space_160_b300 import build as b
-    lib = ctypes.CDLL(b.build_probe())
+    lib = ctypes.CDLL(b.build_fixtures())
     lib.msc_probe_tc_gemm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.msc_probe_tc_gemm.restype = ctypes.c_int
