@@ -131,7 +131,10 @@ msc_status msc_selective_scan_fwd_ex(int64_t batch, int64_t dim, int64_t seqlen,
  *   scratch is used when it fits in the array and left out when it does not.
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current, and caches it; make that
- *   first call before any stream capture.
+ *   first call before any stream capture.  The cache is kept per device
+ *   ordinal for the life of the process: after cudaDeviceReset the module is
+ *   loaded again and the array may move, so a process that resets a device
+ *   must not call this entry point on it afterwards.
  * - All calls share the one array and its contents persist between calls:
  *   calls that overlap on the GPU (other streams, other host threads) race.
  * - Allocates nothing itself (no cudaMalloc / cudaFree). */

@@ -5,8 +5,12 @@ CPU-baseline leg may import this module.  It shares nothing with the CUDA librar
 and never touches the GPU.  Inputs are converted to float64 exactly (fp32 and
 bf16-rounded values are exact in double), outputs are float64.
 
-The arithmetic lives in msc_oracle.c; this file only marshals arrays.  Parity of
-each function is pinned in tests/test_oracle_pins.py (closed forms, special
+The S6 forward, its backward, the decode step and the SSD forward are computed
+in msc_oracle.c (plain C, double); this file marshals their arrays.  Four
+oracle functions are written here in numpy, in float64: the causal conv1d with
+SiLU, its decode step and its backward, and the SSD backward (the S6 backward
+composed over the channels that share a head's Delta and A and a group's B, C).
+Parity of each function is pinned in tests/test_oracle_pins.py (closed forms, special
 cases, brute force and finite differences), so none of them is "parity unpinned".
 """
 from __future__ import annotations
