@@ -143,6 +143,19 @@ msc_status msc_selective_scan_fwd_ex(int64_t batch, int64_t dim, int64_t seqlen,
                                      const float* D, const void* z, const float* delta_bias, const float* h0,
                                      float* y, float* h_last, void* workspace, size_t workspace_bytes,
                                      void* stream) {
+    return msc_host::s6_fwd_entry(batch, dim, seqlen, dstate, in_dtype, (int)disc, u, delta, A, B, C, D, z,
+                                  delta_bias, h0, y, h_last, workspace, workspace_bytes, stream, SIZE_MAX);
+}
+
+}  // extern "C"
+
+namespace msc_host {
+
+msc_status s6_fwd_entry(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, msc_dtype in_dtype, int disc,
+                        const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, const float* h0, float* y,
+                        float* h_last, void* workspace, size_t workspace_bytes, void* stream,
+                        size_t max_required) {
     clear_error();
     msc_status s = check_s6_dims(batch, dim, seqlen, dstate, in_dtype);
     if (s != MSC_OK) return s;
@@ -152,7 +165,7 @@ msc_status msc_selective_scan_fwd_ex(int64_t batch, int64_t dim, int64_t seqlen,
     MSC_PTR(C, "C"); MSC_PTR(y, "y");
     MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z"); MSC_OPT_PTR(delta_bias, "delta_bias");
     MSC_OPT_PTR(h0, "h0"); MSC_OPT_PTR(h_last, "h_last");
-    S6Plan plan = s6_fwd_plan(batch, dim, seqlen, dstate);
+    S6Plan plan = s6_fwd_plan(batch, dim, seqlen, dstate, max_required);
     if (plan.workspace_required && (workspace == nullptr || workspace_bytes < plan.workspace))
         return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", plan.workspace,
                     workspace ? workspace_bytes : (size_t)0);
@@ -164,9 +177,13 @@ msc_status msc_selective_scan_fwd_ex(int64_t batch, int64_t dim, int64_t seqlen,
     a.A = A; a.D = D; a.delta_bias = delta_bias; a.h0 = h0; a.y = y; a.h_last = h_last;
     a.workspace = workspace;
     a.workspace_bytes = workspace ? workspace_bytes : 0;
-    a.disc = (int)disc;
+    a.disc = disc;
     return s6_fwd_launch(a, plan, static_cast<cudaStream_t>(stream));
 }
+
+}  // namespace msc_host
+
+extern "C" {
 
 msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                        int64_t conv_width, msc_dtype in_dtype, const void* x,

@@ -19,7 +19,8 @@ struct S6Plan {
     size_t seg_state_off = 0, seg_dsum_off = 0, ctrl_off = 0, ctrl_bytes = 0, chain_state_off = 0, bc_off = 0;
 };
 
-S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
+// max_required: the largest required (segment) scratch the plan may use.
+S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, size_t max_required = SIZE_MAX);
 
 struct S6FwdArgs {
     int64_t batch, dim, L;
@@ -38,6 +39,14 @@ struct S6FwdArgs {
 };
 
 msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t stream);
+
+// The S6 forward entry point's validation, plan and launch; disc is an
+// msc_discretization; max_required caps the plan's required scratch.
+msc_status s6_fwd_entry(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, msc_dtype in_dtype, int disc,
+                        const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, const float* h0, float* y,
+                        float* h_last, void* workspace, size_t workspace_bytes, void* stream,
+                        size_t max_required);
 
 // Checkpoint pass used by the backward: writes the state entering every
 // 8-step group of every row to ckpt [batch * dim, ceil(L / 8), 16] (fp32).

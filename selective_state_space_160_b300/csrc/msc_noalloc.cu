@@ -39,11 +39,15 @@ extern "C" msc_status msc_selective_scan_fwd_noalloc(int64_t batch, int64_t dim,
                                                      const void* z, const float* delta_bias, const float* h0,
                                                      float* y, float* h_last, void* stream) {
     msc_host::clear_error();
-    // Only the segment scratch of long sequences with few rows is required; the
-    // chained schedule's scratch is used when it fits and skipped when not.
+    // Only the segment scratch of long sequences with few rows is required: the
+    // plan picks its segment count among those whose scratch fits the array
+    // (with none, it runs the sequence unsegmented), so `need` stays within it;
+    // the check below guards that.  The chained schedule's optional scratch is
+    // used when it fits.
     size_t need = 0;
     if (batch >= 1 && dim >= 1 && seqlen >= 1 && dstate >= 1 && dstate <= 16) {
-        const msc_host::S6Plan plan = msc_host::s6_fwd_plan(batch, dim, seqlen, dstate);
+        const msc_host::S6Plan plan =
+            msc_host::s6_fwd_plan(batch, dim, seqlen, dstate, (size_t)MSC_STATIC_SCRATCH_BYTES);
         if (plan.workspace_required) need = plan.workspace;
     }
     if (need > (size_t)MSC_STATIC_SCRATCH_BYTES)
@@ -69,6 +73,7 @@ extern "C" msc_status msc_selective_scan_fwd_noalloc(int64_t batch, int64_t dim,
     }
     // Nothing in the scratch has to start at zero: every value the kernels read
     // from it was written earlier in the same call.
-    return msc_selective_scan_fwd(batch, dim, seqlen, dstate, in_dtype, u, delta, A, B, C, D, z, delta_bias, h0, y,
-                                  h_last, scratch, (size_t)MSC_STATIC_SCRATCH_BYTES, stream);
+    return msc_host::s6_fwd_entry(batch, dim, seqlen, dstate, in_dtype, (int)MSC_DISC_EULER, u, delta, A, B, C, D,
+                                  z, delta_bias, h0, y, h_last, scratch, (size_t)MSC_STATIC_SCRATCH_BYTES, stream,
+                                  (size_t)MSC_STATIC_SCRATCH_BYTES);
 }

@@ -1047,9 +1047,10 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 //    chunk to chunk) is optional: without it the pass runs one CTA per row block.
 //  - Few row blocks and a long sequence: independent segments (aggregate pass,
 //    carry pass, full pass), the number chosen by the cost of the busiest CTA
-//    in steps, the aggregate pass counted at 3/4 of the full pass per step.
-//    Its workspace is required.
-S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
+//    in steps, the aggregate pass counted at 3/4 of the full pass per step,
+//    among the counts whose scratch stays within max_required.  Its workspace
+//    is required.
+S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, size_t max_required) {
     // Chunks per row and their least length: each item restarts the CTA's TMA
     // pipeline (a few microseconds), so that 4 chunks of 512 steps balance the
     // batch-8 x 5120 x 2048 workload as well as 8 of 256 (0.412 vs 0.414 ms on a
@@ -1087,6 +1088,8 @@ S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
         const int64_t seg = cdiv64(cdiv64(seqlen, G), kT) * kT;
         const int64_t Gc = cdiv64(seqlen, seg);
         if (Gc < 2) continue;
+        const size_t need = align256((size_t)rows * Gc * (size_t)dstate * sizeof(float)) + (size_t)rows * Gc * sizeof(float);
+        if (need > max_required) continue;
         const double per = (double)seg + ovh;
         const double cost = 0.75 * (double)cdiv64(chains * (Gc - 1), W) * per + (double)cdiv64(chains * Gc, W) * per;
         if (cost < best) {
