@@ -743,13 +743,13 @@ def run_ours(args):
 
     # end to end through the C ABI with HOST buffers (msc_selective_scan_fwd_host):
     # every step uploads its inputs from pinned memory, scans and downloads y,
-    # two batch entries at a time on three streams so that the copies overlap
+    # one batch entry at a time on three streams so that the copies overlap
     # the scan; the device staging is allocated once
     host = {k: (inp[k].cpu().pin_memory() if inp[k] is not None else None) for k in ("u", "delta", "z", "B", "C")}
     yh = torch.empty((b, dim, L), dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = yh.numel() * 4
-    e2e_chunk = 2
+    e2e_chunk = 1
     lib = msc.load_library()
     st_bytes = lib.msc_selective_scan_fwd_host_staging_size(b, dim, L, N, 1, 1, e2e_chunk)
     st_buf = torch.empty(st_bytes + 256, dtype=torch.uint8, device="cuda")
@@ -808,7 +808,7 @@ def run_ours(args):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "path": "msc_selective_scan_fwd_host (C ABI, pinned host buffers, 2 batch entries per chunk, "
+                    "path": "msc_selective_scan_fwd_host (C ABI, pinned host buffers, 1 batch entry per chunk, "
                             "upload / scan / download overlapped on three streams)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": dict(clk.summary(), note="sampled every 100 ms while the step ran back to back "

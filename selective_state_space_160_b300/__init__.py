@@ -228,7 +228,7 @@ def _host_ptr(t, name, dtype=None, shape=None, optional=False):
     return t.data_ptr()
 
 
-def msc_selective_scan_fwd_host(u, delta, A, B, C, D=None, z=None, delta_bias=None, y=None, chunk_batch=2,
+def msc_selective_scan_fwd_host(u, delta, A, B, C, D=None, z=None, delta_bias=None, y=None, chunk_batch=1,
                                 staging=None, stream=None):
     """S6 forward from and to host memory.  u, delta, z [batch, dim, L] and
     B, C [batch, N, L] are CPU tensors (pinned for overlap), A [dim, N], D and
