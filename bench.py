@@ -275,10 +275,13 @@ def _leg_summary(res):
 
 
 # ----------------------------------------------------------------------------- legs
+LONG_LEN = 1 << 20  # steps of the long-sequence leg (--long-len; smaller for a profiling-size run)
+
+
 def leg_fwd_long(peaks, pipes, steps=3, warmup=1):
     import torch
     import selective_state_space_160_b300 as msc
-    batch, dim, L, N = 1, 1536, 1 << 20, 16
+    batch, dim, L, N = 1, 1536, LONG_LEN, 16
     inp = s6_fwd_workload(batch, dim, L, N, False, 160_002, device_gen=True)
     y = torch.empty((batch, dim, L), dtype=torch.float32, device="cuda")
     ws = torch.empty(msc.msc_selective_scan_fwd_workspace_size(batch, dim, L, N) + 1024,
@@ -291,7 +294,7 @@ def leg_fwd_long(peaks, pipes, steps=3, warmup=1):
     ms = statistics.median(time_launches(fn, steps, warmup, st))
     el = batch * dim * L
     nbytes = el * 16 + 2 * batch * N * L * 4
-    res = {"workload": "S6 fwd batch 1, D 1536, L 2^20, N 16, fp32, segmented", "elements_per_s": el / (ms * 1e-3),
+    res = {"workload": "S6 fwd batch 1, D 1536, L %d, N 16, fp32, segmented" % L, "elements_per_s": el / (ms * 1e-3),
            "ms": ms, "roofline": roofline_s6(el, N, nbytes, ms, peaks, pipes)}
     del inp, y, ws
     torch.cuda.empty_cache()
@@ -835,9 +838,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ssd-batch", type=int, default=4, help="batch of the SSD legs (4 = the timed workload)")
+    ap.add_argument("--long-len", type=int, default=1 << 20,
+                    help="steps of the long-sequence leg (2^20 = the timed workload)")
     args = ap.parse_args(argv)
-    global SSD_BATCH
+    global SSD_BATCH, LONG_LEN
     SSD_BATCH = args.ssd_batch
+    LONG_LEN = args.long_len
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

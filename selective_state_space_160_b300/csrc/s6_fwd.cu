@@ -896,15 +896,24 @@ __global__ void s6_seg_carry_kernel(const float* __restrict__ A, const float* __
     const int64_t d = row % dim;
     const float a2 = __ldg(A + d * N + n) * MSC_LOG2E;
     float h = h0 ? __ldg(h0 + row * N + n) : 0.f;
-    for (int g = 0; g < G; ++g) {
-        const size_t i = ((size_t)row * G + g) * N + n;
-        // the aggregate pass writes segments 0 .. G-2; the last slot only receives its carry
-        if (g + 1 < G) {
-            const float agg = seg_state[i];
-            seg_state[i] = h;
-            h = fmaf(msc::ex2_approx(a2 * seg_dsum[(size_t)row * G + g]), h, agg);
-        } else {
-            seg_state[i] = h;
+    // The aggregates and sums of eight segments are loaded ahead of the
+    // dependent chain (each slot is read before this thread overwrites it).
+    // The aggregate pass writes segments 0 .. G-2; the last slot only receives
+    // its carry.
+    for (int g0 = 0; g0 < G; g0 += 8) {
+        float agg[8], ds[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int g = g0 + k;
+            agg[k] = g + 1 < G ? seg_state[((size_t)row * G + g) * N + n] : 0.f;
+            ds[k] = g + 1 < G ? seg_dsum[(size_t)row * G + g] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int g = g0 + k;
+            if (g >= G) break;
+            seg_state[((size_t)row * G + g) * N + n] = h;
+            if (g + 1 < G) h = fmaf(msc::ex2_approx(a2 * ds[k]), h, agg[k]);
         }
     }
 }
@@ -1037,8 +1046,8 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 }  // namespace
 
 // Work plan of the forward.  A CTA of the two-lane kernel runs 32 channel rows
-// ("row block"); about ten are resident per SM (64 threads, 96 registers,
-// 21 KB of shared memory).
+// ("row block"); eight are resident per SM in the full pass (64 threads, 126 to
+// 128 registers, 21 KB of shared memory).
 //  - Enough row blocks to fill the GPU: one pass.  Sequences of 512 steps or
 //    more are cut into chained chunks (at least 256 steps, at most 4 per row)
 //    taken by persistent CTAs in order, so that a row block's work moves
@@ -1046,10 +1055,9 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 //    set the time.  Its workspace (ticket counter, flags, the state handed from
 //    chunk to chunk) is optional: without it the pass runs one CTA per row block.
 //  - Few row blocks and a long sequence: independent segments (aggregate pass,
-//    carry pass, full pass), the number chosen by the cost of the busiest CTA
-//    in steps, the aggregate pass counted at 3/4 of the full pass per step,
-//    among the counts whose scratch stays within max_required.  Its workspace
-//    is required.
+//    carry pass, full pass) of at least 512 steps, about twelve per resident
+//    CTA slot, at most as many as keep the scratch within max_required.  Its
+//    workspace is required.
 S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, size_t max_required) {
     // Chunks per row and their least length: each item restarts the CTA's TMA
     // pipeline (a few microseconds), so that 4 chunks of 512 steps balance the
@@ -1059,7 +1067,7 @@ S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, s
     S6Plan plan;
     const int64_t rows = batch * dim;
     const int64_t chains = batch * cdiv64(dim, kRows);
-    const int64_t W = 10 * (int64_t)num_sms();
+    const int64_t W = 8 * (int64_t)num_sms();  // full-pass CTAs resident per SM (126-128 registers)
     plan.G = 1;
     plan.seg_len = seqlen;
     plan.chunks = 1;
@@ -1079,23 +1087,19 @@ S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, s
         }
         return plan;
     }
-    const double ovh = 16.0;  // steps' worth of per-CTA start-up
-    double best = (double)cdiv64(chains, W) * ((double)seqlen + ovh);
+    // About twelve segments per resident CTA slot: CTAs that share an SM finish
+    // at different times, and many short items keep that tail short (at
+    // 1 x 1536 x 2^20: 17.5 ms with 154 segments, 17.1 with 296, 19.7 with 74).
     int bestG = 1;
     int64_t best_seg = seqlen;
-    const int64_t max_G = std::min<int64_t>({(int64_t)65535, seqlen / 256, 64 * W / chains + 1});
-    for (int64_t G = 2; G <= max_G; ++G) {
+    for (int64_t G = std::min<int64_t>({cdiv64(12 * W, chains), seqlen / 512, (int64_t)65535}); G >= 2; --G) {
         const int64_t seg = cdiv64(cdiv64(seqlen, G), kT) * kT;
         const int64_t Gc = cdiv64(seqlen, seg);
-        if (Gc < 2) continue;
         const size_t need = align256((size_t)rows * Gc * (size_t)dstate * sizeof(float)) + (size_t)rows * Gc * sizeof(float);
-        if (need > max_required) continue;
-        const double per = (double)seg + ovh;
-        const double cost = 0.75 * (double)cdiv64(chains * (Gc - 1), W) * per + (double)cdiv64(chains * Gc, W) * per;
-        if (cost < best) {
-            best = cost;
+        if (Gc >= 2 && need <= max_required) {
             bestG = (int)Gc;
             best_seg = seg;
+            break;
         }
     }
     if (bestG > 1) {
