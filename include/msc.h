@@ -65,7 +65,12 @@ typedef enum { MSC_F32 = 0, MSC_BF16 = 1 } msc_dtype;
  * y: [batch, dim, seqlen] fp32.
  * Optional (may be NULL): D (no feed-through), z (no gate), delta_bias (0),
  * h0 (zero initial state), h_last (final state not returned).
- * Limits: batch, dim, seqlen >= 1; 1 <= dstate <= 16.
+ * Limits: batch, dim, seqlen >= 1; 1 <= dstate <= MSC_S6_FWD_MAX_DSTATE (64).
+ * Above 16 states the rows must be TMA-streamable (see below) and the fused
+ * conv front end is not offered; the backward and the decode step take up to
+ * MSC_S6_MAX_DSTATE (16), the SSD entry points dstate 128.  Each row holds its
+ * states in 16, 32 or 64 slots (the next of these at or above dstate); the
+ * slots past dstate carry zeros.
  * Workspace (256-byte aligned, size from msc_selective_scan_fwd_workspace_size):
  *  - long sequences with few rows are split into segments whose carries are
  *    combined in the workspace (three launches); there it is REQUIRED and a
@@ -78,7 +83,10 @@ typedef enum { MSC_F32 = 0, MSC_BF16 = 1 } msc_dtype;
  *  - a workspace must not be shared by calls that overlap on the GPU.
  * Rows whose byte stride (seqlen * element size) is a multiple of 16 are
  * streamed with TMA; other lengths take a plain-load kernel with identical
- * arithmetic. */
+ * arithmetic, for dstate <= 16 only (MSC_ERR_UNSUPPORTED above). */
+#define MSC_S6_FWD_MAX_DSTATE 64
+#define MSC_S6_MAX_DSTATE 16
+
 size_t msc_selective_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
                                              int64_t dstate);
 
@@ -184,8 +192,8 @@ msc_status msc_selective_scan_fwd_host(int64_t batch, int64_t dim, int64_t seqle
  * the result equals msc_causal_conv1d_fwd (fp32 out) followed by
  * msc_selective_scan_fwd with fp32 u up to rounding.  Needs 16-byte row
  * strides (seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) and seqlen,
- * dim below 2^31, else MSC_ERR_UNSUPPORTED; exponential-Euler form only; no
- * backward. */
+ * dim below 2^31, else MSC_ERR_UNSUPPORTED; exponential-Euler form and
+ * dstate <= 16 only; no backward. */
 msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                        int64_t conv_width, msc_dtype in_dtype, const void* x,
                                        const float* conv_weight, const float* conv_bias, const void* delta,
@@ -198,7 +206,8 @@ msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqle
  * gradient dy [batch, dim, seqlen] (in_dtype).  Outputs (fp32, overwritten):
  * du, ddelta: [batch, dim, seqlen]; dA: [dim, dstate]; dB, dC: [batch, dstate, seqlen];
  * dD [dim] (required iff D != NULL); dz [batch, dim, seqlen] (required iff z != NULL);
- * ddelta_bias [dim] (required iff delta_bias != NULL).
+ * ddelta_bias [dim] (required iff delta_bias != NULL).  dstate <= 16
+ * (MSC_S6_MAX_DSTATE), else MSC_ERR_UNSUPPORTED.
  * The forward states are recomputed from checkpoints kept every 8 steps in the
  * workspace (16 fp32 per row and group: 8 bytes per element); dB, dC, dA, dD and
  * ddelta_bias are sums accumulated with fp32 atomics, so their low bits depend
@@ -226,7 +235,7 @@ msc_status msc_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, in
  *   y = (sum_n C[b, n] state[n] + D[d] u) * silu(z)
  * Shapes: u, delta, z, y: [batch, dim]; B, C: [batch, dstate]; A: [dim, dstate];
  * D, delta_bias: [dim]; state: [batch, dim, dstate] fp32, read and overwritten
- * in place.  Same limits as the forward (dstate 1..16); no workspace.  Calling
+ * in place.  dstate 1..16 (MSC_S6_MAX_DSTATE); no workspace.  Calling
  * it seqlen times on tokens t = 0.. reproduces msc_selective_scan_fwd with
  * h0 = the initial state, up to fp32 rounding.  A state row of 16 states is
  * moved with one 32-byte load and store per thread (two threads per row).

@@ -94,13 +94,16 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
         if ((p) != nullptr) MSC_REQUIRE(aligned16(p), "%s must be 16-byte aligned", name); \
     } while (0)
 
+// max_dstate: 64 for the forward scan (exponential Euler, zero-order hold,
+// trapezoid), 16 for the backward, the decode step and the fused conv front end.
 static msc_status check_s6_dims(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
-                                msc_dtype dt) {
+                                msc_dtype dt, int64_t max_dstate = 16) {
     MSC_REQUIRE(batch >= 1 && dim >= 1 && seqlen >= 1, "batch, dim and seqlen must be >= 1 (got %lld, %lld, %lld)",
                 (long long)batch, (long long)dim, (long long)seqlen);
     MSC_REQUIRE(dt == MSC_F32 || dt == MSC_BF16, "in_dtype must be MSC_F32 or MSC_BF16");
-    if (dstate < 1 || dstate > 16)
-        return fail(MSC_ERR_UNSUPPORTED, "dstate must be in [1, 16] (got %lld)", (long long)dstate);
+    if (dstate < 1 || dstate > max_dstate)
+        return fail(MSC_ERR_UNSUPPORTED, "dstate must be in [1, %lld] (got %lld)", (long long)max_dstate,
+                    (long long)dstate);
     if (batch > 65535) return fail(MSC_ERR_UNSUPPORTED, "batch must be <= 65535");
     if (dim > (int64_t)1 << 36) return fail(MSC_ERR_UNSUPPORTED, "dim too large");
     // the largest element index must fit comfortably in int64 arithmetic
@@ -133,7 +136,7 @@ const char* msc_last_error(void) { return g_last_error; }
 
 size_t msc_selective_scan_fwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
                                              int64_t dstate) {
-    if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > 16) return 0;
+    if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > MSC_S6_FWD_MAX_DSTATE) return 0;
     return s6_fwd_plan(batch, dim, seqlen, dstate).workspace;
 }
 
@@ -157,7 +160,7 @@ msc_status s6_fwd_entry(int64_t batch, int64_t dim, int64_t seqlen, int64_t dsta
                         float* h_last, void* workspace, size_t workspace_bytes, void* stream,
                         size_t max_required) {
     clear_error();
-    msc_status s = check_s6_dims(batch, dim, seqlen, dstate, in_dtype);
+    msc_status s = check_s6_dims(batch, dim, seqlen, dstate, in_dtype, MSC_S6_FWD_MAX_DSTATE);
     if (s != MSC_OK) return s;
     MSC_REQUIRE(disc == MSC_DISC_EULER || disc == MSC_DISC_ZOH || disc == MSC_DISC_TRAPEZOID,
                 "disc must be MSC_DISC_EULER, MSC_DISC_ZOH or MSC_DISC_TRAPEZOID");

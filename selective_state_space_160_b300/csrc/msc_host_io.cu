@@ -69,7 +69,7 @@ extern "C" {
 
 size_t msc_selective_scan_fwd_host_staging_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                                 msc_dtype in_dtype, int has_z, int64_t chunk_batch) {
-    if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > 16 || chunk_batch < 1) return 0;
+    if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > MSC_S6_FWD_MAX_DSTATE || chunk_batch < 1) return 0;
     if (in_dtype != MSC_F32 && in_dtype != MSC_BF16) return 0;
     const int64_t cb = chunk_batch < batch ? chunk_batch : batch;
     const size_t es = in_dtype == MSC_BF16 ? 2 : 4;

@@ -45,7 +45,7 @@ extern "C" msc_status msc_selective_scan_fwd_noalloc(int64_t batch, int64_t dim,
     // the check below guards that.  The chained schedule's optional scratch is
     // used when it fits.
     size_t need = 0;
-    if (batch >= 1 && dim >= 1 && seqlen >= 1 && dstate >= 1 && dstate <= 16) {
+    if (batch >= 1 && dim >= 1 && seqlen >= 1 && dstate >= 1 && dstate <= MSC_S6_FWD_MAX_DSTATE) {
         const msc_host::S6Plan plan =
             msc_host::s6_fwd_plan(batch, dim, seqlen, dstate, (size_t)MSC_STATIC_SCRATCH_BYTES);
         if (plan.workspace_required) need = plan.workspace;

@@ -59,8 +59,11 @@ namespace {
 
 constexpr int kRows = 32;  // channel rows per CTA (one per lane)
 constexpr int kT = 32;     // timesteps per staged tile
-constexpr int kNS = 16;    // state slots per lane (dstate <= 16)
+constexpr int kNS = 16;    // state slots of the plain-load kernel, the checkpoints and the fused conv
 constexpr int kStride = kT + 4;
+
+// State slots of a row in the TMA forward: 16, 32 or 64 (dstate <= 64).
+inline int state_slots(int64_t N) { return N <= 16 ? 16 : N <= 32 ? 32 : 64; }
 
 enum { kModeFull = 0, kModeAgg = 1, kModeCkpt = 2 };
 // input-term discretisation (values of msc_discretization)
@@ -341,10 +344,9 @@ __device__ __forceinline__ bool wait_flag_geq(const unsigned* flag, unsigned tar
 
 constexpr int kStages = 2;
 constexpr int kRowTile = 2048;               // bytes of one 32-row x 64-byte tile
-constexpr int kBCTile = 1024;                // bytes of one 16-slot x 64-byte tile
-constexpr int kStageBytes = 3 * kRowTile + 2 * kBCTile;
 // Issues the TMA loads of one tile (u, delta, [z], B, [C]) into `st`.
 __device__ __forceinline__ void issue_tile(int, int64_t tj64, uint8_t* st, uint64_t* bar, uint32_t tx_bytes,
+                                           uint32_t bc_tile,
                                            const CUtensorMap* tu, const CUtensorMap* td, const CUtensorMap* tz,
                                            const CUtensorMap* tb, const CUtensorMap* tc, int64_t d0, int64_t b,
                                            bool has_z, bool with_c) {
@@ -354,7 +356,7 @@ __device__ __forceinline__ void issue_tile(int, int64_t tj64, uint8_t* st, uint6
     msc::tma_load_3d(st + kRowTile, td, bar, tj, (int)d0, (int)b);
     if (has_z) msc::tma_load_3d(st + 2 * kRowTile, tz, bar, tj, (int)d0, (int)b);
     msc::tma_load_3d(st + 3 * kRowTile, tb, bar, tj, 0, (int)b);
-    if (with_c) msc::tma_load_3d(st + 3 * kRowTile + kBCTile, tc, bar, tj, 0, (int)b);
+    if (with_c) msc::tma_load_3d(st + 3 * kRowTile + bc_tile, tc, bar, tj, 0, (int)b);
 }
 
 // One level of the readout reduce-scatter: lanes that differ in bit `kSL` of
@@ -394,7 +396,7 @@ __device__ __forceinline__ void reduce_scatter_level(float* v, int j) {
 // previous group, which the second lane keeps in registers across groups and
 // tiles; at a segment start they are read from memory), so u never goes
 // through HBM.
-template <bool kBF16, int kMode, int kNG, int kDisc = kDiscEuler, bool kConv = false>
+template <bool kBF16, int kMode, int kNG, int kDisc = kDiscEuler, bool kConv = false, int kSN = kNS>
 __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                                                               const __grid_constant__ CUtensorMap tm_d,
                                                               const __grid_constant__ CUtensorMap tm_z,
@@ -406,10 +408,18 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
     constexpr int kGroups = kTT / 8;
     constexpr int kPitch = 2 * kTT + 4;   // floats per n-pair row of s_bc (padded: conflict-free stores)
     constexpr int kES = kBF16 ? 2 : 4;    // bytes per element
-    constexpr int kPPL = 8 / kNG;         // state pairs per lane
+    constexpr int kPPL = kSN / (2 * kNG); // state pairs per lane
     constexpr int kSPG = 8 / kNG;         // steps per lane per 8-step group
-    __shared__ __align__(1024) uint8_t s_raw[kStages][kStageBytes];
-    __shared__ __align__(16) float s_bc[2][kNS / 2][kPitch];  // [B|C][n pair][t * 2 + n parity]
+    constexpr int kBCT = kSN * 64;        // bytes of one B or C tile (kSN slots x 64 bytes)
+    constexpr int kSB = 3 * kRowTile + 2 * kBCT;
+    static_assert(kSN == kNS || (kMode == kModeFull || kMode == kModeAgg), "checkpoints are kept for 16 states");
+    static_assert(!kConv || kSN == kNS, "the fused conv front end runs with up to 16 states");
+    __shared__ __align__(1024) uint8_t s_raw[kStages][kSB];
+    // [B|C][lane j of a row][n pair q - kPPL j][t * 2 + n parity]: each lane's kPPL
+    // rows, then kSkew floats, so that the four lanes of a row read distinct banks
+    // (without the skew their rows are 0 mod 32 banks apart)
+    constexpr int kSkew = kSN == kNS ? 0 : 8;
+    __shared__ __align__(16) float s_bc[2][kNG][kPPL * kPitch + kSkew];
     __shared__ __align__(8) uint64_t s_full[kStages];
 
     const int tid = threadIdx.x;
@@ -485,7 +495,7 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
             h[e] = 0.f;
             if (kFull && row_ok && n < N) {
                 if (chained_in)
-                    h[e] = __ldcg(p.chain_state + row * 16 + n);
+                    h[e] = __ldcg(p.chain_state + row * kSN + n);
                 else if (p.G > 1)
                     h[e] = p.seg_state[((size_t)row * p.G + seg) * N + n];
                 else if (p.h0 && seg == 0)
@@ -554,12 +564,12 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
         }
     }
     const int ntiles = (int)((t_end - t_begin + kTT - 1) / kTT);
-    const uint32_t tx_bytes = kRowTile * (has_z ? 3 : 2) + kBCTile * (kFull ? 2 : 1);
+    const uint32_t tx_bytes = kRowTile * (has_z ? 3 : 2) + kBCT * (kFull ? 2 : 1);
 
     if (tid == 0)
         for (int jt = 0; jt < kStages && jt < ntiles; ++jt)
             issue_tile(jt, t_begin + (int64_t)jt * kTT, s_raw[(tbase + jt) % kStages], &s_full[(tbase + jt) % kStages],
-                       tx_bytes, &tm_u, &tm_d, &tm_z, &tm_B, &tm_C, d0, b, has_z, kFull);
+                       tx_bytes, kBCT, &tm_u, &tm_d, &tm_z, &tm_B, &tm_C, d0, b, has_z, kFull);
     int issued = ntiles < kStages ? ntiles : kStages;
 
     bool failed = false;
@@ -577,14 +587,18 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
         const int64_t t0 = t_begin + (int64_t)i * kTT;
         const int nt = (int)imin64(kTT, t_end - t0);
 
-        // B (and C) of this tile -> fp32 pairs s_bc[x][q][2t + e] = X[n = 2q + e][t]
-        if (tid < 64) {
-            const int x = tid >> 5, q = lane & 7, c = lane >> 3;
-            if (x == 0 || kFull) {
-                const uint8_t* src = raw + 3 * kRowTile + x * kBCTile;
+        // B (and C) of this tile -> fp32 pairs s_bc[x][q][2t + e] = X[n = 2q + e][t];
+        // one task per (B|C, n pair q, 16-byte chunk c)
+        constexpr int kTasks = (kFull ? 2 : 1) * 2 * kSN;
+#pragma unroll
+        for (int it = 0; it < (kTasks + 32 * kNG - 1) / (32 * kNG); ++it) {
+            const int task = tid + it * 32 * kNG;
+            const int x = task / (2 * kSN), q = task % (kSN / 2), c = (task % (2 * kSN)) / (kSN / 2);
+            if (task < kTasks) {
+                const uint8_t* src = raw + 3 * kRowTile + x * kBCT;
                 const uint4 v0 = *reinterpret_cast<const uint4*>(src + msc::sw64(2 * q, c));
                 const uint4 v1 = *reinterpret_cast<const uint4*>(src + msc::sw64(2 * q + 1, c));
-                float* dst = &s_bc[x][q][0];
+                float* dst = &s_bc[x][q / kPPL][(q % kPPL) * kPitch];
                 if constexpr (kBF16) {
                     const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
@@ -716,8 +730,8 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
             }
             // ---- the scan: 8 steps, kPPL independent state pairs per step
             uint64_t acc[8];
-            const float* bsrc = &s_bc[0][kPPL * j][16 * g];
-            const float* csrc = &s_bc[1][kPPL * j][16 * g];
+            const float* bsrc = &s_bc[0][j][16 * g];
+            const float* csrc = &s_bc[1][j][16 * g];
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 uint64_t Bp[kPPL][2], Cp[kPPL][2];
@@ -831,7 +845,7 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
         __syncthreads();
         if (tid == 0 && issued < ntiles) {
             const uint32_t si = (tbase + issued) % kStages;
-            issue_tile(issued, t_begin + (int64_t)issued * kTT, s_raw[si], &s_full[si], tx_bytes, &tm_u, &tm_d,
+            issue_tile(issued, t_begin + (int64_t)issued * kTT, s_raw[si], &s_full[si], tx_bytes, kBCT, &tm_u, &tm_d,
                        &tm_z, &tm_B, &tm_C, d0, b, has_z, kFull);
         }
         ++issued;
@@ -861,7 +875,7 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
             const int n = 2 * (kPPL * j + q);
             if (kFull) {
                 if (publish) {
-                    *reinterpret_cast<uint64_t*>(p.chain_state + row * 16 + n) = h2[q];
+                    *reinterpret_cast<uint64_t*>(p.chain_state + row * kSN + n) = h2[q];
                 } else if (p.h_last && t_end == p.L) {
                     if (n < N) p.h_last[row * N + n] = v0;
                     if (n + 1 < N) p.h_last[row * N + n + 1] = v1;
@@ -941,7 +955,7 @@ bool make_maps(FwdMaps& m, const FwdParams& p, int64_t batch, bool bf16) {
     const uint32_t rbox[3] = {tt, (uint32_t)kRows, 1};
     const uint64_t bdims[3] = {(uint64_t)p.L, (uint64_t)p.N, (uint64_t)batch};
     const uint64_t bstr[2] = {(uint64_t)p.L * es, (uint64_t)p.N * p.L * es};
-    const uint32_t bbox[3] = {tt, (uint32_t)kNS, 1};
+    const uint32_t bbox[3] = {tt, (uint32_t)state_slots(p.N), 1};
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
     if (!msc_host::encode_tmap(&m.u, dt, 3, p.u, rdims, rstr, rbox, sw)) return false;
     if (!msc_host::encode_tmap(&m.d, dt, 3, p.delta, rdims, rstr, rbox, sw)) return false;
@@ -973,38 +987,60 @@ int resident_ctas(K kernel, int threads) {
     return per_sm[dev & 63].load();
 }
 
-template <bool kBF16, int kNG, int kDisc = kDiscEuler, bool kConv = false>
+template <bool kBF16, int kNG, int kDisc = kDiscEuler, bool kConv = false, int kSN = kNS>
 msc_status launch_tma_ng(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
     if (mode == kModeFull && p.ctr) {
         // persistent: at most one CTA per row block, so that the chunk before a
         // ticket's chunk was taken a full round earlier and is normally done
-        auto kern = s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc, kConv>;
+        auto kern = s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc, kConv, kSN>;
         const int64_t slots = (int64_t)resident_ctas(kern, 32 * kNG) * msc_host::num_sms();
         const int64_t n = std::min<int64_t>(slots, std::min<int64_t>(p.chains, p.total_items));
         kern<<<(unsigned)n, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
-    } else if (mode == kModeFull)
-        s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc, kConv><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
-    else if (mode == kModeAgg)
-        s6_fwd_tma_kernel<kBF16, kModeAgg, kNG, kDisc, kConv><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
-    else if (kDisc == kDiscEuler && !kConv)
+    } else if (mode == kModeFull) {
+        s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc, kConv, kSN>
+            <<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    } else if (mode == kModeAgg) {
+        s6_fwd_tma_kernel<kBF16, kModeAgg, kNG, kDisc, kConv, kSN>
+            <<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    } else if constexpr (kDisc == kDiscEuler && !kConv && kSN == kNS) {
         s6_fwd_tma_kernel<kBF16, kModeCkpt, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
-    else
-        return msc_host::fail(MSC_ERR_UNSUPPORTED, "checkpoints are kept for the exponential-Euler form only");
+    } else {
+        return msc_host::fail(MSC_ERR_UNSUPPORTED,
+                              "checkpoints are kept for the exponential-Euler form with up to 16 states only");
+    }
     return msc_host::check_launch("s6_fwd_tma");
+}
+
+// Up to 16 states: two lanes per row, eight states each.  17 to 32: four lanes
+// of eight states; 33 to 64: four lanes of sixteen.  Slots past N hold A = 0,
+// B = C = 0 (the TMA box reads zeros past the tensor's state extent), so they
+// add nothing to the readout.
+template <bool kBF16, int kSN>
+msc_status launch_tma_sn(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, int disc,
+                         cudaStream_t st) {
+    constexpr int kNG = kSN == kNS ? kLanesPerRow : 4;
+    if (p.conv_w) {
+        if constexpr (kSN == kNS) {
+            if (disc != kDiscEuler)
+                return msc_host::fail(MSC_ERR_UNSUPPORTED,
+                                      "the fused conv front end runs with the exponential-Euler form");
+            return launch_tma_ng<kBF16, 2, kDiscEuler, true>(m, p, batch, G, mode, st);
+        } else {
+            return msc_host::fail(MSC_ERR_UNSUPPORTED, "the fused conv front end runs with up to 16 states");
+        }
+    }
+    if (disc == kDiscZoh) return launch_tma_ng<kBF16, kNG, kDiscZoh, false, kSN>(m, p, batch, G, mode, st);
+    if (disc == kDiscTrap) return launch_tma_ng<kBF16, kNG, kDiscTrap, false, kSN>(m, p, batch, G, mode, st);
+    return launch_tma_ng<kBF16, kNG, kDiscEuler, false, kSN>(m, p, batch, G, mode, st);
 }
 
 template <bool kBF16>
 msc_status launch_tma(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, int disc,
                       cudaStream_t st) {
-    if (p.conv_w) {
-        if (disc != kDiscEuler)
-            return msc_host::fail(MSC_ERR_UNSUPPORTED, "the fused conv front end runs with the exponential-Euler form");
-        return launch_tma_ng<kBF16, 2, kDiscEuler, true>(m, p, batch, G, mode, st);
-    }
-    if (disc == kDiscZoh) return launch_tma_ng<kBF16, kLanesPerRow, kDiscZoh>(m, p, batch, G, mode, st);
-    if (disc == kDiscTrap) return launch_tma_ng<kBF16, kLanesPerRow, kDiscTrap>(m, p, batch, G, mode, st);
-    return launch_tma_ng<kBF16, kLanesPerRow>(m, p, batch, G, mode, st);
+    if (p.N <= 16) return launch_tma_sn<kBF16, 16>(m, p, batch, G, mode, disc, st);
+    if (p.N <= 32) return launch_tma_sn<kBF16, 32>(m, p, batch, G, mode, disc, st);
+    return launch_tma_sn<kBF16, 64>(m, p, batch, G, mode, disc, st);
 }
 
 // TMA needs every row stride to be a multiple of 16 bytes.
@@ -1022,6 +1058,11 @@ msc_status launch_mode(const FwdParams& p, const FwdMaps* maps, bool bf16, bool 
     if (maps)
         return bf16 ? launch_tma<true>(*maps, p, batch, G, mode, disc, st)
                     : launch_tma<false>(*maps, p, batch, G, mode, disc, st);
+    if (p.N > kNS)
+        return msc_host::fail(MSC_ERR_UNSUPPORTED,
+                              "more than 16 states need 16-byte row strides "
+                              "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) "
+                              "and seqlen, dim below 2^31");
     if (p.conv_w)
         return msc_host::fail(MSC_ERR_UNSUPPORTED,
                               "the fused conv front end needs 16-byte row strides "
@@ -1067,7 +1108,10 @@ S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, s
     S6Plan plan;
     const int64_t rows = batch * dim;
     const int64_t chains = batch * cdiv64(dim, kRows);
-    const int64_t W = 8 * (int64_t)num_sms();  // full-pass CTAs resident per SM (126-128 registers)
+    // full-pass CTAs resident per SM: 8 with up to 16 states (64 threads, 126-128
+    // registers), 4 with 32 or 64 state slots (128 threads, 126-128 registers)
+    const int slots = state_slots(dstate);
+    const int64_t W = (slots == 16 ? 8 : 4) * (int64_t)num_sms();
     plan.G = 1;
     plan.seg_len = seqlen;
     plan.chunks = 1;
@@ -1082,7 +1126,7 @@ S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, s
             plan.ctrl_off = 0;
             plan.ctrl_bytes = align256(256 + (size_t)chains * sizeof(unsigned));
             plan.chain_state_off = plan.ctrl_bytes;
-            plan.workspace = plan.chain_state_off + (size_t)rows * 16 * sizeof(float);
+            plan.workspace = plan.chain_state_off + (size_t)rows * slots * sizeof(float);
             plan.workspace_required = false;
         }
         return plan;

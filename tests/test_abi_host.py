@@ -69,8 +69,12 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, L=0) == msc.MSC_ERR_INVALID_ARG
     assert _fwd(lib, batch=-1) == msc.MSC_ERR_INVALID_ARG
     assert _fwd(lib, dt=7) == msc.MSC_ERR_INVALID_ARG
-    assert _fwd(lib, N=17) == msc.MSC_ERR_UNSUPPORTED
+    assert _fwd(lib, N=65) == msc.MSC_ERR_UNSUPPORTED
     assert _fwd(lib, N=0) == msc.MSC_ERR_UNSUPPORTED
+    # 17..64 states stream through TMA only: rows of 63 fp32 steps (252 bytes)
+    # are refused before any launch
+    assert _fwd(lib, N=17, L=63) == msc.MSC_ERR_UNSUPPORTED
+    assert "16 states" in msc.msc_last_error()
     assert _fwd(lib, z=20) == msc.MSC_ERR_INVALID_ARG
 
 
@@ -88,6 +92,12 @@ def test_fwd_workspace_query_and_check(lib):
     assert _fwd(lib, batch=1, dim=1536, L=1 << 20) == msc.MSC_ERR_WORKSPACE
     assert _fwd(lib, batch=1, dim=1536, L=1 << 20, ws=4096, wsb=need - 1) == msc.MSC_ERR_WORKSPACE
     assert msc.msc_selective_scan_fwd_workspace_size(0, 4, 4, 4) == 0
+    # 32 and 64 state slots: the hand-over holds every slot; 65 states: no plan
+    for N, slots in ((17, 32), (32, 32), (33, 64), (64, 64)):
+        need = msc.msc_selective_scan_fwd_workspace_size(8, 5120, 2048, N)
+        assert 40960 * slots * 4 + 256 + 1280 * 4 <= need <= 40960 * slots * 4 + 256 + 1280 * 4 + 256, N
+    assert msc.msc_selective_scan_fwd_workspace_size(8, 5120, 2048, 65) == 0
+    assert msc.msc_selective_scan_fwd_workspace_size(1, 1536, 1 << 20, 64) > 0
 
 
 def test_bwd_rejects_bad_arguments(lib):
@@ -105,6 +115,10 @@ def test_bwd_rejects_bad_arguments(lib):
     ws = msc.msc_selective_scan_bwd_workspace_size(1, 4, big, 16)
     st = f(1, 4, big, 16, 1, *ok, None, None, None, 16, 16, 16, 16, 16, 16, None, None, None, 4096, ws, None)
     assert st == msc.MSC_ERR_UNSUPPORTED and "2^31" in msc.msc_last_error()
+    # the backward keeps 16 states (the forward takes up to 64)
+    st = f(1, 4, 64, 17, 0, *ok, None, None, None, 16, 16, 16, 16, 16, 16, None, None, None, None, 0, None)
+    assert st == msc.MSC_ERR_UNSUPPORTED and "[1, 16]" in msc.msc_last_error()
+    assert msc.msc_selective_scan_bwd_workspace_size(1, 4, 64, 17) == 0
 
 
 def test_ssd_rejects_bad_arguments(lib):
