@@ -27,23 +27,31 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
-// softplus(x) = log(1 + e^x) = max(x, 0) + log1p(w), w = e^{-|x|} in (0, 1].
-// log1p(w) = 2 atanh(s) with s = w / (2 + w) in (0, 1/3], summed as the odd
-// series 2 (s + s^3/3 + ... + s^13/13); the first omitted term is below 2e-8 of
-// the result, so the value is good to a few fp32 ulps for every x.  For x > 20
-// the log1p term is below 2.1e-9 and x itself is returned.
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2(1 + w) for w in [0, 1]: MUFU lg2 of 1 + w for w >= 2^-6; below, where
+// lg2's absolute error and the rounding of 1 + w are large against the
+// result, the series log2(e) (w - w^2/2 + w^3/3), whose first omitted term
+// (w^4/4) is below 3e-7 of the result there.
+__device__ __forceinline__ float log2_1p_unit(float w) {
+    const float l = lg2_approx(1.f + w);
+    const float s = w * fmaf(w, fmaf(w, MSC_LOG2E / 3.f, -0.5f * MSC_LOG2E), MSC_LOG2E);
+    return w < 0x1p-6f ? s : l;
+}
+
+// softplus(x) = log(1 + e^x) = max(x, 0) + ln2 log2(1 + w), w = e^{-|x|} in (0, 1].
+// The log1p term takes MUFU lg2 and a few ALU ops rather than a long FMA-pipe
+// series, which leaves the FMA pipe to the recurrence.  For x > 20 the term is
+// below half an ulp of x, so the sum rounds to x exactly.  softplus_2 in
+// msc_tma.cuh runs the same operations on each half of a pair, so the two give
+// identical bits.
 __device__ __forceinline__ float softplus_f(float x) {
-    if (x > 20.f) return x;
-    float w = ex2_approx(-fabsf(x) * MSC_LOG2E);
-    float s = w * rcp_approx(2.f + w);
-    float s2 = s * s;
-    float p = fmaf(s2, 1.f / 13.f, 1.f / 11.f);
-    p = fmaf(s2, p, 1.f / 9.f);
-    p = fmaf(s2, p, 1.f / 7.f);
-    p = fmaf(s2, p, 1.f / 5.f);
-    p = fmaf(s2, p, 1.f / 3.f);
-    p = fmaf(s2, p, 1.f);
-    return fmaxf(x, 0.f) + 2.f * s * p;
+    const float w = ex2_approx(-fabsf(x) * MSC_LOG2E);
+    return fmaf(log2_1p_unit(w), MSC_LN2, fmaxf(x, 0.f));
 }
 
 // logistic sigmoid 1 / (1 + e^-x); for x -> -inf, e^-x -> inf and rcp -> 0.

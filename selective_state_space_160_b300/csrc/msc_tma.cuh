@@ -180,22 +180,15 @@ __device__ __forceinline__ uint64_t rcp_2(uint64_t x) {
     return pk2(ra, rb);
 }
 
-// softplus of two values at once: max(x, 0) + log1p(e^-|x|), log1p(w) =
-// 2 atanh(w / (2 + w)) summed to s^13 (see softplus_f); for x > 20 the log1p
-// term is below half an ulp of x, so the sum rounds to x exactly.
+// softplus of two values, each half exactly as softplus_f (msc_common.cuh):
+// max(x, 0) + ln2 log2(1 + e^{-|x|}), the log term by MUFU lg2 (a series for
+// e^{-|x|} < 2^-6).
 __device__ __forceinline__ uint64_t softplus_2(uint64_t x) {
     float x0, x1;
     upk2(x, x0, x1);
-    const uint64_t w = ex2_2(pk2(-fabsf(x0) * MSC_LOG2E, -fabsf(x1) * MSC_LOG2E));
-    const uint64_t s = mul2(w, rcp_2(add2(w, pk2(2.f, 2.f))));
-    const uint64_t s2 = mul2(s, s);
-    uint64_t p = fma2(s2, pk2(2.f / 13.f, 2.f / 13.f), pk2(2.f / 11.f, 2.f / 11.f));
-    p = fma2(s2, p, pk2(2.f / 9.f, 2.f / 9.f));
-    p = fma2(s2, p, pk2(2.f / 7.f, 2.f / 7.f));
-    p = fma2(s2, p, pk2(2.f / 5.f, 2.f / 5.f));
-    p = fma2(s2, p, pk2(2.f / 3.f, 2.f / 3.f));
-    p = fma2(s2, p, pk2(2.f, 2.f));
-    return fma2(s, p, pk2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)));
+    float w0, w1;
+    upk2(ex2_2(pk2(-fabsf(x0) * MSC_LOG2E, -fabsf(x1) * MSC_LOG2E)), w0, w1);
+    return fma2(pk2(log2_1p_unit(w0), log2_1p_unit(w1)), pk2(MSC_LN2, MSC_LN2), pk2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)));
 }
 
 // silu of two values: z / (1 + e^-z)

@@ -749,7 +749,7 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
                     const int k = 2 * kk + e;
                     const uint64_t dt2 = msc::pk2(dts[k], dts[k]);
                     const uint64_t dtu2 = msc::pk2(dtus[k], dtus[k]);
-                    uint64_t acc_a = 0ull, acc_b = 0ull;
+                    uint64_t acc_a = 0ull;
                     float rdt = 0.f;
                     if constexpr (kDisc == kDiscZoh) rdt = dts[k] > 0.f ? msc::rcp_approx(dts[k]) : 0.f;
                     if constexpr (kDisc == kDiscTrap) {
@@ -783,14 +783,11 @@ __global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_const
                             h2[q] = msc::fma2(a, msc::add2(h2[q], ep2[q]), e2);
                             ep2[q] = e2;
                         }
-                        if (kFull) {
-                            if (q == 0) acc_a = msc::mul2(Cp[q][e], h2[q]);
-                            else if (q == 1) acc_b = msc::mul2(Cp[q][e], h2[q]);
-                            else if (q % 2 == 0) acc_a = msc::fma2(Cp[q][e], h2[q], acc_a);
-                            else acc_b = msc::fma2(Cp[q][e], h2[q], acc_b);
-                        }
+                        // readout: one accumulator chain over the lane's pairs (the
+                        // eight steps in flight hide its latency)
+                        if (kFull) acc_a = q == 0 ? msc::mul2(Cp[q][e], h2[q]) : msc::fma2(Cp[q][e], h2[q], acc_a);
                     }
-                    if (kFull) acc[k] = (kPPL > 1) ? msc::add2(acc_a, acc_b) : acc_a;
+                    if (kFull) acc[k] = acc_a;
                 }
             }
             // ---- readout + skip + gate of this lane's steps

@@ -151,3 +151,36 @@ def test_device_status_clean_after_runs():
     inp = s6_inputs(1, 64, 512, 16, seed=2, bf16=True)
     _run(inp, True)
     msc.msc_check_device_status()
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_softplus_of_delta_through_one_step(bf16):
+    """With A = 0, B = C = u = 1 and no skip or gate, y at t = 0 is Delta_0 =
+    softplus(delta_0 + Delta_bias) itself ("Mamba: Linear-Time Sequence
+    Modeling with Selective State Spaces", sec. 3.2: tau_Delta = softplus):
+    checked against log(1 + e^x) in fp64 over x in [-30, 30], relative error
+    at most 2e-5 (the kernel takes log1p from MUFU lg2, with a series below
+    e^-|x| = 2^-6)."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    x = np.linspace(-30.0, 30.0, 24001)
+    if bf16:
+        # bf16 delta: the values the kernel sees, plus a bias in fp32 to fill the gaps
+        xd = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    else:
+        xd = x.astype(np.float32)
+    dim, L = x.size, 8
+    dt = torch.bfloat16 if bf16 else torch.float32
+    delta = torch.zeros((1, dim, L), dtype=dt, device="cuda")
+    delta[0, :, 0] = torch.from_numpy(xd).to(dt).cuda()
+    bias = torch.from_numpy((x - xd).astype(np.float32)).cuda() if bf16 else None
+    u = torch.ones((1, dim, L), dtype=dt, device="cuda")
+    B = torch.ones((1, 1, L), dtype=dt, device="cuda")
+    A = torch.zeros((dim, 1), dtype=torch.float32, device="cuda")
+    y = msc.msc_selective_scan_fwd(u, delta, A, B, B.clone(), None, None, bias)
+    got = y[0, :, 0].double().cpu().numpy()
+    xin = xd.astype(np.float64) + (0.0 if bias is None else bias.double().cpu().numpy())
+    ref = np.logaddexp(0.0, xin)
+    rel = np.abs(got - ref) / ref
+    assert np.all(np.isfinite(got))
+    assert rel.max() <= 2e-5, (xin[rel.argmax()], rel.max())
