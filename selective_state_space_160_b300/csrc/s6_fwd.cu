@@ -396,8 +396,14 @@ __device__ __forceinline__ void reduce_scatter_level(float* v, int j) {
 // previous group, which the second lane keeps in registers across groups and
 // tiles; at a segment start they are read from memory), so u never goes
 // through HBM.
+// Resident CTAs asked of the compiler (0: its own choice), as timed best at
+// 8 x 5120 x 2048: 16 slots: its choice (126-128 registers, 8 per SM); 32 slots:
+// its choice with bf16 (96 registers, 5 per SM), 4 with fp32; 64 slots: 3.
+template <bool kBF16, int kSN>
+constexpr int fwd_min_ctas() { return kSN == 16 ? 0 : kSN == 32 ? (kBF16 ? 0 : 4) : 3; }
+
 template <bool kBF16, int kMode, int kNG, int kDisc = kDiscEuler, bool kConv = false, int kSN = kNS>
-__global__ void __launch_bounds__(32 * kNG) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
+__global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                                                               const __grid_constant__ CUtensorMap tm_d,
                                                               const __grid_constant__ CUtensorMap tm_z,
                                                               const __grid_constant__ CUtensorMap tm_B,
@@ -1106,9 +1112,9 @@ S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, s
     const int64_t rows = batch * dim;
     const int64_t chains = batch * cdiv64(dim, kRows);
     // full-pass CTAs resident per SM: 8 with up to 16 states (64 threads, 126-128
-    // registers), 4 with 32 or 64 state slots (128 threads, 126-128 registers)
+    // registers), 4 or 5 with 32 state slots, 3 with 64 (128 threads)
     const int slots = state_slots(dstate);
-    const int64_t W = (slots == 16 ? 8 : 4) * (int64_t)num_sms();
+    const int64_t W = (slots == 16 ? 8 : slots == 32 ? 4 : 3) * (int64_t)num_sms();
     plan.G = 1;
     plan.seg_len = seqlen;
     plan.chunks = 1;
