@@ -399,8 +399,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
     uint8_t* sX = sBM + 65536;                   // 2 x: x [Qi j][64 p], MN-major
     uint8_t* sH = sX + 65536;                    // Hin hi [2 kb][64 p][128 B], then lo
     float* s_dc = reinterpret_cast<float*>(sH + 32768);  // [2 buffers][Delta, cs][256]
-    float* s_w = s_dc + 1024;                    // per compute warp: log2(Delta_j) - cs_j log2(e), 64 columns
-    float* s_D = s_w + kScanCompute * 64;        // D of the block's heads
+    float* s_w = s_dc + 1024;                    // per compute warp: log2(Delta_j), then -cs_j, 64 columns each
+    float* s_D = s_w + kScanCompute * 128;       // D of the block's heads
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_D + 64);
     // 0 C+B loaded, 1 G done, 2-3 x full, 4 Hin full, 5 Y_off done, 6-7 quarter built (16 arrivals),
     // 8-9 quarter consumed, 10-11 x free, 12-13 head done, 14-15 accumulator free (16 arrivals), 16 drain
@@ -546,7 +546,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
         const int i_chk = ib * 128 + i_loc;
         const int row_lo = ib * 128 + 32 * lq;     // first row of this warp
         const uint32_t lane_off = (uint32_t)(32 * lq) << 16;
-        float* my_w = s_w + warp * 64;
+        float* my_w = s_w + warp * 128;  // log2(Delta_j)
+        float* my_c = my_w + 64;         // -cs_j
         bool ok = __all_sync(0xffffffffu, msc::wait_bounded(&bars[1], 0, abort, kSleepNs));
         msc::tc_fence_after();
         float csi_prev = 0.f;
@@ -568,7 +569,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
             if (release && lane == 0) msc::mbar_arrive(&bars[14 + sp]);
             const int64_t t = tc0 + i_chk;
             if (i_loc < rows_valid && t < p.L) {
-                const float e_i = msc::ex2_approx(csi_prev);
+                const float e_i = msc::ex2_approx(csi_prev * MSC_LOG2E);
                 float out[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) out[e] = fmaf(e_i, yo[e], yd[e]);
@@ -600,14 +601,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
                 for (int r = 0; r < 2; ++r) {
                     const int idx = lane + 32 * r;
                     const int j = 64 * (idx >> 4) + 16 * cslot + (idx & 15);
-                    float wv = 0.f;
+                    float wv = 0.f, cv = 0.f;
                     if (j < Qi) {
                         const float dtj = s_dt[j];
-                        wv = (dtj > 0.f ? __log2f(dtj) : -INFINITY) - s_cs[j] * MSC_LOG2E;
+                        wv = dtj > 0.f ? __log2f(dtj) : -INFINITY;
+                        cv = -s_cs[j];
                     }
                     my_w[idx] = wv;
+                    my_c[idx] = cv;
                 }
-                const float csi = s_cs[i_chk < Qi ? i_chk : 0] * MSC_LOG2E;
+                // the decay exponent is formed as (cs_i - cs_j) log2(e) + log2(Delta_j):
+                // the difference of two nearby cumulative sums is exact, so the
+                // decays near the diagonal, where they are close to 1, keep full
+                // precision however large cs grows along the chunk
+                const float csi = s_cs[i_chk < Qi ? i_chk : 0];
                 const float Dh = s_D[it];
                 __syncwarp();
                 for (int q = 0; q < nq; ++q) {
@@ -627,29 +634,37 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
                     } else {
                         float gv[16];
                         msc::tmem_ld16(tmem + tG + lane_off + (uint32_t)j0, gv);
-                        float wv[16];
+                        float wv[16], cv[16];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float4 w4 = reinterpret_cast<const float4*>(my_w + 16 * q)[e];
+                            const float4 c4 = reinterpret_cast<const float4*>(my_c + 16 * q)[e];
                             wv[4 * e] = w4.x; wv[4 * e + 1] = w4.y; wv[4 * e + 2] = w4.z; wv[4 * e + 3] = w4.w;
+                            cv[4 * e] = c4.x; cv[4 * e + 1] = c4.y; cv[4 * e + 2] = c4.z; cv[4 * e + 3] = c4.w;
                         }
                         msc::tmem_ld_wait();
                         if (j0 + 15 <= row_lo) {
                             // every column at or below every row of the warp: packed
                             // pair arithmetic, no masks
                             const uint64_t csi2 = msc::pk2(csi, csi);
+                            const uint64_t l2e2 = msc::pk2(MSC_LOG2E, MSC_LOG2E);
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
-                                const uint64_t v = msc::mul2(msc::ex2_2(msc::add2(csi2, msc::pk2(wv[2 * e], wv[2 * e + 1]))),
-                                                             msc::pk2(gv[2 * e], gv[2 * e + 1]));
+                                const uint64_t x = msc::fma2(msc::add2(csi2, msc::pk2(cv[2 * e], cv[2 * e + 1])), l2e2,
+                                                             msc::pk2(wv[2 * e], wv[2 * e + 1]));
+                                const uint64_t v = msc::mul2(msc::ex2_2(x), msc::pk2(gv[2 * e], gv[2 * e + 1]));
                                 split_bf16x2_packed(v, ph[e], pl[e]);
                             }
                         } else {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const int ja = j0 + 2 * e, jb = ja + 1;
-                                float va = (ja <= i_chk) ? gv[2 * e] * msc::ex2_approx(csi + wv[2 * e]) : 0.f;
-                                float vb = (jb <= i_chk) ? gv[2 * e + 1] * msc::ex2_approx(csi + wv[2 * e + 1]) : 0.f;
+                                float va = (ja <= i_chk)
+                                               ? gv[2 * e] * msc::ex2_approx(fmaf(csi + cv[2 * e], MSC_LOG2E, wv[2 * e]))
+                                               : 0.f;
+                                float vb = (jb <= i_chk)
+                                               ? gv[2 * e + 1] * msc::ex2_approx(fmaf(csi + cv[2 * e + 1], MSC_LOG2E, wv[2 * e + 1]))
+                                               : 0.f;
                                 if (ja == i_chk) va += Dh;
                                 if (jb == i_chk) vb += Dh;
                                 split_bf16x2(va, vb, ph[e], pl[e]);
@@ -700,7 +715,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_kernel(const __grid_
 
 size_t a256(size_t x) { return (x + 255) / 256 * 256; }
 
-constexpr int kScanSmem = 1024 + 32768 + 65536 + 65536 + 32768 + 4096 + 4096 + 256 + 17 * 8 + 8;
+constexpr int kScanSmem = 1024 + 32768 + 65536 + 65536 + 32768 + 4096 + 8192 + 256 + 17 * 8 + 8;
 
 int state_smem(int Q) { return 1024 + 6 * Q * 128 + 4096 + 64; }
 

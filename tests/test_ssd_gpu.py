@@ -84,3 +84,21 @@ def test_ssd_config_full_size_sampled_heads():
     assert max_rel_err(y[:, :, hs, :], ry) <= TOL
     assert max_rel_err(fs[:, hs], rfs) <= TOL
     msc.msc_check_device_status()
+
+
+def test_large_cumulative_decay_near_the_diagonal():
+    """A = -16 and Delta near 4: the in-chunk cumulative sum cs reaches about
+    -16 000 by the end of a 256-step chunk, while the decays that matter (the
+    diagonal and its neighbours, exp(cs_i - cs_j) for j close to i) are near 1
+    ("Mamba 解密" sec. 6.2: M_ij = a_{j+1} ... a_i).  The kernel forms the
+    exponent from the difference cs_i - cs_j, which is exact for nearby steps;
+    forming cs_i log2(e) and cs_j log2(e) apart would round each to about 1e-3
+    at this size.  The result must match the oracle to 5e-4, a quarter of the
+    bf16 tolerance."""
+    inp = ssd_inputs(1, 512, 16, 64, 128, seed=4242, with_z=True)
+    inp["A"] = np.full_like(inp["A"], -16.0)
+    inp["delta_bias"] = np.full_like(inp["delta_bias"], np.log(np.expm1(4.0)))
+    y = _run(inp, 256)
+    ref = _ref(inp)
+    assert np.all(np.isfinite(y))
+    assert max_rel_err(y, ref) <= 5e-4
