@@ -297,7 +297,11 @@ msc_status msc_causal_conv1d_update(int64_t batch, int64_t dim, int64_t width, m
  * nheads; chunk in {64, 128, 256}; seqlen >= 1 (ragged last chunk allowed).
  * The result does not depend on `chunk` beyond rounding: it only sets where
  * the chunk states are materialised.  A device-side bounded wait that runs out
- * is reported by msc_check_device_status(). */
+ * is reported by msc_check_device_status().
+ * Workspace: REQUIRED, of msc_ssd_chunked_fwd_workspace_size() bytes and
+ * 1024-byte aligned (it holds the chunk states as tensor-core operand tiles
+ * with a 128-byte swizzle, whose atoms are 1024 bytes): a smaller one returns
+ * MSC_ERR_WORKSPACE, a misaligned one MSC_ERR_INVALID_ARG. */
 size_t msc_ssd_chunked_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
                                           int64_t headdim, int64_t dstate, int64_t ngroups,
                                           int64_t chunk);
@@ -323,7 +327,9 @@ msc_status msc_ssd_chunked_fwd(int64_t batch, int64_t seqlen, int64_t nheads, in
  * With z the pre-gate output is recomputed by the forward into the workspace
  * (has_z selects the larger workspace).  dB, dC, dA, dD, ddelta_bias and the
  * cumulative-sum gradients are fp32 atomic sums: their low bits depend on the
- * order in which blocks finish. */
+ * order in which blocks finish.  Workspace: required, of
+ * msc_ssd_chunked_bwd_workspace_size() bytes, 1024-byte aligned (as the
+ * forward's). */
 size_t msc_ssd_chunked_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
                                           int64_t headdim, int64_t dstate, int64_t ngroups,
                                           int64_t chunk, int has_z);

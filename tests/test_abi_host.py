@@ -134,6 +134,8 @@ def test_ssd_rejects_bad_arguments(lib):
     assert call(dt=0) == msc.MSC_ERR_UNSUPPORTED
     assert call(ws=None, wsb=0) == msc.MSC_ERR_WORKSPACE
     assert call(ws=2048 + 16) == msc.MSC_ERR_INVALID_ARG        # workspace misaligned
+    assert call(ws=2048 + 256) == msc.MSC_ERR_INVALID_ARG       # 256-byte aligned is not enough: 1024
+    assert "1024-byte" in msc.msc_last_error()
 
 
 def test_check_device_status_null_workspace_signature(lib):
@@ -210,6 +212,8 @@ def test_ssd_bwd_rejects_bad_arguments(lib):
     assert call(bias=16) == msc.MSC_ERR_INVALID_ARG and "ddelta_bias" in msc.msc_last_error()
     assert call(ws=None, wsb=0) == msc.MSC_ERR_WORKSPACE
     assert call(ws=2048 + 16) == msc.MSC_ERR_INVALID_ARG        # workspace misaligned
+    assert call(ws=2048 + 256) == msc.MSC_ERR_INVALID_ARG       # 256-byte aligned is not enough: 1024
+    assert "1024-byte" in msc.msc_last_error()
     # the gate needs room for the recomputed pre-gate output and the forward's workspace
     no_z = msc.msc_ssd_chunked_bwd_workspace_size(2, 1000, 8, 64, 128, 1, 256, False)
     with_z = msc.msc_ssd_chunked_bwd_workspace_size(2, 1000, 8, 64, 128, 1, 256, True)
