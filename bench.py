@@ -2,7 +2,7 @@
 """Benchmark of the Mamba selective scan on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--legs fwd_long,bwd,ssd,ssd_bwd,decode,conv1d,conv1d_bwd,conv_scan,disc|none]
+                    [--legs fwd_long,bwd,train,ssd,ssd_bwd,decode,conv1d,conv1d_bwd,conv_scan,disc|none]
                     [--no-cpu-baseline]
 
 One step = one S6 forward of the Mamba-2.8B-layer workload (batch 8, d_inner
@@ -345,6 +345,43 @@ def leg_bwd(peaks, pipes, steps=5, warmup=2):
     res = {"workload": "S6 bwd batch 16, D 2048, L 2048, N 16, bf16 in / fp32 grads", "elements_per_s": el / (ms * 1e-3),
            "ms": ms, "roofline": roofline_s6(el, N, nbytes, ms, peaks, pipes, fp32_per_elem_n=12.0)}
     del inp, dy
+    torch.cuda.empty_cache()
+    return res
+
+
+def leg_train(peaks, pipes, steps=5, warmup=2):
+    """One training step of the scan (forward, then backward) at the backward's
+    workload, batch 16 x D 2048 x L 2048, N 16, bf16: the plain pair
+    (msc_selective_scan_fwd, then msc_selective_scan_bwd, which recomputes its
+    checkpoints) against the training pair (msc_selective_scan_fwd_train keeps
+    them, msc_selective_scan_bwd_ckpt starts from them)."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    batch, dim, L, N = 16, 2048, 2048, 16
+    inp = s6_fwd_workload(batch, dim, L, N, True, 160_003)
+    dy = torch.randn((batch, dim, L), device="cuda", generator=torch.Generator(device="cuda").manual_seed(3)).to(torch.bfloat16)
+    st = torch.cuda.current_stream()
+    y = torch.empty((batch, dim, L), dtype=torch.float32, device="cuda")
+    ckpt = torch.empty((batch * dim, L // 8, 16), dtype=torch.float32, device="cuda")
+    args = (inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["delta_bias"])
+
+    def plain():
+        msc.msc_selective_scan_fwd(*args, y=y)
+        msc.msc_selective_scan_bwd(*args, dy)
+
+    def paired():
+        msc.msc_selective_scan_fwd_train(*args, y=y, ckpt=ckpt)
+        msc.msc_selective_scan_bwd_ckpt(*args, dy, ckpt)
+
+    ms_plain = statistics.median(time_launches(plain, steps, warmup, st))
+    ms_pair = statistics.median(time_launches(paired, steps, warmup, st))
+    ms_fwd_train = statistics.median(time_launches(lambda: msc.msc_selective_scan_fwd_train(*args, y=y, ckpt=ckpt),
+                                                   steps, warmup, st))
+    el = batch * dim * L
+    res = {"workload": "S6 training step (fwd + bwd) batch 16, D 2048, L 2048, N 16, bf16 in / fp32 out and grads",
+           "elements_per_s": el / (ms_pair * 1e-3), "ms": ms_pair, "ms_fwd_train": ms_fwd_train,
+           "ms_fwd_then_bwd": ms_plain, "ckpt_bytes": int(ckpt.numel() * 4)}
+    del inp, dy, y, ckpt
     torch.cuda.empty_cache()
     return res
 
@@ -787,7 +824,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         for name in args.legs.split(","):
             try:
-                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "ssd": leg_ssd, "ssd_bwd": leg_ssd_bwd, "decode": leg_decode, "conv1d": leg_conv1d, "conv1d_bwd": leg_conv1d_bwd, "conv_scan": leg_conv_scan, "disc": leg_disc}[name]
+                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "train": leg_train, "ssd": leg_ssd, "ssd_bwd": leg_ssd_bwd, "decode": leg_decode, "conv1d": leg_conv1d, "conv1d_bwd": leg_conv1d_bwd, "conv_scan": leg_conv_scan, "disc": leg_disc}[name]
                 legs[name] = fn(peaks, pipes)
             except Exception as ex:  # report, do not hide: a failing leg is printed as such
                 legs[name] = {"error": "%s: %s" % (type(ex).__name__, ex)}
@@ -833,7 +870,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="fwd_long,bwd,ssd,ssd_bwd,decode,conv1d,conv1d_bwd,conv_scan,disc")
+    ap.add_argument("--legs", default="fwd_long,bwd,train,ssd,ssd_bwd,decode,conv1d,conv1d_bwd,conv_scan,disc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ssd-batch", type=int, default=4, help="batch of the SSD legs (4 = the timed workload)")

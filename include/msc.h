@@ -225,6 +225,42 @@ msc_status msc_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, in
                                   float* dD, float* dz, float* ddelta_bias,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* -------------------------------------------------------- S6 training pair
+ * For training, the forward can keep what the backward otherwise recomputes
+ * first: the state entering every 8-step group of every row, the checkpoints
+ * the backward runs its adjoint from (1/8 of the states, fp32; bqwf survey
+ * sec. 2.2: the backward recomputes the states rather than storing them all).
+ *  - msc_selective_scan_fwd_train is msc_selective_scan_fwd (zero initial
+ *    state, no final state, same workspace rules) that also writes ckpt
+ *    [batch * dim, seqlen / 8, 16] fp32, msc_selective_scan_ckpt_size() bytes:
+ *    state n entering group g of row r at ckpt[(r * (seqlen / 8) + g) * 16 + n],
+ *    zero for n >= dstate.  y equals msc_selective_scan_fwd's bit for bit.
+ *  - msc_selective_scan_bwd_ckpt is msc_selective_scan_bwd run from those
+ *    checkpoints: it skips its own checkpoint pass and takes no workspace.
+ *    When the forward runs as one pass or in chained chunks (sequences under
+ *    512 steps, or enough rows to fill the GPU) the checkpoints equal the ones
+ *    msc_selective_scan_bwd computes bit for bit, and the gradients agree up
+ *    to the order of the atomic sums; with segments (few rows, long
+ *    sequences) each segment starts from a carry that combines the states in
+ *    another order, so checkpoints and gradients differ by rounding.
+ * Limits: the backward's (dstate 1..16), seqlen a multiple of 8 and seqlen,
+ * dim below 2^31, else MSC_ERR_UNSUPPORTED; the checkpoints must come from
+ * msc_selective_scan_fwd_train on the same inputs. */
+size_t msc_selective_scan_ckpt_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
+
+msc_status msc_selective_scan_fwd_train(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                        msc_dtype in_dtype, const void* u, const void* delta, const float* A,
+                                        const void* B, const void* C, const float* D, const void* z,
+                                        const float* delta_bias, float* y, float* ckpt, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+msc_status msc_selective_scan_bwd_ckpt(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                       msc_dtype in_dtype, const void* u, const void* delta, const float* A,
+                                       const void* B, const void* C, const float* D, const void* z,
+                                       const float* delta_bias, const void* dy, const float* ckpt, float* du,
+                                       float* ddelta, float* dA, float* dB, float* dC, float* dD, float* dz,
+                                       float* ddelta_bias, void* stream);
+
 /* ------------------------------------------------------------ S6 decode step
  * One token of the same recurrence for every channel row, the state carried
  * from call to call ("Mamba — 选择性状态空间模型", 实践案例 1: what happens when

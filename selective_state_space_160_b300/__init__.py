@@ -19,6 +19,7 @@ __all__ = [
     "msc_selective_state_update", "msc_ssd_chunked_bwd_workspace_size",
     "msc_causal_conv1d_fwd", "msc_causal_conv1d_update", "msc_selective_scan_fwd_ex",
     "msc_selective_scan_fwd_conv", "msc_causal_conv1d_bwd", "msc_selective_scan_fwd_host",
+    "msc_selective_scan_fwd_train", "msc_selective_scan_bwd_ckpt", "msc_selective_scan_ckpt_size",
     "MSC_DISC_EULER", "MSC_DISC_ZOH", "MSC_DISC_TRAPEZOID",
     "msc_selective_scan_fwd_workspace_size", "msc_selective_scan_bwd_workspace_size",
     "msc_ssd_chunked_fwd_workspace_size", "msc_check_device_status", "msc_status_string",
@@ -44,6 +45,11 @@ SIGNATURES = {
     "msc_selective_scan_fwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 11 + [_vp, _sz, _vp]),
     "msc_selective_scan_bwd_workspace_size": (_sz, [_i64] * 4),
     "msc_selective_scan_bwd": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 9 + [_vp] * 8 + [_vp, _sz, _vp]),
+    "msc_selective_scan_ckpt_size": (_sz, [_i64] * 4),
+    "msc_selective_scan_fwd_train": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 8 + [_vp, _vp] +
+                                     [_vp, _sz, _vp]),
+    "msc_selective_scan_bwd_ckpt": (ctypes.c_int, [_i64] * 4 + [ctypes.c_int] + [_vp] * 9 + [_vp] + [_vp] * 8 +
+                                    [_vp]),
     "msc_ssd_chunked_fwd_workspace_size": (_sz, [_i64] * 7),
     "msc_ssd_chunked_fwd": (ctypes.c_int, [_i64] * 7 + [ctypes.c_int] + [_vp] * 10 + [_vp, _sz, _vp]),
     "msc_ssd_chunked_bwd_workspace_size": (_sz, [_i64] * 7 + [ctypes.c_int]),
@@ -433,6 +439,79 @@ def msc_selective_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, d
         *[(_dev_ptr(out[k], k, optional=True)) for k in
           ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")],
         ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream))
+    _check(st)
+    return out
+
+
+def msc_selective_scan_ckpt_size(batch, dim, seqlen, dstate) -> int:
+    return int(load_library().msc_selective_scan_ckpt_size(batch, dim, seqlen, dstate))
+
+
+def msc_selective_scan_fwd_train(u, delta, A, B, C, D=None, z=None, delta_bias=None, y=None, ckpt=None,
+                                 workspace=None, stream=None):
+    """Training forward: y as msc_selective_scan_fwd (zero initial state) and the
+    backward's checkpoints (fp32, [batch * dim, L / 8, 16]).  Returns (y, ckpt)."""
+    torch = _torch()
+    lib = load_library()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dt = _in_dtype(u)
+    tdt = u.dtype
+    f32 = torch.float32
+    if y is None:
+        y = torch.empty((batch, dim, L), dtype=f32, device=u.device)
+    if ckpt is None:
+        ckpt = torch.empty((batch * dim, max(L // 8, 1), 16), dtype=f32, device=u.device)
+    nbytes = msc_selective_scan_fwd_workspace_size(batch, dim, L, N)
+    ws, wsb = _workspace(nbytes, u.device, workspace)
+    st = lib.msc_selective_scan_fwd_train(
+        batch, dim, L, N, dt,
+        _dev_ptr(u, "u"), _dev_ptr(delta, "delta", tdt, (batch, dim, L)),
+        _dev_ptr(A, "A", f32, (dim, N)),
+        _dev_ptr(B, "B", tdt, (batch, N, L)), _dev_ptr(C, "C", tdt, (batch, N, L)),
+        _dev_ptr(D, "D", f32, (dim,), optional=True),
+        _dev_ptr(z, "z", tdt, (batch, dim, L), optional=True),
+        _dev_ptr(delta_bias, "delta_bias", f32, (dim,), optional=True),
+        _dev_ptr(y, "y", f32, (batch, dim, L)), _dev_ptr(ckpt, "ckpt", f32),
+        ws.data_ptr() if ws is not None else None, wsb, _stream_ptr(stream))
+    _check(st)
+    return y, ckpt
+
+
+def msc_selective_scan_bwd_ckpt(u, delta, A, B, C, D=None, z=None, delta_bias=None, dy=None, ckpt=None,
+                                stream=None):
+    """S6 backward from the training forward's checkpoints; gradients as
+    msc_selective_scan_bwd (a dict), no workspace."""
+    torch = _torch()
+    lib = load_library()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dt = _in_dtype(u)
+    tdt = u.dtype
+    dev = u.device
+    f32 = torch.float32
+    out = {
+        "du": torch.empty((batch, dim, L), dtype=f32, device=dev),
+        "ddelta": torch.empty((batch, dim, L), dtype=f32, device=dev),
+        "dA": torch.empty((dim, N), dtype=f32, device=dev),
+        "dB": torch.empty((batch, N, L), dtype=f32, device=dev),
+        "dC": torch.empty((batch, N, L), dtype=f32, device=dev),
+        "dD": torch.empty((dim,), dtype=f32, device=dev) if D is not None else None,
+        "dz": torch.empty((batch, dim, L), dtype=f32, device=dev) if z is not None else None,
+        "ddelta_bias": torch.empty((dim,), dtype=f32, device=dev) if delta_bias is not None else None,
+    }
+    st = lib.msc_selective_scan_bwd_ckpt(
+        batch, dim, L, N, dt,
+        _dev_ptr(u, "u"), _dev_ptr(delta, "delta", tdt, (batch, dim, L)),
+        _dev_ptr(A, "A", f32, (dim, N)),
+        _dev_ptr(B, "B", tdt, (batch, N, L)), _dev_ptr(C, "C", tdt, (batch, N, L)),
+        _dev_ptr(D, "D", f32, (dim,), optional=True),
+        _dev_ptr(z, "z", tdt, (batch, dim, L), optional=True),
+        _dev_ptr(delta_bias, "delta_bias", f32, (dim,), optional=True),
+        _dev_ptr(dy, "dy", tdt, (batch, dim, L)), _dev_ptr(ckpt, "ckpt", f32),
+        *[(_dev_ptr(out[k], k, optional=True)) for k in
+          ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")],
+        _stream_ptr(stream))
     _check(st)
     return out
 

@@ -349,6 +349,80 @@ msc_status msc_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, in
     return s6_bwd_launch(a, static_cast<cudaStream_t>(stream));
 }
 
+// The training pair's common limits: the backward's (dstate <= 16), seqlen a
+// multiple of 8 (whole checkpoint groups, 16-byte rows in both dtypes) and
+// seqlen, dim below 2^31 (32-bit TMA tile coordinates).
+static msc_status check_train_dims(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, msc_dtype dt) {
+    msc_status s = check_s6_dims(batch, dim, seqlen, dstate, dt);
+    if (s != MSC_OK) return s;
+    if (seqlen % 8 != 0)
+        return fail(MSC_ERR_UNSUPPORTED, "the training pair needs seqlen a multiple of 8 (got %lld)",
+                    (long long)seqlen);
+    constexpr int64_t kMaxCoord = ((int64_t)1 << 31) - 64;
+    if (seqlen > kMaxCoord || dim > kMaxCoord)
+        return fail(MSC_ERR_UNSUPPORTED, "the training pair needs seqlen and dim below 2^31");
+    return MSC_OK;
+}
+
+size_t msc_selective_scan_ckpt_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
+    if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > 16 || seqlen % 8 != 0) return 0;
+    return (size_t)batch * (size_t)dim * (size_t)(seqlen / 8) * 16 * sizeof(float);
+}
+
+msc_status msc_selective_scan_fwd_train(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                        msc_dtype in_dtype, const void* u, const void* delta, const float* A,
+                                        const void* B, const void* C, const float* D, const void* z,
+                                        const float* delta_bias, float* y, float* ckpt, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    clear_error();
+    msc_status s = check_train_dims(batch, dim, seqlen, dstate, in_dtype);
+    if (s != MSC_OK) return s;
+    MSC_PTR(u, "u"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A"); MSC_PTR(B, "B");
+    MSC_PTR(C, "C"); MSC_PTR(y, "y"); MSC_PTR(ckpt, "ckpt");
+    MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z"); MSC_OPT_PTR(delta_bias, "delta_bias");
+    S6Plan plan = s6_fwd_plan(batch, dim, seqlen, dstate);
+    if (plan.workspace_required && (workspace == nullptr || workspace_bytes < plan.workspace))
+        return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", plan.workspace,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (workspace != nullptr)
+        MSC_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "workspace must be 256-byte aligned");
+    S6FwdArgs a{};
+    a.batch = batch; a.dim = dim; a.L = seqlen; a.N = (int)dstate; a.bf16 = in_dtype == MSC_BF16;
+    a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C;
+    a.A = A; a.D = D; a.delta_bias = delta_bias; a.h0 = nullptr; a.y = y; a.h_last = nullptr;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace ? workspace_bytes : 0;
+    a.ckpt = ckpt;
+    return s6_fwd_launch(a, plan, static_cast<cudaStream_t>(stream));
+}
+
+msc_status msc_selective_scan_bwd_ckpt(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                       msc_dtype in_dtype, const void* u, const void* delta, const float* A,
+                                       const void* B, const void* C, const float* D, const void* z,
+                                       const float* delta_bias, const void* dy, const float* ckpt, float* du,
+                                       float* ddelta, float* dA, float* dB, float* dC, float* dD, float* dz,
+                                       float* ddelta_bias, void* stream) {
+    clear_error();
+    msc_status s = check_train_dims(batch, dim, seqlen, dstate, in_dtype);
+    if (s != MSC_OK) return s;
+    MSC_PTR(u, "u"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A"); MSC_PTR(B, "B");
+    MSC_PTR(C, "C"); MSC_PTR(dy, "dy"); MSC_PTR(ckpt, "ckpt");
+    MSC_PTR(du, "du"); MSC_PTR(ddelta, "ddelta"); MSC_PTR(dA, "dA"); MSC_PTR(dB, "dB"); MSC_PTR(dC, "dC");
+    MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z"); MSC_OPT_PTR(delta_bias, "delta_bias");
+    MSC_REQUIRE((D == nullptr) == (dD == nullptr), "dD must be given exactly when D is given");
+    MSC_REQUIRE((z == nullptr) == (dz == nullptr), "dz must be given exactly when z is given");
+    MSC_REQUIRE((delta_bias == nullptr) == (ddelta_bias == nullptr),
+                "ddelta_bias must be given exactly when delta_bias is given");
+    MSC_OPT_PTR(dD, "dD"); MSC_OPT_PTR(dz, "dz"); MSC_OPT_PTR(ddelta_bias, "ddelta_bias");
+    S6BwdArgs a{};
+    a.batch = batch; a.dim = dim; a.L = seqlen; a.N = (int)dstate; a.bf16 = in_dtype == MSC_BF16;
+    a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C; a.dy = dy;
+    a.A = A; a.D = D; a.delta_bias = delta_bias;
+    a.du = du; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dz = dz;
+    a.ddelta_bias = ddelta_bias; a.workspace = nullptr; a.ckpt_in = ckpt;
+    return s6_bwd_launch(a, static_cast<cudaStream_t>(stream));
+}
+
 size_t msc_ssd_chunked_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
                                           int64_t headdim, int64_t dstate, int64_t ngroups,
                                           int64_t chunk) {

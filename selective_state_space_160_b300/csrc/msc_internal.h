@@ -36,6 +36,8 @@ struct S6FwdArgs {
     const float* conv_w = nullptr;  // [dim, conv_k]
     const float* conv_b = nullptr;  // [dim] or null
     int conv_k = 0;
+    // training forward: also the state entering every 8-step group, [rows, L / 8, 16]
+    float* ckpt = nullptr;
 };
 
 msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t stream);
@@ -69,6 +71,9 @@ struct S6BwdArgs {
     const float *A, *D, *delta_bias;
     float *du, *ddelta, *dA, *dB, *dC, *dD, *dz, *ddelta_bias;
     void* workspace;
+    // checkpoints from the training forward ([rows, L / 8, 16], L a multiple of
+    // 8); when set the backward skips its own checkpoint pass and needs no workspace
+    const float* ckpt_in = nullptr;
 };
 
 msc_status s6_bwd_launch(const S6BwdArgs& a, cudaStream_t stream);

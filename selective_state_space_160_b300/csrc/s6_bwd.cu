@@ -535,9 +535,13 @@ msc_status s6_bwd_launch(const S6BwdArgs& a0, cudaStream_t st) {
     if (Lp > kMaxCoord || a.dim > kMaxCoord)
         return fail(MSC_ERR_UNSUPPORTED, "the backward needs seqlen and dim below 2^31");
     const size_t es = a.bf16 ? 2 : 4;
+    if (a.ckpt_in && Lp != L) return fail(MSC_ERR_UNSUPPORTED, "checkpoints need seqlen a multiple of 8");
     char* ws = static_cast<char*>(a.workspace);
-    float* ckpt = reinterpret_cast<float*>(ws);
-    ws += align256((size_t)rows * (size_t)((Lp + 7) / 8) * 16 * sizeof(float));
+    const float* ckpt = a.ckpt_in;
+    if (!ckpt) {
+        ckpt = reinterpret_cast<float*>(ws);
+        ws += align256((size_t)rows * (size_t)((Lp + 7) / 8) * 16 * sizeof(float));
+    }
 
     // outputs that are sums start at zero
     cudaError_t e = cudaSuccess;
@@ -580,12 +584,15 @@ msc_status s6_bwd_launch(const S6BwdArgs& a0, cudaStream_t st) {
         du = pdu; ddl = pdd; dz = a.dz ? pdz : nullptr; dB = pdB; dC = pdC;
     }
 
-    // (1) states entering every 8-step group
-    S6FwdArgs f{};
-    f.batch = a.batch; f.dim = a.dim; f.L = Lp; f.N = a.N; f.bf16 = a.bf16;
-    f.u = u; f.delta = dl; f.B = B; f.C = C; f.A = a.A; f.delta_bias = a.delta_bias;
-    msc_status s = s6_fwd_checkpoints(f, ckpt, st);
-    if (s != MSC_OK) return s;
+    // (1) states entering every 8-step group (unless the training forward kept them)
+    msc_status s = MSC_OK;
+    if (!a.ckpt_in) {
+        S6FwdArgs f{};
+        f.batch = a.batch; f.dim = a.dim; f.L = Lp; f.N = a.N; f.bf16 = a.bf16;
+        f.u = u; f.delta = dl; f.B = B; f.C = C; f.A = a.A; f.delta_bias = a.delta_bias;
+        s = s6_fwd_checkpoints(f, const_cast<float*>(ckpt), st);
+        if (s != MSC_OK) return s;
+    }
 
     // (2) the reverse pass
     CUtensorMap maps[6];

@@ -65,7 +65,9 @@ constexpr int kStride = kT + 4;
 // State slots of a row in the TMA forward: 16, 32 or 64 (dstate <= 64).
 inline int state_slots(int64_t N) { return N <= 16 ? 16 : N <= 32 ? 32 : 64; }
 
-enum { kModeFull = 0, kModeAgg = 1, kModeCkpt = 2 };
+// Full: y (and h_last); Agg: segment end states and Delta sums; Ckpt: the
+// state entering every 8-step group only; FullCkpt: y and those states.
+enum { kModeFull = 0, kModeAgg = 1, kModeCkpt = 2, kModeFullCkpt = 3 };
 // input-term discretisation (values of msc_discretization)
 enum { kDiscEuler = 0, kDiscZoh = 1, kDiscTrap = 2 };
 
@@ -409,7 +411,8 @@ __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd
                                                               const __grid_constant__ CUtensorMap tm_B,
                                                               const __grid_constant__ CUtensorMap tm_C,
                                                               const FwdParams p) {
-    constexpr bool kFull = (kMode == kModeFull);
+    constexpr bool kFull = (kMode == kModeFull || kMode == kModeFullCkpt);
+    constexpr bool kWriteCk = (kMode == kModeCkpt || kMode == kModeFullCkpt);
     constexpr int kTT = kBF16 ? 32 : 16;  // steps per 64-byte tile row
     constexpr int kGroups = kTT / 8;
     constexpr int kPitch = 2 * kTT + 4;   // floats per n-pair row of s_bc (padded: conflict-free stores)
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd
     constexpr int kSPG = 8 / kNG;         // steps per lane per 8-step group
     constexpr int kBCT = kSN * 64;        // bytes of one B or C tile (kSN slots x 64 bytes)
     constexpr int kSB = 3 * kRowTile + 2 * kBCT;
-    static_assert(kSN == kNS || (kMode == kModeFull || kMode == kModeAgg), "checkpoints are kept for 16 states");
+    static_assert(kSN == kNS || !kWriteCk, "checkpoints are kept for 16 states");
     static_assert(!kConv || kSN == kNS, "the fused conv front end runs with up to 16 states");
     __shared__ __align__(1024) uint8_t s_raw[kStages][kSB];
     // [B|C][lane j of a row][n pair q - kPPL j][t * 2 + n parity]: each lane's kPPL
@@ -726,7 +729,7 @@ __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd
                     dtus[k] = __shfl_sync(0xffffffffu, mdtu[k % kSPG], src);
                 }
             }
-            if (kMode == kModeCkpt && row_ok) {
+            if (kWriteCk && row_ok) {
                 // state entering this 8-step group, for the recomputing backward
                 float* cp = p.ckpt + ((size_t)row * p.ckpt_groups + (size_t)((t0 + 8 * g) >> 3)) * kNS +
                             2 * kPPL * j;
@@ -990,24 +993,37 @@ int resident_ctas(K kernel, int threads) {
     return per_sm[dev & 63].load();
 }
 
-template <bool kBF16, int kNG, int kDisc = kDiscEuler, bool kConv = false, int kSN = kNS>
-msc_status launch_tma_ng(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
-    dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
-    if (mode == kModeFull && p.ctr) {
+// A full pass: persistent CTAs taking (row block, chunk) tickets when the
+// chained schedule's control block is set, else one CTA per (row block, batch
+// entry, segment).
+template <bool kBF16, int kMode, int kNG, int kDisc, bool kConv, int kSN>
+void launch_full(const FwdMaps& m, const FwdParams& p, dim3 grid, cudaStream_t st) {
+    auto kern = s6_fwd_tma_kernel<kBF16, kMode, kNG, kDisc, kConv, kSN>;
+    if (p.ctr) {
         // persistent: at most one CTA per row block, so that the chunk before a
         // ticket's chunk was taken a full round earlier and is normally done
-        auto kern = s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc, kConv, kSN>;
         const int64_t slots = (int64_t)resident_ctas(kern, 32 * kNG) * msc_host::num_sms();
         const int64_t n = std::min<int64_t>(slots, std::min<int64_t>(p.chains, p.total_items));
         kern<<<(unsigned)n, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
-    } else if (mode == kModeFull) {
-        s6_fwd_tma_kernel<kBF16, kModeFull, kNG, kDisc, kConv, kSN>
-            <<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    } else {
+        kern<<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    }
+}
+
+template <bool kBF16, int kNG, int kDisc = kDiscEuler, bool kConv = false, int kSN = kNS>
+msc_status launch_tma_ng(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
+    constexpr bool kCkOk = kDisc == kDiscEuler && !kConv && kSN == kNS;
+    dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
+    if (mode == kModeFull) {
+        launch_full<kBF16, kModeFull, kNG, kDisc, kConv, kSN>(m, p, grid, st);
     } else if (mode == kModeAgg) {
         s6_fwd_tma_kernel<kBF16, kModeAgg, kNG, kDisc, kConv, kSN>
             <<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
-    } else if constexpr (kDisc == kDiscEuler && !kConv && kSN == kNS) {
-        s6_fwd_tma_kernel<kBF16, kModeCkpt, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+    } else if constexpr (kCkOk) {
+        if (mode == kModeFullCkpt)
+            launch_full<kBF16, kModeFullCkpt, kNG, kDisc, kConv, kSN>(m, p, grid, st);
+        else
+            s6_fwd_tma_kernel<kBF16, kModeCkpt, kNG><<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
     } else {
         return msc_host::fail(MSC_ERR_UNSUPPORTED,
                               "checkpoints are kept for the exponential-Euler form with up to 16 states only");
@@ -1061,6 +1077,9 @@ msc_status launch_mode(const FwdParams& p, const FwdMaps* maps, bool bf16, bool 
     if (maps)
         return bf16 ? launch_tma<true>(*maps, p, batch, G, mode, disc, st)
                     : launch_tma<false>(*maps, p, batch, G, mode, disc, st);
+    if (mode == kModeFullCkpt)
+        return msc_host::fail(MSC_ERR_UNSUPPORTED,
+                              "the forward with checkpoints needs 16-byte row strides and seqlen, dim below 2^31");
     if (p.N > kNS)
         return msc_host::fail(MSC_ERR_UNSUPPORTED,
                               "more than 16 states need 16-byte row strides "
@@ -1207,7 +1226,12 @@ msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st
         p.total_items = p.chains * plan.chunks;
         p.chained = 1;
     }
-    return launch_mode(p, mp, a.bf16, vec, a.batch, plan.G, kModeFull, a.disc, st);
+    if (a.ckpt) {
+        // the training forward also keeps the state entering every 8-step group
+        p.ckpt = a.ckpt;
+        p.ckpt_groups = (a.L + 7) / 8;
+    }
+    return launch_mode(p, mp, a.bf16, vec, a.batch, plan.G, a.ckpt ? kModeFullCkpt : kModeFull, a.disc, st);
 }
 
 // Checkpoint pass of the backward: the state entering every 8-step group of
