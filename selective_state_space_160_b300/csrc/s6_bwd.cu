@@ -17,14 +17,17 @@
 // entering every 8-step group (1/8 of the states, fp32) to the workspace.
 // (2) This kernel walks each row backwards: TMA streams the tiles of u, delta,
 // z, dy, B, C in reverse order into a two-stage ring; for each 8-step group it
-// takes the checkpoint (loaded one group ahead), recomputes the 8 steps forward keeping abar and
-// h_{t-1} in registers (reading only B), then runs the adjoint backwards through
-// them; the readout C h_t (for dz) and dC = g' h_t are formed there too, where C
-// is loaded anyway and h_t is the next step's h_{t-1}.  Four
+// takes the checkpoint (loaded one group ahead), recomputes the 8 steps forward keeping abar,
+// h_{t-1} and B in registers, then runs the adjoint backwards through them,
+// loading only C; the readout C h_t (for dz) and dC = g' h_t are formed there
+// too, where h_t is the next step's h_{t-1}.  Each B and C value is read from
+// shared memory once per group.  Four
 // lanes share a row (4 states each) so the two 8-step histories fit in
 // registers.  dB and dC, sums over all channels of a batch entry, are first
-// summed over the CTA's 32 rows in shared memory (conflict-free layout) and
-// then added to global memory with one 4-wide vector reduction per 4 steps.
+// summed over row pairs in registers (one shuffle exchange: each row of a pair
+// keeps half of its states), then over the CTA's 16 row pairs in shared memory
+// (conflict-free layout), and added to global memory with one 4-wide vector
+// reduction per 4 steps.
 // dA, dD and dbias are per-lane sums added once per row at the end.
 #include <cstdio>
 #include <cstdlib>
@@ -46,6 +49,9 @@ constexpr int kStageBytes = 4 * kRowTile + 2 * kBCTile;
 // 16 floats so that the two row halves summed side by side use different banks
 constexpr int kRedBlock = 32 * 16 + 32;  // floats per (x, k) block
 __host__ __device__ constexpr int red_row(int r) { return r * 16 + (r >= 16 ? 16 : 0); }
+// row pair p = r / 2 after the pairs are summed in registers; pairs 8.. shifted
+// by 16 floats so that the two halves read side by side use different banks
+__host__ __device__ constexpr int red_pair(int p) { return p * 16 + (p >= 8 ? 16 : 0); }
 
 __device__ unsigned int g_s6_bwd_status[2];
 
@@ -111,10 +117,13 @@ __device__ __forceinline__ void load2(const uint8_t* tile, int r, uint32_t boff,
     }
 }
 
-// Three CTAs per SM (168 registers, a few spilled bytes) beat the compiler's
-// own choice of two (16 x 2048 x 2048 bf16: 1.72 against 1.80 ms).
+// Two CTAs per SM (248-254 registers: the group's B pairs stay in registers
+// from the recompute to the adjoint, so the adjoint loads only C).  At 16 x
+// 2048 x 2048 bf16: 1.64 ms, against 1.72 with B loaded twice at three CTAs per
+// SM and 2.4 with B kept but squeezed into three CTAs per SM (spills); the
+// row-pair exchange of the dB/dC sums then 1.61.
 template <bool kBF16>
-__global__ void __launch_bounds__(kThreads, 3) s6_bwd_kernel(const __grid_constant__ CUtensorMap tm_u,
+__global__ void __launch_bounds__(kThreads, 2) s6_bwd_kernel(const __grid_constant__ CUtensorMap tm_u,
                                                          const __grid_constant__ CUtensorMap tm_d,
                                                          const __grid_constant__ CUtensorMap tm_z,
                                                          const __grid_constant__ CUtensorMap tm_dy,
@@ -293,16 +302,15 @@ __global__ void __launch_bounds__(kThreads, 3) s6_bwd_kernel(const __grid_consta
             float yp[8];
             const float* bsrc = &s_bc[0][2 * j][16 * g];
             const float* csrc = &s_bc[1][2 * j][16 * g];
-            // B (and, in the adjoint, C) pairs of steps (k, k + 1), k even, of state
-            // pair q: one 16-byte load each
-            uint64_t Bk[2][2], Ck[2][2];
+            // B pairs of all 8 steps, kept for the adjoint; C pairs of steps (k, k + 1)
+            uint64_t Bs[8][2], Ck[2][2];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 if ((k & 1) == 0) {
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
                         const ulonglong2 vb = *reinterpret_cast<const ulonglong2*>(bsrc + q * kPitch + 2 * k);
-                        Bk[0][q] = vb.x; Bk[1][q] = vb.y;
+                        Bs[k][q] = vb.x; Bs[k + 1][q] = vb.y;
                     }
                 }
                 const uint64_t dt2 = msc::pk2(dts[k], dts[k]);
@@ -312,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 3) s6_bwd_kernel(const __grid_consta
                     const uint64_t a = msc::ex2_2(msc::mul2(dt2, A2p[q]));
                     ah[k][q] = a;
                     hp[k][q] = h[q];
-                    h[q] = msc::fma2(a, h[q], msc::mul2(dtu2, Bk[k & 1][q]));
+                    h[q] = msc::fma2(a, h[q], msc::mul2(dtu2, Bs[k][q]));
                 }
             }
             // ---- the adjoint, backwards through the group
@@ -322,9 +330,7 @@ __global__ void __launch_bounds__(kThreads, 3) s6_bwd_kernel(const __grid_consta
                 if (k & 1) {
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
-                        const ulonglong2 vb = *reinterpret_cast<const ulonglong2*>(bsrc + q * kPitch + 2 * (k - 1));
                         const ulonglong2 vc = *reinterpret_cast<const ulonglong2*>(csrc + q * kPitch + 2 * (k - 1));
-                        Bk[0][q] = vb.x; Bk[1][q] = vb.y;
                         Ck[0][q] = vc.x; Ck[1][q] = vc.y;
                     }
                 }
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 3) s6_bwd_kernel(const __grid_consta
                 uint64_t db[2], dc[2];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const uint64_t Bq = Bk[k & 1][q];
+                    const uint64_t Bq = Bs[k][q];
                     const uint64_t Cq = Ck[k & 1][q];
                     // h_t of this step: the state entering the next step (h after the
                     // group for its last step); readout C h for dz, and dC_{t,n} = g'_t h_{t,n}
@@ -352,10 +358,21 @@ __global__ void __launch_bounds__(kThreads, 3) s6_bwd_kernel(const __grid_consta
                     // dB_{t,n} contribution of this row: lambda_{t,n} Delta_t u_t
                     db[q] = msc::mul2(lam[q], dtu2);
                 }
-                *reinterpret_cast<ulonglong2*>(s_red + k * kRedBlock + red_row(r) + 4 * j) =
-                    make_ulonglong2(db[0], db[1]);
-                *reinterpret_cast<ulonglong2*>(s_red + (8 + k) * kRedBlock + red_row(r) + 4 * j) =
-                    make_ulonglong2(dc[0], dc[1]);
+                {
+                    // rows r and r ^ 1 (lanes 4 apart) add their halves here: the even
+                    // row keeps states 4j, 4j + 1, the odd row 4j + 2, 4j + 3
+                    const bool odd = (r & 1) != 0;
+                    auto xch = [](uint64_t v) {
+                        float a, c;
+                        msc::upk2(v, a, c);
+                        return msc::pk2(__shfl_xor_sync(0xffffffffu, a, 4), __shfl_xor_sync(0xffffffffu, c, 4));
+                    };
+                    const uint64_t rb = xch(odd ? db[0] : db[1]);
+                    const uint64_t rc = xch(odd ? dc[0] : dc[1]);
+                    const int o = red_pair(r >> 1) + 4 * j + 2 * (r & 1);
+                    *reinterpret_cast<uint64_t*>(s_red + k * kRedBlock + o) = msc::add2(odd ? db[1] : db[0], rb);
+                    *reinterpret_cast<uint64_t*>(s_red + (8 + k) * kRedBlock + o) = msc::add2(odd ? dc[1] : dc[0], rc);
+                }
                 float lo, hi;
                 msc::upk2(ysum, lo, hi);
                 yp[k] = lo + hi;
@@ -387,14 +404,14 @@ __global__ void __launch_bounds__(kThreads, 3) s6_bwd_kernel(const __grid_consta
                 if (has_z) *reinterpret_cast<float2*>(p.dz + off) = make_float2(o_dz[0], o_dz[1]);
             }
             __syncthreads();
-            // ---- dB, dC of this group: sum the CTA's 32 rows (thread = (x, k, 4 states, row half)),
+            // ---- dB, dC of this group: sum the CTA's 16 row pairs (thread = (x, k, 4 states, half of the pairs)),
             // transpose through s_sum, one vector add per 4 steps
             {
                 const int half = tid & 1, n4 = (tid >> 1) & 3, k = (tid >> 3) & 7, x = tid >> 6;
-                const float* src = s_red + (8 * x + k) * kRedBlock + red_row(16 * half) + 4 * n4;
+                const float* src = s_red + (8 * x + k) * kRedBlock + red_pair(8 * half) + 4 * n4;
                 uint64_t a01 = 0ull, a23 = 0ull;
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
+                for (int rr = 0; rr < 8; ++rr) {
                     const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + 16 * rr);
                     a01 = msc::add2(a01, v.x);
                     a23 = msc::add2(a23, v.y);
