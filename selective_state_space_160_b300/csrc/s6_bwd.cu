@@ -52,6 +52,7 @@ __host__ __device__ constexpr int red_row(int r) { return r * 16 + (r >= 16 ? 16
 // row pair p = r / 2 after the pairs are summed in registers; pairs 8.. shifted
 // by 16 floats so that the two halves read side by side use different banks
 __host__ __device__ constexpr int red_pair(int p) { return p * 16 + (p >= 8 ? 16 : 0); }
+constexpr int kSumPitch = 12;  // floats per (x, n) row of the per-group sums
 
 __device__ unsigned int g_s6_bwd_status[2];
 
@@ -141,8 +142,10 @@ __global__ void __launch_bounds__(kThreads, 2) s6_bwd_kernel(const __grid_consta
     uint8_t (*s_raw)[kStageBytes] = reinterpret_cast<uint8_t (*)[kStageBytes]>(base);
     float (*s_bc)[8][kPitch] = reinterpret_cast<float (*)[8][kPitch]>(base + kStages * kStageBytes);
     float* s_red = reinterpret_cast<float*>(base + kStages * kStageBytes + 2 * 8 * kPitch * 4);
-    float* s_sum = s_red + 2 * 8 * kRedBlock;  // [x][n][k] row sums of one group
-    uint64_t* s_full = reinterpret_cast<uint64_t*>(s_sum + 2 * 16 * 8);
+    // [x][n][k] row sums of one group, rows of kSumPitch floats (8 steps and a
+    // pad: the four n of a warp's stores fall on two bank groups, not one)
+    float* s_sum = s_red + 2 * 8 * kRedBlock;
+    uint64_t* s_full = reinterpret_cast<uint64_t*>(s_sum + 2 * 16 * kSumPitch);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -423,13 +426,13 @@ __global__ void __launch_bounds__(kThreads, 2) s6_bwd_kernel(const __grid_consta
                 for (int e = 0; e < 4; ++e) s4[e] += __shfl_xor_sync(0xffffffffu, s4[e], 1);
                 if (half == 0) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) s_sum[(16 * x + 4 * n4 + e) * 8 + k] = s4[e];
+                    for (int e = 0; e < 4; ++e) s_sum[(16 * x + 4 * n4 + e) * kSumPitch + k] = s4[e];
                 }
             }
             __syncthreads();
             if (tid < 64) {
                 const int x = tid >> 5, n = (tid >> 1) & 15, kq = tid & 1;
-                const float4 v = *reinterpret_cast<const float4*>(s_sum + (16 * x + n) * 8 + 4 * kq);
+                const float4 v = *reinterpret_cast<const float4*>(s_sum + (16 * x + n) * kSumPitch + 4 * kq);
                 if (n < N) {
                     float* dst = (x == 0 ? p.dB : p.dC) + ((size_t)b * N + n) * p.L + tg + 4 * kq;
                     red_add_v4(dst, v.x, v.y, v.z, v.w);
@@ -470,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 2) s6_bwd_kernel(const __grid_consta
 template <bool kBF16>
 constexpr int bwd_smem_bytes() {
     return 1024 + kStages * kStageBytes + 2 * 8 * (2 * (kBF16 ? 32 : 16) + 4) * 4 + 2 * 8 * kRedBlock * 4 +
-           2 * 16 * 8 * 4 + kStages * 8;
+           2 * 16 * kSumPitch * 4 + kStages * 8;
 }
 
 template <bool kBF16>
