@@ -2,7 +2,7 @@
 """Benchmark of the Mamba selective scan on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--legs fwd_long,bwd,train,ssd,ssd_bwd,decode,conv1d,conv1d_bwd,conv_scan,disc|none]
+                    [--legs fwd_long,bwd,train,ssd,ssd_bwd,decode,conv1d,conv1d_bwd,conv_scan,disc,wide|none]
                     [--no-cpu-baseline]
 
 One step = one S6 forward of the Mamba-2.8B-layer workload (batch 8, d_inner
@@ -324,6 +324,32 @@ def leg_disc(peaks, pipes, steps=10, warmup=3):
                      "roofline": roofline_s6(el, N, nbytes, ms, peaks, pipes, fp32_per_elem_n=ops)}
     del inp, y
     torch.cuda.empty_cache()
+    return res
+
+
+def leg_wide(peaks, pipes, steps=10, warmup=3):
+    """The headline forward's shape (batch 8, D 5120, L 2048, bf16) with 32 and
+    64 states: four lanes per row of 8 or 16 states."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    batch, dim, L = 8, 5120, 2048
+    el = batch * dim * L
+    st = torch.cuda.current_stream()
+    res = {}
+    for N in (32, 64):
+        inp = s6_fwd_workload(batch, dim, L, N, True, 160_001)
+        y = torch.empty((batch, dim, L), dtype=torch.float32, device="cuda")
+
+        def fn():
+            msc.msc_selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                       inp["z"], inp["delta_bias"], y=y)
+        ms = statistics.median(time_launches(fn, steps, warmup, st))
+        nbytes = el * 10 + 2 * batch * N * L * 2
+        res["n%d" % N] = {"workload": "S6 fwd batch 8, D 5120, L 2048, N %d, bf16 in / fp32 y" % N,
+                          "elements_per_s": el / (ms * 1e-3), "ms": ms,
+                          "roofline": roofline_s6(el, N, nbytes, ms, peaks, pipes)}
+        del inp, y
+        torch.cuda.empty_cache()
     return res
 
 
@@ -824,7 +850,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         for name in args.legs.split(","):
             try:
-                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "train": leg_train, "ssd": leg_ssd, "ssd_bwd": leg_ssd_bwd, "decode": leg_decode, "conv1d": leg_conv1d, "conv1d_bwd": leg_conv1d_bwd, "conv_scan": leg_conv_scan, "disc": leg_disc}[name]
+                fn = {"fwd_long": leg_fwd_long, "bwd": leg_bwd, "train": leg_train, "wide": leg_wide, "ssd": leg_ssd, "ssd_bwd": leg_ssd_bwd, "decode": leg_decode, "conv1d": leg_conv1d, "conv1d_bwd": leg_conv1d_bwd, "conv_scan": leg_conv_scan, "disc": leg_disc}[name]
                 legs[name] = fn(peaks, pipes)
             except Exception as ex:  # report, do not hide: a failing leg is printed as such
                 legs[name] = {"error": "%s: %s" % (type(ex).__name__, ex)}
@@ -870,7 +896,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="fwd_long,bwd,train,ssd,ssd_bwd,decode,conv1d,conv1d_bwd,conv_scan,disc")
+    ap.add_argument("--legs", default="fwd_long,bwd,train,ssd,ssd_bwd,decode,conv1d,conv1d_bwd,conv_scan,disc,wide")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ssd-batch", type=int, default=4, help="batch of the SSD legs (4 = the timed workload)")
