@@ -111,3 +111,28 @@ def test_pair_limits():
         msc.msc_selective_scan_fwd_train(*args, ckpt=torch.empty(64, device="cuda"))
     assert e.value.status == msc.MSC_ERR_UNSUPPORTED and "multiple of 8" in str(e.value)
     msc.msc_check_device_status()
+
+
+@pytest.mark.parametrize("with_z,with_D,with_bias,bf16", [(False, True, True, True), (True, False, False, False),
+                                                          (False, False, False, True)])
+def test_pair_optional_inputs_against_the_oracle(with_z, with_D, with_bias, bf16):
+    import selective_state_space_160_b300 as msc
+    batch, dim, L, N = 2, 33, 96, 16
+    inp = s6_inputs(batch, dim, L, N, seed=41_700 + 4 * with_z + 2 * with_D + with_bias, bf16=bf16, with_dy=True,
+                    with_z=with_z, with_D=with_D, with_bias=with_bias)
+    dev = {k: (to_dev(inp[k], bf16) if inp[k] is not None else None) for k in ("u", "delta", "z", "B", "C", "dy")}
+    args = (dev["u"], dev["delta"], to_dev(inp["A"]), dev["B"], dev["C"], to_dev(inp["D"]), dev["z"],
+            to_dev(inp["delta_bias"]))
+    y, ckpt = msc.msc_selective_scan_fwd_train(*args)
+    grads = msc.msc_selective_scan_bwd_ckpt(*args, dev["dy"], ckpt)
+    tol = TOL_BF16 if bf16 else 1e-3
+    ry = oracle.s6_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                       inp["delta_bias"])
+    assert max_rel_err(y.cpu().numpy(), ry) <= (TOL_BF16 if bf16 else 1e-4)
+    ref = oracle.s6_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                        inp["delta_bias"], inp["dy"])
+    for k, v in ref.items():
+        if v is None or grads.get(k) is None:
+            assert grads.get(k) is None or v is None, k
+            continue
+        assert max_rel_err(grads[k].cpu().numpy(), v) <= tol, k
