@@ -66,11 +66,16 @@ typedef enum { MSC_F32 = 0, MSC_BF16 = 1 } msc_dtype;
  * Optional (may be NULL): D (no feed-through), z (no gate), delta_bias (0),
  * h0 (zero initial state), h_last (final state not returned).
  * Limits: batch, dim, seqlen >= 1; 1 <= dstate <= MSC_S6_FWD_MAX_DSTATE (64).
- * Above 16 states the rows must be TMA-streamable (see below) and the fused
- * conv front end is not offered; the backward and the decode step take up to
- * MSC_S6_MAX_DSTATE (16), the SSD entry points dstate 128.  Each row holds its
- * states in 16, 32 or 64 slots (the next of these at or above dstate); the
- * slots past dstate carry zeros.
+ * Above 16 states the fused conv front end is not offered; the backward and
+ * the decode step take up to MSC_S6_MAX_DSTATE (16), the SSD entry points
+ * dstate 128.  Each row holds its states in 16, 32 or 64 slots (the next of
+ * these at or above dstate); the slots past dstate carry zeros.  Above 16
+ * states, rows that TMA cannot stream as they are (seqlen not a multiple of 8
+ * with bf16 inputs, of 4 with fp32) are copied to a padded pitch inside the
+ * workspace, which the size query then includes and which is REQUIRED: the
+ * padded steps take delta = -inf, so that Delta = 0 there and the state passes
+ * them unchanged.  The trapezoidal form cannot take padded steps and returns
+ * MSC_ERR_UNSUPPORTED for such rows.
  * Workspace (256-byte aligned, size from msc_selective_scan_fwd_workspace_size):
  *  - long sequences with few rows are split into segments whose carries are
  *    combined in the workspace (three launches); there it is REQUIRED and a
@@ -83,7 +88,7 @@ typedef enum { MSC_F32 = 0, MSC_BF16 = 1 } msc_dtype;
  *  - a workspace must not be shared by calls that overlap on the GPU.
  * Rows whose byte stride (seqlen * element size) is a multiple of 16 are
  * streamed with TMA; other lengths take a plain-load kernel with identical
- * arithmetic, for dstate <= 16 only (MSC_ERR_UNSUPPORTED above). */
+ * arithmetic for dstate <= 16, and the padded copies above. */
 #define MSC_S6_FWD_MAX_DSTATE 64
 #define MSC_S6_MAX_DSTATE 16
 

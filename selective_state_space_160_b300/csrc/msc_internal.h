@@ -17,6 +17,11 @@ struct S6Plan {
     size_t workspace = 0; // bytes the plan uses
     bool workspace_required = false;  // segmented plans cannot run without it
     size_t seg_state_off = 0, seg_dsum_off = 0, ctrl_off = 0, ctrl_bytes = 0, chain_state_off = 0, bc_off = 0;
+    // More than 16 states with rows that are not a multiple of 8 steps: the rows
+    // are copied to a pitch of padded_len steps in the workspace (from pad_off)
+    // and the fields above plan the padded problem.  0: no padding.
+    int64_t padded_len = 0;
+    size_t pad_off = 0;
 };
 
 // max_required: the largest required (segment) scratch the plan may use.

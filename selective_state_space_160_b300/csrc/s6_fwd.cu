@@ -938,6 +938,19 @@ __global__ void s6_seg_carry_kernel(const float* __restrict__ A, const float* __
     }
 }
 
+// Sets steps [L, Lp) of every row of a padded copy to the bit pattern `fill`
+// (4-byte or 2-byte elements).
+__global__ void s6_pad_tail_kernel(void* dst, int64_t rows, int64_t L, int64_t Lp, int es, uint32_t fill) {
+    const int64_t tail = Lp - L;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= rows * tail) return;
+    const int64_t r = idx / tail, t = L + idx % tail;
+    if (es == 4)
+        reinterpret_cast<uint32_t*>(dst)[r * Lp + t] = fill;
+    else
+        reinterpret_cast<uint16_t*>(dst)[r * Lp + t] = (uint16_t)fill;
+}
+
 template <bool kBF16, bool kVec>
 msc_status launch_rows(const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
@@ -1121,7 +1134,34 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 //    carry pass, full pass) of at least 512 steps, about twelve per resident
 //    CTA slot, at most as many as keep the scratch within max_required.  Its
 //    workspace is required.
+// Bytes of the padded copies (u, delta, z, B, C and y at a pitch of Lp steps,
+// 4 bytes an element, which covers both input dtypes).
+static size_t pad_bytes(int64_t batch, int64_t dim, int64_t Lp, int64_t dstate) {
+    const size_t row = align256((size_t)batch * dim * Lp * 4), bc = align256((size_t)batch * dstate * Lp * 4);
+    return 4 * row + 2 * bc;
+}
+
+static S6Plan plan_rows(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, size_t max_required);
+
 S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, size_t max_required) {
+    if (dstate > kNS && seqlen % 8 != 0) {
+        // only the TMA kernel takes more than 16 states: rows of a pitch it can
+        // stream (a multiple of 8 steps, which holds for both input dtypes) are
+        // made in the workspace; the launch skips the copies for fp32 rows of a
+        // multiple of 4 steps, which TMA streams as they are
+        const int64_t Lp = cdiv64(seqlen, 8) * 8;
+        S6Plan plan = plan_rows(batch, dim, Lp, dstate, max_required);
+        plan.padded_len = Lp;
+        plan.pad_off = align256(plan.workspace);
+        plan.workspace = plan.pad_off + pad_bytes(batch, dim, Lp, dstate);
+        plan.workspace_required = true;
+        return plan;
+    }
+    return plan_rows(batch, dim, seqlen, dstate, max_required);
+}
+
+// The plan for rows of seqlen steps as they are.
+static S6Plan plan_rows(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, size_t max_required) {
     // Chunks per row and their least length: each item restarts the CTA's TMA
     // pipeline (a few microseconds), so that 4 chunks of 512 steps balance the
     // batch-8 x 5120 x 2048 workload as well as 8 of 256 (0.412 vs 0.414 ms on a
@@ -1179,7 +1219,64 @@ S6Plan s6_fwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, s
     return plan;
 }
 
+// Copies rows of L elements to a pitch of Lp (tail set to `fill`).
+static msc_status pad_rows(void* dst, const void* src, size_t es, int64_t rows, int64_t L, int64_t Lp,
+                           uint32_t fill, cudaStream_t st) {
+    cudaError_t e = cudaMemcpy2DAsync(dst, Lp * es, src, L * es, L * es, rows, cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "padded copy: %s", cudaGetErrorString(e));
+    const int64_t n = rows * (Lp - L);
+    if (n > 0) {
+        s6_pad_tail_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(dst, rows, L, Lp, (int)es, fill);
+        return check_launch("s6_pad_tail");
+    }
+    return MSC_OK;
+}
+
 msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t st) {
+    if (plan.padded_len > 0 && !a.bf16 && a.L % 4 == 0) {
+        // fp32 rows of a multiple of 4 steps stream through TMA as they are
+        const S6Plan direct = plan_rows(a.batch, a.dim, a.L, a.N, a.workspace_bytes);
+        if (!direct.workspace_required || (a.workspace && a.workspace_bytes >= direct.workspace))
+            return s6_fwd_launch(a, direct, st);
+    }
+    if (plan.padded_len > 0) {
+        // Rows of a pitch TMA can stream: delta's padded steps are -inf, so that
+        // Delta = softplus(-inf) = 0 there: the decay is 1 and the input term 0, and
+        // the state (h_last included) passes them unchanged.  The trapezoid's
+        // carried half-term would enter the first padded step, so it is refused.
+        if (a.disc == kDiscTrap)
+            return fail(MSC_ERR_UNSUPPORTED,
+                        "the trapezoidal form with more than 16 states needs seqlen a multiple of 8 "
+                        "with bf16 inputs, of 4 with fp32");
+        if (a.conv_w) return fail(MSC_ERR_UNSUPPORTED, "the fused conv front end runs with up to 16 states");
+        const int64_t L = a.L, Lp = plan.padded_len, rows = a.batch * a.dim, bcrows = a.batch * a.N;
+        if (Lp > ((int64_t)1 << 31) - 64 || a.dim > ((int64_t)1 << 31) - 64)
+            return fail(MSC_ERR_UNSUPPORTED, "seqlen and dim must be below 2^31");
+        const size_t es = a.bf16 ? 2 : 4;
+        const size_t rb = align256((size_t)rows * Lp * 4), bb = align256((size_t)bcrows * Lp * 4);
+        char* pad = static_cast<char*>(a.workspace) + plan.pad_off;
+        char *pu = pad, *pd = pu + rb, *pz = pd + rb, *py = pz + rb, *pB = py + rb, *pC = pB + bb;
+        const uint32_t ninf = a.bf16 ? 0xFF80u : 0xFF800000u;
+        msc_status s;
+        if ((s = pad_rows(pu, a.u, es, rows, L, Lp, 0u, st)) != MSC_OK) return s;
+        if ((s = pad_rows(pd, a.delta, es, rows, L, Lp, ninf, st)) != MSC_OK) return s;
+        if (a.z && (s = pad_rows(pz, a.z, es, rows, L, Lp, 0u, st)) != MSC_OK) return s;
+        if ((s = pad_rows(pB, a.B, es, bcrows, L, Lp, 0u, st)) != MSC_OK) return s;
+        if ((s = pad_rows(pC, a.C, es, bcrows, L, Lp, 0u, st)) != MSC_OK) return s;
+        S6FwdArgs b = a;
+        b.L = Lp;
+        b.u = pu; b.delta = pd; b.z = a.z ? pz : nullptr; b.B = pB; b.C = pC;
+        b.y = reinterpret_cast<float*>(py);
+        b.workspace_bytes = plan.pad_off;
+        S6Plan inner = plan;  // the padded problem's plan, its scratch below pad_off
+        inner.padded_len = 0;
+        inner.pad_off = 0;
+        inner.workspace = plan.pad_off;
+        if ((s = s6_fwd_launch(b, inner, st)) != MSC_OK) return s;
+        const cudaError_t e = cudaMemcpy2DAsync(a.y, L * 4, py, Lp * 4, L * 4, rows, cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "padded copy: %s", cudaGetErrorString(e));
+        return MSC_OK;
+    }
     FwdParams p{};
     p.u = a.u; p.delta = a.delta; p.z = a.z; p.B = a.B; p.C = a.C;
     p.A = a.A; p.D = a.D; p.delta_bias = a.delta_bias; p.h0 = a.h0;

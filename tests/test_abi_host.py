@@ -72,9 +72,14 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, N=65) == msc.MSC_ERR_UNSUPPORTED
     assert _fwd(lib, N=0) == msc.MSC_ERR_UNSUPPORTED
     # 17..64 states stream through TMA only: rows of 63 fp32 steps (252 bytes)
-    # are refused before any launch
-    assert _fwd(lib, N=17, L=63) == msc.MSC_ERR_UNSUPPORTED
-    assert "16 states" in msc.msc_last_error()
+    # are copied to a padded pitch in the workspace, which is then required
+    need = msc.msc_selective_scan_fwd_workspace_size(1, 4, 63, 17)
+    assert need >= 4 * (4 * 64 * 4) + 2 * (17 * 64 * 4)  # u, delta, z, y and B, C at a pitch of 64
+    assert _fwd(lib, N=17, L=63) == msc.MSC_ERR_WORKSPACE
+    # the trapezoid cannot take padded steps: refused before any launch
+    st = lib.msc_selective_scan_fwd_ex(1, 4, 63, 17, 0, 2, 16, 16, 16, 16, 16, None, None, None, None, 16, None,
+                                       4096, need, None)
+    assert st == msc.MSC_ERR_UNSUPPORTED and "trapezoidal" in msc.msc_last_error()
     assert _fwd(lib, z=20) == msc.MSC_ERR_INVALID_ARG
 
 

@@ -174,16 +174,82 @@ def test_host_buffer_entry_point():
     assert max_rel_err(y.numpy(), _ref(inp)[0]) <= TOL_BF16
 
 
+@pytest.mark.parametrize("batch,dim,L,N,bf16,disc", [
+    (2, 37, 61, 20, True, 0),       # bf16 rows of 122 bytes: padded to 64 steps
+    (1, 33, 63, 64, False, 0),      # fp32 rows of 252 bytes
+    (2, 5, 1003, 48, True, 0),      # few rows: segments over the padded length
+    (1, 9500, 1001, 32, True, 0),   # enough rows for the chained plan
+    (2, 20, 77, 40, False, 1),      # zero-order hold
+    (1, 3, 1, 17, True, 0),         # a single step
+])
+def test_unaligned_rows_through_padded_copies(batch, dim, L, N, bf16, disc):
+    """Rows whose byte stride is not a multiple of 16 are copied to a padded pitch
+    in the workspace; delta's padded steps are -inf, so Delta is 0 there and the
+    state passes them unchanged: y and h_last match the oracle."""
+    import selective_state_space_160_b300 as msc
+    assert msc.msc_selective_scan_fwd_workspace_size(batch, dim, L, N) > 0  # the padded copies are required
+    inp = s6_inputs(batch, dim, L, N, seed=17_800 + L + N, bf16=bf16)
+    h0 = np.random.default_rng(L).standard_normal((batch, dim, N)).astype(np.float32)
+    d = _dev(inp, bf16)
+    y, hl = msc.msc_selective_scan_fwd(d["u"], d["delta"], to_dev(inp["A"]), d["B"], d["C"], to_dev(inp["D"]),
+                                       d["z"], to_dev(inp["delta_bias"]), h0=to_dev(h0), return_last_state=True,
+                                       disc=disc)
+    msc.msc_check_device_status()
+    tol = TOL_BF16 if bf16 else TOL_F32
+    if dim > 100:  # sampled rows
+        ds = [0, 33, dim // 2, dim - 1]
+        sub = dict(inp)
+        for k in ("u", "delta", "z"):
+            sub[k] = inp[k][:, ds, :]
+        sub["A"], sub["D"], sub["delta_bias"] = inp["A"][ds], inp["D"][ds], inp["delta_bias"][ds]
+        ry, rh = oracle.s6_fwd_disc(disc, sub["u"], sub["delta"], sub["A"], sub["B"], sub["C"], sub["D"], sub["z"],
+                                    sub["delta_bias"], h0=h0[:, ds], return_last_state=True)
+        assert max_rel_err(y.cpu().numpy()[:, ds], ry) <= tol
+        assert max_rel_err(hl.cpu().numpy()[:, ds], rh) <= tol
+    else:
+        ry, rh = _ref(inp, h0=h0, disc=disc)
+        assert max_rel_err(y.cpu().numpy(), ry) <= tol
+        assert max_rel_err(hl.cpu().numpy(), rh) <= tol
+
+
 def test_wide_state_limits():
-    """Above 16 states: unaligned rows (no TMA) and the fused conv front end are
-    refused with MSC_ERR_UNSUPPORTED, before any launch."""
+    """Above 16 states the trapezoid (whose carried half-term would enter a
+    padded step) takes no unaligned rows, and the fused conv front end is not
+    offered: both refused with MSC_ERR_UNSUPPORTED before any launch."""
     import torch
     import selective_state_space_160_b300 as msc
     inp = s6_inputs(1, 4, 63, 20, seed=17_700)
     d = _dev(inp, False)
     with pytest.raises(msc.MscError) as e:
         msc.msc_selective_scan_fwd(d["u"], d["delta"], to_dev(inp["A"]), d["B"], d["C"], to_dev(inp["D"]),
-                                   d["z"], to_dev(inp["delta_bias"]))
-    assert "16 states" in str(e.value)
+                                   d["z"], to_dev(inp["delta_bias"]), disc=msc.MSC_DISC_TRAPEZOID)
+    assert "trapezoidal" in str(e.value)
+    inp = s6_inputs(1, 4, 64, 20, seed=17_701)
+    d = _dev(inp, False)
+    w = torch.ones((4, 4), device="cuda")
+    with pytest.raises(msc.MscError) as e:
+        msc.msc_selective_scan_fwd_conv(d["u"], w, None, d["delta"], to_dev(inp["A"]), d["B"], d["C"],
+                                        to_dev(inp["D"]), d["z"], to_dev(inp["delta_bias"]))
+    assert "16" in str(e.value)
     msc.msc_check_device_status()
     torch.cuda.synchronize()
+
+
+def test_noalloc_unaligned_rows():
+    """The allocation-free entry point pads small problems inside its array."""
+    import torch
+    import selective_state_space_160_b300 as msc
+    batch, dim, L, N = 1, 6, 45, 24
+    inp = s6_inputs(batch, dim, L, N, seed=17_900)
+    d = _dev(inp, False)
+    A, D, bias = to_dev(inp["A"]), to_dev(inp["D"]), to_dev(inp["delta_bias"])
+    y = torch.empty((batch, dim, L), dtype=torch.float32, device="cuda")
+    hl = torch.empty((batch, dim, N), dtype=torch.float32, device="cuda")
+    st = msc.load_library().msc_selective_scan_fwd_noalloc(
+        batch, dim, L, N, 0, d["u"].data_ptr(), d["delta"].data_ptr(), A.data_ptr(), d["B"].data_ptr(),
+        d["C"].data_ptr(), D.data_ptr(), d["z"].data_ptr(), bias.data_ptr(), None, y.data_ptr(), hl.data_ptr(),
+        torch.cuda.current_stream().cuda_stream)
+    assert st == 0, msc.msc_last_error()
+    ry, rh = _ref(inp)
+    assert max_rel_err(y.cpu().numpy(), ry) <= TOL_F32
+    assert max_rel_err(hl.cpu().numpy(), rh) <= TOL_F32
