@@ -114,10 +114,10 @@ msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, in
  *    b_t = 1/2 (Delta_t B_t u_t + abar_t Delta_{t-1} B_{t-1} u_{t-1}), with no
  *    input term before t = 0 (h0, if given, is the state only).
  * Arguments, workspace (msc_selective_scan_fwd_workspace_size) and errors as
- * msc_selective_scan_fwd.  The ZOH and trapezoidal forms need 16-byte row
- * strides (seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) and seqlen,
- * dim below 2^31 (their TMA tile coordinates are 32-bit), and
- * return MSC_ERR_UNSUPPORTED otherwise; no backward is provided for them.
+ * msc_selective_scan_fwd, including rows of any length (up to 16 states the
+ * plain-load kernel takes every form; above, the padded copies take the
+ * zero-order hold but not the trapezoid, which returns MSC_ERR_UNSUPPORTED for
+ * rows TMA cannot stream).  No backward is provided for these forms.
  */
 typedef enum { MSC_DISC_EULER = 0, MSC_DISC_ZOH = 1, MSC_DISC_TRAPEZOID = 2 } msc_discretization;
 

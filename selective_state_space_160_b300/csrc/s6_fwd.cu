@@ -193,7 +193,7 @@ __device__ __forceinline__ void store_rows(float* dst, float (*src)[kStride], in
     }
 }
 
-template <bool kBF16, bool kVec, int kMode>
+template <bool kBF16, bool kVec, int kMode, int kDisc = kDiscEuler>
 __global__ void __launch_bounds__(32) s6_fwd_rows_kernel(const FwdParams p) {
     __shared__ __align__(16) float s_u[kRows][kStride];
     __shared__ __align__(16) float s_d[kRows][kStride];  // delta in, y out
@@ -234,6 +234,30 @@ __global__ void __launch_bounds__(32) s6_fwd_rows_kernel(const FwdParams p) {
     const int64_t t_end = imin64(p.L, t_begin + p.seg_len);
     const int64_t row0 = b * p.dim + d0;
 
+    // zero-order hold: 1/A per state (0 where A = 0: the series branch covers it);
+    // trapezoid: the half input term of the previous step, per state (from the
+    // step before the segment, none before t = 0)
+    float invA[kDisc == kDiscZoh ? kNS : 1];
+    float ep[kDisc == kDiscTrap ? kNS : 1];
+    if constexpr (kDisc == kDiscZoh) {
+#pragma unroll
+        for (int n = 0; n < kNS; ++n) {
+            const float a = A2[n] * MSC_LN2;
+            invA[n] = a != 0.f ? 1.f / a : 0.f;
+        }
+    }
+    if constexpr (kDisc == kDiscTrap) {
+        float eu = 0.f;
+        if (row_ok && t_begin > 0) {
+            const int64_t tp = t_begin - 1;
+            eu = 0.5f * msc::softplus_f(msc::ld_elem<kBF16>(p.delta, row * p.L + tp) + bias) *
+                 msc::ld_elem<kBF16>(p.u, row * p.L + tp);
+        }
+#pragma unroll
+        for (int n = 0; n < kNS; ++n)
+            ep[n] = (eu != 0.f && n < N) ? eu * msc::ld_elem<kBF16>(p.B, (b * N + n) * p.L + t_begin - 1) : 0.f;
+    }
+
     for (int64_t t0 = t_begin; t0 < t_end; t0 += kT) {
         const int nt = (int)imin64(kT, t_end - t0);
         __syncwarp();
@@ -259,7 +283,8 @@ __global__ void __launch_bounds__(32) s6_fwd_rows_kernel(const FwdParams p) {
                 if (tq + k < nt) {
                     const int t = tq + k;
                     const float dt = msc::softplus_f(dd[k] + bias);
-                    const float dtu = dt * uu[k];
+                    const float dtu = kDisc == kDiscTrap ? 0.5f * dt * uu[k] : dt * uu[k];
+                    const float rdt = kDisc == kDiscZoh ? (dt > 0.f ? msc::rcp_approx(dt) : 0.f) : 0.f;
                     if (!kFull) dsum += dt;
                     float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
@@ -274,8 +299,23 @@ __global__ void __launch_bounds__(32) s6_fwd_rows_kernel(const FwdParams p) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int n = 4 * q + j;
-                            const float a = msc::ex2_approx(dt * A2[n]);
-                            h[n] = fmaf(a, h[n], dtu * bv[j]);
+                            const float arg = dt * A2[n];
+                            const float a = msc::ex2_approx(arg);
+                            if constexpr (kDisc == kDiscEuler) {
+                                h[n] = fmaf(a, h[n], dtu * bv[j]);
+                            } else if constexpr (kDisc == kDiscZoh) {
+                                // phi = (e^x - 1) / x with x = Delta A: a series near 0
+                                const float x = arg * MSC_LN2;
+                                float ps = fmaf(x, 1.f / 24.f, 1.f / 6.f);
+                                ps = fmaf(x, ps, 0.5f);
+                                ps = fmaf(x, ps, 1.f);
+                                const float phi = fabsf(x) < 0.03f ? ps : (a - 1.f) * invA[n] * rdt;
+                                h[n] = fmaf(a, h[n], phi * (dtu * bv[j]));
+                            } else {
+                                const float e2 = dtu * bv[j];  // half the Euler term
+                                h[n] = fmaf(a, h[n] + ep[n], e2);
+                                ep[n] = e2;
+                            }
                             if (kFull) {
                                 if (j == 0) acc0 = fmaf(cv[j], h[n], acc0);
                                 if (j == 1) acc1 = fmaf(cv[j], h[n], acc1);
@@ -951,14 +991,21 @@ __global__ void s6_pad_tail_kernel(void* dst, int64_t rows, int64_t L, int64_t L
         reinterpret_cast<uint16_t*>(dst)[r * Lp + t] = (uint16_t)fill;
 }
 
-template <bool kBF16, bool kVec>
+template <bool kBF16, bool kVec, int kDisc>
 msc_status launch_rows(const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
     if (mode == kModeFull)
-        s6_fwd_rows_kernel<kBF16, kVec, kModeFull><<<grid, kRows, 0, st>>>(p);
+        s6_fwd_rows_kernel<kBF16, kVec, kModeFull, kDisc><<<grid, kRows, 0, st>>>(p);
     else
-        s6_fwd_rows_kernel<kBF16, kVec, kModeAgg><<<grid, kRows, 0, st>>>(p);
+        s6_fwd_rows_kernel<kBF16, kVec, kModeAgg, kDisc><<<grid, kRows, 0, st>>>(p);
     return msc_host::check_launch("s6_fwd_rows");
+}
+
+template <bool kBF16, bool kVec>
+msc_status launch_rows_disc(const FwdParams& p, int64_t batch, int G, int mode, int disc, cudaStream_t st) {
+    if (disc == kDiscZoh) return launch_rows<kBF16, kVec, kDiscZoh>(p, batch, G, mode, st);
+    if (disc == kDiscTrap) return launch_rows<kBF16, kVec, kDiscTrap>(p, batch, G, mode, st);
+    return launch_rows<kBF16, kVec, kDiscEuler>(p, batch, G, mode, st);
 }
 
 struct FwdMaps {
@@ -1103,13 +1150,11 @@ msc_status launch_mode(const FwdParams& p, const FwdMaps* maps, bool bf16, bool 
                               "the fused conv front end needs 16-byte row strides "
                               "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) "
                               "and seqlen, dim below 2^31");
-    if (disc != kDiscEuler)
-        return msc_host::fail(MSC_ERR_UNSUPPORTED,
-                              "the zero-order-hold and trapezoidal forms need 16-byte row strides "
-                              "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) "
-                              "and seqlen, dim below 2^31");
-    if (bf16) return vec ? launch_rows<true, true>(p, batch, G, mode, st) : launch_rows<true, false>(p, batch, G, mode, st);
-    return vec ? launch_rows<false, true>(p, batch, G, mode, st) : launch_rows<false, false>(p, batch, G, mode, st);
+    if (bf16)
+        return vec ? launch_rows_disc<true, true>(p, batch, G, mode, disc, st)
+                   : launch_rows_disc<true, false>(p, batch, G, mode, disc, st);
+    return vec ? launch_rows_disc<false, true>(p, batch, G, mode, disc, st)
+               : launch_rows_disc<false, false>(p, batch, G, mode, disc, st);
 }
 
 }  // namespace

@@ -184,17 +184,22 @@ def test_conv1d_rejects_bad_arguments(lib):
 def test_fwd_ex_rejects_bad_arguments(lib):
     f = lib.msc_selective_scan_fwd_ex
 
-    def call(L=64, dt=1, disc=1):
-        return f(1, 4, L, 16, dt, disc, 16, 16, 16, 16, 16, None, None, None, None, 16, None, None, 0, None)
+    def call(L=64, dt=1, disc=1, N=16, ws=None, wsb=0):
+        return f(1, 4, L, N, dt, disc, 16, 16, 16, 16, 16, None, None, None, None, 16, None, ws, wsb, None)
 
     assert call(disc=7) == msc.MSC_ERR_INVALID_ARG
     assert "disc" in msc.msc_last_error()
-    assert call(L=63, disc=msc.MSC_DISC_ZOH) == msc.MSC_ERR_UNSUPPORTED        # bf16 rows not 16-byte strided
-    assert call(L=66, dt=0, disc=msc.MSC_DISC_TRAPEZOID) == msc.MSC_ERR_UNSUPPORTED
-    # rows of 2^31 steps do not fit the 32-bit TMA coordinates: refused before any launch
+    # rows that TMA cannot stream: up to 16 states the plain-load kernel takes
+    # every form (a GPU test covers it); above, the padded copies need the
+    # workspace, and the trapezoid cannot take padded steps at all
+    assert call(L=63, N=20, disc=msc.MSC_DISC_ZOH) == msc.MSC_ERR_WORKSPACE
+    need = msc.msc_selective_scan_fwd_workspace_size(1, 4, 66, 20)
+    assert call(L=66, dt=1, N=20, disc=msc.MSC_DISC_TRAPEZOID, ws=4096, wsb=need) == msc.MSC_ERR_UNSUPPORTED
+    # rows of 2^31 steps do not fit the 32-bit TMA coordinates, and above 16
+    # states only the TMA kernel runs: refused before any launch
     big = 1 << 31
-    ws = msc.msc_selective_scan_fwd_workspace_size(1, 4, big, 16)
-    r = f(1, 4, big, 16, 1, msc.MSC_DISC_ZOH, 16, 16, 16, 16, 16, None, None, None, None, 16, None, 4096, ws, None)
+    ws = msc.msc_selective_scan_fwd_workspace_size(1, 4, big, 20)
+    r = f(1, 4, big, 20, 1, msc.MSC_DISC_ZOH, 16, 16, 16, 16, 16, None, None, None, None, 16, None, 4096, ws, None)
     assert r == msc.MSC_ERR_UNSUPPORTED and "2^31" in msc.msc_last_error()
 
 

@@ -68,12 +68,27 @@ def test_euler_through_ex_is_the_plain_forward():
     assert np.array_equal(y0, y1)
 
 
-def test_unaligned_rows_are_unsupported():
-    import selective_state_space_160_b300 as msc
-    inp = s6_inputs(1, 4, 63, 16, seed=3300, bf16=True)
-    with pytest.raises(msc.MscError) as ex:
-        _run(inp, True, msc.MSC_DISC_ZOH)
-    assert ex.value.status == msc.MSC_ERR_UNSUPPORTED
+@pytest.mark.parametrize("disc", DISCS)
+@pytest.mark.parametrize("batch,dim,L,bf16", [(1, 4, 63, True), (2, 37, 61, False), (1, 3, 4097, True)])
+def test_unaligned_rows_through_the_plain_kernel(disc, batch, dim, L, bf16):
+    """Rows whose byte stride is not a multiple of 16 take the plain-load kernel,
+    which runs every form; L 4097 with few rows takes segments (the trapezoid's
+    half-term from the step before each segment)."""
+    inp = s6_inputs(batch, dim, L, 16, seed=3300 + L + disc, bf16=bf16)
+    h0 = np.random.default_rng(L).standard_normal((batch, dim, 16)).astype(np.float32)
+    _check(_run(inp, bf16, disc, h0=h0), _ref(inp, disc, h0=h0), 2e-3 if bf16 else 1e-4)
+
+
+@pytest.mark.parametrize("disc", DISCS)
+def test_plain_and_tma_kernels_agree(disc, monkeypatch):
+    """Aligned rows sent to the plain-load kernel (MSC_S6_FWD_PLAIN) give the
+    TMA kernel's results to 1e-5."""
+    inp = s6_inputs(2, 40, 256, 16, seed=3400 + disc, bf16=True)
+    y_tma, h_tma = _run(inp, True, disc)
+    monkeypatch.setenv("MSC_S6_FWD_PLAIN", "1")
+    y_plain, h_plain = _run(inp, True, disc)
+    assert max_rel_err(y_plain, y_tma) <= 1e-5
+    assert max_rel_err(h_plain, h_tma) <= 1e-5
 
 
 @pytest.mark.parametrize("disc", DISCS)
