@@ -1,6 +1,6 @@
 """Randomised parity sweep: seeded draws of shapes and options for the S6
 forward (every discretisation, 1..64 states, optional inputs, initial state,
-aligned and unaligned rows), the S6 backward, the decode step and the SSD
+aligned and unaligned rows: the plain-load kernel, the padded copies), the S6 backward, the decode step and the SSD
 forward, each checked against the oracle on the same inputs.  The draws are
 fixed by the seed, so a failure names a reproducible case; sizes stay small
 enough for the oracle to finish in seconds.
@@ -23,8 +23,8 @@ def _draw_fwd(i):
     disc = int(r.integers(3))
     N = int(r.choice([1, 3, 8, 16, 16, 17, 24, 32, 40, 64]))
     L = int(r.choice([1, 7, 8, 33, 64, 100, 256, 520, 1031, 2048]))
-    if disc != 0 or N > 16:
-        # these take the TMA path only: 16-byte row strides
+    if disc == 2 and N > 16:
+        # the trapezoid above 16 states takes only rows TMA streams as they are
         m = 8 if bf16 else 4
         L = max(m, (L // m) * m)
     dim = int(r.integers(1, 80))
