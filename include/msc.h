@@ -195,10 +195,12 @@ msc_status msc_selective_scan_fwd_host(int64_t batch, int64_t dim, int64_t seqle
  * (msc_selective_scan_fwd_workspace_size) and the errors as
  * msc_selective_scan_fwd.  u is kept in fp32 (not rounded to in_dtype), so
  * the result equals msc_causal_conv1d_fwd (fp32 out) followed by
- * msc_selective_scan_fwd with fp32 u up to rounding.  Needs 16-byte row
- * strides (seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) and seqlen,
- * dim below 2^31, else MSC_ERR_UNSUPPORTED; exponential-Euler form and
- * dstate <= 16 only; no backward. */
+ * msc_selective_scan_fwd with fp32 u up to rounding.  Any seqlen >= 1: rows
+ * TMA can stream (seqlen a multiple of 8 with bf16 inputs, of 4 with fp32,
+ * seqlen and dim below 2^31) take the TMA kernel, the rest the plain-load
+ * kernel, which reads the three inputs before each segment from memory.
+ * Exponential-Euler form and 1 <= dstate <= 16 only (else
+ * MSC_ERR_UNSUPPORTED); no backward. */
 msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                        int64_t conv_width, msc_dtype in_dtype, const void* x,
                                        const float* conv_weight, const float* conv_bias, const void* delta,

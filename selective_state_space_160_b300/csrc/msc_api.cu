@@ -203,9 +203,6 @@ msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqle
     MSC_PTR(B, "B"); MSC_PTR(C, "C"); MSC_PTR(y, "y");
     MSC_OPT_PTR(conv_bias, "conv_bias"); MSC_OPT_PTR(D, "D"); MSC_OPT_PTR(z, "z");
     MSC_OPT_PTR(delta_bias, "delta_bias"); MSC_OPT_PTR(h0, "h0"); MSC_OPT_PTR(h_last, "h_last");
-    if (seqlen % (in_dtype == MSC_BF16 ? 8 : 4) != 0)
-        return fail(MSC_ERR_UNSUPPORTED, "the fused conv front end needs seqlen a multiple of %d (got %lld)",
-                    in_dtype == MSC_BF16 ? 8 : 4, (long long)seqlen);
     S6Plan plan = s6_fwd_plan(batch, dim, seqlen, dstate);
     if (plan.workspace_required && (workspace == nullptr || workspace_bytes < plan.workspace))
         return fail(MSC_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", plan.workspace,

@@ -193,7 +193,7 @@ __device__ __forceinline__ void store_rows(float* dst, float (*src)[kStride], in
     }
 }
 
-template <bool kBF16, bool kVec, int kMode, int kDisc = kDiscEuler>
+template <bool kBF16, bool kVec, int kMode, int kDisc = kDiscEuler, bool kConv = false>
 __global__ void __launch_bounds__(32) s6_fwd_rows_kernel(const FwdParams p) {
     __shared__ __align__(16) float s_u[kRows][kStride];
     __shared__ __align__(16) float s_d[kRows][kStride];  // delta in, y out
@@ -234,6 +234,21 @@ __global__ void __launch_bounds__(32) s6_fwd_rows_kernel(const FwdParams p) {
     const int64_t t_end = imin64(p.L, t_begin + p.seg_len);
     const int64_t row0 = b * p.dim + d0;
 
+    // fused conv front end: taps right-aligned in a 4-tap window (cw[m] multiplies
+    // x_{t-3+m}) and the three inputs before the current step (0 before t = 0);
+    // the staged u tile then holds x, and u = silu(conv) is formed step by step
+    float cw[4] = {0.f, 0.f, 0.f, 0.f}, cbias = 0.f, xw[3] = {0.f, 0.f, 0.f};
+    if constexpr (kConv) {
+        const int K = p.conv_k;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) cw[m] = (row_ok && m + K >= 4) ? __ldg(p.conv_w + d * K + (m + K - 4)) : 0.f;
+        cbias = (row_ok && p.conv_b) ? __ldg(p.conv_b + d) : 0.f;
+#pragma unroll
+        for (int m = 0; m < 3; ++m) {
+            const int64_t tp = t_begin - 3 + m;
+            xw[m] = (row_ok && tp >= 0) ? msc::ld_elem<kBF16>(p.u, row * p.L + tp) : 0.f;
+        }
+    }
     // zero-order hold: 1/A per state (0 where A = 0: the series branch covers it);
     // trapezoid: the half input term of the previous step, per state (from the
     // step before the segment, none before t = 0)
@@ -273,8 +288,25 @@ __global__ void __launch_bounds__(32) s6_fwd_rows_kernel(const FwdParams p) {
             const float4 d4 = *reinterpret_cast<const float4*>(&s_d[lane][tq]);
             float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (has_z) z4 = *reinterpret_cast<const float4*>(&s_z[lane][tq]);
-            const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
+            float uu[4] = {u4.x, u4.y, u4.z, u4.w};
             const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+            if constexpr (kConv) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (tq + k < nt) {
+                        const float x = uu[k];
+                        float acc = cbias;
+                        acc = fmaf(cw[0], xw[0], acc);
+                        acc = fmaf(cw[1], xw[1], acc);
+                        acc = fmaf(cw[2], xw[2], acc);
+                        acc = fmaf(cw[3], x, acc);
+                        uu[k] = msc::silu_f(acc);
+                        xw[0] = xw[1];
+                        xw[1] = xw[2];
+                        xw[2] = x;
+                    }
+                }
+            }
             const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
             float yy[4];
 #pragma unroll
@@ -991,18 +1023,23 @@ __global__ void s6_pad_tail_kernel(void* dst, int64_t rows, int64_t L, int64_t L
         reinterpret_cast<uint16_t*>(dst)[r * Lp + t] = (uint16_t)fill;
 }
 
-template <bool kBF16, bool kVec, int kDisc>
+template <bool kBF16, bool kVec, int kDisc, bool kConv = false>
 msc_status launch_rows(const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
     if (mode == kModeFull)
-        s6_fwd_rows_kernel<kBF16, kVec, kModeFull, kDisc><<<grid, kRows, 0, st>>>(p);
+        s6_fwd_rows_kernel<kBF16, kVec, kModeFull, kDisc, kConv><<<grid, kRows, 0, st>>>(p);
     else
-        s6_fwd_rows_kernel<kBF16, kVec, kModeAgg, kDisc><<<grid, kRows, 0, st>>>(p);
+        s6_fwd_rows_kernel<kBF16, kVec, kModeAgg, kDisc, kConv><<<grid, kRows, 0, st>>>(p);
     return msc_host::check_launch("s6_fwd_rows");
 }
 
 template <bool kBF16, bool kVec>
 msc_status launch_rows_disc(const FwdParams& p, int64_t batch, int G, int mode, int disc, cudaStream_t st) {
+    if (p.conv_w) {
+        if (disc != kDiscEuler)
+            return msc_host::fail(MSC_ERR_UNSUPPORTED, "the fused conv front end runs with the exponential-Euler form");
+        return launch_rows<kBF16, kVec, kDiscEuler, true>(p, batch, G, mode, st);
+    }
     if (disc == kDiscZoh) return launch_rows<kBF16, kVec, kDiscZoh>(p, batch, G, mode, st);
     if (disc == kDiscTrap) return launch_rows<kBF16, kVec, kDiscTrap>(p, batch, G, mode, st);
     return launch_rows<kBF16, kVec, kDiscEuler>(p, batch, G, mode, st);
@@ -1143,11 +1180,6 @@ msc_status launch_mode(const FwdParams& p, const FwdMaps* maps, bool bf16, bool 
     if (p.N > kNS)
         return msc_host::fail(MSC_ERR_UNSUPPORTED,
                               "more than 16 states need 16-byte row strides "
-                              "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) "
-                              "and seqlen, dim below 2^31");
-    if (p.conv_w)
-        return msc_host::fail(MSC_ERR_UNSUPPORTED,
-                              "the fused conv front end needs 16-byte row strides "
                               "(seqlen a multiple of 8 with bf16 inputs, of 4 with fp32) "
                               "and seqlen, dim below 2^31");
     if (bf16)

@@ -252,8 +252,8 @@ def test_fwd_conv_rejects_bad_arguments(lib):
     assert call(K=5) == msc.MSC_ERR_UNSUPPORTED
     assert call(x=None) == msc.MSC_ERR_INVALID_ARG and "x" in msc.msc_last_error()
     assert call(w=None) == msc.MSC_ERR_INVALID_ARG and "conv_weight" in msc.msc_last_error()
-    assert call(L=100) == msc.MSC_ERR_UNSUPPORTED                # bf16 rows need seqlen % 8 == 0
-    assert call(N=17) == msc.MSC_ERR_UNSUPPORTED
+    assert call(N=17) == msc.MSC_ERR_UNSUPPORTED                # up to 16 states
+    assert call(L=100, N=17) == msc.MSC_ERR_UNSUPPORTED         # at any seqlen
 
 
 def test_conv1d_bwd_rejects_bad_arguments(lib):

@@ -125,10 +125,11 @@ def test_s6_forward_discretisations(disc):
     _check({"y": y, "h_last": hl}, msc, st)
 
 
-def test_s6_forward_fused_conv():
+@pytest.mark.parametrize("L", [96, 101])  # TMA kernel; plain-load kernel (unaligned rows)
+def test_s6_forward_fused_conv(L):
     import torch
     msc, lib = _lib()
-    batch, dim, L, N, K = 2, 37, 96, 16, 4
+    batch, dim, N, K = 2, 37, 16, 4
     inp = s6_inputs(batch, dim, L, N, seed=31_200, bf16=True)
     d = _s6_dev(inp, True)
     A, D, bias = to_dev(inp["A"]), to_dev(inp["D"]), to_dev(inp["delta_bias"])

@@ -1,7 +1,9 @@
 """GPU parity of the S6 forward with the causal conv1d + SiLU front end fused
 into the scan (msc_selective_scan_fwd_conv, through the C ABI) against the
 oracle's conv1d followed by its scan, u kept in double precision (the fused
-kernel keeps u in fp32, never rounding it to the input dtype).
+kernel keeps u in fp32, never rounding it to the input dtype).  Rows of any
+length: the TMA kernel takes rows it can stream, the plain-load kernel the
+rest.
 
 Tolerances (max |gpu - ref| / (1 + |ref|)) as the S6 forward: 1e-4 with fp32
 inputs, 2e-3 with bf16 inputs (the oracle consumes the same bf16-rounded x)."""
@@ -101,10 +103,41 @@ def test_mamba_layer_size_sampled_rows():
     assert max_rel_err(y[:, ds, :], _ref(sub, w[ds], cb[ds])) <= TOL_BF16
 
 
-def test_rejects_unaligned_length():
-    import selective_state_space_160_b300 as msc
-    inp = s6_inputs(1, 4, 100, 16, seed=4600, bf16=True)
-    w, cb = conv_taps(4, 4, seed=4601)
-    with pytest.raises(msc.MscError) as e:
-        _run(inp, w, cb, True)
-    assert e.value.status == msc.MSC_ERR_UNSUPPORTED
+@pytest.mark.parametrize("batch,dim,L,N,K,bf16", [
+    (1, 4, 100, 16, 4, True), (2, 37, 1, 16, 4, True), (1, 33, 3, 5, 3, False), (2, 40, 1031, 16, 4, False),
+    (3, 65, 257, 16, 2, True), (1, 9, 7, 1, 1, True)])
+def test_unaligned_rows(batch, dim, L, N, K, bf16):
+    """Rows TMA cannot stream as they are (seqlen not a multiple of 8 with bf16
+    inputs, of 4 with fp32): the plain-load kernel forms the conv step by step,
+    the first three steps reading zeros before t = 0."""
+    inp = s6_inputs(batch, dim, L, N, seed=4700 + batch + dim + L + N + K, bf16=bf16)
+    w, cb = conv_taps(dim, K, seed=4701 + K)
+    h0 = np.random.default_rng(4702).standard_normal((batch, dim, N)).astype(np.float32)
+    y, hl = _run(inp, w, cb, bf16, h0=h0, last=True)
+    ry, rhl = _ref(inp, w, cb, h0=h0, last=True)
+    tol = TOL_BF16 if bf16 else TOL_F32
+    assert max_rel_err(y, ry) <= tol
+    assert max_rel_err(hl, rhl) <= tol
+
+
+def test_unaligned_rows_segments():
+    """Few rows and a long, unaligned sequence: the plain-load kernel's segments
+    each read the conv's three-step halo of the previous segment from memory."""
+    inp = s6_inputs(1, 20, 9001, 16, seed=4800, bf16=True)
+    w, cb = conv_taps(20, 4, seed=4801)
+    y, hl = _run(inp, w, cb, True, last=True)
+    ry, rhl = _ref(inp, w, cb, last=True)
+    assert max_rel_err(y, ry) <= TOL_BF16
+    assert max_rel_err(hl, rhl) <= TOL_BF16
+
+
+@pytest.mark.parametrize("batch,dim,L,bf16", [(2, 37, 96, True), (1, 24, 2048, False)])
+def test_plain_kernel_agrees_with_tma_kernel(monkeypatch, batch, dim, L, bf16):
+    """On rows both kernels take, the plain-load kernel (forced by
+    MSC_S6_FWD_PLAIN) and the TMA kernel agree to fp32 rounding."""
+    inp = s6_inputs(batch, dim, L, 16, seed=4900 + L, bf16=bf16)
+    w, cb = conv_taps(dim, 4, seed=4901)
+    y_tma = _run(inp, w, cb, bf16)
+    monkeypatch.setenv("MSC_S6_FWD_PLAIN", "1")
+    y_plain = _run(inp, w, cb, bf16)
+    assert max_rel_err(y_plain, y_tma) <= 1e-5
