@@ -57,6 +57,10 @@ NCU_TRAFFIC = {
     "conv1d_fwd_w4_kernel": {"src_sha": "fa8b0f4c9b59", "bytes_per_launch": 293.1e6},
     # profiles/conv1d_bwd_8x5120x2048_bf16.md: mean of 3 launches, read 504.5 MB + write 296.8 MB
     "conv1d_bwd_w4_kernel": {"src_sha": "fa8b0f4c9b59", "bytes_per_launch": 801.4e6},
+    # profiles/s6_fwd_long_1x1536_fp32_segmented.md: one call of the long-sequence
+    # forward, aggregate pass (12.98 GB read + 0.04 GB written) + full pass with y
+    # staged (19.57 + 6.42 GB); the carry pass adds about 2 MB.
+    "s6_fwd_long_call": {"src_sha": "b57cce0f3360", "bytes_per_launch": 39.01e9},
 }
 
 
@@ -295,6 +299,11 @@ def leg_fwd_long(peaks, pipes, steps=3, warmup=1):
     nbytes = el * 16 + 2 * batch * N * L * 4
     res = {"workload": "S6 fwd batch 1, D 1536, L %d, N 16, fp32, segmented" % L, "elements_per_s": el / (ms * 1e-3),
            "ms": ms, "roofline": roofline_s6(el, N, nbytes, ms, peaks, pipes)}
+    if L == 1 << 20:
+        # DRAM bytes of the whole call (both passes), from the committed capture
+        res["roofline"]["traffic"] = _ncu_traffic(
+            "s6_fwd_long_call", os.path.join(ROOT, "selective_state_space_160_b300", "csrc", "s6_fwd.cu"))
+        res["roofline"]["traffic_scope"] = "aggregate + carry + full pass, per call"
     del inp, y, ws
     torch.cuda.empty_cache()
     return res

@@ -476,7 +476,8 @@ __device__ __forceinline__ void reduce_scatter_level(float* v, int j) {
 template <bool kBF16, int kSN>
 constexpr int fwd_min_ctas() { return kSN == 16 ? 0 : kSN == 32 ? (kBF16 ? 0 : 4) : 3; }
 
-template <bool kBF16, int kMode, int kNG, int kDisc = kDiscEuler, bool kConv = false, int kSN = kNS>
+template <bool kBF16, int kMode, int kNG, int kDisc = kDiscEuler, bool kConv = false, int kSN = kNS,
+          bool kLongRows = false>
 __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_u,
                                                               const __grid_constant__ CUtensorMap tm_d,
                                                               const __grid_constant__ CUtensorMap tm_z,
@@ -510,6 +511,17 @@ __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd
     // warps may still read tile i - 1.
     constexpr int kSkew = kSN == kNS ? 0 : 8;
     __shared__ __align__(16) float s_bc[kEarly ? 2 : 1][2][kNG][kPPL * kPitch + kSkew];
+    // kLongRows (rows of y a megabyte or more apart): y of a 32-step window of
+    // every row (one tile with bf16 inputs, two with fp32) is staged here and
+    // written out after the tile-end barrier as whole 128-byte row runs.
+    // Stored 16 bytes a lane straight from the groups, each row's line is
+    // assembled from four to eight separate stores, which at 1 x 1536 x 2^20
+    // (rows 4 MB apart) cost a sixth of the time; with short rows the staging
+    // costs more than it saves (3% at 8 x 5120 x 2048).  Row pitch 40 floats:
+    // the eight lanes of a store phase (four rows, two chunks) hit distinct banks.
+    constexpr bool kStageY = kLongRows && kFull && !kEarly;
+    static_assert(!kLongRows || kStageY, "long-row staging is for the 16-slot full pass");
+    __shared__ __align__(16) float s_y[kStageY ? kRows : 1][kStageY ? 40 : 4];
     __shared__ __align__(8) uint64_t s_full[kStages];
 
     const int tid = threadIdx.x;
@@ -923,7 +935,11 @@ __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd
                         y2[e] = msc::mul2(y2[e], msc::silu_2(z2));
                     }
                 }
-                if (row_ok) {
+                if constexpr (kStageY) {
+                    static_assert(kSPG == 4, "staged y: four steps a lane");
+                    const int c = (kBF16 ? 0 : (i & 1) * 4) + 2 * g + j;  // 16-byte chunk of the window
+                    *reinterpret_cast<ulonglong2*>(&s_y[r][4 * c]) = make_ulonglong2(y2[0], y2[1]);
+                } else if (row_ok) {
                     const int rem = nt - 8 * g - j * kSPG;
                     float* qy = p.y + row * p.L + t0 + 8 * g + j * kSPG;
                     if (rem >= kSPG) {
@@ -943,13 +959,35 @@ __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd
             }
         }
         if constexpr (!kEarly) {
-            __syncthreads();  // every thread is done with this tile's stage
+            __syncthreads();  // every thread is done with this tile's stage (and its y is staged)
             if (tid == 0 && issued < ntiles) {
                 const uint32_t si = (tbase + issued) % kStages;
                 issue_tile(issued, t_begin + (int64_t)issued * kTT, s_raw[si], &s_full[si], tx_bytes, kBCT, &tm_u,
                            &tm_d, &tm_z, &tm_B, &tm_C, d0, b, has_z, kFull);
             }
             ++issued;
+            if constexpr (kStageY) {
+                // the window is complete (or the item ends): eight lanes a row, 16 bytes
+                // each; the next tile's groups write s_y only after its first barrier
+                if (kBF16 || (i & 1) || i + 1 == ntiles) {
+                    const int64_t tw = t_begin + (int64_t)(kBF16 ? i : (i & ~1)) * kTT;
+                    const int nw = (int)imin64(32, t_end - tw);
+                    for (int e = tid; e < kRows * 8; e += 32 * kNG) {
+                        const int rr = e >> 3, c = e & 7;
+                        if (rr < nrows && 4 * c < nw) {
+                            const float4 v = *reinterpret_cast<const float4*>(&s_y[rr][4 * c]);
+                            float* q = p.y + (b * p.dim + d0 + rr) * p.L + tw + 4 * c;
+                            if (4 * c + 4 <= nw) {
+                                __stcs(reinterpret_cast<float4*>(q), v);
+                            } else {
+                                q[0] = v.x;
+                                if (4 * c + 1 < nw) q[1] = v.y;
+                                if (4 * c + 2 < nw) q[2] = v.z;
+                            }
+                        }
+                    }
+                }
+            }
         }
     }
 
@@ -1117,9 +1155,9 @@ int resident_ctas(K kernel, int threads) {
 // A full pass: persistent CTAs taking (row block, chunk) tickets when the
 // chained schedule's control block is set, else one CTA per (row block, batch
 // entry, segment).
-template <bool kBF16, int kMode, int kNG, int kDisc, bool kConv, int kSN>
+template <bool kBF16, int kMode, int kNG, int kDisc, bool kConv, int kSN, bool kLongRows = false>
 void launch_full(const FwdMaps& m, const FwdParams& p, dim3 grid, cudaStream_t st) {
-    auto kern = s6_fwd_tma_kernel<kBF16, kMode, kNG, kDisc, kConv, kSN>;
+    auto kern = s6_fwd_tma_kernel<kBF16, kMode, kNG, kDisc, kConv, kSN, kLongRows>;
     if (p.ctr) {
         // persistent: at most one CTA per row block, so that the chunk before a
         // ticket's chunk was taken a full round earlier and is normally done
@@ -1131,12 +1169,18 @@ void launch_full(const FwdMaps& m, const FwdParams& p, dim3 grid, cudaStream_t s
     }
 }
 
+// Rows of at least this many steps take the full pass that stages y (kLongRows).
+constexpr int64_t kLongRowSteps = (int64_t)1 << 19;
+
 template <bool kBF16, int kNG, int kDisc = kDiscEuler, bool kConv = false, int kSN = kNS>
 msc_status launch_tma_ng(const FwdMaps& m, const FwdParams& p, int64_t batch, int G, int mode, cudaStream_t st) {
     constexpr bool kCkOk = kDisc == kDiscEuler && !kConv && kSN == kNS;
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, (unsigned)G);
     if (mode == kModeFull) {
-        launch_full<kBF16, kModeFull, kNG, kDisc, kConv, kSN>(m, p, grid, st);
+        if (kSN == kNS && p.L >= kLongRowSteps)
+            launch_full<kBF16, kModeFull, kNG, kDisc, kConv, kSN, kSN == kNS>(m, p, grid, st);
+        else
+            launch_full<kBF16, kModeFull, kNG, kDisc, kConv, kSN>(m, p, grid, st);
     } else if (mode == kModeAgg) {
         s6_fwd_tma_kernel<kBF16, kModeAgg, kNG, kDisc, kConv, kSN>
             <<<grid, 32 * kNG, 0, st>>>(m.u, m.d, m.z, m.B, m.C, p);
