@@ -50,6 +50,9 @@
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "msc_common.cuh"
 #include "msc_internal.h"
@@ -1135,21 +1138,25 @@ bool make_maps(FwdMaps& m, const FwdParams& p, int64_t batch, bool bf16) {
 // warps but add more exchange work than the extra latency hiding recovers.
 constexpr int kLanesPerRow = 2;
 
-// Resident CTAs per SM of a kernel instance, once per device.
+// Resident CTAs per SM of a kernel instance, queried once per (instance,
+// block size, device).  Keyed by the kernel's address: every instance of
+// s6_fwd_tma_kernel has the same function type, so a cache per type would
+// hand one instance's occupancy (8 CTAs per SM with 16 slots, 3 with 64) to
+// all of them.
 template <typename K>
 int resident_ctas(K kernel, int threads) {
-    static std::atomic<uint64_t> known{0};
-    static std::atomic<int> per_sm[64];
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, int, int>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const uint64_t bit = msc_host::device_bit();
-    if (!(known.load() & bit)) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
-        per_sm[dev & 63] = n;
-        known |= bit;
-    }
-    return per_sm[dev & 63].load();
+    const auto key = std::make_tuple(reinterpret_cast<const void*>(kernel), threads, dev);
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
+    cache.emplace(key, n);
+    return n;
 }
 
 // A full pass: persistent CTAs taking (row block, chunk) tickets when the
