@@ -25,7 +25,12 @@
 // runs the n loop on packed fp32 pairs (fma.rn.f32x2: two states per issue
 // slot) with B / C converted once per tile into an n-pair-interleaved fp32
 // layout (each pair is one 64-bit broadcast operand).  The readout partial sums
-// are reduce-scattered between the pair and y is stored from registers.
+// are reduce-scattered between the pair and y is stored from registers; rows of
+// 2^19 steps or more stage y in shared memory instead and write each row's
+// 32-step window as one 128-byte run (kLongRows).  A tile takes two CTA
+// barriers with 16 state slots (the wait's vote with the end of the B/C
+// conversion, and the tile's end before its stage is refilled) and one with
+// more slots (the next tile issued at the first).
 // Rows whose byte stride is not a multiple of 16 cannot be described to TMA;
 // they take the plain-load kernel (s6_fwd_rows_kernel), which stages each tile
 // with coalesced loads and computes the same way in scalar fp32.
