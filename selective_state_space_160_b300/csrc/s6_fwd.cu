@@ -444,14 +444,15 @@ __device__ __forceinline__ void issue_tile(int, int64_t tj64, uint8_t* st, uint6
 // One level of the readout reduce-scatter: lanes that differ in bit `kSL` of
 // their group position exchange halves of v[0..kSpan) and keep the half of
 // their side, summed, in v[0..kSpan/2).
-template <int kSL, int kSpan>
+// kJShift: the lane bit at which the position j within the group starts.
+template <int kSL, int kSpan, int kJShift = 0>
 __device__ __forceinline__ void reduce_scatter_level(float* v, int j) {
     const bool side = (j & kSL) != 0;
 #pragma unroll
     for (int k = 0; k < kSpan / 2; ++k) {
         const float send = side ? v[k] : v[k + kSpan / 2];
         const float keep = side ? v[k + kSpan / 2] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, kSL);
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, kSL << kJShift);
     }
 }
 
@@ -480,7 +481,8 @@ __device__ __forceinline__ void reduce_scatter_level(float* v, int j) {
 // through HBM.
 // Resident CTAs asked of the compiler (0: its own choice), as timed best at
 // 8 x 5120 x 2048: 16 slots: its choice (126-128 registers, 8 per SM); 32 slots:
-// its choice with bf16 (96 registers, 5 per SM), 4 with fp32; 64 slots: 3.
+// its choice with bf16 (126 registers, 4 per SM; held to 5 it spills and runs
+// 3-4% slower), 4 with fp32; 64 slots: 3.
 template <bool kBF16, int kSN>
 constexpr int fwd_min_ctas() { return kSN == 16 ? 0 : kSN == 32 ? (kBF16 ? 0 : 4) : 3; }
 
@@ -532,11 +534,18 @@ __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd
     __shared__ __align__(16) float s_y[kStageY ? kRows : 1][kStageY ? 40 : 4];
     __shared__ __align__(8) uint64_t s_full[kStages];
 
+    // Lanes of a row: with two lanes, adjacent lanes (j = lane bit 0).  With
+    // four, lanes 8 apart (j = lane >> 3; a warp holds 8 rows): a 16-byte shared
+    // load costs two wavefronts when each quarter-warp reads one address (all
+    // its lanes the same state quarter), about four when the quarter-warp's
+    // lanes read four (measured: the B/C loads of the adjacent layout cost 3.9
+    // wavefronts each with the shared-memory pipe 94% busy).
+    constexpr int kJShift = kNG == 4 ? 3 : 0;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
-    const int r = tid / kNG;          // row within the CTA
-    const int j = lane & (kNG - 1);   // position within the row's lane group
-    const int glane0 = lane & ~(kNG - 1);
+    const int r = kNG == 4 ? (tid >> 5) * 8 + (lane & 7) : tid / kNG;  // row within the CTA
+    const int j = (lane >> kJShift) & (kNG - 1);                       // position within the row's lane group
+    const int glane0 = lane & ~((kNG - 1) << kJShift);
     const int N = p.N;
     const bool has_z = kFull && p.z != nullptr;
     __shared__ long long s_ticket;
@@ -834,7 +843,7 @@ __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd
             float dts[8], dtus[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const int src = glane0 | (k / kSPG);
+                const int src = glane0 | ((k / kSPG) << kJShift);
                 if constexpr (kNG == 1) {
                     dts[k] = mdt[k];
                     dtus[k] = mdtu[k];
@@ -923,8 +932,8 @@ __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd
                     v[k] = lo + hi;
                 }
                 // reduce-scatter over the group: lane j ends with steps j*kSPG ..
-                if constexpr (kNG > 1) reduce_scatter_level<kNG / 2, 8>(v, j);
-                if constexpr (kNG == 4) reduce_scatter_level<1, 4>(v, j);
+                if constexpr (kNG > 1) reduce_scatter_level<kNG / 2, 8, kJShift>(v, j);
+                if constexpr (kNG == 4) reduce_scatter_level<1, 4, kJShift>(v, j);
                 uint64_t y2[kSPG / 2];
 #pragma unroll
                 for (int e = 0; e < kSPG / 2; ++e) y2[e] = msc::add2(msc::pk2(v[2 * e], v[2 * e + 1]), mdu2[e]);
@@ -1011,7 +1020,7 @@ __global__ void __launch_bounds__(32 * kNG, (fwd_min_ctas<kBF16, kSN>())) s6_fwd
     if (kMode == kModeCkpt) return;
     if (!kFull) {
 #pragma unroll
-        for (int sl = 1; sl < kNG; sl *= 2) dsum += __shfl_xor_sync(0xffffffffu, dsum, sl);
+        for (int sl = 1; sl < kNG; sl *= 2) dsum += __shfl_xor_sync(0xffffffffu, dsum, sl << kJShift);
     }
     // a chained chunk that is not the row's last hands its state to the next chunk
     const bool publish = kFull && p.ctr && p.chained && t_end < p.L;
