@@ -51,6 +51,12 @@ def _time(wide_first):
 
 
 def test_headline_grid_does_not_depend_on_the_first_instance():
-    fresh = _time(False)
-    after_wide = _time(True)
+    # one re-measurement of both before failing, so that a passing slowdown of a
+    # shared GPU is not taken for the grid (the fault it guards against costs
+    # a third: 0.582 against 0.436 ms)
+    for attempt in range(2):
+        fresh = _time(False)
+        after_wide = _time(True)
+        if after_wide <= 1.25 * fresh:
+            break
     assert after_wide <= 1.25 * fresh, (fresh, after_wide)
