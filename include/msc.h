@@ -66,8 +66,8 @@ typedef enum { MSC_F32 = 0, MSC_BF16 = 1 } msc_dtype;
  * Optional (may be NULL): D (no feed-through), z (no gate), delta_bias (0),
  * h0 (zero initial state), h_last (final state not returned).
  * Limits: batch, dim, seqlen >= 1; 1 <= dstate <= MSC_S6_FWD_MAX_DSTATE (64).
- * Above 16 states the fused conv front end is not offered; the backward and
- * the decode step take up to MSC_S6_MAX_DSTATE (16), the SSD entry points
+ * Above 16 states the fused conv front end is not offered; the backward takes
+ * up to MSC_S6_MAX_DSTATE (16), the decode step 64 like the forward, the SSD entry points
  * dstate 128.  Each row holds its states in 16, 32 or 64 slots (the next of
  * these at or above dstate); the slots past dstate carry zeros.  Above 16
  * states, rows that TMA cannot stream as they are (seqlen not a multiple of 8
@@ -278,10 +278,11 @@ msc_status msc_selective_scan_bwd_ckpt(int64_t batch, int64_t dim, int64_t seqle
  *   y = (sum_n C[b, n] state[n] + D[d] u) * silu(z)
  * Shapes: u, delta, z, y: [batch, dim]; B, C: [batch, dstate]; A: [dim, dstate];
  * D, delta_bias: [dim]; state: [batch, dim, dstate] fp32, read and overwritten
- * in place.  dstate 1..16 (MSC_S6_MAX_DSTATE); no workspace.  Calling
- * it seqlen times on tokens t = 0.. reproduces msc_selective_scan_fwd with
- * h0 = the initial state, up to fp32 rounding.  A state row of 16 states is
- * moved with one 32-byte load and store per thread (two threads per row).
+ * in place.  dstate 1..64 (MSC_S6_FWD_MAX_DSTATE, as the forward); no
+ * workspace.  Calling it seqlen times on tokens t = 0.. reproduces
+ * msc_selective_scan_fwd with h0 = the initial state, up to fp32 rounding.
+ * Each thread moves 8 states of a row with one 32-byte load and store (two,
+ * four or eight threads per row up to 16, 32 or 64 states).
  */
 msc_status msc_selective_state_update(int64_t batch, int64_t dim, int64_t dstate, msc_dtype in_dtype,
                                       const void* u, const void* delta, const float* A,

@@ -224,7 +224,7 @@ msc_status msc_selective_state_update(int64_t batch, int64_t dim, int64_t dstate
                                       const void* C, const float* D, const void* z, const float* delta_bias,
                                       float* state, float* y, void* stream) {
     clear_error();
-    msc_status s = check_s6_dims(batch, dim, 1, dstate, in_dtype);
+    msc_status s = check_s6_dims(batch, dim, 1, dstate, in_dtype, MSC_S6_FWD_MAX_DSTATE);
     if (s != MSC_OK) return s;
     MSC_PTR(u, "u"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A"); MSC_PTR(B, "B");
     MSC_PTR(C, "C"); MSC_PTR(state, "state"); MSC_PTR(y, "y");

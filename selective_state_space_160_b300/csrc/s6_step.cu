@@ -9,12 +9,13 @@
 //
 // Design.  The step is bound by HBM: per row the fp32 state (dstate floats) is
 // read and written once, u / delta / z are a few bytes, and A (shared across the
-// batch) and B, C (shared across channels) are served from L2 and L1.  Two
-// threads share a row: thread j owns states [8 j, 8 j + 8), so a warp moves 16
-// consecutive rows = one contiguous 1 KB block of state per 16-byte access
-// (dstate 16; smaller dstate takes scalar accesses).  The two readout partial
-// sums meet in one shuffle; thread 0 of the pair applies skip and gate and
-// stores y.  16 exps per row ride on the MUFU pipe, far below the bytes.
+// batch) and B, C (shared across channels) are served from L2 and L1.  kLanes
+// threads share a row (2 up to 16 states, 4 up to 32, 8 up to 64): thread j
+// owns states [8 j, 8 j + 8), so a warp moves 32 / kLanes consecutive rows =
+// one contiguous 1 KB block of state per 16-byte access (dstate 16, 32 or 64;
+// other sizes take scalar accesses).  The readout partial sums meet in a
+// shuffle butterfly; thread 0 of the row applies skip and gate and stores y.
+// dstate exps per row ride on the MUFU pipe, far below the bytes.
 #include <cuda_runtime.h>
 
 #include "msc_common.cuh"
@@ -37,12 +38,12 @@ struct StepParams {
     int N;
 };
 
-// kVec: dstate == 16 (every row and half-row 16-byte aligned)
-template <bool kBF16, bool kVec>
+// kVec: dstate == 8 kLanes (every row and 8-state slice 16-byte aligned)
+template <bool kBF16, bool kVec, int kLanes>
 __global__ void __launch_bounds__(256) s6_step_kernel(const StepParams p) {
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int j = threadIdx.x & 1;
-    const int64_t row_raw = idx >> 1;
+    const int j = threadIdx.x & (kLanes - 1);
+    const int64_t row_raw = idx / kLanes;
     const bool row_ok = row_raw < p.rows;
     const int64_t row = row_ok ? row_raw : p.rows - 1;  // out-of-range pairs compute on the last row, store nothing
     const int64_t b = row / p.dim, d = row % p.dim;
@@ -87,7 +88,8 @@ __global__ void __launch_bounds__(256) s6_step_kernel(const StepParams p) {
             acc0 = fmaf(cv[k], h[k], acc0);
     }
     float acc = acc0 + acc1;
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+#pragma unroll
+    for (int m = 1; m < kLanes; m *= 2) acc += __shfl_xor_sync(0xffffffffu, acc, m);
     if (!row_ok) return;
     if (kVec) {
         *reinterpret_cast<float4*>(st) = make_float4(h[0], h[1], h[2], h[3]);
@@ -104,16 +106,23 @@ __global__ void __launch_bounds__(256) s6_step_kernel(const StepParams p) {
     }
 }
 
-template <bool kBF16>
-msc_status launch(const StepParams& p, cudaStream_t st) {
-    const int64_t blocks = (2 * p.rows + 255) / 256;
+template <bool kBF16, int kLanes>
+msc_status launch_lanes(const StepParams& p, cudaStream_t st) {
+    const int64_t blocks = (kLanes * p.rows + 255) / 256;
     if (blocks > 0x7FFFFFFF) return msc_host::fail(MSC_ERR_UNSUPPORTED, "batch * dim too large for one launch");
     const unsigned grid = (unsigned)blocks;
-    if (p.N == 16)
-        s6_step_kernel<kBF16, true><<<grid, 256, 0, st>>>(p);
+    if (p.N == 8 * kLanes)
+        s6_step_kernel<kBF16, true, kLanes><<<grid, 256, 0, st>>>(p);
     else
-        s6_step_kernel<kBF16, false><<<grid, 256, 0, st>>>(p);
+        s6_step_kernel<kBF16, false, kLanes><<<grid, 256, 0, st>>>(p);
     return msc_host::check_launch("s6_step");
+}
+
+template <bool kBF16>
+msc_status launch(const StepParams& p, cudaStream_t st) {
+    if (p.N <= 16) return launch_lanes<kBF16, 2>(p, st);
+    if (p.N <= 32) return launch_lanes<kBF16, 4>(p, st);
+    return launch_lanes<kBF16, 8>(p, st);
 }
 
 }  // namespace

@@ -159,7 +159,8 @@ def test_step_rejects_bad_arguments(lib):
     assert call(y=None) == msc.MSC_ERR_INVALID_ARG
     assert call(u=24) == msc.MSC_ERR_INVALID_ARG                 # misaligned
     assert call(z=40) == msc.MSC_ERR_INVALID_ARG
-    assert call(N=17) == msc.MSC_ERR_UNSUPPORTED
+    assert call(N=65) == msc.MSC_ERR_UNSUPPORTED                 # up to 64 states
+    assert call(N=0) == msc.MSC_ERR_UNSUPPORTED
     assert call(dim=0) == msc.MSC_ERR_INVALID_ARG
     assert call(dt=5) == msc.MSC_ERR_INVALID_ARG
 

@@ -199,7 +199,7 @@ def test_s6_backward(batch, dim, L, bf16):
     _check(outs, msc, st)
 
 
-@pytest.mark.parametrize("N,bf16", [(16, True), (5, False)])
+@pytest.mark.parametrize("N,bf16", [(16, True), (5, False), (64, True), (40, False)])
 def test_s6_decode_step(N, bf16):
     import torch
     msc, lib = _lib()

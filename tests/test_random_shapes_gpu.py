@@ -79,7 +79,7 @@ def test_decode_step_random(i):
     import selective_state_space_160_b300 as msc
     r = np.random.default_rng(94_000 + i)
     bf16 = bool(r.integers(2))
-    N = int(r.choice([1, 5, 16]))
+    N = int(r.choice([1, 5, 16, 24, 32, 64]))
     dim, batch = int(r.integers(1, 70)), int(r.integers(1, 5))
     inp = s6_inputs(batch, dim, 1, N, seed=95_000 + i, bf16=bf16)
     st0 = np.random.default_rng(i).standard_normal((batch, dim, N)).astype(np.float32)

@@ -1,6 +1,6 @@
 """GPU parity of the S6 decode step (msc_selective_state_update, through the C
 ABI) against the oracle's decode step, and against the scan run over the same
-tokens.
+tokens, for 1 to 64 states (two, four or eight lanes per row).
 
 Tolerances (max |gpu - ref| / (1 + |ref|)): 1e-4 with fp32 inputs, 2e-3 with
 bf16 inputs (the oracle consumes the same bf16-rounded values); chained steps
@@ -46,7 +46,9 @@ def _oracle_steps(inp, h0, T):
 
 
 @pytest.mark.parametrize("batch,dim,N", [(1, 4, 16), (3, 37, 16), (2, 130, 16), (1, 5, 7), (4, 33, 1),
-                                         (2, 64, 12), (1, 1, 16)])
+                                         (2, 64, 12), (1, 1, 16),
+                                         # four and eight lanes per row: vector and scalar state rows
+                                         (2, 37, 32), (3, 9, 20), (2, 33, 64), (1, 70, 48), (1, 3, 17)])
 @pytest.mark.parametrize("bf16", [False, True])
 def test_single_step(batch, dim, N, bf16):
     inp = s6_inputs(batch, dim, 1, N, seed=7000 + batch * 100 + dim + N, bf16=bf16)
@@ -69,14 +71,14 @@ def test_optional_inputs(with_z, with_D, with_bias):
     assert max_rel_err(h, hr) <= TOL_F32
 
 
-@pytest.mark.parametrize("bf16", [False, True])
-def test_steps_match_scan(bf16):
+@pytest.mark.parametrize("bf16,N", [(False, 16), (True, 16), (True, 64), (False, 40)])
+def test_steps_match_scan(bf16, N):
     """64 decode steps from a random state equal the GPU scan over the same 64
     tokens from that state, and both match the oracle scan."""
     import selective_state_space_160_b300 as msc
     T = 64
-    inp = s6_inputs(2, 96, T, 16, seed=72, bf16=bf16)
-    h0 = np.random.default_rng(3).standard_normal((2, 96, 16)).astype(np.float32)
+    inp = s6_inputs(2, 96, T, N, seed=72 + N, bf16=bf16)
+    h0 = np.random.default_rng(3).standard_normal((2, 96, N)).astype(np.float32)
     y_step, h_step = _steps(inp, bf16, h0, T)
     dev = {k: to_dev(inp[k], bf16) for k in ("u", "delta", "z", "B", "C")}
     y_scan, h_scan = msc.msc_selective_scan_fwd(dev["u"], dev["delta"], to_dev(inp["A"]), dev["B"], dev["C"],
