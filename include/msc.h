@@ -66,8 +66,9 @@ typedef enum { MSC_F32 = 0, MSC_BF16 = 1 } msc_dtype;
  * Optional (may be NULL): D (no feed-through), z (no gate), delta_bias (0),
  * h0 (zero initial state), h_last (final state not returned).
  * Limits: batch, dim, seqlen >= 1; 1 <= dstate <= MSC_S6_FWD_MAX_DSTATE (64).
- * Above 16 states the fused conv front end is not offered; the backward takes
- * up to MSC_S6_MAX_DSTATE (16), the decode step 64 like the forward, the SSD entry points
+ * Above 16 states the fused conv front end and the training pair are not
+ * offered (MSC_S6_MAX_DSTATE, 16); the backward and the decode step take 64
+ * like the forward, the SSD entry points
  * dstate 128.  Each row holds its states in 16, 32 or 64 slots (the next of
  * these at or above dstate); the slots past dstate carry zeros.  Above 16
  * states, rows that TMA cannot stream as they are (seqlen not a multiple of 8
@@ -213,8 +214,11 @@ msc_status msc_selective_scan_fwd_conv(int64_t batch, int64_t dim, int64_t seqle
  * gradient dy [batch, dim, seqlen] (in_dtype).  Outputs (fp32, overwritten):
  * du, ddelta: [batch, dim, seqlen]; dA: [dim, dstate]; dB, dC: [batch, dstate, seqlen];
  * dD [dim] (required iff D != NULL); dz [batch, dim, seqlen] (required iff z != NULL);
- * ddelta_bias [dim] (required iff delta_bias != NULL).  dstate <= 16
- * (MSC_S6_MAX_DSTATE), else MSC_ERR_UNSUPPORTED.
+ * ddelta_bias [dim] (required iff delta_bias != NULL).  dstate <= 64
+ * (MSC_S6_FWD_MAX_DSTATE, as the forward), else MSC_ERR_UNSUPPORTED.  Above 16
+ * states the backward runs once per slice of 16 (every gradient is a sum of
+ * per-state terms or is per state): the slices' du, ddelta and dz add up in
+ * the outputs, and the workspace also holds one slice of A and of dA.
  * The forward states are recomputed from checkpoints kept every 8 steps in the
  * workspace (16 fp32 per row and group: 8 bytes per element); dB, dC, dA, dD and
  * ddelta_bias are sums accumulated with fp32 atomics, so their low bits depend

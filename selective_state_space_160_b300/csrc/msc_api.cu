@@ -307,7 +307,7 @@ msc_status msc_selective_scan_fwd(int64_t batch, int64_t dim, int64_t seqlen, in
 
 size_t msc_selective_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen,
                                              int64_t dstate) {
-    if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > 16) return 0;
+    if (batch < 1 || dim < 1 || seqlen < 1 || dstate < 1 || dstate > MSC_S6_FWD_MAX_DSTATE) return 0;
     return s6_bwd_workspace(batch, dim, seqlen, dstate);
 }
 
@@ -319,7 +319,7 @@ msc_status msc_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, in
                                   float* dD, float* dz, float* ddelta_bias, void* workspace,
                                   size_t workspace_bytes, void* stream) {
     clear_error();
-    msc_status s = check_s6_dims(batch, dim, seqlen, dstate, in_dtype);
+    msc_status s = check_s6_dims(batch, dim, seqlen, dstate, in_dtype, MSC_S6_FWD_MAX_DSTATE);
     if (s != MSC_OK) return s;
     MSC_PTR(u, "u"); MSC_PTR(delta, "delta"); MSC_PTR(A, "A"); MSC_PTR(B, "B");
     MSC_PTR(C, "C"); MSC_PTR(dy, "dy");

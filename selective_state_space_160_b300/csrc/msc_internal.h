@@ -43,6 +43,9 @@ struct S6FwdArgs {
     int conv_k = 0;
     // training forward: also the state entering every 8-step group, [rows, L / 8, 16]
     float* ckpt = nullptr;
+    // checkpoint pass on a slice of the states: B and C point at the slice's
+    // first state row, bc_rows state rows apart per batch entry (0: N)
+    int bc_rows = 0;
 };
 
 msc_status s6_fwd_launch(const S6FwdArgs& a, const S6Plan& plan, cudaStream_t stream);

@@ -74,6 +74,17 @@ struct BwdParams {
     int has_z;
 };
 
+// More than 16 states run as slices of up to 16 (every gradient is a sum over
+// states of per-state terms, or per state): A, dA and ckpt hold the slice
+// only, dB and dC point at its first state row, bc_rows state rows apart per
+// batch entry.  The first slice adds the terms without states (D u in the
+// readout, g' D in du, dD); later slices add du, ddelta and dz to what is
+// there.  A parameter of its own, which the whole-state instance never reads.
+struct BwdSlice {
+    int64_t bc_rows;
+    int first, accumulate;
+};
+
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
@@ -123,14 +134,16 @@ __device__ __forceinline__ void load2(const uint8_t* tile, int r, uint32_t boff,
 // 2048 x 2048 bf16: 1.64 ms, against 1.72 with B loaded twice at three CTAs per
 // SM and 2.4 with B kept but squeezed into three CTAs per SM (spills); the
 // row-pair exchange of the dB/dC sums then 1.61.
-template <bool kBF16>
+// kSlice: one 16-state slice of a wider state (the flags and dB / dC stride of
+// BwdParams apply); otherwise the whole state, 16 or fewer.
+template <bool kBF16, bool kSlice>
 __global__ void __launch_bounds__(kThreads, 2) s6_bwd_kernel(const __grid_constant__ CUtensorMap tm_u,
                                                          const __grid_constant__ CUtensorMap tm_d,
                                                          const __grid_constant__ CUtensorMap tm_z,
                                                          const __grid_constant__ CUtensorMap tm_dy,
                                                          const __grid_constant__ CUtensorMap tm_B,
                                                          const __grid_constant__ CUtensorMap tm_C,
-                                                         const BwdParams p) {
+                                                         const BwdParams p, const BwdSlice sl) {
     constexpr int kTT = kBF16 ? 32 : 16;  // steps per 64-byte tile row
     constexpr int kGroups = kTT / 8;
     constexpr int kPitch = 2 * kTT + 4;
@@ -173,7 +186,10 @@ __global__ void __launch_bounds__(kThreads, 2) s6_bwd_kernel(const __grid_consta
         Ap[q] = msc::pk2(a[0], a[1]);
         A2p[q] = msc::pk2(a[0] * MSC_LOG2E, a[1] * MSC_LOG2E);
     }
-    const float Dd = (p.D && row_ok) ? __ldg(p.D + d) : 0.f;
+    const bool first = !kSlice || sl.first != 0;
+    const bool accumulate = kSlice && sl.accumulate != 0;
+    const int64_t bc_rows = kSlice ? sl.bc_rows : (int64_t)p.N;
+    const float Dd = (p.D && row_ok && first) ? __ldg(p.D + d) : 0.f;
     const float bias = (p.delta_bias && row_ok) ? __ldg(p.delta_bias + d) : 0.f;
 
     uint64_t lam[2] = {0ull, 0ull};      // lambda of the step after the current one
@@ -402,6 +418,16 @@ __global__ void __launch_bounds__(kThreads, 2) s6_bwd_kernel(const __grid_consta
             }
             if (row_ok) {
                 const size_t off = (size_t)row * p.L + tg + 2 * j;
+                if (accumulate) {
+                    const float2 a = *reinterpret_cast<const float2*>(p.du + off);
+                    const float2 c = *reinterpret_cast<const float2*>(p.ddelta + off);
+                    o_du[0] += a.x; o_du[1] += a.y;
+                    o_dd[0] += c.x; o_dd[1] += c.y;
+                    if (has_z) {
+                        const float2 e = *reinterpret_cast<const float2*>(p.dz + off);
+                        o_dz[0] += e.x; o_dz[1] += e.y;
+                    }
+                }
                 *reinterpret_cast<float2*>(p.du + off) = make_float2(o_du[0], o_du[1]);
                 *reinterpret_cast<float2*>(p.ddelta + off) = make_float2(o_dd[0], o_dd[1]);
                 if (has_z) *reinterpret_cast<float2*>(p.dz + off) = make_float2(o_dz[0], o_dz[1]);
@@ -434,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 2) s6_bwd_kernel(const __grid_consta
                 const int x = tid >> 5, n = (tid >> 1) & 15, kq = tid & 1;
                 const float4 v = *reinterpret_cast<const float4*>(s_sum + (16 * x + n) * kSumPitch + 4 * kq);
                 if (n < N) {
-                    float* dst = (x == 0 ? p.dB : p.dC) + ((size_t)b * N + n) * p.L + tg + 4 * kq;
+                    float* dst = (x == 0 ? p.dB : p.dC) + ((size_t)b * bc_rows + n) * p.L + tg + 4 * kq;
                     red_add_v4(dst, v.x, v.y, v.z, v.w);
                 }
             }
@@ -465,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 2) s6_bwd_kernel(const __grid_consta
         if (n + 1 < N) atomicAdd(p.dA + d * N + n + 1, v1);
     }
     if (j == 0) {
-        if (p.dD) atomicAdd(p.dD + d, dD_acc);
+        if (p.dD && first) atomicAdd(p.dD + d, dD_acc);
         if (p.dbias) atomicAdd(p.dbias + d, dbias_acc);
     }
 }
@@ -476,17 +502,19 @@ constexpr int bwd_smem_bytes() {
            2 * 16 * kSumPitch * 4 + kStages * 8;
 }
 
-template <bool kBF16>
-msc_status launch_bwd(const CUtensorMap* maps, const BwdParams& p, int64_t batch, cudaStream_t st) {
+template <bool kBF16, bool kSlice>
+msc_status launch_bwd(const CUtensorMap* maps, const BwdParams& p, const BwdSlice& sl, int64_t batch,
+                      cudaStream_t st) {
     constexpr int smem = bwd_smem_bytes<kBF16>();
     static std::atomic<uint64_t> configured{0};  // the attribute, set once per device (per instantiation)
     if (!(configured & msc_host::device_bit())) {
-        cudaError_t e = cudaFuncSetAttribute(s6_bwd_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(s6_bwd_kernel<kBF16, kSlice>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return msc_host::fail(MSC_ERR_CUDA, "s6_bwd smem attribute: %s", cudaGetErrorString(e));
         configured |= msc_host::device_bit();
     }
     dim3 grid((unsigned)((p.dim + kRows - 1) / kRows), (unsigned)batch, 1);
-    s6_bwd_kernel<kBF16><<<grid, kThreads, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    s6_bwd_kernel<kBF16, kSlice><<<grid, kThreads, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+                                                                sl);
     return msc_host::check_launch("s6_bwd");
 }
 
@@ -505,23 +533,24 @@ static int64_t padded_len(int64_t L, bool bf16) {
 }
 
 size_t s6_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
-    (void)dstate;
     const int64_t rows = batch * dim;
     const int64_t Lp = padded_len(seqlen, true);
-    size_t ws = align256((size_t)rows * (size_t)((Lp + 7) / 8) * 16 * sizeof(float));  // checkpoints
+    size_t ws = align256((size_t)rows * (size_t)((Lp + 7) / 8) * 16 * sizeof(float));  // checkpoints (one slice)
+    if (dstate > 16) ws += 2 * align256((size_t)dim * 16 * sizeof(float));             // A and dA of a slice
     if (Lp != seqlen) {
         // padded copies: u, delta, z, dy (4 bytes is the larger element) and
         // du, ddelta, dz; B, C, dB, dC
-        ws += 7 * align256((size_t)rows * Lp * 4) + 4 * align256((size_t)batch * 16 * Lp * 4);
+        ws += 7 * align256((size_t)rows * Lp * 4) + 4 * align256((size_t)batch * dstate * Lp * 4);
     }
     return ws;
 }
 
+// rows_per_b rows of L steps per batch entry, stride_rows rows apart (0: rows_per_b)
 static msc_status make_row_map(CUtensorMap* m, const void* base, bool bf16, int64_t L, int64_t rows_per_b,
-                               int64_t batch, uint32_t box_rows) {
+                               int64_t batch, uint32_t box_rows, int64_t stride_rows = 0) {
     const uint64_t es = bf16 ? 2 : 4;
     const uint64_t dims[3] = {(uint64_t)L, (uint64_t)rows_per_b, (uint64_t)batch};
-    const uint64_t str[2] = {(uint64_t)L * es, (uint64_t)rows_per_b * L * es};
+    const uint64_t str[2] = {(uint64_t)L * es, (uint64_t)(stride_rows ? stride_rows : rows_per_b) * L * es};
     const uint32_t box[3] = {bf16 ? 32u : 16u, box_rows, 1};
     return encode_tmap(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims,
                        str, box, CU_TENSOR_MAP_SWIZZLE_64B)
@@ -577,8 +606,17 @@ msc_status s6_bwd_launch(const S6BwdArgs& a0, cudaStream_t st) {
     // padded copies for rows whose stride TMA cannot describe
     const void *u = a.u, *dl = a.delta, *z = a.z, *dy = a.dy, *B = a.B, *C = a.C;
     float *du = a.du, *ddl = a.ddelta, *dz = a.dz, *dB = a.dB, *dC = a.dC;
+    // A and dA of one slice of 16 states (more than 16 states)
+    const int nslices = (a.N + 15) / 16;
+    float* A_s = nullptr;
+    float* dA_s = nullptr;
+    if (nslices > 1) {
+        if (a.ckpt_in) return fail(MSC_ERR_UNSUPPORTED, "kept checkpoints are for up to 16 states");
+        A_s = reinterpret_cast<float*>(ws); ws += align256((size_t)a.dim * 16 * sizeof(float));
+        dA_s = reinterpret_cast<float*>(ws); ws += align256((size_t)a.dim * 16 * sizeof(float));
+    }
     if (Lp != L) {
-        const size_t rbytes = align256((size_t)rows * Lp * 4), bbytes = align256((size_t)a.batch * 16 * Lp * 4);
+        const size_t rbytes = align256((size_t)rows * Lp * 4), bbytes = align256((size_t)a.batch * a.N * Lp * 4);
         void* pu = ws; ws += rbytes;
         void* pd = ws; ws += rbytes;
         void* pz = ws; ws += rbytes;
@@ -604,32 +642,57 @@ msc_status s6_bwd_launch(const S6BwdArgs& a0, cudaStream_t st) {
         du = pdu; ddl = pdd; dz = a.dz ? pdz : nullptr; dB = pdB; dC = pdC;
     }
 
-    // (1) states entering every 8-step group (unless the training forward kept them)
+    // Per slice of up to 16 states: (1) the states entering every 8-step group
+    // (unless the training forward kept them), (2) the reverse pass.
     msc_status s = MSC_OK;
-    if (!a.ckpt_in) {
-        S6FwdArgs f{};
-        f.batch = a.batch; f.dim = a.dim; f.L = Lp; f.N = a.N; f.bf16 = a.bf16;
-        f.u = u; f.delta = dl; f.B = B; f.C = C; f.A = a.A; f.delta_bias = a.delta_bias;
-        s = s6_fwd_checkpoints(f, const_cast<float*>(ckpt), st);
+    for (int sl = 0; sl < nslices; ++sl) {
+        const int n0 = 16 * sl, ns = a.N - n0 < 16 ? a.N - n0 : 16;
+        const float* A = a.A;
+        float* dA = a.dA;
+        const void* Bs = static_cast<const char*>(B) + (size_t)n0 * Lp * es;
+        const void* Cs = static_cast<const char*>(C) + (size_t)n0 * Lp * es;
+        if (nslices > 1) {
+            e = cudaMemcpy2DAsync(A_s, ns * sizeof(float), a.A + n0, a.N * sizeof(float), ns * sizeof(float),
+                                  a.dim, cudaMemcpyDeviceToDevice, st);
+            if (e == cudaSuccess) e = cudaMemsetAsync(dA_s, 0, (size_t)a.dim * ns * sizeof(float), st);
+            if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "state slice: %s", cudaGetErrorString(e));
+            A = A_s;
+            dA = dA_s;
+        }
+        if (!a.ckpt_in) {
+            S6FwdArgs f{};
+            f.batch = a.batch; f.dim = a.dim; f.L = Lp; f.N = ns; f.bf16 = a.bf16;
+            f.u = u; f.delta = dl; f.B = Bs; f.C = Cs; f.A = A; f.delta_bias = a.delta_bias;
+            f.bc_rows = a.N;
+            s = s6_fwd_checkpoints(f, const_cast<float*>(ckpt), st);
+            if (s != MSC_OK) return s;
+        }
+        CUtensorMap maps[6];
+        if ((s = make_row_map(&maps[0], u, a.bf16, Lp, a.dim, a.batch, kRows)) != MSC_OK) return s;
+        if ((s = make_row_map(&maps[1], dl, a.bf16, Lp, a.dim, a.batch, kRows)) != MSC_OK) return s;
+        if ((s = make_row_map(&maps[2], z ? z : u, a.bf16, Lp, a.dim, a.batch, kRows)) != MSC_OK) return s;
+        if ((s = make_row_map(&maps[3], dy, a.bf16, Lp, a.dim, a.batch, kRows)) != MSC_OK) return s;
+        if ((s = make_row_map(&maps[4], Bs, a.bf16, Lp, ns, a.batch, 16, a.N)) != MSC_OK) return s;
+        if ((s = make_row_map(&maps[5], Cs, a.bf16, Lp, ns, a.batch, 16, a.N)) != MSC_OK) return s;
+        BwdParams p{};
+        p.A = A; p.D = a.D; p.delta_bias = a.delta_bias; p.ckpt = ckpt;
+        p.du = du; p.ddelta = ddl; p.dz = dz; p.dA = dA; p.dB = dB + (size_t)n0 * Lp; p.dC = dC + (size_t)n0 * Lp;
+        p.dD = a.dD; p.dbias = a.ddelta_bias;
+        p.dim = a.dim; p.L = Lp; p.ckpt_groups = (Lp + 7) / 8; p.N = ns; p.has_z = z != nullptr;
+        BwdSlice sp{};
+        sp.bc_rows = a.N; sp.first = sl == 0; sp.accumulate = sl > 0;
+        if (nslices > 1)
+            s = a.bf16 ? launch_bwd<true, true>(maps, p, sp, a.batch, st) : launch_bwd<false, true>(maps, p, sp, a.batch, st);
+        else
+            s = a.bf16 ? launch_bwd<true, false>(maps, p, sp, a.batch, st)
+                       : launch_bwd<false, false>(maps, p, sp, a.batch, st);
         if (s != MSC_OK) return s;
+        if (nslices > 1) {
+            e = cudaMemcpy2DAsync(a.dA + n0, a.N * sizeof(float), dA_s, ns * sizeof(float), ns * sizeof(float),
+                                  a.dim, cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) return fail(MSC_ERR_CUDA, "state slice: %s", cudaGetErrorString(e));
+        }
     }
-
-    // (2) the reverse pass
-    CUtensorMap maps[6];
-    if ((s = make_row_map(&maps[0], u, a.bf16, Lp, a.dim, a.batch, kRows)) != MSC_OK) return s;
-    if ((s = make_row_map(&maps[1], dl, a.bf16, Lp, a.dim, a.batch, kRows)) != MSC_OK) return s;
-    if ((s = make_row_map(&maps[2], z ? z : u, a.bf16, Lp, a.dim, a.batch, kRows)) != MSC_OK) return s;
-    if ((s = make_row_map(&maps[3], dy, a.bf16, Lp, a.dim, a.batch, kRows)) != MSC_OK) return s;
-    if ((s = make_row_map(&maps[4], B, a.bf16, Lp, a.N, a.batch, 16)) != MSC_OK) return s;
-    if ((s = make_row_map(&maps[5], C, a.bf16, Lp, a.N, a.batch, 16)) != MSC_OK) return s;
-    BwdParams p{};
-    p.A = a.A; p.D = a.D; p.delta_bias = a.delta_bias; p.ckpt = ckpt;
-    p.du = du; p.ddelta = ddl; p.dz = dz; p.dA = a.dA; p.dB = dB; p.dC = dC;
-    p.dD = a.dD; p.dbias = a.ddelta_bias;
-    p.dim = a.dim; p.L = Lp; p.ckpt_groups = (Lp + 7) / 8; p.N = a.N; p.has_z = z != nullptr;
-    s = a.bf16 ? launch_bwd<true>(maps, p, a.batch, st) : launch_bwd<false>(maps, p, a.batch, st);
-    if (s != MSC_OK) return s;
-
     if (Lp != L) {
         if ((s = unpad_copy(a.du, du, 4, rows, L, Lp, st)) != MSC_OK) return s;
         if ((s = unpad_copy(a.ddelta, ddl, 4, rows, L, Lp, st)) != MSC_OK) return s;

@@ -1128,7 +1128,8 @@ struct FwdMaps {
     CUtensorMap u, d, z, B, C;
 };
 
-bool make_maps(FwdMaps& m, const FwdParams& p, int64_t batch, bool bf16) {
+// bc_rows: state rows between batch entries of B and C (0: N)
+bool make_maps(FwdMaps& m, const FwdParams& p, int64_t batch, bool bf16, int64_t bc_rows = 0) {
     const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const uint64_t es = bf16 ? 2 : 4;
     const uint32_t tt = bf16 ? 32 : 16;
@@ -1136,7 +1137,7 @@ bool make_maps(FwdMaps& m, const FwdParams& p, int64_t batch, bool bf16) {
     const uint64_t rstr[2] = {(uint64_t)p.L * es, (uint64_t)p.dim * p.L * es};
     const uint32_t rbox[3] = {tt, (uint32_t)kRows, 1};
     const uint64_t bdims[3] = {(uint64_t)p.L, (uint64_t)p.N, (uint64_t)batch};
-    const uint64_t bstr[2] = {(uint64_t)p.L * es, (uint64_t)p.N * p.L * es};
+    const uint64_t bstr[2] = {(uint64_t)p.L * es, (uint64_t)(bc_rows ? bc_rows : p.N) * p.L * es};
     const uint32_t bbox[3] = {tt, (uint32_t)state_slots(p.N), 1};
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
     if (!msc_host::encode_tmap(&m.u, dt, 3, p.u, rdims, rstr, rbox, sw)) return false;
@@ -1511,7 +1512,7 @@ msc_status s6_fwd_checkpoints(const S6FwdArgs& a, float* ckpt, cudaStream_t st) 
     if (!tma_ok(p, a.bf16))
         return fail(MSC_ERR_UNSUPPORTED, "checkpoint pass needs a 16-byte row stride and seqlen, dim below 2^31");
     FwdMaps maps;
-    if (!make_maps(maps, p, a.batch, a.bf16)) return MSC_ERR_CUDA;
+    if (!make_maps(maps, p, a.batch, a.bf16, a.bc_rows)) return MSC_ERR_CUDA;
     return a.bf16 ? launch_tma_ng<true, 2>(maps, p, a.batch, 1, kModeCkpt, st)
                   : launch_tma_ng<false, 2>(maps, p, a.batch, 1, kModeCkpt, st);
 }

@@ -120,10 +120,17 @@ def test_bwd_rejects_bad_arguments(lib):
     ws = msc.msc_selective_scan_bwd_workspace_size(1, 4, big, 16)
     st = f(1, 4, big, 16, 1, *ok, None, None, None, 16, 16, 16, 16, 16, 16, None, None, None, 4096, ws, None)
     assert st == msc.MSC_ERR_UNSUPPORTED and "2^31" in msc.msc_last_error()
-    # the backward keeps 16 states (the forward takes up to 64)
-    st = f(1, 4, 64, 17, 0, *ok, None, None, None, 16, 16, 16, 16, 16, 16, None, None, None, None, 0, None)
-    assert st == msc.MSC_ERR_UNSUPPORTED and "[1, 16]" in msc.msc_last_error()
-    assert msc.msc_selective_scan_bwd_workspace_size(1, 4, 64, 17) == 0
+    # up to 64 states, as the forward; above 16 the workspace also holds one
+    # 16-state slice of A and of dA
+    st = f(1, 4, 64, 65, 0, *ok, None, None, None, 16, 16, 16, 16, 16, 16, None, None, None, None, 0, None)
+    assert st == msc.MSC_ERR_UNSUPPORTED and "[1, 64]" in msc.msc_last_error()
+    assert msc.msc_selective_scan_bwd_workspace_size(1, 4, 64, 65) == 0
+    w16 = msc.msc_selective_scan_bwd_workspace_size(1, 4, 64, 16)
+    assert msc.msc_selective_scan_bwd_workspace_size(1, 4, 64, 17) == w16 + 2 * 256
+    assert msc.msc_selective_scan_bwd_workspace_size(1, 4, 64, 64) == w16 + 2 * 256
+    # a smaller workspace above 16 states is refused before any launch
+    st = f(1, 4, 64, 40, 0, *ok, None, None, None, 16, 16, 16, 16, 16, 16, None, None, None, 4096, w16, None)
+    assert st == msc.MSC_ERR_WORKSPACE
 
 
 def test_ssd_rejects_bad_arguments(lib):

@@ -174,11 +174,12 @@ def test_s6_forward_from_host_buffers():
     _check({"y": y, "staging": stg}, msc, st)
 
 
-@pytest.mark.parametrize("batch,dim,L,bf16", [(2, 37, 64, True), (1, 36, 48, False), (2, 33, 2048, True)])
-def test_s6_backward(batch, dim, L, bf16):
+@pytest.mark.parametrize("batch,dim,L,bf16,N", [(2, 37, 64, True, 16), (1, 36, 48, False, 16),
+                                                (2, 33, 2048, True, 16),
+                                                (2, 37, 64, True, 40), (1, 9, 100, False, 64)])  # state slices
+def test_s6_backward(batch, dim, L, bf16, N):
     import torch
     msc, lib = _lib()
-    N = 16
     inp = s6_inputs(batch, dim, L, N, seed=31_500 + dim + L, bf16=bf16)
     d = _s6_dev(inp, bf16)
     A, D, bias = to_dev(inp["A"]), to_dev(inp["D"]), to_dev(inp["delta_bias"])

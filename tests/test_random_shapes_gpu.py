@@ -57,7 +57,7 @@ def test_backward_random(i):
     import selective_state_space_160_b300 as msc
     r = np.random.default_rng(92_000 + i)
     bf16 = bool(r.integers(2))
-    N = int(r.choice([1, 4, 16, 16]))
+    N = int(r.choice([1, 4, 16, 16, 24, 40]))
     L = int(r.choice([1, 9, 48, 64, 130, 300]))
     dim, batch = int(r.integers(1, 40)), int(r.integers(1, 3))
     opts = dict(with_z=bool(r.integers(2)), with_D=bool(r.integers(2)), with_bias=bool(r.integers(2)))

@@ -48,6 +48,24 @@ def test_shapes(batch, dim, L, N, bf16):
     _check(_run(inp, bf16), _ref(inp), TOL_BF16 if bf16 else TOL_F32)
 
 
+@pytest.mark.parametrize("batch,dim,L,N,bf16", [
+    (1, 8, 64, 32, False), (2, 37, 96, 64, True), (1, 33, 128, 20, False), (2, 6, 100, 40, True),
+    (1, 5, 9, 17, False), (3, 40, 256, 48, False)])
+def test_more_than_16_states(batch, dim, L, N, bf16):
+    """Above 16 states the backward runs once per 16-state slice: du, ddelta
+    and dz add up over the slices, D terms count once, dA / dB / dC land in
+    their slice (ragged last slices, unaligned rows on the padded copies)."""
+    inp = s6_inputs(batch, dim, L, N, seed=2500 + dim + L + N, bf16=bf16, with_dy=True)
+    _check(_run(inp, bf16), _ref(inp), TOL_BF16 if bf16 else TOL_F32)
+
+
+@pytest.mark.parametrize("with_z,with_D,with_bias", [(False, True, True), (True, False, True),
+                                                     (True, True, False), (False, False, False)])
+def test_more_than_16_states_optional_inputs(with_z, with_D, with_bias):
+    inp = s6_inputs(2, 36, 64, 33, seed=2600, with_z=with_z, with_D=with_D, with_bias=with_bias, with_dy=True)
+    _check(_run(inp, False), _ref(inp), TOL_F32)
+
+
 @pytest.mark.parametrize("with_z,with_D,with_bias", [(False, True, True), (True, False, True),
                                                      (True, True, False), (False, False, False)])
 def test_optional_inputs(with_z, with_D, with_bias):
