@@ -47,10 +47,10 @@ HEADLINE = dict(batch=8, dim=5120, L=2048, N=16)
 # dram__bytes_read.sum + dram__bytes_write.sum per launch, from one ncu capture,
 # keyed by kernel; valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
-    # profiles/s6_fwd_tma_8x5120x2048_bf16.md: DRAM read 506.2 MB + write 305.3 MB per launch
+    # profiles/s6_fwd_tma_8x5120x2048_bf16.md: DRAM read 506.5 MB + write 304.6 MB per launch
     # (chained schedule), taken from the source whose hash is src_sha (any later
     # change makes the traffic null).
-    "s6_fwd_tma_kernel": {"src_sha": "e120c3e8b8b9", "bytes_per_launch": 811.54e6},
+    "s6_fwd_tma_kernel": {"src_sha": "dfa52c154012", "bytes_per_launch": 811.13e6},
     # profiles/conv1d_8x5120x2048_bf16.md: mean of 13 launches, read 170.6 MB + write 122.5 MB.
     # Captured on conv1d.cu with hash ed63d8777b5a; the file's later edits touch only the
     # host launchers' occupancy cache and comments (no device code), so the hash moves on.
@@ -59,8 +59,8 @@ NCU_TRAFFIC = {
     "conv1d_bwd_w4_kernel": {"src_sha": "fa8b0f4c9b59", "bytes_per_launch": 801.4e6},
     # profiles/s6_fwd_long_1x1536_fp32_segmented.md: one call of the long-sequence
     # forward, aggregate pass (12.98 GB read + 0.04 GB written) + full pass with y
-    # staged (19.56 + 6.42 GB); the carry pass adds about 2 MB.
-    "s6_fwd_long_call": {"src_sha": "e120c3e8b8b9", "bytes_per_launch": 38.99e9},
+    # staged (19.57 + 6.42 GB); the carry pass adds about 2 MB.
+    "s6_fwd_long_call": {"src_sha": "dfa52c154012", "bytes_per_launch": 39.01e9},
 }
 
 
