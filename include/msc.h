@@ -254,8 +254,8 @@ msc_status msc_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, in
  *    to the order of the atomic sums; with segments (few rows, long
  *    sequences) each segment starts from a carry that combines the states in
  *    another order, so checkpoints and gradients differ by rounding.
- * Limits: the backward's (dstate 1..16), seqlen a multiple of 8 and seqlen,
- * dim below 2^31, else MSC_ERR_UNSUPPORTED; the checkpoints must come from
+ * Limits: dstate 1..16 (MSC_S6_MAX_DSTATE: a checkpoint holds 16 states), seqlen
+ * a multiple of 8 and seqlen, dim below 2^31, else MSC_ERR_UNSUPPORTED; the checkpoints must come from
  * msc_selective_scan_fwd_train on the same inputs. */
 size_t msc_selective_scan_ckpt_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
 

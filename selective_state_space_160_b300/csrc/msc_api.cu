@@ -346,8 +346,8 @@ msc_status msc_selective_scan_bwd(int64_t batch, int64_t dim, int64_t seqlen, in
     return s6_bwd_launch(a, static_cast<cudaStream_t>(stream));
 }
 
-// The training pair's common limits: the backward's (dstate <= 16), seqlen a
-// multiple of 8 (whole checkpoint groups, 16-byte rows in both dtypes) and
+// The training pair's common limits: dstate <= 16 (a checkpoint holds 16
+// states), seqlen a multiple of 8 (whole checkpoint groups, 16-byte rows in both dtypes) and
 // seqlen, dim below 2^31 (32-bit TMA tile coordinates).
 static msc_status check_train_dims(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, msc_dtype dt) {
     msc_status s = check_s6_dims(batch, dim, seqlen, dstate, dt);
